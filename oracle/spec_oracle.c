@@ -1,0 +1,528 @@
+/*
+ * spec_oracle.c -- CPU oracle for the target-side verification step of speculative decoding.
+ *
+ * TEST INFRASTRUCTURE.  This file is the plain, slow, scalar reference that the CUDA library is
+ * checked against.  Only the test suite, the package's smoke check and the benchmark's CPU
+ * baseline leg load it; the product path never does.  It shares no code with the CUDA library.
+ *
+ * Arithmetic: IEEE double throughout (inputs are widened exactly from fp32 / bf16 / fp16),
+ * scalar loops in index order, no blocking, no reordering.  Compile with -ffp-contract=off.
+ *
+ * Source of the method -- "Speculative Decoding in Production: From Draft Models to EAGLE-3
+ * Dynamic Trees for 3x-5x Lossless Acceleration" (blog.llmgo.top), section I.1 "Verification
+ * via Modified Rejection Sampling":
+ *   step 1  acceptance probability  alpha = min(1, p(x_k) / q(x_k))
+ *   step 2  r ~ Uniform(0,1); accept x_k iff r <= alpha, otherwise reject and stop verifying
+ *           the later draft tokens
+ *   step 3  after a rejection at position k, resample from
+ *           max(0, p(x) - q(x)) / sum_x max(0, p(x) - q(x))
+ *   the "Invariance Theorem" paragraph below it: the emitted tokens follow p exactly, for
+ *   greedy decoding as well as temperature sampling.
+ * Tree verification -- same page, section III.2 "The Tree Attention Verification Mechanism"
+ * (the branch whose tokens match is accepted, a rejected sibling branch is skipped), and
+ * "Speculative Decoding with Medusa, EAGLE and vLLM" (vikram-blog.pages.dev), "System Topology
+ * & Data Flow" diagram (branch A accepted, branch B rejected).
+ *
+ * Readings where the pages are silent (each one also listed in the design notes):
+ *   R1  p = softmax(logits / T) with the row maximum subtracted; T = 0 means greedy.
+ *   R2  alpha = 1 when q(x_k) == 0 (p/0 taken as +inf) or p(x_k) >= q(x_k).
+ *   R3  r in (0, 1]; u in [0, 1); one u per request serves both the residual and the bonus draw.
+ *   R4  inverse-CDF sampling: the smallest i with C_i = sum_{t<=i} w_t > u * S (strict), so a
+ *       zero-weight token is never drawn; if rounding leaves no such i, the largest i with w_i > 0.
+ *   R5  if the residual mass S is not positive, draw from p at that position instead (flagged).
+ *   R6  all K drafts accepted: a bonus token is drawn from p at row K (the (K+1)-th target row).
+ *   R7  greedy: argmax over the raw logits, lowest index on ties; accept x_k iff it equals the
+ *       target argmax; the emitted token after the accepted prefix is the argmax of that row.
+ *   R8  n-gram prompt lookup: q is one-hot at the draft token.
+ *   R9  tree: from the root, move to the child whose token equals the argmax of the current
+ *       node's row (lowest node index if several), until no child matches; the final token is
+ *       the argmax of the last node's row.
+ *   R10 flagged ties: |r_k - alpha_k| <= tol at an evaluated position, or u within tol of
+ *       C_{i*-1}/S or C_{i*}/S at the drawn index i*.
+ *   R11 invalid input: a draft token outside [0, V), a logits row holding NaN (or, when a softmax
+ *       is taken, +inf, or only -inf), or a malformed parent array sets an error bit; the request
+ *       then accepts nothing and emits no token (-1).
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2 };
+
+/* per-request / per-position tie flags (R10, R5) */
+enum { ORF_ACCEPT_TIE = 1, ORF_CDF_TIE = 2, ORF_ZERO_RESIDUAL = 4 };
+/* per-request error bits (R11) */
+enum { ORE_BAD_TOKEN = 1, ORE_NONFINITE = 2, ORE_BAD_TREE = 8 };
+
+/* ---------------------------------------------------------------- exact input widening ---- */
+static double half_to_double(uint16_t h)
+{
+    int sign = (h >> 15) & 1, ex = (h >> 10) & 31, man = h & 1023;
+    double v;
+    if (ex == 0)
+        v = ldexp((double)man, -24);
+    else if (ex == 31)
+        v = man ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + man), ex - 25);
+    return sign ? -v : v;
+}
+
+double oracle_load(const void *base, int dtype, size_t i)
+{
+    if (dtype == OR_F32)
+        return (double)((const float *)base)[i];
+    if (dtype == OR_BF16) {
+        uint32_t bits = (uint32_t)((const uint16_t *)base)[i] << 16;
+        float f;
+        memcpy(&f, &bits, sizeof f);
+        return (double)f;
+    }
+    return half_to_double(((const uint16_t *)base)[i]);
+}
+
+static void load_row(const void *base, int dtype, size_t row, int V, double *out)
+{
+    for (int i = 0; i < V; i++)
+        out[i] = oracle_load(base, dtype, row * (size_t)V + (size_t)i);
+}
+
+/* ------------------------------------------------------------------- temperature softmax ---- */
+/* R1: p_i = exp((l_i - m) / T) / sum_j exp((l_j - m) / T), m = max_j l_j.
+ * Returns ORE_NONFINITE (and leaves p unspecified) for NaN, +inf, or an all -inf row. */
+int oracle_softmax(const double *l, int V, double T, double *p)
+{
+    double m = -INFINITY;
+    for (int i = 0; i < V; i++) {
+        if (isnan(l[i]) || l[i] == INFINITY)
+            return ORE_NONFINITE;
+        if (l[i] > m)
+            m = l[i];
+    }
+    if (m == -INFINITY)
+        return ORE_NONFINITE;
+    double Z = 0.0;
+    for (int i = 0; i < V; i++) {
+        p[i] = exp((l[i] - m) / T);
+        Z += p[i];
+    }
+    for (int i = 0; i < V; i++)
+        p[i] = p[i] / Z;
+    return 0;
+}
+
+/* R7: first index of the maximum (strict > keeps the lowest index on ties). */
+int oracle_argmax(const double *l, int V)
+{
+    int a = 0;
+    for (int i = 1; i < V; i++)
+        if (l[i] > l[a])
+            a = i;
+    return a;
+}
+
+static int row_has_nan(const double *l, int V)
+{
+    for (int i = 0; i < V; i++)
+        if (isnan(l[i]))
+            return 1;
+    return 0;
+}
+
+/* ------------------------------------------------------------------- inverse-CDF sampling ---- */
+/* R4: smallest i with C_i > u * S; S = sum of w.  Returns -1 when S is not positive.
+ * *flag is set when u lies within tol of C_{i-1}/S or C_i/S (R10). */
+int oracle_inverse_cdf(const double *w, int V, double u, double tol, double *S_out, int *flag)
+{
+    double S = 0.0;
+    for (int i = 0; i < V; i++)
+        S += w[i];
+    *S_out = S;
+    *flag = 0;
+    if (!(S > 0.0))
+        return -1;
+    double target = u * S, C = 0.0, Cprev = 0.0;
+    int pick = -1;
+    for (int i = 0; i < V; i++) {
+        Cprev = C;
+        C += w[i];
+        if (C > target) {
+            pick = i;
+            break;
+        }
+    }
+    if (pick < 0) { /* rounding left u*S at or above the total: the last positive weight */
+        for (int i = V - 1; i >= 0; i--)
+            if (w[i] > 0.0) {
+                pick = i;
+                break;
+            }
+        *flag = 1;
+        return pick;
+    }
+    if (fabs(Cprev / S - u) <= tol || fabs(C / S - u) <= tol)
+        *flag = 1;
+    return pick;
+}
+
+/* ------------------------------------------------------ chain verification on probabilities ---- */
+/*
+ * p: [K+1][V] target probabilities (row K = bonus row), q: [K][V] draft probabilities,
+ * x: [K] draft tokens (must lie in [0, V)), r: [K], u: scalar.
+ * Outputs (all per request):
+ *   n_acc, out_tokens[K+1] (accepted prefix, then the drawn token, then -1),
+ *   alpha[K] (step 1 at every position), cand[K+1] (the token step 3 would draw at position k,
+ *   and the bonus draw at K), mass[K+1] (the residual mass S at k; sum of p at K),
+ *   pos_flag[K+1] (CDF tie / zero-residual at k), req_flag (flags of the evaluated positions).
+ */
+void oracle_verify_probs(int K, int V, const double *p, const double *q, const int *x,
+                         const float *r, float u, double tol, int *n_acc, int *out_tokens,
+                         double *alpha, int *cand, double *mass, int *pos_flag, int *req_flag)
+{
+    double *w = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    *req_flag = 0;
+    for (int k = 0; k <= K; k++) {
+        const double *pk = p + (size_t)k * V;
+        int f = 0;
+        if (k < K) {
+            const double *qk = q + (size_t)k * V;
+            double px = pk[x[k]], qx = qk[x[k]];
+            alpha[k] = (qx == 0.0 || px >= qx) ? 1.0 : px / qx; /* step 1, R2 */
+            for (int i = 0; i < V; i++) {                       /* step 3 residual */
+                double d = pk[i] - qk[i];
+                w[i] = d > 0.0 ? d : 0.0;
+            }
+        } else {
+            for (int i = 0; i < V; i++) /* R6 bonus: draw from p */
+                w[i] = pk[i];
+        }
+        double S;
+        int fl;
+        int c = oracle_inverse_cdf(w, V, (double)u, tol, &S, &fl);
+        mass[k] = S;
+        if (c < 0) { /* R5: no residual mass left, draw from p instead */
+            double S2;
+            c = oracle_inverse_cdf(pk, V, (double)u, tol, &S2, &fl);
+            f |= ORF_ZERO_RESIDUAL;
+        }
+        if (fl)
+            f |= ORF_CDF_TIE;
+        cand[k] = c;
+        pos_flag[k] = f;
+    }
+    /* step 2: accept while r_k <= alpha_k, stop at the first rejection */
+    int n = 0;
+    while (n < K) {
+        if (fabs((double)r[n] - alpha[n]) <= tol)
+            *req_flag |= ORF_ACCEPT_TIE;
+        if ((double)r[n] <= alpha[n])
+            n++;
+        else
+            break;
+    }
+    *req_flag |= pos_flag[n];
+    *n_acc = n;
+    for (int i = 0; i <= K; i++)
+        out_tokens[i] = i < n ? x[i] : (i == n ? cand[n] : -1);
+    free(w);
+}
+
+static void fail_request(int K, int *n_acc, int *out_tokens, double *alpha, int *cand,
+                         double *mass)
+{
+    *n_acc = 0;
+    for (int i = 0; i <= K; i++) {
+        out_tokens[i] = -1;
+        cand[i] = -1;
+        mass[i] = 0.0;
+        if (i < K)
+            alpha[i] = 0.0;
+    }
+}
+
+/* R7, greedy chain on logits rows lt: [K+1][V]. */
+static int greedy_chain(int K, int V, const double *lt, const int *x, int *n_acc,
+                        int *out_tokens, double *alpha, int *cand, double *mass)
+{
+    for (int k = 0; k <= K; k++) {
+        if (row_has_nan(lt + (size_t)k * V, V))
+            return ORE_NONFINITE;
+        cand[k] = oracle_argmax(lt + (size_t)k * V, V);
+        mass[k] = 1.0; /* one-hot p minus one-hot q leaves mass 1 (or p itself at the bonus) */
+        if (k < K)
+            alpha[k] = (x[k] == cand[k]) ? 1.0 : 0.0;
+    }
+    int n = 0;
+    while (n < K && x[n] == cand[n])
+        n++;
+    *n_acc = n;
+    for (int i = 0; i <= K; i++)
+        out_tokens[i] = i < n ? x[i] : (i == n ? cand[n] : -1);
+    return 0;
+}
+
+/*
+ * Chain verification on logits (draft model / EAGLE head: the draft side is logits).
+ * target: [B][K+1][V], draft: [B][K][V] (ignored when T == 0), dtype OR_*.
+ * Per request b the outputs are laid out as in oracle_verify_probs:
+ *   n_acc[B], out_tokens[B][K+1], alpha[B][K], cand[B][K+1], mass[B][K+1],
+ *   pos_flag[B][K+1], req_flag[B], err[B].
+ * Requests [b0, b1) only are processed (lets a caller split the batch across threads).
+ */
+void oracle_verify_chain(int dtype, const void *target, const void *draft, int B, int K, int V,
+                         float T, const int *x, const float *r, const float *u, double tol,
+                         int b0, int b1, int *n_acc, int *out_tokens, double *alpha, int *cand,
+                         double *mass, int *pos_flag, int *req_flag, int *err)
+{
+    size_t rowsT = (size_t)(K + 1) * V, rowsD = (size_t)K * V;
+    double *lt = (double *)malloc(sizeof(double) * (rowsT ? rowsT : 1));
+    double *ld = (double *)malloc(sizeof(double) * (rowsD ? rowsD : 1));
+    double *p = (double *)malloc(sizeof(double) * (rowsT ? rowsT : 1));
+    double *q = (double *)malloc(sizeof(double) * (rowsD ? rowsD : 1));
+    (void)B;
+    for (int b = b0; b < b1; b++) {
+        const int *xb = x + (size_t)b * K;
+        int *o_n = n_acc + b, *o_tok = out_tokens + (size_t)b * (K + 1);
+        double *o_al = alpha + (size_t)b * K, *o_ms = mass + (size_t)b * (K + 1);
+        int *o_cd = cand + (size_t)b * (K + 1), *o_pf = pos_flag + (size_t)b * (K + 1);
+        int e = 0;
+        req_flag[b] = 0;
+        for (int k = 0; k < K + 1; k++)
+            o_pf[k] = 0;
+        for (int k = 0; k < K; k++)
+            if (xb[k] < 0 || xb[k] >= V)
+                e |= ORE_BAD_TOKEN;
+        for (int k = 0; k <= K; k++)
+            load_row(target, dtype, (size_t)b * (K + 1) + k, V, lt + (size_t)k * V);
+        if (!e && T == 0.0f) {
+            e |= greedy_chain(K, V, lt, xb, o_n, o_tok, o_al, o_cd, o_ms);
+        } else if (!e) {
+            for (int k = 0; k < K; k++)
+                load_row(draft, dtype, (size_t)b * K + k, V, ld + (size_t)k * V);
+            for (int k = 0; k <= K; k++)
+                e |= oracle_softmax(lt + (size_t)k * V, V, (double)T, p + (size_t)k * V);
+            for (int k = 0; k < K; k++)
+                e |= oracle_softmax(ld + (size_t)k * V, V, (double)T, q + (size_t)k * V);
+            if (!e)
+                oracle_verify_probs(K, V, p, q, xb, r + (size_t)b * K, u[b], tol, o_n, o_tok, o_al,
+                                    o_cd, o_ms, o_pf, req_flag + b);
+        }
+        if (e) {
+            fail_request(K, o_n, o_tok, o_al, o_cd, o_ms);
+            req_flag[b] = 0;
+        }
+        err[b] = e;
+    }
+    free(lt);
+    free(ld);
+    free(p);
+    free(q);
+}
+
+/*
+ * n-gram (prompt lookup) verification, R8: q_k is one-hot at x_k.  This is the general path of
+ * oracle_verify_probs with explicit one-hot q rows.  Same layout as oracle_verify_chain.
+ */
+void oracle_verify_ngram(int dtype, const void *target, int B, int K, int V, float T,
+                         const int *x, const float *r, const float *u, double tol, int b0, int b1,
+                         int *n_acc, int *out_tokens, double *alpha, int *cand, double *mass,
+                         int *pos_flag, int *req_flag, int *err)
+{
+    size_t rowsT = (size_t)(K + 1) * V, rowsD = (size_t)K * V;
+    double *lt = (double *)malloc(sizeof(double) * (rowsT ? rowsT : 1));
+    double *p = (double *)malloc(sizeof(double) * (rowsT ? rowsT : 1));
+    double *q = (double *)malloc(sizeof(double) * (rowsD ? rowsD : 1));
+    (void)B;
+    for (int b = b0; b < b1; b++) {
+        const int *xb = x + (size_t)b * K;
+        int *o_n = n_acc + b, *o_tok = out_tokens + (size_t)b * (K + 1);
+        double *o_al = alpha + (size_t)b * K, *o_ms = mass + (size_t)b * (K + 1);
+        int *o_cd = cand + (size_t)b * (K + 1), *o_pf = pos_flag + (size_t)b * (K + 1);
+        int e = 0;
+        req_flag[b] = 0;
+        for (int k = 0; k < K + 1; k++)
+            o_pf[k] = 0;
+        for (int k = 0; k < K; k++)
+            if (xb[k] < 0 || xb[k] >= V)
+                e |= ORE_BAD_TOKEN;
+        for (int k = 0; k <= K; k++)
+            load_row(target, dtype, (size_t)b * (K + 1) + k, V, lt + (size_t)k * V);
+        if (!e && T == 0.0f) {
+            e |= greedy_chain(K, V, lt, xb, o_n, o_tok, o_al, o_cd, o_ms);
+        } else if (!e) {
+            for (int k = 0; k <= K; k++)
+                e |= oracle_softmax(lt + (size_t)k * V, V, (double)T, p + (size_t)k * V);
+            for (size_t i = 0; i < rowsD; i++)
+                q[i] = 0.0;
+            for (int k = 0; k < K; k++)
+                q[(size_t)k * V + xb[k]] = 1.0;
+            if (!e)
+                oracle_verify_probs(K, V, p, q, xb, r + (size_t)b * K, u[b], tol, o_n, o_tok, o_al,
+                                    o_cd, o_ms, o_pf, req_flag + b);
+        }
+        if (e) {
+            fail_request(K, o_n, o_tok, o_al, o_cd, o_ms);
+            req_flag[b] = 0;
+        }
+        err[b] = e;
+    }
+    free(lt);
+    free(p);
+    free(q);
+}
+
+/*
+ * n-gram shortcut on probabilities, written directly from R8: with q one-hot at x_k,
+ * alpha_k = min(1, p_k(x_k)) and the residual is p_k with x_k's entry zeroed; the bonus draws
+ * from p_K.  Used by the tests to pin the general path; same outputs as oracle_verify_probs.
+ */
+void oracle_verify_ngram_direct(int K, int V, const double *p, const int *x, const float *r,
+                                float u, double tol, int *n_acc, int *out_tokens, double *alpha,
+                                int *cand, double *mass, int *pos_flag, int *req_flag)
+{
+    double *w = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    *req_flag = 0;
+    for (int k = 0; k <= K; k++) {
+        const double *pk = p + (size_t)k * V;
+        int f = 0;
+        for (int i = 0; i < V; i++)
+            w[i] = pk[i];
+        if (k < K) {
+            alpha[k] = pk[x[k]] >= 1.0 ? 1.0 : pk[x[k]];
+            w[x[k]] = 0.0;
+        }
+        double S;
+        int fl;
+        int c = oracle_inverse_cdf(w, V, (double)u, tol, &S, &fl);
+        mass[k] = S;
+        if (c < 0) {
+            double S2;
+            c = oracle_inverse_cdf(pk, V, (double)u, tol, &S2, &fl);
+            f |= ORF_ZERO_RESIDUAL;
+        }
+        if (fl)
+            f |= ORF_CDF_TIE;
+        cand[k] = c;
+        pos_flag[k] = f;
+    }
+    int n = 0;
+    while (n < K) {
+        if (fabs((double)r[n] - alpha[n]) <= tol)
+            *req_flag |= ORF_ACCEPT_TIE;
+        if ((double)r[n] <= alpha[n])
+            n++;
+        else
+            break;
+    }
+    *req_flag |= pos_flag[n];
+    *n_acc = n;
+    for (int i = 0; i <= K; i++)
+        out_tokens[i] = i < n ? x[i] : (i == n ? cand[n] : -1);
+    free(w);
+}
+
+/* ---------------------------------------------------------------------- greedy tree walk ---- */
+/* Parent array check: parents[0] == -1, 0 <= parents[i] < i; node tokens in [0, V) (root
+ * excluded). */
+int oracle_tree_check(int N1, int V, const int *parents, const int *tokens)
+{
+    if (N1 < 1 || parents[0] != -1)
+        return ORE_BAD_TREE;
+    for (int i = 1; i < N1; i++) {
+        if (parents[i] < 0 || parents[i] >= i)
+            return ORE_BAD_TREE;
+        if (tokens[i] < 0 || tokens[i] >= V)
+            return ORE_BAD_TOKEN;
+    }
+    return 0;
+}
+
+/* R9: walk from the root along children whose token equals the argmax of the current node's
+ * row.  amax[n] = argmax of row n.  Outputs: *accept_len, path[N1] (root first, -1 padded),
+ * out_tokens[N1] (accepted tokens then the final argmax token, -1 padded). */
+void oracle_tree_walk(int N1, const int *parents, const int *tokens, const int *amax,
+                      int *accept_len, int *path, int *out_tokens)
+{
+    int cur = 0, len = 0;
+    for (int i = 0; i < N1; i++) {
+        path[i] = -1;
+        out_tokens[i] = -1;
+    }
+    path[0] = 0;
+    for (int step = 0; step < N1; step++) {
+        int a = amax[cur], next = -1;
+        for (int c = cur + 1; c < N1; c++)
+            if (parents[c] == cur && tokens[c] == a) {
+                next = c;
+                break;
+            }
+        if (next < 0)
+            break;
+        out_tokens[len] = tokens[next];
+        len++;
+        path[len] = next;
+        cur = next;
+    }
+    out_tokens[len] = amax[cur];
+    *accept_len = len;
+}
+
+/* Brute force over every node v: v is reachable when every edge u->w on the root-to-v path has
+ * tokens[w] == amax[u].  Returns the deepest reachable node (lowest index among the deepest)
+ * and its depth in *depth.  Independent of the walk; used to pin it. */
+int oracle_tree_bruteforce(int N1, const int *parents, const int *tokens, const int *amax,
+                           int *depth)
+{
+    int best = 0, best_d = 0;
+    for (int v = 1; v < N1; v++) {
+        int ok = 1, d = 0;
+        for (int w = v; w != 0; w = parents[w]) {
+            if (tokens[w] != amax[parents[w]]) {
+                ok = 0;
+                break;
+            }
+            d++;
+        }
+        if (ok && d > best_d) {
+            best = v;
+            best_d = d;
+        }
+    }
+    *depth = best_d;
+    return best;
+}
+
+/* Greedy tree verification on logits: target [B][N+1][V]; node_tokens, parents [B][N+1].
+ * Outputs: accept_len[B], path[B][N+1], out_tokens[B][N+1], amax[B][N+1], err[B]. */
+void oracle_verify_tree_greedy(int dtype, const void *target, int B, int N, int V,
+                               const int *node_tokens, const int *parents, int b0, int b1,
+                               int *accept_len, int *path, int *out_tokens, int *amax, int *err)
+{
+    int N1 = N + 1;
+    double *row = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    (void)B;
+    for (int b = b0; b < b1; b++) {
+        const int *pb = parents + (size_t)b * N1, *tb = node_tokens + (size_t)b * N1;
+        int *ab = amax + (size_t)b * N1;
+        int e = oracle_tree_check(N1, V, pb, tb);
+        for (int n = 0; n < N1; n++) {
+            load_row(target, dtype, (size_t)b * N1 + n, V, row);
+            if (row_has_nan(row, V))
+                e |= ORE_NONFINITE;
+            ab[n] = oracle_argmax(row, V);
+        }
+        if (e) {
+            accept_len[b] = 0;
+            for (int i = 0; i < N1; i++) {
+                path[(size_t)b * N1 + i] = -1;
+                out_tokens[(size_t)b * N1 + i] = -1;
+            }
+        } else {
+            oracle_tree_walk(N1, pb, tb, ab, accept_len + b, path + (size_t)b * N1,
+                             out_tokens + (size_t)b * N1);
+        }
+        err[b] = e;
+    }
+    free(row);
+}

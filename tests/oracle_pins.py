@@ -1,0 +1,380 @@
+"""Pins that tie the CPU oracle to what the pages and the mathematics fix.
+
+Each `pin_*` takes a loaded oracle library (so the same checks can run against deliberately
+broken builds of the oracle, see test_oracle_mutants.py) and raises AssertionError on a
+mismatch.  Sources of truth, none of them the oracle itself:
+  * hand-worked dyadic cases (tests/golden/hand_cases.json, derived from section I.1 of the
+    llmgo page, "Verification via Modified Rejection Sampling");
+  * closed forms: V=2 softmax is a logistic function; residual mass = 1 - sum min(p, q);
+  * library routines on special cases: numpy argmax (first occurrence), scipy softmax,
+    numpy float16 / bit-shift bf16 widening;
+  * brute force over tiny inputs (inverse CDF, tree paths);
+  * the invariance theorem (section I.1, last paragraph) by chi-squared tests.
+"""
+
+from __future__ import annotations
+
+import json
+import math
+import os
+
+import numpy as np
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "hand_cases.json")
+TOL = oracle.DEFAULT_TOL
+
+
+def _golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------------- hand cases ----
+def pin_hand_chain_cases(lib):
+    for case in _golden()["chain"]:
+        p = np.asarray(case["p"], np.float64)
+        K = p.shape[0] - 1
+        q = np.asarray(case["q"], np.float64).reshape(K, p.shape[1])
+        for run in case["runs"]:
+            o = oracle.verify_probs(p, q, case["x"], run["r"], run["u"], TOL, lib=lib)
+            tag = f"{case['name']} r={run['r']} u={run['u']}"
+            assert int(o["num_accepted"]) == run["n_acc"], (tag, o)
+            assert list(o["out_tokens"]) == run["out_tokens"], (tag, o)
+            assert np.allclose(o["alpha"], case["alpha"], rtol=0, atol=1e-15), (tag, o["alpha"])
+            assert np.allclose(o["mass"], case["mass"], rtol=0, atol=1e-15), (tag, o["mass"])
+            assert bool(o["req_flag"] & oracle.FLAG_ACCEPT_TIE) == run["accept_tie"], (tag, o)
+            assert bool(o["req_flag"] & oracle.FLAG_CDF_TIE) == run["cdf_tie"], (tag, o)
+            if "cand" in run:
+                assert list(o["cand"]) == run["cand"], (tag, o["cand"])
+                zr = [bool(f & oracle.FLAG_ZERO_RESIDUAL) for f in o["pos_flag"]]
+                assert zr == run["zero_residual"], (tag, o["pos_flag"])
+
+
+def pin_hand_tree_cases(lib):
+    for case in _golden()["tree"]:
+        o = oracle.tree_walk(case["parents"], case["tokens"], case["amax"], lib=lib)
+        assert o["accept_len"] == case["accept_len"], (case["name"], o)
+        assert list(o["path"]) == case["path"], (case["name"], o)
+        assert list(o["out_tokens"]) == case["out_tokens"], (case["name"], o)
+        v, d = oracle.tree_bruteforce(case["parents"], case["tokens"], case["amax"], lib=lib)
+        assert d == case["accept_len"] and (d == 0 or v == case["path"][d]), (case["name"], v, d)
+
+
+# ------------------------------------------------------------------------------ softmax ----
+def pin_softmax_closed_forms(lib):
+    # V = 2 reduces to the logistic function of the logit gap over T.
+    for a, b, T in [(0.0, 1.0, 1.0), (1.5, -2.0, 0.7), (3.0, 3.5, 2.0), (-7.0, 9.0, 0.25)]:
+        p, e = oracle.softmax([a, b], T, lib=lib)
+        assert e == 0
+        want1 = 1.0 / (1.0 + math.exp(-(b - a) / T))
+        assert abs(p[1] - want1) < 1e-15 and abs(p[0] - (1 - want1)) < 1e-15, (a, b, T, p)
+    # Equal logits give the uniform distribution for any T.
+    p, _ = oracle.softmax(np.full(7, 2.5), 0.3, lib=lib)
+    assert np.allclose(p, 1 / 7, atol=1e-16)
+    # Temperature divides the logits: softmax(l, T) == softmax(l / T, 1).
+    rng = np.random.default_rng(1)
+    l = rng.normal(0, 3, 50)
+    p1, _ = oracle.softmax(l, 0.7, lib=lib)
+    p2, _ = oracle.softmax(l / 0.7, 1.0, lib=lib)
+    assert np.allclose(p1, p2, rtol=1e-13, atol=0)
+    # Shift invariance and normalisation.
+    p3, _ = oracle.softmax(l + 123.0, 0.7, lib=lib)
+    assert np.allclose(p1, p3, rtol=1e-12, atol=0)
+    assert abs(p1.sum() - 1.0) < 1e-12
+    # Library routine on the same row.
+    from scipy.special import softmax as sp_softmax
+
+    assert np.allclose(p1, sp_softmax(l / 0.7), rtol=1e-12, atol=1e-300)
+    # -inf is a masked token with probability 0; NaN / +inf / all -inf are errors.
+    p4, e4 = oracle.softmax([0.0, -np.inf, 0.0], 1.0, lib=lib)
+    assert e4 == 0 and p4[1] == 0.0 and abs(p4[0] - 0.5) < 1e-16
+    for bad in ([0.0, np.nan], [0.0, np.inf], [-np.inf, -np.inf]):
+        assert oracle.softmax(bad, 1.0, lib=lib)[1] == oracle.ERR_NONFINITE
+
+
+def pin_argmax_first_occurrence(lib):
+    rng = np.random.default_rng(2)
+    for _ in range(200):
+        l = rng.integers(-3, 4, size=rng.integers(1, 40)).astype(np.float64)  # many ties
+        assert oracle.argmax(l, lib=lib) == int(np.argmax(l))
+    assert oracle.argmax([-0.0, 0.0, -1.0], lib=lib) == 0  # -0 == +0: lowest index
+    assert oracle.argmax([-np.inf, -np.inf], lib=lib) == 0
+
+
+# -------------------------------------------------------------------------- inverse CDF ----
+def _brute_inverse_cdf(w, u):
+    """The definition with exact rational arithmetic on dyadic weights."""
+    from fractions import Fraction
+
+    W = [Fraction(x) for x in w]
+    S = sum(W)
+    t = Fraction(u) * S
+    C = Fraction(0)
+    for i, x in enumerate(W):
+        C += x
+        if C > t:
+            return i
+    return max(i for i, x in enumerate(W) if x > 0)
+
+
+def pin_inverse_cdf_definition(lib):
+    rng = np.random.default_rng(3)
+    for _ in range(300):
+        V = int(rng.integers(1, 12))
+        w = rng.integers(0, 5, size=V).astype(np.float64) / 8.0  # dyadic, zeros included
+        if w.sum() == 0:
+            w[rng.integers(V)] = 0.125
+        for u in [0.0, 0.25, 0.5, float(rng.integers(0, 1 << 24)) / (1 << 24), 1 - 2**-24]:
+            i, S, _ = oracle.inverse_cdf(w, u, lib=lib)
+            assert i == _brute_inverse_cdf(w, u), (w, u, i)
+            assert w[i] > 0  # a zero-weight token is never drawn
+            assert S == w.sum()
+    assert oracle.inverse_cdf(np.zeros(4), 0.5, lib=lib)[0] == -1
+
+
+def pin_inverse_cdf_frequencies(lib):
+    """On a grid of u the draw frequencies equal the normalised weights (up to grid size)."""
+    w = np.array([0.0, 3.0, 1.0, 0.0, 4.0])
+    n = 4096
+    counts = np.zeros(w.size)
+    for j in range(n):
+        counts[oracle.inverse_cdf(w, (j + 0.5) / n, lib=lib)[0]] += 1
+    assert np.allclose(counts / n, w / w.sum(), atol=1.0 / n)
+
+
+# ---------------------------------------------------------------- residual closed forms ----
+def _rand_dist(rng, V, sigma=2.0):
+    l = rng.normal(0, sigma, V)
+    e = np.exp(l - l.max())
+    return e / e.sum()
+
+
+def pin_residual_mass_closed_form(lib):
+    rng = np.random.default_rng(4)
+    for _ in range(50):
+        V, K = int(rng.integers(2, 30)), int(rng.integers(1, 6))
+        p = np.stack([_rand_dist(rng, V) for _ in range(K + 1)])
+        q = np.stack([_rand_dist(rng, V) for _ in range(K)])
+        x = rng.integers(0, V, K)
+        o = oracle.verify_probs(p, q, x, np.full(K, 0.5, np.float32), 0.5, lib=lib)
+        for k in range(K):
+            tv = 1.0 - np.minimum(p[k], q[k]).sum()  # total-variation distance
+            assert abs(o["mass"][k] - tv) < 1e-12, (k, o["mass"][k], tv)
+            want = min(1.0, p[k, x[k]] / q[k, x[k]])
+            assert abs(o["alpha"][k] - want) < 1e-15
+        assert abs(o["mass"][K] - 1.0) < 1e-12
+
+
+def pin_ngram_general_equals_shortcut(lib):
+    rng = np.random.default_rng(5)
+    for _ in range(100):
+        V, K = int(rng.integers(2, 40)), int(rng.integers(1, 7))
+        p = np.stack([_rand_dist(rng, V, 3.0) for _ in range(K + 1)])
+        x = rng.integers(0, V, K)
+        q = np.zeros((K, V))
+        q[np.arange(K), x] = 1.0
+        r = ((rng.integers(0, 1 << 24, K) + 1) / (1 << 24)).astype(np.float32)
+        u = np.float32(rng.integers(0, 1 << 24) / (1 << 24))
+        g = oracle.verify_probs(p, q, x, r, u, lib=lib)
+        d = oracle.verify_ngram_direct(p, x, r, u, lib=lib)
+        for key in ("num_accepted", "out_tokens", "cand", "pos_flag", "req_flag"):
+            assert np.array_equal(g[key], d[key]), key
+        assert np.array_equal(g["alpha"], d["alpha"]) and np.array_equal(g["mass"], d["mass"])
+        assert np.allclose(g["alpha"], p[np.arange(K), x], atol=0)  # alpha = p(x) for one-hot q
+
+
+def pin_ngram_on_logits(lib):
+    """The logits-level n-gram call (explicit one-hot q) equals the shortcut on library softmax."""
+    from scipy.special import softmax as sp_softmax
+
+    rng = np.random.default_rng(10)
+    B, K, V, T = 40, 4, 33, np.float32(0.8)
+    lt = rng.normal(0, 3, (B, K + 1, V)).astype(np.float32)
+    x = rng.integers(0, V, (B, K)).astype(np.int32)
+    lt[np.arange(B)[:, None], np.arange(K)[None, :], x] += 4.0
+    r = ((rng.integers(0, 1 << 24, (B, K)) + 1) / (1 << 24)).astype(np.float32)
+    u = (rng.integers(0, 1 << 24, B) / (1 << 24)).astype(np.float32)
+    o = oracle.verify_ngram("f32", lt, B, K, V, T, x, r, u, lib=lib)
+    for b in range(B):
+        p = sp_softmax(lt[b].astype(np.float64) / float(T), axis=-1)
+        d = oracle.verify_ngram_direct(p, x[b], r[b], u[b], lib=lib)
+        assert np.allclose(o["alpha"][b], d["alpha"], rtol=1e-12, atol=0)
+        assert np.allclose(o["mass"][b], d["mass"], rtol=1e-10, atol=1e-15)
+        if not d["req_flag"]:
+            assert o["num_accepted"][b] == d["num_accepted"]
+            assert np.array_equal(o["out_tokens"][b], d["out_tokens"])
+
+
+# ------------------------------------------------------------------------------ greedy ----
+def pin_greedy_chain(lib):
+    rng = np.random.default_rng(6)
+    for _ in range(100):
+        K, V = int(rng.integers(0, 6)), int(rng.integers(1, 20))
+        lt = rng.integers(-2, 3, size=(1, K + 1, V)).astype(np.float32)  # ties on purpose
+        a = np.argmax(lt[0], axis=-1)
+        x = np.where(rng.random(K) < 0.7, a[:K], rng.integers(0, V, K)).astype(np.int32)
+        o = oracle.verify_chain("f32", lt, None, 1, K, V, 0.0, x[None], None, None, lib=lib)
+        n = 0
+        while n < K and x[n] == a[n]:
+            n += 1
+        assert o["num_accepted"][0] == n
+        want = list(x[:n]) + [a[n]] + [-1] * (K - n)
+        assert list(o["out_tokens"][0]) == want
+        assert o["err"][0] == 0
+
+
+def pin_greedy_is_low_temperature_limit(lib):
+    """T -> 0 makes p one-hot; with a greedy draft the sampled call equals the greedy call."""
+    rng = np.random.default_rng(7)
+    for _ in range(40):
+        K, V = 4, 16
+        lt = rng.normal(0, 3, (1, K + 1, V)).astype(np.float32)
+        ld = lt[:, :K] + rng.normal(0, 1, (1, K, V)).astype(np.float32)
+        x = np.argmax(ld, -1).astype(np.int32)
+        r = np.full((1, K), 0.5, np.float32)
+        u = np.full(1, 0.5, np.float32)
+        g = oracle.verify_chain("f32", lt, ld, 1, K, V, 0.0, x, r, u, lib=lib)
+        s = oracle.verify_chain("f32", lt, ld, 1, K, V, 1e-4, x, r, u, lib=lib)
+        assert np.array_equal(g["out_tokens"], s["out_tokens"]), (g, s)
+        assert np.array_equal(g["num_accepted"], s["num_accepted"])
+
+
+# --------------------------------------------------------------------- input widening ----
+def pin_input_widening(lib):
+    h = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    f16 = h.view(np.float16).astype(np.float64)
+    got = oracle.load_elems(h, "f16", lib=lib)
+    fin = np.isfinite(f16)
+    assert np.array_equal(got[fin], f16[fin]) and np.array_equal(np.isnan(got), np.isnan(f16))
+    with np.errstate(invalid="ignore"):
+        bf = (h.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    got = oracle.load_elems(h, "bf16", lib=lib)
+    fin = np.isfinite(bf)
+    assert np.array_equal(got[fin], bf[fin]) and np.array_equal(np.isnan(got), np.isnan(bf))
+
+
+# ------------------------------------------------------------------------- error bits ----
+def pin_error_semantics(lib):
+    K, V = 2, 5
+    rng = np.random.default_rng(8)
+    lt = rng.normal(0, 1, (3, K + 1, V)).astype(np.float32)
+    ld = rng.normal(0, 1, (3, K, V)).astype(np.float32)
+    x = np.array([[0, 1], [0, V], [1, 2]], np.int32)  # request 1 has an out-of-range token
+    lt[2, 1, 3] = np.nan  # request 2 has a NaN target logit
+    r = np.full((3, K), 0.5, np.float32)
+    u = np.full(3, 0.5, np.float32)
+    o = oracle.verify_chain("f32", lt, ld, 3, K, V, 1.0, x, r, u, lib=lib)
+    assert list(o["err"]) == [0, oracle.ERR_BAD_TOKEN, oracle.ERR_NONFINITE]
+    for b in (1, 2):
+        assert o["num_accepted"][b] == 0 and (o["out_tokens"][b] == -1).all()
+    g = oracle.verify_chain("f32", lt, None, 3, K, V, 0.0, x, None, None, lib=lib)
+    assert list(g["err"]) == [0, oracle.ERR_BAD_TOKEN, oracle.ERR_NONFINITE]
+
+
+# ---------------------------------------------------------------------------- trees ----
+def random_tree(rng, N1, V, distinct=True):
+    parents = np.full(N1, -1, np.int32)
+    tokens = np.zeros(N1, np.int32)
+    for i in range(1, N1):
+        parents[i] = rng.integers(0, i)
+    for p in range(N1):
+        kids = np.nonzero(parents == p)[0]
+        if kids.size:
+            if distinct and kids.size <= V:
+                tokens[kids] = rng.choice(V, size=kids.size, replace=False)
+            else:
+                tokens[kids] = rng.integers(0, V, kids.size)
+    return parents, tokens
+
+
+def pin_tree_walk_vs_bruteforce(lib, n_trees=2000):
+    rng = np.random.default_rng(9)
+    for _ in range(n_trees):
+        N1, V = int(rng.integers(1, 21)), 24  # V >= N1 keeps every sibling set distinct
+        parents, tokens = random_tree(rng, N1, V)
+        amax = rng.integers(0, V, N1).astype(np.int32)
+        # bias toward long accepted paths: copy a child's token into its parent's argmax
+        for i in range(1, N1):
+            if rng.random() < 0.6:
+                amax[parents[i]] = tokens[i]
+        o = oracle.tree_walk(parents, tokens, amax, lib=lib)
+        v, d = oracle.tree_bruteforce(parents, tokens, amax, lib=lib)
+        assert o["accept_len"] == d, (parents, tokens, amax, o, v, d)
+        if d:
+            assert o["path"][d] == v
+        # the path is a chain of parent links with matching tokens
+        path = o["path"][: d + 1]
+        for j in range(1, d + 1):
+            assert parents[path[j]] == path[j - 1] and tokens[path[j]] == amax[path[j - 1]]
+            assert o["out_tokens"][j - 1] == tokens[path[j]]
+        assert o["out_tokens"][d] == amax[path[d]]
+
+
+def pin_tree_check(lib):
+    assert oracle.tree_check([-1, 0, 1], [0, 1, 2], 3, lib=lib) == 0
+    assert oracle.tree_check([0, 0, 1], [0, 1, 2], 3, lib=lib) == oracle.ERR_BAD_TREE
+    assert oracle.tree_check([-1, 2, 1], [0, 1, 2], 3, lib=lib) == oracle.ERR_BAD_TREE
+    assert oracle.tree_check([-1, 0, 1], [0, 1, 3], 3, lib=lib) == oracle.ERR_BAD_TOKEN
+
+
+# ------------------------------------------------------------------ invariance theorem ----
+def chi2_pvalue(counts: np.ndarray, probs: np.ndarray, min_expected: float = 5.0) -> float:
+    """Pearson chi-squared p-value, bins with expected count < min_expected merged."""
+    from scipy.stats import chi2
+
+    n = counts.sum()
+    exp = probs * n
+    order = np.argsort(exp)
+    c_m, e_m, acc_c, acc_e = [], [], 0.0, 0.0
+    for i in order:
+        acc_c += counts[i]
+        acc_e += exp[i]
+        if acc_e >= min_expected:
+            c_m.append(acc_c)
+            e_m.append(acc_e)
+            acc_c = acc_e = 0.0
+    if acc_e > 0 and e_m:
+        c_m[-1] += acc_c
+        e_m[-1] += acc_e
+    c_m, e_m = np.asarray(c_m), np.asarray(e_m)
+    if c_m.size < 2:
+        return 1.0
+    stat = ((c_m - e_m) ** 2 / e_m).sum()
+    return float(chi2.sf(stat, c_m.size - 1))
+
+
+def invariance_check(out_tokens, n_acc, p_rows, K, alpha_min=1e-3):
+    """At every position k, the token emitted there (by trials that reached k) follows p_k."""
+    pvals = []
+    for k in range(K + 1):
+        reached = n_acc >= k
+        toks = out_tokens[reached, k]
+        counts = np.bincount(toks, minlength=p_rows.shape[1]).astype(np.float64)
+        pv = chi2_pvalue(counts, p_rows[k])
+        pvals.append(pv)
+        assert pv > alpha_min, (k, pv, counts, p_rows[k] * counts.sum())
+    return pvals
+
+
+def acceptance_check(n_acc, p_rows, q_rows, K, sigmas=4.0):
+    """P(accept at k | reached k) = sum_i min(p_k(i), q_k(i)); E[n_acc] = sum_k prod_{t<=k} beta_t."""
+    beta = np.minimum(p_rows[:K], q_rows[:K]).sum(axis=1)
+    for k in range(K):
+        reached = (n_acc >= k).sum()
+        acc = (n_acc > k).sum()
+        sd = math.sqrt(reached * beta[k] * (1 - beta[k])) + 1e-9
+        assert abs(acc - reached * beta[k]) <= sigmas * sd + 1, (k, acc, reached * beta[k], sd)
+    expect = sum(np.prod(beta[: k + 1]) for k in range(K))
+    sd = n_acc.std() / math.sqrt(n_acc.size)
+    assert abs(n_acc.mean() - expect) <= sigmas * sd, (n_acc.mean(), expect, sd)
+    return beta
+
+
+FAST_PINS = [pin_hand_chain_cases, pin_hand_tree_cases, pin_softmax_closed_forms,
+             pin_argmax_first_occurrence, pin_inverse_cdf_definition, pin_inverse_cdf_frequencies,
+             pin_residual_mass_closed_form, pin_ngram_general_equals_shortcut, pin_ngram_on_logits,
+             pin_greedy_chain,
+             pin_greedy_is_low_temperature_limit, pin_input_widening, pin_error_semantics,
+             pin_tree_check]

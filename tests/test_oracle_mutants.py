@@ -1,0 +1,78 @@
+"""The pins have power: each plausible mistake planted in a copy of the oracle (a dropped term,
+a wrong sign, a wrong index, a flipped comparison) makes at least one pin fail.
+
+The mistakes are planted by text substitution into a temporary copy of oracle/spec_oracle.c,
+compiled on the CPU; the real oracle is never modified.
+"""
+
+import os
+import tempfile
+
+import pytest
+
+import oracle
+import oracle_pins as pins
+
+# (name, original text, planted mistake); every original must occur in the oracle source.
+MUTANTS = [
+    ("alpha_inverted", "px / qx;", "qx / px;"),
+    ("alpha_without_min", "(qx == 0.0 || px >= qx) ? 1.0 : px / qx", "(qx == 0.0) ? 1.0 : px / qx"),
+    ("accept_strict_less", "if ((double)r[n] <= alpha[n])", "if ((double)r[n] < alpha[n])"),
+    ("accept_test_dropped", "if ((double)r[n] <= alpha[n])", "if (1)"),
+    ("residual_sign_flipped", "double d = pk[i] - qk[i];", "double d = qk[i] - pk[i];"),
+    ("residual_not_clamped", "w[i] = d > 0.0 ? d : 0.0;", "w[i] = d;"),
+    ("bonus_from_first_row", "/* R6 bonus: draw from p */\n                w[i] = pk[i];",
+     "/* R6 bonus: draw from p */\n                w[i] = p[i];"),
+    ("softmax_temperature_dropped", "p[i] = exp((l[i] - m) / T);", "p[i] = exp(l[i] - m);"),
+    ("softmax_temperature_multiplied", "p[i] = exp((l[i] - m) / T);", "p[i] = exp((l[i] - m) * T);"),
+    ("softmax_not_normalised", "p[i] = p[i] / Z;", "p[i] = p[i];"),
+    ("cdf_non_strict", "if (C > target) {", "if (C >= target) {"),
+    ("cdf_off_by_one", "if (C > target) {\n            pick = i;",
+     "if (C > target) {\n            pick = i + 1 < V ? i + 1 : i;"),
+    ("cdf_tie_flag_dropped", "if (fabs(Cprev / S - u) <= tol || fabs(C / S - u) <= tol)", "if (0)"),
+    ("accept_tie_flag_dropped", "if (fabs((double)r[n] - alpha[n]) <= tol)", "if (0)"),
+    ("zero_residual_fallback_dropped", "c = oracle_inverse_cdf(pk, V, (double)u, tol, &S2, &fl);",
+     "c = 0;"),
+    ("argmax_last_on_ties", "if (l[i] > l[a])", "if (l[i] >= l[a])"),
+    ("tree_compares_child_row", "tokens[c] == a)", "tokens[c] == amax[c])"),
+    ("tree_final_token_from_root", "out_tokens[len] = amax[cur];", "out_tokens[len] = amax[0];"),
+    ("tree_parent_check_dropped", "if (parents[i] < 0 || parents[i] >= i)", "if (0)"),
+    ("bf16_widening_shift", "[i] << 16;", "[i] << 15;"),
+    ("f16_subnormal_scale", "ldexp((double)man, -24)", "ldexp((double)man, -25)"),
+    ("ngram_onehot_weight", "q[(size_t)k * V + xb[k]] = 1.0;", "q[(size_t)k * V + xb[k]] = 0.5;"),
+    ("greedy_compares_next_row", "while (n < K && x[n] == cand[n])", "while (n < K && x[n] == cand[n + 1])"),
+    ("bad_token_check_dropped", "if (xb[k] < 0 || xb[k] >= V)\n                e |= ORE_BAD_TOKEN;\n"
+     "        for (int k = 0; k <= K; k++)\n            load_row(target, dtype, (size_t)b * (K + 1) + k, V, lt + (size_t)k * V);\n"
+     "        if (!e && T == 0.0f) {\n            e |= greedy_chain(K, V, lt, xb, o_n, o_tok, o_al, o_cd, o_ms);\n"
+     "        } else if (!e) {\n            for (int k = 0; k < K; k++)\n                load_row(draft",
+     "if (0)\n                e |= ORE_BAD_TOKEN;\n"
+     "        for (int k = 0; k <= K; k++)\n            load_row(target, dtype, (size_t)b * (K + 1) + k, V, lt + (size_t)k * V);\n"
+     "        if (!e && T == 0.0f) {\n            e |= greedy_chain(K, V, lt, xb, o_n, o_tok, o_al, o_cd, o_ms);\n"
+     "        } else if (!e) {\n            for (int k = 0; k < K; k++)\n                load_row(draft"),
+]
+
+SRC = open(oracle.SRC).read()
+
+
+def _first_failing_pin(lib):
+    for pin in pins.FAST_PINS + [lambda l: pins.pin_tree_walk_vs_bruteforce(l, n_trees=300),
+                                 pins.pin_hand_tree_cases]:
+        try:
+            pin(lib)
+        except (AssertionError, IndexError, ValueError):
+            return getattr(pin, "__name__", "tree_bruteforce")
+    return None
+
+
+def test_real_oracle_passes_every_pin():
+    assert _first_failing_pin(oracle.load()) is None
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_planted_mistake_is_caught(name, old, new, tmp_path):
+    assert old in SRC, f"mutant {name}: original text not found in the oracle source"
+    src = tmp_path / "mutant.c"
+    src.write_text(SRC.replace(old, new))
+    so = oracle.build(str(src), str(tmp_path / f"lib_{name}.so"))
+    caught = _first_failing_pin(oracle.load(so))
+    assert caught is not None, f"no pin catches the planted mistake '{name}'"
