@@ -40,8 +40,8 @@
  *   R10 flagged ties: |r_k - alpha_k| <= tol at an evaluated position, or u within tol of
  *       C_{i*-1}/S or C_{i*}/S at the drawn index i*.
  *   R11 invalid input: a draft token outside [0, V), a logits row holding NaN (or, when a softmax
- *       is taken, +inf, or only -inf), or a malformed parent array sets an error bit; the request
- *       then accepts nothing and emits no token (-1).
+ *       is taken, +inf, or only -inf), or a malformed parent array sets an error bit (every bit
+ *       that applies, all rows checked); the request then accepts nothing and emits no token (-1).
  */
 #include <math.h>
 #include <stdint.h>
@@ -295,9 +295,9 @@ void oracle_verify_chain(int dtype, const void *target, const void *draft, int B
                 e |= ORE_BAD_TOKEN;
         for (int k = 0; k <= K; k++)
             load_row(target, dtype, (size_t)b * (K + 1) + k, V, lt + (size_t)k * V);
-        if (!e && T == 0.0f) {
+        if (T == 0.0f) {
             e |= greedy_chain(K, V, lt, xb, o_n, o_tok, o_al, o_cd, o_ms);
-        } else if (!e) {
+        } else {
             for (int k = 0; k < K; k++)
                 load_row(draft, dtype, (size_t)b * K + k, V, ld + (size_t)k * V);
             for (int k = 0; k <= K; k++)
@@ -348,14 +348,14 @@ void oracle_verify_ngram(int dtype, const void *target, int B, int K, int V, flo
                 e |= ORE_BAD_TOKEN;
         for (int k = 0; k <= K; k++)
             load_row(target, dtype, (size_t)b * (K + 1) + k, V, lt + (size_t)k * V);
-        if (!e && T == 0.0f) {
+        if (T == 0.0f) {
             e |= greedy_chain(K, V, lt, xb, o_n, o_tok, o_al, o_cd, o_ms);
-        } else if (!e) {
+        } else {
             for (int k = 0; k <= K; k++)
                 e |= oracle_softmax(lt + (size_t)k * V, V, (double)T, p + (size_t)k * V);
             for (size_t i = 0; i < rowsD; i++)
                 q[i] = 0.0;
-            for (int k = 0; k < K; k++)
+            for (int k = 0; k < K && !e; k++)
                 q[(size_t)k * V + xb[k]] = 1.0;
             if (!e)
                 oracle_verify_probs(K, V, p, q, xb, r + (size_t)b * K, u[b], tol, o_n, o_tok, o_al,

@@ -378,3 +378,21 @@ FAST_PINS = [pin_hand_chain_cases, pin_hand_tree_cases, pin_softmax_closed_forms
              pin_greedy_chain,
              pin_greedy_is_low_temperature_limit, pin_input_widening, pin_error_semantics,
              pin_tree_check]
+
+
+def pin_error_bits_accumulate(lib):
+    """Reading R11: every applicable error bit is reported (a bad token and a NaN row together)."""
+    K, V = 2, 6
+    lt = np.zeros((1, K + 1, V), np.float32)
+    lt[0, 2, 1] = np.nan
+    ld = np.zeros((1, K, V), np.float32)
+    x = np.array([[0, V + 3]], np.int32)
+    r = np.full((1, K), 0.5, np.float32)
+    u = np.full(1, 0.5, np.float32)
+    both = oracle.ERR_BAD_TOKEN | oracle.ERR_NONFINITE
+    assert oracle.verify_chain("f32", lt, ld, 1, K, V, 1.0, x, r, u, lib=lib)["err"][0] == both
+    assert oracle.verify_chain("f32", lt, None, 1, K, V, 0.0, x, None, None, lib=lib)["err"][0] == both
+    assert oracle.verify_ngram("f32", lt, 1, K, V, 1.0, x, r, u, lib=lib)["err"][0] == both
+
+
+FAST_PINS.append(pin_error_bits_accumulate)
