@@ -38,7 +38,9 @@
  *       node's row (lowest node index if several), until no child matches; the final token is
  *       the argmax of the last node's row.
  *   R10 flagged ties: |r_k - alpha_k| <= tol at an evaluated position, or u within tol of
- *       C_{i*-1}/S or C_{i*}/S at the drawn index i*.
+ *       C_{i*-1}/S or C_{i*}/S at the drawn index i*.  For the draft-model residual
+ *       max(0, p - q), whose total S < 1 comes from cancelling p against q, the band is tol / S
+ *       (the resolution of that normalised CDF in fp32 arithmetic; tol at S = 1).
  *   R11 invalid input: a draft token outside [0, V), a logits row holding NaN (or, when a softmax
  *       is taken, +inf, or only -inf), or a malformed parent array sets an error bit (every bit
  *       that applies, all rows checked); the request then accepts nothing and emits no token (-1).
@@ -176,9 +178,10 @@ int oracle_inverse_cdf(const double *w, int V, double u, double tol, double *S_o
  *   and the bonus draw at K), mass[K+1] (the residual mass S at k; sum of p at K),
  *   pos_flag[K+1] (CDF tie / zero-residual at k), req_flag (flags of the evaluated positions).
  */
-void oracle_verify_probs(int K, int V, const double *p, const double *q, const int *x,
-                         const float *r, float u, double tol, int *n_acc, int *out_tokens,
-                         double *alpha, int *cand, double *mass, int *pos_flag, int *req_flag)
+static void verify_probs_impl(int K, int V, const double *p, const double *q, const int *x,
+                              const float *r, float u, double tol, int scale_band, int *n_acc,
+                              int *out_tokens, double *alpha, int *cand, double *mass,
+                              int *pos_flag, int *req_flag)
 {
     double *w = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
     *req_flag = 0;
@@ -205,6 +208,11 @@ void oracle_verify_probs(int K, int V, const double *p, const double *q, const i
             double S2;
             c = oracle_inverse_cdf(pk, V, (double)u, tol, &S2, &fl);
             f |= ORF_ZERO_RESIDUAL;
+        } else if (scale_band && k < K && S < 1.0) {
+            /* R10: the residual max(0, p - q) cancels where p and q overlap; its normalised CDF
+             * is resolved only to about tol / S, so the tie band widens to tol / S */
+            double S3;
+            oracle_inverse_cdf(w, V, (double)u, tol / S, &S3, &fl);
         }
         if (fl)
             f |= ORF_CDF_TIE;
@@ -226,6 +234,15 @@ void oracle_verify_probs(int K, int V, const double *p, const double *q, const i
     for (int i = 0; i <= K; i++)
         out_tokens[i] = i < n ? x[i] : (i == n ? cand[n] : -1);
     free(w);
+}
+
+/* Draft-model chain on probabilities (the residual tie band scales with 1 / S, reading R10). */
+void oracle_verify_probs(int K, int V, const double *p, const double *q, const int *x,
+                         const float *r, float u, double tol, int *n_acc, int *out_tokens,
+                         double *alpha, int *cand, double *mass, int *pos_flag, int *req_flag)
+{
+    verify_probs_impl(K, V, p, q, x, r, u, tol, 1, n_acc, out_tokens, alpha, cand, mass, pos_flag,
+                      req_flag);
 }
 
 static void fail_request(int K, int *n_acc, int *out_tokens, double *alpha, int *cand,
@@ -358,8 +375,8 @@ void oracle_verify_ngram(int dtype, const void *target, int B, int K, int V, flo
             for (int k = 0; k < K && !e; k++)
                 q[(size_t)k * V + xb[k]] = 1.0;
             if (!e)
-                oracle_verify_probs(K, V, p, q, xb, r + (size_t)b * K, u[b], tol, o_n, o_tok, o_al,
-                                    o_cd, o_ms, o_pf, req_flag + b);
+                verify_probs_impl(K, V, p, q, xb, r + (size_t)b * K, u[b], tol, 0, o_n, o_tok,
+                                  o_al, o_cd, o_ms, o_pf, req_flag + b);
         }
         if (e) {
             fail_request(K, o_n, o_tok, o_al, o_cd, o_ms);

@@ -179,8 +179,12 @@ def pin_ngram_general_equals_shortcut(lib):
         u = np.float32(rng.integers(0, 1 << 24) / (1 << 24))
         g = oracle.verify_probs(p, q, x, r, u, lib=lib)
         d = oracle.verify_ngram_direct(p, x, r, u, lib=lib)
-        for key in ("num_accepted", "out_tokens", "cand", "pos_flag", "req_flag"):
+        for key in ("num_accepted", "out_tokens", "cand"):
             assert np.array_equal(g[key], d[key]), key
+        # the draft-model path widens its residual tie band to tol / S: its flags contain the
+        # shortcut's
+        assert np.all((g["pos_flag"] & d["pos_flag"]) == d["pos_flag"])
+        assert (g["req_flag"] & d["req_flag"]) == d["req_flag"]
         assert np.array_equal(g["alpha"], d["alpha"]) and np.array_equal(g["mass"], d["mass"])
         assert np.allclose(g["alpha"], p[np.arange(K), x], atol=0)  # alpha = p(x) for one-hot q
 
@@ -396,3 +400,23 @@ def pin_error_bits_accumulate(lib):
 
 
 FAST_PINS.append(pin_error_bits_accumulate)
+
+
+def pin_residual_band_scales_with_mass(lib):
+    """Reading R10: the tie band of the max(0, p - q) draw is tol / S (tol when S = 1)."""
+    p = np.array([[0.6, 0.4], [0.5, 0.5]])
+    q = np.array([[0.5, 0.5]])  # residual [0.1, 0]: S = 0.1, C/S = [1, 1]
+    x, r = [1], [0.9375]  # alpha = 0.8, rejected
+    for u, tie in [(2e-6, True), (5e-7, True), (2e-5, False), (0.5, False)]:
+        o = oracle.verify_probs(p, q, x, r, u, TOL, lib=lib)
+        assert o["num_accepted"] == 0 and o["out_tokens"][0] == 0
+        assert abs(o["mass"][0] - 0.1) < 1e-15
+        assert bool(o["req_flag"] & oracle.FLAG_CDF_TIE) == tie, (u, o)
+    # disjoint supports: S = 1, the band stays tol
+    p2 = np.array([[1.0, 0.0], [0.5, 0.5]])
+    q2 = np.array([[0.0, 1.0]])
+    o = oracle.verify_probs(p2, q2, [1], [0.5], 2e-6, TOL, lib=lib)
+    assert not (o["req_flag"] & oracle.FLAG_CDF_TIE)
+
+
+FAST_PINS.append(pin_residual_band_scales_with_mass)

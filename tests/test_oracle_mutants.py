@@ -41,6 +41,8 @@ MUTANTS = [
     ("f16_subnormal_scale", "ldexp((double)man, -24)", "ldexp((double)man, -25)"),
     ("ngram_onehot_weight", "q[(size_t)k * V + xb[k]] = 1.0;", "q[(size_t)k * V + xb[k]] = 0.5;"),
     ("greedy_compares_next_row", "while (n < K && x[n] == cand[n])", "while (n < K && x[n] == cand[n + 1])"),
+    ("residual_band_not_scaled", "oracle_inverse_cdf(w, V, (double)u, tol / S, &S3, &fl);",
+     "oracle_inverse_cdf(w, V, (double)u, tol, &S3, &fl);"),
     ("bad_token_check_dropped", "if (xb[k] < 0 || xb[k] >= V)\n                e |= ORE_BAD_TOKEN;",
      "if (0)\n                e |= ORE_BAD_TOKEN;"),
 ]
