@@ -1,0 +1,485 @@
+#!/usr/bin/env python
+"""Benchmark of the speculative-decoding verification step on GB300.
+
+One "step" is one verification call over one batch of the workload (all steps of the hot path:
+softmax statistics, acceptance scan, residual / bonus draw, or the tree argmax and walk): a
+ticket-clearing memset and one kernel launch, two for draft-model chains (the residual draw
+re-reads the rejected pair).  Default workload: chain verification with draft-model logits,
+B=64, K=5, V=128256, fp32, T=1.0 (704 logits rows, 361 MB per step).
+
+Prints ONE JSON line (rank 0).  `value` = verified logits rows per second (whole job), timed on
+the device with CUDA events, inputs resident in HBM; `e2e` = the same metric through the public
+API with the step's inputs copied from pinned host memory and the results read back;
+`roofline` = algorithmic bytes per call over the call's mean device time (CUDA events around
+each call on the launching stream), against the measured HBM copy bandwidth; `cpu_baseline` =
+the CPU oracle on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload chain_batched|tree_greedy|ngram]
+  python bench.py --impl reference ...   (the CPU oracle as the reference arm)
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "verify rows/sec and achieved HBM GB/s (fraction of GB300 peak) at V=128256"
+WORKLOADS = {
+    "chain_batched": dict(kind="chain", B=64, K=5, V=128256, dtype="f32", T=1.0,
+                          desc="chain verify, batched: B=64 K=5 V=128256 fp32 T=1.0, draft-model logits"),
+    "tree_greedy": dict(kind="tree", B=16, N=60, V=128256, dtype="bf16",
+                        desc="greedy tree verify: B=16, 61-node EAGLE-2-like tree (depth 6), V=128256 bf16"),
+    "ngram": dict(kind="ngram", B=256, K=5, V=151936, dtype="bf16", T=0.8,
+                  desc="n-gram prompt-lookup verify: B=256 K=5 V=151936 bf16 T=0.8, one-hot draft"),
+}
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["speculative_decoding_verification_82_gb300/csrc/verify_kernel.cuh",
+                  "speculative_decoding_verification_82_gb300/csrc/verify_common.cuh",
+                  "speculative_decoding_verification_82_gb300/csrc/spec_verify_api.cu"]
+
+
+# ----------------------------------------------------------------------------- inputs ----
+def make_inputs(name: str, seed: int):
+    from speculative_decoding_verification_82_gb300 import synth
+
+    if name == "chain_batched":
+        return synth.chain_batched(seed=seed)
+    if name == "tree_greedy":
+        return synth.tree_greedy(seed=seed)
+    if name == "ngram":
+        return synth.ngram(seed=seed)
+    raise ValueError(name)
+
+
+def rows_per_request(w: dict) -> int:
+    if w["kind"] == "chain":
+        return 2 * w["K"] + 1
+    if w["kind"] == "ngram":
+        return w["K"] + 1
+    return w["N"] + 1
+
+
+def launches_per_step(w: dict) -> int:
+    """Kernel launches of one call: the stats kernel, plus the residual kernel for draft-model
+    chains (the ticket-clearing memset is not a kernel of this library)."""
+    return 2 if w["kind"] == "chain" else 1
+
+
+def algorithmic_bytes(w: dict) -> int:
+    """Logits read once, the small inputs read once, the outputs written once."""
+    B, V = w["B"], w["V"]
+    es = 4 if w["dtype"] == "f32" else 2
+    logits = B * rows_per_request(w) * V * es
+    if w["kind"] == "tree":
+        small_in = 2 * B * (w["N"] + 1) * 4
+        out = B * 4 + 2 * B * (w["N"] + 1) * 4 + B * 4
+    else:
+        K = w["K"]
+        small_in = B * K * 4 * 2 + B * 4
+        out = B * 4 + B * (K + 1) * 4 + B * 4 + B * 4
+    return logits + small_in + out
+
+
+# ------------------------------------------------------------------------------ clocks ----
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def stop(self, t0: float, t1: float) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.12)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        inside = [l for t, l in self.lines if t0 <= t <= t1]
+        window = "timed region"
+        if not inside:  # timed region shorter than the sampling interval: nearest samples
+            inside = [l for t, l in self.lines if t0 - 0.2 <= t <= t1 + 0.2]
+            window = "timed region +- 0.2 s"
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in inside:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm), "window": window}
+
+
+# --------------------------------------------------------------------- peaks / traffic ----
+def hbm_peak() -> tuple[float, str]:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            return float(json.load(f)["hbm_gbs"]), "of measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "of fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload: str):
+    """DRAM bytes per call from the committed ncu summary, if it matches the current kernels."""
+    p = os.path.join(ROOT, "profiles", f"verify_{workload}.md")
+    try:
+        text = open(p).read()
+    except OSError:
+        return None
+    m_b = re.search(r"traffic_bytes_per_call:\s*([0-9]+)", text)
+    m_h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
+    if not m_b or not m_h or m_h.group(1) != kernel_source_hash():
+        return None
+    return int(m_b.group(1))
+
+
+# -------------------------------------------------------------------------- CPU oracle ----
+def oracle_run(w: dict, inp, requests, threads: int):
+    import oracle
+
+    if w["kind"] == "chain":
+        return oracle.verify_chain(inp.dtype, inp.target, inp.draft, inp.B, inp.K, inp.V,
+                                   float(inp.temperature), inp.draft_tokens, inp.r, inp.u,
+                                   threads=threads, requests=requests)
+    if w["kind"] == "ngram":
+        return oracle.verify_ngram(inp.dtype, inp.target, inp.B, inp.K, inp.V, float(inp.temperature),
+                                   inp.draft_tokens, inp.r, inp.u, threads=threads, requests=requests)
+    return oracle.verify_tree_greedy(inp.dtype, inp.target, inp.B, inp.N, inp.V, inp.node_tokens,
+                                     inp.parents, threads=threads, requests=requests)
+
+
+def oracle_timed(w: dict, inp, n_req: int, threads: int) -> float:
+    """Wall time of the oracle over requests [0, n_req), requests split across threads (ctypes
+    releases the GIL, so each thread runs on its own core)."""
+    import oracle
+
+    rngs = oracle._ranges(n_req, threads)
+    t0 = time.perf_counter()
+    ts = [threading.Thread(target=oracle_run, args=(w, inp, rg, 1)) for rg in rngs]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(w: dict, inp, min_wall: float = 1.0) -> dict:
+    cores = os.cpu_count() or 1
+    n_req = w["B"]
+    threads = min(cores, n_req)
+    reps, wall = 0, 0.0
+    while wall < min_wall or reps < 2:
+        wall += oracle_timed(w, inp, n_req, threads)
+        reps += 1
+    rows = reps * n_req * rows_per_request(w)
+    return {"value": rows / wall, "unit": "rows/s", "cores": threads, "kind": "oracle",
+            "sample": f"all {n_req} requests of the workload ({n_req * rows_per_request(w)} rows), "
+                      f"{reps} repetitions, requests split over {threads} threads, {wall:.2f} s wall"}
+
+
+# ------------------------------------------------------------------------ GPU arm ----
+def dist_setup():
+    import torch
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    return rank, world, local
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+class DeviceCase:
+    """One input set (on the device, or in pinned host memory) plus preallocated outputs;
+    `call()` is one step through the public binding."""
+
+    def __init__(self, w, inp, dev, workspace, host_pinned: bool = False):
+        import torch
+
+        from speculative_decoding_verification_82_gb300 import binding
+
+        self.w, self.binding = w, binding
+        tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w["dtype"]]
+
+        def tens(a, dt=None):
+            a = np.ascontiguousarray(a)
+            t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if dt == torch.bfloat16 else torch.from_numpy(a)
+            return t.pin_memory() if host_pinned else t.to(dev)
+
+        self.target = tens(inp.target, tdt)
+        B = w["B"]
+        self.draft = None
+        if w["kind"] == "tree":
+            self.tokens, self.parents = tens(inp.node_tokens), tens(inp.parents)
+            N1 = w["N"] + 1
+            shapes = dict(accept_len=(B,), path_nodes=(B, N1), out_tokens=(B, N1), err_flags=(B,))
+        else:
+            self.draft = tens(inp.draft, tdt) if w["kind"] == "chain" else None
+            self.x, self.r, self.u = tens(inp.draft_tokens), tens(inp.r), tens(inp.u)
+            self.T = float(inp.temperature)
+            K1 = w["K"] + 1
+            shapes = dict(num_accepted=(B,), out_tokens=(B, K1), residual_mass=(B,), err_flags=(B,))
+        fdt = {"residual_mass": torch.float32}
+        if host_pinned:
+            self.out = {k: torch.empty(s, dtype=fdt.get(k, torch.int32)).pin_memory() for k, s in shapes.items()}
+        else:
+            self.out = {k: torch.empty(s, dtype=fdt.get(k, torch.int32), device=dev) for k, s in shapes.items()}
+        self.ws = workspace
+
+    def inputs(self):
+        if self.w["kind"] == "tree":
+            return [self.target, self.tokens, self.parents]
+        return [t for t in (self.target, self.draft, self.x, self.r, self.u) if t is not None]
+
+    def call(self):
+        b = self.binding
+        if self.w["kind"] == "tree":
+            return b.spec_verify_tree_greedy(self.target, self.tokens, self.parents, workspace=self.ws, out=self.out)
+        if self.w["kind"] == "ngram":
+            return b.spec_verify_ngram(self.target, self.x, self.r, self.u, self.T, workspace=self.ws, out=self.out)
+        return b.spec_verify_chain(self.target, self.draft, self.x, self.r, self.u, self.T, workspace=self.ws,
+                                   out=self.out)
+
+
+def _e2e_step(dev_case: DeviceCase, host_case: DeviceCase):
+    for d, h in zip(dev_case.inputs(), host_case.inputs()):
+        d.copy_(h, non_blocking=True)
+    dev_case.call()
+    for k, t in dev_case.out.items():
+        host_case.out[k].copy_(t, non_blocking=True)
+
+
+def run_gpu(args, w) -> None:
+    import torch
+
+    from speculative_decoding_verification_82_gb300 import binding
+
+    rank, world, local = dist_setup()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    binding.library()  # fail loudly if the CUDA library is missing
+
+    n_sets = 2  # alternate two input sets; each is larger than L2 as well
+    inputs = [make_inputs(args.workload, seed=1000 * rank + s) for s in range(n_sets)]
+    rows_req = rows_per_request(w)
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w["dtype"]]
+    ws = binding.make_workspace(w["B"], rows_req, w["V"], tdt, dev)
+    cases = [DeviceCase(w, inp, dev, ws) for inp in inputs]
+    stream = torch.cuda.current_stream(dev)
+
+    for i in range(args.warmup):
+        cases[i % n_sets].call()
+    torch.cuda.synchronize()
+    barrier(world)
+
+    K = args.steps
+    ev0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.15)
+    torch.cuda.synchronize()
+    barrier(world)
+    t_host0 = time.perf_counter()
+    start.record(stream)
+    for i in range(K):
+        ev0[i].record(stream)
+        cases[i % n_sets].call()
+        ev1[i].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    t_host1 = time.perf_counter()
+    barrier(world)
+    clk = clocks.stop(t_host0, t_host1)
+    elapsed_ms = max_over_ranks(start.elapsed_time(end), world)
+    mean_call_ms = statistics.fmean(a.elapsed_time(b) for a, b in zip(ev0, ev1))
+
+    rows_step = w["B"] * rows_req
+    value = world * rows_step * K / (elapsed_ms / 1e3)
+    alg_bytes = algorithmic_bytes(w)
+    achieved = alg_bytes / (mean_call_ms / 1e3) / 1e9
+    peak, peak_src = hbm_peak()
+
+    # ---- end to end through the public API: pinned host -> device, call, results -> host ----
+    host = [DeviceCase(w, inp, dev, ws, host_pinned=True) for inp in inputs]
+    e2e_steps = max(3, min(K, args.e2e_steps))
+    h2d = sum(t.numel() * t.element_size() for t in host[0].inputs())
+    d2h = sum(t.numel() * t.element_size() for t in host[0].out.values())
+    for i in range(2):
+        _e2e_step(cases[i % n_sets], host[i % n_sets])
+    torch.cuda.synchronize()
+    barrier(world)
+    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_s.record(stream)
+    for i in range(e2e_steps):
+        _e2e_step(cases[i % n_sets], host[i % n_sets])
+    e_e.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e_s.elapsed_time(e_e), world)
+    e2e_value = world * rows_step * e2e_steps / (e2e_ms / 1e3)
+
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": elapsed_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w["dtype"],
+        "data": "synthetic (seeded Philox; logits, tokens and uniforms per the workload recipe)",
+        "config": {"workload": w["desc"], "B": w["B"], "V": w["V"],
+                   **({"K": w["K"]} if "K" in w else {"N": w["N"]}),
+                   "rows_per_step": rows_step, "requests_per_s": value / rows_req,
+                   "l2": f"inputs {alg_bytes / 2**20:.0f} MiB per step > 129 MiB L2; {n_sets} input sets alternated",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "peak_source": peak_src,
+                     "traffic": profiled_traffic(args.workload), "algorithmic_bytes_per_call": alg_bytes,
+                     "mean_call_us": mean_call_ms * 1e3,
+                     "kernel": (f"stats_kernel<{w['kind']},{w['dtype']}>"
+                                + (" + residual_kernel (one call)" if w["kind"] == "chain" else ""))},
+        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
+        "gpu_launches": K * launches_per_step(w),
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inputs[0])
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ reference arm ----
+def run_reference(args, w) -> None:
+    """The CPU oracle as the reference arm (the pages give no implementation to install)."""
+    if int(os.environ.get("RANK", "0")) != 0:
+        return
+    inp = make_inputs(args.workload, seed=0)
+    cores = os.cpu_count() or 1
+    t_one = oracle_timed(w, inp, 1, 1)
+    budget = 150.0 / max(1, args.steps + args.warmup)  # keep the whole run within a few minutes
+    n_req = int(max(1, min(w["B"], cores * budget / max(t_one, 1e-6))))
+    threads = min(cores, n_req)
+    for _ in range(args.warmup):
+        oracle_timed(w, inp, n_req, threads)
+    t = 0.0
+    for _ in range(args.steps):
+        t += oracle_timed(w, inp, n_req, threads)
+    value = args.steps * n_req * rows_per_request(w) / t
+    line = {
+        "impl": "reference",
+        "metric": METRIC,
+        "value": value, "unit": "rows/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"],
+        "data": "synthetic (seeded Philox)",
+        "config": {"workload": w["desc"], "B": w["B"], "V": w["V"],
+                   "rows_per_step": n_req * rows_per_request(w)},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{n_req} request(s) of the workload per step "
+                                   f"({n_req * rows_per_request(w)} rows), split over {threads} threads"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="chain_batched", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=40)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w)
+    else:
+        run_gpu(args, w)
+
+
+if __name__ == "__main__":
+    main()

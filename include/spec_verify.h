@@ -1,0 +1,169 @@
+/*
+ * spec_verify.h -- C ABI of a GB300 (sm_103a) library for the target-side verification step of
+ * lossless speculative decoding.
+ *
+ * The method: "Speculative Decoding in Production: From Draft Models to EAGLE-3 Dynamic Trees
+ * for 3x-5x Lossless Acceleration" (blog.llmgo.top), section I.1 "Verification via Modified
+ * Rejection Sampling": for each draft token x_k, alpha = min(1, p(x_k)/q(x_k)); draw r ~ U(0,1);
+ * accept iff r <= alpha, and stop at the first rejection; after a rejection, resample from the
+ * normalised positive residual max(0, p - q) / sum max(0, p - q).  The "Invariance Theorem"
+ * paragraph that follows states that the emitted tokens then follow p exactly, for greedy
+ * decoding and for temperature sampling.  Tree verification: same page, section III.2 "The Tree
+ * Attention Verification Mechanism" (a rejected branch is skipped, the matching sibling branch
+ * is accepted).  Draft mechanisms (draft model, EAGLE head, prompt n-gram lookup): "Accelerating
+ * Autoregressive LLM Inference 3x with Lossless Speculative Decoding and EAGLE Heads"
+ * (x078.com), opening section.
+ *
+ * Conventions common to every call
+ *  - Every pointer argument is a DEVICE pointer (cudaMalloc / torch CUDA tensor) unless stated;
+ *    the caller owns every buffer; the library allocates nothing.
+ *  - Layouts are row-major and contiguous with the vocabulary innermost.  Logits pointers must
+ *    be aligned to their element size (16-byte alignment is fastest).
+ *  - Calls are asynchronous on `stream` and never synchronise the host.  A status other than
+ *    SPEC_OK means nothing was launched (argument errors) or a launch failed (SPEC_ERR_CUDA).
+ *  - Per-request problems found on the device (a draft token outside [0, V), a logits row with
+ *    NaN, or with +inf / only -inf where a softmax is taken, a malformed parent array, a device
+ *    wait that timed out) set bits in err_flags[b]; that request then accepts nothing and emits
+ *    no token (num_accepted = 0 / accept_len = 0, every output token -1).  Nothing traps.
+ *  - Temperature: p = softmax(logits / T) for T > 0.  T == 0 selects greedy verification: the
+ *    target distribution is one-hot at the row argmax (lowest index on ties) and draft logits
+ *    are not read.
+ *  - Uniforms: r[b][k] in (0, 1] for the acceptance test; u[b] in [0, 1) for the draw after the
+ *    accepted prefix (residual resample or bonus token).  Draws use the inverse CDF: the smallest
+ *    token i whose cumulative weight exceeds u * (total weight); zero-weight tokens are never
+ *    drawn.
+ *  - Workspace: `workspace` (device memory, 256-byte aligned) must hold
+ *    spec_verify_workspace_bytes(...) bytes.  Its contents need no initialisation and are
+ *    scratch between calls: each call first clears its ticket counters (one cudaMemsetAsync of a
+ *    few bytes per request on `stream`).  A workspace must not be shared by calls that may run
+ *    concurrently.
+ *  - Reads: every logits row is read from HBM once; a draft-model chain call that rejects at
+ *    position n reads the target and draft rows at n a second time (the residual max(0, p - q)
+ *    needs both rows' normalisers first).  A call is one memset and one kernel launch, or two
+ *    launches for draft-model chains with T > 0 (three when probability rows are requested).
+ */
+#ifndef SPEC_VERIFY_H
+#define SPEC_VERIFY_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; NULL is the legacy default stream. */
+typedef struct CUstream_st *spec_stream_t;
+
+typedef enum {
+    SPEC_OK = 0,
+    SPEC_ERR_INVALID_ARG = 1, /* bad shape, NULL required pointer, bad temperature, ... */
+    SPEC_ERR_CUDA = 2,        /* a CUDA runtime call or a kernel launch failed */
+    SPEC_ERR_WORKSPACE = 3,   /* workspace NULL, misaligned or smaller than required */
+    SPEC_ERR_UNSUPPORTED = 4  /* a size beyond the supported maximum */
+} spec_status_t;
+
+typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1, SPEC_DTYPE_F16 = 2 } spec_dtype_t;
+
+/* Bits of err_flags[b]. */
+#define SPEC_ERRF_BAD_TOKEN 1 /* a draft / node token outside [0, V) */
+#define SPEC_ERRF_NONFINITE 2 /* NaN logits, or +inf / all -inf where a softmax is taken */
+#define SPEC_ERRF_TIMEOUT 4   /* a bounded device wait gave up (should never happen) */
+#define SPEC_ERRF_BAD_TREE 8  /* parents[0] != -1 or parents[i] not in [0, i) */
+
+/* Largest supported sizes. */
+#define SPEC_MAX_K 256           /* draft tokens per request (chain / n-gram) */
+#define SPEC_MAX_TREE_NODES 4096 /* N + 1 for tree verification */
+
+/* Bytes of workspace for a call on B requests with vocabulary V of `dtype`, where
+ * rows_per_request is the number of logits rows the call reads per request:
+ *   spec_verify_chain with T > 0: 2K + 1;  spec_verify_chain with T == 0 and spec_verify_ngram:
+ *   K + 1;  spec_verify_tree_greedy: N + 1.
+ * A workspace sized for more rows (or a larger B) also serves a smaller call.  Returns 0 for
+ * invalid sizes. */
+size_t spec_verify_workspace_bytes(int B, int rows_per_request, int V, spec_dtype_t dtype);
+
+/*
+ * Chain verification with a draft model or an EAGLE head (the draft side is logits).
+ *
+ * target_logits  [B][K+1][V] dtype; row k scores draft position k given the accepted prefix,
+ *                row K scores the bonus position.
+ * draft_logits   [B][K][V] dtype; the draft distribution at each draft position.  Not read
+ *                (may be NULL) when temperature == 0.
+ * draft_tokens   [B][K] int32, the drafted tokens x_k.
+ * r              [B][K] float, acceptance uniforms in (0, 1].  Not read when temperature == 0.
+ * u              [B] float, uniforms in [0, 1) for the residual / bonus draw.  Not read when
+ *                temperature == 0.
+ * Outputs:
+ * num_accepted   [B] int32, n in [0, K]: the length of the accepted prefix.
+ * out_tokens     [B][K+1] int32: x_1..x_n, then the drawn token (residual resample at position
+ *                n if n < K, bonus token from row K if n == K), then -1.
+ * residual_mass  [B] float or NULL: the total weight the draw used, i.e. sum max(0, p - q) at
+ *                the rejected position (the total-variation distance of p and q there), 1 for a
+ *                bonus draw, 1 in greedy mode.
+ * err_flags      [B] int32 or NULL: SPEC_ERRF_* bits, 0 when the request verified normally.
+ * Optional per-position diagnostics (NULL to skip):
+ * accept_prob    [B][K] float: alpha_k = min(1, p_k(x_k)/q_k(x_k)) at every position (greedy:
+ *                1 if x_k equals the target argmax, else 0).
+ * cand_tokens    [B][K+1] int32: the token the draw would emit at position k (residual at
+ *                k < K, bonus at K; greedy: the argmax of row k).
+ * pos_mass       [B][K+1] float: the residual mass at each position (bonus row: 1).
+ * target_probs   [B][K+1][V] float: p rows (T > 0 only; an extra launch, for testing).
+ * draft_probs    [B][K][V] float: q rows (T > 0 only).
+ * Requesting cand_tokens or pos_mass makes the call draw at every position, which re-reads the
+ * pair (draft-model chain) or one chunk per row (n-gram); leave them NULL on the hot path.
+ */
+spec_status_t spec_verify_chain(const void *target_logits, const void *draft_logits,
+                                spec_dtype_t dtype, int B, int K, int V, float temperature,
+                                const int32_t *draft_tokens, const float *r, const float *u,
+                                int32_t *num_accepted, int32_t *out_tokens, float *residual_mass,
+                                int32_t *err_flags, float *accept_prob, int32_t *cand_tokens,
+                                float *pos_mass, float *target_probs, float *draft_probs,
+                                void *workspace, size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * Chain verification with a prompt n-gram lookup draft: q_k is one-hot at x_k, so
+ * alpha_k = p_k(x_k) and the residual at a rejected position is p_k with x_k removed.  No draft
+ * logits exist.  Arguments and outputs as spec_verify_chain (target_probs likewise optional);
+ * temperature == 0 gives the greedy chain.
+ */
+spec_status_t spec_verify_ngram(const void *target_logits, spec_dtype_t dtype, int B, int K,
+                                int V, float temperature, const int32_t *draft_tokens,
+                                const float *r, const float *u, int32_t *num_accepted,
+                                int32_t *out_tokens, float *residual_mass, int32_t *err_flags,
+                                float *accept_prob, int32_t *cand_tokens, float *pos_mass,
+                                float *target_probs, void *workspace, size_t workspace_bytes,
+                                spec_stream_t stream);
+
+/*
+ * Greedy verification of a draft tree (EAGLE-2 style).  Node 0 is the root (the last accepted
+ * token); nodes 1..N are draft tokens, each with a parent of smaller index.
+ *
+ * target_logits  [B][N+1][V] dtype; row n is the target's prediction after node n.
+ * node_tokens    [B][N+1] int32; entry 0 is ignored.
+ * parents        [B][N+1] int32; parents[0] = -1 and 0 <= parents[i] < i.
+ * The walk starts at the root and repeatedly moves to the child whose token equals the argmax
+ * of the current node's row (the lowest node index if several do), until no child matches.
+ * Outputs:
+ * accept_len     [B] int32: accepted draft tokens on the path (0..depth).
+ * path_nodes     [B][N+1] int32: node ids on the accepted path, root first, then -1.
+ * out_tokens     [B][N+1] int32: the accepted tokens, then the argmax of the last node's row
+ *                (the correction or bonus token), then -1.
+ * err_flags      [B] int32 or NULL.
+ * node_argmax    [B][N+1] int32 or NULL: the argmax of every row.
+ */
+spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t dtype, int B,
+                                      int N, int V, const int32_t *node_tokens,
+                                      const int32_t *parents, int32_t *accept_len,
+                                      int32_t *path_nodes, int32_t *out_tokens,
+                                      int32_t *err_flags, int32_t *node_argmax, void *workspace,
+                                      size_t workspace_bytes, spec_stream_t stream);
+
+/* Human-readable name of a status code (static string). */
+const char *spec_status_string(spec_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H */

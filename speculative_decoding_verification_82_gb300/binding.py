@@ -1,0 +1,195 @@
+"""Thin ctypes binding of the C ABI declared in include/spec_verify.h.
+
+Argument marshalling only: the functions take torch CUDA tensors, check their shape, dtype and
+device, allocate outputs and the workspace when the caller did not supply them, and pass raw
+pointers and the current CUDA stream to the library.  Every step of the verification runs in the
+library's kernels; there is no other implementation to fall back on, so a missing library raises.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+from ctypes import c_float, c_int, c_size_t, c_void_p
+
+import torch
+
+from .build import LIB_PATH
+
+SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_CUDA, SPEC_ERR_WORKSPACE, SPEC_ERR_UNSUPPORTED = range(5)
+ERRF_BAD_TOKEN, ERRF_NONFINITE, ERRF_TIMEOUT, ERRF_BAD_TREE = 1, 2, 4, 8
+MAX_K, MAX_TREE_NODES = 256, 4096
+DTYPE_CODE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+
+EXPORTED = ("spec_verify_workspace_bytes", "spec_verify_chain", "spec_verify_ngram",
+            "spec_verify_tree_greedy", "spec_status_string")
+
+_lib = None
+
+
+class SpecVerifyError(RuntimeError):
+    pass
+
+
+def library(path: str | None = None) -> ctypes.CDLL:
+    """Load libspecverify.so (built by __graft_entry__.build()); raises if it is missing."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    p = path or LIB_PATH
+    if not os.path.exists(p):
+        raise SpecVerifyError(f"CUDA library not built: {p} is missing (run __graft_entry__.build())")
+    lib = ctypes.CDLL(p)
+    P, I, F, Z = c_void_p, c_int, c_float, c_size_t
+    lib.spec_verify_workspace_bytes.argtypes = [I, I, I, I]
+    lib.spec_verify_workspace_bytes.restype = Z
+    lib.spec_verify_chain.argtypes = [P, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
+    lib.spec_verify_chain.restype = I
+    lib.spec_verify_ngram.argtypes = [P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
+    lib.spec_verify_ngram.restype = I
+    lib.spec_verify_tree_greedy.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, P, Z, P]
+    lib.spec_verify_tree_greedy.restype = I
+    lib.spec_status_string.argtypes = [I]
+    lib.spec_status_string.restype = ctypes.c_char_p
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _check(status: int) -> None:
+    if status != SPEC_OK:
+        name = library().spec_status_string(status).decode()
+        raise SpecVerifyError(f"{name} ({status})")
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else c_void_p(t.data_ptr())
+
+
+def _stream(device) -> c_void_p:
+    return c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _need(t, name: str, dtype, shape, device) -> torch.Tensor:
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch tensor")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t
+
+
+def workspace_bytes(B: int, rows_per_request: int, V: int, dtype: torch.dtype) -> int:
+    """Workspace bytes for B requests reading `rows_per_request` logits rows of V elements each
+    (draft-model chain: 2K+1, greedy chain / n-gram: K+1, tree: N+1)."""
+    return int(library().spec_verify_workspace_bytes(B, rows_per_request, V, DTYPE_CODE[dtype]))
+
+
+def make_workspace(B: int, rows_per_request: int, V: int, dtype: torch.dtype, device) -> torch.Tensor:
+    """A workspace for such calls (its contents need no initialisation)."""
+    n = max(256, workspace_bytes(B, rows_per_request, V, dtype))
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def _out(given, name, dtype, shape, device):
+    if given is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    return _need(given, name, dtype, shape, device)
+
+
+def _opt(given, name, dtype, shape, device):
+    return None if given is None else _need(given, name, dtype, shape, device)
+
+
+def _chain_like(ngram: bool, target_logits, draft_logits, draft_tokens, r, u, temperature,
+                workspace, out, accept_prob, cand_tokens, pos_mass, target_probs, draft_probs):
+    lib = library()
+    dev = target_logits.device
+    if target_logits.dtype not in DTYPE_CODE or target_logits.dim() != 3:
+        raise TypeError("target_logits must be a [B][K+1][V] float32/bfloat16/float16 tensor")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    T = float(temperature)
+    _need(target_logits, "target_logits", None, (B, K1, V), dev)
+    if draft_tokens is None:
+        draft_tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
+    _need(draft_tokens, "draft_tokens", torch.int32, (B, K), dev)
+    if not ngram and T > 0 and K > 0:
+        _need(draft_logits, "draft_logits", target_logits.dtype, (B, K, V), dev)
+    if T > 0:
+        _need(r, "r", torch.float32, (B, K), dev)
+        _need(u, "u", torch.float32, (B,), dev)
+    if workspace is None:
+        rows = 2 * K + 1 if (not ngram and T > 0 and K > 0) else K1
+        workspace = make_workspace(B, rows, V, target_logits.dtype, dev)
+    out = dict(out or {})
+    na = _out(out.get("num_accepted"), "num_accepted", torch.int32, (B,), dev)
+    ot = _out(out.get("out_tokens"), "out_tokens", torch.int32, (B, K1), dev)
+    rm = _out(out.get("residual_mass"), "residual_mass", torch.float32, (B,), dev)
+    ef = _out(out.get("err_flags"), "err_flags", torch.int32, (B,), dev)
+    ap = _opt(accept_prob, "accept_prob", torch.float32, (B, K), dev)
+    ct = _opt(cand_tokens, "cand_tokens", torch.int32, (B, K1), dev)
+    pm = _opt(pos_mass, "pos_mass", torch.float32, (B, K1), dev)
+    tp = _opt(target_probs, "target_probs", torch.float32, (B, K1, V), dev)
+    tail = (_ptr(na), _ptr(ot), _ptr(rm), _ptr(ef), _ptr(ap), _ptr(ct), _ptr(pm), _ptr(tp))
+    if ngram:
+        st = lib.spec_verify_ngram(_ptr(target_logits), DTYPE_CODE[target_logits.dtype], B, K, V, T,
+                                   _ptr(draft_tokens), _ptr(r), _ptr(u), *tail, _ptr(workspace),
+                                   workspace.numel(), _stream(dev))
+    else:
+        dp = _opt(draft_probs, "draft_probs", torch.float32, (B, K, V), dev)
+        st = lib.spec_verify_chain(_ptr(target_logits), _ptr(draft_logits),
+                                   DTYPE_CODE[target_logits.dtype], B, K, V, T, _ptr(draft_tokens),
+                                   _ptr(r), _ptr(u), *tail, _ptr(dp), _ptr(workspace),
+                                   workspace.numel(), _stream(dev))
+    _check(st)
+    return dict(num_accepted=na, out_tokens=ot, residual_mass=rm, err_flags=ef)
+
+
+def spec_verify_chain(target_logits, draft_logits, draft_tokens, r, u, temperature, *,
+                      workspace=None, out=None, accept_prob=None, cand_tokens=None, pos_mass=None,
+                      target_probs=None, draft_probs=None) -> dict:
+    """Chain verification with draft logits (draft model / EAGLE head).  See spec_verify.h."""
+    return _chain_like(False, target_logits, draft_logits, draft_tokens, r, u, temperature,
+                       workspace, out, accept_prob, cand_tokens, pos_mass, target_probs,
+                       draft_probs)
+
+
+def spec_verify_ngram(target_logits, draft_tokens, r, u, temperature, *, workspace=None, out=None,
+                      accept_prob=None, cand_tokens=None, pos_mass=None,
+                      target_probs=None) -> dict:
+    """Chain verification with a one-hot (prompt n-gram lookup) draft.  See spec_verify.h."""
+    return _chain_like(True, target_logits, None, draft_tokens, r, u, temperature, workspace, out,
+                       accept_prob, cand_tokens, pos_mass, target_probs, None)
+
+
+def spec_verify_tree_greedy(target_logits, node_tokens, parents, *, workspace=None, out=None,
+                            node_argmax=None) -> dict:
+    """Greedy verification of a draft tree.  See spec_verify.h."""
+    lib = library()
+    dev = target_logits.device
+    if target_logits.dtype not in DTYPE_CODE or target_logits.dim() != 3:
+        raise TypeError("target_logits must be a [B][N+1][V] float32/bfloat16/float16 tensor")
+    B, N1, V = target_logits.shape
+    _need(target_logits, "target_logits", None, (B, N1, V), dev)
+    _need(node_tokens, "node_tokens", torch.int32, (B, N1), dev)
+    _need(parents, "parents", torch.int32, (B, N1), dev)
+    if workspace is None:
+        workspace = make_workspace(B, N1, V, target_logits.dtype, dev)
+    out = dict(out or {})
+    al = _out(out.get("accept_len"), "accept_len", torch.int32, (B,), dev)
+    pn = _out(out.get("path_nodes"), "path_nodes", torch.int32, (B, N1), dev)
+    ot = _out(out.get("out_tokens"), "out_tokens", torch.int32, (B, N1), dev)
+    ef = _out(out.get("err_flags"), "err_flags", torch.int32, (B,), dev)
+    am = _opt(node_argmax, "node_argmax", torch.int32, (B, N1), dev)
+    st = lib.spec_verify_tree_greedy(_ptr(target_logits), DTYPE_CODE[target_logits.dtype], B, N1 - 1,
+                                     V, _ptr(node_tokens), _ptr(parents), _ptr(al), _ptr(pn),
+                                     _ptr(ot), _ptr(ef), _ptr(am), _ptr(workspace),
+                                     workspace.numel(), _stream(dev))
+    _check(st)
+    return dict(accept_len=al, path_nodes=pn, out_tokens=ot, err_flags=ef)

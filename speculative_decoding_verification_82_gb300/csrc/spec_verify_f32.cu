@@ -1,0 +1,3 @@
+// f32 instantiations of the verification kernels.
+#include "verify_kernel.cuh"
+template cudaError_t specv::launch_verify<float>(int, const specv::Params&, const specv::LaunchPlan&, cudaStream_t);

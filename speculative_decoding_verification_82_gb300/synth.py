@@ -253,7 +253,9 @@ def eagle_tree_parents(levels=TREE_LEVELS) -> np.ndarray:
 
 def tree_greedy(seed: int = 0, B: int = 16, V: int = 128256, boost: float = 6.0,
                 boost_frac: float = 0.7, dtype: str = "bf16",
-                parents: np.ndarray | None = None) -> TreeInputs:
+                parents: np.ndarray | None = None, path_boost: float = 0.0) -> TreeInputs:
+    """`path_boost` > 0 additionally boosts, per request, every node on the path from the root to
+    one seeded deepest leaf (in its parent's row), so long paths occur."""
     par = eagle_tree_parents() if parents is None else np.asarray(parents, dtype=np.int32)
     N1 = par.size
     trng = _rng(seed, _S_TREE)
@@ -269,6 +271,17 @@ def tree_greedy(seed: int = 0, B: int = 16, V: int = 128256, boost: float = 6.0,
         for n in range(1, N1):
             if brng.random() < boost_frac:
                 t32[b, par[n], tokens[b, n]] += np.float32(boost)
+    if path_boost > 0:
+        depth = np.zeros(N1, np.int64)
+        for i in range(1, N1):
+            depth[i] = depth[par[i]] + 1
+        deepest = np.nonzero(depth == depth.max())[0]
+        lrng = _rng(seed, _S_SPIKE)
+        for b in range(B):
+            v = int(lrng.choice(deepest))
+            while v != 0:
+                t32[b, par[v], tokens[b, v]] += np.float32(path_boost)
+                v = int(par[v])
     return TreeInputs("tree_greedy", dtype, B, N1 - 1, V, encode(t32, dtype), tokens,
                       np.broadcast_to(par, (B, N1)).copy())
 

@@ -1,0 +1,106 @@
+"""The C-ABI library loads, exports every symbol include/spec_verify.h declares, and rejects bad
+arguments on the host before any CUDA call (so these run without a GPU)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from speculative_decoding_verification_82_gb300 import binding
+from speculative_decoding_verification_82_gb300.build import INCLUDE, build
+
+HEADER = os.path.join(INCLUDE, "spec_verify.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build()
+    return binding.library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(spec_\w+)\s*\(", text)))
+
+
+def test_header_declarations_match_binding():
+    assert declared_functions() == sorted(binding.EXPORTED)
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_workspace_size(lib):
+    # V = 128256 fp32 -> 16 chunks of 8016 elements.  Layout: tickets (B + B*rows u32, padded to
+    # 256 B), chunk stats, row stats, request state, residual sums (each padded to 256 B).
+    def up(x):
+        return (x + 255) // 256 * 256
+
+    B, rows, n = 64, 11, 16
+    want = up(B * 4 + B * rows * 4) + up(B * rows * n * 16) + up(B * rows * 32) + up(B * 16) + up(B * rows * n * 4)
+    assert lib.spec_verify_workspace_bytes(B, rows, 128256, 0) == want
+    assert lib.spec_verify_workspace_bytes(-1, 6, 100, 0) == 0
+    assert lib.spec_verify_workspace_bytes(4, 0, 100, 0) == 0
+    assert lib.spec_verify_workspace_bytes(4, 6, 0, 0) == 0
+    assert lib.spec_verify_workspace_bytes(4, 6, 100, 7) == 0
+    # bf16 halves the bytes per element: 128256 bf16 rows are 8 chunks
+    assert lib.spec_verify_workspace_bytes(64, 11, 128256, 1) < lib.spec_verify_workspace_bytes(64, 11, 128256, 0)
+
+
+def test_status_strings(lib):
+    assert lib.spec_status_string(0) == b"SPEC_OK"
+    assert lib.spec_status_string(3) == b"SPEC_ERR_WORKSPACE"
+
+
+def _chain(lib, **kw):
+    a = dict(target=1 << 20, draft=2 << 20, dtype=0, B=2, K=3, V=100, T=1.0, x=3 << 20, r=4 << 20,
+             u=5 << 20, na=6 << 20, ot=7 << 20, ws=1 << 30, wsb=10 ** 6)
+    a.update(kw)
+    P = ctypes.c_void_p
+    return lib.spec_verify_chain(P(a["target"]), P(a["draft"]), a["dtype"], a["B"], a["K"], a["V"],
+                                 a["T"], P(a["x"]), P(a["r"]), P(a["u"]), P(a["na"]), P(a["ot"]),
+                                 None, None, None, None, None, None, None, P(a["ws"]), a["wsb"], None)
+
+
+def test_host_validation_rejects_before_launch(lib):
+    # Each call fails its checks on the host, so no device pointer is ever touched.
+    assert _chain(lib, B=0) == binding.SPEC_OK  # empty batch: nothing to do
+    assert _chain(lib, V=0) == binding.SPEC_ERR_INVALID_ARG
+    assert _chain(lib, K=-1) == binding.SPEC_ERR_INVALID_ARG
+    assert _chain(lib, dtype=9) == binding.SPEC_ERR_INVALID_ARG
+    assert _chain(lib, T=-0.5) == binding.SPEC_ERR_INVALID_ARG
+    assert _chain(lib, T=float("nan")) == binding.SPEC_ERR_INVALID_ARG
+    assert _chain(lib, T=float("inf")) == binding.SPEC_ERR_INVALID_ARG
+    assert _chain(lib, K=300) == binding.SPEC_ERR_UNSUPPORTED  # beyond SPEC_MAX_K
+    assert _chain(lib, draft=0) == binding.SPEC_ERR_INVALID_ARG  # T > 0 needs draft logits
+    assert _chain(lib, r=0) == binding.SPEC_ERR_INVALID_ARG
+    assert _chain(lib, target=0) == binding.SPEC_ERR_INVALID_ARG
+    assert _chain(lib, target=(1 << 20) + 2) == binding.SPEC_ERR_INVALID_ARG  # misaligned fp32
+    assert _chain(lib, ws=0) == binding.SPEC_ERR_WORKSPACE
+    assert _chain(lib, wsb=100) == binding.SPEC_ERR_WORKSPACE
+    assert _chain(lib, ws=(1 << 30) + 16) == binding.SPEC_ERR_WORKSPACE  # workspace 256-B aligned
+    assert _chain(lib, wsb=20000, V=10 ** 6) == binding.SPEC_ERR_WORKSPACE  # too small for this V
+
+
+def test_tree_validation(lib):
+    P = ctypes.c_void_p
+    f = lib.spec_verify_tree_greedy
+    ok = dict(t=1 << 20, dt=1, B=2, N=5, V=64, tok=2 << 20, par=3 << 20, al=4 << 20, pn=5 << 20,
+              ot=6 << 20, ws=1 << 30, wsb=10 ** 6)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(P(a["t"]), a["dt"], a["B"], a["N"], a["V"], P(a["tok"]), P(a["par"]), P(a["al"]),
+                 P(a["pn"]), P(a["ot"]), None, None, P(a["ws"]), a["wsb"], None)
+
+    assert call(B=0) == binding.SPEC_OK
+    assert call(N=-1) == binding.SPEC_ERR_INVALID_ARG
+    assert call(N=5000) == binding.SPEC_ERR_UNSUPPORTED
+    assert call(par=0) == binding.SPEC_ERR_INVALID_ARG
+    assert call(wsb=10) == binding.SPEC_ERR_WORKSPACE

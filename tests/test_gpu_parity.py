@@ -1,0 +1,271 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on seeded inputs.
+
+Covers the five verification workloads (chain tiny / small vocabulary / batched, greedy tree,
+n-gram), at sizes the oracle finishes in seconds and at the full benchmark sizes (in the hot-path
+configuration the benchmark times, and with per-position outputs), plus edge cases: ragged
+vocabularies, misaligned rows, K = 0, N = 0, masked (-inf) tokens, invalid tokens, NaN / +inf /
+all -inf rows, extreme temperatures, fp16, a very large vocabulary, workspace reuse with stale
+contents, determinism and non-default streams.
+"""
+
+import numpy as np
+import pytest
+import torch
+from scipy.special import softmax as sp_softmax
+
+import oracle
+import oracle_pins as pins
+import parity
+from speculative_decoding_verification_82_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    binding.library()  # raises when the library was not built
+
+
+def _show(name, st):
+    print(f"\n[{name}] {st}")
+
+
+# ------------------------------------------------------------------ workload 1: chain tiny ----
+def test_chain_tiny_parity_and_invariance():
+    ci = synth.chain_tiny(seed=0, trials=100_000)
+    g = parity.run_gpu_chain(ci)
+    st = parity.compare_chain(g, parity.run_oracle_chain(ci), ci)
+    _show("chain tiny 1e5", st)
+    T = float(ci.temperature)
+    p = sp_softmax(ci.meta["target_rows"].astype(np.float64) / T, axis=-1)
+    q = sp_softmax(ci.meta["draft_rows"].astype(np.float64) / T, axis=-1)
+    pins.invariance_check(g["out_tokens"], g["num_accepted"], p, ci.K)
+    pins.acceptance_check(g["num_accepted"], p, q, ci.K)
+
+
+def test_invariance_v8_1e6_trials_on_gpu():
+    """Invariance theorem on the CUDA path: 10^6 seeded trials at V = 8, K = 5."""
+    ci = synth.chain_tiny(seed=100, trials=1_000_000, V=8)
+    g = parity.run_gpu_chain(ci, diag=False)
+    st = parity.compare_chain(g, parity.run_oracle_chain(ci, threads=16), ci)
+    _show("chain V=8 1e6", st)
+    T = float(ci.temperature)
+    p = sp_softmax(ci.meta["target_rows"].astype(np.float64) / T, axis=-1)
+    q = sp_softmax(ci.meta["draft_rows"].astype(np.float64) / T, axis=-1)
+    pins.invariance_check(g["out_tokens"], g["num_accepted"], p, ci.K)
+    pins.acceptance_check(g["num_accepted"], p, q, ci.K)
+
+
+# --------------------------------------------------------- workload 2: chain, small vocab ----
+@pytest.mark.parametrize("T", [0.7, 0.0])
+def test_chain_small_vocab(T):
+    for seed in range(4):
+        ci = synth.chain_small_vocab(seed=seed, B=16, temperature=T)
+        st = parity.compare_chain(parity.run_gpu_chain(ci), parity.run_oracle_chain(ci), ci)
+        parity.compare_chain(parity.run_gpu_chain(ci, diag=False), parity.run_oracle_chain(ci), ci)
+    _show(f"chain V=32000 bf16 T={T}", st)
+
+
+def test_chain_small_vocab_single_request():
+    for seed in range(10):
+        ci = synth.chain_small_vocab(seed=seed, B=1, temperature=0.7)
+        parity.compare_chain(parity.run_gpu_chain(ci), parity.run_oracle_chain(ci), ci)
+
+
+# ------------------------------------------------------------- workload 3: chain batched ----
+def _check_probs(g, ci):
+    """p and q rows within 1e-5 absolute of the oracle's double-precision softmax."""
+    T = float(ci.temperature)
+    worst = 0.0
+    for b in range(ci.B):
+        for k in range(ci.K + 1):
+            row = synth.decode(ci.target[b, k], ci.dtype).astype(np.float64)
+            p, e = oracle.softmax(row, T)
+            assert e == 0
+            worst = max(worst, float(np.abs(g["target_probs"][b, k] - p).max()))
+            if k < ci.K and "draft_probs" in g:
+                q, _ = oracle.softmax(synth.decode(ci.draft[b, k], ci.dtype).astype(np.float64), T)
+                worst = max(worst, float(np.abs(g["draft_probs"][b, k] - q).max()))
+    assert worst <= parity.PROB_TOL, worst
+    return worst
+
+
+@pytest.mark.parametrize("seed", [0, 1, 2])
+def test_chain_batched_reduced_with_probabilities(seed):
+    ci = synth.chain_batched(seed=seed, B=6)
+    g = parity.run_gpu_chain(ci, probs=True)
+    st = parity.compare_chain(g, parity.run_oracle_chain(ci), ci)
+    st["max_prob_err"] = _check_probs(g, ci)
+    _show(f"chain batched B=6 seed={seed}", st)
+
+
+@pytest.mark.parametrize("diag", [False, True])
+def test_chain_batched_full_size(diag):
+    """B = 64, K = 5, V = 128256, fp32: every request against the oracle, in the benchmark's
+    configuration (diag=False) and with per-position outputs."""
+    ci = synth.chain_batched(seed=0)
+    g = parity.run_gpu_chain(ci, diag=diag)
+    st = parity.compare_chain(g, parity.run_oracle_chain(ci, threads=16), ci)
+    _show(f"chain batched full diag={diag}", st)
+
+
+# ---------------------------------------------------------------- workload 4: greedy tree ----
+@pytest.mark.parametrize("path_boost", [0.0, 40.0])
+def test_tree_full_size(path_boost):
+    """B = 16, 61-node EAGLE-2-like tree, V = 128256 bf16.  path_boost = 40 boosts one root-to-
+    deepest-leaf path per request, so the walk accepts long paths (up to depth 6)."""
+    ti = synth.tree_greedy(seed=0, path_boost=path_boost)
+    g = parity.run_gpu_tree(ti)
+    st = parity.compare_tree(g, parity.run_oracle_tree(ti))
+    _show(f"tree path_boost={path_boost}", st)
+    if path_boost > 0:
+        assert st["mean_accepted"] >= 5.0
+
+
+# --------------------------------------------------------------------- workload 5: n-gram ----
+@pytest.mark.parametrize("boost,diag", [(5.0, False), (5.0, True), (14.0, False)])
+def test_ngram_full_size(boost, diag):
+    """B = 256, K = 5, V = 151936 bf16, T = 0.8; boost 14 makes drafts likely (bonus path)."""
+    ci = synth.ngram(seed=0, boost=boost)
+    g = parity.run_gpu_chain(ci, ngram=True, diag=diag)
+    st = parity.compare_chain(g, parity.run_oracle_chain(ci, ngram=True, threads=16), ci)
+    _show(f"ngram boost={boost} diag={diag}", st)
+
+
+def test_ngram_probabilities_and_greedy():
+    ci = synth.ngram(seed=3, B=4, V=20000, boost=6.0)
+    g = parity.run_gpu_chain(ci, ngram=True, probs=True)
+    parity.compare_chain(g, parity.run_oracle_chain(ci, ngram=True), ci)
+    _check_probs(g, ci)
+    ci.temperature = np.float32(0.0)
+    g = parity.run_gpu_chain(ci, ngram=True)
+    parity.compare_chain(g, parity.run_oracle_chain(ci, ngram=True), ci)
+
+
+# ------------------------------------------------------------------------------ edge cases ----
+def _random_chain(seed, B, K, V, dtype="f32", T=1.0, sigma=3.0):
+    rng = np.random.default_rng(seed)
+    t32 = rng.normal(0, sigma, (B, K + 1, V)).astype(np.float32)
+    d32 = (t32[:, :K] + rng.normal(0, 1.5, (B, K, V))).astype(np.float32)
+    x = rng.integers(0, V, (B, K)).astype(np.int32)
+    t32[np.arange(B)[:, None], np.arange(K)[None, :], x] += 2.0
+    r = ((rng.integers(0, 1 << 24, (B, K)) + 1) * synth.U24).astype(np.float32)
+    u = (rng.integers(0, 1 << 24, B) * synth.U24).astype(np.float32)
+    return synth.ChainInputs("edge", dtype, B, K, V, np.float32(T), synth.encode(t32, dtype),
+                             synth.encode(d32, dtype), x, r, u)
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("V", [1, 7, 33, 1000, 4097, 65537])
+def test_ragged_vocab_all_modes(dtype, V):
+    """Vocabularies that are not a multiple of the vector width put rows at every 16-B phase."""
+    ci = _random_chain(V, 5, 3, V, dtype)
+    parity.compare_chain(parity.run_gpu_chain(ci), parity.run_oracle_chain(ci), ci)
+    parity.compare_chain(parity.run_gpu_chain(ci, diag=False), parity.run_oracle_chain(ci), ci)
+    parity.compare_chain(parity.run_gpu_chain(ci, ngram=True), parity.run_oracle_chain(ci, ngram=True), ci)
+    ci.temperature = np.float32(0.0)
+    parity.compare_chain(parity.run_gpu_chain(ci), parity.run_oracle_chain(ci), ci)
+    if V >= 16:
+        par = np.array([-1] + [int(np.random.default_rng(i).integers(0, i)) for i in range(1, 6)], np.int32)
+        ti = synth.tree_greedy(seed=V % 97, B=3, V=V, dtype=dtype, parents=par)
+        parity.compare_tree(parity.run_gpu_tree(ti), parity.run_oracle_tree(ti))
+
+
+def test_k_zero_and_tree_root_only():
+    ci = _random_chain(1, 4, 0, 500)
+    parity.compare_chain(parity.run_gpu_chain(ci), parity.run_oracle_chain(ci), ci)
+    parity.compare_chain(parity.run_gpu_chain(ci, ngram=True), parity.run_oracle_chain(ci, ngram=True), ci)
+    ti = synth.tree_greedy(seed=2, B=3, V=300, parents=np.array([-1], np.int32))
+    parity.compare_tree(parity.run_gpu_tree(ti), parity.run_oracle_tree(ti))
+
+
+def test_masked_tokens_and_invalid_inputs():
+    ci = _random_chain(5, 12, 4, 3000)
+    t = ci.target.view(np.float32)
+    d = ci.draft.view(np.float32)
+    t[0, :, 100:900] = -np.inf  # masked tokens are legal
+    d[1, :, ::3] = -np.inf
+    ci.draft_tokens[1, 0] = 3  # a token the draft masked: q(x) = 0
+    ci.draft_tokens[2, 1] = ci.V  # out of range
+    ci.draft_tokens[3, 3] = -5
+    t[4, 2, 17] = np.nan
+    d[5, 0, 8] = np.nan
+    t[6, 4, 1] = np.inf
+    t[7, 1, :] = -np.inf  # a whole row masked: no distribution
+    t[8, 0, 5] = np.nan
+    ci.draft_tokens[8, 2] = ci.V + 1  # two faults at once
+    for T in (1.0, 0.0):
+        ci.temperature = np.float32(T)
+        o = parity.run_oracle_chain(ci)
+        parity.compare_chain(parity.run_gpu_chain(ci), o, ci)
+        parity.compare_chain(parity.run_gpu_chain(ci, diag=False), o, ci)
+        assert (o["err"] != 0).sum() >= 4
+        on = parity.run_oracle_chain(ci, ngram=True)
+        parity.compare_chain(parity.run_gpu_chain(ci, ngram=True), on, ci)
+
+
+def test_malformed_trees():
+    ti = synth.tree_greedy(seed=4, B=6, V=5000)
+    ti.parents[1, 0] = 0  # root must have parent -1
+    ti.parents[2, 7] = 9  # parent index not smaller than the node
+    ti.node_tokens[3, 4] = 5000  # token out of range
+    ti.node_tokens[4, 9] = -1
+    t = synth.bf16_bits_to_f32(ti.target)
+    t[5, 3, 11] = np.nan
+    ti.target = synth.to_bf16_bits(t)
+    g = parity.run_gpu_tree(ti)
+    o = parity.run_oracle_tree(ti)
+    parity.compare_tree(g, o)
+    assert list(o["err"][1:6] != 0) == [True] * 5 and o["err"][0] == 0
+
+
+@pytest.mark.parametrize("T", [0.05, 0.3, 2.5, 8.0])
+def test_temperatures(T):
+    ci = _random_chain(int(T * 100), 16, 5, 9000, "bf16", T=T)
+    st = parity.compare_chain(parity.run_gpu_chain(ci), parity.run_oracle_chain(ci), ci)
+    parity.compare_chain(parity.run_gpu_chain(ci, ngram=True), parity.run_oracle_chain(ci, ngram=True), ci)
+    _show(f"temperature {T}", st)
+
+
+def test_very_large_vocab():
+    """A vocabulary far above the workloads' (2^20 + 3 elements, ragged): many chunks per row."""
+    ci = _random_chain(9, 2, 2, (1 << 20) + 3, "bf16")
+    parity.compare_chain(parity.run_gpu_chain(ci), parity.run_oracle_chain(ci), ci)
+    parity.compare_chain(parity.run_gpu_chain(ci, ngram=True), parity.run_oracle_chain(ci, ngram=True), ci)
+
+
+def test_many_small_requests():
+    ci = _random_chain(11, 4096, 5, 64)
+    parity.compare_chain(parity.run_gpu_chain(ci), parity.run_oracle_chain(ci, threads=16), ci)
+
+
+def test_workspace_reuse_and_determinism():
+    """One workspace serves calls of different modes, batch sizes and vocabularies in turn, stale
+    contents do not matter, and repeated calls give identical results."""
+    ws = binding.make_workspace(64, 11, 20000, torch.float32, "cuda")
+    a = synth.chain_batched(seed=5, B=4, V=20000)
+    b = synth.ngram(seed=5, B=64, V=20000)
+    t = synth.tree_greedy(seed=5, B=8, V=20000, dtype="f32")
+    ga1 = parity.run_gpu_chain(a, workspace=ws)
+    gb = parity.run_gpu_chain(b, ngram=True, workspace=ws)
+    gt = parity.run_gpu_tree(t, workspace=ws)
+    ga2 = parity.run_gpu_chain(a, workspace=ws)
+    for key in ga1:
+        assert np.array_equal(ga1[key], ga2[key]), key
+    parity.compare_chain(ga1, parity.run_oracle_chain(a), a)
+    parity.compare_chain(gb, parity.run_oracle_chain(b, ngram=True), b)
+    parity.compare_tree(gt, parity.run_oracle_tree(t))
+    ws.fill_(0xAB)  # arbitrary stale contents must not matter
+    ga3 = parity.run_gpu_chain(a, workspace=ws)
+    for key in ga1:
+        assert np.array_equal(ga1[key], ga3[key]), key
+
+
+def test_non_default_stream():
+    ci = synth.chain_batched(seed=6, B=3, V=50000)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        g = parity.run_gpu_chain(ci)
+    parity.compare_chain(g, parity.run_oracle_chain(ci), ci)
