@@ -59,20 +59,23 @@ Chunking plan_chunks(int V, int S) {
 }
 
 // Workspace layout:
-//   tick_a  [B] u32              request tickets    } one region, cleared by one
-//   tick_b  [B][Kc] u32          residual tickets   } cudaMemsetAsync per call (Kc = rows >= K)
+//   work    u32                  work-item counter  } one region, cleared by one
+//   tick_a  [B] u32              request tickets    } cudaMemsetAsync per call
+//   tick_b  [B][Kc] u32          residual tickets   } (Kc = rows >= K)
 //   cstat   [B][rows][nchunk]    ChunkStat          (256-byte aligned regions from here on)
 //   rstat   [B][rows]            RowStat
 //   req     [B]                  ReqState
 //   wsum    [B][Kc][nchunk]      float
 struct Layout {
-  size_t tick_a, tick_b, cstat, rstat, req, wsum, total;
+  size_t work, tick_a, tick_b, cstat, rstat, req, wsum, total;
 };
 
 Layout layout(int B, int rows, int nchunk) {
   Layout L;
   const size_t b = (size_t)B, r = (size_t)rows, n = (size_t)nchunk;
   size_t off = 0;
+  L.work = off;
+  off += 4;
   L.tick_a = off;
   off += b * 4;
   L.tick_b = off;
@@ -107,9 +110,10 @@ spec_status_t attach_workspace(Params& P, void* ws, size_t bytes, int B, int row
   if (ws == nullptr || bytes < L.total) return SPEC_ERR_WORKSPACE;
   if (((uintptr_t)ws & 255u) != 0) return SPEC_ERR_WORKSPACE;
   char* w = static_cast<char*>(ws);
+  P.work = reinterpret_cast<unsigned*>(w + L.work);
   P.tick_a = reinterpret_cast<unsigned*>(w + L.tick_a);
   P.tick_b = reinterpret_cast<unsigned*>(w + L.tick_b);
-  P.tick_bytes = L.cstat - L.tick_a;
+  P.tick_bytes = L.cstat - L.work;
   P.cstat = reinterpret_cast<ChunkStat*>(w + L.cstat);
   P.rstat = reinterpret_cast<RowStat*>(w + L.rstat);
   P.req = reinterpret_cast<ReqState*>(w + L.req);
@@ -123,7 +127,7 @@ spec_status_t launch(spec_dtype_t dtype, int mode, Params& P, specv::LaunchPlan&
   L.smem_stats = 2 * (size_t)P.buf_bytes;
   L.smem_resid = 2 * (size_t)P.buf_bytes;
   // the ticket counters start every call at zero, whatever the workspace held before
-  cudaError_t e = cudaMemsetAsync(P.tick_a, 0, P.tick_bytes, stream);
+  cudaError_t e = cudaMemsetAsync(P.work, 0, P.tick_bytes, stream);
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   switch (dtype) {
     case SPEC_DTYPE_F32: e = specv::launch_verify<float>(mode, P, L, stream); break;

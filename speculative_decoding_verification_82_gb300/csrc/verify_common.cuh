@@ -204,6 +204,28 @@ __device__ __forceinline__ int warp_or(int v) {
   for (int o = 16; o; o >>= 1) v |= __shfl_xor_sync(kFull, v, o);
   return v;
 }
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+  return v;
+}
+__device__ __forceinline__ double warp_incl_scan_d(double v, int lane) {
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double t = __shfl_up_sync(kFull, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+// 2^x in double with fp32 relative accuracy (~3e-7): the integer part of x scales exactly, the
+// fractional part goes through the special-function unit.  Avoids double-precision
+// transcendentals, which are slow on this part.
+__device__ __forceinline__ double exp2_split(double x) {
+  if (!(x > -1070.0)) return x != x ? x : 0.0;
+  if (x > 1020.0) return __longlong_as_double(0x7ff0000000000000LL);
+  const double n = floor(x);
+  return ldexp((double)ex2((float)(x - n)), (int)n);
+}
 // Inclusive prefix sum across the warp (Kogge-Stone), fixed association.
 __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
 #pragma unroll

@@ -85,7 +85,8 @@ struct Params {
   RowStat* rstat;    // [B][rows]
   ReqState* req;     // [B]
   float* wsum;       // [B][K][nchunk] (per-position outputs) or [B][nchunk]
-  unsigned* tick_a;  // [B] request tickets of stats_kernel (zeroed by the host before each call)
+  unsigned* work;    // work-item counter of stats_kernel (zeroed by the host before each call)
+  unsigned* tick_a;  // [B] request tickets of stats_kernel (zeroed likewise)
   unsigned* tick_b;  // [B][K] or [B] tickets of residual_kernel (zeroed likewise)
   size_t tick_bytes; // bytes of the two ticket arrays (one contiguous region)
 };
@@ -98,81 +99,150 @@ __device__ __forceinline__ const char* row_ptr(const Params& P, int b, int r) {
 }
 __device__ __forceinline__ int chunk_len(const Params& P, int ch) { return min(P.chunk, P.V - ch * P.chunk); }
 
-// Weight of a chunk in units of the row normaliser: s (or sx) * 2^(a c - mc).
+// Weight of a chunk in units of the row normaliser: s (or sx) * 2^(RN(a c) - mc).
 __device__ __forceinline__ double chunk_weight(float a, float s, float c, float mc) {
   if (a == -INFINITY) return 0.0;
-  return (double)s * exp2((double)__fmul_rn(a, c) - (double)mc);
+  return (double)s * (double)ex2(__fsub_rn(__fmul_rn(a, c), mc));
 }
 
 // ------------------------------------------------------------------ chunk reductions ----
-// Softmax statistics of a staged chunk: block max m, s = sum 2^(l c - m c), and the same sum
-// with slot (vx, jx) left out (vx < 0: nothing left out).
+// Online-softmax partial: s (and sx) are sums of 2^(l c - RN(m c)) over the elements seen.
+struct Soft {
+  float m, s, sx;
+};
+// 2^(RN(m c) - RN(M c)): rescales a partial taken at maximum m to maximum M (0 when empty).
+__device__ __forceinline__ float rescale(float m, float M, float c) {
+  return m == -INFINITY ? 0.f : ex2(__fsub_rn(__fmul_rn(m, c), __fmul_rn(M, c)));
+}
+__device__ __forceinline__ Soft soft_merge(const Soft& a, const Soft& b, float c) {
+  const float M = fmax_nan(a.m, b.m);
+  if (M == -INFINITY) return a;  // both partials empty
+  const float fa = rescale(a.m, M, c), fb = rescale(b.m, M, c);
+  Soft r;
+  r.m = M;
+  r.s = __fmaf_rn(a.s, fa, __fmul_rn(b.s, fb));
+  r.sx = __fmaf_rn(a.sx, fa, __fmul_rn(b.sx, fb));
+  return r;
+}
+
+// This thread's softmax partial over its vectors of a staged chunk; sx leaves out slot (vx, jx).
+template <typename T>
+__device__ __forceinline__ Soft thread_softmax(const unsigned char* buf, int nvec, float c, int vx, int jx) {
+  constexpr int VE = Elem<T>::kPerVec;
+  Soft t;
+  t.m = thread_max<T>(buf, nvec);
+  t.s = t.sx = 0.f;
+  if (!(t.m > -INFINITY && t.m < INFINITY)) return t;  // empty, +inf or NaN: the max tells
+  const float mc = __fmul_rn(t.m, c);
+  for (int v = (int)threadIdx.x; v < nvec; v += kThreads) {
+    float f[VE];
+    Elem<T>::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)v * 16), f);
+    float e[VE];
+#pragma unroll
+    for (int j = 0; j < VE; ++j) e[j] = ex2(__fmaf_rn(f[j], c, -mc));
+    float vs = 0.f;
+#pragma unroll
+    for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, e[j]);
+    t.s = __fadd_rn(t.s, vs);
+    if (v == vx) {
+      float vsx = 0.f;
+#pragma unroll
+      for (int j = 0; j < VE; ++j) vsx = __fadd_rn(vsx, j == jx ? 0.f : e[j]);
+      t.sx = __fadd_rn(t.sx, vsx);
+    } else {
+      t.sx = __fadd_rn(t.sx, vs);
+    }
+  }
+  return t;
+}
+
+// Softmax statistics of a staged chunk, merged thread -> warp (shuffles) -> block (thread 0).
+// One block barrier.  The result is valid in thread 0 only.
 template <typename T>
 __device__ __forceinline__ ChunkStat chunk_softmax_stats(const unsigned char* buf, const Geo& g, float c, int vx,
-                                                         int jx, float* red) {
-  constexpr int VE = Elem<T>::kPerVec;
-  ChunkStat q;
-  const float m = block_max_nan(thread_max<T>(buf, g.nvec), red);
-  float s = 0.f, sx = 0.f;
-  int fl = 0;
-  if (isnan(m) || m == INFINITY) {
-    fl = SPEC_ERRF_NONFINITE;
-  } else if (m != -INFINITY) {
-    const float mc = __fmul_rn(m, c);
-    for (int v = (int)threadIdx.x; v < g.nvec; v += kThreads) {
-      float f[VE];
-      Elem<T>::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)v * 16), f);
-      float e[VE];
+                                                         int jx, float* red /*3*kWarps*/) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  Soft t = thread_softmax<T>(buf, g.nvec, c, vx, jx);
 #pragma unroll
-      for (int j = 0; j < VE; ++j) e[j] = ex2(__fmaf_rn(f[j], c, -mc));
-      float vs = 0.f;
-#pragma unroll
-      for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, e[j]);
-      s = __fadd_rn(s, vs);
-      if (v == vx) {
-        float vsx = 0.f;
-#pragma unroll
-        for (int j = 0; j < VE; ++j) vsx = __fadd_rn(vsx, j == jx ? 0.f : e[j]);
-        sx = __fadd_rn(sx, vsx);
-      } else {
-        sx = __fadd_rn(sx, vs);
-      }
-    }
-    block_sum2(s, sx, red);
+  for (int o = 16; o; o >>= 1) {
+    Soft u;
+    u.m = __shfl_xor_sync(kFull, t.m, o);
+    u.s = __shfl_xor_sync(kFull, t.s, o);
+    u.sx = __shfl_xor_sync(kFull, t.sx, o);
+    t = soft_merge(t, u, c);
   }
-  q.a = m;
-  q.s = s;
-  q.sx = sx;
-  q.i = fl;
+  if (lane == 0) {
+    red[warp] = t.m;
+    red[kWarps + warp] = t.s;
+    red[2 * kWarps + warp] = t.sx;
+  }
+  __syncthreads();
+  ChunkStat q;
+  q.a = red[0];
+  q.s = red[kWarps];
+  q.sx = red[2 * kWarps];
+  q.i = 0;
+  if (threadIdx.x == 0) {
+    Soft acc{red[0], red[kWarps], red[2 * kWarps]};
+    for (int w = 1; w < kWarps; ++w) acc = soft_merge(acc, Soft{red[w], red[kWarps + w], red[2 * kWarps + w]}, c);
+    q.a = acc.m;
+    q.s = acc.s;
+    q.sx = acc.sx;
+    q.i = (isnan(acc.m) || acc.m == INFINITY) ? SPEC_ERRF_NONFINITE : 0;
+    if (q.i) q.s = q.sx = 0.f;
+  }
   return q;
 }
 
-// (max, first index) of a staged chunk; index -1 when the chunk holds a NaN.
+// (max, first index) partials: index -1 marks a NaN, INT_MAX an empty partial.
+__device__ __forceinline__ void argmax_merge(float& v, int& i, float v2, int i2) {
+  if (i < 0 || i2 == INT_MAX) return;
+  if (i2 < 0 || i == INT_MAX || v2 > v || (v2 == v && i2 < i)) {
+    v = v2;
+    i = i2;
+  }
+}
+
+// (max, first index) of a staged chunk; index -1 when it holds a NaN.  One block barrier; the
+// result is valid in thread 0 only.
 template <typename T>
 __device__ __forceinline__ ChunkStat chunk_argmax(const unsigned char* buf, const Geo& g, float* red, int* redi) {
   constexpr int VE = Elem<T>::kPerVec;
-  const float tm = thread_max<T>(buf, g.nvec);
-  const float M = block_max_nan(tm, red);
-  ChunkStat q;
-  q.a = M;
-  q.s = q.sx = 0.f;
-  if (isnan(M)) {
-    q.i = -1;
-    return q;
-  }
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  float v = thread_max<T>(buf, g.nvec);
   int idx = INT_MAX;
-  if (tm == M) {  // only threads holding a maximal element look for its first position
-    for (int v = (int)threadIdx.x; v < g.nvec && idx == INT_MAX; v += kThreads) {
+  if (isnan(v)) {
+    idx = -1;
+  } else {  // this thread's first element equal to its maximum (its vectors are in index order)
+    for (int vv = (int)threadIdx.x; vv < g.nvec && idx == INT_MAX; vv += kThreads) {
       float f[VE];
-      Elem<T>::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)v * 16), f);
+      Elem<T>::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)vv * 16), f);
 #pragma unroll
       for (int j = 0; j < VE; ++j) {
-        const int e = g.e0 - g.slot0 + v * VE + j;
-        if (idx == INT_MAX && e >= g.e0 && e < g.e0 + g.n && f[j] == M) idx = e;
+        const int e = g.e0 - g.slot0 + vv * VE + j;
+        if (idx == INT_MAX && e >= g.e0 && e < g.e0 + g.n && f[j] == v) idx = e;
       }
     }
   }
-  q.i = block_min_i(idx, redi);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float v2 = __shfl_xor_sync(kFull, v, o);
+    const int i2 = __shfl_xor_sync(kFull, idx, o);
+    argmax_merge(v, idx, v2, i2);
+  }
+  if (lane == 0) {
+    red[warp] = v;
+    redi[warp] = idx;
+  }
+  __syncthreads();
+  ChunkStat q;
+  q.a = red[0];
+  q.i = redi[0];
+  q.s = q.sx = 0.f;
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kWarps; ++w) argmax_merge(q.a, q.i, red[w], redi[w]);
+    if (q.i == INT_MAX) q.i = -1;  // a chunk always holds at least one element
+  }
   return q;
 }
 
@@ -188,6 +258,46 @@ struct FinishSmem {
   unsigned* xphase;
 };
 
+// Warp-wide inverse CDF over per-chunk weights W(c) (double), in chunk order: the first chunk
+// with positive weight whose running total exceeds u * S, else the last positive one.  Every
+// lane gets the chunk, the total weight before it and S.
+template <typename WF>
+__device__ __forceinline__ void chunk_select(int nchunk, double u, WF W, int& cstar, double& bstar, double& S) {
+  const int lane = threadIdx.x & 31;
+  double part = 0.0;
+  for (int c = lane; c < nchunk; c += 32) part += W(c);
+  S = warp_sum_d(part);
+  const double tgt = u * S;
+  double base = 0.0, blast = 0.0;
+  int clast = -1;
+  cstar = -1;
+  bstar = 0.0;
+  for (int c0 = 0; c0 < nchunk; c0 += 32) {
+    const int cc = c0 + lane;
+    const double w = cc < nchunk ? W(cc) : 0.0;
+    const double incl = warp_incl_scan_d(w, lane);
+    double ex = __shfl_up_sync(kFull, incl, 1);
+    if (lane == 0) ex = 0.0;
+    const unsigned hit = __ballot_sync(kFull, w > 0.0 && base + incl > tgt);
+    const unsigned pos = __ballot_sync(kFull, w > 0.0);
+    if (cstar < 0 && hit) {
+      const int L = __ffs(hit) - 1;
+      cstar = c0 + L;
+      bstar = base + __shfl_sync(kFull, ex, L);
+    }
+    if (pos) {
+      const int L = 31 - __clz(pos);
+      clast = c0 + L;
+      blast = base + __shfl_sync(kFull, ex, L);
+    }
+    base += __shfl_sync(kFull, incl, 31);
+  }
+  if (cstar < 0) {
+    cstar = clast;
+    bstar = blast;
+  }
+}
+
 // Inverse-CDF draw for target row `row` of request b from its chunk statistics: weights p
 // (kFullP) or p without token x (kExcl).  Finds the crossing chunk from the chunk weights, then
 // stages that one chunk (into `buf`) and searches it.  Block-wide; every thread gets the token
@@ -198,42 +308,25 @@ __device__ int draw_from_chunks(const Params& P, int b, int row, int kind, int x
   constexpr int VE = Elem<T>::kPerVec;
   const RowStat rs = P.rstat[(size_t)b * P.rows + row];
   const ChunkStat* cs = P.cstat + ((size_t)b * P.rows + row) * P.nchunk;
-  if (threadIdx.x == 0) {
-    auto weight = [&](int c, int kd) {
-      return chunk_weight(__ldcg(&cs[c].a), kd == kExcl ? __ldcg(&cs[c].sx) : __ldcg(&cs[c].s), P.c, rs.mc);
+  if (threadIdx.x < 32) {
+    const double u = (double)__ldg(P.u + b);
+    int cstar, k2 = kind;
+    double bstar, S;
+    auto weight = [&](int c) {
+      return chunk_weight(__ldcg(&cs[c].a), k2 == kExcl ? __ldcg(&cs[c].sx) : __ldcg(&cs[c].s), P.c, rs.mc);
     };
-    double S = 0.0;
-    for (int c = 0; c < P.nchunk; ++c) S += weight(c, kind);
+    chunk_select(P.nchunk, u, weight, cstar, bstar, S);
     const double S0 = S;
-    int k2 = kind;
     if (!(S > 0.0)) {  // no residual mass: draw from p
       k2 = kFullP;
-      S = 0.0;
-      for (int c = 0; c < P.nchunk; ++c) S += weight(c, k2);
+      chunk_select(P.nchunk, u, weight, cstar, bstar, S);
     }
-    const double tgt = (double)__ldg(P.u + b) * S;
-    double base = 0.0, bstar = 0.0, blast = 0.0;
-    int cstar = -1, clast = -1;
-    for (int c = 0; c < P.nchunk; ++c) {
-      const double W = weight(c, k2);
-      if (W > 0.0) {
-        if (cstar < 0 && base + W > tgt) {
-          cstar = c;
-          bstar = base;
-        }
-        clast = c;
-        blast = base;
-        base += W;
-      }
+    if (threadIdx.x == 0) {
+      F.s_misc[0] = cstar;
+      F.s_misc[1] = k2;
+      F.s_dbl[0] = u * S - bstar;
+      F.s_dbl[1] = S0 / rs.Z;
     }
-    if (cstar < 0) {
-      cstar = clast;
-      bstar = blast;
-    }
-    F.s_misc[0] = cstar;
-    F.s_misc[1] = k2;
-    F.s_dbl[0] = tgt - bstar;
-    F.s_dbl[1] = S0 / rs.Z;
   }
   __syncthreads();
   const int cstar = F.s_misc[0], k2 = F.s_misc[1];
@@ -287,10 +380,10 @@ __device__ void combine_rows(const Params& P, int b) {
     if (kSoftmax) {
       const float mc = __fmul_rn(m, P.c);
       const bool finite_m = !isnan(m) && m != INFINITY && m != -INFINITY;
-      double Z = 0.0;
-      if (lane == 0 && !fl && finite_m) {
-        for (int c = 0; c < P.nchunk; ++c) Z += chunk_weight(__ldcg(&cs[c].a), __ldcg(&cs[c].s), P.c, mc);
-      }
+      double z = 0.0;
+      if (!fl && finite_m)
+        for (int c = lane; c < P.nchunk; c += 32) z += chunk_weight(__ldcg(&cs[c].a), __ldcg(&cs[c].s), P.c, mc);
+      const double Z = warp_sum_d(z);
       rs.Z = Z;
       rs.mc = mc;
       rs.amax = -1;
@@ -346,11 +439,11 @@ __device__ void finish_chain(const Params& P, int b, unsigned char* buf, const F
             alpha = 0.0;  // p(x) = 0
           } else {
             const double exd = (double)dx * (double)P.c - (double)d.mc;
-            const double ratio = exp2(ext - exd) * (d.Z / t.Z);
+            const double ratio = exp2_split(ext - exd) * (d.Z / t.Z);
             alpha = ratio >= 1.0 ? 1.0 : ratio;
           }
         } else {
-          const double px = lx == -INFINITY ? 0.0 : exp2(ext) / t.Z;
+          const double px = lx == -INFINITY ? 0.0 : exp2_split(ext) / t.Z;
           alpha = px >= 1.0 ? 1.0 : px;
         }
       } else {
@@ -492,6 +585,11 @@ __device__ inline void walk_tree(const Params& P, int b) {
 }
 
 // ---------------------------------------------------------------------- stats kernel ----
+// Persistent: each CTA claims work items (one chunk of one row; request-major order) from an
+// atomic counter, one item ahead of use, and keeps two of them in flight in its two stages.  The
+// ticket of an item is taken after its statistics are written; its result is examined one item
+// later (so the atomic's latency overlaps the next item), and the CTA whose ticket completed a
+// request finishes that request before going on.
 template <int MODE, typename T>
 __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
   constexpr int VE = Elem<T>::kPerVec;
@@ -500,59 +598,72 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
   __shared__ uint64_t bar[2];
   __shared__ uint64_t bar_x;
   __shared__ unsigned xphase;
-  __shared__ float red[2 * kWarps];
+  __shared__ float red[3 * kWarps];
   __shared__ int redi[kWarps];
   __shared__ float tileW[kMaxTiles][kWarps];
   __shared__ int s_int[4];
   __shared__ float s_flt[4];
   __shared__ double s_dbl[4];
   __shared__ int s_misc[8];
-  __shared__ int s_last;
+  __shared__ int s_fin;
+  __shared__ unsigned s_item[2];
   __shared__ double s_alpha[MODE == kTree ? 1 : SPEC_MAX_K];
 
   const int tid = threadIdx.x;
   const int per_req = P.rows * P.nchunk;
-  const long long total = (long long)P.B * per_req;
-  const long long G = gridDim.x;
+  const unsigned total = (unsigned)((long long)P.B * per_req);
   if (tid == 0) {
     mbar_init(&bar[0], 1);
     mbar_init(&bar[1], 1);
     mbar_init(&bar_x, 1);
     xphase = 0;
     fence_mbar_init();
+    s_item[0] = atomicAdd(P.work, 1u);
+    s_item[1] = atomicAdd(P.work, 1u);
   }
   __syncthreads();
   const uint64_t pol = l2_policy_evict_first();
   const FinishSmem F{tileW, s_int, s_flt, s_dbl, s_alpha, s_misc, &bar_x, &xphase};
 
-  auto locate = [&](long long w, int& b, int& r, int& ch, const char*& rp) {
-    b = (int)(w / per_req);
-    const int rem = (int)(w - (long long)b * per_req);
+  auto locate = [&](unsigned w, int& b, int& r, int& ch, const char*& rp) {
+    b = (int)(w / (unsigned)per_req);
+    const int rem = (int)(w - (unsigned)b * (unsigned)per_req);
     r = rem / P.nchunk;
     ch = rem - r * P.nchunk;
     rp = row_ptr<T>(P, b, r);
     return make_geo<T>(rp, ch * P.chunk, chunk_len(P, ch));
   };
-  // prologue: fill both stages
+  auto finish = [&](int b, unsigned char* buf) {
+    __threadfence();
+    if constexpr (MODE == kTree) {
+      combine_rows<MODE>(P, b);
+      if (tid < 32) walk_tree(P, b);
+    } else {
+      finish_chain<MODE, T>(P, b, buf, F);
+    }
+  };
   for (int s = 0; s < 2; ++s) {
-    const long long w = blockIdx.x + s * G;
-    if (w < total) {
+    if (s_item[s] < total) {
       int b, r, ch;
       const char* rp;
-      const Geo g = locate(w, b, r, ch, rp);
+      const Geo g = locate(s_item[s], b, r, ch, rp);
       issue_chunk<T>(smem + s * P.buf_bytes, rp, g, &bar[s], pol);
     }
   }
-  int it = 0;
-  for (long long w = blockIdx.x; w < total; w += G, ++it) {
+  int pend_b = -1;      // thread 0: request of the previous item's ticket
+  unsigned pend_old = 0;  // thread 0: that ticket's value before the increment
+  for (int it = 0;; ++it) {
     const int st = it & 1;
-    const uint32_t par = (uint32_t)(it >> 1) & 1u;
+    const unsigned w = s_item[st];
+    if (w >= total) break;  // claims increase, so the other stage is empty too
+    unsigned claim = 0;
+    if (tid == 0) claim = atomicAdd(P.work, 1u);  // the item this stage takes next
     unsigned char* buf = smem + st * P.buf_bytes;
     int b, r, ch;
     const char* rp;
     const Geo g = locate(w, b, r, ch, rp);
-    bool ok = mbar_wait_bounded(&bar[st], par);
-    if (!ok) ok = mbar_wait_bounded(&bar[st], par);  // never proceed with a copy in flight
+    bool ok = mbar_wait_bounded(&bar[st], (uint32_t)(it >> 1) & 1u);
+    if (!ok) ok = mbar_wait_bounded(&bar[st], (uint32_t)(it >> 1) & 1u);  // never go on with a copy in flight
     __syncthreads();  // plain-loaded slots of this stage are visible
 
     ChunkStat q;
@@ -561,9 +672,9 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
       if (MODE == kNgram && r < P.K) {
         const int x = __ldg(P.draft_tokens + (size_t)b * P.K + r);
         if (x >= g.e0 && x < g.e0 + g.n) {
-          const int s = x - g.e0 + g.slot0;
-          vx = s / VE;
-          jx = s - vx * VE;
+          const int sl = x - g.e0 + g.slot0;
+          vx = sl / VE;
+          jx = sl - vx * VE;
         }
       }
       q = chunk_softmax_stats<T>(buf, g, P.c, vx, jx, red);
@@ -573,27 +684,24 @@ __global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
       if (!ok) q.i = -1;
     }
     if (tid == 0) {
+      s_fin = (pend_b >= 0 && pend_old == (unsigned)(per_req - 1)) ? pend_b : -1;
       P.cstat[((size_t)b * P.rows + r) * P.nchunk + ch] = q;
       __threadfence();
-      s_last = (atomicAdd(P.tick_a + b, 1u) == (unsigned)(per_req - 1));
+      pend_old = atomicAdd(P.tick_a + b, 1u);
+      pend_b = b;
     }
     __syncthreads();
-    if (s_last) {  // this CTA completed request b
-      __threadfence();
-      if constexpr (MODE == kTree) {
-        combine_rows<MODE>(P, b);
-        if (tid < 32) walk_tree(P, b);
-      } else {
-        finish_chain<MODE, T>(P, b, buf, F);
-      }
-    }
-    __syncthreads();  // every thread is done with this stage
-    const long long nxt = w + 2 * G;
-    if (nxt < total) {
-      const Geo g2 = locate(nxt, b, r, ch, rp);
+    if (s_fin >= 0) finish(s_fin, buf);  // the previous item's ticket completed its request
+    if (tid == 0) s_item[st] = claim;
+    __syncthreads();  // every thread is done with this stage and sees the claim
+    if (claim < total) {
+      const Geo g2 = locate(claim, b, r, ch, rp);
       issue_chunk<T>(buf, rp, g2, &bar[st], pol);
     }
   }
+  if (tid == 0) s_fin = (pend_b >= 0 && pend_old == (unsigned)(per_req - 1)) ? pend_b : -1;
+  __syncthreads();
+  if (s_fin >= 0) finish(s_fin, smem);  // no copy is in flight once the loop has ended
 }
 
 // ------------------------------------------------------------------- residual kernel ----
@@ -627,7 +735,7 @@ __global__ void __launch_bounds__(kThreads, 3) residual_kernel(const Params P) {
   const RowStat ts = P.rstat[(size_t)b * P.rows + k];
   const RowStat ds = P.rstat[(size_t)b * P.rows + P.R + k];
   const float c = P.c, mct = ts.mc, mcd = ds.mc;
-  const float rho = (float)(ts.Z / ds.Z);  // max(0, p - q) * Z_t = max(0, e - f * Z_t / Z_d)
+  const float rho = __fdiv_rn((float)ts.Z, (float)ds.Z);  // max(0, p - q) Z_t = max(0, e - f Z_t / Z_d)
   const char* rT = row_ptr<T>(P, b, k);
   const char* rD = row_ptr<T>(P, b, P.R + k);
   if (tid == 0) {
@@ -674,41 +782,27 @@ __global__ void __launch_bounds__(kThreads, 3) residual_kernel(const Params P) {
   if (!s_last) return;
   __threadfence();
   // last chunk of (b, k): total residual weight, crossing chunk, search
-  if (tid == 0) {
+  if (tid < 32) {
     const ChunkStat* cs = P.cstat + ((size_t)b * P.rows + k) * P.nchunk;
-    double S = 0.0;
-    for (int q = 0; q < P.nchunk; ++q) S += (double)__ldcg(P.wsum + bk * P.nchunk + q);
+    const double u = (double)__ldg(P.u + b);
+    int kind = kResid, cstar;
+    double bstar, S;
+    auto weight = [&](int q) {
+      return kind == kResid ? (double)__ldcg(P.wsum + bk * P.nchunk + q)
+                            : chunk_weight(__ldcg(&cs[q].a), __ldcg(&cs[q].s), c, mct);
+    };
+    chunk_select(P.nchunk, u, weight, cstar, bstar, S);
     const double mass = S / ts.Z;
-    int kind = kResid;
     if (!(S > 0.0)) {  // no residual mass: draw from p
       kind = kFullP;
-      S = 0.0;
-      for (int q = 0; q < P.nchunk; ++q) S += chunk_weight(__ldcg(&cs[q].a), __ldcg(&cs[q].s), c, mct);
+      chunk_select(P.nchunk, u, weight, cstar, bstar, S);
     }
-    const double tgt = (double)__ldg(P.u + b) * S;
-    double base = 0.0, bstar = 0.0, blast = 0.0;
-    int cstar = -1, clast = -1;
-    for (int q = 0; q < P.nchunk; ++q) {
-      const double W = kind == kResid ? (double)__ldcg(P.wsum + bk * P.nchunk + q)
-                                      : chunk_weight(__ldcg(&cs[q].a), __ldcg(&cs[q].s), c, mct);
-      if (W > 0.0) {
-        if (cstar < 0 && base + W > tgt) {
-          cstar = q;
-          bstar = base;
-        }
-        clast = q;
-        blast = base;
-        base += W;
-      }
+    if (tid == 0) {
+      s_misc[0] = cstar;
+      s_misc[1] = kind;
+      s_dbl[0] = u * S - bstar;
+      s_dbl[1] = mass;
     }
-    if (cstar < 0) {
-      cstar = clast;
-      bstar = blast;
-    }
-    s_misc[0] = cstar;
-    s_misc[1] = kind;
-    s_dbl[0] = tgt - bstar;
-    s_dbl[1] = mass;
   }
   __syncthreads();
   const int cstar = s_misc[0], kind = s_misc[1];

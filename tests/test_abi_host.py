@@ -36,13 +36,13 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_workspace_size(lib):
-    # V = 128256 fp32 -> 16 chunks of 8016 elements.  Layout: tickets (B + B*rows u32, padded to
+    # V = 128256 fp32 -> 16 chunks of 8016 elements.  Layout: counters (1 + B + B*rows u32, padded to
     # 256 B), chunk stats, row stats, request state, residual sums (each padded to 256 B).
     def up(x):
         return (x + 255) // 256 * 256
 
     B, rows, n = 64, 11, 16
-    want = up(B * 4 + B * rows * 4) + up(B * rows * n * 16) + up(B * rows * 32) + up(B * 16) + up(B * rows * n * 4)
+    want = up(4 + B * 4 + B * rows * 4) + up(B * rows * n * 16) + up(B * rows * 32) + up(B * 16) + up(B * rows * n * 4)
     assert lib.spec_verify_workspace_bytes(B, rows, 128256, 0) == want
     assert lib.spec_verify_workspace_bytes(-1, 6, 100, 0) == 0
     assert lib.spec_verify_workspace_bytes(4, 0, 100, 0) == 0
