@@ -159,6 +159,30 @@ spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t dt
                                       int32_t *err_flags, int32_t *node_argmax, void *workspace,
                                       size_t workspace_bytes, spec_stream_t stream);
 
+/*
+ * spec_verify_chain without a workspace argument, for callers that cannot allocate device memory
+ * (a plugin inside an engine that has reserved all GPU memory for its own pool, a hook that must
+ * not call cudaMalloc because it can synchronise the device, a binding with no CUDA allocator).
+ * The pages have no counterpart of this entry point; it is an interface convenience.
+ *
+ * Scratch lives in one device array of SPEC_STATIC_WORKSPACE_BYTES inside the library, which every
+ * GPU that loads the library holds until the process exits.  Calls whose scratch would not fit
+ * (spec_verify_workspace_bytes(B, 2K + 1, V, dtype) above the limit, K + 1 rows for T == 0) return
+ * SPEC_ERR_UNSUPPORTED.  The first call on a device looks up that device's copy of the array
+ * (cudaGetSymbolAddress, with the device current); make that first call before any stream
+ * capture.  Every call on a device shares the same array and leaves its contents behind; each call
+ * clears the counters it needs, but calls that may overlap on the GPU (other streams, other host
+ * threads) race on the array and must be serialised by the caller.  The call allocates nothing.
+ * Arguments and outputs as spec_verify_chain, without the optional per-position outputs.
+ */
+#define SPEC_STATIC_WORKSPACE_BYTES (4u << 20)
+spec_status_t spec_verify_chain_static(const void *target_logits, const void *draft_logits,
+                                       spec_dtype_t dtype, int B, int K, int V, float temperature,
+                                       const int32_t *draft_tokens, const float *r, const float *u,
+                                       int32_t *num_accepted, int32_t *out_tokens,
+                                       float *residual_mass, int32_t *err_flags,
+                                       spec_stream_t stream);
+
 /* Human-readable name of a status code (static string). */
 const char *spec_status_string(spec_status_t status);
 

@@ -22,7 +22,8 @@ MAX_K, MAX_TREE_NODES = 256, 4096
 DTYPE_CODE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 
 EXPORTED = ("spec_verify_workspace_bytes", "spec_verify_chain", "spec_verify_ngram",
-            "spec_verify_tree_greedy", "spec_status_string")
+            "spec_verify_tree_greedy", "spec_verify_chain_static", "spec_status_string")
+STATIC_WORKSPACE_BYTES = 4 << 20
 
 _lib = None
 
@@ -49,6 +50,8 @@ def library(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_ngram.restype = I
     lib.spec_verify_tree_greedy.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, P, Z, P]
     lib.spec_verify_tree_greedy.restype = I
+    lib.spec_verify_chain_static.argtypes = [P, P, I, I, I, I, F, P, P, P, P, P, P, P, P]
+    lib.spec_verify_chain_static.restype = I
     lib.spec_status_string.argtypes = [I]
     lib.spec_status_string.restype = ctypes.c_char_p
     if path is None:
