@@ -49,6 +49,7 @@ WORKLOADS = {
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["speculative_decoding_verification_82_gb300/csrc/verify_kernel.cuh",
                   "speculative_decoding_verification_82_gb300/csrc/verify_common.cuh",
+                  "speculative_decoding_verification_82_gb300/csrc/fastdiv.h",
                   "speculative_decoding_verification_82_gb300/csrc/spec_verify_api.cu"]
 
 
@@ -74,9 +75,9 @@ def rows_per_request(w: dict) -> int:
 
 
 def launches_per_step(w: dict) -> int:
-    """Kernel launches of one call: the stats kernel, plus the residual kernel for draft-model
-    chains (the ticket-clearing memset is not a kernel of this library)."""
-    return 2 if w["kind"] == "chain" else 1
+    """Kernel launches of one call: verify_kernel, which also makes the residual pass of
+    draft-model chains (the ticket-clearing memset is not a kernel of this library)."""
+    return 1
 
 
 def algorithmic_bytes(w: dict) -> int:
@@ -416,8 +417,7 @@ def run_gpu(args, w) -> None:
                      "frac": achieved / peak, "peak_source": peak_src,
                      "traffic": profiled_traffic(args.workload), "algorithmic_bytes_per_call": alg_bytes,
                      "mean_call_us": mean_call_ms * 1e3,
-                     "kernel": (f"stats_kernel<{w['kind']},{w['dtype']}>"
-                                + (" + residual_kernel (one call)" if w["kind"] == "chain" else ""))},
+                     "kernel": f"verify_kernel<{w['kind']},{w['dtype']}> (one launch per call)"},
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
         "gpu_launches": K * launches_per_step(w),

@@ -3,6 +3,7 @@
 // Host side only; the kernels live in verify_kernel.cuh (instantiated per element type in
 // spec_verify_{f32,bf16,f16}.cu).  No call allocates memory or synchronises the host.
 #include <math.h>
+#include <stdint.h>
 #include <stdlib.h>
 
 #include <climits>
@@ -23,71 +24,64 @@ using specv::Params;
 using specv::ReqState;
 using specv::RowStat;
 
-constexpr size_t kDefaultChunkBytes = 32 * 1024;
-
 int elem_size(spec_dtype_t dt) { return dt == SPEC_DTYPE_F32 ? 4 : 2; }
 bool dtype_ok(int dt) { return dt == SPEC_DTYPE_F32 || dt == SPEC_DTYPE_BF16 || dt == SPEC_DTYPE_F16; }
 size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
-// Bytes of logits staged per chunk.  ~32 KB: two stages per CTA and three CTAs per SM keep
-// about six chunks in flight per SM.  SPEC_VERIFY_CHUNK_BYTES overrides it (tuning; 4 KB..64 KB).
-size_t chunk_target() {
-  static const size_t v = [] {
-    const char* s = getenv("SPEC_VERIFY_CHUNK_BYTES");
-    const long x = s ? atol(s) : 0;
-    return (x >= 4096 && x <= 65536) ? (size_t)x : kDefaultChunkBytes;
-  }();
-  return v;
-}
-
+// A row of V elements spans at most ceil((V + VE - 1) / VE) 16-byte vectors (VE elements per
+// vector; the row may start anywhere inside its first vector).  Stats chunks take kChunkVec of
+// them, residual items kResVec.
 struct Chunking {
-  int chunk, nchunk, buf_bytes;
+  int nchunk, nchunk_r;
 };
-
-// Splits a row of V elements into nchunk near-equal chunks of `chunk` elements (a multiple of 8).
 Chunking plan_chunks(int V, int S) {
+  const long long VE = 16 / S;
+  const long long nvec = ((long long)V + VE - 1 + VE - 1) / VE;
   Chunking c;
-  const size_t row = (size_t)V * S;
-  size_t n0 = (row + chunk_target() - 1) / chunk_target();
-  if (n0 < 1) n0 = 1;
-  long long chunk = ((long long)V + (long long)n0 - 1) / (long long)n0;
-  chunk = (chunk + 7) / 8 * 8;
-  c.chunk = (int)chunk;
-  c.nchunk = (int)(((long long)V + chunk - 1) / chunk);
-  c.buf_bytes = c.chunk * S + 32;
+  c.nchunk = (int)((nvec + specv::kChunkVec - 1) / specv::kChunkVec);
+  c.nchunk_r = (int)((nvec + specv::kResVec - 1) / specv::kResVec);
   return c;
 }
 
 // Workspace layout:
-//   work    u32                  work-item counter  } one region, cleared by one
+//   work, gerr, exit_tick, pad   u32 x 4            } one region, cleared by one
 //   tick_a  [B] u32              request tickets    } cudaMemsetAsync per call
-//   tick_b  [B][Kc] u32          residual tickets   } (Kc = rows >= K)
+//   tick_b  [B][rows] u32        residual tickets   }
+//   req     [B]                  ReqState           }  (16-byte aligned)
 //   cstat   [B][rows][nchunk]    ChunkStat          (256-byte aligned regions from here on)
+//   sstat   [B][rows][nchunk][G] ChunkStat          sub-chunk partials (G consumer warps a group)
 //   rstat   [B][rows]            RowStat
-//   req     [B]                  ReqState
-//   wsum    [B][Kc][nchunk]      float
+//   wsum    [B][rows][nchunk_r]  float
+//   wsub    [B][rows][nchunk_r][G] float
 struct Layout {
-  size_t work, tick_a, tick_b, cstat, rstat, req, wsum, total;
+  size_t work, tick_a, tick_b, req, clear_end, cstat, sstat, rstat, wsum, wsub, total;
 };
 
-Layout layout(int B, int rows, int nchunk) {
+Layout layout(int B, int rows, const Chunking& ck) {
   Layout L;
-  const size_t b = (size_t)B, r = (size_t)rows, n = (size_t)nchunk;
+  const size_t b = (size_t)B, r = (size_t)rows;
   size_t off = 0;
   L.work = off;
-  off += 4;
+  off += 16;
   L.tick_a = off;
   off += b * 4;
   L.tick_b = off;
-  off = align_up(off + b * r * 4, 256);
+  off = align_up(off + b * r * 4, 16);
+  L.req = off;
+  off += b * sizeof(ReqState);
+  L.clear_end = off;
+  off = align_up(off, 256);
+  const size_t G = specv::kGroupWarps;
   L.cstat = off;
-  off = align_up(off + b * r * n * sizeof(ChunkStat), 256);
+  off = align_up(off + b * r * (size_t)ck.nchunk * sizeof(ChunkStat), 256);
+  L.sstat = off;
+  off = align_up(off + b * r * (size_t)ck.nchunk * G * sizeof(ChunkStat), 256);
   L.rstat = off;
   off = align_up(off + b * r * sizeof(RowStat), 256);
-  L.req = off;
-  off = align_up(off + b * sizeof(ReqState), 256);
   L.wsum = off;
-  off = align_up(off + b * r * n * sizeof(float), 256);
+  off = align_up(off + b * r * (size_t)ck.nchunk_r * sizeof(float), 256);
+  L.wsub = off;
+  off = align_up(off + b * r * (size_t)ck.nchunk_r * G * sizeof(float), 256);
   L.total = off;
   return L;
 }
@@ -105,29 +99,55 @@ int sm_count() {
 
 bool aligned_to(const void* p, int a) { return ((uintptr_t)p % (uintptr_t)a) == 0; }
 
-spec_status_t attach_workspace(Params& P, void* ws, size_t bytes, int B, int rows) {
-  const Layout L = layout(B, rows, P.nchunk);
+spec_status_t attach_workspace(Params& P, void* ws, size_t bytes, int B, int rows, const Chunking& ck) {
+  const Layout L = layout(B, rows, ck);
   if (ws == nullptr || bytes < L.total) return SPEC_ERR_WORKSPACE;
   if (((uintptr_t)ws & 255u) != 0) return SPEC_ERR_WORKSPACE;
   char* w = static_cast<char*>(ws);
   P.work = reinterpret_cast<unsigned*>(w + L.work);
+  P.gerr = P.work + 1;
+  P.exit_tick = P.work + 2;
   P.tick_a = reinterpret_cast<unsigned*>(w + L.tick_a);
   P.tick_b = reinterpret_cast<unsigned*>(w + L.tick_b);
-  P.tick_bytes = L.cstat - L.work;
-  P.cstat = reinterpret_cast<ChunkStat*>(w + L.cstat);
-  P.rstat = reinterpret_cast<RowStat*>(w + L.rstat);
   P.req = reinterpret_cast<ReqState*>(w + L.req);
+  P.clear_bytes = L.clear_end - L.work;
+  P.cstat = reinterpret_cast<ChunkStat*>(w + L.cstat);
+  P.sstat = reinterpret_cast<ChunkStat*>(w + L.sstat);
+  P.rstat = reinterpret_cast<RowStat*>(w + L.rstat);
   P.wsum = reinterpret_cast<float*>(w + L.wsum);
+  P.wsub = reinterpret_cast<float*>(w + L.wsub);
   return SPEC_OK;
 }
 
+// Requests between a request's stats items and its residual items: enough for the request's
+// chunks in flight to land and its acceptance result to be published before a producer stages the
+// residual items (a producer that gets there first waits).  SPEC_VERIFY_RESID_LAG overrides it.
+int residual_lag(int B, int items_per_request, int sms) {
+  static const int env = [] {
+    const char* s = getenv("SPEC_VERIFY_RESID_LAG");
+    return s ? atoi(s) : -1;
+  }();
+  long long L = env >= 0 ? env : 2 + ((long long)sms * 12 + items_per_request - 1) / items_per_request;
+  if (L > B) L = B;
+  return (int)L;
+}
+
+// Constants of the item decoding's divisions (see fastdiv.h).
+void set_divisors(Params& P, int rows) {
+  const unsigned A = (unsigned)rows * (unsigned)P.nchunk;
+  const unsigned R = (unsigned)P.npos * (unsigned)P.nchunk_r;
+  P.fd_A = specv::make_fastdiv(A);
+  P.fd_R = specv::make_fastdiv(R > 0 ? R : 1u);
+  P.fd_AR = specv::make_fastdiv(A + R);
+  P.fd_nchunk = specv::make_fastdiv((unsigned)P.nchunk);
+  P.fd_nchunk_r = specv::make_fastdiv((unsigned)P.nchunk_r);
+}
+
 spec_status_t launch(spec_dtype_t dtype, int mode, Params& P, specv::LaunchPlan& L, cudaStream_t stream) {
-  L.sm_count = sm_count();
-  if (L.sm_count <= 0) return SPEC_ERR_CUDA;
-  L.smem_stats = 2 * (size_t)P.buf_bytes;
-  L.smem_resid = 2 * (size_t)P.buf_bytes;
-  // the ticket counters start every call at zero, whatever the workspace held before
-  cudaError_t e = cudaMemsetAsync(P.work, 0, P.tick_bytes, stream);
+  L.smem = (size_t)specv::kStages * specv::kStageBytes + specv::kFinBytes;
+  // the ticket counters and acceptance flags start every call at zero, whatever the workspace
+  // held before
+  cudaError_t e = cudaMemsetAsync(P.work, 0, P.clear_bytes, stream);
   if (e != cudaSuccess) return SPEC_ERR_CUDA;
   switch (dtype) {
     case SPEC_DTYPE_F32: e = specv::launch_verify<float>(mode, P, L, stream); break;
@@ -161,14 +181,19 @@ spec_status_t verify_chain_common(bool ngram, const void* target, const void* dr
 
   Params P = {};
   const Chunking ck = plan_chunks(V, S);
-  P.chunk = ck.chunk;
   P.nchunk = ck.nchunk;
-  P.buf_bytes = ck.buf_bytes;
+  P.nchunk_r = ck.nchunk_r;
   const int diag = (cand_tokens || pos_mass) ? 1 : 0;
-  if ((long long)B * rows * P.nchunk > INT_MAX || (long long)B * (diag ? K : 1) * P.nchunk > INT_MAX)
-    return SPEC_ERR_UNSUPPORTED;
-  spec_status_t st = attach_workspace(P, ws, ws_bytes, B, rows);
+  P.npos = two_rows ? (diag ? K : 1) : 0;
+  const long long per_req = (long long)rows * ck.nchunk + (long long)P.npos * ck.nchunk_r;
+  if ((long long)B * per_req > INT_MAX) return SPEC_ERR_UNSUPPORTED;
+  spec_status_t st = attach_workspace(P, ws, ws_bytes, B, rows, ck);
   if (st != SPEC_OK) return st;
+  const int sms = sm_count();
+  if (sms <= 0) return SPEC_ERR_CUDA;
+  P.total = (unsigned)(B * per_req);
+  P.lag = P.npos ? residual_lag(B, rows * ck.nchunk, sms) : 0;
+  set_divisors(P, rows);
   P.target = target;
   P.draft = two_rows ? draft : nullptr;
   P.B = B;
@@ -191,7 +216,7 @@ spec_status_t verify_chain_common(bool ngram, const void* target, const void* dr
   P.target_probs = greedy ? nullptr : target_probs;
   P.draft_probs = two_rows ? draft_probs : nullptr;
   specv::LaunchPlan L = {};
-  L.launch_resid = two_rows ? 1 : 0;
+  L.sm_count = sms;
   L.launch_probs = (P.target_probs || P.draft_probs) ? 1 : 0;
   const int mode = greedy ? specv::kGreedy : (ngram ? specv::kNgram : specv::kChain);
   return launch(dtype, mode, P, L, reinterpret_cast<cudaStream_t>(stream));
@@ -204,7 +229,7 @@ extern "C" {
 size_t spec_verify_workspace_bytes(int B, int rows_per_request, int V, spec_dtype_t dtype) {
   if (B < 0 || rows_per_request < 1 || V < 1 || !dtype_ok(dtype)) return 0;
   const Chunking ck = plan_chunks(V, elem_size(dtype));
-  return layout(B, rows_per_request, ck.nchunk).total;
+  return layout(B, rows_per_request, ck).total;
 }
 
 spec_status_t spec_verify_chain(const void* target_logits, const void* draft_logits, spec_dtype_t dtype, int B,
@@ -243,12 +268,16 @@ spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t dt
   const int rows = N + 1;
   Params P = {};
   const Chunking ck = plan_chunks(V, S);
-  P.chunk = ck.chunk;
   P.nchunk = ck.nchunk;
-  P.buf_bytes = ck.buf_bytes;
+  P.nchunk_r = ck.nchunk_r;
   if ((long long)B * rows * P.nchunk > INT_MAX) return SPEC_ERR_UNSUPPORTED;
-  spec_status_t st = attach_workspace(P, workspace, workspace_bytes, B, rows);
+  spec_status_t st = attach_workspace(P, workspace, workspace_bytes, B, rows, ck);
   if (st != SPEC_OK) return st;
+  const int sms = sm_count();
+  if (sms <= 0) return SPEC_ERR_CUDA;
+  P.total = (unsigned)((long long)B * rows * P.nchunk);
+  P.npos = 0;
+  set_divisors(P, rows);
   P.target = target_logits;
   P.B = B;
   P.K = 0;
@@ -263,6 +292,7 @@ spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t dt
   P.err_flags = err_flags;
   P.node_argmax = node_argmax;
   specv::LaunchPlan L = {};
+  L.sm_count = sms;
   return launch(dtype, specv::kTree, P, L, reinterpret_cast<cudaStream_t>(stream));
 }
 

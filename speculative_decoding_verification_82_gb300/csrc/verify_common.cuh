@@ -1,5 +1,6 @@
-// verify_common.cuh -- element formats, PTX wrappers, reductions, chunk staging and the
-// inverse-CDF search shared by the verification kernels (sm_103a).
+// verify_common.cuh -- element formats, PTX wrappers (mbarrier, bulk TMA copies), warp
+// reductions, row staging and the warp-level inverse-CDF search used by the verification kernel
+// (sm_103a).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -11,11 +12,40 @@
 
 namespace specv {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
-constexpr int kMaxTiles = 32;  // tiles of 256 16-byte vectors: chunks up to 128 KB
+// ------------------------------------------------------------------ kernel geometry ----
+// One CTA per SM, warp-specialised: two groups of eight consumer warps reduce staged chunks (the
+// groups take alternate stages; four consumer warps per SM sub-partition hide the latency of the
+// special-function unit), one producer warp per group claims work and drives the bulk copies,
+// one bookkeeping warp publishes per-chunk results and counts them per request, one finishing
+// warp completes the requests assigned to this CTA.
+constexpr int kConsWarps = 16;
+constexpr int kGroups = 2;
+constexpr int kGroupWarps = kConsWarps / kGroups;
+constexpr int kProducerWarp = 16;  // and 17
+constexpr int kBookWarp = 18;
+constexpr int kFinWarp = 19;
+constexpr int kThreads = 20 * 32;
+constexpr int kStages = 6;                         // staged-chunk ring depth (a multiple of kGroups)
+constexpr int kSlots = 16;                         // ring of per-chunk results (partials, merged)
+constexpr int kClaim = 4;                          // work items claimed per atomic
+constexpr int kChunkVec = 2048;                    // 16-byte vectors per chunk of a row (32 KB)
+constexpr int kSubVec = kChunkVec / kGroupWarps;   // vectors per consumer warp (a sub-chunk)
+constexpr int kVecPerLane = kSubVec / 32;
+constexpr int kResVec = 1024;                      // target vectors per residual work item
+constexpr int kResSub = kResVec / kGroupWarps;     // target vectors per consumer warp
+constexpr int kDraftSlot = kResVec + 1;            // first slot of the draft range in a stage
+constexpr int kStageVec = 2056;                    // >= kChunkVec and >= kDraftSlot + kResVec + 1
+constexpr int kStageBytes = kStageVec * 16;
+constexpr int kFinDraftSlot = kResSub + 1;         // finishing buffer: draft slot of a residual pair
+constexpr int kFinVec = 264;                       // >= kSubVec and >= kFinDraftSlot + kResSub + 1
+constexpr int kFinBytes = kFinVec * 16;
 constexpr unsigned kFull = 0xffffffffu;
 constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at GB300 clocks
+static_assert(kVecPerLane * 32 == kSubVec && kResSub % 32 == 0, "warp split");
+static_assert(kStageVec >= kChunkVec && kStageVec >= kDraftSlot + kResVec + 1, "stage size");
+static_assert(kFinVec >= kSubVec && kFinVec >= kFinDraftSlot + kResSub + 1, "finishing buffer size");
+static_assert(kStageBytes % 128 == 0 && kFinBytes % 128 == 0, "alignment");
+static_assert(kStages % kGroups == 0 && kSlots % kGroups == 0, "a stage and a slot always serve the same group");
 
 // ------------------------------------------------------------------- element formats ----
 // Each logits element type knows how to unpack a 16-byte vector into floats, how to take a
@@ -41,6 +71,9 @@ struct Elem<float> {
     *reinterpret_cast<uint32_t*>(p) = v;
   }
   __device__ __forceinline__ static float to_float(uint32_t raw) { return __uint_as_float(raw); }
+  __device__ __forceinline__ static float smem_elem(const unsigned char* p) {
+    return *reinterpret_cast<const float*>(p);
+  }
   // NaN-propagating max of two packed words (one fp32 each)
   __device__ __forceinline__ static uint32_t max_word(uint32_t a, uint32_t b) {
     float r;
@@ -70,6 +103,9 @@ struct Elem<__nv_bfloat16> {
     *reinterpret_cast<uint16_t*>(p) = (uint16_t)v;
   }
   __device__ __forceinline__ static float to_float(uint32_t raw) { return __uint_as_float(raw << 16); }
+  __device__ __forceinline__ static float smem_elem(const unsigned char* p) {
+    return __uint_as_float((uint32_t)(*reinterpret_cast<const uint16_t*>(p)) << 16);
+  }
   __device__ __forceinline__ static uint32_t max_word(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -105,6 +141,9 @@ struct Elem<__half> {
   __device__ __forceinline__ static float to_float(uint32_t raw) {
     return __half2float(__ushort_as_half((unsigned short)raw));
   }
+  __device__ __forceinline__ static float smem_elem(const unsigned char* p) {
+    return __half2float(*reinterpret_cast<const __half*>(p));
+  }
   __device__ __forceinline__ static uint32_t max_word(uint32_t a, uint32_t b) {
     uint32_t r;
     asm("max.NaN.f16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -133,15 +172,21 @@ __device__ __forceinline__ float fmax_nan(float a, float b) {
   asm("max.NaN.f32 %0, %1, %2;" : "=f"(r) : "f"(a), "f"(b));
   return r;
 }
+__device__ __forceinline__ uint4 lds128(const unsigned char* p) { return *reinterpret_cast<const uint4*>(p); }
+
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
 }
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;\n\tfence.proxy.async.shared::cta;" ::: "memory");
 }
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+// Raises the transaction count of the current phase (no arrival).
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
                : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -154,34 +199,38 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Waits for phase `parity` of `bar`; gives up after kWaitLimitCycles and returns false.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Non-blocking test of the phase of `bar` with parity `parity`.
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_addr(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for the phase of `bar` with parity `parity`.  Gives up (returns false) after
+// kWaitLimitCycles, or early once *abort is set.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitLimitCycles) return false;
+  for (;;) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (*abort || clock64() - t0 > kWaitLimitCycles) return false;
   }
-  return true;
 }
 // Bulk (non-tensor) TMA copy global -> this CTA's shared memory, completing on `bar`.
 // Both addresses 16-byte aligned, size a multiple of 16.
-__device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                            uint64_t policy) {
+__device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
   asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], "
-      "%4;" ::"r"(smem_addr(dst)),
-      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
+__device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 
 // -------------------------------------------------------------------- reductions ----
 __device__ __forceinline__ float warp_sum(float v) {
@@ -217,15 +266,6 @@ __device__ __forceinline__ double warp_incl_scan_d(double v, int lane) {
   }
   return v;
 }
-// 2^x in double with fp32 relative accuracy (~3e-7): the integer part of x scales exactly, the
-// fractional part goes through the special-function unit.  Avoids double-precision
-// transcendentals, which are slow on this part.
-__device__ __forceinline__ double exp2_split(double x) {
-  if (!(x > -1070.0)) return x != x ? x : 0.0;
-  if (x > 1020.0) return __longlong_as_double(0x7ff0000000000000LL);
-  const double n = floor(x);
-  return ldexp((double)ex2((float)(x - n)), (int)n);
-}
 // Inclusive prefix sum across the warp (Kogge-Stone), fixed association.
 __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
 #pragma unroll
@@ -235,206 +275,189 @@ __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
   }
   return v;
 }
-// Block-wide reductions; every thread gets the same value.  `scratch` holds kWarps entries
-// (2 * kWarps for block_sum2).
-__device__ __forceinline__ float block_max_nan(float v, float* scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_max_nan(v);
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  float r = scratch[0];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) r = fmax_nan(r, scratch[w]);
-  __syncthreads();
-  return r;
+// 2^x in double with fp32 relative accuracy (~3e-7): the integer part of x scales exactly, the
+// fractional part goes through the special-function unit.  Avoids double-precision
+// transcendentals, which are slow on this part.
+__device__ __forceinline__ double exp2_split(double x) {
+  if (!(x > -1020.0)) return x != x ? x : 0.0;
+  if (x > 1020.0) return __longlong_as_double(0x7ff0000000000000LL);
+  const int n = __double2int_rd(x);
+  const double scale = __hiloint2double((n + 1023) << 20, 0);  // 2^n
+  return (double)ex2((float)(x - (double)n)) * scale;
 }
-__device__ __forceinline__ void block_sum2(float& a, float& b, float* scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  a = warp_sum(a);
-  b = warp_sum(b);
-  if (lane == 0) {
-    scratch[warp] = a;
-    scratch[kWarps + warp] = b;
-  }
-  __syncthreads();
-  float ra = scratch[0], rb = scratch[kWarps];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) {
-    ra = __fadd_rn(ra, scratch[w]);
-    rb = __fadd_rn(rb, scratch[kWarps + w]);
-  }
-  __syncthreads();
-  a = ra;
-  b = rb;
-}
-__device__ __forceinline__ int block_min_i(int v, int* scratch) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  v = warp_min_i(v);
-  if (lane == 0) scratch[warp] = v;
-  __syncthreads();
-  int r = scratch[0];
-#pragma unroll
-  for (int w = 1; w < kWarps; ++w) r = min(r, scratch[w]);
-  __syncthreads();
-  return r;
+// a / b in double without the division sequence: an fp32 reciprocal refined by two Newton steps
+// (relative error ~1e-15 for finite, positive, normal b).
+__device__ __forceinline__ double div_pos(double a, double b) {
+  double r = (double)__frcp_rn((float)b);
+  r = r * __fma_rn(-b, r, 2.0);
+  r = r * __fma_rn(-b, r, 2.0);
+  return a * r;
 }
 
-// ------------------------------------------------------------------- chunk staging ----
-// A chunk is the element range [e0, e0 + n) of one logits row, staged in shared memory as whole
-// 16-byte vectors.  Element e0 sits at slot `slot0`, chosen so that a slot's shared-memory address
-// has the same 16-byte phase as the element's global address (then the whole vectors inside the
-// chunk can come by one bulk TMA copy).  Slots outside [e0, e0 + n) hold -inf.
-struct Geo {
-  int e0, n, slot0, nvec;
-};
-
+// ------------------------------------------------------------------------ row staging ----
+// A logits row is read as a grid of 16-byte vectors starting at the row's address rounded down to
+// 16 bytes: grid vector v holds elements v * VE - phase .. v * VE - phase + VE - 1, where phase is
+// the number of elements of the first vector that precede the row.  Vectors lying wholly inside
+// the row go by one bulk TMA copy; the (at most two) vectors that straddle the row's start or end
+// are read element by element, with -inf in the positions outside the row.
 template <typename T>
-__device__ __forceinline__ Geo make_geo(const char* row, int e0, int n) {
+struct RowGrid {
+  const char* grid;  // 16-byte aligned address of grid vector 0
+  int phase;         // elements of vector 0 before the row start
+  int nvec;          // vectors covering the row
+};
+template <typename T>
+__device__ __forceinline__ RowGrid<T> row_grid(const char* row, int V) {
   constexpr int S = Elem<T>::kSize, VE = Elem<T>::kPerVec;
-  Geo g;
-  g.e0 = e0;
-  g.n = n;
-  g.slot0 = (int)((((uintptr_t)row + (size_t)e0 * S) & 15u) / S);
-  g.nvec = n > 0 ? (g.slot0 + n + VE - 1) / VE : 0;
+  RowGrid<T> g;
+  const uintptr_t a = (uintptr_t)row;
+  g.grid = row - (a & 15u);
+  g.phase = (int)((a & 15u) / S);
+  g.nvec = (g.phase + V + VE - 1) / VE;
   return g;
 }
 
-// Issues the loads of chunk `g` of `row` into `buf` (laid out with g.slot0).  The whole vectors
-// go by one TMA copy when the row's phase matches the layout, the rest by plain loads of all
-// threads.  Thread 0 always arrives once on `bar` (expecting 0 bytes when nothing goes by TMA),
-// so every issue completes exactly one phase of `bar`.
+// Stages grid vectors [v0, v1) of a row (V elements) at `dst`, one warp.  Lane 0 raises the
+// transaction count of `bar` and issues the bulk copy; the lanes fill the straddling vectors
+// with plain loads.  The caller arrives on `bar` after a __syncwarp().
 template <typename T>
-__device__ __forceinline__ void issue_chunk(unsigned char* buf, const char* row, const Geo& g, uint64_t* bar,
-                                            uint64_t pol) {
+__device__ __forceinline__ void warp_stage(unsigned char* dst, const RowGrid<T>& g, int V, int v0, int v1,
+                                           uint64_t* bar, int lane) {
   constexpr int S = Elem<T>::kSize, VE = Elem<T>::kPerVec;
-  const char* p = row + (size_t)g.e0 * S;
-  const bool phase_ok = (int)(((uintptr_t)p & 15u) / S) == g.slot0;
-  int vA = g.slot0 > 0 ? 1 : 0, vB = (g.slot0 + g.n) / VE;
-  if (g.n <= 0 || vB <= vA || !phase_ok) vA = vB = 0;
-  const uint32_t bytes = (uint32_t)(vB - vA) * 16u;
-  if (threadIdx.x == 0) {
-    mbar_arrive_expect_tx(bar, bytes);
-    if (bytes) tma_load_1d(buf + vA * 16, p + (ptrdiff_t)(vA * VE - g.slot0) * S, bytes, bar, pol);
+  if (v1 <= v0) return;
+  const int fa = g.phase > 0 ? 1 : 0;
+  const int fb = (g.phase + V) / VE;  // vectors [fa, fb) lie wholly inside the row
+  const int a = max(v0, fa), e = min(v1, fb);
+  if (a < e && lane == 0) {
+    const uint32_t bytes = (uint32_t)(e - a) * 16u;
+    mbar_expect_tx(bar, bytes);
+    tma_load_1d(dst + (size_t)(a - v0) * 16, g.grid + (size_t)a * 16, bytes, bar);
   }
-  // plain loads: everything when no TMA copy, else only the (at most two) ragged end vectors
-  const int total = g.nvec * VE;
-  const int head = bytes ? vA * VE : total;
-  const int tail0 = bytes ? vB * VE : total;
-  const int nplain = head + (total - tail0);
-  for (int i = (int)threadIdx.x; i < nplain; i += kThreads) {
-    const int s = i < head ? i : tail0 + (i - head);
-    const int e = s - g.slot0;
-    const uint32_t raw = (e >= 0 && e < g.n) ? Elem<T>::load_raw(p + (ptrdiff_t)e * S) : Elem<T>::kNegInf;
-    Elem<T>::store_raw(buf + (size_t)s * S, raw);
+  // straddling vectors: grid vector 0 when the row starts mid-vector, grid vector fb when it
+  // ends mid-vector
+  const int first = (fa == 1 && v0 == 0) ? 0 : -1;
+  int last = (fb < g.nvec && fb >= v0 && fb < v1) ? fb : -1;
+  if (last == first) last = -1;  // a row inside one vector: the first pass fills it
+  if (lane < 2 * VE) {
+    const int rv = lane < VE ? first : last;
+    const int j = lane % VE;
+    if (rv >= 0) {
+      const int el = rv * VE + j - g.phase;
+      const uint32_t raw =
+          (el >= 0 && el < V) ? Elem<T>::load_raw(g.grid + (size_t)g.phase * S + (size_t)el * S) : Elem<T>::kNegInf;
+      Elem<T>::store_raw(dst + (size_t)(rv - v0) * 16 + (size_t)j * S, raw);
+    }
   }
-}
-
-// NaN-propagating maximum of this thread's vectors of a staged chunk (padding is -inf).
-template <typename T>
-__device__ __forceinline__ float thread_max(const unsigned char* buf, int nvec) {
-  using E = Elem<T>;
-  uint32_t m0 = E::kNegInfWord, m1 = E::kNegInfWord;
-  for (int v = (int)threadIdx.x; v < nvec; v += kThreads) {
-    const uint4 w = *reinterpret_cast<const uint4*>(buf + (size_t)v * 16);
-    m0 = E::max_word(m0, E::max_word(w.x, w.y));
-    m1 = E::max_word(m1, E::max_word(w.z, w.w));
-  }
-  return E::word_max(E::max_word(m0, m1));
 }
 
 // ---------------------------------------------------------------- inverse-CDF search ----
-// Finds in a staged chunk the element where the running weight, taken in index order, first
-// exceeds `t`; `wf(v, w)` fills the weights of vector v.  The search is hierarchical: tiles of
-// 256 vectors -> warps of 32 vectors -> the lane's vector -> its elements.  At each level it
-// takes the first part with positive weight whose running total exceeds t, otherwise the last
-// part with positive weight (rounding), so a zero-weight element is never returned.  Returns the
-// element's vocabulary index in every thread, or -1 when the chunk holds no positive weight.
+// One warp finds, in a staged range of `nvec` vectors, the element where the running weight taken
+// in index order first exceeds t; wf(v, w) fills the VE weights of vector v.  The range is cut
+// into 32 blocks of Bs consecutive vectors (Bs a multiple of 8, so that the lanes' rotated reads
+// hit distinct shared-memory banks); each lane sums one block, a warp scan over the block sums
+// picks the crossing block, the lanes then split that block (q consecutive vectors each), and a
+// second scan picks the lane, then the vector, then the element.  At every level the first part
+// with positive weight whose running total exceeds t is taken, otherwise the last part with
+// positive weight (rounding), so a zero-weight element is never returned.  Returns the position
+// (vector * VE + element) in every lane, or -1 when the range holds no positive weight.
 template <int VE, typename WF>
-__device__ int chunk_crossing(const Geo& g, float t, WF wf, float (*tileW)[kWarps], int* s_int, float* s_flt) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int ntiles = (g.nvec + kThreads - 1) / kThreads;
-  for (int j = 0; j < ntiles; ++j) {
-    const int v = j * kThreads + (int)threadIdx.x;
-    float vs = 0.f;
-    if (v < g.nvec) {
+__device__ int warp_crossing(int nvec, float t, WF wf) {
+  const int lane = threadIdx.x & 31;
+  if (nvec <= 0) return -1;
+  const int Bs = ((nvec + 31) / 32 + 7) / 8 * 8;  // vectors per block
+  // level 1: block sums
+  float bsum = 0.f;
+  {
+    const int v0 = lane * Bs;
+    for (int i = 0; i < Bs; ++i) {
+      int r = i + (lane & 7);  // rotated start: the 8 lanes of a quarter-warp hit distinct banks
+      r -= (r >= Bs) ? Bs : 0;
+      const int v = v0 + r;
+      if (v < nvec) {
+        float w[VE];
+        wf(v, w);
+        float vs = 0.f;
+#pragma unroll
+        for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, w[j]);
+        bsum = __fadd_rn(bsum, vs);
+      }
+    }
+  }
+  float incl = warp_incl_scan(bsum, lane);
+  float excl = __shfl_up_sync(kFull, incl, 1);
+  if (lane == 0) excl = 0.f;
+  unsigned hit = __ballot_sync(kFull, bsum > 0.f && incl > t);
+  unsigned pos = __ballot_sync(kFull, bsum > 0.f);
+  if (!pos) return -1;
+  const int L = hit ? (__ffs(hit) - 1) : (31 - __clz(pos));
+  const float base = __shfl_sync(kFull, excl, L);
+  // level 2: block L split over the lanes, q consecutive vectors each (q <= 2 for ranges of at
+  // most 2048 vectors; larger blocks loop)
+  const int bend = min((L + 1) * Bs, nvec);
+  const int q = (Bs + 31) / 32;
+  const int v0 = L * Bs + lane * q;
+  float lsum = 0.f;
+  for (int qq = 0; qq < q; ++qq) {
+    const int v = v0 + qq;
+    if (v < bend) {
       float w[VE];
       wf(v, w);
-      vs = w[0];
+      float vs = 0.f;
 #pragma unroll
-      for (int q = 1; q < VE; ++q) vs = __fadd_rn(vs, w[q]);
+      for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, w[j]);
+      lsum = __fadd_rn(lsum, vs);
     }
-    const float incl = warp_incl_scan(vs, lane);
-    if (lane == 31) tileW[j][warp] = incl;
   }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float run = 0.f, pickR = 0.f, lastR = 0.f;
-    int pick = -1, last = -1;
-    for (int q = 0; q < ntiles * kWarps; ++q) {
-      const float W = tileW[q / kWarps][q % kWarps];
-      if (W > 0.f) {
-        const float nxt = __fadd_rn(run, W);
-        if (nxt > t) {
-          pick = q;
-          pickR = run;
-          break;
-        }
-        last = q;
-        lastR = run;
-        run = nxt;
-      }
-    }
-    if (pick < 0) {
-      pick = last;
-      pickR = lastR;
-    }
-    s_int[0] = pick;
-    s_int[1] = -1;
-    s_flt[0] = pickR;
-  }
-  __syncthreads();
-  const int pick = s_int[0];
-  const float pickR = s_flt[0];
-  if (pick >= 0 && warp == pick % kWarps) {
-    const int v = (pick / kWarps) * kThreads + warp * 32 + lane;
-    float w[VE];
-    float vs = 0.f;
-    if (v < g.nvec) {
+  incl = warp_incl_scan(lsum, lane);
+  excl = __shfl_up_sync(kFull, incl, 1);
+  if (lane == 0) excl = 0.f;
+  hit = __ballot_sync(kFull, lsum > 0.f && __fadd_rn(base, incl) > t);
+  pos = __ballot_sync(kFull, lsum > 0.f);
+  if (!pos) return -1;  // cannot happen: block L holds positive weight
+  const int L2 = hit ? (__ffs(hit) - 1) : (31 - __clz(pos));
+  int found = -1;
+  if (lane == L2) {
+    // the lane's vectors in order, then the elements of the chosen vector
+    float acc = __fadd_rn(base, excl);
+    int pv = -1, lv = -1;
+    float pacc = 0.f, lacc = 0.f;
+    for (int qq = 0; qq < q; ++qq) {
+      const int v = v0 + qq;
+      if (v >= bend) break;
+      float w[VE];
       wf(v, w);
-      vs = w[0];
+      float vs = 0.f;
 #pragma unroll
-      for (int q = 1; q < VE; ++q) vs = __fadd_rn(vs, w[q]);
-    } else {
-#pragma unroll
-      for (int q = 0; q < VE; ++q) w[q] = 0.f;
-    }
-    const float incl = warp_incl_scan(vs, lane);
-    float excl = __shfl_up_sync(kFull, incl, 1);
-    if (lane == 0) excl = 0.f;
-    const float end = __fadd_rn(pickR, incl);
-    const unsigned hit = __ballot_sync(kFull, vs > 0.f && end > t);
-    const unsigned pos = __ballot_sync(kFull, vs > 0.f);
-    const int L = hit ? (__ffs(hit) - 1) : (pos ? 31 - __clz(pos) : -1);
-    if (lane == L) {
-      const float acc = __fadd_rn(pickR, excl);
-      float run = 0.f;
-      int pj = -1, lj = -1;
-#pragma unroll
-      for (int q = 0; q < VE; ++q) {
-        run = __fadd_rn(run, w[q]);
-        if (w[q] > 0.f) {
-          if (pj < 0 && __fadd_rn(acc, run) > t) pj = q;
-          lj = q;
+      for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, w[j]);
+      if (vs > 0.f) {
+        if (pv < 0 && __fadd_rn(acc, vs) > t) {
+          pv = v;
+          pacc = acc;
         }
+        lv = v;
+        lacc = acc;
       }
-      if (pj < 0) pj = lj;
-      s_int[1] = g.e0 - g.slot0 + v * VE + pj;
+      acc = __fadd_rn(acc, vs);
     }
+    if (pv < 0) {
+      pv = lv;
+      pacc = lacc;
+    }
+    float w[VE];
+    wf(pv, w);
+    float r2 = 0.f;
+    int pj = -1, lj = -1;
+#pragma unroll
+    for (int j = 0; j < VE; ++j) {
+      r2 = __fadd_rn(r2, w[j]);
+      if (w[j] > 0.f) {
+        if (pj < 0 && __fadd_rn(pacc, r2) > t) pj = j;
+        lj = j;
+      }
+    }
+    found = pv * VE + (pj >= 0 ? pj : lj);
   }
-  __syncthreads();
-  const int tok = s_int[1];
-  __syncthreads();
-  return tok;
+  return __shfl_sync(kFull, found, L2);
 }
 
 }  // namespace specv

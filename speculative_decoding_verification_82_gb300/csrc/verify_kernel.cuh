@@ -1,23 +1,27 @@
-// verify_kernel.cuh -- the verification kernels (sm_103a).
+// verify_kernel.cuh -- the verification kernel (sm_103a).
 //
-// stats_kernel (every call).  A persistent grid streams every logits row once, in chunks of
-// ~32 KB staged in shared memory by bulk TMA copies through a two-stage ring per CTA (the next
-// chunk is in flight while the current one is reduced).  Per chunk it records either the chunk
-// maximum m_c and s_c = sum 2^(l c - m_c c) (temperature softmax, c = log2(e)/T, in the
-// online-softmax form so chunks combine exactly), or the chunk's (max, first index) for greedy
-// modes.  Work items are ordered request-major; the CTA that completes a request's last chunk
-// (an atomic ticket, never a spin) finishes that request: it combines the chunk statistics into
-// (m, Z) per row, computes alpha_k = min(1, p_k(x_k)/q_k(x_k)) in double, runs the acceptance
-// scan, and draws the emitted token by inverse CDF for the bonus row and the n-gram residual (it
-// knows the per-chunk weights, so it re-reads only the one chunk holding the crossing), or takes
-// the argmax (greedy chain), or walks the draft tree.
-//
-// residual_kernel (draft-model chain with T > 0 only).  For a request rejected at position n the
-// weights max(0, p_n - q_n) need both rows' global statistics, so this second launch reads the
-// pair at n once more, chunk by chunk, and sums the residual per chunk; the last chunk's CTA
-// re-reads the crossing chunk and draws the token.
-//
-// probs_kernel (testing only) writes the normalised p / q rows.
+// verify_kernel is persistent (one CTA per SM) and warp-specialised:
+//  - two groups of eight consumer warps take alternate stages of a six-stage shared-memory ring;
+//    each group has a producer warp that claims work items from an atomic counter (a batch of
+//    items per claim, the next batch claimed ahead) and stages each item's logits into its
+//    group's stages with bulk TMA copies (an mbarrier per stage for "full" and one for "empty");
+//    each consumer warp reduces one contiguous sub-chunk of the staged chunk
+//    (temperature-softmax statistics, argmax, or the residual sum) and leaves its partial in a
+//    ring of slots; the group's last warp to do so merges the partials and writes the chunk's
+//    statistics and its sub-chunk partials;
+//  - the bookkeeping warp counts each written chunk on its request (one memory fence per batch
+//    of ready chunks, then fire-and-forget reductions);
+//  - the finishing warp owns requests b = blockIdx.x, blockIdx.x + gridDim.x, ...: once a
+//    request's count says every chunk is in, it combines the chunk statistics into per-row
+//    normalisers, computes alpha_k = min(1, p_k(x_k)/q_k(x_k)), runs the acceptance scan, and
+//    draws the emitted token by inverse CDF from the chunk and sub-chunk weights (re-reading only
+//    the sub-chunk that holds the crossing), or walks the draft tree.
+// Work items are ordered request-major.  For chains with draft logits and T > 0 the draw after a
+// rejection at position n needs max(0, p_n - q_n), which needs both rows' normalisers first; the
+// pair at n is then read a second time by residual work items, placed in the item order a fixed
+// number of requests after the request's own items, so that the pair is read again shortly after
+// its first read (normally still in L2).  Their producer waits (bounded) for the request's
+// acceptance result before staging them.
 //
 // Formulas: "Speculative Decoding in Production: From Draft Models to EAGLE-3 Dynamic Trees for
 // 3x-5x Lossless Acceleration", section I.1 (acceptance ratio, uniform test, first-rejection
@@ -26,21 +30,24 @@
 
 #include <climits>
 
+#include "fastdiv.h"
 #include "verify_common.cuh"
 
 namespace specv {
 
 enum Mode : int { kChain = 0, kNgram = 1, kGreedy = 2, kTree = 3 };
-enum Kind : int { kFullP = 0, kExcl = 1, kResid = 2 };
+enum Kind : int { kFullP = 0, kExcl = 1 };
+enum ItemKind : int { kItemStats = 0, kItemResid = 1, kItemSkip = 2, kItemEnd = 3 };
 
-// Per chunk of a logits row, written by stats_kernel.
+// Per chunk of a logits row (and, with the same layout, per sub-chunk).
 struct __align__(16) ChunkStat {
-  float a;   // chunk maximum
-  float s;   // softmax: sum over the chunk of 2^(l c - a c)
-  float sx;  // softmax, n-gram target rows: the same sum without the draft token; else = s
-  int i;     // softmax: SPEC_ERRF_* bits; argmax modes: first index of the maximum (-1: NaN)
+  float a;    // maximum (NaN if the range holds a NaN)
+  float s;    // softmax: sum over the range of 2^(l c - RN(a c))
+  float rsv;  // 0
+  int i;      // softmax: SPEC_ERRF_* bits; argmax modes: first index of the maximum
+              // (-1: the range holds a NaN; INT_MAX: the range is empty)
 };
-// Per logits row, written by the request's finishing CTA.
+// Per logits row, written by the request's finishing warp.
 struct __align__(16) RowStat {
   double Z;  // sum over the row of 2^(l c - mc)
   float mc;  // fp32 product (row maximum) * c
@@ -48,22 +55,30 @@ struct __align__(16) RowStat {
   int amax;  // argmax modes: row argmax
   int pad[3];
 };
+// Per request: the acceptance result, published (ready = 1) for the residual work items.
 struct __align__(16) ReqState {
   int n;    // accepted prefix length
   int err;  // SPEC_ERRF_* bits
-  int pad[2];
+  int ready;
+  int pad;
 };
 static_assert(sizeof(ChunkStat) == 16 && sizeof(RowStat) == 32 && sizeof(ReqState) == 16, "layout");
 
 struct Params {
   const void* target;
   const void* draft;
-  int B, K, V, R;     // R: target rows per request (K + 1, or N + 1 for trees)
-  int rows;           // logits rows per request read by stats_kernel (draft-model chain: 2K + 1)
-  int chunk, nchunk;  // elements per chunk (multiple of 8), chunks per row
-  int buf_bytes;      // shared-memory bytes of one staged chunk
-  int diag;           // 1: draw at every position (per-position outputs requested)
-  float c;            // log2(e) / T
+  int B, K, V, R;  // R: target rows per request (K + 1, or N + 1 for trees)
+  int rows;        // logits rows per request read by the stats items (draft-model chain: 2K + 1)
+  int nchunk;      // stats chunks per row (kChunkVec vectors each)
+  int nchunk_r;    // residual items per row (kResVec target vectors each)
+  int npos;        // residual positions per request (K with per-position outputs, else 1); 0: none
+  int lag;         // requests between a request's stats items and its residual items
+  int diag;        // 1: draw at every position (per-position outputs requested)
+  float c;         // log2(e) / T
+  unsigned total;  // work items
+  // the divisors of the item decoding: A = rows * nchunk stats items per request, R = npos *
+  // nchunk_r residual items per request, A + R, nchunk, nchunk_r
+  FastDiv fd_A, fd_R, fd_AR, fd_nchunk, fd_nchunk_r;
   const int32_t* draft_tokens;
   const float* r;
   const float* u;
@@ -81,14 +96,18 @@ struct Params {
   int32_t* accept_len;
   int32_t* path_nodes;
   int32_t* node_argmax;
-  ChunkStat* cstat;  // [B][rows][nchunk]
-  RowStat* rstat;    // [B][rows]
-  ReqState* req;     // [B]
-  float* wsum;       // [B][K][nchunk] (per-position outputs) or [B][nchunk]
-  unsigned* work;    // work-item counter of stats_kernel (zeroed by the host before each call)
-  unsigned* tick_a;  // [B] request tickets of stats_kernel (zeroed likewise)
-  unsigned* tick_b;  // [B][K] or [B] tickets of residual_kernel (zeroed likewise)
-  size_t tick_bytes; // bytes of the two ticket arrays (one contiguous region)
+  ChunkStat* cstat;     // [B][rows][nchunk]
+  ChunkStat* sstat;     // [B][rows][nchunk][kGroupWarps] sub-chunk partials (softmax modes)
+  RowStat* rstat;       // [B][rows]
+  ReqState* req;        // [B]
+  float* wsum;          // [B][npos][nchunk_r] residual weight per residual item
+  float* wsub;          // [B][npos][nchunk_r][kGroupWarps] residual weight per sub-range
+  unsigned* work;       // work-item counter    } cleared by the host before each call
+  unsigned* gerr;       // timeout flag           }
+  unsigned* exit_tick;  // exiting CTAs           }
+  unsigned* tick_a;     // [B] chunks in, per request          }
+  unsigned* tick_b;     // [B][npos] residual items in         }  (req[] is cleared too)
+  size_t clear_bytes;   // bytes from `work` through req[B - 1]
 };
 
 template <typename T>
@@ -97,18 +116,36 @@ __device__ __forceinline__ const char* row_ptr(const Params& P, int b, int r) {
   if (r < P.R) return static_cast<const char*>(P.target) + ((size_t)b * P.R + r) * (size_t)P.V * S;
   return static_cast<const char*>(P.draft) + ((size_t)b * P.K + (r - P.R)) * (size_t)P.V * S;
 }
-__device__ __forceinline__ int chunk_len(const Params& P, int ch) { return min(P.chunk, P.V - ch * P.chunk); }
 
-// Weight of a chunk in units of the row normaliser: s (or sx) * 2^(RN(a c) - mc).
-__device__ __forceinline__ double chunk_weight(float a, float s, float c, float mc) {
-  if (a == -INFINITY) return 0.0;
-  return (double)s * (double)ex2(__fsub_rn(__fmul_rn(a, c), mc));
+// Weight of a chunk (or sub-chunk) relative to the row maximum: s * 2^(RN(a c) - mc), in fp32 (the
+// factor 2^(...) already carries the special-function unit's ~2 ulp).
+__device__ __forceinline__ float chunk_weight(float a, float s, float c, float mc) {
+  if (a == -INFINITY) return 0.f;
+  return __fmul_rn(s, ex2(__fsub_rn(__fmul_rn(a, c), mc)));
+}
+__device__ __forceinline__ ChunkStat ld_chunkstat(const ChunkStat* p) {
+  const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
+  ChunkStat q;
+  q.a = v.x;
+  q.s = v.y;
+  q.rsv = v.z;
+  q.i = __float_as_int(v.w);
+  return q;
+}
+__device__ __forceinline__ RowStat ld_rowstat(const RowStat* p) {
+  RowStat r;
+  r.Z = __ldcg(&p->Z);
+  r.mc = __ldcg(&p->mc);
+  r.err = __ldcg(&p->err);
+  r.amax = __ldcg(&p->amax);
+  r.pad[0] = r.pad[1] = r.pad[2] = 0;
+  return r;
 }
 
-// ------------------------------------------------------------------ chunk reductions ----
-// Online-softmax partial: s (and sx) are sums of 2^(l c - RN(m c)) over the elements seen.
+// ------------------------------------------------------------------- online softmax ----
+// Softmax partial: s is the sum of 2^(l c - RN(m c)) over the elements seen.
 struct Soft {
-  float m, s, sx;
+  float m, s;
 };
 // 2^(RN(m c) - RN(M c)): rescales a partial taken at maximum m to maximum M (0 when empty).
 __device__ __forceinline__ float rescale(float m, float M, float c) {
@@ -121,79 +158,8 @@ __device__ __forceinline__ Soft soft_merge(const Soft& a, const Soft& b, float c
   Soft r;
   r.m = M;
   r.s = __fmaf_rn(a.s, fa, __fmul_rn(b.s, fb));
-  r.sx = __fmaf_rn(a.sx, fa, __fmul_rn(b.sx, fb));
   return r;
 }
-
-// This thread's softmax partial over its vectors of a staged chunk; sx leaves out slot (vx, jx).
-template <typename T>
-__device__ __forceinline__ Soft thread_softmax(const unsigned char* buf, int nvec, float c, int vx, int jx) {
-  constexpr int VE = Elem<T>::kPerVec;
-  Soft t;
-  t.m = thread_max<T>(buf, nvec);
-  t.s = t.sx = 0.f;
-  if (!(t.m > -INFINITY && t.m < INFINITY)) return t;  // empty, +inf or NaN: the max tells
-  const float mc = __fmul_rn(t.m, c);
-  for (int v = (int)threadIdx.x; v < nvec; v += kThreads) {
-    float f[VE];
-    Elem<T>::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)v * 16), f);
-    float e[VE];
-#pragma unroll
-    for (int j = 0; j < VE; ++j) e[j] = ex2(__fmaf_rn(f[j], c, -mc));
-    float vs = 0.f;
-#pragma unroll
-    for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, e[j]);
-    t.s = __fadd_rn(t.s, vs);
-    if (v == vx) {
-      float vsx = 0.f;
-#pragma unroll
-      for (int j = 0; j < VE; ++j) vsx = __fadd_rn(vsx, j == jx ? 0.f : e[j]);
-      t.sx = __fadd_rn(t.sx, vsx);
-    } else {
-      t.sx = __fadd_rn(t.sx, vs);
-    }
-  }
-  return t;
-}
-
-// Softmax statistics of a staged chunk, merged thread -> warp (shuffles) -> block (thread 0).
-// One block barrier.  The result is valid in thread 0 only.
-template <typename T>
-__device__ __forceinline__ ChunkStat chunk_softmax_stats(const unsigned char* buf, const Geo& g, float c, int vx,
-                                                         int jx, float* red /*3*kWarps*/) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  Soft t = thread_softmax<T>(buf, g.nvec, c, vx, jx);
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    Soft u;
-    u.m = __shfl_xor_sync(kFull, t.m, o);
-    u.s = __shfl_xor_sync(kFull, t.s, o);
-    u.sx = __shfl_xor_sync(kFull, t.sx, o);
-    t = soft_merge(t, u, c);
-  }
-  if (lane == 0) {
-    red[warp] = t.m;
-    red[kWarps + warp] = t.s;
-    red[2 * kWarps + warp] = t.sx;
-  }
-  __syncthreads();
-  ChunkStat q;
-  q.a = red[0];
-  q.s = red[kWarps];
-  q.sx = red[2 * kWarps];
-  q.i = 0;
-  if (threadIdx.x == 0) {
-    Soft acc{red[0], red[kWarps], red[2 * kWarps]};
-    for (int w = 1; w < kWarps; ++w) acc = soft_merge(acc, Soft{red[w], red[kWarps + w], red[2 * kWarps + w]}, c);
-    q.a = acc.m;
-    q.s = acc.s;
-    q.sx = acc.sx;
-    q.i = (isnan(acc.m) || acc.m == INFINITY) ? SPEC_ERRF_NONFINITE : 0;
-    if (q.i) q.s = q.sx = 0.f;
-  }
-  return q;
-}
-
 // (max, first index) partials: index -1 marks a NaN, INT_MAX an empty partial.
 __device__ __forceinline__ void argmax_merge(float& v, int& i, float v2, int i2) {
   if (i < 0 || i2 == INT_MAX) return;
@@ -203,187 +169,760 @@ __device__ __forceinline__ void argmax_merge(float& v, int& i, float v2, int i2)
   }
 }
 
-// (max, first index) of a staged chunk; index -1 when it holds a NaN.  One block barrier; the
-// result is valid in thread 0 only.
-template <typename T>
-__device__ __forceinline__ ChunkStat chunk_argmax(const unsigned char* buf, const Geo& g, float* red, int* redi) {
-  constexpr int VE = Elem<T>::kPerVec;
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  float v = thread_max<T>(buf, g.nvec);
-  int idx = INT_MAX;
-  if (isnan(v)) {
-    idx = -1;
-  } else {  // this thread's first element equal to its maximum (its vectors are in index order)
-    for (int vv = (int)threadIdx.x; vv < g.nvec && idx == INT_MAX; vv += kThreads) {
-      float f[VE];
-      Elem<T>::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)vv * 16), f);
-#pragma unroll
-      for (int j = 0; j < VE; ++j) {
-        const int e = g.e0 - g.slot0 + vv * VE + j;
-        if (idx == INT_MAX && e >= g.e0 && e < g.e0 + g.n && f[j] == v) idx = e;
-      }
+// ---------------------------------------------------------------- shared-memory state ----
+struct StageMeta {
+  int kind;        // ItemKind
+  int b, row, ch;  // request; stats: row and chunk; residual: position row k and residual chunk
+  int kk;          // residual: position slot of the counts (k with per-position outputs, else 0)
+  int nvec;        // vectors to reduce (stats: the chunk; residual: the target range)
+  int e_base;      // element index of the first element of slot 0 (target range)
+  int e_lo, e_hi;  // residual: elements [e_lo, e_hi)
+  int dshift;      // residual: draft position = kDraftSlot * VE + (e - e_base) + dshift
+  float mct, mcd, rho;
+};
+struct SlotMeta {
+  int kind;        // ItemKind
+  unsigned* tick;  // the count this chunk adds to (stats and residual items)
+};
+constexpr int kFinCs = 512;   // chunk statistics of one request staged for its finishing
+constexpr int kFinRows = 64;  // row statistics kept in shared memory for finishing
+struct Shared {
+  uint64_t full[kStages], empty[kStages], pfull[kSlots], pempty[kSlots], fin_bar;
+  StageMeta meta[kStages];
+  float4 part[kSlots][kGroupWarps];  // warp partials
+  SlotMeta pmeta[kSlots];
+  int pcnt[kSlots];  // warps of the group that have left their partial
+  int abort, last;
+  double alpha[SPEC_MAX_K];
+  ChunkStat fin_cs[kFinCs];
+  RowStat fin_rs[kFinRows];
+  int fin_par[kFinRows], fin_tok[kFinRows];  // a small tree's parents and tokens
+};
+
+__device__ __forceinline__ void raise_abort(const Params& P, Shared& sm) {
+  *reinterpret_cast<volatile int*>(&sm.abort) = 1;
+  atomicOr(P.gerr, 1u);
+}
+__device__ __forceinline__ bool aborted(const Shared& sm) {
+  return *reinterpret_cast<const volatile int*>(&sm.abort) != 0;
+}
+
+// -------------------------------------------------------------------- item decoding ----
+// Item order: stats items of requests 0 .. lag-1; then, per group g, the stats items of request
+// lag + g followed by the residual items of request g; then the residual items of the last lag
+// requests.  Without a residual pass: the stats items of every request in order.
+__device__ __forceinline__ int decode_item(const Params& P, unsigned w, int& b, int& off) {
+  if (w >= P.total) return kItemEnd;
+  const unsigned A = P.fd_A.d;
+  if (P.npos == 0) {
+    b = (int)fdiv(w, P.fd_A);
+    off = (int)(w - (unsigned)b * A);
+    return kItemStats;
+  }
+  const unsigned Rr = P.fd_R.d;
+  const unsigned L = (unsigned)P.lag;
+  const unsigned head = L * A;
+  if (w < head) {
+    b = (int)fdiv(w, P.fd_A);
+    off = (int)(w - (unsigned)b * A);
+    return kItemStats;
+  }
+  const unsigned w2 = w - head;
+  const unsigned g = fdiv(w2, P.fd_AR);
+  if (g < (unsigned)P.B - L) {
+    const unsigned o = w2 - g * (A + Rr);
+    if (o < A) {
+      b = (int)(L + g);
+      off = (int)o;
+      return kItemStats;
     }
+    b = (int)g;
+    off = (int)(o - A);
+    return kItemResid;
   }
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
-    const float v2 = __shfl_xor_sync(kFull, v, o);
-    const int i2 = __shfl_xor_sync(kFull, idx, o);
-    argmax_merge(v, idx, v2, i2);
+  const unsigned w3 = w2 - ((unsigned)P.B - L) * (A + Rr);
+  const unsigned q = fdiv(w3, P.fd_R);
+  b = (int)((unsigned)P.B - L + q);
+  off = (int)(w3 - q * Rr);
+  return kItemResid;
+}
+
+// Geometry of the target grid vectors [vt0, vt0 + span) of the pair at position k (a residual
+// item, or one sub-range of it), with the draft vectors covering the same elements.
+template <typename T>
+struct ResGeo {
+  RowGrid<T> gt, gd;
+  int vt0, vt1, vd0, vd1;
+  int e_base, e_lo, e_hi, dshift;
+};
+template <typename T>
+__device__ __forceinline__ ResGeo<T> res_geo(const Params& P, int b, int k, int vt0, int span) {
+  constexpr int VE = Elem<T>::kPerVec;
+  ResGeo<T> q;
+  q.gt = row_grid<T>(row_ptr<T>(P, b, k), P.V);
+  q.gd = row_grid<T>(row_ptr<T>(P, b, P.R + k), P.V);
+  q.vt0 = vt0;
+  q.vt1 = min(vt0 + span, q.gt.nvec);
+  q.e_base = q.vt0 * VE - q.gt.phase;
+  q.e_lo = max(0, q.e_base);
+  q.e_hi = min(P.V, q.e_base + span * VE);
+  if (q.vt1 > q.vt0) {
+    q.vd0 = (q.e_lo + q.gd.phase) / VE;
+    q.vd1 = (q.e_hi - 1 + q.gd.phase) / VE + 1;
+  } else {
+    q.vd0 = q.vd1 = 0;
   }
-  if (lane == 0) {
-    red[warp] = v;
-    redi[warp] = idx;
-  }
-  __syncthreads();
-  ChunkStat q;
-  q.a = red[0];
-  q.i = redi[0];
-  q.s = q.sx = 0.f;
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < kWarps; ++w) argmax_merge(q.a, q.i, red[w], redi[w]);
-    if (q.i == INT_MAX) q.i = -1;  // a chunk always holds at least one element
-  }
+  q.dshift = q.e_base - (q.vd0 * VE - q.gd.phase);
   return q;
 }
 
-// ------------------------------------------------------------------ request finishing ----
-struct FinishSmem {
-  float (*tileW)[kWarps];
-  int* s_int;
-  float* s_flt;
-  double* s_dbl;
-  double* s_alpha;
-  int* s_misc;
-  uint64_t* bar_x;
-  unsigned* xphase;
-};
+// Residual weights max(0, e - q rho) of target vector v of a staged residual range (draft copy
+// from slot dslot), where e = 2^(l_t c - mct) and q = 2^(l_d c - mcd): max(0, p - q) in units of
+// 1 / Z_t.  Elements outside [e_lo, e_hi) weigh 0.
+template <typename T>
+__device__ __forceinline__ void resid_weights(const unsigned char* buf, int dslot, int v, int e_base, int e_lo,
+                                              int e_hi, int dshift, float c, float mct, float mcd, float rho,
+                                              float (&w)[Elem<T>::kPerVec]) {
+  constexpr int VE = Elem<T>::kPerVec, S = Elem<T>::kSize;
+  float f[VE], d[VE];
+  Elem<T>::unpack(lds128(buf + (size_t)v * 16), f);
+  if (dshift % VE == 0) {
+    Elem<T>::unpack(lds128(buf + (size_t)(dslot + v + dshift / VE) * 16), d);
+  } else {
+#pragma unroll
+    for (int j = 0; j < VE; ++j) d[j] = Elem<T>::smem_elem(buf + (size_t)(dslot * VE + v * VE + j + dshift) * S);
+  }
+#pragma unroll
+  for (int j = 0; j < VE; ++j) {
+    const int e = e_base + v * VE + j;
+    const float et = ex2(__fmaf_rn(f[j], c, -mct));
+    const float qd = ex2(__fmaf_rn(d[j], c, -mcd));
+    const bool in = (unsigned)(e - e_lo) < (unsigned)(e_hi - e_lo);
+    w[j] = in ? fmaxf(0.f, __fmaf_rn(-qd, rho, et)) : 0.f;
+  }
+}
 
-// Warp-wide inverse CDF over per-chunk weights W(c) (double), in chunk order: the first chunk
-// with positive weight whose running total exceeds u * S, else the last positive one.  Every
-// lane gets the chunk, the total weight before it and S.
-template <typename WF>
-__device__ __forceinline__ void chunk_select(int nchunk, double u, WF W, int& cstar, double& bstar, double& S) {
+// ------------------------------------------------------------------------ producer ----
+// Producer of group grp: items it = grp, grp + kGroups, ... of this CTA's sequence (stage
+// it % kStages).  It publishes one end marker when its claims run out.
+template <int MODE, typename T>
+__device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages, int grp) {
+  constexpr int VE = Elem<T>::kPerVec;
   const int lane = threadIdx.x & 31;
-  double part = 0.0;
-  for (int c = lane; c < nchunk; c += 32) part += W(c);
-  S = warp_sum_d(part);
-  const double tgt = u * S;
-  double base = 0.0, blast = 0.0;
+  // claims: kClaim consecutive items per atomic, the next batch claimed one batch ahead
+  unsigned cur = 0, nxt = 0;
+  int pos = 0;
+  if (lane == 0) {
+    cur = atomicAdd(P.work, (unsigned)kClaim);
+    nxt = atomicAdd(P.work, (unsigned)kClaim);
+  }
+  int it = grp;
+  // residual parameters of the last request seen (consecutive residual items share them)
+  int rb = -1, rk = 0, rerr = 1;
+  float rmct = 0.f, rmcd = 0.f, rrho = 0.f;
+  for (;; it += kGroups) {
+    const int s = it % kStages;
+    if (!mbar_wait(&sm.empty[s], ((uint32_t)(it / kStages) & 1u) ^ 1u, &sm.abort)) {
+      if (lane == 0) raise_abort(P, sm);
+      break;
+    }
+    const unsigned w = __shfl_sync(kFull, cur + (unsigned)pos, 0);
+    if (++pos == kClaim) {
+      pos = 0;
+      if (lane == 0) {
+        cur = nxt;
+        if (cur < P.total) nxt = atomicAdd(P.work, (unsigned)kClaim);
+      }
+    }
+    unsigned char* buf = stages + (size_t)s * kStageBytes;
+    StageMeta m;
+    m.b = m.row = m.ch = m.kk = 0;
+    m.nvec = 0;
+    m.e_base = 0;
+    m.e_lo = m.e_hi = m.dshift = 0;
+    m.mct = m.mcd = m.rho = 0.f;
+    int off = 0;
+    m.kind = decode_item(P, w, m.b, off);
+    if (m.kind == kItemStats) {
+      m.row = (int)fdiv((unsigned)off, P.fd_nchunk);
+      m.ch = off - m.row * P.nchunk;
+      const RowGrid<T> g = row_grid<T>(row_ptr<T>(P, m.b, m.row), P.V);
+      const int v0 = m.ch * kChunkVec, v1 = min(v0 + kChunkVec, g.nvec);
+      m.nvec = max(0, v1 - v0);
+      m.e_base = v0 * VE - g.phase;
+      warp_stage<T>(buf, g, P.V, v0, v1, &sm.full[s], lane);
+    } else if (m.kind == kItemResid) {
+      m.kk = (int)fdiv((unsigned)off, P.fd_nchunk_r);
+      m.ch = off - m.kk * P.nchunk_r;
+      if (m.b != rb || P.diag) {
+        // the request's acceptance result (published by the finishing warp of its owner CTA)
+        int ready = 0;
+        if (lane == 0) {
+          const long long t0 = clock64();
+          for (;;) {
+            ready = ld_volatile(&P.req[m.b].ready);
+            if (ready || aborted(sm)) break;
+            if (clock64() - t0 > kWaitLimitCycles) {
+              raise_abort(P, sm);
+              break;
+            }
+            __nanosleep(128);
+          }
+          __threadfence();
+        }
+        ready = __shfl_sync(kFull, ready, 0);
+        rb = m.b;
+        rerr = 1;
+        if (ready) {
+          const int n = __ldcg(&P.req[m.b].n);
+          rerr = __ldcg(&P.req[m.b].err);
+          rk = P.diag ? m.kk : n;
+          if (!rerr && rk < P.K) {
+            const RowStat ts = ld_rowstat(P.rstat + (size_t)m.b * P.rows + rk);
+            const RowStat ds = ld_rowstat(P.rstat + (size_t)m.b * P.rows + P.R + rk);
+            rmct = ts.mc;
+            rmcd = ds.mc;
+            rrho = __fdiv_rn((float)ts.Z, (float)ds.Z);  // max(0, p - q) Z_t = max(0, e - f Z_t / Z_d)
+          }
+        }
+      }
+      m.kind = kItemSkip;
+      if (!rerr && rk < P.K) {
+        m.kind = kItemResid;
+        m.row = rk;
+        m.mct = rmct;
+        m.mcd = rmcd;
+        m.rho = rrho;
+        const ResGeo<T> q = res_geo<T>(P, m.b, rk, m.ch * kResVec, kResVec);
+        m.nvec = max(0, q.vt1 - q.vt0);
+        m.e_base = q.e_base;
+        m.e_lo = q.e_lo;
+        m.e_hi = q.e_hi;
+        m.dshift = q.dshift;
+        if (m.nvec > 0) {
+          warp_stage<T>(buf, q.gt, P.V, q.vt0, q.vt1, &sm.full[s], lane);
+          warp_stage<T>(buf + (size_t)kDraftSlot * 16, q.gd, P.V, q.vd0, q.vd1, &sm.full[s], lane);
+        }
+      }
+    }
+    if (lane == 0) sm.meta[s] = m;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.full[s]);
+    if (m.kind == kItemEnd) {
+      it += kGroups;
+      break;
+    }
+  }
+  // Never leave with a copy in flight: wait (bounded, ignoring the abort flag) for the stages
+  // this producer filled last.
+  const int zero = 0;
+  for (int j = it - kStages; j < it; j += kGroups)
+    if (j >= 0) mbar_wait(&sm.full[j % kStages], (uint32_t)(j / kStages) & 1u, &zero);
+}
+
+// ------------------------------------------------------------------------ consumers ----
+// Warp gw of a group reduces vectors [gw * kSubVec, (gw + 1) * kSubVec) of a staged chunk; lane l
+// takes vectors gw * kSubVec + l + 32 i.
+template <int MODE, typename T>
+__device__ __forceinline__ float4 consume_stats(const unsigned char* buf, const StageMeta& m, float c, int gw) {
+  using E = Elem<T>;
+  constexpr int VE = E::kPerVec;
+  constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
+  const int lane = threadIdx.x & 31;
+  const int vbase = gw * kSubVec + lane;
+  uint4 vv[kVecPerLane];
+#pragma unroll
+  for (int i = 0; i < kVecPerLane; ++i) {
+    const int v = vbase + 32 * i;
+    vv[i] = v < m.nvec ? lds128(buf + (size_t)v * 16) : make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+  }
+  if constexpr (kSoftmax) {
+    uint32_t m0 = E::kNegInfWord, m1 = E::kNegInfWord;
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+      m0 = E::max_word(m0, E::max_word(vv[i].x, vv[i].y));
+      m1 = E::max_word(m1, E::max_word(vv[i].z, vv[i].w));
+    }
+    const float M = warp_max_nan(E::word_max(E::max_word(m0, m1)));
+    if (!(M > -INFINITY && M < INFINITY)) return make_float4(M, 0.f, 0.f, 0.f);  // empty, NaN or +inf
+    const float mc = __fmul_rn(M, c);
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i) {
+      float f[VE];
+      E::unpack(vv[i], f);
+      float vs = 0.f;
+#pragma unroll
+      for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, ex2(__fmaf_rn(f[j], c, -mc)));
+      s = __fadd_rn(s, vs);
+    }
+    return make_float4(M, warp_sum(s), 0.f, 0.f);
+  } else {
+    // per-vector maxima; a lane holding the warp maximum finds its first vector holding it, then
+    // the first element of that vector (its vectors are in index order)
+    float vmax[kVecPerLane];
+#pragma unroll
+    for (int i = 0; i < kVecPerLane; ++i)
+      vmax[i] = E::word_max(E::max_word(E::max_word(vv[i].x, vv[i].y), E::max_word(vv[i].z, vv[i].w)));
+    float mt = vmax[0];
+#pragma unroll
+    for (int i = 1; i < kVecPerLane; ++i) mt = fmax_nan(mt, vmax[i]);
+    const float M = warp_max_nan(mt);
+    int idx = INT_MAX;
+    if (isnan(M)) {
+      idx = -1;
+    } else if (M == -INFINITY) {
+      // nothing but -inf: the first row element this lane holds (every staged vector holds one)
+      if (vbase < m.nvec) idx = max(m.e_base + vbase * VE, 0);
+    } else if (mt == M) {
+      uint4 sel = vv[0];
+      int vi = 0;
+#pragma unroll
+      for (int i = kVecPerLane - 1; i >= 0; --i) {
+        if (vmax[i] == M) {
+          sel = vv[i];
+          vi = i;
+        }
+      }
+      float f[VE];
+      E::unpack(sel, f);
+      int jj = VE - 1;
+#pragma unroll
+      for (int j = VE - 1; j >= 0; --j)
+        if (f[j] == M) jj = j;
+      idx = m.e_base + (vbase + 32 * vi) * VE + jj;
+    }
+    idx = warp_min_i(idx);
+    return make_float4(M, __int_as_float(idx), 0.f, 0.f);
+  }
+}
+
+// Residual item: warp gw sums the weights of target vectors [gw * kResSub, (gw + 1) * kResSub).
+template <typename T>
+__device__ __forceinline__ float4 consume_resid(const unsigned char* buf, const StageMeta& m, float c, int gw) {
+  constexpr int VE = Elem<T>::kPerVec;
+  const int lane = threadIdx.x & 31;
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kResSub / 32; ++i) {
+    const int v = gw * kResSub + lane + 32 * i;
+    if (v < m.nvec) {
+      float w[VE];
+      resid_weights<T>(buf, kDraftSlot, v, m.e_base, m.e_lo, m.e_hi, m.dshift, c, m.mct, m.mcd, m.rho, w);
+      float vs = 0.f;
+#pragma unroll
+      for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, w[j]);
+      s = __fadd_rn(s, vs);
+    }
+  }
+  return make_float4(warp_sum(s), 0.f, 0.f, 0.f);
+}
+
+// The group's last warp to leave its partial in slot j merges the partials, writes the chunk's
+// statistics (stats items: the chunk and its sub-chunks; residual items: the sum and the sub-range
+// sums) and hands the slot to the bookkeeping warp.
+template <int MODE>
+__device__ __forceinline__ void publish_chunk(const Params& P, Shared& sm, const StageMeta& m, int j) {
+  constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
+  const int lane = threadIdx.x & 31;
+  const bool mine = lane < kGroupWarps;
+  const float4 pw = sm.part[j][lane % kGroupWarps];
+  const float c = P.c;
+  SlotMeta pm;
+  pm.kind = m.kind;
+  pm.tick = nullptr;
+  if (m.kind == kItemStats) {
+    const size_t ci = ((size_t)m.b * P.rows + m.row) * P.nchunk + m.ch;
+    float4 q;
+    // lanes 0..kGroupWarps-1 hold the warp partials; xor-shuffles within those lanes merge them
+    if constexpr (kSoftmax) {
+      float M = mine ? pw.x : -INFINITY;
+#pragma unroll
+      for (int o = 1; o < kGroupWarps; o <<= 1) M = fmax_nan(M, __shfl_xor_sync(kFull, M, o));
+      const int fl = (isnan(M) || M == INFINITY) ? SPEC_ERRF_NONFINITE : 0;
+      float sv = (mine && !fl && M != -INFINITY) ? __fmul_rn(pw.y, rescale(pw.x, M, c)) : 0.f;
+#pragma unroll
+      for (int o = 1; o < kGroupWarps; o <<= 1) sv = __fadd_rn(sv, __shfl_xor_sync(kFull, sv, o));
+      q = make_float4(M, sv, 0.f, __int_as_float(fl));
+      if (mine)  // the sub-chunk partials, for the draws
+        *reinterpret_cast<float4*>(P.sstat + ci * kGroupWarps + lane) = make_float4(pw.x, pw.y, 0.f, 0.f);
+    } else {
+      float v = mine ? pw.x : -INFINITY;
+      int i = mine ? __float_as_int(pw.y) : INT_MAX;
+#pragma unroll
+      for (int o = 1; o < kGroupWarps; o <<= 1)
+        argmax_merge(v, i, __shfl_xor_sync(kFull, v, o), __shfl_xor_sync(kFull, i, o));
+      q = make_float4(v, 0.f, 0.f, __int_as_float(i));
+    }
+    if (lane == 0) *reinterpret_cast<float4*>(P.cstat + ci) = q;
+    pm.tick = P.tick_a + m.b;
+  } else if (m.kind == kItemResid) {
+    float sum = mine ? pw.x : 0.f;
+#pragma unroll
+    for (int o = 1; o < kGroupWarps; o <<= 1) sum = __fadd_rn(sum, __shfl_xor_sync(kFull, sum, o));
+    const size_t bk = (size_t)m.b * P.npos + m.kk;
+    const size_t ri = bk * P.nchunk_r + m.ch;
+    if (lane == 0) P.wsum[ri] = sum;
+    if (mine) P.wsub[ri * kGroupWarps + lane] = pw.x;
+    pm.tick = P.tick_b + bk;
+  }
+  __syncwarp();
+  if (lane == 0) {
+    sm.pmeta[j] = pm;
+    sm.pcnt[j] = 0;
+    mbar_arrive(&sm.pfull[j]);
+  }
+}
+
+// Group g takes items g, g + 2, g + 4, ... (stage it % kStages, slot it % kSlots).
+template <int MODE, typename T>
+__device__ void consumer_loop(const Params& P, Shared& sm, const unsigned char* stages) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int grp = warp / kGroupWarps, gw = warp % kGroupWarps;
+  for (int it = grp;; it += kGroups) {
+    const int s = it % kStages;
+    if (!mbar_wait(&sm.full[s], (uint32_t)(it / kStages) & 1u, &sm.abort)) {
+      if (lane == 0) raise_abort(P, sm);
+      return;
+    }
+    const StageMeta m = sm.meta[s];
+    const unsigned char* buf = stages + (size_t)s * kStageBytes;
+    float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (m.kind == kItemStats)
+      part = consume_stats<MODE, T>(buf, m, P.c, gw);
+    else if (m.kind == kItemResid)
+      part = consume_resid<T>(buf, m, P.c, gw);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.empty[s]);
+    const int j = it % kSlots;
+    if (!mbar_wait(&sm.pempty[j], ((uint32_t)(it / kSlots) & 1u) ^ 1u, &sm.abort)) {
+      if (lane == 0) raise_abort(P, sm);
+      return;
+    }
+    int last = 0;
+    if (lane == 0) {
+      sm.part[j][gw] = part;
+      __threadfence_block();
+      last = atomicAdd(&sm.pcnt[j], 1) == kGroupWarps - 1;
+      __threadfence_block();
+    }
+    if (__shfl_sync(kFull, last, 0)) publish_chunk<MODE>(P, sm, m, j);
+    if (m.kind == kItemEnd) return;
+  }
+}
+
+// ----------------------------------------------------------------------- bookkeeper ----
+template <int MODE>
+__device__ void book_loop(const Params& P, Shared& sm) {
+  const int lane = threadIdx.x & 31;
+  // The two groups' item sequences (it = g, g + 2, ...) are each taken in order; the warp takes
+  // whichever group's next chunk is ready (never blocking on one group: a group's producer may be
+  // waiting for a result that depends on a chunk of the other group).  A group that has published
+  // its end marker is passed over.
+  static_assert(kGroups == 2, "two consumer groups");
+  int nxt0 = 0, nxt1 = 1, g = 0;
+  bool ended0 = false, ended1 = false;
+  long long t_idle = clock64();
+  while (!(ended0 && ended1)) {
+    int nb = 0;
+    unsigned* tick = nullptr;  // lane i: the count of the i-th chunk of this batch
+    while (nb < kSlots && !(ended0 && ended1)) {  // the chunks ready now
+      int pick = -1;
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        const int gg = g ^ t;
+        if (gg == 0 ? ended0 : ended1) continue;
+        const int itg = gg == 0 ? nxt0 : nxt1;
+        if (mbar_test_wait(&sm.pfull[itg % kSlots], (uint32_t)(itg / kSlots) & 1u)) {
+          pick = gg;
+          break;
+        }
+      }
+      pick = __shfl_sync(kFull, pick, 0);
+      if (pick < 0) {
+        if (nb > 0) break;  // publish what this batch holds
+        if (aborted(sm) || clock64() - t_idle > kWaitLimitCycles) {
+          if (lane == 0) raise_abort(P, sm);
+          ended0 = ended1 = true;
+          break;
+        }
+        __nanosleep(32);
+        continue;
+      }
+      t_idle = clock64();
+      g = pick;
+      const int it = g == 0 ? nxt0 : nxt1;
+      const int j = it % kSlots;
+      const SlotMeta pm = sm.pmeta[j];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.pempty[j]);
+      if (g == 0)
+        nxt0 += kGroups;
+      else
+        nxt1 += kGroups;
+      const int gdone = g;
+      g ^= 1;
+      if (pm.kind == kItemEnd) {
+        if (gdone == 0)
+          ended0 = true;
+        else
+          ended1 = true;
+        continue;
+      }
+      if (pm.kind == kItemSkip) continue;
+      unsigned* tk = pm.tick;
+      if (lane == nb) tick = tk;
+      ++nb;
+    }
+    if (nb > 0) {
+      __threadfence();                      // this batch's statistics before its counts
+      if (lane < nb) atomicAdd(tick, 1u);  // result unused: a fire-and-forget reduction
+    }
+  }
+}
+
+// ------------------------------------------------------------------------ finishing ----
+// Warp-wide inverse CDF over part weights W(c) (fp32), in order: the first part with positive
+// weight whose running total exceeds tgt, else the last positive one.  Every lane gets the part
+// and the total weight before it.
+template <typename WF>
+__device__ __forceinline__ void select_part(int nparts, float tgt, WF W, int& cstar, float& bstar) {
+  const int lane = threadIdx.x & 31;
+  float base = 0.f, blast = 0.f;
   int clast = -1;
   cstar = -1;
-  bstar = 0.0;
-  for (int c0 = 0; c0 < nchunk; c0 += 32) {
+  bstar = 0.f;
+  for (int c0 = 0; c0 < nparts; c0 += 32) {
     const int cc = c0 + lane;
-    const double w = cc < nchunk ? W(cc) : 0.0;
-    const double incl = warp_incl_scan_d(w, lane);
-    double ex = __shfl_up_sync(kFull, incl, 1);
-    if (lane == 0) ex = 0.0;
-    const unsigned hit = __ballot_sync(kFull, w > 0.0 && base + incl > tgt);
-    const unsigned pos = __ballot_sync(kFull, w > 0.0);
-    if (cstar < 0 && hit) {
+    const float w = cc < nparts ? W(cc) : 0.f;
+    const float incl = warp_incl_scan(w, lane);
+    float ex = __shfl_up_sync(kFull, incl, 1);
+    if (lane == 0) ex = 0.f;
+    const unsigned hit = __ballot_sync(kFull, w > 0.f && __fadd_rn(base, incl) > tgt);
+    const unsigned pos = __ballot_sync(kFull, w > 0.f);
+    if (hit) {
       const int L = __ffs(hit) - 1;
       cstar = c0 + L;
-      bstar = base + __shfl_sync(kFull, ex, L);
+      bstar = __fadd_rn(base, __shfl_sync(kFull, ex, L));
+      return;
     }
     if (pos) {
       const int L = 31 - __clz(pos);
       clast = c0 + L;
-      blast = base + __shfl_sync(kFull, ex, L);
+      blast = __fadd_rn(base, __shfl_sync(kFull, ex, L));
     }
-    base += __shfl_sync(kFull, incl, 31);
+    base = __fadd_rn(base, __shfl_sync(kFull, incl, 31));
   }
-  if (cstar < 0) {
-    cstar = clast;
-    bstar = blast;
-  }
+  cstar = clast;
+  bstar = blast;
+}
+template <typename WF>
+__device__ __forceinline__ float total_weight(int nparts, WF W) {
+  const int lane = threadIdx.x & 31;
+  float part = 0.f;
+  for (int c = lane; c < nparts; c += 32) part = __fadd_rn(part, W(c));
+  return warp_sum(part);
 }
 
-// Inverse-CDF draw for target row `row` of request b from its chunk statistics: weights p
-// (kFullP) or p without token x (kExcl).  Finds the crossing chunk from the chunk weights, then
-// stages that one chunk (into `buf`) and searches it.  Block-wide; every thread gets the token
-// and the residual mass S / Z (taken before any zero-residual fallback).
-template <typename T>
-__device__ int draw_from_chunks(const Params& P, int b, int row, int kind, int x, unsigned char* buf,
-                                const FinishSmem& F, float* mass_out) {
-  constexpr int VE = Elem<T>::kPerVec;
-  const RowStat rs = P.rstat[(size_t)b * P.rows + row];
-  const ChunkStat* cs = P.cstat + ((size_t)b * P.rows + row) * P.nchunk;
-  if (threadIdx.x < 32) {
-    const double u = (double)__ldg(P.u + b);
-    int cstar, k2 = kind;
-    double bstar, S;
-    auto weight = [&](int c) {
-      return chunk_weight(__ldcg(&cs[c].a), k2 == kExcl ? __ldcg(&cs[c].sx) : __ldcg(&cs[c].s), P.c, rs.mc);
-    };
-    chunk_select(P.nchunk, u, weight, cstar, bstar, S);
-    const double S0 = S;
-    if (!(S > 0.0)) {  // no residual mass: draw from p
-      k2 = kFullP;
-      chunk_select(P.nchunk, u, weight, cstar, bstar, S);
-    }
-    if (threadIdx.x == 0) {
-      F.s_misc[0] = cstar;
-      F.s_misc[1] = k2;
-      F.s_dbl[0] = u * S - bstar;
-      F.s_dbl[1] = S0 / rs.Z;
-    }
+// Waits for the finishing buffer's copy (bounded; the wait ignores the abort flag so that no
+// copy is left in flight).  Returns false on a timeout.
+__device__ __forceinline__ bool fin_wait(const Params& P, Shared& sm, uint32_t& fph) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  if (lane == 0) mbar_arrive(&sm.fin_bar);
+  const int zero = 0;
+  bool ok = mbar_wait(&sm.fin_bar, fph & 1u, &zero);
+  if (!ok) {
+    if (lane == 0) raise_abort(P, sm);
+    mbar_wait(&sm.fin_bar, fph & 1u, &zero);
   }
-  __syncthreads();
-  const int cstar = F.s_misc[0], k2 = F.s_misc[1];
-  const float t = (float)F.s_dbl[0];
-  *mass_out = (float)F.s_dbl[1];
-  if (cstar < 0) return -1;
-  const char* rp = row_ptr<T>(P, b, row);
-  const Geo g = make_geo<T>(rp, cstar * P.chunk, chunk_len(P, cstar));
-  issue_chunk<T>(buf, rp, g, F.bar_x, l2_policy_evict_first());
-  bool ok = mbar_wait_bounded(F.bar_x, *F.xphase & 1u);
-  if (!ok) ok = mbar_wait_bounded(F.bar_x, *F.xphase & 1u);
-  __syncthreads();
-  if (threadIdx.x == 0) ++*F.xphase;
+  ++fph;
+  return ok;
+}
+
+// Chunk statistics of request b as the finishing warp reads them: from the shared-memory copy
+// when the request's block fits there, else from global memory.
+struct CsReader {
+  const ChunkStat* g;
+  const ChunkStat* s;
+  int nchunk;
+  __device__ __forceinline__ ChunkStat operator()(int r, int c) const {
+    if (s) return s[r * nchunk + c];
+    return ld_chunkstat(g + (size_t)r * nchunk + c);
+  }
+};
+// Copies the chunk statistics of request b into shared memory when they fit (one round trip).
+__device__ __forceinline__ CsReader stage_request_stats(const Params& P, ChunkStat* dst, int b, bool allow) {
+  const int lane = threadIdx.x & 31;
+  const int n = P.rows * P.nchunk;
+  CsReader rd;
+  rd.g = P.cstat + (size_t)b * n;
+  rd.nchunk = P.nchunk;
+  rd.s = nullptr;
+  if (allow && n <= kFinCs) {
+    constexpr int U = 8;
+    for (int i0 = 0; i0 < n; i0 += 32 * U) {
+      ChunkStat tmp[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * 32 + lane;
+        if (i < n) tmp[u] = ld_chunkstat(rd.g + i);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + u * 32 + lane;
+        if (i < n) dst[i] = tmp[u];
+      }
+    }
+    __syncwarp();
+    rd.s = dst;
+  }
+  return rd;
+}
+// Row statistics of request b (shared-memory copy for the first kFinRows rows).
+__device__ __forceinline__ RowStat read_rowstat(const Params& P, const Shared& sm, int b, int r) {
+  if (r < kFinRows) return sm.fin_rs[r];
+  return ld_rowstat(P.rstat + (size_t)b * P.rows + r);
+}
+
+// Inverse-CDF draw from target row `row` of request b using its chunk statistics: weights p
+// (kFullP) or p without token x (kExcl).  Picks the crossing chunk from the chunk weights, then
+// the crossing sub-chunk from the sub-chunk partials, stages that sub-chunk and searches it.  For
+// kExcl the sub-chunk holding x is staged first and summed without x, so that no weight is ever
+// obtained by subtraction.  Returns the token (every lane) and the residual mass S / Z (taken
+// before any zero-residual fallback).
+template <typename T>
+__device__ int draw_from_chunks(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, int b, int row,
+                                int kind, int x, const CsReader& rd, const RowStat& rs, float* mass_out) {
+  constexpr int VE = Elem<T>::kPerVec;
+  const int lane = threadIdx.x & 31;
+  const double u = (double)__ldg(P.u + b);
   const float c = P.c, mc = rs.mc;
+  const RowGrid<T> g = row_grid<T>(row_ptr<T>(P, b, row), P.V);
+  const ChunkStat* srow = P.sstat + ((size_t)b * P.rows + row) * P.nchunk * kGroupWarps;
+  auto stage_sub = [&](int ch, int sub, int& v0, int& v1) {
+    v0 = ch * kChunkVec + sub * kSubVec;
+    v1 = min(v0 + kSubVec, g.nvec);
+    warp_stage<T>(fbuf, g, P.V, v0, v1, &sm.fin_bar, lane);
+    return fin_wait(P, sm, fph);
+  };
+  bool ok = true;
+  int staged_ch = -1, staged_sub = -1, sv0 = 0, sv1 = 0;
+  // kExcl: the chunk and sub-chunk holding x; lane i < kGroupWarps keeps sub-chunk i's weight in
+  // that chunk, with x left out of sub-chunk ix (summed from the staged sub-chunk, never by
+  // subtraction)
+  int cx = -1, ix = -1;
+  float wsub_x = 0.f, wcx = 0.f;
+  if (kind == kExcl && x >= 0 && x < P.V) {
+    const int pv = (x + g.phase) / VE;
+    cx = pv / kChunkVec;
+    ix = (pv - cx * kChunkVec) / kSubVec;
+    float wl = 0.f;
+    if (lane < kGroupWarps && lane != ix) {
+      const ChunkStat q = ld_chunkstat(srow + (size_t)cx * kGroupWarps + lane);
+      wl = chunk_weight(q.a, q.s, c, mc);
+    }
+    ok = stage_sub(cx, ix, sv0, sv1);
+    staged_ch = cx;
+    staged_sub = ix;
+    const int e_base = sv0 * VE - g.phase;
+    float part = 0.f;
+    for (int v = lane; v < sv1 - sv0; v += 32) {
+      float f[VE];
+      Elem<T>::unpack(lds128(fbuf + (size_t)v * 16), f);
+      float vs = 0.f;
+#pragma unroll
+      for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, e_base + v * VE + j == x ? 0.f : ex2(__fmaf_rn(f[j], c, -mc)));
+      part = __fadd_rn(part, vs);
+    }
+    const float wx = warp_sum(part);
+    wsub_x = lane == ix ? wx : wl;
+    float t = lane < kGroupWarps ? wsub_x : 0.f;
+#pragma unroll
+    for (int o = 1; o < kGroupWarps; o <<= 1) t = __fadd_rn(t, __shfl_xor_sync(kFull, t, o));
+    wcx = __shfl_sync(kFull, t, 0);
+  }
+  int k2 = cx >= 0 ? kExcl : kFullP;
+  auto weight = [&](int ch) {
+    if (k2 == kExcl && ch == cx) return wcx;
+    const ChunkStat q = rd(row, ch);
+    return chunk_weight(q.a, q.s, c, mc);
+  };
+  float S = total_weight(P.nchunk, weight);
+  const float S0 = S;
+  if (!(S > 0.f)) {  // no residual mass: draw from p
+    k2 = kFullP;
+    S = total_weight(P.nchunk, weight);
+  }
+  *mass_out = (float)((double)S0 / rs.Z);
+  int cstar;
+  float bstar;
+  const float tgt = __fmul_rn((float)u, S);
+  select_part(P.nchunk, tgt, weight, cstar, bstar);
+  if (cstar < 0) return -1;
+  const bool subx = k2 == kExcl && cstar == cx;
+  const ChunkStat* sp = srow + (size_t)cstar * kGroupWarps;
+  auto sweight = [&](int i) {  // select_part evaluates part i in lane i
+    if (subx) return wsub_x;
+    const ChunkStat q = ld_chunkstat(sp + i);
+    return chunk_weight(q.a, q.s, c, mc);
+  };
+  int sstar;
+  float sbase;
+  select_part(kGroupWarps, __fsub_rn(tgt, bstar), sweight, sstar, sbase);
+  if (sstar < 0) return -1;  // cannot happen: the chunk holds positive weight
+  const float t = __fsub_rn(__fsub_rn(tgt, bstar), sbase);
+  if (cstar != staged_ch || sstar != staged_sub) ok = stage_sub(cstar, sstar, sv0, sv1) && ok;
+  const int e_base = sv0 * VE - g.phase;
   const int xe = (k2 == kExcl) ? x : -1;
   auto wf = [&](int v, float (&w)[VE]) {
     float f[VE];
-    Elem<T>::unpack(*reinterpret_cast<const uint4*>(buf + (size_t)v * 16), f);
+    Elem<T>::unpack(lds128(fbuf + (size_t)v * 16), f);
 #pragma unroll
     for (int j = 0; j < VE; ++j) {
       w[j] = ex2(__fmaf_rn(f[j], c, -mc));
-      if (g.e0 - g.slot0 + v * VE + j == xe) w[j] = 0.f;
+      if (e_base + v * VE + j == xe) w[j] = 0.f;
     }
   };
-  const int tok = chunk_crossing<VE>(g, t, wf, F.tileW, F.s_int, F.s_flt);
-  return ok ? tok : -1;
+  const int pos = warp_crossing<VE>(sv1 - sv0, t, wf);
+  __syncwarp();
+  return (ok && pos >= 0) ? e_base + pos : -1;
 }
 
-// Combines the chunk statistics of every row of request b into RowStat (one warp per row).
+// Combines the chunk statistics of every row of request b into RowStat (lanes over rows).
 template <int MODE>
-__device__ void combine_rows(const Params& P, int b) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+__device__ void combine_rows(const Params& P, Shared& sm, int b, const CsReader& rd) {
   constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
-  for (int r = warp; r < P.rows; r += kWarps) {
-    const ChunkStat* cs = P.cstat + ((size_t)b * P.rows + r) * P.nchunk;
+  const int lane = threadIdx.x & 31;
+  for (int r = lane; r < P.rows; r += 32) {
     float m = -INFINITY;
     int fl = 0;
-    for (int c = lane; c < P.nchunk; c += 32) {
-      const float a = __ldcg(&cs[c].a);
-      const int i = __ldcg(&cs[c].i);
-      m = fmax_nan(m, a);
+#pragma unroll 4
+    for (int c = 0; c < P.nchunk; ++c) {
+      const ChunkStat q = rd(r, c);
+      m = fmax_nan(m, q.a);
       if (kSoftmax)
-        fl |= i;
-      else if (i < 0)
+        fl |= q.i;
+      else if (q.i < 0)
         fl |= SPEC_ERRF_NONFINITE;
     }
-    m = warp_max_nan(m);
-    fl = warp_or(fl);
     RowStat rs;
     rs.pad[0] = rs.pad[1] = rs.pad[2] = 0;
     if (kSoftmax) {
       const float mc = __fmul_rn(m, P.c);
       const bool finite_m = !isnan(m) && m != INFINITY && m != -INFINITY;
-      double z = 0.0;
-      if (!fl && finite_m)
-        for (int c = lane; c < P.nchunk; c += 32) z += chunk_weight(__ldcg(&cs[c].a), __ldcg(&cs[c].s), P.c, mc);
-      const double Z = warp_sum_d(z);
+      double Z = 0.0;
+      if (!fl && finite_m) {
+        float zs = 0.f, zc = 0.f;  // compensated (Kahan) sum of the chunk weights
+        for (int c = 0; c < P.nchunk; ++c) {
+          const ChunkStat q = rd(r, c);
+          const float y = __fsub_rn(chunk_weight(q.a, q.s, P.c, mc), zc);
+          const float t = __fadd_rn(zs, y);
+          zc = __fsub_rn(__fsub_rn(t, zs), y);
+          zs = t;
+        }
+        Z = (double)zs - (double)zc;
+      }
       rs.Z = Z;
       rs.mc = mc;
       rs.amax = -1;
@@ -391,128 +930,132 @@ __device__ void combine_rows(const Params& P, int b) {
     } else {
       // lowest index among the chunks whose maximum equals the row maximum
       int idx = INT_MAX;
-      for (int c = lane; c < P.nchunk; c += 32) {
-        const float a = __ldcg(&cs[c].a);
-        const int i = __ldcg(&cs[c].i);
-        if (a == m && i >= 0) idx = min(idx, i);
+      for (int c = 0; c < P.nchunk; ++c) {
+        const ChunkStat q = rd(r, c);
+        if (q.a == m && q.i >= 0) idx = min(idx, q.i);
       }
-      idx = warp_min_i(idx);
       rs.Z = 0.0;
       rs.mc = m;
       rs.amax = (fl || idx == INT_MAX) ? -1 : idx;
       rs.err = fl ? SPEC_ERRF_NONFINITE : 0;
     }
-    if (lane == 0) P.rstat[(size_t)b * P.rows + r] = rs;
+    P.rstat[(size_t)b * P.rows + r] = rs;
+    if (r < kFinRows) sm.fin_rs[r] = rs;
   }
-  __syncthreads();
+  __syncwarp();
+  __threadfence();
 }
 
-// Chain / n-gram finishing: alpha, acceptance scan (section I.1 step 2), outputs, and the draws
-// this CTA makes (bonus row; n-gram residual).  Block-wide.
+// Chain / n-gram / greedy-chain finishing: alpha, acceptance scan (section I.1 step 2), outputs,
+// publication of the acceptance result, and the draws made here (bonus row; n-gram residual).
+// Returns the accepted length (or -1 after an error) in every lane.
 template <int MODE, typename T>
-__device__ void finish_chain(const Params& P, int b, unsigned char* buf, const FinishSmem& F) {
+__device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, int b) {
   constexpr int S = Elem<T>::kSize;
   constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int K = P.K;
-  combine_rows<MODE>(P, b);
-  if (threadIdx.x == 0) F.s_misc[3] = 0;
-  __syncthreads();
-  // acceptance probability of every draft position
-  for (int k = (int)threadIdx.x; k < K; k += kThreads) {
-    const int x = __ldg(P.draft_tokens + (size_t)b * K + k);
+  // prefetch (positions k < 32 in lane k): the draft token and uniform, then the logits at it
+  int x0 = 0;
+  float r0 = 0.f, lx0 = 0.f, dx0 = 0.f;
+  if (lane < K) {
+    x0 = __ldg(P.draft_tokens + (size_t)b * K + lane);
+    if (kSoftmax) r0 = __ldg(P.r + (size_t)b * K + lane);
+  }
+  const CsReader rd = stage_request_stats(P, sm.fin_cs, b, true);
+  if (kSoftmax && lane < K && x0 >= 0 && x0 < P.V) {
+    lx0 = Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, lane) + (size_t)x0 * S));
+    if (MODE == kChain) dx0 = Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, P.R + lane) + (size_t)x0 * S));
+  }
+  combine_rows<MODE>(P, sm, b, rd);
+  int e = 0;
+  for (int k = lane; k < K; k += 32) {
+    const int x = k < 32 ? x0 : __ldg(P.draft_tokens + (size_t)b * K + k);
     double alpha = 0.0;
-    int e = 0;
     if (x < 0 || x >= P.V) {
-      e = SPEC_ERRF_BAD_TOKEN;
+      e |= SPEC_ERRF_BAD_TOKEN;
     } else {
-      const RowStat t = P.rstat[(size_t)b * P.rows + k];
+      const RowStat t = read_rowstat(P, sm, b, k);
       if (kSoftmax) {
-        const float lx = Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, k) + (size_t)x * S));
+        const float lx = k < 32 ? lx0 : Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, k) + (size_t)x * S));
         const double ext = (double)lx * (double)P.c - (double)t.mc;
         if (MODE == kChain) {
-          const RowStat d = P.rstat[(size_t)b * P.rows + P.R + k];
-          const float dx = Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, P.R + k) + (size_t)x * S));
+          const RowStat d = read_rowstat(P, sm, b, P.R + k);
+          const float dx =
+              k < 32 ? dx0 : Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, P.R + k) + (size_t)x * S));
           if (dx == -INFINITY) {
             alpha = 1.0;  // q(x) = 0
           } else if (lx == -INFINITY) {
             alpha = 0.0;  // p(x) = 0
           } else {
             const double exd = (double)dx * (double)P.c - (double)d.mc;
-            const double ratio = exp2_split(ext - exd) * (d.Z / t.Z);
+            const double ratio = exp2_split(ext - exd) * div_pos(d.Z, t.Z);
             alpha = ratio >= 1.0 ? 1.0 : ratio;
           }
         } else {
-          const double px = lx == -INFINITY ? 0.0 : exp2_split(ext) / t.Z;
+          const double px = lx == -INFINITY ? 0.0 : div_pos(exp2_split(ext), t.Z);
           alpha = px >= 1.0 ? 1.0 : px;
         }
       } else {
         alpha = (x == t.amax) ? 1.0 : 0.0;
       }
     }
-    F.s_alpha[k] = alpha;
-    if (e) atomicOr(&F.s_misc[3], e);
+    sm.alpha[k] = alpha;
   }
-  __syncthreads();
-  if (warp == 0) {
-    int err = F.s_misc[3];
-    for (int r = lane; r < P.rows; r += 32) err |= P.rstat[(size_t)b * P.rows + r].err;
-    err = warp_or(err);
-    int n = 0;
-    if (!err) {
-      n = K;
-      for (int k0 = 0; k0 < K; k0 += 32) {
-        const int k = k0 + lane;
-        bool rej = false;
-        if (k < K) {
-          const double a = F.s_alpha[k];
-          rej = kSoftmax ? !((double)__ldg(P.r + (size_t)b * K + k) <= a) : (a != 1.0);
-        }
-        const unsigned m = __ballot_sync(kFull, rej);
-        if (m) {
-          n = k0 + __ffs(m) - 1;
-          break;
-        }
+  for (int r = lane; r < P.rows; r += 32) e |= read_rowstat(P, sm, b, r).err;
+  const int err = warp_or(e);
+  __syncwarp();
+  int n = 0;
+  if (!err) {
+    n = K;
+    for (int k0 = 0; k0 < K; k0 += 32) {
+      const int k = k0 + lane;
+      bool rej = false;
+      if (k < K) {
+        const double a = sm.alpha[k];
+        const float rk = k < 32 ? r0 : __ldg(P.r + (size_t)b * K + k);
+        rej = kSoftmax ? !((double)rk <= a) : (a != 1.0);
+      }
+      const unsigned msk = __ballot_sync(kFull, rej);
+      if (msk) {
+        n = k0 + __ffs(msk) - 1;
+        break;
       }
     }
-    for (int i = lane; i <= K; i += 32) {
-      const size_t o_i = (size_t)b * (K + 1) + i;
-      int o = -1;
-      if (!err && i < n) o = __ldg(P.draft_tokens + (size_t)b * K + i);
-      if (!err && i == n && !kSoftmax) o = P.rstat[(size_t)b * P.rows + n].amax;
-      P.out_tokens[o_i] = o;
-      if (P.accept_prob && i < K) P.accept_prob[(size_t)b * K + i] = err ? 0.f : (float)F.s_alpha[i];
-      if (P.cand_tokens && (err || !kSoftmax)) P.cand_tokens[o_i] = err ? -1 : P.rstat[(size_t)b * P.rows + i].amax;
-      if (P.pos_mass && (err || !kSoftmax)) P.pos_mass[o_i] = err ? 0.f : 1.f;
-    }
-    if (lane == 0) {
-      P.num_accepted[b] = n;
-      if (P.err_flags) P.err_flags[b] = err;
-      if (P.residual_mass && (err || !kSoftmax)) P.residual_mass[b] = err ? 0.f : 1.f;
-      ReqState rq;
-      rq.n = n;
-      rq.err = err;
-      rq.pad[0] = rq.pad[1] = 0;
-      P.req[b] = rq;
-      F.s_misc[4] = n;
-      F.s_misc[5] = err;
-    }
   }
-  __syncthreads();
+  for (int i = lane; i <= K; i += 32) {
+    const size_t o_i = (size_t)b * (K + 1) + i;
+    int o = -1;
+    if (!err && i < n) o = i < 32 ? x0 : __ldg(P.draft_tokens + (size_t)b * K + i);
+    if (!err && i == n && !kSoftmax) o = read_rowstat(P, sm, b, n).amax;
+    P.out_tokens[o_i] = o;
+    if (P.accept_prob && i < K) P.accept_prob[(size_t)b * K + i] = err ? 0.f : (float)sm.alpha[i];
+    if (P.cand_tokens && (err || !kSoftmax)) P.cand_tokens[o_i] = err ? -1 : read_rowstat(P, sm, b, i).amax;
+    if (P.pos_mass && (err || !kSoftmax)) P.pos_mass[o_i] = err ? 0.f : 1.f;
+  }
+  if (lane == 0) {
+    P.num_accepted[b] = n;
+    if (P.err_flags) P.err_flags[b] = err;
+    if (P.residual_mass && (err || !kSoftmax)) P.residual_mass[b] = err ? 0.f : 1.f;
+    P.req[b].n = n;
+    P.req[b].err = err;
+    __threadfence();
+    *reinterpret_cast<volatile int*>(&P.req[b].ready) = 1;
+  }
+  __syncwarp();
   if constexpr (kSoftmax) {
-    const int n = F.s_misc[4], err = F.s_misc[5];
-    if (err) return;
+    if (err) return -1;
     // draws made here: the bonus row (both modes) and the n-gram residual; with per-position
     // outputs requested every such position, otherwise only the emitted one
     const int kfirst = P.diag ? (MODE == kChain ? K : 0) : n;
     const int klast = P.diag ? K : n;
     for (int k = kfirst; k <= klast; ++k) {
-      if (MODE == kChain && k < K) continue;  // residual_kernel draws from max(0, p - q)
+      if (MODE == kChain && k < K) continue;  // residual work items draw from max(0, p - q)
       const int kind = (MODE == kNgram && k < K) ? kExcl : kFullP;
       const int x = k < K ? __ldg(P.draft_tokens + (size_t)b * K + k) : -1;
       float mass;
-      const int tok = draw_from_chunks<T>(P, b, k, kind, x, buf, F, &mass);
-      if (threadIdx.x == 0) {
+      const int tok = draw_from_chunks<T>(P, sm, fbuf, fph, b, k, kind, x, rd, read_rowstat(P, sm, b, k), &mass);
+      if (lane == 0) {
         const size_t o_k = (size_t)b * (K + 1) + k;
         if (k == n) {
           P.out_tokens[o_k] = tok;
@@ -523,28 +1066,93 @@ __device__ void finish_chain(const Params& P, int b, unsigned char* buf, const F
       }
     }
   }
+  return err ? -1 : n;
+}
+
+// Draft-model chain: the draw from max(0, p_k - q_k) once every residual item of (b, position
+// slot kk) is in.
+template <typename T>
+__device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, int b, int kk,
+                              int n) {
+  constexpr int VE = Elem<T>::kPerVec;
+  const int lane = threadIdx.x & 31;
+  const int k = P.diag ? kk : n;
+  const RowStat ts = read_rowstat(P, sm, b, k);
+  const RowStat ds = read_rowstat(P, sm, b, P.R + k);
+  const size_t bk = (size_t)b * P.npos + kk;
+  const float* ws = P.wsum + bk * P.nchunk_r;
+  const float u = __ldg(P.u + b);
+  auto weight = [&](int c) { return __ldcg(ws + c); };
+  const float S = total_weight(P.nchunk_r, weight);
+  const float mass = (float)((double)S / ts.Z);
+  int tok = -1;
+  if (S > 0.f) {
+    const float tgt = __fmul_rn(u, S);
+    int cstar, sstar;
+    float bstar, sbase;
+    select_part(P.nchunk_r, tgt, weight, cstar, bstar);
+    const float* wsb = P.wsub + (bk * P.nchunk_r + (cstar < 0 ? 0 : cstar)) * kGroupWarps;
+    select_part(kGroupWarps, __fsub_rn(tgt, bstar), [&](int i) { return __ldcg(wsb + i); }, sstar, sbase);
+    if (cstar >= 0 && sstar >= 0) {
+      const float t = __fsub_rn(__fsub_rn(tgt, bstar), sbase);
+      const ResGeo<T> q = res_geo<T>(P, b, k, cstar * kResVec + sstar * kResSub, kResSub);
+      warp_stage<T>(fbuf, q.gt, P.V, q.vt0, q.vt1, &sm.fin_bar, lane);
+      warp_stage<T>(fbuf + (size_t)kFinDraftSlot * 16, q.gd, P.V, q.vd0, q.vd1, &sm.fin_bar, lane);
+      const bool ok = fin_wait(P, sm, fph);
+      const float c = P.c, mct = ts.mc, mcd = ds.mc;
+      const float rho = __fdiv_rn((float)ts.Z, (float)ds.Z);
+      auto wf = [&](int v, float (&w)[VE]) {
+        resid_weights<T>(fbuf, kFinDraftSlot, v, q.e_base, q.e_lo, q.e_hi, q.dshift, c, mct, mcd, rho, w);
+      };
+      const int pos = warp_crossing<VE>(q.vt1 - q.vt0, t, wf);
+      __syncwarp();
+      tok = (ok && pos >= 0) ? q.e_base + pos : -1;
+    }
+  } else {  // no residual mass: draw from p
+    float unused;
+    const CsReader rd = stage_request_stats(P, sm.fin_cs, b, false);
+    tok = draw_from_chunks<T>(P, sm, fbuf, fph, b, k, kFullP, -1, rd, ts, &unused);
+  }
+  if (lane == 0) {
+    const size_t o_k = (size_t)b * (P.K + 1) + k;
+    if (k == n) {
+      P.out_tokens[o_k] = tok;
+      if (P.residual_mass) P.residual_mass[b] = mass;
+    }
+    if (P.cand_tokens) P.cand_tokens[o_k] = tok;
+    if (P.pos_mass) P.pos_mass[o_k] = mass;
+  }
 }
 
 // Greedy tree walk (section III.2): from the root, move to the child whose token equals the
-// argmax of the current node's row (lowest node index first) until none does.  Warp 0.
-__device__ inline void walk_tree(const Params& P, int b) {
+// argmax of the current node's row (lowest node index first) until none does.
+__device__ inline void walk_tree(const Params& P, Shared& sm, int b) {
   const int lane = threadIdx.x & 31;
   const int N1 = P.R, V = P.V;
   const RowStat* rs = P.rstat + (size_t)b * N1;
   const int32_t* par = P.parents + (size_t)b * N1;
   const int32_t* tok = P.node_tokens + (size_t)b * N1;
+  if (N1 <= kFinRows) {  // walk a small tree from shared memory
+    for (int i = lane; i < N1; i += 32) {
+      sm.fin_par[i] = par[i];
+      sm.fin_tok[i] = tok[i];
+    }
+    __syncwarp();
+    par = sm.fin_par;
+    tok = sm.fin_tok;
+  }
   int32_t* path = P.path_nodes + (size_t)b * N1;
   int32_t* out = P.out_tokens + (size_t)b * N1;
   int err = 0;
   for (int i = lane; i < N1; i += 32) {
-    err |= rs[i].err;
-    const int p = __ldg(par + i);
+    err |= i < kFinRows ? sm.fin_rs[i].err : __ldcg(&rs[i].err);
+    const int p = par[i];
     if (i == 0 ? (p != -1) : (p < 0 || p >= i)) err |= SPEC_ERRF_BAD_TREE;
     if (i > 0) {
-      const int t = __ldg(tok + i);
+      const int t = tok[i];
       if (t < 0 || t >= V) err |= SPEC_ERRF_BAD_TOKEN;
     }
-    if (P.node_argmax) P.node_argmax[(size_t)b * N1 + i] = rs[i].amax;
+    if (P.node_argmax) P.node_argmax[(size_t)b * N1 + i] = i < kFinRows ? sm.fin_rs[i].amax : __ldcg(&rs[i].amax);
   }
   err = warp_or(err);
   int len = 0;
@@ -552,11 +1160,11 @@ __device__ inline void walk_tree(const Params& P, int b) {
     int cur = 0;
     if (lane == 0) path[0] = 0;
     for (int step = 0; step < N1; ++step) {  // cur strictly increases: at most N1 - 1 moves
-      const int a = rs[cur].amax;
+      const int a = cur < kFinRows ? sm.fin_rs[cur].amax : __ldcg(&rs[cur].amax);
       int next = -1;
       for (int c0 = cur + 1; c0 < N1 && next < 0; c0 += 32) {
         const int cc = c0 + lane;
-        const bool m = cc < N1 && __ldg(par + cc) == cur && __ldg(tok + cc) == a;
+        const bool m = cc < N1 && par[cc] == cur && tok[cc] == a;
         const unsigned bal = __ballot_sync(kFull, m);
         if (bal) next = c0 + __ffs(bal) - 1;
       }
@@ -565,13 +1173,14 @@ __device__ inline void walk_tree(const Params& P, int b) {
         break;
       }
       if (lane == 0) {
-        out[len] = __ldg(tok + next);
+        out[len] = tok[next];
         path[len + 1] = next;
       }
       ++len;
       cur = next;
     }
   }
+  __syncwarp();
   for (int i = lane; i < N1; i += 32) {
     if (err || i > len) {
       path[i] = -1;
@@ -584,266 +1193,115 @@ __device__ inline void walk_tree(const Params& P, int b) {
   }
 }
 
-// ---------------------------------------------------------------------- stats kernel ----
-// Persistent: each CTA claims work items (one chunk of one row; request-major order) from an
-// atomic counter, one item ahead of use, and keeps two of them in flight in its two stages.  The
-// ticket of an item is taken after its statistics are written; its result is examined one item
-// later (so the atomic's latency overlaps the next item), and the CTA whose ticket completed a
-// request finishes that request before going on.
-template <int MODE, typename T>
-__global__ void __launch_bounds__(kThreads, 3) stats_kernel(const Params P) {
-  constexpr int VE = Elem<T>::kPerVec;
-  constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
-  extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ uint64_t bar[2];
-  __shared__ uint64_t bar_x;
-  __shared__ unsigned xphase;
-  __shared__ float red[3 * kWarps];
-  __shared__ int redi[kWarps];
-  __shared__ float tileW[kMaxTiles][kWarps];
-  __shared__ int s_int[4];
-  __shared__ float s_flt[4];
-  __shared__ double s_dbl[4];
-  __shared__ int s_misc[8];
-  __shared__ int s_fin;
-  __shared__ unsigned s_item[2];
-  __shared__ double s_alpha[MODE == kTree ? 1 : SPEC_MAX_K];
-
-  const int tid = threadIdx.x;
-  const int per_req = P.rows * P.nchunk;
-  const unsigned total = (unsigned)((long long)P.B * per_req);
-  if (tid == 0) {
-    mbar_init(&bar[0], 1);
-    mbar_init(&bar[1], 1);
-    mbar_init(&bar_x, 1);
-    xphase = 0;
-    fence_mbar_init();
-    s_item[0] = atomicAdd(P.work, 1u);
-    s_item[1] = atomicAdd(P.work, 1u);
-  }
-  __syncthreads();
-  const uint64_t pol = l2_policy_evict_first();
-  const FinishSmem F{tileW, s_int, s_flt, s_dbl, s_alpha, s_misc, &bar_x, &xphase};
-
-  auto locate = [&](unsigned w, int& b, int& r, int& ch, const char*& rp) {
-    b = (int)(w / (unsigned)per_req);
-    const int rem = (int)(w - (unsigned)b * (unsigned)per_req);
-    r = rem / P.nchunk;
-    ch = rem - r * P.nchunk;
-    rp = row_ptr<T>(P, b, r);
-    return make_geo<T>(rp, ch * P.chunk, chunk_len(P, ch));
-  };
-  auto finish = [&](int b, unsigned char* buf) {
-    __threadfence();
-    if constexpr (MODE == kTree) {
-      combine_rows<MODE>(P, b);
-      if (tid < 32) walk_tree(P, b);
-    } else {
-      finish_chain<MODE, T>(P, b, buf, F);
-    }
-  };
-  for (int s = 0; s < 2; ++s) {
-    if (s_item[s] < total) {
-      int b, r, ch;
-      const char* rp;
-      const Geo g = locate(s_item[s], b, r, ch, rp);
-      issue_chunk<T>(smem + s * P.buf_bytes, rp, g, &bar[s], pol);
-    }
-  }
-  int pend_b = -1;      // thread 0: request of the previous item's ticket
-  unsigned pend_old = 0;  // thread 0: that ticket's value before the increment
-  for (int it = 0;; ++it) {
-    const int st = it & 1;
-    const unsigned w = s_item[st];
-    if (w >= total) break;  // claims increase, so the other stage is empty too
-    unsigned claim = 0;
-    if (tid == 0) claim = atomicAdd(P.work, 1u);  // the item this stage takes next
-    unsigned char* buf = smem + st * P.buf_bytes;
-    int b, r, ch;
-    const char* rp;
-    const Geo g = locate(w, b, r, ch, rp);
-    bool ok = mbar_wait_bounded(&bar[st], (uint32_t)(it >> 1) & 1u);
-    if (!ok) ok = mbar_wait_bounded(&bar[st], (uint32_t)(it >> 1) & 1u);  // never go on with a copy in flight
-    __syncthreads();  // plain-loaded slots of this stage are visible
-
-    ChunkStat q;
-    if constexpr (kSoftmax) {
-      int vx = -1, jx = -1;
-      if (MODE == kNgram && r < P.K) {
-        const int x = __ldg(P.draft_tokens + (size_t)b * P.K + r);
-        if (x >= g.e0 && x < g.e0 + g.n) {
-          const int sl = x - g.e0 + g.slot0;
-          vx = sl / VE;
-          jx = sl - vx * VE;
-        }
+// Waits (bounded) until *count reaches `want`; false on a timeout or abort.
+__device__ __forceinline__ bool wait_count(const Params& P, Shared& sm, const unsigned* count, unsigned want) {
+  const int lane = threadIdx.x & 31;
+  int ok = 0;
+  if (lane == 0) {
+    const long long t0 = clock64();
+    for (;;) {
+      if ((unsigned)ld_volatile(reinterpret_cast<const int*>(count)) >= want) {
+        ok = 1;
+        break;
       }
-      q = chunk_softmax_stats<T>(buf, g, P.c, vx, jx, red);
-      if (!ok) q.i |= SPEC_ERRF_TIMEOUT;
-    } else {
-      q = chunk_argmax<T>(buf, g, red, redi);
-      if (!ok) q.i = -1;
+      if (aborted(sm)) break;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        raise_abort(P, sm);
+        break;
+      }
+      __nanosleep(128);
     }
-    if (tid == 0) {
-      s_fin = (pend_b >= 0 && pend_old == (unsigned)(per_req - 1)) ? pend_b : -1;
-      P.cstat[((size_t)b * P.rows + r) * P.nchunk + ch] = q;
-      __threadfence();
-      pend_old = atomicAdd(P.tick_a + b, 1u);
-      pend_b = b;
-    }
-    __syncthreads();
-    if (s_fin >= 0) finish(s_fin, buf);  // the previous item's ticket completed its request
-    if (tid == 0) s_item[st] = claim;
-    __syncthreads();  // every thread is done with this stage and sees the claim
-    if (claim < total) {
-      const Geo g2 = locate(claim, b, r, ch, rp);
-      issue_chunk<T>(buf, rp, g2, &bar[st], pol);
-    }
+    __threadfence();  // acquire: every chunk's statistics
   }
-  if (tid == 0) s_fin = (pend_b >= 0 && pend_old == (unsigned)(per_req - 1)) ? pend_b : -1;
-  __syncthreads();
-  if (s_fin >= 0) finish(s_fin, smem);  // no copy is in flight once the loop has ended
+  return __shfl_sync(kFull, ok, 0) != 0;
 }
 
-// ------------------------------------------------------------------- residual kernel ----
-// Draft-model chain, T > 0: the draw from max(0, p_k - q_k) at the rejected position (with
-// per-position outputs requested: at every draft position).  One CTA per (request, position,
-// chunk); the last chunk of a (request, position) finds the crossing chunk and searches it.
-template <typename T>
-__global__ void __launch_bounds__(kThreads, 3) residual_kernel(const Params P) {
-  constexpr int VE = Elem<T>::kPerVec;
+// The finishing warp: requests b = blockIdx.x, blockIdx.x + gridDim.x, ...
+template <int MODE, typename T>
+__device__ void fin_loop(const Params& P, Shared& sm, unsigned char* fbuf) {
+  uint32_t fph = 0;
+  const unsigned per_req = (unsigned)(P.rows * P.nchunk);
+  for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
+    if (!wait_count(P, sm, P.tick_a + b, per_req)) return;
+    if constexpr (MODE == kTree) {
+      const CsReader rd = stage_request_stats(P, sm.fin_cs, b, true);
+      combine_rows<MODE>(P, sm, b, rd);
+      walk_tree(P, sm, b);
+    } else {
+      const int n = finish_chain<MODE, T>(P, sm, fbuf, fph, b);
+      if constexpr (MODE == kChain) {
+        if (P.npos > 0 && n >= 0) {
+          for (int kk = 0; kk < P.npos; ++kk) {
+            if (!P.diag && n >= P.K) break;  // everything accepted: the bonus draw was made above
+            if (!wait_count(P, sm, P.tick_b + (size_t)b * P.npos + kk, (unsigned)P.nchunk_r)) return;
+            residual_draw<T>(P, sm, fbuf, fph, b, kk, n);
+          }
+        }
+      }
+    }
+  }
+}
+
+// --------------------------------------------------------------------------- kernel ----
+template <int MODE, typename T>
+__global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ uint64_t bar;
-  __shared__ float red[2 * kWarps];
-  __shared__ float tileW[kMaxTiles][kWarps];
-  __shared__ int s_int[4];
-  __shared__ float s_flt[4];
-  __shared__ double s_dbl[4];
-  __shared__ int s_misc[4];
-  __shared__ int s_last;
-
-  const int tid = threadIdx.x;
-  const int npos = P.diag ? P.K : 1;
-  const int b = (int)(blockIdx.x / (unsigned)(npos * P.nchunk));
-  const int pk = (int)(blockIdx.x / (unsigned)P.nchunk) % npos;
-  const int ch = (int)(blockIdx.x % (unsigned)P.nchunk);
-  const ReqState rq = P.req[b];
-  const int k = P.diag ? pk : rq.n;
-  if (rq.err || k >= P.K) return;  // accepted everything, or failed: nothing to draw here
-
-  unsigned char* bufT = smem;
-  unsigned char* bufD = smem + P.buf_bytes;
-  const RowStat ts = P.rstat[(size_t)b * P.rows + k];
-  const RowStat ds = P.rstat[(size_t)b * P.rows + P.R + k];
-  const float c = P.c, mct = ts.mc, mcd = ds.mc;
-  const float rho = __fdiv_rn((float)ts.Z, (float)ds.Z);  // max(0, p - q) Z_t = max(0, e - f Z_t / Z_d)
-  const char* rT = row_ptr<T>(P, b, k);
-  const char* rD = row_ptr<T>(P, b, P.R + k);
+  __shared__ Shared sm;
+  const int tid = threadIdx.x, warp = tid >> 5;
   if (tid == 0) {
-    mbar_init(&bar, 2);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], kGroupWarps);
+    }
+    for (int j = 0; j < kSlots; ++j) {
+      mbar_init(&sm.pfull[j], 1);
+      mbar_init(&sm.pempty[j], 1);
+      sm.pcnt[j] = 0;
+    }
+    mbar_init(&sm.fin_bar, 1);
+    sm.abort = 0;
     fence_mbar_init();
   }
   __syncthreads();
-  const uint64_t pol = l2_policy_evict_last();  // the crossing chunk is read again right away
-  Geo g = make_geo<T>(rT, ch * P.chunk, chunk_len(P, ch));
-  issue_chunk<T>(bufT, rT, g, &bar, pol);
-  issue_chunk<T>(bufD, rD, g, &bar, pol);  // laid out like the target row (plain loads if phases differ)
-  bool ok = mbar_wait_bounded(&bar, 0);
-  if (!ok) ok = mbar_wait_bounded(&bar, 0);
+  unsigned char* fbuf = smem + (size_t)kStages * kStageBytes;
+  if (warp < kConsWarps)
+    consumer_loop<MODE, T>(P, sm, smem);
+  else if (warp < kProducerWarp + kGroups)
+    producer_loop<MODE, T>(P, sm, smem, warp - kProducerWarp);
+  else if (warp == kBookWarp)
+    book_loop<MODE>(P, sm);
+  else
+    fin_loop<MODE, T>(P, sm, fbuf);
   __syncthreads();
-
-  auto resid = [&](int v, float (&w)[VE]) {
-    float f[VE], d[VE];
-    Elem<T>::unpack(*reinterpret_cast<const uint4*>(bufT + (size_t)v * 16), f);
-    Elem<T>::unpack(*reinterpret_cast<const uint4*>(bufD + (size_t)v * 16), d);
-#pragma unroll
-    for (int j = 0; j < VE; ++j) {
-      const float e = ex2(__fmaf_rn(f[j], c, -mct));
-      const float q = ex2(__fmaf_rn(d[j], c, -mcd));
-      w[j] = fmaxf(0.f, __fmaf_rn(-q, rho, e));
-    }
-  };
-  float sw = 0.f, unused = 0.f;
-  for (int v = tid; v < g.nvec; v += kThreads) {
-    float w[VE];
-    resid(v, w);
-    float vs = 0.f;
-#pragma unroll
-    for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, w[j]);
-    sw = __fadd_rn(sw, vs);
-  }
-  block_sum2(sw, unused, red);
-  const size_t bk = P.diag ? (size_t)b * P.K + k : (size_t)b;
+  // The last CTA out reports a timed-out call (never expected) on every request.
   if (tid == 0) {
-    P.wsum[bk * P.nchunk + ch] = ok ? sw : 0.f;
     __threadfence();
-    s_last = (atomicAdd(P.tick_b + bk, 1u) == (unsigned)(P.nchunk - 1));
+    sm.last = atomicAdd(P.exit_tick, 1u) == gridDim.x - 1;
   }
   __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // last chunk of (b, k): total residual weight, crossing chunk, search
-  if (tid < 32) {
-    const ChunkStat* cs = P.cstat + ((size_t)b * P.rows + k) * P.nchunk;
-    const double u = (double)__ldg(P.u + b);
-    int kind = kResid, cstar;
-    double bstar, S;
-    auto weight = [&](int q) {
-      return kind == kResid ? (double)__ldcg(P.wsum + bk * P.nchunk + q)
-                            : chunk_weight(__ldcg(&cs[q].a), __ldcg(&cs[q].s), c, mct);
-    };
-    chunk_select(P.nchunk, u, weight, cstar, bstar, S);
-    const double mass = S / ts.Z;
-    if (!(S > 0.0)) {  // no residual mass: draw from p
-      kind = kFullP;
-      chunk_select(P.nchunk, u, weight, cstar, bstar, S);
+  if (sm.last) {
+    __threadfence();
+    if (ld_volatile(reinterpret_cast<const int*>(P.gerr))) {
+      const int width = (MODE == kTree) ? P.R : P.K + 1;
+      for (int b = tid; b < P.B; b += kThreads) {
+        if (P.err_flags) P.err_flags[b] = SPEC_ERRF_TIMEOUT;
+        if (MODE == kTree) {
+          P.accept_len[b] = 0;
+          for (int i = 0; i < width; ++i) P.path_nodes[(size_t)b * width + i] = -1;
+        } else {
+          P.num_accepted[b] = 0;
+          if (P.residual_mass) P.residual_mass[b] = 0.f;
+        }
+        for (int i = 0; i < width; ++i) P.out_tokens[(size_t)b * width + i] = -1;
+      }
     }
-    if (tid == 0) {
-      s_misc[0] = cstar;
-      s_misc[1] = kind;
-      s_dbl[0] = u * S - bstar;
-      s_dbl[1] = mass;
-    }
-  }
-  __syncthreads();
-  const int cstar = s_misc[0], kind = s_misc[1];
-  const float t = (float)s_dbl[0];
-  const float mass = (float)s_dbl[1];
-  int tok = -1;
-  if (cstar >= 0) {
-    g = make_geo<T>(rT, cstar * P.chunk, chunk_len(P, cstar));
-    issue_chunk<T>(bufT, rT, g, &bar, l2_policy_evict_first());
-    issue_chunk<T>(bufD, rD, g, &bar, l2_policy_evict_first());
-    bool ok2 = mbar_wait_bounded(&bar, 1);
-    if (!ok2) ok2 = mbar_wait_bounded(&bar, 1);
-    __syncthreads();
-    if (kind == kResid) {
-      tok = chunk_crossing<VE>(g, t, resid, tileW, s_int, s_flt);
-    } else {
-      auto full = [&](int v, float (&w)[VE]) {
-        float f[VE];
-        Elem<T>::unpack(*reinterpret_cast<const uint4*>(bufT + (size_t)v * 16), f);
-#pragma unroll
-        for (int j = 0; j < VE; ++j) w[j] = ex2(__fmaf_rn(f[j], c, -mct));
-      };
-      tok = chunk_crossing<VE>(g, t, full, tileW, s_int, s_flt);
-    }
-    if (!ok2) tok = -1;
-  }
-  if (tid == 0) {
-    const size_t o_k = (size_t)b * (P.K + 1) + k;
-    if (k == rq.n) {
-      P.out_tokens[o_k] = tok;
-      if (P.residual_mass) P.residual_mass[b] = mass;
-    }
-    if (P.cand_tokens) P.cand_tokens[o_k] = tok;
-    if (P.pos_mass) P.pos_mass[o_k] = mass;
   }
 }
 
 // ---------------------------------------------------------------------- probs kernel ----
 // Testing aid: p_i = 2^(l_i c - mc) / Z for every target row, q likewise for draft rows.
 template <typename T>
-__global__ void __launch_bounds__(kThreads) probs_kernel(const Params P) {
+__global__ void __launch_bounds__(256) probs_kernel(const Params P) {
   const int rowid = blockIdx.x;  // b * rows + r
   const int b = rowid / P.rows, r = rowid - b * P.rows;
   if (P.req[b].err) return;
@@ -853,7 +1311,7 @@ __global__ void __launch_bounds__(kThreads) probs_kernel(const Params P) {
   const RowStat rs = P.rstat[rowid];
   const char* rp = row_ptr<T>(P, b, r);
   const float invZ = (float)(1.0 / rs.Z);
-  for (int i = (int)threadIdx.x; i < P.V; i += kThreads) {
+  for (int i = (int)threadIdx.x; i < P.V; i += 256) {
     const float l = Elem<T>::to_float(Elem<T>::load_raw(rp + (size_t)i * Elem<T>::kSize));
     out[i] = __fmul_rn(ex2(__fmaf_rn(l, P.c, -rs.mc)), invZ);
   }
@@ -861,39 +1319,27 @@ __global__ void __launch_bounds__(kThreads) probs_kernel(const Params P) {
 
 // -------------------------------------------------------------------------- launchers ----
 struct LaunchPlan {
-  size_t smem_stats;  // dynamic shared memory of stats_kernel (two stages)
-  size_t smem_resid;  // dynamic shared memory of residual_kernel (target + draft chunk)
-  int launch_resid;   // launch residual_kernel
-  int launch_probs;   // launch probs_kernel
-  int sm_count;       // multiprocessors of the current device
+  size_t smem;       // dynamic shared memory of verify_kernel
+  int launch_probs;  // launch probs_kernel
+  int sm_count;      // multiprocessors of the current device
 };
 
 template <int MODE, typename T>
 cudaError_t launch_mode(const Params& P, const LaunchPlan& L, cudaStream_t stream) {
-  auto ks = stats_kernel<MODE, T>;
-  cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem_stats);
+  auto ks = verify_kernel<MODE, T>;
+  cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ks, kThreads, L.smem_stats);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ks, kThreads, L.smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const long long items = (long long)P.B * P.rows * P.nchunk;
   const long long cap = (long long)per_sm * L.sm_count;
-  const long long grid = items < cap ? items : cap;
-  ks<<<(unsigned)grid, kThreads, L.smem_stats, stream>>>(P);
+  const long long grid = (long long)P.total < cap ? (long long)P.total : cap;
+  ks<<<(unsigned)grid, kThreads, L.smem, stream>>>(P);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (L.launch_resid) {
-    auto kr = residual_kernel<T>;
-    e = cudaFuncSetAttribute(kr, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem_resid);
-    if (e != cudaSuccess) return e;
-    const long long nb = (long long)P.B * (P.diag ? P.K : 1) * P.nchunk;
-    kr<<<(unsigned)nb, kThreads, L.smem_resid, stream>>>(P);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-  }
   if (L.launch_probs) {
-    probs_kernel<T><<<(unsigned)((long long)P.B * P.rows), kThreads, 0, stream>>>(P);
+    probs_kernel<T><<<(unsigned)((long long)P.B * P.rows), 256, 0, stream>>>(P);
     e = cudaGetLastError();
   }
   return e;
