@@ -86,9 +86,11 @@ Layout layout(int B, int rows, const Chunking& ck) {
   return L;
 }
 
-int sm_count() {
+// Multiprocessors of the current device (cached per device); *device receives the device.
+int sm_count(int* device) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+  *device = dev;
   static int cache[64] = {0};
   if (dev < 64 && cache[dev] > 0) return cache[dev];
   int n = 0;
@@ -119,17 +121,17 @@ spec_status_t attach_workspace(Params& P, void* ws, size_t bytes, int B, int row
   return SPEC_OK;
 }
 
-// Requests between a request's stats items and its residual items: enough for the request's
-// chunks in flight to land and its acceptance result to be published before a producer stages the
-// residual items (a producer that gets there first waits).  SPEC_VERIFY_RESID_LAG overrides it.
-int residual_lag(int B, int items_per_request, int sms) {
+// Requests between a request's stats items and its residual items.  A producer that reaches a
+// residual item before its request's acceptance result is published waits, and measured on GB300
+// that waiting costs more than reading the rejected pair again from HBM instead of L2; so by
+// default every residual item follows every stats item (lag = B).  SPEC_VERIFY_RESID_LAG
+// overrides it (tuning).
+int residual_lag(int B) {
   static const int env = [] {
     const char* s = getenv("SPEC_VERIFY_RESID_LAG");
     return s ? atoi(s) : -1;
   }();
-  long long L = env >= 0 ? env : 2 + ((long long)sms * 12 + items_per_request - 1) / items_per_request;
-  if (L > B) L = B;
-  return (int)L;
+  return (env >= 0 && env < B) ? env : B;
 }
 
 // Constants of the item decoding's divisions (see fastdiv.h).
@@ -189,10 +191,11 @@ spec_status_t verify_chain_common(bool ngram, const void* target, const void* dr
   if ((long long)B * per_req > INT_MAX) return SPEC_ERR_UNSUPPORTED;
   spec_status_t st = attach_workspace(P, ws, ws_bytes, B, rows, ck);
   if (st != SPEC_OK) return st;
-  const int sms = sm_count();
+  int device = -1;
+  const int sms = sm_count(&device);
   if (sms <= 0) return SPEC_ERR_CUDA;
   P.total = (unsigned)(B * per_req);
-  P.lag = P.npos ? residual_lag(B, rows * ck.nchunk, sms) : 0;
+  P.lag = P.npos ? residual_lag(B) : 0;
   set_divisors(P, rows);
   P.target = target;
   P.draft = two_rows ? draft : nullptr;
@@ -217,6 +220,7 @@ spec_status_t verify_chain_common(bool ngram, const void* target, const void* dr
   P.draft_probs = two_rows ? draft_probs : nullptr;
   specv::LaunchPlan L = {};
   L.sm_count = sms;
+  L.device = device;
   L.launch_probs = (P.target_probs || P.draft_probs) ? 1 : 0;
   const int mode = greedy ? specv::kGreedy : (ngram ? specv::kNgram : specv::kChain);
   return launch(dtype, mode, P, L, reinterpret_cast<cudaStream_t>(stream));
@@ -273,7 +277,8 @@ spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t dt
   if ((long long)B * rows * P.nchunk > INT_MAX) return SPEC_ERR_UNSUPPORTED;
   spec_status_t st = attach_workspace(P, workspace, workspace_bytes, B, rows, ck);
   if (st != SPEC_OK) return st;
-  const int sms = sm_count();
+  int device = -1;
+  const int sms = sm_count(&device);
   if (sms <= 0) return SPEC_ERR_CUDA;
   P.total = (unsigned)((long long)B * rows * P.nchunk);
   P.npos = 0;
@@ -293,6 +298,7 @@ spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t dt
   P.node_argmax = node_argmax;
   specv::LaunchPlan L = {};
   L.sm_count = sms;
+  L.device = device;
   return launch(dtype, specv::kTree, P, L, reinterpret_cast<cudaStream_t>(stream));
 }
 

@@ -275,25 +275,6 @@ __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
   }
   return v;
 }
-// 2^x in double with fp32 relative accuracy (~3e-7): the integer part of x scales exactly, the
-// fractional part goes through the special-function unit.  Avoids double-precision
-// transcendentals, which are slow on this part.
-__device__ __forceinline__ double exp2_split(double x) {
-  if (!(x > -1020.0)) return x != x ? x : 0.0;
-  if (x > 1020.0) return __longlong_as_double(0x7ff0000000000000LL);
-  const int n = __double2int_rd(x);
-  const double scale = __hiloint2double((n + 1023) << 20, 0);  // 2^n
-  return (double)ex2((float)(x - (double)n)) * scale;
-}
-// a / b in double without the division sequence: an fp32 reciprocal refined by two Newton steps
-// (relative error ~1e-15 for finite, positive, normal b).
-__device__ __forceinline__ double div_pos(double a, double b) {
-  double r = (double)__frcp_rn((float)b);
-  r = r * __fma_rn(-b, r, 2.0);
-  r = r * __fma_rn(-b, r, 2.0);
-  return a * r;
-}
-
 // ------------------------------------------------------------------------ row staging ----
 // A logits row is read as a grid of 16-byte vectors starting at the row's address rounded down to
 // 16 bytes: grid vector v holds elements v * VE - phase .. v * VE - phase + VE - 1, where phase is

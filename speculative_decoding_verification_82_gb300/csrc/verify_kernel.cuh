@@ -18,10 +18,9 @@
 //    the sub-chunk that holds the crossing), or walks the draft tree.
 // Work items are ordered request-major.  For chains with draft logits and T > 0 the draw after a
 // rejection at position n needs max(0, p_n - q_n), which needs both rows' normalisers first; the
-// pair at n is then read a second time by residual work items, placed in the item order a fixed
-// number of requests after the request's own items, so that the pair is read again shortly after
-// its first read (normally still in L2).  Their producer waits (bounded) for the request's
-// acceptance result before staging them.
+// pair at n is then read a second time by residual work items, placed in the item order `lag`
+// requests after the request's own items (by default after every stats item).  Their producer
+// waits (bounded) for the request's acceptance result before staging them.
 //
 // Formulas: "Speculative Decoding in Production: From Draft Models to EAGLE-3 Dynamic Trees for
 // 3x-5x Lossless Acceleration", section I.1 (acceptance ratio, uniform test, first-rejection
@@ -913,15 +912,23 @@ __device__ void combine_rows(const Params& P, Shared& sm, int b, const CsReader&
       const bool finite_m = !isnan(m) && m != INFINITY && m != -INFINITY;
       double Z = 0.0;
       if (!fl && finite_m) {
-        float zs = 0.f, zc = 0.f;  // compensated (Kahan) sum of the chunk weights
-        for (int c = 0; c < P.nchunk; ++c) {
-          const ChunkStat q = rd(r, c);
-          const float y = __fsub_rn(chunk_weight(q.a, q.s, P.c, mc), zc);
-          const float t = __fadd_rn(zs, y);
-          zc = __fsub_rn(__fsub_rn(t, zs), y);
-          zs = t;
+        float z4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains, summed pairwise
+        int c = 0;
+        for (; c + 4 <= P.nchunk; c += 4) {
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const ChunkStat q = rd(r, c + u);
+            z4[u] = __fadd_rn(z4[u], chunk_weight(q.a, q.s, P.c, mc));
+          }
         }
-        Z = (double)zs - (double)zc;
+#pragma unroll
+        for (int u = 0; u < 3; ++u) {
+          if (c + u < P.nchunk) {
+            const ChunkStat q = rd(r, c + u);
+            z4[u] = __fadd_rn(z4[u], chunk_weight(q.a, q.s, P.c, mc));
+          }
+        }
+        Z = (double)__fadd_rn(__fadd_rn(z4[0], z4[1]), __fadd_rn(z4[2], z4[3]));
       }
       rs.Z = Z;
       rs.mc = mc;
@@ -944,6 +951,24 @@ __device__ void combine_rows(const Params& P, Shared& sm, int b, const CsReader&
   }
   __syncwarp();
   __threadfence();
+}
+
+// l c - mc with the product l c carried exactly (an fp32 pair from one FMA) and the difference
+// taken in double: the exponent of 2^(l c - mc) must not lose the digits that a large |l c|
+// would round away in fp32.
+__device__ __forceinline__ double scaled_logit(float l, float c, float mc) {
+  const float p = __fmul_rn(l, c);
+  const float e = __fmaf_rn(l, c, -p);  // l c = p + e exactly
+  return ((double)p - (double)mc) + (double)e;
+}
+// 2^x * f for double x and fp32 f > 0, in fp32: the fractional part of x through the
+// special-function unit, the integer part as an exact power of two.  Saturates to +inf / 0.
+__device__ __forceinline__ float exp2_times(double x, float f) {
+  if (!(x > -300.0)) return 0.f;
+  if (x > 300.0) return INFINITY;
+  const int n = __double2int_rd(x);
+  const float r = __fmul_rn(ex2((float)(x - (double)n)), f);  // in [0, 2) * f
+  return ldexpf(r, n);
 }
 
 // Chain / n-gram / greedy-chain finishing: alpha, acceptance scan (section I.1 step 2), outputs,
@@ -977,8 +1002,10 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
     } else {
       const RowStat t = read_rowstat(P, sm, b, k);
       if (kSoftmax) {
+        // alpha = p(x) / q(x) = 2^((l_x c - mc_t) - (d_x c - mc_d)) Z_d / Z_t (draft model), or
+        // p(x) = 2^(l_x c - mc_t) / Z_t (one-hot draft); capped at 1
         const float lx = k < 32 ? lx0 : Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, k) + (size_t)x * S));
-        const double ext = (double)lx * (double)P.c - (double)t.mc;
+        const double ext = scaled_logit(lx, P.c, t.mc);
         if (MODE == kChain) {
           const RowStat d = read_rowstat(P, sm, b, P.R + k);
           const float dx =
@@ -988,13 +1015,12 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
           } else if (lx == -INFINITY) {
             alpha = 0.0;  // p(x) = 0
           } else {
-            const double exd = (double)dx * (double)P.c - (double)d.mc;
-            const double ratio = exp2_split(ext - exd) * div_pos(d.Z, t.Z);
-            alpha = ratio >= 1.0 ? 1.0 : ratio;
+            const float ratio = exp2_times(ext - scaled_logit(dx, P.c, d.mc), __fdiv_rn((float)d.Z, (float)t.Z));
+            alpha = ratio >= 1.f ? 1.0 : (double)ratio;
           }
         } else {
-          const double px = lx == -INFINITY ? 0.0 : div_pos(exp2_split(ext), t.Z);
-          alpha = px >= 1.0 ? 1.0 : px;
+          const float px = lx == -INFINITY ? 0.f : exp2_times(ext, __frcp_rn((float)t.Z));
+          alpha = px >= 1.f ? 1.0 : (double)px;
         }
       } else {
         alpha = (x == t.amax) ? 1.0 : 0.0;
@@ -1322,17 +1348,25 @@ struct LaunchPlan {
   size_t smem;       // dynamic shared memory of verify_kernel
   int launch_probs;  // launch probs_kernel
   int sm_count;      // multiprocessors of the current device
+  int device;        // the current device
 };
 
 template <int MODE, typename T>
 cudaError_t launch_mode(const Params& P, const LaunchPlan& L, cudaStream_t stream) {
   auto ks = verify_kernel<MODE, T>;
-  cudaError_t e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
-  if (e != cudaSuccess) return e;
-  int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ks, kThreads, L.smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // the shared-memory opt-in and the occupancy, once per device (the same values every call)
+  constexpr int kMaxDev = 64;
+  static int resident[kMaxDev] = {0};
+  int per_sm = (L.device >= 0 && L.device < kMaxDev) ? resident[L.device] : 0;
+  cudaError_t e = cudaSuccess;
+  if (per_sm < 1) {
+    e = cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L.smem);
+    if (e != cudaSuccess) return e;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, ks, kThreads, L.smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorInvalidConfiguration;
+    if (L.device >= 0 && L.device < kMaxDev) resident[L.device] = per_sm;
+  }
   const long long cap = (long long)per_sm * L.sm_count;
   const long long grid = (long long)P.total < cap ? (long long)P.total : cap;
   ks<<<(unsigned)grid, kThreads, L.smem, stream>>>(P);
