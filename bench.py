@@ -258,9 +258,21 @@ def max_over_ranks(x: float, world: int) -> float:
     import torch
     import torch.distributed as dist
 
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def rank_seeds(rank: int, n_sets: int) -> list[int]:
+    """Input seeds of one rank: each rank verifies its own requests (the path shards by request)."""
+    return [1000 * rank + s for s in range(n_sets)]
+
+
+def job_rows_per_s(world: int, rows_per_step: int, steps: int, elapsed_ms: float) -> float:
+    """Whole-job throughput: every rank processed `rows_per_step` rows per step; the slowest
+    rank's time (max over ranks) bounds the job."""
+    return world * rows_per_step * steps / (elapsed_ms / 1e3)
 
 
 class DeviceCase:
@@ -362,7 +374,7 @@ def run_gpu(args, w) -> None:
     binding.library()  # fail loudly if the CUDA library is missing
 
     n_sets = 2  # alternate two input sets; each is larger than L2 as well
-    inputs = [make_inputs(args.workload, seed=1000 * rank + s) for s in range(n_sets)]
+    inputs = [make_inputs(args.workload, seed=s) for s in rank_seeds(rank, n_sets)]
     rows_req = rows_per_request(w)
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w["dtype"]]
     ws = binding.make_workspace(w["B"], rows_req, w["V"], tdt, dev)
@@ -414,7 +426,7 @@ def run_gpu(args, w) -> None:
     mean_call_ms = statistics.fmean(a.elapsed_time(b) for a, b in zip(ev0, ev1))
 
     rows_step = w["B"] * rows_req
-    value = world * rows_step * K / (elapsed_ms / 1e3)
+    value = job_rows_per_s(world, rows_step, K, elapsed_ms)
     alg_bytes = algorithmic_bytes(w)
     achieved = alg_bytes / (mean_call_ms / 1e3) / 1e9
     peak, peak_src = hbm_peak()
