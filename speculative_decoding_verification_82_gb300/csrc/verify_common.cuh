@@ -231,6 +231,15 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
       : "memory");
 }
 __device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+// Orders this thread's earlier generic-proxy accesses of global memory before its later
+// async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+// The same for shared memory: earlier reads of a buffer before a bulk copy overwrites it.
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 // -------------------------------------------------------------------- reductions ----
 __device__ __forceinline__ float warp_sum(float v) {

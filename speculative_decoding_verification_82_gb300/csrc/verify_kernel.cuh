@@ -186,7 +186,7 @@ struct SlotMeta {
 constexpr int kFinCs = 512;   // chunk statistics of one request staged for its finishing
 constexpr int kFinRows = 64;  // row statistics kept in shared memory for finishing
 struct Shared {
-  uint64_t full[kStages], empty[kStages], pfull[kSlots], pempty[kSlots], fin_bar;
+  uint64_t full[kStages], empty[kStages], pfull[kSlots], pempty[kSlots], fin_bar, cs_bar;
   StageMeta meta[kStages];
   float4 part[kSlots][kGroupWarps];  // warp partials
   SlotMeta pmeta[kSlots];
@@ -750,8 +750,12 @@ struct CsReader {
     return ld_chunkstat(g + (size_t)r * nchunk + c);
   }
 };
-// Copies the chunk statistics of request b into shared memory when they fit (one round trip).
-__device__ __forceinline__ CsReader stage_request_stats(const Params& P, ChunkStat* dst, int b, bool allow) {
+// Copies the chunk statistics of request b into shared memory when they fit: one bulk copy (the
+// block is contiguous, 16-byte aligned, a multiple of 16 bytes), completing on cs_bar.  The
+// caller has acquired the request's count; the proxy fence orders that acquisition before the
+// copy's reads.
+__device__ __forceinline__ CsReader stage_request_stats(const Params& P, Shared& sm, int b, bool allow,
+                                                        uint32_t& csph) {
   const int lane = threadIdx.x & 31;
   const int n = P.rows * P.nchunk;
   CsReader rd;
@@ -759,25 +763,27 @@ __device__ __forceinline__ CsReader stage_request_stats(const Params& P, ChunkSt
   rd.nchunk = P.nchunk;
   rd.s = nullptr;
   if (allow && n <= kFinCs) {
-    constexpr int U = 8;
-    for (int i0 = 0; i0 < n; i0 += 32 * U) {
-      ChunkStat tmp[U];
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * 32 + lane;
-        if (i < n) tmp[u] = ld_chunkstat(rd.g + i);
-      }
-#pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int i = i0 + u * 32 + lane;
-        if (i < n) dst[i] = tmp[u];
-      }
-    }
     __syncwarp();
-    rd.s = dst;
+    if (lane == 0) {
+      fence_proxy_async_global();
+      fence_proxy_async_shared();  // the previous request's reads of fin_cs come first
+      const uint32_t bytes = (uint32_t)n * (uint32_t)sizeof(ChunkStat);
+      mbar_expect_tx(&sm.cs_bar, bytes);
+      tma_load_1d(sm.fin_cs, rd.g, bytes, &sm.cs_bar);
+      mbar_arrive(&sm.cs_bar);
+    }
+    const int zero = 0;
+    bool ok = mbar_wait(&sm.cs_bar, csph & 1u, &zero);
+    if (!ok) {
+      if (lane == 0) raise_abort(P, sm);
+      mbar_wait(&sm.cs_bar, csph & 1u, &zero);
+    }
+    ++csph;
+    rd.s = ok ? sm.fin_cs : nullptr;  // after a timeout, read global memory instead
   }
   return rd;
 }
+
 // Row statistics of request b (shared-memory copy for the first kFinRows rows).
 __device__ __forceinline__ RowStat read_rowstat(const Params& P, const Shared& sm, int b, int r) {
   if (r < kFinRows) return sm.fin_rs[r];
@@ -802,6 +808,8 @@ __device__ int draw_from_chunks(const Params& P, Shared& sm, unsigned char* fbuf
   auto stage_sub = [&](int ch, int sub, int& v0, int& v1) {
     v0 = ch * kChunkVec + sub * kSubVec;
     v1 = min(v0 + kSubVec, g.nvec);
+    __syncwarp();
+    if (lane == 0) fence_proxy_async_shared();  // earlier reads of fbuf before the copy
     warp_stage<T>(fbuf, g, P.V, v0, v1, &sm.fin_bar, lane);
     return fin_wait(P, sm, fph);
   };
@@ -950,7 +958,6 @@ __device__ void combine_rows(const Params& P, Shared& sm, int b, const CsReader&
     if (r < kFinRows) sm.fin_rs[r] = rs;
   }
   __syncwarp();
-  __threadfence();
 }
 
 // l c - mc with the product l c carried exactly (an fp32 pair from one FMA) and the difference
@@ -974,24 +981,43 @@ __device__ __forceinline__ float exp2_times(double x, float f) {
 // Chain / n-gram / greedy-chain finishing: alpha, acceptance scan (section I.1 step 2), outputs,
 // publication of the acceptance result, and the draws made here (bonus row; n-gram residual).
 // Returns the accepted length (or -1 after an error) in every lane.
+// Inputs of request b that do not depend on its statistics, loaded while the finishing warp
+// waits for them (positions k < 32 in lane k): the draft token, its uniform, and the target and
+// draft logits at the token.
+struct ReqPrefetch {
+  int x0;
+  float r0, lx0, dx0;
+};
 template <int MODE, typename T>
-__device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, int b) {
+__device__ __forceinline__ ReqPrefetch prefetch_request(const Params& P, int b) {
+  constexpr int S = Elem<T>::kSize;
+  constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
+  const int lane = threadIdx.x & 31;
+  ReqPrefetch f{0, 0.f, 0.f, 0.f};
+  if (lane < P.K) {
+    f.x0 = __ldg(P.draft_tokens + (size_t)b * P.K + lane);
+    if (kSoftmax) {
+      f.r0 = __ldg(P.r + (size_t)b * P.K + lane);
+      if (f.x0 >= 0 && f.x0 < P.V) {
+        f.lx0 = Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, lane) + (size_t)f.x0 * S));
+        if (MODE == kChain)
+          f.dx0 = Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, P.R + lane) + (size_t)f.x0 * S));
+      }
+    }
+  }
+  return f;
+}
+
+template <int MODE, typename T>
+__device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& csph,
+                            int b, const ReqPrefetch& pf) {
   constexpr int S = Elem<T>::kSize;
   constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
   const int lane = threadIdx.x & 31;
   const int K = P.K;
-  // prefetch (positions k < 32 in lane k): the draft token and uniform, then the logits at it
-  int x0 = 0;
-  float r0 = 0.f, lx0 = 0.f, dx0 = 0.f;
-  if (lane < K) {
-    x0 = __ldg(P.draft_tokens + (size_t)b * K + lane);
-    if (kSoftmax) r0 = __ldg(P.r + (size_t)b * K + lane);
-  }
-  const CsReader rd = stage_request_stats(P, sm.fin_cs, b, true);
-  if (kSoftmax && lane < K && x0 >= 0 && x0 < P.V) {
-    lx0 = Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, lane) + (size_t)x0 * S));
-    if (MODE == kChain) dx0 = Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, P.R + lane) + (size_t)x0 * S));
-  }
+  const int x0 = pf.x0;
+  const float r0 = pf.r0, lx0 = pf.lx0, dx0 = pf.dx0;
+  const CsReader rd = stage_request_stats(P, sm, b, true, csph);
   combine_rows<MODE>(P, sm, b, rd);
   int e = 0;
   for (int k = lane; k < K; k += 32) {
@@ -1065,8 +1091,13 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
     if (P.residual_mass && (err || !kSoftmax)) P.residual_mass[b] = err ? 0.f : 1.f;
     P.req[b].n = n;
     P.req[b].err = err;
-    __threadfence();
-    *reinterpret_cast<volatile int*>(&P.req[b].ready) = 1;
+  }
+  if constexpr (MODE == kChain) {
+    if (P.npos > 0) {  // residual items read n, err and the row statistics: publish them
+      __syncwarp();
+      __threadfence();
+      if (lane == 0) *reinterpret_cast<volatile int*>(&P.req[b].ready) = 1;
+    }
   }
   __syncwarp();
   if constexpr (kSoftmax) {
@@ -1122,6 +1153,8 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
     if (cstar >= 0 && sstar >= 0) {
       const float t = __fsub_rn(__fsub_rn(tgt, bstar), sbase);
       const ResGeo<T> q = res_geo<T>(P, b, k, cstar * kResVec + sstar * kResSub, kResSub);
+      __syncwarp();
+      if (lane == 0) fence_proxy_async_shared();  // earlier reads of fbuf before the copy
       warp_stage<T>(fbuf, q.gt, P.V, q.vt0, q.vt1, &sm.fin_bar, lane);
       warp_stage<T>(fbuf + (size_t)kFinDraftSlot * 16, q.gd, P.V, q.vd0, q.vd1, &sm.fin_bar, lane);
       const bool ok = fin_wait(P, sm, fph);
@@ -1136,7 +1169,8 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
     }
   } else {  // no residual mass: draw from p
     float unused;
-    const CsReader rd = stage_request_stats(P, sm.fin_cs, b, false);
+    uint32_t unused_ph = 0;
+    const CsReader rd = stage_request_stats(P, sm, b, false, unused_ph);
     tok = draw_from_chunks<T>(P, sm, fbuf, fph, b, k, kFullP, -1, rd, ts, &unused);
   }
   if (lane == 0) {
@@ -1158,12 +1192,7 @@ __device__ inline void walk_tree(const Params& P, Shared& sm, int b) {
   const RowStat* rs = P.rstat + (size_t)b * N1;
   const int32_t* par = P.parents + (size_t)b * N1;
   const int32_t* tok = P.node_tokens + (size_t)b * N1;
-  if (N1 <= kFinRows) {  // walk a small tree from shared memory
-    for (int i = lane; i < N1; i += 32) {
-      sm.fin_par[i] = par[i];
-      sm.fin_tok[i] = tok[i];
-    }
-    __syncwarp();
+  if (N1 <= kFinRows) {  // a small tree's parents and tokens were staged in shared memory
     par = sm.fin_par;
     tok = sm.fin_tok;
   }
@@ -1242,19 +1271,30 @@ __device__ __forceinline__ bool wait_count(const Params& P, Shared& sm, const un
   return __shfl_sync(kFull, ok, 0) != 0;
 }
 
-// The finishing warp: requests b = blockIdx.x, blockIdx.x + gridDim.x, ...
+// The finishing warp: requests b = blockIdx.x, blockIdx.x + gridDim.x, ...  The request's
+// inputs are loaded while its chunks are still being read.
 template <int MODE, typename T>
 __device__ void fin_loop(const Params& P, Shared& sm, unsigned char* fbuf) {
-  uint32_t fph = 0;
+  const int lane = threadIdx.x & 31;
+  uint32_t fph = 0, csph = 0;
   const unsigned per_req = (unsigned)(P.rows * P.nchunk);
   for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
-    if (!wait_count(P, sm, P.tick_a + b, per_req)) return;
     if constexpr (MODE == kTree) {
-      const CsReader rd = stage_request_stats(P, sm.fin_cs, b, true);
+      const int N1 = P.R;
+      if (N1 <= kFinRows) {
+        for (int i = lane; i < N1; i += 32) {
+          sm.fin_par[i] = __ldg(P.parents + (size_t)b * N1 + i);
+          sm.fin_tok[i] = __ldg(P.node_tokens + (size_t)b * N1 + i);
+        }
+      }
+      if (!wait_count(P, sm, P.tick_a + b, per_req)) return;
+      const CsReader rd = stage_request_stats(P, sm, b, true, csph);
       combine_rows<MODE>(P, sm, b, rd);
       walk_tree(P, sm, b);
     } else {
-      const int n = finish_chain<MODE, T>(P, sm, fbuf, fph, b);
+      const ReqPrefetch pf = prefetch_request<MODE, T>(P, b);
+      if (!wait_count(P, sm, P.tick_a + b, per_req)) return;
+      const int n = finish_chain<MODE, T>(P, sm, fbuf, fph, csph, b, pf);
       if constexpr (MODE == kChain) {
         if (P.npos > 0 && n >= 0) {
           for (int kk = 0; kk < P.npos; ++kk) {
@@ -1285,6 +1325,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
       sm.pcnt[j] = 0;
     }
     mbar_init(&sm.fin_bar, 1);
+    mbar_init(&sm.cs_bar, 1);
     sm.abort = 0;
     fence_mbar_init();
   }
