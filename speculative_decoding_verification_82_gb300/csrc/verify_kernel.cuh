@@ -184,9 +184,10 @@ struct SlotMeta {
   unsigned* tick;  // the count this chunk adds to (stats and residual items)
 };
 constexpr int kFinCs = 512;   // chunk statistics of one request staged for its finishing
+constexpr int kFinSs = 256;   // sub-chunk statistics of one row staged for a draw
 constexpr int kFinRows = 64;  // row statistics kept in shared memory for finishing
 struct Shared {
-  uint64_t full[kStages], empty[kStages], pfull[kSlots], pempty[kSlots], fin_bar, cs_bar;
+  uint64_t full[kStages], empty[kStages], pfull[kSlots], pempty[kSlots], fin_bar, cs_bar, ss_bar;
   StageMeta meta[kStages];
   float4 part[kSlots][kGroupWarps];  // warp partials
   SlotMeta pmeta[kSlots];
@@ -194,6 +195,7 @@ struct Shared {
   int abort, last;
   double alpha[SPEC_MAX_K];
   ChunkStat fin_cs[kFinCs];
+  ChunkStat fin_ss[kFinSs];
   RowStat fin_rs[kFinRows];
   int fin_par[kFinRows], fin_tok[kFinRows];  // a small tree's parents and tokens
 };
@@ -790,48 +792,95 @@ __device__ __forceinline__ RowStat read_rowstat(const Params& P, const Shared& s
   return ld_rowstat(P.rstat + (size_t)b * P.rows + r);
 }
 
-// Inverse-CDF draw from target row `row` of request b using its chunk statistics: weights p
-// (kFullP) or p without token x (kExcl).  Picks the crossing chunk from the chunk weights, then
-// the crossing sub-chunk from the sub-chunk partials, stages that sub-chunk and searches it.  For
-// kExcl the sub-chunk holding x is staged first and summed without x, so that no weight is ever
-// obtained by subtraction.  Returns the token (every lane) and the residual mass S / Z (taken
-// before any zero-residual fallback).
+// Waits (bounded, ignoring the abort flag so that no copy is left in flight) for phase ph of a
+// finishing-warp barrier that the warp has already arrived on.  Returns false on a timeout.
+__device__ __forceinline__ bool fin_wait_only(const Params& P, Shared& sm, uint64_t* bar, uint32_t& ph) {
+  const int lane = threadIdx.x & 31;
+  const int zero = 0;
+  bool ok = mbar_wait(bar, ph & 1u, &zero);
+  if (!ok) {
+    if (lane == 0) raise_abort(P, sm);
+    mbar_wait(bar, ph & 1u, &zero);
+  }
+  ++ph;
+  return ok;
+}
+
+// A draw from target row `row` of request b by inverse CDF: weights p (kFullP) or p without
+// token x (kExcl).  draw_begin issues the bulk copies the draw needs (the row's sub-chunk
+// statistics; for kExcl the sub-chunk holding x) so that they overlap other work; draw_end picks
+// the crossing chunk from the chunk weights, the crossing sub-chunk from the sub-chunk weights,
+// stages that sub-chunk (unless it is the one already staged) and searches it.  For kExcl the
+// sub-chunk holding x is summed without x, so no weight is ever obtained by subtraction.
+struct DrawPlan {
+  int row, kind, x;
+  int cx, ix;    // kExcl: chunk and sub-chunk holding x
+  int sv0, sv1;  // grid vectors staged in the finishing buffer (sv1 <= sv0: none)
+  bool ss;       // the row's sub-chunk statistics are being staged in fin_ss
+};
 template <typename T>
-__device__ int draw_from_chunks(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, int b, int row,
-                                int kind, int x, const CsReader& rd, const RowStat& rs, float* mass_out) {
+__device__ DrawPlan draw_begin(const Params& P, Shared& sm, unsigned char* fbuf, int b, int row, int kind, int x) {
   constexpr int VE = Elem<T>::kPerVec;
   const int lane = threadIdx.x & 31;
-  const double u = (double)__ldg(P.u + b);
+  DrawPlan d;
+  d.row = row;
+  d.kind = kFullP;
+  d.x = -1;
+  d.cx = d.ix = -1;
+  d.sv0 = d.sv1 = 0;
+  const int nss = P.nchunk * kGroupWarps;
+  d.ss = nss <= kFinSs;
+  __syncwarp();
+  if (lane == 0) {
+    fence_proxy_async_global();  // the statistics were acquired with the request's count
+    fence_proxy_async_shared();  // earlier reads of fin_ss and the finishing buffer come first
+    if (d.ss) {
+      const uint32_t bytes = (uint32_t)nss * (uint32_t)sizeof(ChunkStat);
+      mbar_expect_tx(&sm.ss_bar, bytes);
+      tma_load_1d(sm.fin_ss, P.sstat + ((size_t)b * P.rows + row) * nss, bytes, &sm.ss_bar);
+      mbar_arrive(&sm.ss_bar);
+    }
+  }
+  if (kind == kExcl && x >= 0 && x < P.V) {
+    const RowGrid<T> g = row_grid<T>(row_ptr<T>(P, b, row), P.V);
+    const int pv = (x + g.phase) / VE;
+    d.kind = kExcl;
+    d.x = x;
+    d.cx = pv / kChunkVec;
+    d.ix = (pv - d.cx * kChunkVec) / kSubVec;
+    d.sv0 = d.cx * kChunkVec + d.ix * kSubVec;
+    d.sv1 = min(d.sv0 + kSubVec, g.nvec);
+    warp_stage<T>(fbuf, g, P.V, d.sv0, d.sv1, &sm.fin_bar, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.fin_bar);
+  }
+  return d;
+}
+
+template <typename T>
+__device__ int draw_end(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph, int b,
+                        const DrawPlan& d, const CsReader& rd, const RowStat& rs, float u, float* mass_out) {
+  constexpr int VE = Elem<T>::kPerVec;
+  const int lane = threadIdx.x & 31;
   const float c = P.c, mc = rs.mc;
+  const int row = d.row;
   const RowGrid<T> g = row_grid<T>(row_ptr<T>(P, b, row), P.V);
   const ChunkStat* srow = P.sstat + ((size_t)b * P.rows + row) * P.nchunk * kGroupWarps;
-  auto stage_sub = [&](int ch, int sub, int& v0, int& v1) {
-    v0 = ch * kChunkVec + sub * kSubVec;
-    v1 = min(v0 + kSubVec, g.nvec);
-    __syncwarp();
-    if (lane == 0) fence_proxy_async_shared();  // earlier reads of fbuf before the copy
-    warp_stage<T>(fbuf, g, P.V, v0, v1, &sm.fin_bar, lane);
-    return fin_wait(P, sm, fph);
-  };
   bool ok = true;
-  int staged_ch = -1, staged_sub = -1, sv0 = 0, sv1 = 0;
-  // kExcl: the chunk and sub-chunk holding x; lane i < kGroupWarps keeps sub-chunk i's weight in
-  // that chunk, with x left out of sub-chunk ix (summed from the staged sub-chunk, never by
-  // subtraction)
-  int cx = -1, ix = -1;
+  if (d.ss) ok = fin_wait_only(P, sm, &sm.ss_bar, ssph);
+  if (d.kind == kExcl) ok = fin_wait_only(P, sm, &sm.fin_bar, fph) && ok;
+  auto sub_weight = [&](int ch, int i) {
+    const ChunkStat q = d.ss ? sm.fin_ss[ch * kGroupWarps + i] : ld_chunkstat(srow + (size_t)ch * kGroupWarps + i);
+    return chunk_weight(q.a, q.s, c, mc);
+  };
+  int sv0 = d.sv0, sv1 = d.sv1;
+  int staged_ch = d.cx, staged_sub = d.ix;
+  // kExcl: lane i < kGroupWarps keeps sub-chunk i's weight in chunk cx, with x left out of
+  // sub-chunk ix (summed from the staged sub-chunk)
+  const int cx = d.cx, ix = d.ix;
   float wsub_x = 0.f, wcx = 0.f;
-  if (kind == kExcl && x >= 0 && x < P.V) {
-    const int pv = (x + g.phase) / VE;
-    cx = pv / kChunkVec;
-    ix = (pv - cx * kChunkVec) / kSubVec;
-    float wl = 0.f;
-    if (lane < kGroupWarps && lane != ix) {
-      const ChunkStat q = ld_chunkstat(srow + (size_t)cx * kGroupWarps + lane);
-      wl = chunk_weight(q.a, q.s, c, mc);
-    }
-    ok = stage_sub(cx, ix, sv0, sv1);
-    staged_ch = cx;
-    staged_sub = ix;
+  if (d.kind == kExcl) {
+    const float wl = (lane < kGroupWarps && lane != ix) ? sub_weight(cx, lane) : 0.f;
     const int e_base = sv0 * VE - g.phase;
     float part = 0.f;
     for (int v = lane; v < sv1 - sv0; v += 32) {
@@ -839,7 +888,7 @@ __device__ int draw_from_chunks(const Params& P, Shared& sm, unsigned char* fbuf
       Elem<T>::unpack(lds128(fbuf + (size_t)v * 16), f);
       float vs = 0.f;
 #pragma unroll
-      for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, e_base + v * VE + j == x ? 0.f : ex2(__fmaf_rn(f[j], c, -mc)));
+      for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, e_base + v * VE + j == d.x ? 0.f : ex2(__fmaf_rn(f[j], c, -mc)));
       part = __fadd_rn(part, vs);
     }
     const float wx = warp_sum(part);
@@ -849,7 +898,7 @@ __device__ int draw_from_chunks(const Params& P, Shared& sm, unsigned char* fbuf
     for (int o = 1; o < kGroupWarps; o <<= 1) t = __fadd_rn(t, __shfl_xor_sync(kFull, t, o));
     wcx = __shfl_sync(kFull, t, 0);
   }
-  int k2 = cx >= 0 ? kExcl : kFullP;
+  int k2 = d.kind;
   auto weight = [&](int ch) {
     if (k2 == kExcl && ch == cx) return wcx;
     const ChunkStat q = rd(row, ch);
@@ -864,24 +913,31 @@ __device__ int draw_from_chunks(const Params& P, Shared& sm, unsigned char* fbuf
   *mass_out = (float)((double)S0 / rs.Z);
   int cstar;
   float bstar;
-  const float tgt = __fmul_rn((float)u, S);
+  const float tgt = __fmul_rn(u, S);
   select_part(P.nchunk, tgt, weight, cstar, bstar);
   if (cstar < 0) return -1;
   const bool subx = k2 == kExcl && cstar == cx;
-  const ChunkStat* sp = srow + (size_t)cstar * kGroupWarps;
   auto sweight = [&](int i) {  // select_part evaluates part i in lane i
     if (subx) return wsub_x;
-    const ChunkStat q = ld_chunkstat(sp + i);
-    return chunk_weight(q.a, q.s, c, mc);
+    return sub_weight(cstar, i);
   };
   int sstar;
   float sbase;
   select_part(kGroupWarps, __fsub_rn(tgt, bstar), sweight, sstar, sbase);
   if (sstar < 0) return -1;  // cannot happen: the chunk holds positive weight
   const float t = __fsub_rn(__fsub_rn(tgt, bstar), sbase);
-  if (cstar != staged_ch || sstar != staged_sub) ok = stage_sub(cstar, sstar, sv0, sv1) && ok;
+  if (cstar != staged_ch || sstar != staged_sub) {
+    sv0 = cstar * kChunkVec + sstar * kSubVec;
+    sv1 = min(sv0 + kSubVec, g.nvec);
+    __syncwarp();
+    if (lane == 0) fence_proxy_async_shared();  // earlier reads of fbuf before the copy
+    warp_stage<T>(fbuf, g, P.V, sv0, sv1, &sm.fin_bar, lane);
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&sm.fin_bar);
+    ok = fin_wait_only(P, sm, &sm.fin_bar, fph) && ok;
+  }
   const int e_base = sv0 * VE - g.phase;
-  const int xe = (k2 == kExcl) ? x : -1;
+  const int xe = (k2 == kExcl) ? d.x : -1;
   auto wf = [&](int v, float (&w)[VE]) {
     float f[VE];
     Elem<T>::unpack(lds128(fbuf + (size_t)v * 16), f);
@@ -986,14 +1042,15 @@ __device__ __forceinline__ float exp2_times(double x, float f) {
 // draft logits at the token.
 struct ReqPrefetch {
   int x0;
-  float r0, lx0, dx0;
+  float r0, lx0, dx0, u;
 };
 template <int MODE, typename T>
 __device__ __forceinline__ ReqPrefetch prefetch_request(const Params& P, int b) {
   constexpr int S = Elem<T>::kSize;
   constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
   const int lane = threadIdx.x & 31;
-  ReqPrefetch f{0, 0.f, 0.f, 0.f};
+  ReqPrefetch f{0, 0.f, 0.f, 0.f, 0.f};
+  if (kSoftmax) f.u = __ldg(P.u + b);
   if (lane < P.K) {
     f.x0 = __ldg(P.draft_tokens + (size_t)b * P.K + lane);
     if (kSoftmax) {
@@ -1010,7 +1067,7 @@ __device__ __forceinline__ ReqPrefetch prefetch_request(const Params& P, int b) 
 
 template <int MODE, typename T>
 __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& csph,
-                            int b, const ReqPrefetch& pf) {
+                            uint32_t& ssph, int b, const ReqPrefetch& pf) {
   constexpr int S = Elem<T>::kSize;
   constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
   const int lane = threadIdx.x & 31;
@@ -1075,6 +1132,15 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
       }
     }
   }
+  // The emitted token's draw (n-gram at any n, the bonus row of a draft-model chain) starts its
+  // copies now, so that they overlap the outputs and the publication below.
+  const bool early = kSoftmax && !err && !P.diag && (MODE == kNgram || n == K);
+  DrawPlan dp{};
+  if (early) {
+    int xn = __shfl_sync(kFull, x0, n < 32 ? n : 0);
+    if (n >= 32 && n < K) xn = __ldg(P.draft_tokens + (size_t)b * K + n);
+    dp = draw_begin<T>(P, sm, fbuf, b, n, (MODE == kNgram && n < K) ? kExcl : kFullP, n < K ? xn : -1);
+  }
   for (int i = lane; i <= K; i += 32) {
     const size_t o_i = (size_t)b * (K + 1) + i;
     int o = -1;
@@ -1102,16 +1168,7 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
   __syncwarp();
   if constexpr (kSoftmax) {
     if (err) return -1;
-    // draws made here: the bonus row (both modes) and the n-gram residual; with per-position
-    // outputs requested every such position, otherwise only the emitted one
-    const int kfirst = P.diag ? (MODE == kChain ? K : 0) : n;
-    const int klast = P.diag ? K : n;
-    for (int k = kfirst; k <= klast; ++k) {
-      if (MODE == kChain && k < K) continue;  // residual work items draw from max(0, p - q)
-      const int kind = (MODE == kNgram && k < K) ? kExcl : kFullP;
-      const int x = k < K ? __ldg(P.draft_tokens + (size_t)b * K + k) : -1;
-      float mass;
-      const int tok = draw_from_chunks<T>(P, sm, fbuf, fph, b, k, kind, x, rd, read_rowstat(P, sm, b, k), &mass);
+    auto emit = [&](int k, int tok, float mass) {
       if (lane == 0) {
         const size_t o_k = (size_t)b * (K + 1) + k;
         if (k == n) {
@@ -1121,6 +1178,22 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
         if (P.cand_tokens) P.cand_tokens[o_k] = tok;
         if (P.pos_mass) P.pos_mass[o_k] = mass;
       }
+    };
+    if (early) {
+      float mass;
+      const int tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, dp, rd, read_rowstat(P, sm, b, n), pf.u, &mass);
+      emit(n, tok, mass);
+    } else if (P.diag) {
+      // per-position outputs: a draw at every position made here (the bonus row, and for
+      // n-gram every residual; draft-model residuals are drawn by residual work items)
+      for (int k = MODE == kChain ? K : 0; k <= K; ++k) {
+        const int kind = (MODE == kNgram && k < K) ? kExcl : kFullP;
+        const int x = k < K ? __ldg(P.draft_tokens + (size_t)b * K + k) : -1;
+        const DrawPlan d = draw_begin<T>(P, sm, fbuf, b, k, kind, x);
+        float mass;
+        const int tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, d, rd, read_rowstat(P, sm, b, k), pf.u, &mass);
+        emit(k, tok, mass);
+      }
     }
   }
   return err ? -1 : n;
@@ -1129,8 +1202,8 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
 // Draft-model chain: the draw from max(0, p_k - q_k) once every residual item of (b, position
 // slot kk) is in.
 template <typename T>
-__device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, int b, int kk,
-                              int n) {
+__device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph,
+                              int b, int kk, int n) {
   constexpr int VE = Elem<T>::kPerVec;
   const int lane = threadIdx.x & 31;
   const int k = P.diag ? kk : n;
@@ -1171,7 +1244,8 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
     float unused;
     uint32_t unused_ph = 0;
     const CsReader rd = stage_request_stats(P, sm, b, false, unused_ph);
-    tok = draw_from_chunks<T>(P, sm, fbuf, fph, b, k, kFullP, -1, rd, ts, &unused);
+    const DrawPlan d = draw_begin<T>(P, sm, fbuf, b, k, kFullP, -1);
+    tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, d, rd, ts, u, &unused);
   }
   if (lane == 0) {
     const size_t o_k = (size_t)b * (P.K + 1) + k;
@@ -1276,7 +1350,7 @@ __device__ __forceinline__ bool wait_count(const Params& P, Shared& sm, const un
 template <int MODE, typename T>
 __device__ void fin_loop(const Params& P, Shared& sm, unsigned char* fbuf) {
   const int lane = threadIdx.x & 31;
-  uint32_t fph = 0, csph = 0;
+  uint32_t fph = 0, csph = 0, ssph = 0;
   const unsigned per_req = (unsigned)(P.rows * P.nchunk);
   for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
     if constexpr (MODE == kTree) {
@@ -1294,13 +1368,13 @@ __device__ void fin_loop(const Params& P, Shared& sm, unsigned char* fbuf) {
     } else {
       const ReqPrefetch pf = prefetch_request<MODE, T>(P, b);
       if (!wait_count(P, sm, P.tick_a + b, per_req)) return;
-      const int n = finish_chain<MODE, T>(P, sm, fbuf, fph, csph, b, pf);
+      const int n = finish_chain<MODE, T>(P, sm, fbuf, fph, csph, ssph, b, pf);
       if constexpr (MODE == kChain) {
         if (P.npos > 0 && n >= 0) {
           for (int kk = 0; kk < P.npos; ++kk) {
             if (!P.diag && n >= P.K) break;  // everything accepted: the bonus draw was made above
             if (!wait_count(P, sm, P.tick_b + (size_t)b * P.npos + kk, (unsigned)P.nchunk_r)) return;
-            residual_draw<T>(P, sm, fbuf, fph, b, kk, n);
+            residual_draw<T>(P, sm, fbuf, fph, ssph, b, kk, n);
           }
         }
       }
@@ -1326,6 +1400,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
     }
     mbar_init(&sm.fin_bar, 1);
     mbar_init(&sm.cs_bar, 1);
+    mbar_init(&sm.ss_bar, 1);
     sm.abort = 0;
     fence_mbar_init();
   }
