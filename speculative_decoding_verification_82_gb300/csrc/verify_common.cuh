@@ -231,6 +231,13 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
       : "memory");
 }
 __device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
+// Load with acquire semantics at GPU scope: later reads see what the writer published before it
+// released the value (no fence, so earlier stores of this thread need not drain first).
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
 // Orders this thread's earlier generic-proxy accesses of global memory before its later
 // async-proxy (bulk copy) accesses.
 __device__ __forceinline__ void fence_proxy_async_global() {

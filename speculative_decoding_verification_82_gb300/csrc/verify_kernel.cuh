@@ -54,14 +54,24 @@ struct __align__(16) RowStat {
   int amax;  // argmax modes: row argmax
   int pad[3];
 };
-// Per request: the acceptance result, published (ready = 1) for the residual work items.
+// Per request: the acceptance result as four self-validating 64-bit words (each a single-copy
+// atomic store whose low half is kReqTag), so that readers need no fence and no other read:
+// w[0] = n | err << 16 in the high half; w[1..3] = the fp32 bits of RN(m_t c), RN(m_d c) and
+// Z_t / Z_d at row n (draft-model chains that rejected, without per-position outputs).  The
+// workspace clearing at the start of every call zeroes them.
 struct __align__(16) ReqState {
-  int n;    // accepted prefix length
-  int err;  // SPEC_ERRF_* bits
-  int ready;
-  int pad;
+  unsigned long long w[4];
 };
-static_assert(sizeof(ChunkStat) == 16 && sizeof(RowStat) == 32 && sizeof(ReqState) == 16, "layout");
+constexpr unsigned kReqTag = 0x5EC0DE01u;
+static_assert(sizeof(ChunkStat) == 16 && sizeof(RowStat) == 32 && sizeof(ReqState) == 32, "layout");
+__device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned long long* p) {
+  return *reinterpret_cast<const volatile unsigned long long*>(p);
+}
+__device__ __forceinline__ void st_volatile_u64(unsigned long long* p, unsigned long long v) {
+  *reinterpret_cast<volatile unsigned long long*>(p) = v;
+}
+__device__ __forceinline__ bool req_word_ok(unsigned long long v) { return (unsigned)v == kReqTag; }
+__device__ __forceinline__ unsigned req_word_hi(unsigned long long v) { return (unsigned)(v >> 32); }
 
 struct Params {
   const void* target;
@@ -310,12 +320,15 @@ template <int MODE, typename T>
 __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages, int grp) {
   constexpr int VE = Elem<T>::kPerVec;
   const int lane = threadIdx.x & 31;
-  // claims: kClaim consecutive items per atomic, the next batch claimed one batch ahead
+  // claims: kClaim consecutive items at a time, the next batch claimed one batch ahead.  Each
+  // producer's first batch is fixed (items kClaim * (blockIdx.x * kGroups + grp) ...), so that its
+  // first copies start without waiting for an atomic; the counter hands out the items after those.
+  const unsigned fixed = (unsigned)kClaim * gridDim.x * (unsigned)kGroups;
   unsigned cur = 0, nxt = 0;
   int pos = 0;
   if (lane == 0) {
-    cur = atomicAdd(P.work, (unsigned)kClaim);
-    nxt = atomicAdd(P.work, (unsigned)kClaim);
+    cur = (unsigned)kClaim * (blockIdx.x * (unsigned)kGroups + (unsigned)grp);
+    nxt = fixed + atomicAdd(P.work, (unsigned)kClaim);
   }
   int it = grp;
   // residual parameters of the last request seen (consecutive residual items share them)
@@ -332,7 +345,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
       pos = 0;
       if (lane == 0) {
         cur = nxt;
-        if (cur < P.total) nxt = atomicAdd(P.work, (unsigned)kClaim);
+        if (cur < P.total) nxt = fixed + atomicAdd(P.work, (unsigned)kClaim);
       }
     }
     unsigned char* buf = stages + (size_t)s * kStageBytes;
@@ -356,34 +369,55 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
       m.kk = (int)fdiv((unsigned)off, P.fd_nchunk_r);
       m.ch = off - m.kk * P.nchunk_r;
       if (m.b != rb || P.diag) {
-        // the request's acceptance result (published by the finishing warp of its owner CTA)
+        // the request's acceptance result, published by the finishing warp of its owner CTA
+        unsigned long long w0 = 0, w1 = 0, w2 = 0, w3 = 0;
         int ready = 0;
         if (lane == 0) {
+          const unsigned long long* rw = P.req[m.b].w;
           const long long t0 = clock64();
           for (;;) {
-            ready = ld_volatile(&P.req[m.b].ready);
+            w0 = ld_volatile_u64(rw);
+            if (req_word_ok(w0)) {
+              const unsigned hi = req_word_hi(w0);
+              const int n = (int)(hi & 0xFFFFu), err = (int)(hi >> 16);
+              if (err || P.diag || n >= P.K) {
+                ready = 1;
+              } else {
+                w1 = ld_volatile_u64(rw + 1);
+                w2 = ld_volatile_u64(rw + 2);
+                w3 = ld_volatile_u64(rw + 3);
+                ready = req_word_ok(w1) && req_word_ok(w2) && req_word_ok(w3);
+              }
+            }
             if (ready || aborted(sm)) break;
             if (clock64() - t0 > kWaitLimitCycles) {
               raise_abort(P, sm);
               break;
             }
-            __nanosleep(128);
+            __nanosleep(64);
           }
-          __threadfence();
+          if (P.diag) __threadfence();  // per-position parameters come from the row statistics
         }
         ready = __shfl_sync(kFull, ready, 0);
+        const unsigned h0 = __shfl_sync(kFull, req_word_hi(w0), 0);
         rb = m.b;
         rerr = 1;
         if (ready) {
-          const int n = __ldcg(&P.req[m.b].n);
-          rerr = __ldcg(&P.req[m.b].err);
+          const int n = (int)(h0 & 0xFFFFu);
+          rerr = (int)(h0 >> 16);
           rk = P.diag ? m.kk : n;
           if (!rerr && rk < P.K) {
-            const RowStat ts = ld_rowstat(P.rstat + (size_t)m.b * P.rows + rk);
-            const RowStat ds = ld_rowstat(P.rstat + (size_t)m.b * P.rows + P.R + rk);
-            rmct = ts.mc;
-            rmcd = ds.mc;
-            rrho = __fdiv_rn((float)ts.Z, (float)ds.Z);  // max(0, p - q) Z_t = max(0, e - f Z_t / Z_d)
+            if (P.diag) {
+              const RowStat ts = ld_rowstat(P.rstat + (size_t)m.b * P.rows + rk);
+              const RowStat ds = ld_rowstat(P.rstat + (size_t)m.b * P.rows + P.R + rk);
+              rmct = ts.mc;
+              rmcd = ds.mc;
+              rrho = __fdiv_rn((float)ts.Z, (float)ds.Z);  // max(0, p - q) Z_t = max(0, e - f Z_t / Z_d)
+            } else {
+              rmct = __uint_as_float(__shfl_sync(kFull, req_word_hi(w1), 0));
+              rmcd = __uint_as_float(__shfl_sync(kFull, req_word_hi(w2), 0));
+              rrho = __uint_as_float(__shfl_sync(kFull, req_word_hi(w3), 0));
+            }
           }
         }
       }
@@ -1155,15 +1189,20 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
     P.num_accepted[b] = n;
     if (P.err_flags) P.err_flags[b] = err;
     if (P.residual_mass && (err || !kSoftmax)) P.residual_mass[b] = err ? 0.f : 1.f;
-    P.req[b].n = n;
-    P.req[b].err = err;
   }
-  if constexpr (MODE == kChain) {
-    if (P.npos > 0) {  // residual items read n, err and the row statistics: publish them
-      __syncwarp();
-      __threadfence();
-      if (lane == 0) *reinterpret_cast<volatile int*>(&P.req[b].ready) = 1;
+  // publication of the acceptance result (read by residual work items and the probability rows)
+  if (MODE == kChain && P.npos > 0 && P.diag) {  // per-position residuals read the row statistics
+    __syncwarp();
+    __threadfence();
+  }
+  const bool resid = MODE == kChain && P.npos > 0 && !P.diag && !err && n < K;
+  if (lane == 0 || (resid && lane < 4)) {
+    unsigned hi = (unsigned)n | ((unsigned)err << 16);
+    if (lane > 0) {
+      const RowStat t = read_rowstat(P, sm, b, n), d = read_rowstat(P, sm, b, P.R + n);
+      hi = __float_as_uint(lane == 1 ? t.mc : lane == 2 ? d.mc : __fdiv_rn((float)t.Z, (float)d.Z));
     }
+    st_volatile_u64(P.req[b].w + lane, ((unsigned long long)hi << 32) | kReqTag);
   }
   __syncwarp();
   if constexpr (kSoftmax) {
@@ -1322,14 +1361,15 @@ __device__ inline void walk_tree(const Params& P, Shared& sm, int b) {
   }
 }
 
-// Waits (bounded) until *count reaches `want`; false on a timeout or abort.
+// Waits (bounded) until *count reaches `want`; false on a timeout or abort.  The count is read
+// with acquire semantics, so the statistics counted before it are visible afterwards.
 __device__ __forceinline__ bool wait_count(const Params& P, Shared& sm, const unsigned* count, unsigned want) {
   const int lane = threadIdx.x & 31;
   int ok = 0;
   if (lane == 0) {
     const long long t0 = clock64();
     for (;;) {
-      if ((unsigned)ld_volatile(reinterpret_cast<const int*>(count)) >= want) {
+      if (ld_acquire_u32(count) >= want) {
         ok = 1;
         break;
       }
@@ -1338,9 +1378,8 @@ __device__ __forceinline__ bool wait_count(const Params& P, Shared& sm, const un
         raise_abort(P, sm);
         break;
       }
-      __nanosleep(128);
+      __nanosleep(64);
     }
-    __threadfence();  // acquire: every chunk's statistics
   }
   return __shfl_sync(kFull, ok, 0) != 0;
 }
@@ -1446,7 +1485,8 @@ template <typename T>
 __global__ void __launch_bounds__(256) probs_kernel(const Params P) {
   const int rowid = blockIdx.x;  // b * rows + r
   const int b = rowid / P.rows, r = rowid - b * P.rows;
-  if (P.req[b].err) return;
+  const unsigned long long w0 = P.req[b].w[0];
+  if (!req_word_ok(w0) || (req_word_hi(w0) >> 16) != 0u) return;  // no result, or an error
   float* out = r < P.R ? (P.target_probs ? P.target_probs + ((size_t)b * P.R + r) * P.V : nullptr)
                        : (P.draft_probs ? P.draft_probs + ((size_t)b * P.K + (r - P.R)) * P.V : nullptr);
   if (!out) return;
