@@ -4,8 +4,8 @@
 // spec_verify_{f32,bf16,f16}.cu).  No call allocates memory or synchronises the host.
 #include <math.h>
 #include <stdint.h>
-#include <stdlib.h>
 
+#include <atomic>
 #include <climits>
 
 #include "spec_verify.h"
@@ -44,15 +44,16 @@ Chunking plan_chunks(int V, int S) {
 }
 
 // Workspace layout:
-//   work, gerr, exit_tick, pad   u32 x 4            } one region, cleared by one
-//   tick_a  [B] u32              request tickets    } cudaMemsetAsync per call
+//   work, gerr, exit_tick        u32 (128 B line)   } one region, cleared by one
+//   rc                           u32 (128 B line)   } cudaMemsetAsync per call
+//   tick_a  [B] u32              request tickets    }
 //   tick_b  [B][rows] u32        residual tickets   }
 //   req     [B]                  ReqState           }  (16-byte aligned)
 //   cstat   [B][rows][nchunk]    ChunkStat          (256-byte aligned regions from here on)
 //   sstat   [B][rows][nchunk][G] ChunkStat          sub-chunk partials (G consumer warps a group)
 //   rstat   [B][rows]            RowStat
-//   wsum    [B][rows][nchunk_r]  float
-//   wsub    [B][rows][nchunk_r][G] float
+//   wsum    [B][rows][nchunk_r]  TagSum (float and tag)
+//   wsub    [B][rows][nchunk_r][G] TagSum
 struct Layout {
   size_t work, tick_a, tick_b, req, clear_end, cstat, sstat, rstat, wsum, wsub, total;
 };
@@ -62,7 +63,7 @@ Layout layout(int B, int rows, const Chunking& ck) {
   const size_t b = (size_t)B, r = (size_t)rows;
   size_t off = 0;
   L.work = off;
-  off += 16;
+  off += 2 * 128;
   L.tick_a = off;
   off += b * 4;
   L.tick_b = off;
@@ -79,9 +80,9 @@ Layout layout(int B, int rows, const Chunking& ck) {
   L.rstat = off;
   off = align_up(off + b * r * sizeof(RowStat), 256);
   L.wsum = off;
-  off = align_up(off + b * r * (size_t)ck.nchunk_r * sizeof(float), 256);
+  off = align_up(off + b * r * (size_t)ck.nchunk_r * sizeof(specv::TagSum), 256);
   L.wsub = off;
-  off = align_up(off + b * r * (size_t)ck.nchunk_r * G * sizeof(float), 256);
+  off = align_up(off + b * r * (size_t)ck.nchunk_r * G * sizeof(specv::TagSum), 256);
   L.total = off;
   return L;
 }
@@ -109,6 +110,7 @@ spec_status_t attach_workspace(Params& P, void* ws, size_t bytes, int B, int row
   P.work = reinterpret_cast<unsigned*>(w + L.work);
   P.gerr = P.work + 1;
   P.exit_tick = P.work + 2;
+  P.rc = reinterpret_cast<unsigned*>(w + L.work + 128);  // residual cursor (a line of its own)
   P.tick_a = reinterpret_cast<unsigned*>(w + L.tick_a);
   P.tick_b = reinterpret_cast<unsigned*>(w + L.tick_b);
   P.req = reinterpret_cast<ReqState*>(w + L.req);
@@ -116,22 +118,9 @@ spec_status_t attach_workspace(Params& P, void* ws, size_t bytes, int B, int row
   P.cstat = reinterpret_cast<ChunkStat*>(w + L.cstat);
   P.sstat = reinterpret_cast<ChunkStat*>(w + L.sstat);
   P.rstat = reinterpret_cast<RowStat*>(w + L.rstat);
-  P.wsum = reinterpret_cast<float*>(w + L.wsum);
-  P.wsub = reinterpret_cast<float*>(w + L.wsub);
+  P.wsum = reinterpret_cast<specv::TagSum*>(w + L.wsum);
+  P.wsub = reinterpret_cast<specv::TagSum*>(w + L.wsub);
   return SPEC_OK;
-}
-
-// Requests between a request's stats items and its residual items.  A producer that reaches a
-// residual item before its request's acceptance result is published waits, and measured on GB300
-// that waiting costs more than reading the rejected pair again from HBM instead of L2; so by
-// default every residual item follows every stats item (lag = B).  SPEC_VERIFY_RESID_LAG
-// overrides it (tuning).
-int residual_lag(int B) {
-  static const int env = [] {
-    const char* s = getenv("SPEC_VERIFY_RESID_LAG");
-    return s ? atoi(s) : -1;
-  }();
-  return (env >= 0 && env < B) ? env : B;
 }
 
 // Constants of the item decoding's divisions (see fastdiv.h).
@@ -140,12 +129,21 @@ void set_divisors(Params& P, int rows) {
   const unsigned R = (unsigned)P.npos * (unsigned)P.nchunk_r;
   P.fd_A = specv::make_fastdiv(A);
   P.fd_R = specv::make_fastdiv(R > 0 ? R : 1u);
-  P.fd_AR = specv::make_fastdiv(A + R);
   P.fd_nchunk = specv::make_fastdiv((unsigned)P.nchunk);
   P.fd_nchunk_r = specv::make_fastdiv((unsigned)P.nchunk_r);
 }
 
+// A fresh tag for every call (never 0, the value of cleared memory): the statistics a call writes
+// carry it, so that its readers can tell them from what earlier calls left in the workspace.
+unsigned next_call_tag() {
+  static std::atomic<unsigned> counter{0};
+  unsigned t = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  if (t == 0u) t = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
+  return t;
+}
+
 spec_status_t launch(spec_dtype_t dtype, int mode, Params& P, specv::LaunchPlan& L, cudaStream_t stream) {
+  P.tag = next_call_tag();
   L.smem = (size_t)specv::kStages * specv::kStageBytes + specv::kFinBytes;
   // the ticket counters and acceptance flags start every call at zero, whatever the workspace
   // held before
@@ -194,8 +192,8 @@ spec_status_t verify_chain_common(bool ngram, const void* target, const void* dr
   int device = -1;
   const int sms = sm_count(&device);
   if (sms <= 0) return SPEC_ERR_CUDA;
-  P.total = (unsigned)(B * per_req);
-  P.lag = P.npos ? residual_lag(B) : 0;
+  P.total = (unsigned)((long long)B * rows * ck.nchunk);
+  P.total_r = (unsigned)((long long)B * P.npos * ck.nchunk_r);
   set_divisors(P, rows);
   P.target = target;
   P.draft = two_rows ? draft : nullptr;

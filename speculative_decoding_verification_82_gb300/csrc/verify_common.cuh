@@ -1,6 +1,6 @@
 // verify_common.cuh -- element formats, PTX wrappers (mbarrier, bulk TMA copies), warp
-// reductions, row staging and the warp-level inverse-CDF search used by the verification kernel
-// (sm_103a).
+// reductions, row staging, and the finishing group's barriers, reductions and inverse-CDF search
+// used by the verification kernel (sm_103a).
 #pragma once
 
 #include <cuda_bf16.h>
@@ -16,15 +16,18 @@ namespace specv {
 // One CTA per SM, warp-specialised: two groups of eight consumer warps reduce staged chunks (the
 // groups take alternate stages; four consumer warps per SM sub-partition hide the latency of the
 // special-function unit), one producer warp per group claims work and drives the bulk copies,
-// one bookkeeping warp publishes per-chunk results and counts them per request, one finishing
-// warp completes the requests assigned to this CTA.
+// one bookkeeping warp publishes per-chunk results and counts them per request, and a group of
+// four finishing warps (one per sub-partition) completes the requests assigned to this CTA.
 constexpr int kConsWarps = 16;
 constexpr int kGroups = 2;
 constexpr int kGroupWarps = kConsWarps / kGroups;
 constexpr int kProducerWarp = 16;  // and 17
 constexpr int kBookWarp = 18;
-constexpr int kFinWarp = 19;
-constexpr int kThreads = 20 * 32;
+constexpr int kFinWarp = 19;   // first of the finishing group's warps
+constexpr int kFinWarps = 4;
+constexpr int kFinThreads = kFinWarps * 32;
+constexpr int kFinBarrier = 1;  // named barrier of the finishing group (0 is __syncthreads)
+constexpr int kThreads = (kFinWarp + kFinWarps) * 32;
 constexpr int kStages = 6;                         // staged-chunk ring depth (a multiple of kGroups)
 constexpr int kSlots = 16;                         // ring of per-chunk results (partials, merged)
 constexpr int kClaim = 4;                          // work items claimed per atomic
@@ -44,6 +47,7 @@ constexpr long long kWaitLimitCycles = 4000000000LL;  // ~2 s at GB300 clocks
 static_assert(kVecPerLane * 32 == kSubVec && kResSub % 32 == 0, "warp split");
 static_assert(kStageVec >= kChunkVec && kStageVec >= kDraftSlot + kResVec + 1, "stage size");
 static_assert(kFinVec >= kSubVec && kFinVec >= kFinDraftSlot + kResSub + 1, "finishing buffer size");
+static_assert(kSubVec <= 2 * kFinThreads && kResSub <= 2 * kFinThreads, "a staged sub-chunk is two vectors per finishing thread");
 static_assert(kStageBytes % 128 == 0 && kFinBytes % 128 == 0, "alignment");
 static_assert(kStages % kGroups == 0 && kSlots % kGroups == 0, "a stage and a slot always serve the same group");
 
@@ -347,80 +351,102 @@ __device__ __forceinline__ void warp_stage(unsigned char* dst, const RowGrid<T>&
   }
 }
 
-// ---------------------------------------------------------------- inverse-CDF search ----
-// One warp finds, in a staged range of `nvec` vectors, the element where the running weight taken
-// in index order first exceeds t; wf(v, w) fills the VE weights of vector v.  The range is cut
-// into 32 blocks of Bs consecutive vectors (Bs a multiple of 8, so that the lanes' rotated reads
-// hit distinct shared-memory banks); each lane sums one block, a warp scan over the block sums
-// picks the crossing block, the lanes then split that block (q consecutive vectors each), and a
-// second scan picks the lane, then the vector, then the element.  At every level the first part
-// with positive weight whose running total exceeds t is taken, otherwise the last part with
-// positive weight (rounding), so a zero-weight element is never returned.  Returns the position
-// (vector * VE + element) in every lane, or -1 when the range holds no positive weight.
-template <int VE, typename WF>
-__device__ int warp_crossing(int nvec, float t, WF wf) {
-  const int lane = threadIdx.x & 31;
-  if (nvec <= 0) return -1;
-  const int Bs = ((nvec + 31) / 32 + 7) / 8 * 8;  // vectors per block
-  // level 1: block sums
-  float bsum = 0.f;
-  {
-    const int v0 = lane * Bs;
-    for (int i = 0; i < Bs; ++i) {
-      int r = i + (lane & 7);  // rotated start: the 8 lanes of a quarter-warp hit distinct banks
-      r -= (r >= Bs) ? Bs : 0;
-      const int v = v0 + r;
-      if (v < nvec) {
-        float w[VE];
-        wf(v, w);
-        float vs = 0.f;
+// ------------------------------------------------------------------ finishing group ----
+// The kFinWarps finishing warps synchronise on named barrier kFinBarrier.
+__device__ __forceinline__ int fin_thread() { return (int)threadIdx.x - kFinWarp * 32; }
+__device__ __forceinline__ void fin_sync() {
+  asm volatile("bar.sync %0, %1;" ::"n"(kFinBarrier), "n"(kFinThreads) : "memory");
+}
+// The group's barrier, returning the AND of every thread's predicate (a uniform decision).
+__device__ __forceinline__ bool fin_all(bool p) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred a, b;\n\t"
+      "setp.ne.u32 a, %1, 0;\n\t"
+      "bar.red.and.pred b, %2, %3, a;\n\t"
+      "selp.u32 %0, 1, 0, b;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)p), "n"(kFinBarrier), "n"(kFinThreads)
+      : "memory");
+  return r != 0;
+}
+// Shared-memory scratch of the group's reductions and broadcasts.
+struct GroupScratch {
+  float wsum[kFinWarps];
+  unsigned hit[kFinWarps], pos[kFinWarps];
+  int out[4];
+  float fout[4];
+};
+// Sum over the group's threads in a fixed association (each warp's butterfly sum, then the warps
+// in order); every thread gets it.
+__device__ __forceinline__ float group_sum(GroupScratch& gs, float v) {
+  const int ft = fin_thread(), lane = ft & 31, fw = ft >> 5;
+  v = warp_sum(v);
+  if (lane == 0) gs.wsum[fw] = v;
+  fin_sync();
+  float s = gs.wsum[0];
 #pragma unroll
-        for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, w[j]);
-        bsum = __fadd_rn(bsum, vs);
-      }
-    }
-  }
-  float incl = warp_incl_scan(bsum, lane);
-  float excl = __shfl_up_sync(kFull, incl, 1);
-  if (lane == 0) excl = 0.f;
-  unsigned hit = __ballot_sync(kFull, bsum > 0.f && incl > t);
-  unsigned pos = __ballot_sync(kFull, bsum > 0.f);
-  if (!pos) return -1;
-  const int L = hit ? (__ffs(hit) - 1) : (31 - __clz(pos));
-  const float base = __shfl_sync(kFull, excl, L);
-  // level 2: block L split over the lanes, q consecutive vectors each (q <= 2 for ranges of at
-  // most 2048 vectors; larger blocks loop)
-  const int bend = min((L + 1) * Bs, nvec);
-  const int q = (Bs + 31) / 32;
-  const int v0 = L * Bs + lane * q;
-  float lsum = 0.f;
-  for (int qq = 0; qq < q; ++qq) {
-    const int v = v0 + qq;
-    if (v < bend) {
+  for (int w = 1; w < kFinWarps; ++w) s = __fadd_rn(s, gs.wsum[w]);
+  fin_sync();
+  return s;
+}
+
+// ---------------------------------------------------------------- inverse-CDF search ----
+// The finishing group finds, in a staged range of `nvec` vectors (nvec <= 2 * kFinThreads), the
+// element where the running weight taken in index order first exceeds t; wf(v, w) fills the VE
+// weights of vector v.  Thread i sums q = ceil(nvec / kFinThreads) consecutive vectors; a scan of
+// the thread sums (each warp, then the warps in order) picks the crossing thread, which walks its
+// vectors, then the elements of the chosen vector.  At every level the first part with positive
+// weight whose running total exceeds t is taken, otherwise the last part with positive weight
+// (rounding), so a zero-weight element is never returned.  Returns the position (vector * VE +
+// element) in every thread, or -1 when the range holds no positive weight.
+template <int VE, typename WF>
+__device__ int group_crossing(GroupScratch& gs, int nvec, float t, WF wf) {
+  const int ft = fin_thread(), lane = ft & 31, fw = ft >> 5;
+  if (nvec <= 0) return -1;
+  const int q = (nvec + kFinThreads - 1) / kFinThreads;
+  const int v0 = ft * q;
+  float s = 0.f;
+  for (int i = 0; i < q; ++i) {
+    const int v = v0 + i;
+    if (v < nvec) {
       float w[VE];
       wf(v, w);
       float vs = 0.f;
 #pragma unroll
       for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, w[j]);
-      lsum = __fadd_rn(lsum, vs);
+      s = __fadd_rn(s, vs);
     }
   }
-  incl = warp_incl_scan(lsum, lane);
-  excl = __shfl_up_sync(kFull, incl, 1);
+  const float incl = warp_incl_scan(s, lane);
+  float excl = __shfl_up_sync(kFull, incl, 1);
   if (lane == 0) excl = 0.f;
-  hit = __ballot_sync(kFull, lsum > 0.f && __fadd_rn(base, incl) > t);
-  pos = __ballot_sync(kFull, lsum > 0.f);
-  if (!pos) return -1;  // cannot happen: block L holds positive weight
-  const int L2 = hit ? (__ffs(hit) - 1) : (31 - __clz(pos));
-  int found = -1;
-  if (lane == L2) {
-    // the lane's vectors in order, then the elements of the chosen vector
+  if (lane == 31) gs.wsum[fw] = incl;
+  fin_sync();
+  float base = 0.f;
+  for (int w = 0; w < fw; ++w) base = __fadd_rn(base, gs.wsum[w]);
+  const unsigned hit = __ballot_sync(kFull, s > 0.f && __fadd_rn(base, incl) > t);
+  const unsigned pos = __ballot_sync(kFull, s > 0.f);
+  if (lane == 0) {
+    gs.hit[fw] = hit;
+    gs.pos[fw] = pos;
+  }
+  fin_sync();
+  int L = -1;
+#pragma unroll
+  for (int w = 0; w < kFinWarps; ++w)
+    if (L < 0 && gs.hit[w]) L = w * 32 + __ffs(gs.hit[w]) - 1;
+#pragma unroll
+  for (int w = kFinWarps - 1; w >= 0; --w)
+    if (L < 0 && gs.pos[w]) L = w * 32 + 31 - __clz(gs.pos[w]);
+  if (ft == L) {
+    // the thread's vectors in order, then the elements of the chosen vector
     float acc = __fadd_rn(base, excl);
     int pv = -1, lv = -1;
     float pacc = 0.f, lacc = 0.f;
-    for (int qq = 0; qq < q; ++qq) {
-      const int v = v0 + qq;
-      if (v >= bend) break;
+    for (int i = 0; i < q; ++i) {
+      const int v = v0 + i;
+      if (v >= nvec) break;
       float w[VE];
       wf(v, w);
       float vs = 0.f;
@@ -452,9 +478,12 @@ __device__ int warp_crossing(int nvec, float t, WF wf) {
         lj = j;
       }
     }
-    found = pv * VE + (pj >= 0 ? pj : lj);
+    gs.out[3] = pv * VE + (pj >= 0 ? pj : lj);
   }
-  return __shfl_sync(kFull, found, L2);
+  fin_sync();
+  const int found = L < 0 ? -1 : gs.out[3];
+  fin_sync();
+  return found;
 }
 
 }  // namespace specv

@@ -11,16 +11,17 @@
 //    statistics and its sub-chunk partials;
 //  - the bookkeeping warp counts each written chunk on its request (one memory fence per batch
 //    of ready chunks, then fire-and-forget reductions);
-//  - the finishing warp owns requests b = blockIdx.x, blockIdx.x + gridDim.x, ...: once a
-//    request's count says every chunk is in, it combines the chunk statistics into per-row
+//  - the finishing group (four warps) owns requests b = blockIdx.x, blockIdx.x + gridDim.x, ...:
+//    once a request's count says every chunk is in, it combines the chunk statistics into per-row
 //    normalisers, computes alpha_k = min(1, p_k(x_k)/q_k(x_k)), runs the acceptance scan, and
 //    draws the emitted token by inverse CDF from the chunk and sub-chunk weights (re-reading only
 //    the sub-chunk that holds the crossing), or walks the draft tree.
-// Work items are ordered request-major.  For chains with draft logits and T > 0 the draw after a
-// rejection at position n needs max(0, p_n - q_n), which needs both rows' normalisers first; the
-// pair at n is then read a second time by residual work items, placed in the item order `lag`
-// requests after the request's own items (by default after every stats item).  Their producer
-// waits (bounded) for the request's acceptance result before staging them.
+// Stats work items are ordered request-major.  For chains with draft logits and T > 0 the draw
+// after a rejection at position n needs max(0, p_n - q_n), which needs both rows' normalisers
+// first; the pair at n is then read a second time by residual work items.  Those are handed out
+// from a cursor over the requests in order, and only for requests whose acceptance result is
+// already published: a producer takes them ahead of its next stats batch whenever there are some,
+// so the second read follows the first closely (often from L2) and no producer ever waits.
 //
 // Formulas: "Speculative Decoding in Production: From Draft Models to EAGLE-3 Dynamic Trees for
 // 3x-5x Lossless Acceleration", section I.1 (acceptance ratio, uniform test, first-rejection
@@ -38,15 +39,24 @@ enum Mode : int { kChain = 0, kNgram = 1, kGreedy = 2, kTree = 3 };
 enum Kind : int { kFullP = 0, kExcl = 1 };
 enum ItemKind : int { kItemStats = 0, kItemResid = 1, kItemSkip = 2, kItemEnd = 3 };
 
-// Per chunk of a logits row (and, with the same layout, per sub-chunk).
+// Per chunk of a logits row (and, with the same layout, per sub-chunk): two 8-byte halves, each a
+// value and the call's tag, written together by one 16-byte store.  A reader takes the entry once
+// both tags equal the call's (an aligned 8-byte half is read whole), so no memory fence has to
+// order these stores before the count that announces them: the count only says when to look.
 struct __align__(16) ChunkStat {
-  float a;    // maximum (NaN if the range holds a NaN)
-  float s;    // softmax: sum over the range of 2^(l c - RN(a c))
-  float rsv;  // 0
-  int i;      // softmax: SPEC_ERRF_* bits; argmax modes: first index of the maximum
-              // (-1: the range holds a NaN; INT_MAX: the range is empty)
+  float a;      // maximum (NaN: the range holds a NaN; softmax: +inf makes the row non-finite)
+  unsigned ta;  // the call's tag
+  float s;      // softmax: sum over the range of 2^(l c - RN(a c)); argmax modes: the bits of the
+                // first index of the maximum (INT_MAX: the range is empty)
+  unsigned ts;  // the call's tag
 };
-// Per logits row, written by the request's finishing warp.
+__device__ __forceinline__ bool cs_ok(const ChunkStat& q, unsigned tag) { return q.ta == tag && q.ts == tag; }
+// A residual sum with the call's tag (one 8-byte store), read like a ChunkStat half.
+struct __align__(8) TagSum {
+  float v;
+  unsigned t;
+};
+// Per logits row, written by the request's finishing group.
 struct __align__(16) RowStat {
   double Z;  // sum over the row of 2^(l c - mc)
   float mc;  // fp32 product (row maximum) * c
@@ -80,14 +90,14 @@ struct Params {
   int rows;        // logits rows per request read by the stats items (draft-model chain: 2K + 1)
   int nchunk;      // stats chunks per row (kChunkVec vectors each)
   int nchunk_r;    // residual items per row (kResVec target vectors each)
-  int npos;        // residual positions per request (K with per-position outputs, else 1); 0: none
-  int lag;         // requests between a request's stats items and its residual items
-  int diag;        // 1: draw at every position (per-position outputs requested)
-  float c;         // log2(e) / T
-  unsigned total;  // work items
+  int npos;          // residual positions per request (K with per-position outputs, else 1); 0: none
+  int diag;          // 1: draw at every position (per-position outputs requested)
+  float c;           // log2(e) / T
+  unsigned total;    // stats items (A per request)
+  unsigned total_r;  // residual items (R per request)
   // the divisors of the item decoding: A = rows * nchunk stats items per request, R = npos *
-  // nchunk_r residual items per request, A + R, nchunk, nchunk_r
-  FastDiv fd_A, fd_R, fd_AR, fd_nchunk, fd_nchunk_r;
+  // nchunk_r residual items per request, nchunk, nchunk_r
+  FastDiv fd_A, fd_R, fd_nchunk, fd_nchunk_r;
   const int32_t* draft_tokens;
   const float* r;
   const float* u;
@@ -109,11 +119,13 @@ struct Params {
   ChunkStat* sstat;     // [B][rows][nchunk][kGroupWarps] sub-chunk partials (softmax modes)
   RowStat* rstat;       // [B][rows]
   ReqState* req;        // [B]
-  float* wsum;          // [B][npos][nchunk_r] residual weight per residual item
-  float* wsub;          // [B][npos][nchunk_r][kGroupWarps] residual weight per sub-range
-  unsigned* work;       // work-item counter    } cleared by the host before each call
-  unsigned* gerr;       // timeout flag           }
-  unsigned* exit_tick;  // exiting CTAs           }
+  TagSum* wsum;         // [B][npos][nchunk_r] residual weight per residual item
+  TagSum* wsub;         // [B][npos][nchunk_r][kGroupWarps] residual weight per sub-range
+  unsigned tag;         // this call's tag (never 0: cleared memory never matches it)
+  unsigned* work;            // stats-item counter   } cleared by the host before each call
+  unsigned* gerr;            // timeout flag           }
+  unsigned* exit_tick;       // exiting CTAs           }
+  unsigned* rc;              // next residual item     }
   unsigned* tick_a;     // [B] chunks in, per request          }
   unsigned* tick_b;     // [B][npos] residual items in         }  (req[] is cleared too)
   size_t clear_bytes;   // bytes from `work` through req[B - 1]
@@ -133,13 +145,20 @@ __device__ __forceinline__ float chunk_weight(float a, float s, float c, float m
   return __fmul_rn(s, ex2(__fsub_rn(__fmul_rn(a, c), mc)));
 }
 __device__ __forceinline__ ChunkStat ld_chunkstat(const ChunkStat* p) {
-  const float4 v = __ldcg(reinterpret_cast<const float4*>(p));
+  const uint4 v = __ldcg(reinterpret_cast<const uint4*>(p));
   ChunkStat q;
-  q.a = v.x;
-  q.s = v.y;
-  q.rsv = v.z;
-  q.i = __float_as_int(v.w);
+  q.a = __uint_as_float(v.x);
+  q.ta = v.y;
+  q.s = __uint_as_float(v.z);
+  q.ts = v.w;
   return q;
+}
+__device__ __forceinline__ TagSum ld_tagsum(const TagSum* p) {
+  const uint2 v = __ldcg(reinterpret_cast<const uint2*>(p));
+  TagSum t;
+  t.v = __uint_as_float(v.x);
+  t.t = v.y;
+  return t;
 }
 __device__ __forceinline__ RowStat ld_rowstat(const RowStat* p) {
   RowStat r;
@@ -194,7 +213,7 @@ struct SlotMeta {
   unsigned* tick;  // the count this chunk adds to (stats and residual items)
 };
 constexpr int kFinCs = 512;   // chunk statistics of one request staged for its finishing
-constexpr int kFinSs = 256;   // sub-chunk statistics of one row staged for a draw
+constexpr int kFinSs = 512;   // sub-chunk statistics of the rows a draw may read
 constexpr int kFinRows = 64;  // row statistics kept in shared memory for finishing
 struct Shared {
   uint64_t full[kStages], empty[kStages], pfull[kSlots], pempty[kSlots], fin_bar, cs_bar, ss_bar;
@@ -208,6 +227,7 @@ struct Shared {
   ChunkStat fin_ss[kFinSs];
   RowStat fin_rs[kFinRows];
   int fin_par[kFinRows], fin_tok[kFinRows];  // a small tree's parents and tokens
+  GroupScratch gs;                            // the finishing group's reductions and broadcasts
 };
 
 __device__ __forceinline__ void raise_abort(const Params& P, Shared& sm) {
@@ -219,43 +239,35 @@ __device__ __forceinline__ bool aborted(const Shared& sm) {
 }
 
 // -------------------------------------------------------------------- item decoding ----
-// Item order: stats items of requests 0 .. lag-1; then, per group g, the stats items of request
-// lag + g followed by the residual items of request g; then the residual items of the last lag
-// requests.  Without a residual pass: the stats items of every request in order.
-__device__ __forceinline__ int decode_item(const Params& P, unsigned w, int& b, int& off) {
-  if (w >= P.total) return kItemEnd;
-  const unsigned A = P.fd_A.d;
-  if (P.npos == 0) {
-    b = (int)fdiv(w, P.fd_A);
-    off = (int)(w - (unsigned)b * A);
-    return kItemStats;
+// Stats items are request-major, then row, then chunk: item w < P.total is chunk item w mod A of
+// request w / A.  Residual items are request-major, then position slot, then residual chunk:
+// residual item w < P.total_r is item w mod R of request w / R.  The stats items are handed out
+// by the counter `work`, the residual items by the cursor `rc`; a producer stages a residual item
+// only once its request's acceptance result is published, and never waits for one while it still
+// has stats items.
+__device__ __forceinline__ void decode_stats(const Params& P, unsigned w, int& b, int& off) {
+  b = (int)fdiv(w, P.fd_A);
+  off = (int)(w - (unsigned)b * P.fd_A.d);
+}
+// Lane 0 of a producer that found request b without a residual draw: moves the cursor past the
+// request's items (when it still points into them).
+__device__ __forceinline__ void skip_residual(const Params& P, unsigned b) {
+  const unsigned lo = b * P.fd_R.d, end = lo + P.fd_R.d;
+  unsigned c = *reinterpret_cast<const volatile unsigned*>(P.rc);
+  for (int tries = 0; tries < 8 && c >= lo && c < end; ++tries) {
+    const unsigned old = atomicCAS(P.rc, c, end);
+    if (old == c) return;
+    c = old;
   }
-  const unsigned Rr = P.fd_R.d;
-  const unsigned L = (unsigned)P.lag;
-  const unsigned head = L * A;
-  if (w < head) {
-    b = (int)fdiv(w, P.fd_A);
-    off = (int)(w - (unsigned)b * A);
-    return kItemStats;
-  }
-  const unsigned w2 = w - head;
-  const unsigned g = fdiv(w2, P.fd_AR);
-  if (g < (unsigned)P.B - L) {
-    const unsigned o = w2 - g * (A + Rr);
-    if (o < A) {
-      b = (int)(L + g);
-      off = (int)o;
-      return kItemStats;
-    }
-    b = (int)g;
-    off = (int)(o - A);
-    return kItemResid;
-  }
-  const unsigned w3 = w2 - ((unsigned)P.B - L) * (A + Rr);
-  const unsigned q = fdiv(w3, P.fd_R);
-  b = (int)((unsigned)P.B - L + q);
-  off = (int)(w3 - q * Rr);
-  return kItemResid;
+}
+// A request's acceptance result as its four words read it: every word valid, or only the first
+// when that one says no residual parameters follow (an error, per-position outputs, or n = K).
+__device__ __forceinline__ bool result_complete(const Params& P, unsigned long long q0, unsigned long long q1,
+                                                unsigned long long q2, unsigned long long q3) {
+  if (!req_word_ok(q0)) return false;
+  const unsigned hi = req_word_hi(q0);
+  if ((hi >> 16) != 0u || P.diag || (int)(hi & 0xFFFFu) >= P.K) return true;
+  return req_word_ok(q1) && req_word_ok(q2) && req_word_ok(q3);
 }
 
 // Geometry of the target grid vectors [vt0, vt0 + span) of the pair at position k (a residual
@@ -315,21 +327,34 @@ __device__ __forceinline__ void resid_weights(const unsigned char* buf, int dslo
 
 // ------------------------------------------------------------------------ producer ----
 // Producer of group grp: items it = grp, grp + kGroups, ... of this CTA's sequence (stage
-// it % kStages).  It publishes one end marker when its claims run out.
+// it % kStages).  The producer holds one batch of up to kClaim residual items from the cursor at a
+// time (claimed at the start of a batch of stats items, or at any item once those are out) and
+// stages its items, ahead of stats items, once their request's result is published; it reads the
+// result words at the start of each stats batch and uses them at the next, so that the read does
+// not hold it up.  Only once its stats items are out does it wait (bounded) for a result.  Once
+// both kinds are exhausted it publishes one end marker.
 template <int MODE, typename T>
 __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages, int grp) {
-  constexpr int VE = Elem<T>::kPerVec;
   const int lane = threadIdx.x & 31;
-  // claims: kClaim consecutive items at a time, the next batch claimed one batch ahead.  Each
-  // producer's first batch is fixed (items kClaim * (blockIdx.x * kGroups + grp) ...), so that its
-  // first copies start without waiting for an atomic; the counter hands out the items after those.
+  // stats claims: batches of consecutive items, the next batch claimed one batch ahead.  Each
+  // producer's first batch is fixed (kClaim items from kClaim * (blockIdx.x * kGroups + grp)), so
+  // that its first copies start without waiting for an atomic; the counter hands out the rest, in
+  // batches of kClaim until fewer than two batches per producer remain, then smaller ones, so that
+  // the producers run out of items at about the same time.
   const unsigned fixed = (unsigned)kClaim * gridDim.x * (unsigned)kGroups;
-  unsigned cur = 0, nxt = 0;
+  const unsigned nprod = gridDim.x * (unsigned)kGroups;
+  unsigned cur = 0, nxt = 0, ccnt = kClaim, ncnt = kClaim;
   int pos = 0;
   if (lane == 0) {
     cur = (unsigned)kClaim * (blockIdx.x * (unsigned)kGroups + (unsigned)grp);
     nxt = fixed + atomicAdd(P.work, (unsigned)kClaim);
   }
+  // residual claims (lane 0): the held items rfirst .. rfirst + rcnt - 1, and q0..q3, the result
+  // words of request qb as last read
+  unsigned rfirst = 0, qb = 0xffffffffu;
+  int rcnt = 0;
+  bool rdone = P.npos == 0, qok = false;  // qok: request qb's result is complete
+  unsigned long long q0 = 0, q1 = 0, q2 = 0, q3 = 0;
   int it = grp;
   // residual parameters of the last request seen (consecutive residual items share them)
   int rb = -1, rk = 0, rerr = 1;
@@ -340,14 +365,6 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
       if (lane == 0) raise_abort(P, sm);
       break;
     }
-    const unsigned w = __shfl_sync(kFull, cur + (unsigned)pos, 0);
-    if (++pos == kClaim) {
-      pos = 0;
-      if (lane == 0) {
-        cur = nxt;
-        if (cur < P.total) nxt = fixed + atomicAdd(P.work, (unsigned)kClaim);
-      }
-    }
     unsigned char* buf = stages + (size_t)s * kStageBytes;
     StageMeta m;
     m.b = m.row = m.ch = m.kk = 0;
@@ -355,75 +372,123 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
     m.e_base = 0;
     m.e_lo = m.e_hi = m.dshift = 0;
     m.mct = m.mcd = m.rho = 0.f;
-    int off = 0;
-    m.kind = decode_item(P, w, m.b, off);
-    if (m.kind == kItemStats) {
-      m.row = (int)fdiv((unsigned)off, P.fd_nchunk);
-      m.ch = off - m.row * P.nchunk;
-      const RowGrid<T> g = row_grid<T>(row_ptr<T>(P, m.b, m.row), P.V);
-      const int v0 = m.ch * kChunkVec, v1 = min(v0 + kChunkVec, g.nvec);
-      m.nvec = max(0, v1 - v0);
-      m.e_base = v0 * VE - g.phase;
-      warp_stage<T>(buf, g, P.V, v0, v1, &sm.full[s], lane);
-    } else if (m.kind == kItemResid) {
-      m.kk = (int)fdiv((unsigned)off, P.fd_nchunk_r);
-      m.ch = off - m.kk * P.nchunk_r;
-      if (m.b != rb || P.diag) {
-        // the request's acceptance result, published by the finishing warp of its owner CTA
-        unsigned long long w0 = 0, w1 = 0, w2 = 0, w3 = 0;
-        int ready = 0;
-        if (lane == 0) {
-          const unsigned long long* rw = P.req[m.b].w;
-          const long long t0 = clock64();
-          for (;;) {
-            w0 = ld_volatile_u64(rw);
-            if (req_word_ok(w0)) {
-              const unsigned hi = req_word_hi(w0);
-              const int n = (int)(hi & 0xFFFFu), err = (int)(hi >> 16);
-              if (err || P.diag || n >= P.K) {
-                ready = 1;
-              } else {
-                w1 = ld_volatile_u64(rw + 1);
-                w2 = ld_volatile_u64(rw + 2);
-                w3 = ld_volatile_u64(rw + 3);
-                ready = req_word_ok(w1) && req_word_ok(w2) && req_word_ok(w3);
-              }
-            }
-            if (ready || aborted(sm)) break;
-            if (clock64() - t0 > kWaitLimitCycles) {
-              raise_abort(P, sm);
-              break;
-            }
-            __nanosleep(64);
+    m.kind = kItemEnd;
+    long long t_poll = 0;
+    for (;;) {  // until this stage has an item (a residual batch of a request without a draw is dropped)
+      int kind = kItemEnd;
+      unsigned w = 0;
+      if (lane == 0) {
+        const bool sdone = cur + (unsigned)pos >= P.total;
+        const bool boundary = pos == 0 || sdone;
+        if (boundary && rcnt == 0 && !rdone) {
+          // once the stats items are out, one item at a time: the last requests' residual items
+          // then spread over as many producers as possible
+          const unsigned rk = sdone ? 1u : (unsigned)kClaim;
+          const unsigned c = atomicAdd(P.rc, rk);
+          if (c >= P.total_r) {
+            rdone = true;
+          } else {
+            rfirst = c;
+            rcnt = (int)min(rk, P.total_r - c);
           }
-          if (P.diag) __threadfence();  // per-position parameters come from the row statistics
         }
-        ready = __shfl_sync(kFull, ready, 0);
-        const unsigned h0 = __shfl_sync(kFull, req_word_hi(w0), 0);
-        rb = m.b;
-        rerr = 1;
-        if (ready) {
+        const unsigned nb = rcnt > 0 ? fdiv(rfirst, P.fd_R) : 0xffffffffu;
+        bool rready = rcnt > 0 && nb == qb && qok;
+        if (rcnt > 0 && !rready && boundary) {
+          // the words read at the previous batch start (in by now), else read them again: used at
+          // the next batch start, or now once the stats items are out
+          if (nb == qb && result_complete(P, q0, q1, q2, q3)) {
+            qok = rready = true;
+          } else {
+            const unsigned long long* rw = P.req[nb].w;
+            qb = nb;
+            q0 = ld_volatile_u64(rw);
+            q1 = ld_volatile_u64(rw + 1);
+            q2 = ld_volatile_u64(rw + 2);
+            q3 = ld_volatile_u64(rw + 3);
+            qok = false;
+            if (sdone) qok = rready = result_complete(P, q0, q1, q2, q3);
+          }
+        }
+        if (rready) {
+          kind = kItemResid;
+          w = rfirst++;
+          --rcnt;
+        } else if (!sdone) {
+          kind = kItemStats;
+          w = cur + (unsigned)pos;
+          if (++pos == (int)ccnt) {
+            pos = 0;
+            cur = nxt;
+            ccnt = ncnt;
+            if (cur < P.total) {
+              const unsigned front = nxt + ncnt, rem = P.total > front ? P.total - front : 0u;
+              ncnt = max(1u, min((unsigned)kClaim, rem / (2u * nprod)));
+              nxt = fixed + atomicAdd(P.work, ncnt);
+            }
+          }
+        } else if (rcnt > 0 || !rdone) {
+          kind = kItemSkip;  // the held residual items' result is not published yet: poll (bounded)
+          if (t_poll == 0) t_poll = clock64();
+          if (aborted(sm) || clock64() - t_poll > kWaitLimitCycles) {
+            raise_abort(P, sm);
+            kind = kItemEnd;
+          } else {
+            __nanosleep(512);
+          }
+        }
+      }
+      kind = __shfl_sync(kFull, kind, 0);
+      w = __shfl_sync(kFull, w, 0);
+      if (kind == kItemSkip) continue;
+      m.kind = kind;
+      if (kind == kItemStats) {
+        int off = 0;
+        decode_stats(P, w, m.b, off);
+        m.row = (int)fdiv((unsigned)off, P.fd_nchunk);
+        m.ch = off - m.row * P.nchunk;
+        const RowGrid<T> g = row_grid<T>(row_ptr<T>(P, m.b, m.row), P.V);
+        const int v0 = m.ch * kChunkVec, v1 = min(v0 + kChunkVec, g.nvec);
+        m.nvec = max(0, v1 - v0);
+        constexpr int VE = Elem<T>::kPerVec;
+        m.e_base = v0 * VE - g.phase;
+        warp_stage<T>(buf, g, P.V, v0, v1, &sm.full[s], lane);
+      } else if (kind == kItemResid) {
+        m.b = (int)fdiv(w, P.fd_R);
+        const int off = (int)(w - (unsigned)m.b * P.fd_R.d);
+        m.kk = (int)fdiv((unsigned)off, P.fd_nchunk_r);
+        m.ch = off - m.kk * P.nchunk_r;
+        if (m.b != rb || P.diag) {
+          // the request's result, as lane 0 read it (complete: the item was taken only then)
+          const unsigned h0 = __shfl_sync(kFull, req_word_hi(q0), 0);
+          const unsigned h1 = __shfl_sync(kFull, req_word_hi(q1), 0);
+          const unsigned h2 = __shfl_sync(kFull, req_word_hi(q2), 0);
+          const unsigned h3 = __shfl_sync(kFull, req_word_hi(q3), 0);
+          rb = m.b;
           const int n = (int)(h0 & 0xFFFFu);
           rerr = (int)(h0 >> 16);
           rk = P.diag ? m.kk : n;
           if (!rerr && rk < P.K) {
             if (P.diag) {
+              // per-position parameters come from the row statistics, written before the result
+              if (lane == 0) __threadfence();
+              __syncwarp();
               const RowStat ts = ld_rowstat(P.rstat + (size_t)m.b * P.rows + rk);
               const RowStat ds = ld_rowstat(P.rstat + (size_t)m.b * P.rows + P.R + rk);
               rmct = ts.mc;
               rmcd = ds.mc;
               rrho = __fdiv_rn((float)ts.Z, (float)ds.Z);  // max(0, p - q) Z_t = max(0, e - f Z_t / Z_d)
             } else {
-              rmct = __uint_as_float(__shfl_sync(kFull, req_word_hi(w1), 0));
-              rmcd = __uint_as_float(__shfl_sync(kFull, req_word_hi(w2), 0));
-              rrho = __uint_as_float(__shfl_sync(kFull, req_word_hi(w3), 0));
+              rmct = __uint_as_float(h1);
+              rmcd = __uint_as_float(h2);
+              rrho = __uint_as_float(h3);
             }
           }
         }
-      }
-      m.kind = kItemSkip;
-      if (!rerr && rk < P.K) {
-        m.kind = kItemResid;
+        if (rerr || rk >= P.K) {  // no residual draw for this request: drop the item
+          if (lane == 0) skip_residual(P, (unsigned)m.b);
+          continue;
+        }
         m.row = rk;
         m.mct = rmct;
         m.mcd = rmcd;
@@ -439,6 +504,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
           warp_stage<T>(buf + (size_t)kDraftSlot * 16, q.gd, P.V, q.vd0, q.vd1, &sm.full[s], lane);
         }
       }
+      break;
     }
     if (lane == 0) sm.meta[s] = m;
     __syncwarp();
@@ -568,7 +634,7 @@ __device__ __forceinline__ void publish_chunk(const Params& P, Shared& sm, const
   pm.tick = nullptr;
   if (m.kind == kItemStats) {
     const size_t ci = ((size_t)m.b * P.rows + m.row) * P.nchunk + m.ch;
-    float4 q;
+    uint4 q;
     // lanes 0..kGroupWarps-1 hold the warp partials; xor-shuffles within those lanes merge them
     if constexpr (kSoftmax) {
       float M = mine ? pw.x : -INFINITY;
@@ -578,18 +644,20 @@ __device__ __forceinline__ void publish_chunk(const Params& P, Shared& sm, const
       float sv = (mine && !fl && M != -INFINITY) ? __fmul_rn(pw.y, rescale(pw.x, M, c)) : 0.f;
 #pragma unroll
       for (int o = 1; o < kGroupWarps; o <<= 1) sv = __fadd_rn(sv, __shfl_xor_sync(kFull, sv, o));
-      q = make_float4(M, sv, 0.f, __int_as_float(fl));
+      // (a NaN or +inf maximum carries the chunk's non-finite flag)
+      q = make_uint4(__float_as_uint(M), P.tag, __float_as_uint(sv), P.tag);
       if (mine)  // the sub-chunk partials, for the draws
-        *reinterpret_cast<float4*>(P.sstat + ci * kGroupWarps + lane) = make_float4(pw.x, pw.y, 0.f, 0.f);
+        *reinterpret_cast<uint4*>(P.sstat + ci * kGroupWarps + lane) =
+            make_uint4(__float_as_uint(pw.x), P.tag, __float_as_uint(pw.y), P.tag);
     } else {
       float v = mine ? pw.x : -INFINITY;
       int i = mine ? __float_as_int(pw.y) : INT_MAX;
 #pragma unroll
       for (int o = 1; o < kGroupWarps; o <<= 1)
         argmax_merge(v, i, __shfl_xor_sync(kFull, v, o), __shfl_xor_sync(kFull, i, o));
-      q = make_float4(v, 0.f, 0.f, __int_as_float(i));
+      q = make_uint4(__float_as_uint(v), P.tag, (unsigned)i, P.tag);
     }
-    if (lane == 0) *reinterpret_cast<float4*>(P.cstat + ci) = q;
+    if (lane == 0) *reinterpret_cast<uint4*>(P.cstat + ci) = q;
     pm.tick = P.tick_a + m.b;
   } else if (m.kind == kItemResid) {
     float sum = mine ? pw.x : 0.f;
@@ -597,8 +665,8 @@ __device__ __forceinline__ void publish_chunk(const Params& P, Shared& sm, const
     for (int o = 1; o < kGroupWarps; o <<= 1) sum = __fadd_rn(sum, __shfl_xor_sync(kFull, sum, o));
     const size_t bk = (size_t)m.b * P.npos + m.kk;
     const size_t ri = bk * P.nchunk_r + m.ch;
-    if (lane == 0) P.wsum[ri] = sum;
-    if (mine) P.wsub[ri * kGroupWarps + lane] = pw.x;
+    if (lane == 0) *reinterpret_cast<uint2*>(P.wsum + ri) = make_uint2(__float_as_uint(sum), P.tag);
+    if (mine) *reinterpret_cast<uint2*>(P.wsub + ri * kGroupWarps + lane) = make_uint2(__float_as_uint(pw.x), P.tag);
     pm.tick = P.tick_b + bk;
   }
   __syncwarp();
@@ -709,17 +777,24 @@ __device__ void book_loop(const Params& P, Shared& sm) {
       if (lane == nb) tick = tk;
       ++nb;
     }
-    if (nb > 0) {
-      __threadfence();                      // this batch's statistics before its counts
-      if (lane < nb) atomicAdd(tick, 1u);  // result unused: a fire-and-forget reduction
-    }
+    // no fence: the statistics carry the call's tag, and their readers wait for it
+    if (nb > 0 && lane < nb) atomicAdd(tick, 1u);  // result unused: a fire-and-forget reduction
   }
 }
 
 // ------------------------------------------------------------------------ finishing ----
+// The finishing group (kFinWarps warps, named barrier kFinBarrier) completes the requests
+// b = blockIdx.x, blockIdx.x + gridDim.x, ...  Its first warp, the leader, waits for the counts,
+// issues the copies and runs the sequential steps (alpha and the acceptance scan, the part
+// selections of a draw, the tree walk); the data-parallel steps (combining chunk statistics,
+// the sum and the search over a staged sub-chunk) take every thread.  Each function below is
+// entered by the whole group with the same arguments unless it says otherwise, and every
+// decision that ends or skips work is agreed by the group (fin_all), so that the group reaches
+// its barriers together.
+
 // Warp-wide inverse CDF over part weights W(c) (fp32), in order: the first part with positive
 // weight whose running total exceeds tgt, else the last positive one.  Every lane gets the part
-// and the total weight before it.
+// and the total weight before it.  (One warp.)
 template <typename WF>
 __device__ __forceinline__ void select_part(int nparts, float tgt, WF W, int& cstar, float& bstar) {
   const int lane = threadIdx.x & 31;
@@ -751,6 +826,7 @@ __device__ __forceinline__ void select_part(int nparts, float tgt, WF W, int& cs
   cstar = clast;
   bstar = blast;
 }
+// (One warp.)
 template <typename WF>
 __device__ __forceinline__ float total_weight(int nparts, WF W) {
   const int lane = threadIdx.x & 31;
@@ -759,23 +835,21 @@ __device__ __forceinline__ float total_weight(int nparts, WF W) {
   return warp_sum(part);
 }
 
-// Waits for the finishing buffer's copy (bounded; the wait ignores the abort flag so that no
-// copy is left in flight).  Returns false on a timeout.
-__device__ __forceinline__ bool fin_wait(const Params& P, Shared& sm, uint32_t& fph) {
-  const int lane = threadIdx.x & 31;
-  __syncwarp();
-  if (lane == 0) mbar_arrive(&sm.fin_bar);
+// Waits (bounded, ignoring the abort flag so that no copy is left in flight) for phase ph of a
+// finishing barrier whose copies have been issued and whose arrival is made; every thread of the
+// group waits.  Returns the group's agreement that the phase completed.
+__device__ __forceinline__ bool fin_wait_only(const Params& P, Shared& sm, uint64_t* bar, uint32_t& ph) {
   const int zero = 0;
-  bool ok = mbar_wait(&sm.fin_bar, fph & 1u, &zero);
+  bool ok = mbar_wait(bar, ph & 1u, &zero);
   if (!ok) {
-    if (lane == 0) raise_abort(P, sm);
-    mbar_wait(&sm.fin_bar, fph & 1u, &zero);
+    raise_abort(P, sm);
+    mbar_wait(bar, ph & 1u, &zero);
   }
-  ++fph;
-  return ok;
+  ++ph;
+  return fin_all(ok);
 }
 
-// Chunk statistics of request b as the finishing warp reads them: from the shared-memory copy
+// Chunk statistics of request b as the finishing group reads them: from the shared-memory copy
 // when the request's block fits there, else from global memory.
 struct CsReader {
   const ChunkStat* g;
@@ -786,37 +860,76 @@ struct CsReader {
     return ld_chunkstat(g + (size_t)r * nchunk + c);
   }
 };
-// Copies the chunk statistics of request b into shared memory when they fit: one bulk copy (the
-// block is contiguous, 16-byte aligned, a multiple of 16 bytes), completing on cs_bar.  The
-// caller has acquired the request's count; the proxy fence orders that acquisition before the
-// copy's reads.
-__device__ __forceinline__ CsReader stage_request_stats(const Params& P, Shared& sm, int b, bool allow,
+// Rows whose sub-chunk statistics sit in fin_ss (row r0 + i at fin_ss[i * nchunk * kGroupWarps]).
+struct SsRows {
+  int r0, n;
+};
+// Waits (bounded) until the n chunk statistics at p in global memory all carry the call's tag;
+// the group splits the checks.  False after a timeout.
+__device__ __forceinline__ bool await_tagged(const Params& P, Shared& sm, const ChunkStat* p, int n) {
+  const long long t0 = clock64();
+  for (;;) {
+    bool good = true;
+    for (int i = fin_thread(); i < n; i += kFinThreads) good = good && cs_ok(ld_chunkstat(p + i), P.tag);
+    if (fin_all(good)) return true;
+    if (clock64() - t0 > kWaitLimitCycles) {
+      raise_abort(P, sm);
+      return false;
+    }
+    __nanosleep(128);
+  }
+}
+// Copies request b's chunk statistics into shared memory when they fit, together with the sub-
+// chunk statistics of rows ss (when those fit too; otherwise ss.n becomes 0): bulk copies (each
+// block contiguous, 16-byte aligned, a multiple of 16 bytes) issued by the leader, completing on
+// cs_bar, and issued again (bounded) until every entry carries the call's tag.  The leader
+// acquired the request's count before the group barrier that precedes this call; its proxy fence
+// orders that acquisition, and the group's earlier reads of the buffers, before the copies.  When
+// the statistics do not fit, the group waits for their tags in global memory instead.
+__device__ __forceinline__ CsReader stage_request_stats(const Params& P, Shared& sm, int b, SsRows& ss,
                                                         uint32_t& csph) {
-  const int lane = threadIdx.x & 31;
   const int n = P.rows * P.nchunk;
+  const int nss = P.nchunk * kGroupWarps;
   CsReader rd;
   rd.g = P.cstat + (size_t)b * n;
   rd.nchunk = P.nchunk;
   rd.s = nullptr;
-  if (allow && n <= kFinCs) {
-    __syncwarp();
-    if (lane == 0) {
+  if (n > kFinCs) {
+    ss.n = 0;
+    await_tagged(P, sm, rd.g, n);
+    return rd;
+  }
+  if (ss.n * nss > kFinSs) ss.n = 0;
+  const int nsx = ss.n * nss;
+  const ChunkStat* sg = P.sstat + ((size_t)b * P.rows + ss.r0) * nss;
+  const long long t0 = clock64();
+  for (;;) {
+    if (fin_thread() == 0) {
       fence_proxy_async_global();
-      fence_proxy_async_shared();  // the previous request's reads of fin_cs come first
+      fence_proxy_async_shared();
       const uint32_t bytes = (uint32_t)n * (uint32_t)sizeof(ChunkStat);
-      mbar_expect_tx(&sm.cs_bar, bytes);
+      const uint32_t sbytes = (uint32_t)nsx * (uint32_t)sizeof(ChunkStat);
+      mbar_expect_tx(&sm.cs_bar, bytes + sbytes);
       tma_load_1d(sm.fin_cs, rd.g, bytes, &sm.cs_bar);
+      if (sbytes) tma_load_1d(sm.fin_ss, sg, sbytes, &sm.cs_bar);
       mbar_arrive(&sm.cs_bar);
     }
-    const int zero = 0;
-    bool ok = mbar_wait(&sm.cs_bar, csph & 1u, &zero);
-    if (!ok) {
-      if (lane == 0) raise_abort(P, sm);
-      mbar_wait(&sm.cs_bar, csph & 1u, &zero);
+    if (!fin_wait_only(P, sm, &sm.cs_bar, csph)) {  // after a timeout, read global memory instead
+      ss.n = 0;
+      return rd;
     }
-    ++csph;
-    rd.s = ok ? sm.fin_cs : nullptr;  // after a timeout, read global memory instead
+    bool good = true;
+    for (int i = fin_thread(); i < n + nsx; i += kFinThreads)
+      good = good && cs_ok(i < n ? sm.fin_cs[i] : sm.fin_ss[i - n], P.tag);
+    if (fin_all(good)) break;  // (the barrier also ends the group's reads before a new copy)
+    if (clock64() - t0 > kWaitLimitCycles) {
+      raise_abort(P, sm);
+      ss.n = 0;
+      return rd;
+    }
+    __nanosleep(128);
   }
+  rd.s = sm.fin_cs;
   return rd;
 }
 
@@ -826,36 +939,25 @@ __device__ __forceinline__ RowStat read_rowstat(const Params& P, const Shared& s
   return ld_rowstat(P.rstat + (size_t)b * P.rows + r);
 }
 
-// Waits (bounded, ignoring the abort flag so that no copy is left in flight) for phase ph of a
-// finishing-warp barrier that the warp has already arrived on.  Returns false on a timeout.
-__device__ __forceinline__ bool fin_wait_only(const Params& P, Shared& sm, uint64_t* bar, uint32_t& ph) {
-  const int lane = threadIdx.x & 31;
-  const int zero = 0;
-  bool ok = mbar_wait(bar, ph & 1u, &zero);
-  if (!ok) {
-    if (lane == 0) raise_abort(P, sm);
-    mbar_wait(bar, ph & 1u, &zero);
-  }
-  ++ph;
-  return ok;
-}
-
 // A draw from target row `row` of request b by inverse CDF: weights p (kFullP) or p without
 // token x (kExcl).  draw_begin issues the bulk copies the draw needs (the row's sub-chunk
-// statistics; for kExcl the sub-chunk holding x) so that they overlap other work; draw_end picks
-// the crossing chunk from the chunk weights, the crossing sub-chunk from the sub-chunk weights,
-// stages that sub-chunk (unless it is the one already staged) and searches it.  For kExcl the
-// sub-chunk holding x is summed without x, so no weight is ever obtained by subtraction.
+// statistics unless they are staged already; for kExcl the sub-chunk holding x) so that they
+// overlap other work; draw_end picks the crossing chunk from the chunk weights, the crossing
+// sub-chunk from the sub-chunk weights, stages that sub-chunk (unless it is the one already
+// staged) and searches it.  For kExcl the sub-chunk holding x is summed without x, so no weight
+// is ever obtained by subtraction.
 struct DrawPlan {
   int row, kind, x;
   int cx, ix;    // kExcl: chunk and sub-chunk holding x
   int sv0, sv1;  // grid vectors staged in the finishing buffer (sv1 <= sv0: none)
-  bool ss;       // the row's sub-chunk statistics are being staged in fin_ss
+  int ss;        // sub-chunk statistics: 0 global memory, 1 being staged at fin_ss, 2 staged already
+  int ss_off;    // their offset in fin_ss
 };
 template <typename T>
-__device__ DrawPlan draw_begin(const Params& P, Shared& sm, unsigned char* fbuf, int b, int row, int kind, int x) {
+__device__ DrawPlan draw_begin(const Params& P, Shared& sm, unsigned char* fbuf, int b, int row, int kind, int x,
+                               SsRows& st) {
   constexpr int VE = Elem<T>::kPerVec;
-  const int lane = threadIdx.x & 31;
+  const int ft = fin_thread(), lane = ft & 31;
   DrawPlan d;
   d.row = row;
   d.kind = kFullP;
@@ -863,20 +965,16 @@ __device__ DrawPlan draw_begin(const Params& P, Shared& sm, unsigned char* fbuf,
   d.cx = d.ix = -1;
   d.sv0 = d.sv1 = 0;
   const int nss = P.nchunk * kGroupWarps;
-  d.ss = nss <= kFinSs;
-  __syncwarp();
-  if (lane == 0) {
-    fence_proxy_async_global();  // the statistics were acquired with the request's count
-    fence_proxy_async_shared();  // earlier reads of fin_ss and the finishing buffer come first
-    if (d.ss) {
-      const uint32_t bytes = (uint32_t)nss * (uint32_t)sizeof(ChunkStat);
-      mbar_expect_tx(&sm.ss_bar, bytes);
-      tma_load_1d(sm.fin_ss, P.sstat + ((size_t)b * P.rows + row) * nss, bytes, &sm.ss_bar);
-      mbar_arrive(&sm.ss_bar);
-    }
+  if (row >= st.r0 && row < st.r0 + st.n) {
+    d.ss = 2;
+    d.ss_off = (row - st.r0) * nss;
+  } else {
+    d.ss = nss <= kFinSs ? 1 : 0;
+    d.ss_off = 0;
+    if (d.ss) st.n = 0;  // the staged rows are overwritten
   }
+  const RowGrid<T> g = row_grid<T>(row_ptr<T>(P, b, row), P.V);
   if (kind == kExcl && x >= 0 && x < P.V) {
-    const RowGrid<T> g = row_grid<T>(row_ptr<T>(P, b, row), P.V);
     const int pv = (x + g.phase) / VE;
     d.kind = kExcl;
     d.x = x;
@@ -884,9 +982,24 @@ __device__ DrawPlan draw_begin(const Params& P, Shared& sm, unsigned char* fbuf,
     d.ix = (pv - d.cx * kChunkVec) / kSubVec;
     d.sv0 = d.cx * kChunkVec + d.ix * kSubVec;
     d.sv1 = min(d.sv0 + kSubVec, g.nvec);
-    warp_stage<T>(fbuf, g, P.V, d.sv0, d.sv1, &sm.fin_bar, lane);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.fin_bar);
+  }
+  fin_sync();  // the group's earlier reads of fin_ss and the finishing buffer come first
+  if (ft < 32) {
+    if (lane == 0) {
+      fence_proxy_async_global();  // the statistics were acquired with the request's count
+      fence_proxy_async_shared();
+      if (d.ss == 1) {
+        const uint32_t bytes = (uint32_t)nss * (uint32_t)sizeof(ChunkStat);
+        mbar_expect_tx(&sm.ss_bar, bytes);
+        tma_load_1d(sm.fin_ss, P.sstat + ((size_t)b * P.rows + row) * nss, bytes, &sm.ss_bar);
+        mbar_arrive(&sm.ss_bar);
+      }
+    }
+    if (d.kind == kExcl) {
+      warp_stage<T>(fbuf, g, P.V, d.sv0, d.sv1, &sm.fin_bar, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.fin_bar);
+    }
   }
   return d;
 }
@@ -895,29 +1008,29 @@ template <typename T>
 __device__ int draw_end(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph, int b,
                         const DrawPlan& d, const CsReader& rd, const RowStat& rs, float u, float* mass_out) {
   constexpr int VE = Elem<T>::kPerVec;
-  const int lane = threadIdx.x & 31;
+  const int ft = fin_thread(), lane = ft & 31;
   const float c = P.c, mc = rs.mc;
   const int row = d.row;
   const RowGrid<T> g = row_grid<T>(row_ptr<T>(P, b, row), P.V);
   const ChunkStat* srow = P.sstat + ((size_t)b * P.rows + row) * P.nchunk * kGroupWarps;
+  const ChunkStat* sss = d.ss ? sm.fin_ss + d.ss_off : nullptr;  // (prestaged rows are checked)
   bool ok = true;
-  if (d.ss) ok = fin_wait_only(P, sm, &sm.ss_bar, ssph);
+  if (d.ss == 1) {
+    ok = fin_wait_only(P, sm, &sm.ss_bar, ssph);
+    // a staged entry without the call's tag is not in yet: take the row from global memory then
+    bool good = true;
+    for (int i = ft; i < P.nchunk * kGroupWarps; i += kFinThreads) good = good && cs_ok(sm.fin_ss[i], P.tag);
+    if (!fin_all(good)) sss = nullptr;
+  }
   if (d.kind == kExcl) ok = fin_wait_only(P, sm, &sm.fin_bar, fph) && ok;
-  auto sub_weight = [&](int ch, int i) {
-    const ChunkStat q = d.ss ? sm.fin_ss[ch * kGroupWarps + i] : ld_chunkstat(srow + (size_t)ch * kGroupWarps + i);
-    return chunk_weight(q.a, q.s, c, mc);
-  };
-  int sv0 = d.sv0, sv1 = d.sv1;
-  int staged_ch = d.cx, staged_sub = d.ix;
-  // kExcl: lane i < kGroupWarps keeps sub-chunk i's weight in chunk cx, with x left out of
-  // sub-chunk ix (summed from the staged sub-chunk)
+  if (!sss) ok = await_tagged(P, sm, srow, P.nchunk * kGroupWarps) && ok;
   const int cx = d.cx, ix = d.ix;
-  float wsub_x = 0.f, wcx = 0.f;
+  // kExcl: the staged sub-chunk's weight without x, summed by the group
+  float wx = 0.f;
   if (d.kind == kExcl) {
-    const float wl = (lane < kGroupWarps && lane != ix) ? sub_weight(cx, lane) : 0.f;
-    const int e_base = sv0 * VE - g.phase;
+    const int e_base = d.sv0 * VE - g.phase;
     float part = 0.f;
-    for (int v = lane; v < sv1 - sv0; v += 32) {
+    for (int v = ft; v < d.sv1 - d.sv0; v += kFinThreads) {
       float f[VE];
       Elem<T>::unpack(lds128(fbuf + (size_t)v * 16), f);
       float vs = 0.f;
@@ -925,49 +1038,78 @@ __device__ int draw_end(const Params& P, Shared& sm, unsigned char* fbuf, uint32
       for (int j = 0; j < VE; ++j) vs = __fadd_rn(vs, e_base + v * VE + j == d.x ? 0.f : ex2(__fmaf_rn(f[j], c, -mc)));
       part = __fadd_rn(part, vs);
     }
-    const float wx = warp_sum(part);
-    wsub_x = lane == ix ? wx : wl;
-    float t = lane < kGroupWarps ? wsub_x : 0.f;
+    wx = group_sum(sm.gs, part);
+  }
+  // the leader picks the chunk and the sub-chunk and stages the crossing sub-chunk
+  if (ft < 32) {
+    auto sub_weight = [&](int ch, int i) {
+      const ChunkStat q = sss ? sss[ch * kGroupWarps + i] : ld_chunkstat(srow + (size_t)ch * kGroupWarps + i);
+      return chunk_weight(q.a, q.s, c, mc);
+    };
+    // kExcl: lane i < kGroupWarps keeps sub-chunk i's weight in chunk cx, with x left out of
+    // sub-chunk ix
+    float wsub_x = 0.f, wcx = 0.f;
+    if (d.kind == kExcl) {
+      const float wl = (lane < kGroupWarps && lane != ix) ? sub_weight(cx, lane) : 0.f;
+      wsub_x = lane == ix ? wx : wl;
+      float t = lane < kGroupWarps ? wsub_x : 0.f;
 #pragma unroll
-    for (int o = 1; o < kGroupWarps; o <<= 1) t = __fadd_rn(t, __shfl_xor_sync(kFull, t, o));
-    wcx = __shfl_sync(kFull, t, 0);
+      for (int o = 1; o < kGroupWarps; o <<= 1) t = __fadd_rn(t, __shfl_xor_sync(kFull, t, o));
+      wcx = __shfl_sync(kFull, t, 0);
+    }
+    int k2 = d.kind;
+    auto weight = [&](int ch) {
+      if (k2 == kExcl && ch == cx) return wcx;
+      const ChunkStat q = rd(row, ch);
+      return chunk_weight(q.a, q.s, c, mc);
+    };
+    float S = total_weight(P.nchunk, weight);
+    const float S0 = S;
+    if (!(S > 0.f)) {  // no residual mass: draw from p
+      k2 = kFullP;
+      S = total_weight(P.nchunk, weight);
+    }
+    int cstar, sstar = -1;
+    float bstar, sbase = 0.f;
+    const float tgt = __fmul_rn(u, S);
+    select_part(P.nchunk, tgt, weight, cstar, bstar);
+    if (cstar >= 0) {
+      const bool subx = k2 == kExcl && cstar == cx;
+      auto sweight = [&](int i) {  // select_part evaluates part i in lane i
+        if (subx) return wsub_x;
+        return sub_weight(cstar, i);
+      };
+      select_part(kGroupWarps, __fsub_rn(tgt, bstar), sweight, sstar, sbase);
+    }
+    const int restage = (cstar >= 0 && sstar >= 0 && (cstar != d.cx || sstar != d.ix)) ? 1 : 0;
+    if (restage) {
+      const int sv0 = cstar * kChunkVec + sstar * kSubVec;
+      // the group's reads of fbuf ended at the barrier of the sum above (or it was never read)
+      if (lane == 0) fence_proxy_async_shared();
+      warp_stage<T>(fbuf, g, P.V, sv0, min(sv0 + kSubVec, g.nvec), &sm.fin_bar, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.fin_bar);
+    }
+    if (lane == 0) {
+      sm.gs.out[0] = cstar;
+      sm.gs.out[1] = sstar;
+      sm.gs.out[2] = k2 | (restage << 4);
+      sm.gs.fout[0] = __fsub_rn(__fsub_rn(tgt, bstar), sbase);
+      sm.gs.fout[1] = (float)((double)S0 / rs.Z);
+    }
   }
-  int k2 = d.kind;
-  auto weight = [&](int ch) {
-    if (k2 == kExcl && ch == cx) return wcx;
-    const ChunkStat q = rd(row, ch);
-    return chunk_weight(q.a, q.s, c, mc);
-  };
-  float S = total_weight(P.nchunk, weight);
-  const float S0 = S;
-  if (!(S > 0.f)) {  // no residual mass: draw from p
-    k2 = kFullP;
-    S = total_weight(P.nchunk, weight);
+  fin_sync();
+  const int cstar = sm.gs.out[0], sstar = sm.gs.out[1], k2 = sm.gs.out[2] & 15, restage = sm.gs.out[2] >> 4;
+  const float t = sm.gs.fout[0];
+  *mass_out = sm.gs.fout[1];
+  if (cstar < 0 || sstar < 0) {
+    fin_sync();
+    return -1;  // the second cannot happen: the chunk holds positive weight
   }
-  *mass_out = (float)((double)S0 / rs.Z);
-  int cstar;
-  float bstar;
-  const float tgt = __fmul_rn(u, S);
-  select_part(P.nchunk, tgt, weight, cstar, bstar);
-  if (cstar < 0) return -1;
-  const bool subx = k2 == kExcl && cstar == cx;
-  auto sweight = [&](int i) {  // select_part evaluates part i in lane i
-    if (subx) return wsub_x;
-    return sub_weight(cstar, i);
-  };
-  int sstar;
-  float sbase;
-  select_part(kGroupWarps, __fsub_rn(tgt, bstar), sweight, sstar, sbase);
-  if (sstar < 0) return -1;  // cannot happen: the chunk holds positive weight
-  const float t = __fsub_rn(__fsub_rn(tgt, bstar), sbase);
-  if (cstar != staged_ch || sstar != staged_sub) {
+  int sv0 = d.sv0, sv1 = d.sv1;
+  if (restage) {
     sv0 = cstar * kChunkVec + sstar * kSubVec;
     sv1 = min(sv0 + kSubVec, g.nvec);
-    __syncwarp();
-    if (lane == 0) fence_proxy_async_shared();  // earlier reads of fbuf before the copy
-    warp_stage<T>(fbuf, g, P.V, sv0, sv1, &sm.fin_bar, lane);
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&sm.fin_bar);
     ok = fin_wait_only(P, sm, &sm.fin_bar, fph) && ok;
   }
   const int e_base = sv0 * VE - g.phase;
@@ -981,53 +1123,52 @@ __device__ int draw_end(const Params& P, Shared& sm, unsigned char* fbuf, uint32
       if (e_base + v * VE + j == xe) w[j] = 0.f;
     }
   };
-  const int pos = warp_crossing<VE>(sv1 - sv0, t, wf);
-  __syncwarp();
+  const int pos = group_crossing<VE>(sm.gs, sv1 - sv0, t, wf);
   return (ok && pos >= 0) ? e_base + pos : -1;
 }
 
-// Combines the chunk statistics of every row of request b into RowStat (lanes over rows).
+// Combines the chunk statistics of every row of request b into RowStat.  G threads share a row
+// (G a power of two: each takes chunks g, g + G, ... and a butterfly over the G threads merges
+// them); G grows while the group still covers every row in one pass.
 template <int MODE>
 __device__ void combine_rows(const Params& P, Shared& sm, int b, const CsReader& rd) {
   constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
-  const int lane = threadIdx.x & 31;
-  for (int r = lane; r < P.rows; r += 32) {
+  const int ft = fin_thread();
+  const int nch = P.nchunk;
+  int G = 1;
+  while (G < 32 && G < nch && P.rows * 2 * G <= kFinThreads) G <<= 1;
+  const int g = ft & (G - 1);
+  const int rpp = kFinThreads / G;
+  for (int r0 = 0; r0 < P.rows; r0 += rpp) {
+    const int r = r0 + ft / G;
+    const bool act = r < P.rows;
     float m = -INFINITY;
     int fl = 0;
-#pragma unroll 4
-    for (int c = 0; c < P.nchunk; ++c) {
-      const ChunkStat q = rd(r, c);
-      m = fmax_nan(m, q.a);
-      if (kSoftmax)
-        fl |= q.i;
-      else if (q.i < 0)
-        fl |= SPEC_ERRF_NONFINITE;
+    if (act) {
+      for (int c = g; c < nch; c += G) {
+        const ChunkStat q = rd(r, c);
+        m = fmax_nan(m, q.a);
+        if (isnan(q.a) || (kSoftmax && q.a == INFINITY)) fl |= SPEC_ERRF_NONFINITE;
+      }
+    }
+    for (int o = G >> 1; o > 0; o >>= 1) {
+      m = fmax_nan(m, __shfl_xor_sync(kFull, m, o));
+      fl |= __shfl_xor_sync(kFull, fl, o);
     }
     RowStat rs;
     rs.pad[0] = rs.pad[1] = rs.pad[2] = 0;
     if (kSoftmax) {
       const float mc = __fmul_rn(m, P.c);
       const bool finite_m = !isnan(m) && m != INFINITY && m != -INFINITY;
-      double Z = 0.0;
-      if (!fl && finite_m) {
-        float z4[4] = {0.f, 0.f, 0.f, 0.f};  // four independent chains, summed pairwise
-        int c = 0;
-        for (; c + 4 <= P.nchunk; c += 4) {
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const ChunkStat q = rd(r, c + u);
-            z4[u] = __fadd_rn(z4[u], chunk_weight(q.a, q.s, P.c, mc));
-          }
+      float z = 0.f;
+      if (act && !fl && finite_m) {
+        for (int c = g; c < nch; c += G) {
+          const ChunkStat q = rd(r, c);
+          z = __fadd_rn(z, chunk_weight(q.a, q.s, P.c, mc));
         }
-#pragma unroll
-        for (int u = 0; u < 3; ++u) {
-          if (c + u < P.nchunk) {
-            const ChunkStat q = rd(r, c + u);
-            z4[u] = __fadd_rn(z4[u], chunk_weight(q.a, q.s, P.c, mc));
-          }
-        }
-        Z = (double)__fadd_rn(__fadd_rn(z4[0], z4[1]), __fadd_rn(z4[2], z4[3]));
       }
+      for (int o = G >> 1; o > 0; o >>= 1) z = __fadd_rn(z, __shfl_xor_sync(kFull, z, o));
+      const double Z = (!fl && finite_m) ? (double)z : 0.0;
       rs.Z = Z;
       rs.mc = mc;
       rs.amax = -1;
@@ -1035,19 +1176,24 @@ __device__ void combine_rows(const Params& P, Shared& sm, int b, const CsReader&
     } else {
       // lowest index among the chunks whose maximum equals the row maximum
       int idx = INT_MAX;
-      for (int c = 0; c < P.nchunk; ++c) {
-        const ChunkStat q = rd(r, c);
-        if (q.a == m && q.i >= 0) idx = min(idx, q.i);
+      if (act) {
+        for (int c = g; c < nch; c += G) {
+          const ChunkStat q = rd(r, c);
+          if (q.a == m) idx = min(idx, __float_as_int(q.s));
+        }
       }
+      for (int o = G >> 1; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(kFull, idx, o));
       rs.Z = 0.0;
       rs.mc = m;
       rs.amax = (fl || idx == INT_MAX) ? -1 : idx;
       rs.err = fl ? SPEC_ERRF_NONFINITE : 0;
     }
-    P.rstat[(size_t)b * P.rows + r] = rs;
-    if (r < kFinRows) sm.fin_rs[r] = rs;
+    if (act && g == 0) {
+      P.rstat[(size_t)b * P.rows + r] = rs;
+      if (r < kFinRows) sm.fin_rs[r] = rs;
+    }
   }
-  __syncwarp();
+  fin_sync();
 }
 
 // l c - mc with the product l c carried exactly (an fp32 pair from one FMA) and the difference
@@ -1068,10 +1214,7 @@ __device__ __forceinline__ float exp2_times(double x, float f) {
   return ldexpf(r, n);
 }
 
-// Chain / n-gram / greedy-chain finishing: alpha, acceptance scan (section I.1 step 2), outputs,
-// publication of the acceptance result, and the draws made here (bonus row; n-gram residual).
-// Returns the accepted length (or -1 after an error) in every lane.
-// Inputs of request b that do not depend on its statistics, loaded while the finishing warp
+// Inputs of request b that do not depend on its statistics, loaded by the leader while the group
 // waits for them (positions k < 32 in lane k): the draft token, its uniform, and the target and
 // draft logits at the token.
 struct ReqPrefetch {
@@ -1099,116 +1242,131 @@ __device__ __forceinline__ ReqPrefetch prefetch_request(const Params& P, int b) 
   return f;
 }
 
+// Chain / n-gram / greedy-chain finishing: alpha, acceptance scan (section I.1 step 2), outputs,
+// publication of the acceptance result, and the draws made here (bonus row; n-gram residual).
+// Returns the accepted length (or -1 after an error) in every thread.  pf is the leader's.
 template <int MODE, typename T>
 __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& csph,
                             uint32_t& ssph, int b, const ReqPrefetch& pf) {
   constexpr int S = Elem<T>::kSize;
   constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
-  const int lane = threadIdx.x & 31;
+  const int ft = fin_thread(), lane = ft & 31;
   const int K = P.K;
-  const int x0 = pf.x0;
-  const float r0 = pf.r0, lx0 = pf.lx0, dx0 = pf.dx0;
-  const CsReader rd = stage_request_stats(P, sm, b, true, csph);
+  // the rows a draw here may read: every n-gram target row, the bonus row of a draft-model chain
+  SsRows st{MODE == kNgram ? 0 : K, kSoftmax ? (MODE == kNgram ? K + 1 : 1) : 0};
+  const CsReader rd = stage_request_stats(P, sm, b, st, csph);
   combine_rows<MODE>(P, sm, b, rd);
-  int e = 0;
-  for (int k = lane; k < K; k += 32) {
-    const int x = k < 32 ? x0 : __ldg(P.draft_tokens + (size_t)b * K + k);
-    double alpha = 0.0;
-    if (x < 0 || x >= P.V) {
-      e |= SPEC_ERRF_BAD_TOKEN;
-    } else {
-      const RowStat t = read_rowstat(P, sm, b, k);
-      if (kSoftmax) {
-        // alpha = p(x) / q(x) = 2^((l_x c - mc_t) - (d_x c - mc_d)) Z_d / Z_t (draft model), or
-        // p(x) = 2^(l_x c - mc_t) / Z_t (one-hot draft); capped at 1
-        const float lx = k < 32 ? lx0 : Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, k) + (size_t)x * S));
-        const double ext = scaled_logit(lx, P.c, t.mc);
-        if (MODE == kChain) {
-          const RowStat d = read_rowstat(P, sm, b, P.R + k);
-          const float dx =
-              k < 32 ? dx0 : Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, P.R + k) + (size_t)x * S));
-          if (dx == -INFINITY) {
-            alpha = 1.0;  // q(x) = 0
-          } else if (lx == -INFINITY) {
-            alpha = 0.0;  // p(x) = 0
+  if (ft < 32) {
+    const int x0 = pf.x0;
+    const float r0 = pf.r0, lx0 = pf.lx0, dx0 = pf.dx0;
+    int e = 0;
+    for (int k = lane; k < K; k += 32) {
+      const int x = k < 32 ? x0 : __ldg(P.draft_tokens + (size_t)b * K + k);
+      double alpha = 0.0;
+      if (x < 0 || x >= P.V) {
+        e |= SPEC_ERRF_BAD_TOKEN;
+      } else {
+        const RowStat t = read_rowstat(P, sm, b, k);
+        if (kSoftmax) {
+          // alpha = p(x) / q(x) = 2^((l_x c - mc_t) - (d_x c - mc_d)) Z_d / Z_t (draft model), or
+          // p(x) = 2^(l_x c - mc_t) / Z_t (one-hot draft); capped at 1
+          const float lx = k < 32 ? lx0 : Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, k) + (size_t)x * S));
+          const double ext = scaled_logit(lx, P.c, t.mc);
+          if (MODE == kChain) {
+            const RowStat d = read_rowstat(P, sm, b, P.R + k);
+            const float dx =
+                k < 32 ? dx0 : Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, P.R + k) + (size_t)x * S));
+            if (dx == -INFINITY) {
+              alpha = 1.0;  // q(x) = 0
+            } else if (lx == -INFINITY) {
+              alpha = 0.0;  // p(x) = 0
+            } else {
+              const float ratio = exp2_times(ext - scaled_logit(dx, P.c, d.mc), __fdiv_rn((float)d.Z, (float)t.Z));
+              alpha = ratio >= 1.f ? 1.0 : (double)ratio;
+            }
           } else {
-            const float ratio = exp2_times(ext - scaled_logit(dx, P.c, d.mc), __fdiv_rn((float)d.Z, (float)t.Z));
-            alpha = ratio >= 1.f ? 1.0 : (double)ratio;
+            const float px = lx == -INFINITY ? 0.f : exp2_times(ext, __frcp_rn((float)t.Z));
+            alpha = px >= 1.f ? 1.0 : (double)px;
           }
         } else {
-          const float px = lx == -INFINITY ? 0.f : exp2_times(ext, __frcp_rn((float)t.Z));
-          alpha = px >= 1.f ? 1.0 : (double)px;
+          alpha = (x == t.amax) ? 1.0 : 0.0;
         }
-      } else {
-        alpha = (x == t.amax) ? 1.0 : 0.0;
+      }
+      sm.alpha[k] = alpha;
+    }
+    for (int r = lane; r < P.rows; r += 32) e |= read_rowstat(P, sm, b, r).err;
+    const int err = warp_or(e);
+    __syncwarp();
+    int n = 0;
+    if (!err) {
+      n = K;
+      for (int k0 = 0; k0 < K; k0 += 32) {
+        const int k = k0 + lane;
+        bool rej = false;
+        if (k < K) {
+          const double a = sm.alpha[k];
+          const float rk = k < 32 ? r0 : __ldg(P.r + (size_t)b * K + k);
+          rej = kSoftmax ? !((double)rk <= a) : (a != 1.0);
+        }
+        const unsigned msk = __ballot_sync(kFull, rej);
+        if (msk) {
+          n = k0 + __ffs(msk) - 1;
+          break;
+        }
       }
     }
-    sm.alpha[k] = alpha;
-  }
-  for (int r = lane; r < P.rows; r += 32) e |= read_rowstat(P, sm, b, r).err;
-  const int err = warp_or(e);
-  __syncwarp();
-  int n = 0;
-  if (!err) {
-    n = K;
-    for (int k0 = 0; k0 < K; k0 += 32) {
-      const int k = k0 + lane;
-      bool rej = false;
-      if (k < K) {
-        const double a = sm.alpha[k];
-        const float rk = k < 32 ? r0 : __ldg(P.r + (size_t)b * K + k);
-        rej = kSoftmax ? !((double)rk <= a) : (a != 1.0);
-      }
-      const unsigned msk = __ballot_sync(kFull, rej);
-      if (msk) {
-        n = k0 + __ffs(msk) - 1;
-        break;
-      }
+    int xn = __shfl_sync(kFull, x0, n < 32 ? n : 0);
+    if (n >= 32 && n < K) xn = __ldg(P.draft_tokens + (size_t)b * K + n);
+    if (lane == 0) {
+      sm.gs.out[0] = n;
+      sm.gs.out[1] = err;
+      sm.gs.out[2] = xn;
     }
   }
+  fin_sync();
+  const int n = sm.gs.out[0], err = sm.gs.out[1], xn = sm.gs.out[2];
   // The emitted token's draw (n-gram at any n, the bonus row of a draft-model chain) starts its
   // copies now, so that they overlap the outputs and the publication below.
   const bool early = kSoftmax && !err && !P.diag && (MODE == kNgram || n == K);
   DrawPlan dp{};
-  if (early) {
-    int xn = __shfl_sync(kFull, x0, n < 32 ? n : 0);
-    if (n >= 32 && n < K) xn = __ldg(P.draft_tokens + (size_t)b * K + n);
-    dp = draw_begin<T>(P, sm, fbuf, b, n, (MODE == kNgram && n < K) ? kExcl : kFullP, n < K ? xn : -1);
-  }
-  for (int i = lane; i <= K; i += 32) {
-    const size_t o_i = (size_t)b * (K + 1) + i;
-    int o = -1;
-    if (!err && i < n) o = i < 32 ? x0 : __ldg(P.draft_tokens + (size_t)b * K + i);
-    if (!err && i == n && !kSoftmax) o = read_rowstat(P, sm, b, n).amax;
-    P.out_tokens[o_i] = o;
-    if (P.accept_prob && i < K) P.accept_prob[(size_t)b * K + i] = err ? 0.f : (float)sm.alpha[i];
-    if (P.cand_tokens && (err || !kSoftmax)) P.cand_tokens[o_i] = err ? -1 : read_rowstat(P, sm, b, i).amax;
-    if (P.pos_mass && (err || !kSoftmax)) P.pos_mass[o_i] = err ? 0.f : 1.f;
-  }
-  if (lane == 0) {
-    P.num_accepted[b] = n;
-    if (P.err_flags) P.err_flags[b] = err;
-    if (P.residual_mass && (err || !kSoftmax)) P.residual_mass[b] = err ? 0.f : 1.f;
-  }
-  // publication of the acceptance result (read by residual work items and the probability rows)
-  if (MODE == kChain && P.npos > 0 && P.diag) {  // per-position residuals read the row statistics
-    __syncwarp();
-    __threadfence();
-  }
-  const bool resid = MODE == kChain && P.npos > 0 && !P.diag && !err && n < K;
-  if (lane == 0 || (resid && lane < 4)) {
-    unsigned hi = (unsigned)n | ((unsigned)err << 16);
-    if (lane > 0) {
-      const RowStat t = read_rowstat(P, sm, b, n), d = read_rowstat(P, sm, b, P.R + n);
-      hi = __float_as_uint(lane == 1 ? t.mc : lane == 2 ? d.mc : __fdiv_rn((float)t.Z, (float)d.Z));
+  if (early) dp = draw_begin<T>(P, sm, fbuf, b, n, (MODE == kNgram && n < K) ? kExcl : kFullP, n < K ? xn : -1, st);
+  if (ft < 32) {
+    const int x0 = pf.x0;
+    for (int i = lane; i <= K; i += 32) {
+      const size_t o_i = (size_t)b * (K + 1) + i;
+      int o = -1;
+      if (!err && i < n) o = i < 32 ? x0 : __ldg(P.draft_tokens + (size_t)b * K + i);
+      if (!err && i == n && !kSoftmax) o = read_rowstat(P, sm, b, n).amax;
+      P.out_tokens[o_i] = o;
+      if (P.accept_prob && i < K) P.accept_prob[(size_t)b * K + i] = err ? 0.f : (float)sm.alpha[i];
+      if (P.cand_tokens && (err || !kSoftmax)) P.cand_tokens[o_i] = err ? -1 : read_rowstat(P, sm, b, i).amax;
+      if (P.pos_mass && (err || !kSoftmax)) P.pos_mass[o_i] = err ? 0.f : 1.f;
     }
-    st_volatile_u64(P.req[b].w + lane, ((unsigned long long)hi << 32) | kReqTag);
+    if (lane == 0) {
+      P.num_accepted[b] = n;
+      if (P.err_flags) P.err_flags[b] = err;
+      if (P.residual_mass && (err || !kSoftmax)) P.residual_mass[b] = err ? 0.f : 1.f;
+    }
+    // publication of the acceptance result (read by residual work items and the probability rows)
+    if (MODE == kChain && P.npos > 0 && P.diag) {  // per-position residuals read the row statistics
+      __syncwarp();
+      __threadfence();
+    }
+    const bool resid = MODE == kChain && P.npos > 0 && !P.diag && !err && n < K;
+    if (lane == 0 || (resid && lane < 4)) {
+      unsigned hi = (unsigned)n | ((unsigned)err << 16);
+      if (lane > 0) {
+        const RowStat t = read_rowstat(P, sm, b, n), d = read_rowstat(P, sm, b, P.R + n);
+        hi = __float_as_uint(lane == 1 ? t.mc : lane == 2 ? d.mc : __fdiv_rn((float)t.Z, (float)d.Z));
+      }
+      st_volatile_u64(P.req[b].w + lane, ((unsigned long long)hi << 32) | kReqTag);
+    }
+    __syncwarp();
   }
-  __syncwarp();
   if constexpr (kSoftmax) {
     if (err) return -1;
     auto emit = [&](int k, int tok, float mass) {
-      if (lane == 0) {
+      if (ft == 0) {
         const size_t o_k = (size_t)b * (K + 1) + k;
         if (k == n) {
           P.out_tokens[o_k] = tok;
@@ -1218,9 +1376,10 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
         if (P.pos_mass) P.pos_mass[o_k] = mass;
       }
     };
+    const float u = pf.u;  // used by the leader only
     if (early) {
       float mass;
-      const int tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, dp, rd, read_rowstat(P, sm, b, n), pf.u, &mass);
+      const int tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, dp, rd, read_rowstat(P, sm, b, n), u, &mass);
       emit(n, tok, mass);
     } else if (P.diag) {
       // per-position outputs: a draw at every position made here (the bonus row, and for
@@ -1228,9 +1387,9 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
       for (int k = MODE == kChain ? K : 0; k <= K; ++k) {
         const int kind = (MODE == kNgram && k < K) ? kExcl : kFullP;
         const int x = k < K ? __ldg(P.draft_tokens + (size_t)b * K + k) : -1;
-        const DrawPlan d = draw_begin<T>(P, sm, fbuf, b, k, kind, x);
+        const DrawPlan d = draw_begin<T>(P, sm, fbuf, b, k, kind, x, st);
         float mass;
-        const int tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, d, rd, read_rowstat(P, sm, b, k), pf.u, &mass);
+        const int tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, d, rd, read_rowstat(P, sm, b, k), u, &mass);
         emit(k, tok, mass);
       }
     }
@@ -1244,63 +1403,106 @@ template <typename T>
 __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph,
                               int b, int kk, int n) {
   constexpr int VE = Elem<T>::kPerVec;
-  const int lane = threadIdx.x & 31;
+  const int ft = fin_thread(), lane = ft & 31;
   const int k = P.diag ? kk : n;
   const RowStat ts = read_rowstat(P, sm, b, k);
   const RowStat ds = read_rowstat(P, sm, b, P.R + k);
   const size_t bk = (size_t)b * P.npos + kk;
-  const float* ws = P.wsum + bk * P.nchunk_r;
   const float u = __ldg(P.u + b);
-  auto weight = [&](int c) { return __ldcg(ws + c); };
-  const float S = total_weight(P.nchunk_r, weight);
-  const float mass = (float)((double)S / ts.Z);
-  int tok = -1;
-  if (S > 0.f) {
-    const float tgt = __fmul_rn(u, S);
-    int cstar, sstar;
-    float bstar, sbase;
-    select_part(P.nchunk_r, tgt, weight, cstar, bstar);
-    const float* wsb = P.wsub + (bk * P.nchunk_r + (cstar < 0 ? 0 : cstar)) * kGroupWarps;
-    select_part(kGroupWarps, __fsub_rn(tgt, bstar), [&](int i) { return __ldcg(wsb + i); }, sstar, sbase);
-    if (cstar >= 0 && sstar >= 0) {
-      const float t = __fsub_rn(__fsub_rn(tgt, bstar), sbase);
-      const ResGeo<T> q = res_geo<T>(P, b, k, cstar * kResVec + sstar * kResSub, kResSub);
-      __syncwarp();
-      if (lane == 0) fence_proxy_async_shared();  // earlier reads of fbuf before the copy
-      warp_stage<T>(fbuf, q.gt, P.V, q.vt0, q.vt1, &sm.fin_bar, lane);
-      warp_stage<T>(fbuf + (size_t)kFinDraftSlot * 16, q.gd, P.V, q.vd0, q.vd1, &sm.fin_bar, lane);
-      const bool ok = fin_wait(P, sm, fph);
-      const float c = P.c, mct = ts.mc, mcd = ds.mc;
-      const float rho = __fdiv_rn((float)ts.Z, (float)ds.Z);
-      auto wf = [&](int v, float (&w)[VE]) {
-        resid_weights<T>(fbuf, kFinDraftSlot, v, q.e_base, q.e_lo, q.e_hi, q.dshift, c, mct, mcd, rho, w);
-      };
-      const int pos = warp_crossing<VE>(q.vt1 - q.vt0, t, wf);
-      __syncwarp();
-      tok = (ok && pos >= 0) ? q.e_base + pos : -1;
+  // the residual sums and sub-range sums of the position, once all carry the call's tag
+  const TagSum* ws = P.wsum + bk * P.nchunk_r;
+  const TagSum* wsb0 = P.wsub + bk * P.nchunk_r * kGroupWarps;
+  {
+    const long long t0 = clock64();
+    for (;;) {
+      bool good = true;
+      for (int i = ft; i < P.nchunk_r * (1 + kGroupWarps); i += kFinThreads)
+        good = good && (i < P.nchunk_r ? ld_tagsum(ws + i).t : ld_tagsum(wsb0 + (i - P.nchunk_r)).t) == P.tag;
+      if (fin_all(good)) break;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        raise_abort(P, sm);
+        break;
+      }
+      __nanosleep(128);
     }
-  } else {  // no residual mass: draw from p
+  }
+  // the leader picks the residual chunk and sub-range and stages the crossing pair
+  if (ft < 32) {
+    auto weight = [&](int c) { return ld_tagsum(ws + c).v; };
+    const float S = total_weight(P.nchunk_r, weight);
+    int state = 0;  // 0: no residual mass, 1: the crossing pair is being staged, 2: none found
+    int cstar = -1, sstar = -1;
+    float t = 0.f;
+    if (S > 0.f) {
+      state = 2;
+      const float tgt = __fmul_rn(u, S);
+      float bstar, sbase;
+      select_part(P.nchunk_r, tgt, weight, cstar, bstar);
+      if (cstar >= 0) {
+        const TagSum* wsb = wsb0 + (size_t)cstar * kGroupWarps;
+        select_part(kGroupWarps, __fsub_rn(tgt, bstar), [&](int i) { return ld_tagsum(wsb + i).v; }, sstar, sbase);
+        if (sstar >= 0) {
+          t = __fsub_rn(__fsub_rn(tgt, bstar), sbase);
+          const ResGeo<T> q = res_geo<T>(P, b, k, cstar * kResVec + sstar * kResSub, kResSub);
+          if (lane == 0) fence_proxy_async_shared();  // the group's earlier reads of fbuf come first
+          warp_stage<T>(fbuf, q.gt, P.V, q.vt0, q.vt1, &sm.fin_bar, lane);
+          warp_stage<T>(fbuf + (size_t)kFinDraftSlot * 16, q.gd, P.V, q.vd0, q.vd1, &sm.fin_bar, lane);
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&sm.fin_bar);
+          state = 1;
+        }
+      }
+    }
+    if (lane == 0) {
+      sm.gs.out[0] = state;
+      sm.gs.out[1] = cstar;
+      sm.gs.out[2] = sstar;
+      sm.gs.fout[0] = t;
+      sm.gs.fout[1] = (float)((double)S / ts.Z);
+    }
+  }
+  fin_sync();
+  const int state = sm.gs.out[0], cstar = sm.gs.out[1], sstar = sm.gs.out[2];
+  const float t = sm.gs.fout[0], rmass = sm.gs.fout[1];
+  fin_sync();
+  int tok = -1;
+  if (state == 1) {
+    const bool ok = fin_wait_only(P, sm, &sm.fin_bar, fph);
+    const ResGeo<T> q = res_geo<T>(P, b, k, cstar * kResVec + sstar * kResSub, kResSub);
+    const float c = P.c, mct = ts.mc, mcd = ds.mc;
+    const float rho = __fdiv_rn((float)ts.Z, (float)ds.Z);
+    auto wf = [&](int v, float (&w)[VE]) {
+      resid_weights<T>(fbuf, kFinDraftSlot, v, q.e_base, q.e_lo, q.e_hi, q.dshift, c, mct, mcd, rho, w);
+    };
+    const int pos = group_crossing<VE>(sm.gs, q.vt1 - q.vt0, t, wf);
+    tok = (ok && pos >= 0) ? q.e_base + pos : -1;
+  } else if (state == 0) {  // no residual mass: draw from p
     float unused;
-    uint32_t unused_ph = 0;
-    const CsReader rd = stage_request_stats(P, sm, b, false, unused_ph);
-    const DrawPlan d = draw_begin<T>(P, sm, fbuf, b, k, kFullP, -1);
+    SsRows none{0, 0};
+    CsReader rd;
+    rd.g = P.cstat + (size_t)b * P.rows * P.nchunk;
+    rd.s = nullptr;
+    rd.nchunk = P.nchunk;
+    const DrawPlan d = draw_begin<T>(P, sm, fbuf, b, k, kFullP, -1, none);
     tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, d, rd, ts, u, &unused);
   }
-  if (lane == 0) {
+  if (ft == 0) {
     const size_t o_k = (size_t)b * (P.K + 1) + k;
     if (k == n) {
       P.out_tokens[o_k] = tok;
-      if (P.residual_mass) P.residual_mass[b] = mass;
+      if (P.residual_mass) P.residual_mass[b] = rmass;
     }
     if (P.cand_tokens) P.cand_tokens[o_k] = tok;
-    if (P.pos_mass) P.pos_mass[o_k] = mass;
+    if (P.pos_mass) P.pos_mass[o_k] = rmass;
   }
 }
 
 // Greedy tree walk (section III.2): from the root, move to the child whose token equals the
-// argmax of the current node's row (lowest node index first) until none does.
+// argmax of the current node's row (lowest node index first) until none does.  The group checks
+// the tree, writes the per-node argmax and clears the outputs; the leader then walks and writes
+// the path.
 __device__ inline void walk_tree(const Params& P, Shared& sm, int b) {
-  const int lane = threadIdx.x & 31;
+  const int ft = fin_thread(), lane = ft & 31;
   const int N1 = P.R, V = P.V;
   const RowStat* rs = P.rstat + (size_t)b * N1;
   const int32_t* par = P.parents + (size_t)b * N1;
@@ -1311,18 +1513,25 @@ __device__ inline void walk_tree(const Params& P, Shared& sm, int b) {
   }
   int32_t* path = P.path_nodes + (size_t)b * N1;
   int32_t* out = P.out_tokens + (size_t)b * N1;
-  int err = 0;
-  for (int i = lane; i < N1; i += 32) {
-    err |= i < kFinRows ? sm.fin_rs[i].err : __ldcg(&rs[i].err);
+  int e = 0;
+  for (int i = ft; i < N1; i += kFinThreads) {
+    e |= i < kFinRows ? sm.fin_rs[i].err : __ldcg(&rs[i].err);
     const int p = par[i];
-    if (i == 0 ? (p != -1) : (p < 0 || p >= i)) err |= SPEC_ERRF_BAD_TREE;
+    if (i == 0 ? (p != -1) : (p < 0 || p >= i)) e |= SPEC_ERRF_BAD_TREE;
     if (i > 0) {
       const int t = tok[i];
-      if (t < 0 || t >= V) err |= SPEC_ERRF_BAD_TOKEN;
+      if (t < 0 || t >= V) e |= SPEC_ERRF_BAD_TOKEN;
     }
     if (P.node_argmax) P.node_argmax[(size_t)b * N1 + i] = i < kFinRows ? sm.fin_rs[i].amax : __ldcg(&rs[i].amax);
+    path[i] = -1;
+    out[i] = -1;
   }
-  err = warp_or(err);
+  // the error bits, agreed by the group (one barrier per bit)
+  int err = 0;
+  if (!fin_all(!(e & SPEC_ERRF_NONFINITE))) err |= SPEC_ERRF_NONFINITE;
+  if (!fin_all(!(e & SPEC_ERRF_BAD_TREE))) err |= SPEC_ERRF_BAD_TREE;
+  if (!fin_all(!(e & SPEC_ERRF_BAD_TOKEN))) err |= SPEC_ERRF_BAD_TOKEN;
+  if (ft >= 32) return;
   int len = 0;
   if (!err) {
     int cur = 0;
@@ -1348,25 +1557,19 @@ __device__ inline void walk_tree(const Params& P, Shared& sm, int b) {
       cur = next;
     }
   }
-  __syncwarp();
-  for (int i = lane; i < N1; i += 32) {
-    if (err || i > len) {
-      path[i] = -1;
-      out[i] = -1;
-    }
-  }
   if (lane == 0) {
     P.accept_len[b] = err ? 0 : len;
     if (P.err_flags) P.err_flags[b] = err;
   }
 }
 
-// Waits (bounded) until *count reaches `want`; false on a timeout or abort.  The count is read
-// with acquire semantics, so the statistics counted before it are visible afterwards.
+// Waits (bounded) until *count reaches `want`: the leader polls (with acquire semantics, so the
+// statistics counted before it are visible afterwards), then the group agrees.  False on a
+// timeout or abort.
 __device__ __forceinline__ bool wait_count(const Params& P, Shared& sm, const unsigned* count, unsigned want) {
-  const int lane = threadIdx.x & 31;
-  int ok = 0;
-  if (lane == 0) {
+  int ok = 1;
+  if (fin_thread() == 0) {
+    ok = 0;
     const long long t0 = clock64();
     for (;;) {
       if (ld_acquire_u32(count) >= want) {
@@ -1381,31 +1584,34 @@ __device__ __forceinline__ bool wait_count(const Params& P, Shared& sm, const un
       __nanosleep(64);
     }
   }
-  return __shfl_sync(kFull, ok, 0) != 0;
+  return fin_all(ok != 0);
 }
 
-// The finishing warp: requests b = blockIdx.x, blockIdx.x + gridDim.x, ...  The request's
-// inputs are loaded while its chunks are still being read.
+// The finishing group's loop over its requests.  A request's inputs are loaded while its chunks
+// are still being read.
 template <int MODE, typename T>
 __device__ void fin_loop(const Params& P, Shared& sm, unsigned char* fbuf) {
-  const int lane = threadIdx.x & 31;
+  const int ft = fin_thread();
   uint32_t fph = 0, csph = 0, ssph = 0;
   const unsigned per_req = (unsigned)(P.rows * P.nchunk);
   for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
     if constexpr (MODE == kTree) {
       const int N1 = P.R;
       if (N1 <= kFinRows) {
-        for (int i = lane; i < N1; i += 32) {
+        for (int i = ft; i < N1; i += kFinThreads) {
           sm.fin_par[i] = __ldg(P.parents + (size_t)b * N1 + i);
           sm.fin_tok[i] = __ldg(P.node_tokens + (size_t)b * N1 + i);
         }
       }
       if (!wait_count(P, sm, P.tick_a + b, per_req)) return;
-      const CsReader rd = stage_request_stats(P, sm, b, true, csph);
+      SsRows none{0, 0};
+      const CsReader rd = stage_request_stats(P, sm, b, none, csph);
       combine_rows<MODE>(P, sm, b, rd);
       walk_tree(P, sm, b);
+      fin_sync();  // the walk's reads of the shared copies come before the next request's writes
     } else {
-      const ReqPrefetch pf = prefetch_request<MODE, T>(P, b);
+      ReqPrefetch pf{0, 0.f, 0.f, 0.f, 0.f};
+      if (ft < 32) pf = prefetch_request<MODE, T>(P, b);
       if (!wait_count(P, sm, P.tick_a + b, per_req)) return;
       const int n = finish_chain<MODE, T>(P, sm, fbuf, fph, csph, ssph, b, pf);
       if constexpr (MODE == kChain) {
@@ -1452,7 +1658,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
   else if (warp == kBookWarp)
     book_loop<MODE>(P, sm);
   else
-    fin_loop<MODE, T>(P, sm, fbuf);
+    fin_loop<MODE, T>(P, sm, fbuf);  // warps kFinWarp .. kFinWarp + kFinWarps - 1
   __syncthreads();
   // The last CTA out reports a timed-out call (never expected) on every request.
   if (tid == 0) {
