@@ -351,7 +351,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
   }
   // residual claims (lane 0): the held items rfirst .. rfirst + rcnt - 1, and q0..q3, the result
   // words of request qb as last read
-  unsigned rfirst = 0, qb = 0xffffffffu;
+  unsigned rfirst = 0, qb = 0xffffffffu, rseen = 0;  // rseen: the cursor as this producer last saw it
   int rcnt = 0;
   bool rdone = P.npos == 0, qok = false;  // qok: request qb's result is complete
   unsigned long long q0 = 0, q1 = 0, q2 = 0, q3 = 0;
@@ -381,10 +381,12 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
         const bool sdone = cur + (unsigned)pos >= P.total;
         const bool boundary = pos == 0 || sdone;
         if (boundary && rcnt == 0 && !rdone) {
-          // once the stats items are out, one item at a time: the last requests' residual items
-          // then spread over as many producers as possible
-          const unsigned rk = sdone ? 1u : (unsigned)kClaim;
+          // batches shrink as the cursor nears the end (one item once the stats items are out), so
+          // that the last requests' residual items spread over as many producers as possible
+          const unsigned rrem = P.total_r > rseen ? P.total_r - rseen : 0u;
+          const unsigned rk = sdone ? 1u : max(1u, min((unsigned)kClaim, rrem / (2u * nprod)));
           const unsigned c = atomicAdd(P.rc, rk);
+          rseen = c + rk;
           if (c >= P.total_r) {
             rdone = true;
           } else {
@@ -434,7 +436,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
             raise_abort(P, sm);
             kind = kItemEnd;
           } else {
-            __nanosleep(512);
+            __nanosleep(128);
           }
         }
       }
@@ -1409,15 +1411,22 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
   const RowStat ds = read_rowstat(P, sm, b, P.R + k);
   const size_t bk = (size_t)b * P.npos + kk;
   const float u = __ldg(P.u + b);
-  // the residual sums and sub-range sums of the position, once all carry the call's tag
+  // the residual sums and sub-range sums of the position, once all carry the call's tag, copied
+  // into shared memory when they fit (the sub-chunk statistics' buffer is free here)
   const TagSum* ws = P.wsum + bk * P.nchunk_r;
   const TagSum* wsb0 = P.wsub + bk * P.nchunk_r * kGroupWarps;
+  const int nsum = P.nchunk_r * (1 + kGroupWarps);
+  float* cache = reinterpret_cast<float*>(sm.fin_ss);
+  const bool cached = nsum <= kFinSs * 4;
   {
     const long long t0 = clock64();
     for (;;) {
       bool good = true;
-      for (int i = ft; i < P.nchunk_r * (1 + kGroupWarps); i += kFinThreads)
-        good = good && (i < P.nchunk_r ? ld_tagsum(ws + i).t : ld_tagsum(wsb0 + (i - P.nchunk_r)).t) == P.tag;
+      for (int i = ft; i < nsum; i += kFinThreads) {
+        const TagSum e = i < P.nchunk_r ? ld_tagsum(ws + i) : ld_tagsum(wsb0 + (i - P.nchunk_r));
+        good = good && e.t == P.tag;
+        if (cached) cache[i] = e.v;
+      }
       if (fin_all(good)) break;
       if (clock64() - t0 > kWaitLimitCycles) {
         raise_abort(P, sm);
@@ -1428,7 +1437,7 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
   }
   // the leader picks the residual chunk and sub-range and stages the crossing pair
   if (ft < 32) {
-    auto weight = [&](int c) { return ld_tagsum(ws + c).v; };
+    auto weight = [&](int c) { return cached ? cache[c] : ld_tagsum(ws + c).v; };
     const float S = total_weight(P.nchunk_r, weight);
     int state = 0;  // 0: no residual mass, 1: the crossing pair is being staged, 2: none found
     int cstar = -1, sstar = -1;
@@ -1440,7 +1449,9 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
       select_part(P.nchunk_r, tgt, weight, cstar, bstar);
       if (cstar >= 0) {
         const TagSum* wsb = wsb0 + (size_t)cstar * kGroupWarps;
-        select_part(kGroupWarps, __fsub_rn(tgt, bstar), [&](int i) { return ld_tagsum(wsb + i).v; }, sstar, sbase);
+        const float* csb = cache + P.nchunk_r + cstar * kGroupWarps;
+        select_part(kGroupWarps, __fsub_rn(tgt, bstar),
+                    [&](int i) { return cached ? csb[i] : ld_tagsum(wsb + i).v; }, sstar, sbase);
         if (sstar >= 0) {
           t = __fsub_rn(__fsub_rn(tgt, bstar), sbase);
           const ResGeo<T> q = res_geo<T>(P, b, k, cstar * kResVec + sstar * kResSub, kResSub);
