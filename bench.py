@@ -2,9 +2,9 @@
 """Benchmark of the speculative-decoding verification step on GB300.
 
 One "step" is one verification call over one batch of the workload (all steps of the hot path:
-softmax statistics, acceptance scan, residual / bonus draw, or the tree argmax and walk): a
-ticket-clearing memset and one kernel launch, two for draft-model chains (the residual draw
-re-reads the rejected pair).  Default workload: chain verification with draft-model logits,
+softmax statistics, acceptance scan, residual / bonus draw, or the tree argmax and walk): one
+kernel launch (the residual pass of draft-model chains, which re-reads the rejected pair, runs
+inside it).  Default workload: chain verification with draft-model logits,
 B=64, K=5, V=128256, fp32, T=1.0 (704 logits rows, 361 MB per step).
 
 Prints ONE JSON line (rank 0).  `value` = verified logits rows per second (whole job), timed on
@@ -76,7 +76,7 @@ def rows_per_request(w: dict) -> int:
 
 def launches_per_step(w: dict) -> int:
     """Kernel launches of one call: verify_kernel, which also makes the residual pass of
-    draft-model chains (the ticket-clearing memset is not a kernel of this library)."""
+    draft-model chains."""
     return 1
 
 

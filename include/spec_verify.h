@@ -33,14 +33,18 @@
  *    token i whose cumulative weight exceeds u * (total weight); zero-weight tokens are never
  *    drawn.
  *  - Workspace: `workspace` (device memory, 256-byte aligned) must hold
- *    spec_verify_workspace_bytes(...) bytes.  Its contents need no initialisation and are
- *    scratch between calls: each call first clears its ticket counters (one cudaMemsetAsync of a
- *    few bytes per request on `stream`).  A workspace must not be shared by calls that may run
- *    concurrently.
+ *    spec_verify_workspace_bytes(...) bytes; its contents need no initialisation.  The first
+ *    call on a workspace (and the first after a change of B, rows or V) clears it with one
+ *    cudaMemsetAsync on `stream`; every call leaves it ready for the next (its counters zero,
+ *    its epoch advanced), so later calls of the same shape, graph replays included, skip the
+ *    clearing.  Between
+ *    calls the workspace belongs to the library: when anything else may have written to it (the
+ *    memory was freed and allocated again, say), call spec_verify_workspace_reset first.  A
+ *    workspace must not be shared by calls that may run concurrently.
  *  - Reads: every logits row is read from HBM once; a draft-model chain call that rejects at
  *    position n reads the target and draft rows at n a second time (the residual max(0, p - q)
- *    needs both rows' normalisers first).  A call is one memset and one kernel launch, or two
- *    launches for draft-model chains with T > 0 (three when probability rows are requested).
+ *    needs both rows' normalisers first).  A call is one kernel launch (two when probability
+ *    rows are requested), after the clearing above when there is one.
  */
 #ifndef SPEC_VERIFY_H
 #define SPEC_VERIFY_H
@@ -82,6 +86,11 @@ typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1, SPEC_DTYPE_F16 = 2 } spe
  * A workspace sized for more rows (or a larger B) also serves a smaller call.  Returns 0 for
  * invalid sizes. */
 size_t spec_verify_workspace_bytes(int B, int rows_per_request, int V, spec_dtype_t dtype);
+
+/* Marks `workspace` (the pointer a call was given) as holding contents the library did not leave
+ * there, so that its next call clears it first.  Host-side only; touches no memory and never
+ * fails.  Needed only when something other than these calls wrote to it. */
+void spec_verify_workspace_reset(const void *workspace);
 
 /*
  * Chain verification with a draft model or an EAGLE head (the draft side is logits).

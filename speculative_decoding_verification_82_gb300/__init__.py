@@ -8,6 +8,7 @@ from .binding import (  # noqa: F401
     SpecVerifyError,
     library,
     make_workspace,
+    workspace_reset,
     spec_verify_chain,
     spec_verify_ngram,
     spec_verify_tree_greedy,

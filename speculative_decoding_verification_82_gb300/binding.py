@@ -21,8 +21,8 @@ ERRF_BAD_TOKEN, ERRF_NONFINITE, ERRF_TIMEOUT, ERRF_BAD_TREE = 1, 2, 4, 8
 MAX_K, MAX_TREE_NODES = 256, 4096
 DTYPE_CODE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 
-EXPORTED = ("spec_verify_workspace_bytes", "spec_verify_chain", "spec_verify_ngram",
-            "spec_verify_tree_greedy", "spec_verify_chain_static", "spec_status_string")
+EXPORTED = ("spec_verify_workspace_bytes", "spec_verify_workspace_reset", "spec_verify_chain",
+            "spec_verify_ngram", "spec_verify_tree_greedy", "spec_verify_chain_static", "spec_status_string")
 STATIC_WORKSPACE_BYTES = 4 << 20
 
 _lib = None
@@ -44,6 +44,8 @@ def library(path: str | None = None) -> ctypes.CDLL:
     P, I, F, Z = c_void_p, c_int, c_float, c_size_t
     lib.spec_verify_workspace_bytes.argtypes = [I, I, I, I]
     lib.spec_verify_workspace_bytes.restype = Z
+    lib.spec_verify_workspace_reset.argtypes = [P]
+    lib.spec_verify_workspace_reset.restype = None
     lib.spec_verify_chain.argtypes = [P, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
     lib.spec_verify_chain.restype = I
     lib.spec_verify_ngram.argtypes = [P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
@@ -94,9 +96,17 @@ def workspace_bytes(B: int, rows_per_request: int, V: int, dtype: torch.dtype) -
 
 
 def make_workspace(B: int, rows_per_request: int, V: int, dtype: torch.dtype, device) -> torch.Tensor:
-    """A workspace for such calls (its contents need no initialisation)."""
+    """A workspace for such calls (new memory: its first call clears it)."""
     n = max(256, workspace_bytes(B, rows_per_request, V, dtype))
-    return torch.empty(n, dtype=torch.uint8, device=device)
+    ws = torch.empty(n, dtype=torch.uint8, device=device)
+    workspace_reset(ws)  # the caching allocator may hand out the block of an earlier workspace
+    return ws
+
+
+def workspace_reset(workspace: torch.Tensor) -> None:
+    """Tells the library that something other than its calls wrote to `workspace` (see
+    spec_verify_workspace_reset): the next call clears it first."""
+    library().spec_verify_workspace_reset(ctypes.c_void_p(workspace.data_ptr()))
 
 
 def _out(given, name, dtype, shape, device):

@@ -7,6 +7,8 @@
 
 #include <atomic>
 #include <climits>
+#include <cstring>
+#include <mutex>
 
 #include "spec_verify.h"
 #include "verify_kernel.cuh"
@@ -44,18 +46,18 @@ Chunking plan_chunks(int V, int S) {
 }
 
 // Workspace layout:
-//   work, gerr, exit_tick        u32 (128 B line)   } one region, cleared by one
-//   rc                           u32 (128 B line)   } cudaMemsetAsync per call
-//   tick_a  [B] u32              request tickets    }
+//   work, gerr, exit_tick, epoch u32 (128 B line)   } counters: zero between calls of one
+//   rc                           u32 (128 B line)   } shape (each call leaves them zero; the
+//   tick_a  [B] u32              request tickets    } first call of a shape clears them)
 //   tick_b  [B][rows] u32        residual tickets   }
-//   req     [B]                  ReqState           }  (16-byte aligned)
+//   req     [B]                  ReqState           (16-byte aligned; tagged per call)
 //   cstat   [B][rows][nchunk]    ChunkStat          (256-byte aligned regions from here on)
 //   sstat   [B][rows][nchunk][G] ChunkStat          sub-chunk partials (G consumer warps a group)
 //   rstat   [B][rows]            RowStat
 //   wsum    [B][rows][nchunk_r]  TagSum (float and tag)
 //   wsub    [B][rows][nchunk_r][G] TagSum
 struct Layout {
-  size_t work, tick_a, tick_b, req, clear_end, cstat, sstat, rstat, wsum, wsub, total;
+  size_t work, tick_a, tick_b, req, hdr_end, cstat, sstat, rstat, wsum, wsub, total;
 };
 
 Layout layout(int B, int rows, const Chunking& ck) {
@@ -70,7 +72,7 @@ Layout layout(int B, int rows, const Chunking& ck) {
   off = align_up(off + b * r * 4, 16);
   L.req = off;
   off += b * sizeof(ReqState);
-  L.clear_end = off;
+  L.hdr_end = off;
   off = align_up(off, 256);
   const size_t G = specv::kGroupWarps;
   L.cstat = off;
@@ -110,17 +112,60 @@ spec_status_t attach_workspace(Params& P, void* ws, size_t bytes, int B, int row
   P.work = reinterpret_cast<unsigned*>(w + L.work);
   P.gerr = P.work + 1;
   P.exit_tick = P.work + 2;
+  P.epoch = P.work + 3;
   P.rc = reinterpret_cast<unsigned*>(w + L.work + 128);  // residual cursor (a line of its own)
   P.tick_a = reinterpret_cast<unsigned*>(w + L.tick_a);
   P.tick_b = reinterpret_cast<unsigned*>(w + L.tick_b);
   P.req = reinterpret_cast<ReqState*>(w + L.req);
-  P.clear_bytes = L.clear_end - L.work;
   P.cstat = reinterpret_cast<ChunkStat*>(w + L.cstat);
   P.sstat = reinterpret_cast<ChunkStat*>(w + L.sstat);
   P.rstat = reinterpret_cast<RowStat*>(w + L.rstat);
   P.wsum = reinterpret_cast<specv::TagSum*>(w + L.wsum);
   P.wsub = reinterpret_cast<specv::TagSum*>(w + L.wsub);
+  P.ws_base = ws;
+  P.ws_bytes = L.total;
+  P.ws_shape[0] = B;
+  P.ws_shape[1] = rows;
+  P.ws_shape[2] = ck.nchunk;
+  P.ws_shape[3] = ck.nchunk_r;
   return SPEC_OK;
+}
+
+// A workspace's counters are zero between calls (each call leaves them so) and its epoch names the
+// last call's tag, but only for calls of one layout: a call of another shape may keep counters
+// where the last one left other data, and the statistics there may carry any tag.  So the whole
+// workspace (of this call's layout) is cleared on the first call of a shape on it (a workspace not
+// seen before included): counters and epoch zero, every tag zero, which no call's tag matches.
+// While the shape stays it is not cleared again.  The shapes of the last kWsSeen workspaces are
+// kept; one that falls out of the table is simply cleared again.
+constexpr int kWsSeen = 64;
+struct WsSeen {
+  const void* ws;
+  int shape[4];
+};
+std::mutex g_ws_mu;
+WsSeen g_ws_seen[kWsSeen];
+int g_ws_next = 0;
+// True when the call must clear the header first; `forget` drops the entry (a failed launch).
+bool workspace_needs_clear(const Params& P, bool forget) {
+  std::lock_guard<std::mutex> g(g_ws_mu);
+  for (int i = 0; i < kWsSeen; ++i) {
+    WsSeen& e = g_ws_seen[i];
+    if (e.ws != P.ws_base) continue;
+    if (forget) {
+      e.ws = nullptr;
+      return false;
+    }
+    if (std::memcmp(e.shape, P.ws_shape, sizeof(e.shape)) == 0) return false;
+    std::memcpy(e.shape, P.ws_shape, sizeof(e.shape));
+    return true;
+  }
+  if (forget) return false;
+  WsSeen& e = g_ws_seen[g_ws_next];
+  g_ws_next = (g_ws_next + 1) % kWsSeen;
+  e.ws = P.ws_base;
+  std::memcpy(e.shape, P.ws_shape, sizeof(e.shape));
+  return true;
 }
 
 // Constants of the item decoding's divisions (see fastdiv.h).
@@ -133,28 +178,23 @@ void set_divisors(Params& P, int rows) {
   P.fd_nchunk_r = specv::make_fastdiv((unsigned)P.nchunk_r);
 }
 
-// A fresh tag for every call (never 0, the value of cleared memory): the statistics a call writes
-// carry it, so that its readers can tell them from what earlier calls left in the workspace.
-unsigned next_call_tag() {
-  static std::atomic<unsigned> counter{0};
-  unsigned t = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
-  if (t == 0u) t = counter.fetch_add(1u, std::memory_order_relaxed) + 1u;
-  return t;
-}
-
 spec_status_t launch(spec_dtype_t dtype, int mode, Params& P, specv::LaunchPlan& L, cudaStream_t stream) {
-  P.tag = next_call_tag();
+  if (workspace_needs_clear(P, false) && cudaMemsetAsync(P.ws_base, 0, P.ws_bytes, stream) != cudaSuccess) {
+    workspace_needs_clear(P, true);
+    return SPEC_ERR_CUDA;
+  }
   L.smem = (size_t)specv::kStages * specv::kStageBytes + specv::kFinBytes;
-  // the ticket counters and acceptance flags start every call at zero, whatever the workspace
-  // held before
-  cudaError_t e = cudaMemsetAsync(P.work, 0, P.clear_bytes, stream);
-  if (e != cudaSuccess) return SPEC_ERR_CUDA;
+  cudaError_t e = cudaSuccess;
   switch (dtype) {
     case SPEC_DTYPE_F32: e = specv::launch_verify<float>(mode, P, L, stream); break;
     case SPEC_DTYPE_BF16: e = specv::launch_verify<__nv_bfloat16>(mode, P, L, stream); break;
     default: e = specv::launch_verify<__half>(mode, P, L, stream); break;
   }
-  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  if (e != cudaSuccess) {
+    workspace_needs_clear(P, true);  // the next call clears again
+    return SPEC_ERR_CUDA;
+  }
+  return SPEC_OK;
 }
 
 // Shared body of spec_verify_chain / spec_verify_ngram.
@@ -232,6 +272,12 @@ size_t spec_verify_workspace_bytes(int B, int rows_per_request, int V, spec_dtyp
   if (B < 0 || rows_per_request < 1 || V < 1 || !dtype_ok(dtype)) return 0;
   const Chunking ck = plan_chunks(V, elem_size(dtype));
   return layout(B, rows_per_request, ck).total;
+}
+
+void spec_verify_workspace_reset(const void* workspace) {
+  Params P = {};
+  P.ws_base = const_cast<void*>(workspace);
+  workspace_needs_clear(P, true);
 }
 
 spec_status_t spec_verify_chain(const void* target_logits, const void* draft_logits, spec_dtype_t dtype, int B,

@@ -225,6 +225,11 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
     if (*abort || clock64() - t0 > kWaitLimitCycles) return false;
   }
 }
+// mbar_wait by every lane of a warp, with one outcome for the whole warp (false if any lane gave
+// up), so that the warp leaves together.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, const volatile int* abort) {
+  return __all_sync(kFull, mbar_wait(bar, parity, abort));
+}
 // Bulk (non-tensor) TMA copy global -> this CTA's shared memory, completing on `bar`.
 // Both addresses 16-byte aligned, size a multiple of 16.
 __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -369,6 +374,12 @@ __device__ __forceinline__ bool fin_all(bool p) {
       : "r"((uint32_t)p), "n"(kFinBarrier), "n"(kFinThreads)
       : "memory");
   return r != 0;
+}
+// True in every thread once the leader has waited longer than the limit since t0: a retry loop
+// of the group must be left by all its threads together (threads that took different ways would
+// meet different barrier instructions), so the leader's clock decides for all.
+__device__ __forceinline__ bool fin_timed_out(long long t0) {
+  return !fin_all(!(fin_thread() == 0 && clock64() - t0 > kWaitLimitCycles));
 }
 // Shared-memory scratch of the group's reductions and broadcasts.
 struct GroupScratch {

@@ -65,14 +65,13 @@ struct __align__(16) RowStat {
   int pad[3];
 };
 // Per request: the acceptance result as four self-validating 64-bit words (each a single-copy
-// atomic store whose low half is kReqTag), so that readers need no fence and no other read:
-// w[0] = n | err << 16 in the high half; w[1..3] = the fp32 bits of RN(m_t c), RN(m_d c) and
-// Z_t / Z_d at row n (draft-model chains that rejected, without per-position outputs).  The
-// workspace clearing at the start of every call zeroes them.
+// atomic store whose low half is the call's tag), so that readers need no fence and no other
+// read, and words an earlier call left never pass: w[0] = n | err << 16 in the high half;
+// w[1..3] = the fp32 bits of RN(m_t c), RN(m_d c) and Z_t / Z_d at row n (draft-model chains that
+// rejected, without per-position outputs).
 struct __align__(16) ReqState {
   unsigned long long w[4];
 };
-constexpr unsigned kReqTag = 0x5EC0DE01u;
 static_assert(sizeof(ChunkStat) == 16 && sizeof(RowStat) == 32 && sizeof(ReqState) == 32, "layout");
 __device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned long long* p) {
   return *reinterpret_cast<const volatile unsigned long long*>(p);
@@ -80,7 +79,7 @@ __device__ __forceinline__ unsigned long long ld_volatile_u64(const unsigned lon
 __device__ __forceinline__ void st_volatile_u64(unsigned long long* p, unsigned long long v) {
   *reinterpret_cast<volatile unsigned long long*>(p) = v;
 }
-__device__ __forceinline__ bool req_word_ok(unsigned long long v) { return (unsigned)v == kReqTag; }
+__device__ __forceinline__ bool req_word_ok(unsigned long long v, unsigned tag) { return (unsigned)v == tag; }
 __device__ __forceinline__ unsigned req_word_hi(unsigned long long v) { return (unsigned)(v >> 32); }
 
 struct Params {
@@ -121,14 +120,19 @@ struct Params {
   ReqState* req;        // [B]
   TagSum* wsum;         // [B][npos][nchunk_r] residual weight per residual item
   TagSum* wsub;         // [B][npos][nchunk_r][kGroupWarps] residual weight per sub-range
-  unsigned tag;         // this call's tag (never 0: cleared memory never matches it)
-  unsigned* work;            // stats-item counter   } cleared by the host before each call
-  unsigned* gerr;            // timeout flag           }
-  unsigned* exit_tick;       // exiting CTAs           }
-  unsigned* rc;              // next residual item     }
-  unsigned* tick_a;     // [B] chunks in, per request          }
-  unsigned* tick_b;     // [B][npos] residual items in         }  (req[] is cleared too)
-  size_t clear_bytes;   // bytes from `work` through req[B - 1]
+  unsigned* epoch;      // the tag of the workspace's last call (0 after the workspace is cleared)
+  // host only: the workspace, its bytes in this call's layout, and the shape of that layout
+  void* ws_base;
+  size_t ws_bytes;
+  int ws_shape[4];
+  // counters, zero between calls: every call leaves them as it found them (see the kernel's end);
+  // `epoch` (below) is the one word that a call advances
+  unsigned* work;            // stats-item counter
+  unsigned* gerr;            // timeout flag
+  unsigned* exit_tick;       // exiting CTAs
+  unsigned* rc;              // next residual item
+  unsigned* tick_a;     // [B] chunks in, per request (zeroed by its finishing group once complete)
+  unsigned* tick_b;     // [B][npos] residual items in (likewise)
 };
 
 template <typename T>
@@ -228,6 +232,7 @@ struct Shared {
   RowStat fin_rs[kFinRows];
   int fin_par[kFinRows], fin_tok[kFinRows];  // a small tree's parents and tokens
   GroupScratch gs;                            // the finishing group's reductions and broadcasts
+  unsigned tag;  // this call's tag: the workspace's epoch + 1 (never 0, the value of cleared memory)
 };
 
 __device__ __forceinline__ void raise_abort(const Params& P, Shared& sm) {
@@ -262,12 +267,12 @@ __device__ __forceinline__ void skip_residual(const Params& P, unsigned b) {
 }
 // A request's acceptance result as its four words read it: every word valid, or only the first
 // when that one says no residual parameters follow (an error, per-position outputs, or n = K).
-__device__ __forceinline__ bool result_complete(const Params& P, unsigned long long q0, unsigned long long q1,
-                                                unsigned long long q2, unsigned long long q3) {
-  if (!req_word_ok(q0)) return false;
+__device__ __forceinline__ bool result_complete(const Params& P, unsigned tag, unsigned long long q0,
+                                                unsigned long long q1, unsigned long long q2, unsigned long long q3) {
+  if (!req_word_ok(q0, tag)) return false;
   const unsigned hi = req_word_hi(q0);
   if ((hi >> 16) != 0u || P.diag || (int)(hi & 0xFFFFu) >= P.K) return true;
-  return req_word_ok(q1) && req_word_ok(q2) && req_word_ok(q3);
+  return req_word_ok(q1, tag) && req_word_ok(q2, tag) && req_word_ok(q3, tag);
 }
 
 // Geometry of the target grid vectors [vt0, vt0 + span) of the pair at position k (a residual
@@ -361,7 +366,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
   float rmct = 0.f, rmcd = 0.f, rrho = 0.f;
   for (;; it += kGroups) {
     const int s = it % kStages;
-    if (!mbar_wait(&sm.empty[s], ((uint32_t)(it / kStages) & 1u) ^ 1u, &sm.abort)) {
+    if (!mbar_wait_warp(&sm.empty[s], ((uint32_t)(it / kStages) & 1u) ^ 1u, &sm.abort)) {
       if (lane == 0) raise_abort(P, sm);
       break;
     }
@@ -399,7 +404,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
         if (rcnt > 0 && !rready && boundary) {
           // the words read at the previous batch start (in by now), else read them again: used at
           // the next batch start, or now once the stats items are out
-          if (nb == qb && result_complete(P, q0, q1, q2, q3)) {
+          if (nb == qb && result_complete(P, sm.tag, q0, q1, q2, q3)) {
             qok = rready = true;
           } else {
             const unsigned long long* rw = P.req[nb].w;
@@ -409,7 +414,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
             q2 = ld_volatile_u64(rw + 2);
             q3 = ld_volatile_u64(rw + 3);
             qok = false;
-            if (sdone) qok = rready = result_complete(P, q0, q1, q2, q3);
+            if (sdone) qok = rready = result_complete(P, sm.tag, q0, q1, q2, q3);
           }
         }
         if (rready) {
@@ -647,17 +652,17 @@ __device__ __forceinline__ void publish_chunk(const Params& P, Shared& sm, const
 #pragma unroll
       for (int o = 1; o < kGroupWarps; o <<= 1) sv = __fadd_rn(sv, __shfl_xor_sync(kFull, sv, o));
       // (a NaN or +inf maximum carries the chunk's non-finite flag)
-      q = make_uint4(__float_as_uint(M), P.tag, __float_as_uint(sv), P.tag);
+      q = make_uint4(__float_as_uint(M), sm.tag, __float_as_uint(sv), sm.tag);
       if (mine)  // the sub-chunk partials, for the draws
         *reinterpret_cast<uint4*>(P.sstat + ci * kGroupWarps + lane) =
-            make_uint4(__float_as_uint(pw.x), P.tag, __float_as_uint(pw.y), P.tag);
+            make_uint4(__float_as_uint(pw.x), sm.tag, __float_as_uint(pw.y), sm.tag);
     } else {
       float v = mine ? pw.x : -INFINITY;
       int i = mine ? __float_as_int(pw.y) : INT_MAX;
 #pragma unroll
       for (int o = 1; o < kGroupWarps; o <<= 1)
         argmax_merge(v, i, __shfl_xor_sync(kFull, v, o), __shfl_xor_sync(kFull, i, o));
-      q = make_uint4(__float_as_uint(v), P.tag, (unsigned)i, P.tag);
+      q = make_uint4(__float_as_uint(v), sm.tag, (unsigned)i, sm.tag);
     }
     if (lane == 0) *reinterpret_cast<uint4*>(P.cstat + ci) = q;
     pm.tick = P.tick_a + m.b;
@@ -667,8 +672,8 @@ __device__ __forceinline__ void publish_chunk(const Params& P, Shared& sm, const
     for (int o = 1; o < kGroupWarps; o <<= 1) sum = __fadd_rn(sum, __shfl_xor_sync(kFull, sum, o));
     const size_t bk = (size_t)m.b * P.npos + m.kk;
     const size_t ri = bk * P.nchunk_r + m.ch;
-    if (lane == 0) *reinterpret_cast<uint2*>(P.wsum + ri) = make_uint2(__float_as_uint(sum), P.tag);
-    if (mine) *reinterpret_cast<uint2*>(P.wsub + ri * kGroupWarps + lane) = make_uint2(__float_as_uint(pw.x), P.tag);
+    if (lane == 0) *reinterpret_cast<uint2*>(P.wsum + ri) = make_uint2(__float_as_uint(sum), sm.tag);
+    if (mine) *reinterpret_cast<uint2*>(P.wsub + ri * kGroupWarps + lane) = make_uint2(__float_as_uint(pw.x), sm.tag);
     pm.tick = P.tick_b + bk;
   }
   __syncwarp();
@@ -686,7 +691,7 @@ __device__ void consumer_loop(const Params& P, Shared& sm, const unsigned char* 
   const int grp = warp / kGroupWarps, gw = warp % kGroupWarps;
   for (int it = grp;; it += kGroups) {
     const int s = it % kStages;
-    if (!mbar_wait(&sm.full[s], (uint32_t)(it / kStages) & 1u, &sm.abort)) {
+    if (!mbar_wait_warp(&sm.full[s], (uint32_t)(it / kStages) & 1u, &sm.abort)) {
       if (lane == 0) raise_abort(P, sm);
       return;
     }
@@ -700,7 +705,7 @@ __device__ void consumer_loop(const Params& P, Shared& sm, const unsigned char* 
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[s]);
     const int j = it % kSlots;
-    if (!mbar_wait(&sm.pempty[j], ((uint32_t)(it / kSlots) & 1u) ^ 1u, &sm.abort)) {
+    if (!mbar_wait_warp(&sm.pempty[j], ((uint32_t)(it / kSlots) & 1u) ^ 1u, &sm.abort)) {
       if (lane == 0) raise_abort(P, sm);
       return;
     }
@@ -746,7 +751,8 @@ __device__ void book_loop(const Params& P, Shared& sm) {
       pick = __shfl_sync(kFull, pick, 0);
       if (pick < 0) {
         if (nb > 0) break;  // publish what this batch holds
-        if (aborted(sm) || clock64() - t_idle > kWaitLimitCycles) {
+        // (lane 0's clock decides for the warp, which leaves together)
+        if (__shfl_sync(kFull, (aborted(sm) || clock64() - t_idle > kWaitLimitCycles) ? 1 : 0, 0)) {
           if (lane == 0) raise_abort(P, sm);
           ended0 = ended1 = true;
           break;
@@ -872,10 +878,10 @@ __device__ __forceinline__ bool await_tagged(const Params& P, Shared& sm, const 
   const long long t0 = clock64();
   for (;;) {
     bool good = true;
-    for (int i = fin_thread(); i < n; i += kFinThreads) good = good && cs_ok(ld_chunkstat(p + i), P.tag);
+    for (int i = fin_thread(); i < n; i += kFinThreads) good = good && cs_ok(ld_chunkstat(p + i), sm.tag);
     if (fin_all(good)) return true;
-    if (clock64() - t0 > kWaitLimitCycles) {
-      raise_abort(P, sm);
+    if (fin_timed_out(t0)) {
+      if (fin_thread() == 0) raise_abort(P, sm);
       return false;
     }
     __nanosleep(128);
@@ -922,10 +928,10 @@ __device__ __forceinline__ CsReader stage_request_stats(const Params& P, Shared&
     }
     bool good = true;
     for (int i = fin_thread(); i < n + nsx; i += kFinThreads)
-      good = good && cs_ok(i < n ? sm.fin_cs[i] : sm.fin_ss[i - n], P.tag);
+      good = good && cs_ok(i < n ? sm.fin_cs[i] : sm.fin_ss[i - n], sm.tag);
     if (fin_all(good)) break;  // (the barrier also ends the group's reads before a new copy)
-    if (clock64() - t0 > kWaitLimitCycles) {
-      raise_abort(P, sm);
+    if (fin_timed_out(t0)) {
+      if (fin_thread() == 0) raise_abort(P, sm);
       ss.n = 0;
       return rd;
     }
@@ -1021,7 +1027,7 @@ __device__ int draw_end(const Params& P, Shared& sm, unsigned char* fbuf, uint32
     ok = fin_wait_only(P, sm, &sm.ss_bar, ssph);
     // a staged entry without the call's tag is not in yet: take the row from global memory then
     bool good = true;
-    for (int i = ft; i < P.nchunk * kGroupWarps; i += kFinThreads) good = good && cs_ok(sm.fin_ss[i], P.tag);
+    for (int i = ft; i < P.nchunk * kGroupWarps; i += kFinThreads) good = good && cs_ok(sm.fin_ss[i], sm.tag);
     if (!fin_all(good)) sss = nullptr;
   }
   if (d.kind == kExcl) ok = fin_wait_only(P, sm, &sm.fin_bar, fph) && ok;
@@ -1361,7 +1367,7 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
         const RowStat t = read_rowstat(P, sm, b, n), d = read_rowstat(P, sm, b, P.R + n);
         hi = __float_as_uint(lane == 1 ? t.mc : lane == 2 ? d.mc : __fdiv_rn((float)t.Z, (float)d.Z));
       }
-      st_volatile_u64(P.req[b].w + lane, ((unsigned long long)hi << 32) | kReqTag);
+      st_volatile_u64(P.req[b].w + lane, ((unsigned long long)hi << 32) | sm.tag);
     }
     __syncwarp();
   }
@@ -1418,31 +1424,34 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
   const int nsum = P.nchunk_r * (1 + kGroupWarps);
   float* cache = reinterpret_cast<float*>(sm.fin_ss);
   const bool cached = nsum <= kFinSs * 4;
+  bool sums_ok = true;
   {
     const long long t0 = clock64();
     for (;;) {
       bool good = true;
       for (int i = ft; i < nsum; i += kFinThreads) {
         const TagSum e = i < P.nchunk_r ? ld_tagsum(ws + i) : ld_tagsum(wsb0 + (i - P.nchunk_r));
-        good = good && e.t == P.tag;
+        good = good && e.t == sm.tag;
         if (cached) cache[i] = e.v;
       }
       if (fin_all(good)) break;
-      if (clock64() - t0 > kWaitLimitCycles) {
-        raise_abort(P, sm);
+      if (fin_timed_out(t0)) {
+        if (ft == 0) raise_abort(P, sm);
+        sums_ok = false;
         break;
       }
       __nanosleep(128);
     }
   }
-  // the leader picks the residual chunk and sub-range and stages the crossing pair
+  // the leader picks the residual chunk and sub-range and stages the crossing pair (no draw
+  // after a timeout)
   if (ft < 32) {
     auto weight = [&](int c) { return cached ? cache[c] : ld_tagsum(ws + c).v; };
-    const float S = total_weight(P.nchunk_r, weight);
-    int state = 0;  // 0: no residual mass, 1: the crossing pair is being staged, 2: none found
+    const float S = sums_ok ? total_weight(P.nchunk_r, weight) : 0.f;
+    int state = sums_ok ? 0 : 2;  // 0: no residual mass, 1: the crossing pair is being staged, 2: none
     int cstar = -1, sstar = -1;
     float t = 0.f;
-    if (S > 0.f) {
+    if (sums_ok && S > 0.f) {
       state = 2;
       const float tgt = __fmul_rn(u, S);
       float bstar, sbase;
@@ -1615,6 +1624,7 @@ __device__ void fin_loop(const Params& P, Shared& sm, unsigned char* fbuf) {
         }
       }
       if (!wait_count(P, sm, P.tick_a + b, per_req)) return;
+      if (ft == 0) P.tick_a[b] = 0;  // complete: the count is left as the next call expects it
       SsRows none{0, 0};
       const CsReader rd = stage_request_stats(P, sm, b, none, csph);
       combine_rows<MODE>(P, sm, b, rd);
@@ -1624,12 +1634,14 @@ __device__ void fin_loop(const Params& P, Shared& sm, unsigned char* fbuf) {
       ReqPrefetch pf{0, 0.f, 0.f, 0.f, 0.f};
       if (ft < 32) pf = prefetch_request<MODE, T>(P, b);
       if (!wait_count(P, sm, P.tick_a + b, per_req)) return;
+      if (ft == 0) P.tick_a[b] = 0;  // complete: the count is left as the next call expects it
       const int n = finish_chain<MODE, T>(P, sm, fbuf, fph, csph, ssph, b, pf);
       if constexpr (MODE == kChain) {
         if (P.npos > 0 && n >= 0) {
           for (int kk = 0; kk < P.npos; ++kk) {
             if (!P.diag && n >= P.K) break;  // everything accepted: the bonus draw was made above
             if (!wait_count(P, sm, P.tick_b + (size_t)b * P.npos + kk, (unsigned)P.nchunk_r)) return;
+            if (ft == 0) P.tick_b[(size_t)b * P.npos + kk] = 0;
             residual_draw<T>(P, sm, fbuf, fph, ssph, b, kk, n);
           }
         }
@@ -1644,6 +1656,10 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ Shared sm;
   const int tid = threadIdx.x, warp = tid >> 5;
+  // this call's tag: one past the workspace's last (its epoch, left by the last CTA of the
+  // previous call), so that calls replayed from a captured graph get fresh tags too; read first,
+  // so that its latency overlaps the barrier setup
+  const unsigned e = tid == 0 ? __ldg(P.epoch) : 0u;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -1658,6 +1674,7 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
     mbar_init(&sm.cs_bar, 1);
     mbar_init(&sm.ss_bar, 1);
     sm.abort = 0;
+    sm.tag = (e + 1u) != 0u ? e + 1u : 1u;
     fence_mbar_init();
   }
   __syncthreads();
@@ -1671,7 +1688,9 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
   else
     fin_loop<MODE, T>(P, sm, fbuf);  // warps kFinWarp .. kFinWarp + kFinWarps - 1
   __syncthreads();
-  // The last CTA out reports a timed-out call (never expected) on every request.
+  // The last CTA out reports a timed-out call (never expected) on every request, and leaves the
+  // counters zero for the next call (after a timeout the counts too: finishing groups that gave
+  // up did not zero theirs).
   if (tid == 0) {
     __threadfence();
     sm.last = atomicAdd(P.exit_tick, 1u) == gridDim.x - 1;
@@ -1679,7 +1698,18 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
   __syncthreads();
   if (sm.last) {
     __threadfence();
-    if (ld_volatile(reinterpret_cast<const int*>(P.gerr))) {
+    const bool timed_out = ld_volatile(reinterpret_cast<const int*>(P.gerr)) != 0;
+    __syncthreads();  // every thread has read the flag before it is reset
+    if (tid == 0) {
+      *P.work = 0u;
+      *P.rc = 0u;
+      *P.gerr = 0u;
+      *P.exit_tick = 0u;
+      *P.epoch = sm.tag;
+    }
+    if (timed_out) {
+      for (int i = tid; i < P.B; i += kThreads) P.tick_a[i] = 0u;
+      for (int i = tid; i < P.B * P.npos; i += kThreads) P.tick_b[i] = 0u;
       const int width = (MODE == kTree) ? P.R : P.K + 1;
       for (int b = tid; b < P.B; b += kThreads) {
         if (P.err_flags) P.err_flags[b] = SPEC_ERRF_TIMEOUT;
@@ -1703,7 +1733,8 @@ __global__ void __launch_bounds__(256) probs_kernel(const Params P) {
   const int rowid = blockIdx.x;  // b * rows + r
   const int b = rowid / P.rows, r = rowid - b * P.rows;
   const unsigned long long w0 = P.req[b].w[0];
-  if (!req_word_ok(w0) || (req_word_hi(w0) >> 16) != 0u) return;  // no result, or an error
+  // (the verification kernel before this one left its tag as the epoch)
+  if (!req_word_ok(w0, *P.epoch) || (req_word_hi(w0) >> 16) != 0u) return;  // no result, or an error
   float* out = r < P.R ? (P.target_probs ? P.target_probs + ((size_t)b * P.R + r) * P.V : nullptr)
                        : (P.draft_probs ? P.draft_probs + ((size_t)b * P.K + (r - P.R)) * P.V : nullptr);
   if (!out) return;

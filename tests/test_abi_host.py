@@ -109,3 +109,10 @@ def test_tree_validation(lib):
     assert call(N=5000) == binding.SPEC_ERR_UNSUPPORTED
     assert call(par=0) == binding.SPEC_ERR_INVALID_ARG
     assert call(wsb=10) == binding.SPEC_ERR_WORKSPACE
+
+
+def test_workspace_reset_is_host_only(lib):
+    # marks a pointer for clearing at its next call; touches no memory, so any pointer is fine
+    lib.spec_verify_workspace_reset(None)
+    lib.spec_verify_workspace_reset(ctypes.c_void_p(0x1000))
+    lib.spec_verify_workspace_reset(ctypes.c_void_p(0x1000))

@@ -242,8 +242,9 @@ def test_many_small_requests():
 
 
 def test_workspace_reuse_and_determinism():
-    """One workspace serves calls of different modes, batch sizes and vocabularies in turn, stale
-    contents do not matter, and repeated calls give identical results."""
+    """One workspace serves calls of different modes, batch sizes and vocabularies in turn (each
+    change of shape clears its counter header), contents written by anything else do not matter
+    after a reset, and repeated calls give identical results."""
     ws = binding.make_workspace(64, 11, 20000, torch.float32, "cuda")
     a = synth.chain_batched(seed=5, B=4, V=20000)
     b = synth.ngram(seed=5, B=64, V=20000)
@@ -257,7 +258,10 @@ def test_workspace_reuse_and_determinism():
     parity.compare_chain(ga1, parity.run_oracle_chain(a), a)
     parity.compare_chain(gb, parity.run_oracle_chain(b, ngram=True), b)
     parity.compare_tree(gt, parity.run_oracle_tree(t))
-    ws.fill_(0xAB)  # arbitrary stale contents must not matter
+    # contents written by something else: after a reset (the calls clear the counter header again)
+    # arbitrary stale contents do not matter
+    ws.fill_(0xAB)
+    binding.workspace_reset(ws)
     ga3 = parity.run_gpu_chain(a, workspace=ws)
     for key in ga1:
         assert np.array_equal(ga1[key], ga3[key]), key
@@ -269,3 +273,41 @@ def test_non_default_stream():
     with torch.cuda.stream(s):
         g = parity.run_gpu_chain(ci)
     parity.compare_chain(g, parity.run_oracle_chain(ci), ci)
+
+
+def test_graph_replays_get_fresh_tags():
+    """A call captured in a CUDA graph and replayed with new inputs in the same buffers: every
+    replay is a new call (its statistics carry a fresh tag from the workspace's epoch), so each
+    replay's outputs match the oracle for the inputs it saw."""
+    cis = [synth.chain_batched(seed=s, B=4, V=20000) for s in (21, 22, 23)]
+    c0 = cis[0]
+    B, K, V = c0.B, c0.K, c0.V
+    tl = parity.to_device(c0.target, c0.dtype)
+    dl = parity.to_device(c0.draft, c0.dtype)
+    x, r, u = parity.i32(c0.draft_tokens), parity.f32(c0.r), parity.f32(c0.u)
+    ws = binding.make_workspace(B, 2 * K + 1, V, tl.dtype, "cuda")
+    out = dict(num_accepted=torch.empty(B, dtype=torch.int32, device="cuda"),
+               out_tokens=torch.empty((B, K + 1), dtype=torch.int32, device="cuda"),
+               residual_mass=torch.empty(B, device="cuda"),
+               err_flags=torch.empty(B, dtype=torch.int32, device="cuda"))
+    ap = torch.empty((B, K), device="cuda")
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):  # the first call (which clears the workspace) outside the graph
+        binding.spec_verify_chain(tl, dl, x, r, u, float(c0.temperature), workspace=ws, out=out, accept_prob=ap)
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        binding.spec_verify_chain(tl, dl, x, r, u, float(c0.temperature), workspace=ws, out=out, accept_prob=ap)
+    for ci in cis + cis[:1]:
+        tl.copy_(parity.to_device(ci.target, ci.dtype))
+        dl.copy_(parity.to_device(ci.draft, ci.dtype))
+        x.copy_(parity.i32(ci.draft_tokens))
+        r.copy_(parity.f32(ci.r))
+        u.copy_(parity.f32(ci.u))
+        g.replay()
+        torch.cuda.synchronize()
+        res = {k: v.cpu().numpy() for k, v in out.items()}
+        res["accept_prob"] = ap.cpu().numpy()
+        parity.compare_chain(res, parity.run_oracle_chain(ci), ci)
