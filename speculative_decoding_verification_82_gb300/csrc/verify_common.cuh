@@ -31,6 +31,7 @@ constexpr int kThreads = (kFinWarp + kFinWarps) * 32;
 constexpr int kStages = 6;                         // staged-chunk ring depth (a multiple of kGroups)
 constexpr int kSlots = 16;                         // ring of per-chunk results (partials, merged)
 constexpr int kClaim = 4;                          // work items claimed per atomic
+constexpr int kL2KeepPositions = 1;                // chains: positions whose rows L2 keeps longer
 constexpr int kChunkVec = 2048;                    // 16-byte vectors per chunk of a row (32 KB)
 constexpr int kSubVec = kChunkVec / kGroupWarps;   // vectors per consumer warp (a sub-chunk)
 constexpr int kVecPerLane = kSubVec / 32;
@@ -239,6 +240,26 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const void* src, uint32_t
       "l"(src), "r"(bytes), "r"(smem_addr(bar))
       : "memory");
 }
+// The same copy with an L2 eviction priority for the lines it reads (a policy from l2_policy).
+__device__ __forceinline__ void tma_load_1d_hint(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                                 uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_addr(dst)),
+      "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+      : "memory");
+}
+// L2 eviction priorities of bulk copies: none (the default), evict-first (read once), or
+// evict-last (read again soon).
+enum L2Hint : int { kL2Normal = 0, kL2First = 1, kL2Last = 2 };
+__device__ __forceinline__ uint64_t l2_policy(int hint) {
+  uint64_t p;
+  if (hint == kL2Last)
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+  else
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
 __device__ __forceinline__ int ld_volatile(const int* p) { return *reinterpret_cast<const volatile int*>(p); }
 // Load with acquire semantics at GPU scope: later reads see what the writer published before it
 // released the value (no fence, so earlier stores of this thread need not drain first).
@@ -324,11 +345,12 @@ __device__ __forceinline__ RowGrid<T> row_grid(const char* row, int V) {
 }
 
 // Stages grid vectors [v0, v1) of a row (V elements) at `dst`, one warp.  Lane 0 raises the
-// transaction count of `bar` and issues the bulk copy; the lanes fill the straddling vectors
-// with plain loads.  The caller arrives on `bar` after a __syncwarp().
+// transaction count of `bar` and issues the bulk copy (with L2 eviction priority `hint`); the
+// lanes fill the straddling vectors with plain loads.  The caller arrives on `bar` after a
+// __syncwarp().
 template <typename T>
 __device__ __forceinline__ void warp_stage(unsigned char* dst, const RowGrid<T>& g, int V, int v0, int v1,
-                                           uint64_t* bar, int lane) {
+                                           uint64_t* bar, int lane, int hint = kL2Normal) {
   constexpr int S = Elem<T>::kSize, VE = Elem<T>::kPerVec;
   if (v1 <= v0) return;
   const int fa = g.phase > 0 ? 1 : 0;
@@ -337,7 +359,10 @@ __device__ __forceinline__ void warp_stage(unsigned char* dst, const RowGrid<T>&
   if (a < e && lane == 0) {
     const uint32_t bytes = (uint32_t)(e - a) * 16u;
     mbar_expect_tx(bar, bytes);
-    tma_load_1d(dst + (size_t)(a - v0) * 16, g.grid + (size_t)a * 16, bytes, bar);
+    if (hint == kL2Normal)
+      tma_load_1d(dst + (size_t)(a - v0) * 16, g.grid + (size_t)a * 16, bytes, bar);
+    else
+      tma_load_1d_hint(dst + (size_t)(a - v0) * 16, g.grid + (size_t)a * 16, bytes, bar, l2_policy(hint));
   }
   // straddling vectors: grid vector 0 when the row starts mid-vector, grid vector fb when it
   // ends mid-vector

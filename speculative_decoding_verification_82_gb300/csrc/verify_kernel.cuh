@@ -459,7 +459,15 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
         m.nvec = max(0, v1 - v0);
         constexpr int VE = Elem<T>::kPerVec;
         m.e_base = v0 * VE - g.phase;
-        warp_stage<T>(buf, g, P.V, v0, v1, &sm.full[s], lane);
+        // With a residual pass, the pair at the rejected position is read again soon after; the
+        // first rejection falls at the early positions far more often (acceptances compound),
+        // so their rows are kept in L2 ahead of the rest
+        int hint = kL2Normal;
+        if (P.npos > 0) {
+          const int k = m.row < P.R ? m.row : m.row - P.R;
+          hint = (k < kL2KeepPositions && k < P.K) ? kL2Last : kL2First;
+        }
+        warp_stage<T>(buf, g, P.V, v0, v1, &sm.full[s], lane, hint);
       } else if (kind == kItemResid) {
         m.b = (int)fdiv(w, P.fd_R);
         const int off = (int)(w - (unsigned)m.b * P.fd_R.d);
@@ -506,9 +514,9 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
         m.e_lo = q.e_lo;
         m.e_hi = q.e_hi;
         m.dshift = q.dshift;
-        if (m.nvec > 0) {
-          warp_stage<T>(buf, q.gt, P.V, q.vt0, q.vt1, &sm.full[s], lane);
-          warp_stage<T>(buf + (size_t)kDraftSlot * 16, q.gd, P.V, q.vd0, q.vd1, &sm.full[s], lane);
+        if (m.nvec > 0) {  // (read for the last time)
+          warp_stage<T>(buf, q.gt, P.V, q.vt0, q.vt1, &sm.full[s], lane, kL2First);
+          warp_stage<T>(buf + (size_t)kDraftSlot * 16, q.gd, P.V, q.vd0, q.vd1, &sm.full[s], lane, kL2First);
         }
       }
       break;
