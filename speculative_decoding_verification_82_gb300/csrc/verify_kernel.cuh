@@ -226,7 +226,7 @@ struct Shared {
   SlotMeta pmeta[kSlots];
   int pcnt[kSlots];  // warps of the group that have left their partial
   int abort, last;
-  double alpha[SPEC_MAX_K];
+  float alpha[SPEC_MAX_K];
   ChunkStat fin_cs[kFinCs];
   ChunkStat fin_ss[kFinSs];
   RowStat fin_rs[kFinRows];
@@ -514,9 +514,9 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
         m.e_lo = q.e_lo;
         m.e_hi = q.e_hi;
         m.dshift = q.dshift;
-        if (m.nvec > 0) {  // (read for the last time)
-          warp_stage<T>(buf, q.gt, P.V, q.vt0, q.vt1, &sm.full[s], lane, kL2First);
-          warp_stage<T>(buf + (size_t)kDraftSlot * 16, q.gd, P.V, q.vd0, q.vd1, &sm.full[s], lane, kL2First);
+        if (m.nvec > 0) {  // (the draw reads one sub-range of these again, soon)
+          warp_stage<T>(buf, q.gt, P.V, q.vt0, q.vt1, &sm.full[s], lane);
+          warp_stage<T>(buf + (size_t)kDraftSlot * 16, q.gd, P.V, q.vd0, q.vd1, &sm.full[s], lane);
         }
       }
       break;
@@ -1212,22 +1212,46 @@ __device__ void combine_rows(const Params& P, Shared& sm, int b, const CsReader&
   fin_sync();
 }
 
-// l c - mc with the product l c carried exactly (an fp32 pair from one FMA) and the difference
-// taken in double: the exponent of 2^(l c - mc) must not lose the digits that a large |l c|
-// would round away in fp32.
-__device__ __forceinline__ double scaled_logit(float l, float c, float mc) {
+// An exponent as an unevaluated fp32 pair hi + lo, |lo| far below one unit of hi's last place
+// plus a few such units: fp32 arithmetic that keeps the digits a double would (GB300's FP64
+// operations take tens of cycles each).
+struct Exp2 {
+  float hi, lo;
+};
+// a + b = s + err exactly (Knuth's two-sum).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& err) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+// l c - mc with the product l c carried exactly (an fp32 pair from one FMA) and the difference as
+// a two-sum: the exponent of 2^(l c - mc) must not lose the digits that a large |l c| would round
+// away in plain fp32.
+__device__ __forceinline__ Exp2 scaled_logit(float l, float c, float mc) {
   const float p = __fmul_rn(l, c);
   const float e = __fmaf_rn(l, c, -p);  // l c = p + e exactly
-  return ((double)p - (double)mc) + (double)e;
+  Exp2 x;
+  float r;
+  two_sum(p, -mc, x.hi, r);
+  x.lo = __fadd_rn(r, e);
+  return x;
 }
-// 2^x * f for double x and fp32 f > 0, in fp32: the fractional part of x through the
-// special-function unit, the integer part as an exact power of two.  Saturates to +inf / 0.
-__device__ __forceinline__ float exp2_times(double x, float f) {
-  if (!(x > -300.0)) return 0.f;
-  if (x > 300.0) return INFINITY;
-  const int n = __double2int_rd(x);
-  const float r = __fmul_rn(ex2((float)(x - (double)n)), f);  // in [0, 2) * f
-  return ldexpf(r, n);
+__device__ __forceinline__ Exp2 exp2_sub(const Exp2& a, const Exp2& b) {
+  Exp2 x;
+  float r;
+  two_sum(a.hi, -b.hi, x.hi, r);
+  x.lo = __fadd_rn(r, __fsub_rn(a.lo, b.lo));
+  return x;
+}
+// 2^x * f for x = hi + lo and fp32 f > 0, in fp32: the integer part of hi as an exact power of
+// two, the rest (hi minus its floor, exact, plus lo) through the special-function unit.
+// Saturates to +inf / 0.
+__device__ __forceinline__ float exp2_times(const Exp2& x, float f) {
+  if (!(x.hi > -300.f)) return 0.f;
+  if (x.hi > 300.f) return INFINITY;
+  const float n = floorf(x.hi);
+  const float r = __fmul_rn(ex2(__fadd_rn(__fsub_rn(x.hi, n), x.lo)), f);  // in (0, 2) * f
+  return ldexpf(r, (int)n);
 }
 
 // Inputs of request b that do not depend on its statistics, loaded by the leader while the group
@@ -1278,7 +1302,7 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
     int e = 0;
     for (int k = lane; k < K; k += 32) {
       const int x = k < 32 ? x0 : __ldg(P.draft_tokens + (size_t)b * K + k);
-      double alpha = 0.0;
+      float alpha = 0.f;
       if (x < 0 || x >= P.V) {
         e |= SPEC_ERRF_BAD_TOKEN;
       } else {
@@ -1287,25 +1311,26 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
           // alpha = p(x) / q(x) = 2^((l_x c - mc_t) - (d_x c - mc_d)) Z_d / Z_t (draft model), or
           // p(x) = 2^(l_x c - mc_t) / Z_t (one-hot draft); capped at 1
           const float lx = k < 32 ? lx0 : Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, k) + (size_t)x * S));
-          const double ext = scaled_logit(lx, P.c, t.mc);
+          const Exp2 ext = scaled_logit(lx, P.c, t.mc);
           if (MODE == kChain) {
             const RowStat d = read_rowstat(P, sm, b, P.R + k);
             const float dx =
                 k < 32 ? dx0 : Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, P.R + k) + (size_t)x * S));
             if (dx == -INFINITY) {
-              alpha = 1.0;  // q(x) = 0
+              alpha = 1.f;  // q(x) = 0
             } else if (lx == -INFINITY) {
-              alpha = 0.0;  // p(x) = 0
+              alpha = 0.f;  // p(x) = 0
             } else {
-              const float ratio = exp2_times(ext - scaled_logit(dx, P.c, d.mc), __fdiv_rn((float)d.Z, (float)t.Z));
-              alpha = ratio >= 1.f ? 1.0 : (double)ratio;
+              const float ratio =
+                  exp2_times(exp2_sub(ext, scaled_logit(dx, P.c, d.mc)), __fdiv_rn((float)d.Z, (float)t.Z));
+              alpha = fminf(ratio, 1.f);
             }
           } else {
             const float px = lx == -INFINITY ? 0.f : exp2_times(ext, __frcp_rn((float)t.Z));
-            alpha = px >= 1.f ? 1.0 : (double)px;
+            alpha = fminf(px, 1.f);
           }
         } else {
-          alpha = (x == t.amax) ? 1.0 : 0.0;
+          alpha = (x == t.amax) ? 1.f : 0.f;
         }
       }
       sm.alpha[k] = alpha;
@@ -1320,9 +1345,9 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
         const int k = k0 + lane;
         bool rej = false;
         if (k < K) {
-          const double a = sm.alpha[k];
+          const float a = sm.alpha[k];
           const float rk = k < 32 ? r0 : __ldg(P.r + (size_t)b * K + k);
-          rej = kSoftmax ? !((double)rk <= a) : (a != 1.0);
+          rej = kSoftmax ? !(rk <= a) : (a != 1.f);
         }
         const unsigned msk = __ballot_sync(kFull, rej);
         if (msk) {
@@ -1333,6 +1358,22 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
     }
     int xn = __shfl_sync(kFull, x0, n < 32 ? n : 0);
     if (n >= 32 && n < K) xn = __ldg(P.draft_tokens + (size_t)b * K + n);
+    // publication of the acceptance result first (read by residual work items, which can start
+    // now, and by the probability rows)
+    if (MODE == kChain && P.npos > 0 && P.diag) {  // per-position residuals read the row statistics
+      __syncwarp();
+      __threadfence();
+    }
+    const bool resid = MODE == kChain && P.npos > 0 && !P.diag && !err && n < K;
+    if (lane == 0 || (resid && lane < 4)) {
+      unsigned hi = (unsigned)n | ((unsigned)err << 16);
+      if (lane > 0) {
+        const RowStat t = read_rowstat(P, sm, b, n), d = read_rowstat(P, sm, b, P.R + n);
+        hi = __float_as_uint(lane == 1 ? t.mc : lane == 2 ? d.mc : __fdiv_rn((float)t.Z, (float)d.Z));
+      }
+      st_volatile_u64(P.req[b].w + lane, ((unsigned long long)hi << 32) | sm.tag);
+    }
+    __syncwarp();
     if (lane == 0) {
       sm.gs.out[0] = n;
       sm.gs.out[1] = err;
@@ -1354,7 +1395,7 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
       if (!err && i < n) o = i < 32 ? x0 : __ldg(P.draft_tokens + (size_t)b * K + i);
       if (!err && i == n && !kSoftmax) o = read_rowstat(P, sm, b, n).amax;
       P.out_tokens[o_i] = o;
-      if (P.accept_prob && i < K) P.accept_prob[(size_t)b * K + i] = err ? 0.f : (float)sm.alpha[i];
+      if (P.accept_prob && i < K) P.accept_prob[(size_t)b * K + i] = err ? 0.f : sm.alpha[i];
       if (P.cand_tokens && (err || !kSoftmax)) P.cand_tokens[o_i] = err ? -1 : read_rowstat(P, sm, b, i).amax;
       if (P.pos_mass && (err || !kSoftmax)) P.pos_mass[o_i] = err ? 0.f : 1.f;
     }
@@ -1363,21 +1404,6 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
       if (P.err_flags) P.err_flags[b] = err;
       if (P.residual_mass && (err || !kSoftmax)) P.residual_mass[b] = err ? 0.f : 1.f;
     }
-    // publication of the acceptance result (read by residual work items and the probability rows)
-    if (MODE == kChain && P.npos > 0 && P.diag) {  // per-position residuals read the row statistics
-      __syncwarp();
-      __threadfence();
-    }
-    const bool resid = MODE == kChain && P.npos > 0 && !P.diag && !err && n < K;
-    if (lane == 0 || (resid && lane < 4)) {
-      unsigned hi = (unsigned)n | ((unsigned)err << 16);
-      if (lane > 0) {
-        const RowStat t = read_rowstat(P, sm, b, n), d = read_rowstat(P, sm, b, P.R + n);
-        hi = __float_as_uint(lane == 1 ? t.mc : lane == 2 ? d.mc : __fdiv_rn((float)t.Z, (float)d.Z));
-      }
-      st_volatile_u64(P.req[b].w + lane, ((unsigned long long)hi << 32) | sm.tag);
-    }
-    __syncwarp();
   }
   if constexpr (kSoftmax) {
     if (err) return -1;

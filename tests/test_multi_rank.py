@@ -73,3 +73,8 @@ def test_single_rank_needs_no_process_group():
     assert bench.max_over_ranks(3.5, 1) == 3.5
     assert bench.rank_seeds(0, 2) == [0, 1] and bench.rank_seeds(1, 2) == [1000, 1001]
     assert bench.job_rows_per_s(1, 704, 2000, 1000.0) == 704 * 2000
+    # calls per captured graph: a divisor of the step count, so whole replays time exactly K calls
+    for K in (1, 2, 3, 7, 97, 100, 2000, 2001):
+        g = bench.graph_calls(K)
+        assert 1 <= g <= 50 and K % g == 0
+    assert bench.graph_calls(2000) == 50 and bench.graph_calls(97) == 1
