@@ -77,6 +77,11 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_tree_bruteforce.restype = I
     lib.oracle_verify_tree_greedy.argtypes = [I, P, I, I, I, P, P, I, I, P, P, P, P, P]
     lib.oracle_verify_tree_greedy.restype = None
+    lib.oracle_tree_sample_probs.argtypes = [I, I, P, P, P, P, P, F, D, P, P, P, P, P, P]
+    lib.oracle_tree_sample_probs.restype = None
+    lib.oracle_verify_tree_sample.argtypes = [I, P, P, I, I, I, F, P, P, P, P, D, I, I,
+                                              P, P, P, P, P, P, P]
+    lib.oracle_verify_tree_sample.restype = None
     lib.oracle_load.argtypes = [P, I, c_size_t]
     lib.oracle_load.restype = D
     return lib
@@ -273,6 +278,52 @@ def verify_tree_greedy(dtype: str, target, B: int, N: int, V: int, node_tokens, 
         run(*requests)
     else:
         _run_threaded(run, B, threads)
+    return o
+
+
+def tree_sample_probs(p, q, parents, tokens, r, u, tol: float = DEFAULT_TOL, lib=None) -> dict:
+    """One request of the stochastic tree walk from probability rows p, q [N+1][V]."""
+    lib = lib or load()
+    p, q = _c(p, np.float64), _c(q, np.float64)
+    N1, V = p.shape
+    pa, tk, rr = _c(parents, np.int32), _c(tokens, np.int32), _c(r, np.float32)
+    L, fl = np.zeros(1, np.int32), np.zeros(1, np.int32)
+    path, out = np.zeros(N1, np.int32), np.zeros(N1, np.int32)
+    alpha, mass = np.zeros(N1, np.float64), np.zeros(1, np.float64)
+    lib.oracle_tree_sample_probs(N1, V, _p(p), _p(q), _p(pa), _p(tk), _p(rr), float(u), tol,
+                                 _p(L), _p(path), _p(out), _p(alpha), _p(mass), _p(fl))
+    return dict(accept_len=int(L[0]), path=path, out_tokens=out, alpha=alpha,
+                mass=float(mass[0]), req_flag=int(fl[0]))
+
+
+def verify_tree_sample(dtype: str, target, draft, B: int, N: int, V: int, T: float, node_tokens,
+                       parents, r, u, tol: float = DEFAULT_TOL, threads: int = 1, requests=None,
+                       lib=None) -> dict:
+    """Tree verification by walking: stochastic (T > 0) or greedy (T == 0) on visited rows."""
+    lib = lib or load()
+    target = np.ascontiguousarray(target)
+    draft_p = _p(np.ascontiguousarray(draft)) if draft is not None else None
+    tk, pa = _c(node_tokens, np.int32), _c(parents, np.int32)
+    N1 = N + 1
+    rr = _c(r, np.float32) if r is not None else np.zeros((B, N1), np.float32)
+    uu = _c(u, np.float32) if u is not None else np.zeros(B, np.float32)
+    o = dict(accept_len=np.zeros(B, np.int32), path=np.zeros((B, N1), np.int32),
+             out_tokens=np.zeros((B, N1), np.int32), alpha=np.zeros((B, N1), np.float64),
+             mass=np.zeros(B, np.float64), req_flag=np.zeros(B, np.int32),
+             err=np.zeros(B, np.int32))
+    keep = (target, draft)
+
+    def run(b0, b1):
+        lib.oracle_verify_tree_sample(DTYPE_CODE[dtype], _p(target), draft_p, B, N, V, float(T),
+                                      _p(tk), _p(pa), _p(rr), _p(uu), tol, b0, b1,
+                                      *(_p(o[k]) for k in ("accept_len", "path", "out_tokens",
+                                                           "alpha", "mass", "req_flag", "err")))
+
+    if requests is not None:
+        run(*requests)
+    else:
+        _run_threaded(run, B, threads)
+    del keep
     return o
 
 

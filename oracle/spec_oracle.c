@@ -543,3 +543,261 @@ void oracle_verify_tree_greedy(int dtype, const void *target, int B, int N, int 
     }
     free(row);
 }
+
+/* ------------------------------------------------------------ stochastic tree verification ---- */
+/*
+ * R12 (tree, T > 0): the step of section I.1 applied to every sibling in turn.  At a node, p is
+ * the target distribution of the node's row and q the draft distribution of the node's draft row
+ * (the distribution its children were drawn from; siblings are read as independent draws from
+ * the same q).  Children are tested in ascending node index.  Child c with token x is accepted
+ * when r[c] <= alpha = min(1, p(x) / q(x)) (R2 when q(x) == 0 or p(x) >= q(x)), and the walk
+ * moves to c.  A rejected child replaces the target by its residual,
+ *     p <- max(0, p - q) / sum_i max(0, p_i - q_i),
+ * and the next sibling is tested against the new p and the same q.  When no child is accepted,
+ * or the node has none, the final token is drawn from the current p with the request's u (R4).
+ * A chain (one child per node) is exactly the chain verification above.
+ * R13: the mass R reported for a request is the product of the residual sums met at its final
+ * node (1 when nothing was rejected there).  The tie band of an accept test, and of the final
+ * draw, at mass R is tol / R (the resolution of the residual in fp32, as in R10).  A residual sum
+ * that is not positive stops the sibling tests; the draw is then taken from the node's own p
+ * (R5, flagged).
+ * R14: the walk reads only the rows of the nodes it visits (a node's draft row only when it has
+ * children); a non-finite value in another row is not seen.  T == 0 is the greedy walk of R9,
+ * with alpha = 1 for the matching child and 0 for the siblings tested before it.
+ */
+
+/* Supplies the probability rows of one node: p always, q when need_q.  Returns error bits. */
+typedef int (*tree_rows_fn)(void *ctx, int node, int need_q, double *p, double *q);
+
+static void tree_fail(int N1, int *accept_len, int *path, int *out_tokens, double *alpha,
+                      double *mass)
+{
+    *accept_len = 0;
+    *mass = 0.0;
+    for (int i = 0; i < N1; i++) {
+        path[i] = -1;
+        out_tokens[i] = -1;
+        alpha[i] = -1.0;
+    }
+}
+
+/* One request.  parents / tokens: [N1]; r: [N1] (r[c] is used when child c is tested; r[0] is
+ * unused); outputs as oracle_verify_tree_sample.  Returns error bits (outputs failed when set). */
+static int tree_sample_walk(int N1, int V, tree_rows_fn rows, void *ctx, const int *parents,
+                            const int *tokens, const float *r, float u, double tol,
+                            int *accept_len, int *path, int *out_tokens, double *alpha,
+                            double *mass, int *req_flag)
+{
+    size_t n = (size_t)(V > 0 ? V : 1);
+    double *p0 = (double *)malloc(sizeof(double) * n), *p = (double *)malloc(sizeof(double) * n);
+    double *q = (double *)malloc(sizeof(double) * n), *w = (double *)malloc(sizeof(double) * n);
+    int e = 0, cur = 0, len = 0;
+    *req_flag = 0;
+    for (int i = 0; i < N1; i++) {
+        path[i] = -1;
+        out_tokens[i] = -1;
+        alpha[i] = -1.0;
+    }
+    path[0] = 0;
+    for (int depth = 0; depth < N1; depth++) {
+        int has_kids = 0;
+        for (int c = cur + 1; c < N1; c++)
+            if (parents[c] == cur)
+                has_kids = 1;
+        e = rows(ctx, cur, has_kids, p0, q);
+        if (e)
+            break;
+        for (int i = 0; i < V; i++)
+            p[i] = p0[i];
+        double R = 1.0;
+        int next = -1, empty = 0;
+        for (int c = cur + 1; c < N1 && next < 0 && !empty; c++) {
+            if (parents[c] != cur)
+                continue;
+            int x = tokens[c];
+            double a = (q[x] == 0.0 || p[x] >= q[x]) ? 1.0 : p[x] / q[x]; /* step 1, R2 */
+            alpha[c] = a;
+            if (fabs((double)r[c] - a) <= tol / R)
+                *req_flag |= ORF_ACCEPT_TIE;
+            if ((double)r[c] <= a) { /* step 2: accepted */
+                next = c;
+                break;
+            }
+            double S = 0.0; /* step 3: the residual becomes the target of the next sibling */
+            for (int i = 0; i < V; i++) {
+                double d = p[i] - q[i];
+                w[i] = d > 0.0 ? d : 0.0;
+                S += w[i];
+            }
+            R *= S;
+            if (!(S > 0.0)) {
+                empty = 1;
+                break;
+            }
+            for (int i = 0; i < V; i++)
+                p[i] = w[i] / S;
+        }
+        if (next >= 0) {
+            out_tokens[len] = tokens[next];
+            len++;
+            path[len] = next;
+            cur = next;
+            continue;
+        }
+        double S2;
+        int fl, tok;
+        if (empty) { /* R13 / R5: nothing left of the residual, draw from the node's own p */
+            tok = oracle_inverse_cdf(p0, V, (double)u, tol, &S2, &fl);
+            *req_flag |= ORF_ZERO_RESIDUAL;
+        } else {
+            tok = oracle_inverse_cdf(p, V, (double)u, tol / R, &S2, &fl);
+        }
+        if (fl)
+            *req_flag |= ORF_CDF_TIE;
+        out_tokens[len] = tok;
+        *mass = R;
+        break;
+    }
+    *accept_len = len;
+    free(p0);
+    free(p);
+    free(q);
+    free(w);
+    return e;
+}
+
+struct probs_ctx {
+    int V;
+    const double *p, *q;
+};
+
+static int probs_rows(void *ctx, int node, int need_q, double *p, double *q)
+{
+    struct probs_ctx *c = (struct probs_ctx *)ctx;
+    for (int i = 0; i < c->V; i++) {
+        p[i] = c->p[(size_t)node * c->V + i];
+        if (need_q)
+            q[i] = c->q[(size_t)node * c->V + i];
+    }
+    return 0;
+}
+
+/* Stochastic tree verification on probability rows p, q: [N1][V] (row n of q = the draft
+ * distribution of node n's children).  Outputs: *accept_len, path[N1], out_tokens[N1],
+ * alpha[N1] (alpha of each tested child, -1 elsewhere), *mass (R13), *req_flag. */
+void oracle_tree_sample_probs(int N1, int V, const double *p, const double *q,
+                              const int *parents, const int *tokens, const float *r, float u,
+                              double tol, int *accept_len, int *path, int *out_tokens,
+                              double *alpha, double *mass, int *req_flag)
+{
+    struct probs_ctx c = {V, p, q};
+    *mass = 0.0;
+    tree_sample_walk(N1, V, probs_rows, &c, parents, tokens, r, u, tol, accept_len, path,
+                     out_tokens, alpha, mass, req_flag);
+}
+
+struct logits_ctx {
+    int dtype, V;
+    double T;
+    const void *target, *draft;
+    size_t row0;
+    double *l;
+};
+
+static int logits_rows(void *ctx, int node, int need_q, double *p, double *q)
+{
+    struct logits_ctx *c = (struct logits_ctx *)ctx;
+    load_row(c->target, c->dtype, c->row0 + (size_t)node, c->V, c->l);
+    int e = oracle_softmax(c->l, c->V, c->T, p);
+    if (need_q) {
+        load_row(c->draft, c->dtype, c->row0 + (size_t)node, c->V, c->l);
+        e |= oracle_softmax(c->l, c->V, c->T, q);
+    }
+    return e;
+}
+
+/* R14, T == 0: the greedy walk on the rows of the visited nodes only. */
+static int tree_greedy_visited(int dtype, const void *target, size_t row0, int N1, int V,
+                               const int *parents, const int *tokens, int *accept_len, int *path,
+                               int *out_tokens, double *alpha)
+{
+    double *l = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    int cur = 0, len = 0, e = 0;
+    for (int i = 0; i < N1; i++) {
+        path[i] = -1;
+        out_tokens[i] = -1;
+        alpha[i] = -1.0;
+    }
+    path[0] = 0;
+    for (int depth = 0; depth < N1; depth++) {
+        load_row(target, dtype, row0 + (size_t)cur, V, l);
+        if (row_has_nan(l, V)) {
+            e = ORE_NONFINITE;
+            break;
+        }
+        int a = oracle_argmax(l, V), next = -1;
+        for (int c = cur + 1; c < N1; c++) {
+            if (parents[c] != cur)
+                continue;
+            alpha[c] = tokens[c] == a ? 1.0 : 0.0;
+            if (tokens[c] == a) {
+                next = c;
+                break;
+            }
+        }
+        if (next < 0) {
+            out_tokens[len] = a;
+            break;
+        }
+        out_tokens[len] = tokens[next];
+        len++;
+        path[len] = next;
+        cur = next;
+    }
+    *accept_len = len;
+    free(l);
+    return e;
+}
+
+/*
+ * Tree verification by walking (R12-R14).  target, draft: [B][N+1][V] (draft ignored when
+ * T == 0); node_tokens, parents: [B][N+1]; r: [B][N+1]; u: [B].
+ * Outputs: accept_len[B], path[B][N+1], out_tokens[B][N+1], alpha[B][N+1], mass[B],
+ * req_flag[B], err[B].  Requests [b0, b1) only are processed.
+ */
+void oracle_verify_tree_sample(int dtype, const void *target, const void *draft, int B, int N,
+                               int V, float T, const int *node_tokens, const int *parents,
+                               const float *r, const float *u, double tol, int b0, int b1,
+                               int *accept_len, int *path, int *out_tokens, double *alpha,
+                               double *mass, int *req_flag, int *err)
+{
+    int N1 = N + 1;
+    double *l = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    (void)B;
+    for (int b = b0; b < b1; b++) {
+        const int *pb = parents + (size_t)b * N1, *tb = node_tokens + (size_t)b * N1;
+        int *o_path = path + (size_t)b * N1, *o_tok = out_tokens + (size_t)b * N1;
+        double *o_al = alpha + (size_t)b * N1;
+        int e = oracle_tree_check(N1, V, pb, tb);
+        req_flag[b] = 0;
+        mass[b] = 0.0;
+        if (!e) {
+            if (T == 0.0f) {
+                e = tree_greedy_visited(dtype, target, (size_t)b * N1, N1, V, pb, tb,
+                                        accept_len + b, o_path, o_tok, o_al);
+                mass[b] = 1.0;
+            } else {
+                struct logits_ctx c = {dtype, V, (double)T, target, draft, (size_t)b * N1, l};
+                e = tree_sample_walk(N1, V, logits_rows, &c, pb, tb, r + (size_t)b * N1, u[b],
+                                     tol, accept_len + b, o_path, o_tok, o_al, mass + b,
+                                     req_flag + b);
+            }
+        }
+        if (e) {
+            tree_fail(N1, accept_len + b, o_path, o_tok, o_al, mass + b);
+            req_flag[b] = 0;
+        }
+        err[b] = e;
+    }
+    free(l);
+}

@@ -131,11 +131,16 @@ class ChainInputs:
 
 @dataclass
 class TreeInputs:
-    """Inputs of one greedy tree verification call.
+    """Inputs of one tree verification call.
 
     target:      [B][N+1][V] storage array; row n scores the children of node n.
     node_tokens: int32 [B][N+1]; node 0 is the root (its token is ignored).
     parents:     int32 [B][N+1]; parents[0] = -1, 0 <= parents[i] < i.
+    Stochastic walks (temperature > 0) also carry
+    draft:       [B][N+1][V] storage array; row n is the draft distribution the children of
+                 node n were drawn from (rows of leaves are never read);
+    r:           float32 [B][N+1], (0, 1]; r[b][c] is the uniform of child c's acceptance test;
+    u:           float32 [B], [0, 1).
     """
 
     name: str
@@ -147,10 +152,23 @@ class TreeInputs:
     node_tokens: np.ndarray
     parents: np.ndarray
     meta: dict = field(default_factory=dict)
+    draft: np.ndarray | None = None
+    r: np.ndarray | None = None
+    u: np.ndarray | None = None
+    temperature: np.float32 = np.float32(0.0)
 
     @property
     def logits_bytes(self) -> int:
         return self.target.nbytes
+
+    @property
+    def internal_nodes(self) -> np.ndarray:
+        """bool [B][N+1]: nodes with at least one child (the rows whose draft side is read)."""
+        out = np.zeros(self.parents.shape, dtype=bool)
+        for b in range(self.B):
+            par = self.parents[b, 1:]
+            out[b, par[par >= 0]] = True
+        return out
 
 
 # ----------------------------------------------------------------------------------------------
@@ -304,3 +322,92 @@ def ngram(seed: int = 0, B: int = 256, K: int = 5, V: int = 151936, temperature:
     return ChainInputs("ngram", dtype, B, K, V, T, encode(t32, dtype), None, x,
                        uniform_r(seed, (B, K)), uniform_u(seed, (B,)),
                        meta={"prompt": prompt, "starts": starts})
+
+
+# ----------------------------------------------------------------------------------------------
+# Stochastic tree verify (T > 0 over an EAGLE-2-like tree): the tree of workload 4 with the
+# value recipe of workload 3 (target ~ N(0, 3^2) with Zipf-shaped spikes, draft = target +
+# N(0, 2^2)); the children of node n are independent draws from the draft distribution of row n.
+# ----------------------------------------------------------------------------------------------
+def _draw_children(par: np.ndarray, drow, T: float, rng: np.random.Generator) -> np.ndarray:
+    """Tokens of one request's nodes: the children of node n drawn independently from the draft
+    distribution of row n (Gumbel-max over drow(n), a float32 [V] row)."""
+    tokens = np.zeros(par.size, dtype=np.int32)
+    for p in range(par.size):
+        kids = np.nonzero(par == p)[0]
+        if kids.size:
+            d = drow(p).astype(np.float64) / T
+            g = rng.random((kids.size, d.size))
+            g = -np.log(-np.log(np.maximum(g, 1e-300)))
+            tokens[kids] = np.argmax(d[None, :] + g, axis=1)
+    return tokens
+
+
+def tree_sample(seed: int = 0, B: int = 16, V: int = 128256, temperature: float = 1.0,
+                dtype: str = "bf16", parents: np.ndarray | None = None,
+                draft_sigma: float = 2.0) -> TreeInputs:
+    T = np.float32(temperature)
+    par = eagle_tree_parents() if parents is None else np.asarray(parents, dtype=np.int32)
+    N1 = par.size
+    t32 = _rng(seed, _S_TARGET).standard_normal((B, N1, V), dtype=np.float32) * np.float32(3.0)
+    boosts = zipf_boosts()
+    srng = _rng(seed, _S_SPIKE)
+    for b in range(B):
+        for n in range(N1):
+            t32[b, n, srng.choice(V, size=boosts.size, replace=False)] += boosts
+    d32 = t32 + _rng(seed, _S_DRAFT).standard_normal((B, N1, V), dtype=np.float32) * np.float32(draft_sigma)
+    target, draft = encode(t32, dtype), encode(d32, dtype)
+    del t32, d32
+    grng = _rng(seed, _S_GUMBEL)
+    tokens = np.stack([_draw_children(par, lambda n, b=b: decode(draft[b, n], dtype), float(T), grng)
+                       for b in range(B)])
+    return TreeInputs("tree_sample", dtype, B, N1 - 1, V, target, tokens,
+                      np.broadcast_to(par, (B, N1)).copy(), draft=draft,
+                      r=uniform_r(seed, (B, N1)), u=uniform_u(seed, (B,)), temperature=T)
+
+
+def tree_sample_tiny(seed: int = 0, trials: int = 100_000, V: int = 8, branching=(3, 2),
+                     temperature: float = 1.0, target_sigma: float = 2.0,
+                     draft_sigma: float = 1.0) -> TreeInputs:
+    """Distribution check of the stochastic walk: a two-level tree whose rows depend only on the
+    token prefix (root; token a at depth 1; tokens (a, b) at depth 2), so that the emitted token
+    after a prefix must follow that prefix's target row.  Fresh children tokens (independent
+    draws from the parent's draft row), r and u per trial; one fixed set of rows."""
+    T = float(temperature)
+    m1, m2 = branching
+    rt = _rng(seed, _S_TARGET)
+    rd = _rng(seed, _S_DRAFT)
+    t0 = rt.standard_normal(V, dtype=np.float32) * np.float32(target_sigma)
+    t1 = rt.standard_normal((V, V), dtype=np.float32) * np.float32(target_sigma)
+    t2 = rt.standard_normal((V, V, V), dtype=np.float32) * np.float32(target_sigma)
+    d0 = t0 + rd.standard_normal(V, dtype=np.float32) * np.float32(draft_sigma)
+    d1 = t1 + rd.standard_normal((V, V), dtype=np.float32) * np.float32(draft_sigma)
+    d2 = t2 + rd.standard_normal((V, V, V), dtype=np.float32) * np.float32(draft_sigma)
+    par = [-1] + [0] * m1
+    for i in range(m1):
+        par += [1 + i] * m2
+    par = np.asarray(par, dtype=np.int32)
+    N1 = par.size
+    g = _rng(seed, _S_GUMBEL)
+
+    def gumbel(shape):
+        x = g.random(shape)
+        return -np.log(-np.log(np.maximum(x, 1e-300)))
+
+    a = np.argmax(d0.astype(np.float64)[None, None, :] / T + gumbel((trials, m1, V)), axis=-1)
+    bt = np.argmax(d1[a].astype(np.float64)[:, :, None, :] / T + gumbel((trials, m1, m2, V)), axis=-1)
+    tokens = np.zeros((trials, N1), dtype=np.int32)
+    tokens[:, 1: 1 + m1] = a
+    tokens[:, 1 + m1:] = bt.reshape(trials, m1 * m2)
+    target = np.empty((trials, N1, V), dtype=np.float32)
+    draft = np.empty((trials, N1, V), dtype=np.float32)
+    target[:, 0], draft[:, 0] = t0, d0
+    target[:, 1: 1 + m1], draft[:, 1: 1 + m1] = t1[a], d1[a]
+    aa = np.repeat(a, m2, axis=1)
+    bb = bt.reshape(trials, m1 * m2)
+    target[:, 1 + m1:], draft[:, 1 + m1:] = t2[aa, bb], d2[aa, bb]
+    return TreeInputs("tree_sample_tiny", "f32", trials, N1 - 1, V, target, tokens,
+                      np.broadcast_to(par, (trials, N1)).copy(),
+                      meta={"t0": t0, "t1": t1, "t2": t2, "d0": d0, "d1": d1},
+                      draft=draft, r=uniform_r(seed, (trials, N1)), u=uniform_u(seed, (trials,)),
+                      temperature=np.float32(T))

@@ -420,3 +420,149 @@ def pin_residual_band_scales_with_mass(lib):
 
 
 FAST_PINS.append(pin_residual_band_scales_with_mass)
+
+
+# -------------------------------------------------------------- stochastic tree walk ----
+def pin_hand_tree_sample_cases(lib):
+    """Hand-worked walks (tests/golden/hand_cases.json, "tree_sample")."""
+    for case in _golden()["tree_sample"]:
+        p, q = np.asarray(case["p"], np.float64), np.asarray(case["q"], np.float64)
+        for run in case["runs"]:
+            o = oracle.tree_sample_probs(p, q, case["parents"], case["tokens"], run["r"], run["u"],
+                                         TOL, lib=lib)
+            tag = f"{case['name']} r={run['r']} u={run['u']}"
+            assert o["accept_len"] == run["accept_len"], (tag, o)
+            assert list(o["path"]) == run["path"], (tag, o)
+            assert list(o["out_tokens"]) == run["out_tokens"], (tag, o)
+            assert np.allclose(o["alpha"], run["alpha"], rtol=0, atol=1e-15), (tag, o["alpha"])
+            assert abs(o["mass"] - run["mass"]) <= 1e-15, (tag, o["mass"])
+            assert bool(o["req_flag"] & oracle.FLAG_ACCEPT_TIE) == run["accept_tie"], (tag, o)
+            assert bool(o["req_flag"] & oracle.FLAG_CDF_TIE) == run["cdf_tie"], (tag, o)
+
+
+def pin_tree_sample_chain_reduction(lib, n_cases=60):
+    """A tree with one child per node is a chain: the walk must give the chain verification of
+    section I.1 (pinned on its own) on the same rows, uniforms and tokens."""
+    rng = np.random.default_rng(31)
+    for i in range(n_cases):
+        K, V = int(rng.integers(0, 6)), int(rng.integers(2, 12))
+        T = float(rng.choice([0.5, 1.0, 1.7]))
+        lt = (rng.normal(0, 2, (1, K + 1, V))).astype(np.float32)
+        ld = (lt[:, :K] + rng.normal(0, 1, (1, K, V))).astype(np.float32)
+        x = rng.integers(0, V, (1, K)).astype(np.int32)
+        r = ((rng.integers(0, 1 << 24, (1, K)) + 1) / float(1 << 24)).astype(np.float32)
+        if i % 3 == 0 and K:
+            r[0, : K // 2 + 1] = np.float32(2.0 ** -24)  # long accepted prefixes too
+        u = (rng.integers(0, 1 << 24, 1) / float(1 << 24)).astype(np.float32)
+        ch = oracle.verify_chain("f32", lt, ld, 1, K, V, T, x, r, u, lib=lib)
+        parents = np.arange(-1, K, dtype=np.int32)[None]
+        tokens = np.concatenate([[[0]], x], axis=1).astype(np.int32)
+        dt = np.concatenate([ld, np.zeros((1, 1, V), np.float32)], axis=1)  # the leaf's draft row
+        rt = np.concatenate([[[1.0]], r], axis=1).astype(np.float32)
+        tr = oracle.verify_tree_sample("f32", lt, dt, 1, K, V, T, tokens, parents, rt, u, lib=lib)
+        n = int(ch["num_accepted"][0])
+        assert tr["accept_len"][0] == n, (i, ch, tr)
+        assert list(tr["out_tokens"][0]) == list(ch["out_tokens"][0]), (i, ch, tr)
+        assert list(tr["path"][0][: n + 1]) == list(range(n + 1)) and (tr["path"][0][n + 1:] == -1).all()
+        assert abs(tr["mass"][0] - (ch["mass"][0][n] if n < K else 1.0)) <= 1e-12, (i, ch, tr)
+        # the children tested are the draft positions up to the rejected one
+        assert np.allclose(tr["alpha"][0][1: min(n + 1, K) + 1], ch["alpha"][0][: min(n + 1, K)],
+                           rtol=0, atol=1e-15)
+        assert tr["req_flag"][0] == ch["req_flag"][0], (i, ch, tr)
+
+
+def pin_tree_sample_residual_closed_form(lib, n_cases=200):
+    """After j rejected siblings the target is max(0, p - c_j q) / R_j with c_1 = 0, R_1 = 1,
+    c_{j+1} = c_j + R_j and R_j = sum_i max(0, p_i - c_j q_i): an identity derived from the
+    residual step (max(0, max(0, p - c q) - R q) = max(0, p - (c + R) q) for q >= 0), checked on
+    the alpha of every sibling, the mass and the drawn token."""
+    rng = np.random.default_rng(47)
+    for _ in range(n_cases):
+        V, m = int(rng.integers(2, 10)), int(rng.integers(1, 6))
+        p = _rand_dist(rng, V)
+        q = _rand_dist(rng, V)
+        toks = rng.integers(0, V, m)
+        parents = np.array([-1] + [0] * m, np.int32)
+        tokens = np.concatenate([[0], toks]).astype(np.int32)
+        r = np.ones(m + 1, np.float32)  # accept only where alpha == 1
+        u = float(rng.integers(0, 1 << 24) / float(1 << 24))
+        P = np.vstack([p] + [p] * m)
+        Q = np.vstack([q] + [q] * m)
+        o = oracle.tree_sample_probs(P, Q, parents, tokens, r, u, TOL, lib=lib)
+        c, R = 0.0, 1.0
+        accepted = None
+        for j, x in enumerate(toks, start=1):
+            num = max(0.0, p[x] - c * q[x])
+            a = 1.0 if (q[x] == 0 or num >= R * q[x]) else num / (R * q[x])
+            assert abs(o["alpha"][j] - a) <= 1e-9 * max(1.0, a), (j, o["alpha"], a)
+            if a >= 1.0:
+                accepted = j
+                break
+            c, R = c + R, np.maximum(0.0, p - (c + R) * q).sum()
+        if accepted is not None:
+            assert o["accept_len"] == 1 and o["path"][1] == accepted
+            continue
+        w = np.maximum(0.0, p - c * q)
+        assert abs(o["mass"] - R) <= 1e-9, (o["mass"], R)
+        if o["req_flag"] & (oracle.FLAG_CDF_TIE | oracle.FLAG_ZERO_RESIDUAL):
+            continue
+        assert o["accept_len"] == 0 and o["out_tokens"][0] == _brute_inverse_cdf(w, u)
+
+
+def pin_tree_sample_greedy_walk(lib, n_cases=300):
+    """T == 0: the walk is the greedy tree walk (R9) of the pinned greedy tree verification."""
+    rng = np.random.default_rng(53)
+    for _ in range(n_cases):
+        N1, V = int(rng.integers(1, 16)), 20
+        parents, tokens = random_tree(rng, N1, V)
+        lt = rng.normal(0, 1, (1, N1, V)).astype(np.float32)
+        for i in range(1, N1):  # make matching paths likely
+            if rng.random() < 0.6:
+                lt[0, parents[i], tokens[i]] += 8.0
+        g = oracle.verify_tree_greedy("f32", lt, 1, N1 - 1, V, tokens[None], parents[None], lib=lib)
+        w = oracle.verify_tree_sample("f32", lt, None, 1, N1 - 1, V, 0.0, tokens[None],
+                                      parents[None], None, None, lib=lib)
+        assert w["accept_len"][0] == g["accept_len"][0]
+        assert (w["path"][0] == g["path"][0]).all() and (w["out_tokens"][0] == g["out_tokens"][0]).all()
+        assert w["err"][0] == 0 and w["mass"][0] == 1.0
+
+
+def pin_tree_sample_errors(lib):
+    """R11 and R14: a malformed tree or a bad token fails the request; a NaN row fails it only
+    when the walk visits that node; a leaf's draft row is never read."""
+    V, N = 4, 3
+    parents = np.array([[-1, 0, 0, 1]], np.int32)
+    tokens = np.array([[0, 1, 2, 3]], np.int32)
+    lt = np.zeros((1, N + 1, V), np.float32)
+    lt[0, 0, 2] = 9.0  # p_root concentrates on token 2: node 1 (token 1) rejected, node 2 accepted
+    ld = np.zeros((1, N + 1, V), np.float32)
+    ld[0, 2:] = np.nan  # leaves' draft rows: never read
+    r = np.full((1, N + 1), 0.5, np.float32)
+    u = np.full(1, 0.5, np.float32)
+    o = oracle.verify_tree_sample("f32", lt, ld, 1, N, V, 1.0, tokens, parents, r, u, lib=lib)
+    assert o["err"][0] == 0 and o["path"][0][1] == 2, o
+    lt3 = lt.copy()
+    lt3[0, 3, 0] = np.nan  # node 3 is not visited
+    o = oracle.verify_tree_sample("f32", lt3, ld, 1, N, V, 1.0, tokens, parents, r, u, lib=lib)
+    assert o["err"][0] == 0, o
+    lt0 = lt.copy()
+    lt0[0, 0, 1] = np.nan
+    for T in (1.0, 0.0):
+        o = oracle.verify_tree_sample("f32", lt0, ld, 1, N, V, T, tokens, parents, r, u, lib=lib)
+        assert o["err"][0] == oracle.ERR_NONFINITE and o["accept_len"][0] == 0
+        assert (o["out_tokens"][0] == -1).all() and (o["path"][0] == -1).all()
+    ldr = np.zeros_like(ld)
+    ldr[0, 0, 3] = np.inf
+    o = oracle.verify_tree_sample("f32", lt, ldr, 1, N, V, 1.0, tokens, parents, r, u, lib=lib)
+    assert o["err"][0] == oracle.ERR_NONFINITE
+    bad = np.array([[-1, 0, 2, 1]], np.int32)
+    o = oracle.verify_tree_sample("f32", lt, ld, 1, N, V, 1.0, tokens, bad, r, u, lib=lib)
+    assert o["err"][0] == oracle.ERR_BAD_TREE
+    o = oracle.verify_tree_sample("f32", lt, ld, 1, N, V, 1.0, np.array([[0, 1, 9, 3]], np.int32),
+                                  parents, r, u, lib=lib)
+    assert o["err"][0] == oracle.ERR_BAD_TOKEN
+
+
+FAST_PINS += [pin_hand_tree_sample_cases, pin_tree_sample_chain_reduction,
+              pin_tree_sample_residual_closed_form, pin_tree_sample_greedy_walk,
+              pin_tree_sample_errors]

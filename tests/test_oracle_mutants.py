@@ -34,7 +34,8 @@ MUTANTS = [
     ("zero_residual_fallback_dropped", "c = oracle_inverse_cdf(pk, V, (double)u, tol, &S2, &fl);",
      "c = 0;"),
     ("argmax_last_on_ties", "if (l[i] > l[a])", "if (l[i] >= l[a])"),
-    ("tree_compares_child_row", "tokens[c] == a)", "tokens[c] == amax[c])"),
+    ("tree_compares_child_row", "parents[c] == cur && tokens[c] == a)",
+     "parents[c] == cur && tokens[c] == amax[c])"),
     ("tree_final_token_from_root", "out_tokens[len] = amax[cur];", "out_tokens[len] = amax[0];"),
     ("tree_parent_check_dropped", "if (parents[i] < 0 || parents[i] >= i)", "if (0)"),
     ("bf16_widening_shift", "[i] << 16;", "[i] << 15;"),
@@ -43,6 +44,18 @@ MUTANTS = [
     ("greedy_compares_next_row", "while (n < K && x[n] == cand[n])", "while (n < K && x[n] == cand[n + 1])"),
     ("residual_band_not_scaled", "oracle_inverse_cdf(w, V, (double)u, tol / S, &S3, &fl);",
      "oracle_inverse_cdf(w, V, (double)u, tol, &S3, &fl);"),
+    ("tree_sample_no_residual_update", "p[i] = w[i] / S;", "p[i] = p[i];"),
+    ("tree_sample_residual_not_normalised", "p[i] = w[i] / S;", "p[i] = w[i];"),
+    ("tree_sample_residual_sign_flipped", "double d = p[i] - q[i];", "double d = q[i] - p[i];"),
+    ("tree_sample_alpha_inverted", "1.0 : p[x] / q[x]; /* step 1, R2 */", "1.0 : q[x] / p[x]; /* step 1, R2 */"),
+    ("tree_sample_draw_from_node_p", "tok = oracle_inverse_cdf(p, V, (double)u, tol / R, &S2, &fl);",
+     "tok = oracle_inverse_cdf(p0, V, (double)u, tol / R, &S2, &fl);"),
+    ("tree_sample_band_not_scaled", "if (fabs((double)r[c] - a) <= tol / R)", "if (fabs((double)r[c] - a) <= tol)"),
+    ("tree_sample_mass_not_accumulated", "R *= S;", "R = S;"),
+    ("tree_sample_accept_strict_less", "if ((double)r[c] <= a) { /* step 2: accepted */",
+     "if ((double)r[c] < a) { /* step 2: accepted */"),
+    ("tree_greedy_walk_final_token", "out_tokens[len] = a;\n            break;",
+     "out_tokens[len] = tokens[cur];\n            break;"),
     ("bad_token_check_dropped", "if (xb[k] < 0 || xb[k] >= V)\n                e |= ORE_BAD_TOKEN;",
      "if (0)\n                e |= ORE_BAD_TOKEN;"),
 ]

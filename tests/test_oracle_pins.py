@@ -125,3 +125,55 @@ def test_chi2_detects_a_wrong_distribution():
     toks = np.searchsorted(np.cumsum(q), rng.random(100_000), side="right").clip(0, 7)
     counts = np.bincount(toks, minlength=8).astype(float)
     assert pins.chi2_pvalue(counts, p) < 1e-6
+
+
+def test_invariance_theorem_tree_walk(lib):
+    """Stochastic tree walk (each rejected sibling replaces the target by its residual): with
+    children drawn independently from the parent's draft row, the token emitted after a prefix
+    follows the target row of that prefix.  2 x 10^5 seeded trials at V=8, tree 1-3-6;
+    chi-squared per prefix (root; each first token; each pair of first tokens with enough
+    trials)."""
+    ti = synth.tree_sample_tiny(seed=5, trials=200_000)
+    T = float(ti.temperature)
+    o = oracle.verify_tree_sample("f32", ti.target, ti.draft, ti.B, ti.N, ti.V, T, ti.node_tokens,
+                                  ti.parents, ti.r, ti.u, threads=8, lib=lib)
+    assert (o["err"] == 0).all()
+    L, out = o["accept_len"], o["out_tokens"]
+    p0 = sp_softmax(ti.meta["t0"].astype(np.float64) / T)
+    p1 = sp_softmax(ti.meta["t1"].astype(np.float64) / T, axis=-1)
+    p2 = sp_softmax(ti.meta["t2"].astype(np.float64) / T, axis=-1)
+    V = ti.V
+    assert pins.chi2_pvalue(np.bincount(out[:, 0], minlength=V).astype(float), p0) > 1e-3
+    tested = 0
+    for a in range(V):
+        sel = (L >= 1) & (out[:, 0] == a)
+        if sel.sum() >= 400:
+            pv = pins.chi2_pvalue(np.bincount(out[sel, 1], minlength=V).astype(float), p1[a])
+            assert pv > 1e-4, (a, pv)
+            tested += 1
+        for b in range(V):
+            sel2 = (L >= 2) & (out[:, 0] == a) & (out[:, 1] == b)
+            if sel2.sum() >= 400:
+                pv = pins.chi2_pvalue(np.bincount(out[sel2, 2], minlength=V).astype(float), p2[a, b])
+                assert pv > 1e-4, (a, b, pv)
+                tested += 1
+    assert tested >= 10
+    # more than one sibling is tested in a good share of the walks (the residual update matters)
+    assert ((o["alpha"][:, 2:4] >= 0).any(axis=1)).mean() > 0.2
+
+
+def test_chi2_detects_a_tree_walk_without_residual_update(lib, tmp_path):
+    """The tree invariance check has power: an oracle copy whose siblings are all tested against
+    the node's own p (no residual update) fails it."""
+    src = open(oracle.SRC).read()
+    bad = src.replace("p[i] = w[i] / S;", "p[i] = p[i];")
+    assert bad != src
+    f = tmp_path / "mut.c"
+    f.write_text(bad)
+    mlib = oracle.load(oracle.build(str(f), str(tmp_path / "mut.so")))
+    ti = synth.tree_sample_tiny(seed=5, trials=100_000)
+    T = float(ti.temperature)
+    o = oracle.verify_tree_sample("f32", ti.target, ti.draft, ti.B, ti.N, ti.V, T, ti.node_tokens,
+                                  ti.parents, ti.r, ti.u, threads=8, lib=mlib)
+    p0 = sp_softmax(ti.meta["t0"].astype(np.float64) / T)
+    assert pins.chi2_pvalue(np.bincount(o["out_tokens"][:, 0], minlength=ti.V).astype(float), p0) < 1e-6
