@@ -77,7 +77,9 @@ typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1, SPEC_DTYPE_F16 = 2 } spe
 
 /* Largest supported sizes. */
 #define SPEC_MAX_K 256           /* draft tokens per request (chain / n-gram) */
-#define SPEC_MAX_TREE_NODES 4096 /* N + 1 for tree verification */
+#define SPEC_MAX_TREE_NODES 4096 /* N + 1 for spec_verify_tree_greedy */
+#define SPEC_MAX_WALK_NODES 1024 /* N + 1 for spec_verify_tree_walk */
+#define SPEC_MAX_WALK_VOCAB 262144 /* V for spec_verify_tree_walk */
 
 /* Bytes of workspace for a call on B requests with vocabulary V of `dtype`, where
  * rows_per_request is the number of logits rows the call reads per request:
@@ -167,6 +169,56 @@ spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t dt
                                       int32_t *path_nodes, int32_t *out_tokens,
                                       int32_t *err_flags, int32_t *node_argmax, void *workspace,
                                       size_t workspace_bytes, spec_stream_t stream);
+
+/*
+ * Verification of a draft tree by walking it from the root, stochastic (T > 0) or greedy
+ * (T == 0).  Reads only the rows of the nodes the walk visits.
+ *
+ * Stochastic walk: section I.1 of the page named at the top, applied to the children of each
+ * visited node in turn.  With p = softmax(target row / T) and q = softmax(draft row / T) of the
+ * visited node, its children are tested in ascending node index: child c with token x is accepted
+ * when r[b][c] <= alpha = min(1, p'(x) / q(x)), where p' is the current target (p at first); the
+ * walk then moves to c.  A rejected child replaces the target by its residual
+ * max(0, p' - q) / sum max(0, p' - q) before the next sibling is tested (same q).  When no child
+ * is accepted, or the node has none, the token is drawn from the current target by the inverse
+ * CDF with u[b].  Lossless when the children of a node are independent draws from its q.  A
+ * chain (one child per node) is exactly spec_verify_chain.  Greedy walk (T == 0): the child whose
+ * token equals the argmax of the node's target row (the lowest node index if several), as in
+ * spec_verify_tree_greedy, but reading only the visited rows.
+ *
+ * target_logits  [B][N+1][V] dtype; row n is the target's prediction after node n.
+ * draft_logits   [B][N+1][V] dtype; row n is the draft distribution the children of node n were
+ *                drawn from.  Rows of nodes without children are never read; not read at all
+ *                (may be NULL) when temperature == 0.
+ * node_tokens    [B][N+1] int32 (entry 0 ignored); parents [B][N+1] int32, parents[0] = -1 and
+ *                0 <= parents[i] < i.
+ * r              [B][N+1] float in (0, 1]: r[b][c] is the uniform of child c's test (entry 0
+ *                unused).  u [B] float in [0, 1).  Neither is read when temperature == 0.
+ * Outputs:
+ * accept_len     [B] int32: accepted draft tokens on the path.
+ * path_nodes     [B][N+1] int32: the accepted path, root first, then -1.
+ * out_tokens     [B][N+1] int32: the accepted tokens, then the drawn (greedy: argmax) token,
+ *                then -1.
+ * residual_mass  [B] float or NULL: the total weight of the draw's residual when siblings were
+ *                rejected at the last node; 1 when none was (and in greedy mode); 0 when the
+ *                residual vanished in rounding and the draw fell back to p.
+ * err_flags      [B] int32 or NULL: SPEC_ERRF_* bits.  A malformed tree or a node token outside
+ *                [0, V) (the lowest offending node decides), or a non-finite visited row, fails
+ *                the request: accept_len 0, path and tokens -1.  Rows the walk does not visit are
+ *                not checked.
+ * accept_prob    [B][N+1] float or NULL: alpha of every child tested (greedy: 1 for the matching
+ *                child, 0 for the siblings tested before it), -1 for the others.
+ * Limits: N + 1 <= SPEC_MAX_WALK_NODES, V <= SPEC_MAX_WALK_VOCAB (SPEC_ERR_UNSUPPORTED beyond).
+ * One kernel launch; no workspace.  A request occupies a cluster of up to 16 CTAs (V / 16384
+ * rounded up to a power of two; one CTA for V <= 4096); as many clusters as fit run at once.
+ */
+spec_status_t spec_verify_tree_walk(const void *target_logits, const void *draft_logits,
+                                    spec_dtype_t dtype, int B, int N, int V, float temperature,
+                                    const int32_t *node_tokens, const int32_t *parents,
+                                    const float *r, const float *u, int32_t *accept_len,
+                                    int32_t *path_nodes, int32_t *out_tokens,
+                                    float *residual_mass, int32_t *err_flags,
+                                    float *accept_prob, spec_stream_t stream);
 
 /*
  * spec_verify_chain without a workspace argument, for callers that cannot allocate device memory

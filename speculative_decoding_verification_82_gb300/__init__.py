@@ -12,5 +12,6 @@ from .binding import (  # noqa: F401
     spec_verify_chain,
     spec_verify_ngram,
     spec_verify_tree_greedy,
+    spec_verify_tree_walk,
     workspace_bytes,
 )

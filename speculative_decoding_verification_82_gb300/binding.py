@@ -18,11 +18,12 @@ from .build import LIB_PATH
 
 SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_CUDA, SPEC_ERR_WORKSPACE, SPEC_ERR_UNSUPPORTED = range(5)
 ERRF_BAD_TOKEN, ERRF_NONFINITE, ERRF_TIMEOUT, ERRF_BAD_TREE = 1, 2, 4, 8
-MAX_K, MAX_TREE_NODES = 256, 4096
+MAX_K, MAX_TREE_NODES, MAX_WALK_NODES, MAX_WALK_VOCAB = 256, 4096, 1024, 262144
 DTYPE_CODE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 
 EXPORTED = ("spec_verify_workspace_bytes", "spec_verify_workspace_reset", "spec_verify_chain",
-            "spec_verify_ngram", "spec_verify_tree_greedy", "spec_verify_chain_static", "spec_status_string")
+            "spec_verify_ngram", "spec_verify_tree_greedy", "spec_verify_tree_walk",
+            "spec_verify_chain_static", "spec_status_string")
 STATIC_WORKSPACE_BYTES = 4 << 20
 
 _lib = None
@@ -52,6 +53,8 @@ def library(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_ngram.restype = I
     lib.spec_verify_tree_greedy.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, P, Z, P]
     lib.spec_verify_tree_greedy.restype = I
+    lib.spec_verify_tree_walk.argtypes = [P, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P]
+    lib.spec_verify_tree_walk.restype = I
     lib.spec_verify_chain_static.argtypes = [P, P, I, I, I, I, F, P, P, P, P, P, P, P, P]
     lib.spec_verify_chain_static.restype = I
     lib.spec_status_string.argtypes = [I]
@@ -206,3 +209,36 @@ def spec_verify_tree_greedy(target_logits, node_tokens, parents, *, workspace=No
                                      workspace.numel(), _stream(dev))
     _check(st)
     return dict(accept_len=al, path_nodes=pn, out_tokens=ot, err_flags=ef)
+
+
+def spec_verify_tree_walk(target_logits, draft_logits, node_tokens, parents, r, u, temperature, *,
+                          out=None, accept_prob=None) -> dict:
+    """Verification of a draft tree by walking it (stochastic for T > 0, greedy for T == 0),
+    reading only the visited rows.  See spec_verify.h."""
+    lib = library()
+    dev = target_logits.device
+    if target_logits.dtype not in DTYPE_CODE or target_logits.dim() != 3:
+        raise TypeError("target_logits must be a [B][N+1][V] float32/bfloat16/float16 tensor")
+    B, N1, V = target_logits.shape
+    T = float(temperature)
+    _need(target_logits, "target_logits", None, (B, N1, V), dev)
+    _need(node_tokens, "node_tokens", torch.int32, (B, N1), dev)
+    _need(parents, "parents", torch.int32, (B, N1), dev)
+    if T > 0:
+        _need(draft_logits, "draft_logits", target_logits.dtype, (B, N1, V), dev)
+        _need(r, "r", torch.float32, (B, N1), dev)
+        _need(u, "u", torch.float32, (B,), dev)
+    out = dict(out or {})
+    al = _out(out.get("accept_len"), "accept_len", torch.int32, (B,), dev)
+    pn = _out(out.get("path_nodes"), "path_nodes", torch.int32, (B, N1), dev)
+    ot = _out(out.get("out_tokens"), "out_tokens", torch.int32, (B, N1), dev)
+    rm = _out(out.get("residual_mass"), "residual_mass", torch.float32, (B,), dev)
+    ef = _out(out.get("err_flags"), "err_flags", torch.int32, (B,), dev)
+    ap = _opt(accept_prob, "accept_prob", torch.float32, (B, N1), dev)
+    st = lib.spec_verify_tree_walk(_ptr(target_logits), _ptr(draft_logits) if T > 0 else None,
+                                   DTYPE_CODE[target_logits.dtype], B, N1 - 1, V, T,
+                                   _ptr(node_tokens), _ptr(parents), _ptr(r) if T > 0 else None,
+                                   _ptr(u) if T > 0 else None, _ptr(al), _ptr(pn), _ptr(ot),
+                                   _ptr(rm), _ptr(ef), _ptr(ap), _stream(dev))
+    _check(st)
+    return dict(accept_len=al, path_nodes=pn, out_tokens=ot, residual_mass=rm, err_flags=ef)

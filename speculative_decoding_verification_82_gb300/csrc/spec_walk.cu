@@ -1,0 +1,142 @@
+// spec_walk.cu -- spec_verify_tree_walk: argument checks, cluster geometry, launch.
+//
+// Host side of the tree walk (tree_walk.cuh).  A request goes to one thread-block cluster of
+// `cl` CTAs of 512 threads; each thread holds E consecutive tokens of the visited rows in
+// registers, so a cluster covers V <= cl * 512 * E.  The grid is as many clusters as fit on the
+// device at once (at most B), each taking requests b, b + grid, ...
+#include <math.h>
+#include <stdint.h>
+
+#include <mutex>
+
+#include "spec_verify.h"
+#include "tree_walk.cuh"
+
+namespace {
+
+using specv::walk::Params;
+
+constexpr int kSmallE = 8;   // V <= 4096: one CTA
+constexpr int kLargeE = 32;  // otherwise clusters of 1..16 CTAs
+
+struct Geometry {
+  int E, cl;
+};
+// The smallest cluster that covers V (larger vocabularies first grow the cluster, which
+// shortens every pass; 16 CTAs is the largest cluster the hardware schedules).
+bool plan(int V, Geometry* g) {
+  if (V <= specv::walk::kThreads * kSmallE) {
+    g->E = kSmallE;
+    g->cl = 1;
+    return true;
+  }
+  const long long per_cta = (long long)specv::walk::kThreads * kLargeE;
+  for (int cl = 1; cl <= specv::walk::kMaxCluster; cl *= 2) {
+    if ((long long)cl * per_cta >= V) {
+      g->E = kLargeE;
+      g->cl = cl;
+      return true;
+    }
+  }
+  return false;
+}
+
+template <typename T, int E>
+cudaError_t launch_one(const Params& P, cudaStream_t stream) {
+  auto kern = specv::walk::walk_kernel<T, E>;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)P.cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(specv::walk::kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // clusters resident at once, per (device, instantiation, cluster size); found once
+  static std::mutex mu;
+  static int cache[64][specv::walk::kMaxCluster + 1] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  int fit = 0;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (dev >= 0 && dev < 64) fit = cache[dev][P.cl];
+  }
+  if (fit <= 0) {
+    if (P.cl > 8) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
+    cfg.gridDim = dim3((unsigned)P.cl);
+    e = cudaOccupancyMaxActiveClusters(&fit, kern, &cfg);
+    if (e != cudaSuccess) return e;
+    if (fit <= 0) return cudaErrorInvalidConfiguration;
+    std::lock_guard<std::mutex> g(mu);
+    if (dev >= 0 && dev < 64) cache[dev][P.cl] = fit;
+  }
+  const int clusters = P.B < fit ? P.B : fit;
+  cfg.gridDim = dim3((unsigned)(clusters * P.cl));
+  return cudaLaunchKernelEx(&cfg, kern, P);
+}
+
+template <typename T>
+cudaError_t launch_typed(int E, const Params& P, cudaStream_t stream) {
+  return E == kSmallE ? launch_one<T, kSmallE>(P, stream) : launch_one<T, kLargeE>(P, stream);
+}
+
+bool aligned(const void* p, unsigned a) { return ((uintptr_t)p % a) == 0; }
+
+}  // namespace
+
+extern "C" spec_status_t spec_verify_tree_walk(const void* target_logits, const void* draft_logits,
+                                               spec_dtype_t dtype, int B, int N, int V, float temperature,
+                                               const int32_t* node_tokens, const int32_t* parents, const float* r,
+                                               const float* u, int32_t* accept_len, int32_t* path_nodes,
+                                               int32_t* out_tokens, float* residual_mass, int32_t* err_flags,
+                                               float* accept_prob, spec_stream_t stream) {
+  if (!(dtype == SPEC_DTYPE_F32 || dtype == SPEC_DTYPE_BF16 || dtype == SPEC_DTYPE_F16)) return SPEC_ERR_INVALID_ARG;
+  if (B < 0 || N < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (!(temperature >= 0.f) || isinf(temperature)) return SPEC_ERR_INVALID_ARG;
+  if (N + 1 > SPEC_MAX_WALK_NODES) return SPEC_ERR_UNSUPPORTED;
+  Geometry g;
+  if (!plan(V, &g)) return SPEC_ERR_UNSUPPORTED;
+  if (B == 0) return SPEC_OK;
+  const bool greedy = temperature == 0.f;
+  if (!target_logits || !node_tokens || !parents || !accept_len || !path_nodes || !out_tokens)
+    return SPEC_ERR_INVALID_ARG;
+  if (!greedy && (!draft_logits || !r || !u)) return SPEC_ERR_INVALID_ARG;
+  const unsigned S = dtype == SPEC_DTYPE_F32 ? 4u : 2u;
+  if (!aligned(target_logits, S) || (!greedy && !aligned(draft_logits, S))) return SPEC_ERR_INVALID_ARG;
+  Params P = {};
+  P.target = target_logits;
+  P.draft = greedy ? nullptr : draft_logits;
+  P.B = B;
+  P.N1 = N + 1;
+  P.V = V;
+  P.c = greedy ? 0.f : (float)(1.4426950408889634 / (double)temperature);  // log2(e) / T
+  P.vec = ((size_t)V * S) % 16 == 0 && aligned(target_logits, 16) && (greedy || aligned(draft_logits, 16));
+  P.cl = g.cl;
+  P.node_tokens = node_tokens;
+  P.parents = parents;
+  P.r = r;
+  P.u = u;
+  P.accept_len = accept_len;
+  P.path_nodes = path_nodes;
+  P.out_tokens = out_tokens;
+  P.residual_mass = residual_mass;
+  P.err_flags = err_flags;
+  P.accept_prob = accept_prob;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e;
+  switch (dtype) {
+    case SPEC_DTYPE_F32: e = launch_typed<float>(g.E, P, st); break;
+    case SPEC_DTYPE_BF16: e = launch_typed<__nv_bfloat16>(g.E, P, st); break;
+    default: e = launch_typed<__half>(g.E, P, st); break;
+  }
+  if (e == cudaErrorInvalidConfiguration) return SPEC_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+}

@@ -321,6 +321,49 @@ __device__ __forceinline__ float warp_incl_scan(float v, int lane) {
   }
   return v;
 }
+// ------------------------------------------------------------- exponent arithmetic ----
+// An exponent as an unevaluated fp32 pair hi + lo, |lo| far below one unit of hi's last place
+// plus a few such units: fp32 arithmetic that keeps the digits a double would (GB300's FP64
+// operations take tens of cycles each).
+struct Exp2 {
+  float hi, lo;
+};
+// a + b = s + err exactly (Knuth's two-sum).
+__device__ __forceinline__ void two_sum(float a, float b, float& s, float& err) {
+  s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+}
+// l c - mc with the product l c carried exactly (an fp32 pair from one FMA) and the difference as
+// a two-sum: the exponent of 2^(l c - mc) must not lose the digits that a large |l c| would round
+// away in plain fp32.
+__device__ __forceinline__ Exp2 scaled_logit(float l, float c, float mc) {
+  const float p = __fmul_rn(l, c);
+  const float e = __fmaf_rn(l, c, -p);  // l c = p + e exactly
+  Exp2 x;
+  float r;
+  two_sum(p, -mc, x.hi, r);
+  x.lo = __fadd_rn(r, e);
+  return x;
+}
+__device__ __forceinline__ Exp2 exp2_sub(const Exp2& a, const Exp2& b) {
+  Exp2 x;
+  float r;
+  two_sum(a.hi, -b.hi, x.hi, r);
+  x.lo = __fadd_rn(r, __fsub_rn(a.lo, b.lo));
+  return x;
+}
+// 2^x * f for x = hi + lo and fp32 f > 0, in fp32: the integer part of hi as an exact power of
+// two, the rest (hi minus its floor, exact, plus lo) through the special-function unit.
+// Saturates to +inf / 0.
+__device__ __forceinline__ float exp2_times(const Exp2& x, float f) {
+  if (!(x.hi > -300.f)) return 0.f;
+  if (x.hi > 300.f) return INFINITY;
+  const float n = floorf(x.hi);
+  const float r = __fmul_rn(ex2(__fadd_rn(__fsub_rn(x.hi, n), x.lo)), f);  // in (0, 2) * f
+  return ldexpf(r, (int)n);
+}
+
 // ------------------------------------------------------------------------ row staging ----
 // A logits row is read as a grid of 16-byte vectors starting at the row's address rounded down to
 // 16 bytes: grid vector v holds elements v * VE - phase .. v * VE - phase + VE - 1, where phase is

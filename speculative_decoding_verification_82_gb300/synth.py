@@ -352,9 +352,10 @@ def tree_sample(seed: int = 0, B: int = 16, V: int = 128256, temperature: float 
     t32 = _rng(seed, _S_TARGET).standard_normal((B, N1, V), dtype=np.float32) * np.float32(3.0)
     boosts = zipf_boosts()
     srng = _rng(seed, _S_SPIKE)
+    ns = min(boosts.size, V)  # a vocabulary smaller than the spike count takes the largest ones
     for b in range(B):
         for n in range(N1):
-            t32[b, n, srng.choice(V, size=boosts.size, replace=False)] += boosts
+            t32[b, n, srng.choice(V, size=ns, replace=False)] += boosts[:ns]
     d32 = t32 + _rng(seed, _S_DRAFT).standard_normal((B, N1, V), dtype=np.float32) * np.float32(draft_sigma)
     target, draft = encode(t32, dtype), encode(d32, dtype)
     del t32, d32

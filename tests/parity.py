@@ -145,3 +145,61 @@ def compare_tree(g: dict, o: dict) -> dict:
     assert np.array_equal(g["path_nodes"], o["path"]), "paths differ"
     assert np.array_equal(g["out_tokens"], o["out_tokens"]), "emitted tokens differ"
     return dict(requests=int(ok.size), mean_accepted=float(o["accept_len"].mean()))
+
+
+# ------------------------------------------------------------------------ tree walk ----
+def run_gpu_walk(ti, temperature=None) -> dict:
+    T = float(ti.temperature if temperature is None else temperature)
+    tl = to_device(ti.target, ti.dtype)
+    dl = to_device(ti.draft, ti.dtype) if (T > 0 and ti.draft is not None) else None
+    r = f32(ti.r) if T > 0 else None
+    u = f32(ti.u) if T > 0 else None
+    ap = torch.full((ti.B, ti.N + 1), -7.0, device="cuda")
+    o = binding.spec_verify_tree_walk(tl, dl, i32(ti.node_tokens), i32(ti.parents), r, u, T,
+                                      accept_prob=ap)
+    torch.cuda.synchronize()
+    res = {k: v.cpu().numpy() for k, v in o.items()}
+    res["accept_prob"] = ap.cpu().numpy()
+    return res
+
+
+def run_oracle_walk(ti, temperature=None, threads: int = 8) -> dict:
+    T = float(ti.temperature if temperature is None else temperature)
+    return oracle.verify_tree_sample(ti.dtype, ti.target, ti.draft if T > 0 else None, ti.B, ti.N,
+                                     ti.V, T, ti.node_tokens, ti.parents,
+                                     ti.r if T > 0 else None, ti.u if T > 0 else None,
+                                     threads=threads)
+
+
+def compare_walk(g: dict, o: dict, ti) -> dict:
+    """Parity of a tree walk: error bits exact; unflagged requests exact (path, tokens, the set of
+    children tested); alpha of the children tested and the residual mass within 1e-5; flagged
+    requests end on a valid path."""
+    assert np.array_equal(g["err_flags"], o["err"]), ("walk error bits differ",
+                                                      np.nonzero(g["err_flags"] != o["err"])[0][:10])
+    ok = o["err"] == 0
+    bad = np.nonzero(~ok)[0]
+    assert (g["accept_len"][bad] == 0).all() and (g["out_tokens"][bad] == -1).all()
+    assert (g["path_nodes"][bad] == -1).all() and (g["accept_prob"][bad] == -1).all()
+    flagged = (o["req_flag"] & (oracle.FLAG_ACCEPT_TIE | oracle.FLAG_CDF_TIE)) != 0
+    ex = np.nonzero(ok & ~flagged)[0]
+    assert np.array_equal(g["accept_len"][ex], o["accept_len"][ex]), "accepted lengths differ"
+    assert np.array_equal(g["path_nodes"][ex], o["path"][ex]), "paths differ"
+    assert np.array_equal(g["out_tokens"][ex], o["out_tokens"][ex]), "emitted tokens differ"
+    tested_g, tested_o = g["accept_prob"][ex] >= 0, o["alpha"][ex] >= 0
+    assert np.array_equal(tested_g, tested_o), "children tested differ"
+    da = np.abs(g["accept_prob"][ex] - o["alpha"][ex])[tested_o]
+    assert da.size == 0 or da.max() <= PROB_TOL, ("alpha", da.max())
+    dm = np.abs(g["residual_mass"][ex] - o["mass"][ex])
+    assert dm.size == 0 or dm.max() <= PROB_TOL, ("residual mass", dm.max())
+    for b in np.nonzero(ok & flagged)[0]:  # any valid outcome
+        L = int(g["accept_len"][b])
+        path = g["path_nodes"][b]
+        assert path[0] == 0 and (path[L + 1:] == -1).all()
+        for j in range(1, L + 1):
+            assert ti.parents[b][path[j]] == path[j - 1]
+            assert g["out_tokens"][b][j - 1] == ti.node_tokens[b][path[j]]
+        assert 0 <= g["out_tokens"][b][L] < ti.V and (g["out_tokens"][b][L + 1:] == -1).all()
+    return dict(requests=int(ok.size), errors=int((~ok).sum()), flagged=int(flagged.sum()),
+                mean_accepted=float(g["accept_len"][ok].mean()) if ok.any() else 0.0,
+                max_alpha_diff=float(da.max()) if da.size else 0.0)

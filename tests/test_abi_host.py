@@ -116,3 +116,30 @@ def test_workspace_reset_is_host_only(lib):
     lib.spec_verify_workspace_reset(None)
     lib.spec_verify_workspace_reset(ctypes.c_void_p(0x1000))
     lib.spec_verify_workspace_reset(ctypes.c_void_p(0x1000))
+
+
+def test_tree_walk_validation(lib):
+    P = ctypes.c_void_p
+    f = lib.spec_verify_tree_walk
+    ok = dict(t=1 << 20, d=7 << 20, dt=1, B=2, N=5, V=64, T=1.0, tok=2 << 20, par=3 << 20,
+              r=8 << 20, u=9 << 20, al=4 << 20, pn=5 << 20, ot=6 << 20)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(P(a["t"]), P(a["d"]), a["dt"], a["B"], a["N"], a["V"], a["T"], P(a["tok"]),
+                 P(a["par"]), P(a["r"]), P(a["u"]), P(a["al"]), P(a["pn"]), P(a["ot"]), None, None,
+                 None, None)
+
+    assert call(B=0) == binding.SPEC_OK
+    assert call(dt=5) == binding.SPEC_ERR_INVALID_ARG
+    assert call(N=-1) == binding.SPEC_ERR_INVALID_ARG
+    assert call(V=0) == binding.SPEC_ERR_INVALID_ARG
+    assert call(T=-1.0) == binding.SPEC_ERR_INVALID_ARG
+    assert call(T=float("nan")) == binding.SPEC_ERR_INVALID_ARG
+    assert call(N=binding.MAX_WALK_NODES) == binding.SPEC_ERR_UNSUPPORTED
+    assert call(V=binding.MAX_WALK_VOCAB + 1) == binding.SPEC_ERR_UNSUPPORTED
+    assert call(par=0) == binding.SPEC_ERR_INVALID_ARG
+    assert call(d=0) == binding.SPEC_ERR_INVALID_ARG        # T > 0 needs draft logits
+    assert call(r=0) == binding.SPEC_ERR_INVALID_ARG
+    assert call(t=(1 << 20) + 1) == binding.SPEC_ERR_INVALID_ARG  # misaligned bf16
