@@ -15,7 +15,8 @@ CUDA-event interval over its calls, which run back to back from a replayed CUDA 
 calls), against the measured HBM copy bandwidth; `cpu_baseline` = the CPU oracle on the host
 cores.
 
-  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload chain_batched|tree_greedy|ngram]
+  python bench.py [--gpus N] [--steps K] [--warmup W]
+                  [--workload chain_batched|tree_greedy|ngram|tree_sample|tree_walk_greedy]
   python bench.py --impl reference ...   (the CPU oracle as the reference arm)
 """
 
@@ -46,12 +47,22 @@ WORKLOADS = {
                         desc="greedy tree verify: B=16, 61-node EAGLE-2-like tree (depth 6), V=128256 bf16"),
     "ngram": dict(kind="ngram", B=256, K=5, V=151936, dtype="bf16", T=0.8,
                   desc="n-gram prompt-lookup verify: B=256 K=5 V=151936 bf16 T=0.8, one-hot draft"),
+    # tree verification by walking (reads only the visited rows)
+    "tree_sample": dict(kind="walk", B=16, N=60, V=128256, dtype="bf16", T=1.0,
+                        desc="stochastic tree verify by walking: B=16, 61-node EAGLE-2-like tree, V=128256 "
+                             "bf16 T=1.0, target + draft logits, children drawn from the draft"),
+    "tree_walk_greedy": dict(kind="walk", B=16, N=60, V=128256, dtype="bf16", T=0.0,
+                             desc="greedy tree verify by walking: B=16, 61-node EAGLE-2-like tree (depth 6), "
+                                  "V=128256 bf16"),
 }
 FALLBACK_HBM_GBS = 6800.0
 KERNEL_SOURCES = ["speculative_decoding_verification_82_gb300/csrc/verify_kernel.cuh",
                   "speculative_decoding_verification_82_gb300/csrc/verify_common.cuh",
                   "speculative_decoding_verification_82_gb300/csrc/fastdiv.h",
                   "speculative_decoding_verification_82_gb300/csrc/spec_verify_api.cu"]
+WALK_SOURCES = ["speculative_decoding_verification_82_gb300/csrc/tree_walk.cuh",
+                "speculative_decoding_verification_82_gb300/csrc/verify_common.cuh",
+                "speculative_decoding_verification_82_gb300/csrc/spec_walk.cu"]
 
 
 # ----------------------------------------------------------------------------- inputs ----
@@ -64,14 +75,25 @@ def make_inputs(name: str, seed: int):
         return synth.tree_greedy(seed=seed)
     if name == "ngram":
         return synth.ngram(seed=seed)
+    if name == "tree_sample":
+        return synth.tree_sample(seed=seed)
+    if name == "tree_walk_greedy":
+        return synth.tree_greedy(seed=seed)
     raise ValueError(name)
 
 
 def rows_per_request(w: dict) -> int:
+    """Logits rows a request supplies: a walk's draft rows count for the nodes with children (the
+    rows that exist as the draft's output), 21 of the 61 nodes of the benchmark tree."""
     if w["kind"] == "chain":
         return 2 * w["K"] + 1
     if w["kind"] == "ngram":
         return w["K"] + 1
+    if w["kind"] == "walk" and w["T"] > 0:
+        from speculative_decoding_verification_82_gb300 import synth
+
+        par = synth.eagle_tree_parents()
+        return par.size + int(np.unique(par[1:]).size)
     return w["N"] + 1
 
 
@@ -92,7 +114,7 @@ def algorithmic_bytes(w: dict) -> int:
     B, V = w["B"], w["V"]
     es = 4 if w["dtype"] == "f32" else 2
     logits = B * rows_per_request(w) * V * es
-    if w["kind"] == "tree":
+    if w["kind"] in ("tree", "walk"):
         small_in = 2 * B * (w["N"] + 1) * 4
         out = B * 4 + 2 * B * (w["N"] + 1) * 4 + B * 4
     else:
@@ -100,6 +122,27 @@ def algorithmic_bytes(w: dict) -> int:
         small_in = B * K * 4 * 2 + B * 4
         out = B * 4 + B * (K + 1) * 4 + B * 4 + B * 4
     return logits + small_in + out
+
+
+def walk_read_bytes(w: dict, case) -> int:
+    """Bytes a tree walk call reads for the outputs it produced: per request, the target row of
+    every visited node and the draft row of every visited node with children (T > 0), plus the
+    tree arrays, the uniforms and the outputs."""
+    B, N1, V = w["B"], w["N"] + 1, w["V"]
+    es = 4 if w["dtype"] == "f32" else 2
+    L = case.out["accept_len"].cpu().numpy()
+    path = case.out["path_nodes"].cpu().numpy()
+    par = case.parents.cpu().numpy()
+    total = 0
+    for b in range(B):
+        has_kids = np.zeros(N1, bool)
+        has_kids[par[b, 1:]] = True
+        nodes = path[b, : L[b] + 1]
+        rows = len(nodes) + (int(has_kids[nodes].sum()) if w["T"] > 0 else 0)
+        total += rows * V * es
+    small = B * N1 * 4 * 2 + (B * N1 * 4 + B * 4 if w["T"] > 0 else 0)
+    out = B * 4 + 2 * B * N1 * 4 + B * 4 + B * 4
+    return total + small + out
 
 
 # ------------------------------------------------------------------------------ clocks ----
@@ -172,9 +215,9 @@ def hbm_peak() -> tuple[float, str]:
         return FALLBACK_HBM_GBS, "of fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(workload: str = "chain_batched") -> str:
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in (WALK_SOURCES if WORKLOADS[workload]["kind"] == "walk" else KERNEL_SOURCES):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -189,7 +232,7 @@ def profiled_traffic(workload: str):
         return None
     m_b = re.search(r"traffic_bytes_per_call:\s*([0-9]+)", text)
     m_h = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]+)", text)
-    if not m_b or not m_h or m_h.group(1) != kernel_source_hash():
+    if not m_b or not m_h or m_h.group(1) != kernel_source_hash(workload):
         return None
     return int(m_b.group(1))
 
@@ -205,6 +248,12 @@ def oracle_run(w: dict, inp, requests, threads: int):
     if w["kind"] == "ngram":
         return oracle.verify_ngram(inp.dtype, inp.target, inp.B, inp.K, inp.V, float(inp.temperature),
                                    inp.draft_tokens, inp.r, inp.u, threads=threads, requests=requests)
+    if w["kind"] == "walk":
+        T = float(w["T"])
+        return oracle.verify_tree_sample(inp.dtype, inp.target, inp.draft if T > 0 else None, inp.B,
+                                         inp.N, inp.V, T, inp.node_tokens, inp.parents,
+                                         inp.r if T > 0 else None, inp.u if T > 0 else None,
+                                         threads=threads, requests=requests)
     return oracle.verify_tree_greedy(inp.dtype, inp.target, inp.B, inp.N, inp.V, inp.node_tokens,
                                      inp.parents, threads=threads, requests=requests)
 
@@ -306,6 +355,16 @@ class DeviceCase:
             self.tokens, self.parents = tens(inp.node_tokens), tens(inp.parents)
             N1 = w["N"] + 1
             shapes = dict(accept_len=(B,), path_nodes=(B, N1), out_tokens=(B, N1), err_flags=(B,))
+        elif w["kind"] == "walk":
+            self.T = float(w["T"])
+            self.tokens, self.parents = tens(inp.node_tokens), tens(inp.parents)
+            stoch = self.T > 0
+            self.draft = tens(inp.draft, tdt) if stoch else None
+            self.r = tens(inp.r) if stoch else None
+            self.u = tens(inp.u) if stoch else None
+            N1 = w["N"] + 1
+            shapes = dict(accept_len=(B,), path_nodes=(B, N1), out_tokens=(B, N1), residual_mass=(B,),
+                          err_flags=(B,))
         else:
             self.draft = tens(inp.draft, tdt) if w["kind"] == "chain" else None
             self.x, self.r, self.u = tens(inp.draft_tokens), tens(inp.r), tens(inp.u)
@@ -322,6 +381,9 @@ class DeviceCase:
     def inputs(self):
         if self.w["kind"] == "tree":
             return [self.target, self.tokens, self.parents]
+        if self.w["kind"] == "walk":
+            return [t for t in (self.target, self.draft, self.tokens, self.parents, self.r, self.u)
+                    if t is not None]
         return [t for t in (self.target, self.draft, self.x, self.r, self.u) if t is not None]
 
     def abi_args(self):
@@ -335,9 +397,15 @@ class DeviceCase:
         ptr = lambda t: P(t.data_ptr()) if t is not None else None  # noqa: E731
         dt = self.binding.DTYPE_CODE[self.target.dtype]
         stream = P(torch.cuda.current_stream().cuda_stream)
-        ws, nbytes = ptr(self.ws), self.ws.numel()
         o = self.out
         B = self.w["B"]
+        if self.w["kind"] == "walk":
+            return ("spec_verify_tree_walk",
+                    (ptr(self.target), ptr(self.draft), dt, B, self.w["N"], self.w["V"], ctypes.c_float(self.T),
+                     ptr(self.tokens), ptr(self.parents), ptr(self.r), ptr(self.u), ptr(o["accept_len"]),
+                     ptr(o["path_nodes"]), ptr(o["out_tokens"]), ptr(o["residual_mass"]), ptr(o["err_flags"]),
+                     None, stream))
+        ws, nbytes = ptr(self.ws), self.ws.numel()
         if self.w["kind"] == "tree":
             return ("spec_verify_tree_greedy",
                     (ptr(self.target), dt, B, self.w["N"], self.w["V"], ptr(self.tokens), ptr(self.parents),
@@ -354,6 +422,9 @@ class DeviceCase:
 
     def call(self):
         b = self.binding
+        if self.w["kind"] == "walk":
+            return b.spec_verify_tree_walk(self.target, self.draft, self.tokens, self.parents, self.r, self.u,
+                                           self.T, out=self.out)
         if self.w["kind"] == "tree":
             return b.spec_verify_tree_greedy(self.target, self.tokens, self.parents, workspace=self.ws, out=self.out)
         if self.w["kind"] == "ngram":
@@ -384,7 +455,7 @@ def run_gpu(args, w) -> None:
     inputs = [make_inputs(args.workload, seed=s) for s in rank_seeds(rank, n_sets)]
     rows_req = rows_per_request(w)
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w["dtype"]]
-    ws = binding.make_workspace(w["B"], rows_req, w["V"], tdt, dev)
+    ws = None if w["kind"] == "walk" else binding.make_workspace(w["B"], rows_req, w["V"], tdt, dev)
     cases = [DeviceCase(w, inp, dev, ws) for inp in inputs]
     stream = torch.cuda.current_stream(dev)
 
@@ -399,10 +470,14 @@ def run_gpu(args, w) -> None:
     for c in cases:
         name, a = c.abi_args()
         abi.append((getattr(lib, name), a))
-    for fn, a in abi:
+    visited = []
+    for c, (fn, a) in zip(cases, abi):
         st = fn(*a)
         if st != binding.SPEC_OK:
             raise RuntimeError(f"C ABI call failed: {lib.spec_status_string(st).decode()}")
+        if w["kind"] == "walk":
+            torch.cuda.synchronize()
+            visited.append(walk_read_bytes(w, c))
     torch.cuda.synchronize()
 
     K = args.steps
@@ -447,7 +522,8 @@ def run_gpu(args, w) -> None:
     rows_step = w["B"] * rows_req
     value = job_rows_per_s(world, rows_step, K, elapsed_ms)
     alg_bytes = algorithmic_bytes(w)
-    achieved = alg_bytes / (mean_call_ms / 1e3) / 1e9
+    read_bytes = float(np.mean(visited)) if visited else float(alg_bytes)
+    achieved = read_bytes / (mean_call_ms / 1e3) / 1e9
     peak, peak_src = hbm_peak()
 
     # ---- end to end through the public API: pinned host -> device, call, results -> host ----
@@ -490,7 +566,7 @@ def run_gpu(args, w) -> None:
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
-                     "traffic": profiled_traffic(args.workload), "algorithmic_bytes_per_call": alg_bytes,
+                     "traffic": profiled_traffic(args.workload), "algorithmic_bytes_per_call": read_bytes,
                      "mean_call_us": mean_call_ms * 1e3,
                      "kernel": f"verify_kernel<{w['kind']},{w['dtype']}> (one launch per call)"},
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
@@ -498,6 +574,15 @@ def run_gpu(args, w) -> None:
         "gpu_launches": K * launches_per_step(w),
         "clocks": clk,
     }
+    if w["kind"] == "walk":
+        line["roofline"].update(
+            kernel=f"walk_kernel<{w['dtype']},32>, clusters of 8 CTAs (one launch per call)",
+            algorithmic_bytes_note="acceptance-aware: the rows the walk reads (visited nodes' target rows, and "
+                                   "draft rows of visited nodes with children), mean over the input sets",
+            all_rows_bytes_per_call=alg_bytes,
+            all_rows_equivalent_GBs=alg_bytes / (mean_call_ms / 1e3) / 1e9,
+            note="latency-bound: one row pair per tree level, read by one cluster per request; the "
+                 "all-rows figure is the bandwidth a pass over every row would need to match this time")
     if not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, inputs[0])
     print(json.dumps(line), flush=True)

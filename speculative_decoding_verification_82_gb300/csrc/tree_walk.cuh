@@ -109,28 +109,43 @@ __device__ __forceinline__ int exchange(Shared& sm, int& round, const uint32_t (
 }
 
 // ------------------------------------------------------------------- reductions ----
-// (m, Z) pairs of partial softmax normalisers, Z relative to 2^(m c); -inf m means empty.
-__device__ __forceinline__ float mz_weight(float m, float M, float c) {
-  return m == -INFINITY ? 0.f : ex2(__fsub_rn(__fmul_rn(m, c), __fmul_rn(M, c)));
-}
+// (m, Z) pairs of partial softmax normalisers, Z relative to 2^(round(m c)); -inf m means empty.
+// The pair with the smaller maximum is rescaled; the combination is commutative (equal maxima
+// add the two sums), so both lanes of a butterfly pair get the same result.
 __device__ __forceinline__ void mz_combine(float& m, float& z, float m2, float z2, float c) {
-  const float M = fmaxf(m, m2);
-  if (M == -INFINITY) return;
-  z = __fadd_rn(__fmul_rn(z, mz_weight(m, M, c)), __fmul_rn(z2, mz_weight(m2, M, c)));
-  m = M;
+  const bool first = m >= m2;
+  const float hi = first ? m : m2, lo = first ? m2 : m;
+  const float zhi = first ? z : z2, zlo = first ? z2 : z;
+  if (hi == -INFINITY || hi != hi) return;
+  z = lo == -INFINITY ? zhi : __fadd_rn(zhi, __fmul_rn(zlo, ex2(__fsub_rn(__fmul_rn(lo, c), __fmul_rn(hi, c)))));
+  m = hi;
 }
-__device__ __forceinline__ void warp_mz(float& m, float& z, float c) {
-#pragma unroll
-  for (int o = 16; o; o >>= 1) {
+__device__ __forceinline__ void warp_mz(float& m, float& z, float c, int width = 32) {
+  for (int o = width >> 1; o; o >>= 1) {
     const float m2 = __shfl_xor_sync(kFull, m, o), z2 = __shfl_xor_sync(kFull, z, o);
-    mz_combine(m, z, m2, z2, c);  // commutative: both lanes of a pair get the same pair
+    mz_combine(m, z, m2, z2, c);
+  }
+  if (width < 32) {  // lanes [0, width) hold the result: give it to every lane
+    m = __shfl_sync(kFull, m, 0);
+    z = __shfl_sync(kFull, z, 0);
   }
 }
+// Smallest power of two >= n (n <= 32).
+__device__ __forceinline__ int pow2_width(int n) { return n <= 1 ? 1 : 1 << (32 - __clz(n - 1)); }
+
 // (value, index) maxima, ties to the lower index; INT_MAX marks no element.
 __device__ __forceinline__ void vi_combine(float& v, int& i, float v2, int i2) {
   if (v2 > v || (v2 == v && i2 < i)) {
     v = v2;
     i = i2;
+  }
+}
+__device__ __forceinline__ void warp_vi(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    const float v2 = __shfl_xor_sync(kFull, v, o);
+    const int i2 = __shfl_xor_sync(kFull, i, o);
+    vi_combine(v, i, v2, i2);
   }
 }
 // Cluster-wide sum of one float per thread: warp butterfly, warps in order, CTAs in rank order.
@@ -140,15 +155,9 @@ __device__ __forceinline__ float cluster_sum(Shared& sm, int& round, float s, in
   if (lane == 0) sm.wa[warp] = s;
   __syncthreads();
   uint32_t w[kXWords] = {};
-  if ((int)threadIdx.x < cl) {
-    float a = 0.f;
-    for (int i = 0; i < kWarps; ++i) a = __fadd_rn(a, sm.wa[i]);
-    w[0] = __float_as_uint(a);
-  }
+  if (warp == 0) w[0] = __float_as_uint(warp_sum(lane < kWarps ? sm.wa[lane] : 0.f));
   const int slot = exchange(sm, round, w, cl, rank);
-  float tot = 0.f;
-  for (int r = 0; r < cl; ++r) tot = __fadd_rn(tot, __uint_as_float(sm.xbuf[slot][r][0]));
-  return tot;
+  return warp_sum(lane < cl ? __uint_as_float(sm.xbuf[slot][lane][0]) : 0.f);
 }
 // Block minimum of one int per thread (every thread gets it).
 __device__ __forceinline__ int block_min(Shared& sm, int v) {
@@ -163,6 +172,10 @@ __device__ __forceinline__ int block_min(Shared& sm, int v) {
 }
 
 // ------------------------------------------------------------------- row access ----
+// Bulk prefetch of `bytes` (a multiple of 16, from a 16-byte aligned address) into L2.
+__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
+  if (bytes) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
 template <typename T>
 __device__ __forceinline__ const char* row_of(const void* base, const Params& P, int b, int node) {
   return static_cast<const char*>(base) + ((size_t)b * P.N1 + node) * (size_t)P.V * Elem<T>::kSize;
@@ -269,12 +282,14 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
     const bool need_q = !greedy && nk > 0;
     const char* trow = row_of<T>(P.target, P, b, cur);
     const char* drow = need_q ? row_of<T>(P.draft, P, b, cur) : nullptr;
-    for (int i = t; i < nk; i += kThreads) {
-      const int node = sm.kid[i], x = sm.tok[node];
-      sm.klx[i] = load_elem<T>(trow, x);
-      if (need_q) {
-        sm.kdx[i] = load_elem<T>(drow, x);
-        sm.kr[i] = __ldg(P.r + (size_t)b * N1 + node);
+    if (nk > 0 && vec && t == 0) {
+      // the first child is the likeliest next node: its rows (this CTA's slice) into L2 now
+      const long long s0 = (long long)rank * kThreads * E;
+      const long long n = min((long long)kThreads * E, (long long)V - s0);
+      if (n > 0) {
+        const uint32_t bytes = (uint32_t)(n * Elem<T>::kSize) & ~15u;
+        l2_prefetch(row_of<T>(P.target, P, b, sm.kid[0]) + s0 * Elem<T>::kSize, bytes);
+        if (!greedy) l2_prefetch(row_of<T>(P.draft, P, b, sm.kid[0]) + s0 * Elem<T>::kSize, bytes);
       }
     }
     float p[E], q[E];
@@ -284,6 +299,15 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
     } else {
 #pragma unroll
       for (int k = 0; k < E; ++k) q[k] = 0.f;
+    }
+    // the children's logits at their tokens and their uniforms (after the row loads are issued)
+    for (int i = t; i < nk; i += kThreads) {
+      const int node = sm.kid[i], x = sm.tok[node];
+      sm.klx[i] = load_elem<T>(trow, x);
+      if (need_q) {
+        sm.kdx[i] = load_elem<T>(drow, x);
+        sm.kr[i] = __ldg(P.r + (size_t)b * N1 + node);
+      }
     }
 
     if (greedy) {
@@ -301,12 +325,7 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
           }
         }
       }
-#pragma unroll
-      for (int o = 16; o; o >>= 1) {
-        const float v2 = __shfl_xor_sync(kFull, bv, o);
-        const int i2 = __shfl_xor_sync(kFull, bi, o);
-        vi_combine(bv, bi, v2, i2);
-      }
+      warp_vi(bv, bi);
       nan = warp_or(nan);
       if (lane == 0) {
         sm.wa[warp] = bv;
@@ -315,24 +334,21 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
       }
       __syncthreads();
       uint32_t w[kXWords] = {};
-      if (t < cl) {
-        float v = -INFINITY;
-        int i = INT_MAX, f = 0;
-        for (int k = 0; k < kWarps; ++k) {
-          vi_combine(v, i, sm.wa[k], sm.wi[k]);
-          f |= sm.wj[k];
-        }
+      if (warp == 0) {
+        const bool in = lane < kWarps;
+        float v = in ? sm.wa[lane] : -INFINITY;
+        int i = in ? sm.wi[lane] : INT_MAX;
+        warp_vi(v, i);
         w[0] = __float_as_uint(v);
         w[1] = (uint32_t)i;
-        w[2] = (uint32_t)f;
+        w[2] = (uint32_t)warp_or(in ? sm.wj[lane] : 0);
       }
       const int slot = exchange(sm, round, w, cl, rank);
-      float v = -INFINITY;
-      int a = INT_MAX, f = 0;
-      for (int r = 0; r < cl; ++r) {
-        vi_combine(v, a, __uint_as_float(sm.xbuf[slot][r][0]), (int)sm.xbuf[slot][r][1]);
-        f |= (int)sm.xbuf[slot][r][2];
-      }
+      const bool in = lane < cl;
+      float v = in ? __uint_as_float(sm.xbuf[slot][lane][0]) : -INFINITY;
+      int a = in ? (int)sm.xbuf[slot][lane][1] : INT_MAX;
+      warp_vi(v, a);
+      const int f = warp_or(in ? (int)sm.xbuf[slot][lane][2] : 0);
       if (f) {
         err = SPEC_ERRF_NONFINITE;
         break;
@@ -364,15 +380,21 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
         md = fmaxf(md, q[k]);
       }
     }
-    if (mt != -INFINITY) {
-      const float mc = __fmul_rn(mt, c);
+    // e_k = 2^(l_k c - round(m c)) for the thread's own maximum m replaces the logit in place;
+    // p_k = e_k 2^(round(m c) - round(M c)) / Z once the row's M and Z are known
+    const float mtl = mt, mdl = md;
+    const float mcl_t = __fmul_rn(mtl, c), mcl_d = __fmul_rn(mdl, c);
 #pragma unroll
-      for (int k = 0; k < E; ++k) zt = __fadd_rn(zt, ex2(__fmaf_rn(p[k], c, -mc)));
+    for (int k = 0; k < E; ++k) {
+      p[k] = mtl == -INFINITY ? 0.f : ex2(__fmaf_rn(p[k], c, -mcl_t));
+      zt = __fadd_rn(zt, p[k]);
     }
-    if (need_q && md != -INFINITY) {
-      const float mc = __fmul_rn(md, c);
+    if (need_q) {
 #pragma unroll
-      for (int k = 0; k < E; ++k) zd = __fadd_rn(zd, ex2(__fmaf_rn(q[k], c, -mc)));
+      for (int k = 0; k < E; ++k) {
+        q[k] = mdl == -INFINITY ? 0.f : ex2(__fmaf_rn(q[k], c, -mcl_d));
+        zd = __fadd_rn(zd, q[k]);
+      }
     }
     warp_mz(mt, zt, c);
     warp_mz(md, zd, c);
@@ -386,32 +408,31 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
     }
     __syncthreads();
     {
+      // warp 0 combines the warp partials, then every warp the CTAs' (butterflies: identical
+      // values and order in every CTA)
       uint32_t w[kXWords] = {};
-      if (t < cl) {
-        float a = -INFINITY, za = 0.f, d = -INFINITY, zd2 = 0.f;
-        int f = 0;
-        for (int k = 0; k < kWarps; ++k) {
-          mz_combine(a, za, sm.wa[k], sm.wb[k], c);
-          mz_combine(d, zd2, sm.wc[k], sm.wd[k], c);
-          f |= sm.wi[k];
-        }
+      if (warp == 0) {
+        const bool in = lane < kWarps;
+        float a = in ? sm.wa[lane] : -INFINITY, za = in ? sm.wb[lane] : 0.f;
+        float d = in ? sm.wc[lane] : -INFINITY, zd2 = in ? sm.wd[lane] : 0.f;
+        warp_mz(a, za, c, kWarps);
+        warp_mz(d, zd2, c, kWarps);
         w[0] = __float_as_uint(a);
         w[1] = __float_as_uint(za);
         w[2] = __float_as_uint(d);
         w[3] = __float_as_uint(zd2);
-        w[4] = (uint32_t)f;
+        w[4] = (uint32_t)warp_or(in ? sm.wi[lane] : 0);
       }
       const int slot = exchange(sm, round, w, cl, rank);
-      mt = -INFINITY;
-      zt = 0.f;
-      md = -INFINITY;
-      zd = 0.f;
-      fl = 0;
-      for (int r = 0; r < cl; ++r) {
-        mz_combine(mt, zt, __uint_as_float(sm.xbuf[slot][r][0]), __uint_as_float(sm.xbuf[slot][r][1]), c);
-        mz_combine(md, zd, __uint_as_float(sm.xbuf[slot][r][2]), __uint_as_float(sm.xbuf[slot][r][3]), c);
-        fl |= (int)sm.xbuf[slot][r][4];
-      }
+      const bool in = lane < cl;
+      mt = in ? __uint_as_float(sm.xbuf[slot][lane][0]) : -INFINITY;
+      zt = in ? __uint_as_float(sm.xbuf[slot][lane][1]) : 0.f;
+      md = in ? __uint_as_float(sm.xbuf[slot][lane][2]) : -INFINITY;
+      zd = in ? __uint_as_float(sm.xbuf[slot][lane][3]) : 0.f;
+      const int wdt = pow2_width(cl);
+      warp_mz(mt, zt, c, wdt);
+      warp_mz(md, zd, c, wdt);
+      fl = warp_or(in ? (int)sm.xbuf[slot][lane][4] : 0);
     }
     if (fl || mt == -INFINITY || (need_q && md == -INFINITY)) {
       err = SPEC_ERRF_NONFINITE;
@@ -419,13 +440,18 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
     }
     const float mct = __fmul_rn(mt, c), mcd = __fmul_rn(md, c);
     {
-      const float it = __frcp_rn(zt);
+      // the thread's scale 2^(round(m c) - round(M c)) / Z, its exponent as an exact pair
+      Exp2 xt;
+      two_sum(mcl_t, -mct, xt.hi, xt.lo);
+      const float st = mtl == -INFINITY ? 0.f : exp2_times(xt, __frcp_rn(zt));
 #pragma unroll
-      for (int k = 0; k < E; ++k) p[k] = __fmul_rn(ex2(__fmaf_rn(p[k], c, -mct)), it);
+      for (int k = 0; k < E; ++k) p[k] = __fmul_rn(p[k], st);
       if (need_q) {
-        const float id = __frcp_rn(zd);
+        Exp2 xd;
+        two_sum(mcl_d, -mcd, xd.hi, xd.lo);
+        const float sd = mdl == -INFINITY ? 0.f : exp2_times(xd, __frcp_rn(zd));
 #pragma unroll
-        for (int k = 0; k < E; ++k) q[k] = __fmul_rn(ex2(__fmaf_rn(q[k], c, -mcd)), id);
+        for (int k = 0; k < E; ++k) q[k] = __fmul_rn(q[k], sd);
       }
     }
 
