@@ -44,6 +44,9 @@
  *   R11 invalid input: a draft token outside [0, V), a logits row holding NaN (or, when a softmax
  *       is taken, +inf, or only -inf), or a malformed parent array sets an error bit (every bit
  *       that applies, all rows checked); the request then accepts nothing and emits no token (-1).
+ *   R12 tree layout: node 0 is the root, parents[0] = -1, 0 <= parents[i] < i; row n of the
+ *       logits scores the children of node n.
+ *   R13-R15 the stochastic tree walk: see the section "stochastic tree verification" below.
  */
 #include <math.h>
 #include <stdint.h>
@@ -546,7 +549,7 @@ void oracle_verify_tree_greedy(int dtype, const void *target, int B, int N, int 
 
 /* ------------------------------------------------------------ stochastic tree verification ---- */
 /*
- * R12 (tree, T > 0): the step of section I.1 applied to every sibling in turn.  At a node, p is
+ * R13 (tree, T > 0): the step of section I.1 applied to every sibling in turn.  At a node, p is
  * the target distribution of the node's row and q the draft distribution of the node's draft row
  * (the distribution its children were drawn from; siblings are read as independent draws from
  * the same q).  Children are tested in ascending node index.  Child c with token x is accepted
@@ -556,12 +559,12 @@ void oracle_verify_tree_greedy(int dtype, const void *target, int B, int N, int 
  * and the next sibling is tested against the new p and the same q.  When no child is accepted,
  * or the node has none, the final token is drawn from the current p with the request's u (R4).
  * A chain (one child per node) is exactly the chain verification above.
- * R13: the mass R reported for a request is the product of the residual sums met at its final
+ * R14: the mass R reported for a request is the product of the residual sums met at its final
  * node (1 when nothing was rejected there).  The tie band of an accept test, and of the final
  * draw, at mass R is tol / R (the resolution of the residual in fp32, as in R10).  A residual sum
  * that is not positive stops the sibling tests; the draw is then taken from the node's own p
  * (R5, flagged).
- * R14: the walk reads only the rows of the nodes it visits (a node's draft row only when it has
+ * R15: the walk reads only the rows of the nodes it visits (a node's draft row only when it has
  * children); a non-finite value in another row is not seen.  T == 0 is the greedy walk of R9,
  * with alpha = 1 for the matching child and 0 for the siblings tested before it.
  */
@@ -646,7 +649,7 @@ static int tree_sample_walk(int N1, int V, tree_rows_fn rows, void *ctx, const i
         }
         double S2;
         int fl, tok;
-        if (empty) { /* R13 / R5: nothing left of the residual, draw from the node's own p */
+        if (empty) { /* R14 / R5: nothing left of the residual, draw from the node's own p */
             tok = oracle_inverse_cdf(p0, V, (double)u, tol, &S2, &fl);
             *req_flag |= ORF_ZERO_RESIDUAL;
         } else {
@@ -684,7 +687,7 @@ static int probs_rows(void *ctx, int node, int need_q, double *p, double *q)
 
 /* Stochastic tree verification on probability rows p, q: [N1][V] (row n of q = the draft
  * distribution of node n's children).  Outputs: *accept_len, path[N1], out_tokens[N1],
- * alpha[N1] (alpha of each tested child, -1 elsewhere), *mass (R13), *req_flag. */
+ * alpha[N1] (alpha of each tested child, -1 elsewhere), *mass (R14), *req_flag. */
 void oracle_tree_sample_probs(int N1, int V, const double *p, const double *q,
                               const int *parents, const int *tokens, const float *r, float u,
                               double tol, int *accept_len, int *path, int *out_tokens,
@@ -716,7 +719,7 @@ static int logits_rows(void *ctx, int node, int need_q, double *p, double *q)
     return e;
 }
 
-/* R14, T == 0: the greedy walk on the rows of the visited nodes only. */
+/* R15, T == 0: the greedy walk on the rows of the visited nodes only. */
 static int tree_greedy_visited(int dtype, const void *target, size_t row0, int N1, int V,
                                const int *parents, const int *tokens, int *accept_len, int *path,
                                int *out_tokens, double *alpha)
@@ -760,7 +763,7 @@ static int tree_greedy_visited(int dtype, const void *target, size_t row0, int N
 }
 
 /*
- * Tree verification by walking (R12-R14).  target, draft: [B][N+1][V] (draft ignored when
+ * Tree verification by walking (R13-R15).  target, draft: [B][N+1][V] (draft ignored when
  * T == 0); node_tokens, parents: [B][N+1]; r: [B][N+1]; u: [B].
  * Outputs: accept_len[B], path[B][N+1], out_tokens[B][N+1], alpha[B][N+1], mass[B],
  * req_flag[B], err[B].  Requests [b0, b1) only are processed.

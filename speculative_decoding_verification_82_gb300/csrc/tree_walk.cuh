@@ -172,10 +172,6 @@ __device__ __forceinline__ int block_min(Shared& sm, int v) {
 }
 
 // ------------------------------------------------------------------- row access ----
-// Bulk prefetch of `bytes` (a multiple of 16, from a 16-byte aligned address) into L2.
-__device__ __forceinline__ void l2_prefetch(const void* p, uint32_t bytes) {
-  if (bytes) asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
 template <typename T>
 __device__ __forceinline__ const char* row_of(const void* base, const Params& P, int b, int node) {
   return static_cast<const char*>(base) + ((size_t)b * P.N1 + node) * (size_t)P.V * Elem<T>::kSize;
@@ -282,16 +278,6 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
     const bool need_q = !greedy && nk > 0;
     const char* trow = row_of<T>(P.target, P, b, cur);
     const char* drow = need_q ? row_of<T>(P.draft, P, b, cur) : nullptr;
-    if (nk > 0 && vec && t == 0) {
-      // the first child is the likeliest next node: its rows (this CTA's slice) into L2 now
-      const long long s0 = (long long)rank * kThreads * E;
-      const long long n = min((long long)kThreads * E, (long long)V - s0);
-      if (n > 0) {
-        const uint32_t bytes = (uint32_t)(n * Elem<T>::kSize) & ~15u;
-        l2_prefetch(row_of<T>(P.target, P, b, sm.kid[0]) + s0 * Elem<T>::kSize, bytes);
-        if (!greedy) l2_prefetch(row_of<T>(P.draft, P, b, sm.kid[0]) + s0 * Elem<T>::kSize, bytes);
-      }
-    }
     float p[E], q[E];
     load_seg<T, E>(trow, first, V, vec, p);
     if (need_q) {
