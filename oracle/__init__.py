@@ -82,6 +82,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_verify_tree_sample.argtypes = [I, P, P, I, I, I, F, P, P, P, P, D, I, I,
                                               P, P, P, P, P, P, P]
     lib.oracle_verify_tree_sample.restype = None
+    lib.oracle_ngram_draft.argtypes = [P, I, I, I, I, P, P, P, P]
+    lib.oracle_ngram_draft.restype = None
+    lib.oracle_ngram_draft_batch.argtypes = [P, P, I, I, I, I, I, I, I, P, P, P, P, P]
+    lib.oracle_ngram_draft_batch.restype = None
     lib.oracle_load.argtypes = [P, I, c_size_t]
     lib.oracle_load.restype = D
     return lib
@@ -324,6 +328,35 @@ def verify_tree_sample(dtype: str, target, draft, B: int, N: int, V: int, T: flo
     else:
         _run_threaded(run, B, threads)
     del keep
+    return o
+
+
+def ngram_draft(ctx, K: int, n_max: int = 4, n_min: int = 1, lib=None) -> dict:
+    """Prompt lookup draft of one context (R16)."""
+    lib = lib or load()
+    c = _c(ctx, np.int32).reshape(-1)
+    d = np.zeros(max(K, 1), np.int32)
+    ln, mn, me = c_int(), c_int(), c_int()
+    lib.oracle_ngram_draft(_p(c), c.size, n_max, n_min, K, _p(d), ctypes.byref(ln), ctypes.byref(mn),
+                           ctypes.byref(me))
+    return dict(draft=d[:K], draft_len=ln.value, match_n=mn.value, match_end=me.value)
+
+
+def ngram_draft_batch(ctx, ctx_len, K: int, n_max: int = 4, n_min: int = 1, threads: int = 1,
+                      lib=None) -> dict:
+    """Prompt lookup drafts of B contexts ctx [B][Lmax] with lengths ctx_len [B]."""
+    lib = lib or load()
+    c, cl = _c(ctx, np.int32), _c(ctx_len, np.int32)
+    B, Lmax = c.shape
+    o = dict(draft=np.zeros((B, K), np.int32), draft_len=np.zeros(B, np.int32),
+             match_n=np.zeros(B, np.int32), match_end=np.zeros(B, np.int32), err=np.zeros(B, np.int32))
+
+    def run(b0, b1):
+        lib.oracle_ngram_draft_batch(_p(c), _p(cl), B, Lmax, n_max, n_min, K, b0, b1,
+                                     *(_p(o[k]) for k in ("draft", "draft_len", "match_n",
+                                                          "match_end", "err")))
+
+    _run_threaded(run, B, threads)
     return o
 
 

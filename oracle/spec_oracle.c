@@ -804,3 +804,65 @@ void oracle_verify_tree_sample(int dtype, const void *target, const void *draft,
     }
     free(l);
 }
+
+/* ------------------------------------------------------------- prompt n-gram lookup draft ---- */
+/*
+ * Prompt lookup drafting: "Accelerating Autoregressive LLM Inference 3x with Lossless
+ * Speculative Decoding and EAGLE Heads" (x078.com), opening section (a zero-VRAM prompt n-gram
+ * lookup proposes K = 5 candidate tokens) and its serving example (--num-speculative-tokens 5
+ * --ngram-prompt-lookup-max 4).
+ * R16: for n = n_max down to n_min, take the context's last n tokens; find their most recent
+ * earlier occurrence, i.e. the largest start i with i + n <= L - 1 and ctx[i + j] == ctx[L - n + j]
+ * for j < n (it may overlap the suffix itself); the first n that has one wins, and the draft is
+ * the tokens that follow it, ctx[i + n .. min(i + n + K, L)) (at least one, at most K).  No
+ * match for any n: an empty draft.  n_min = 1 (the pages give only the maximum).
+ * Outputs: draft[K] (then -1), *draft_len, *match_n (0 when empty), *match_end (i + n, or -1).
+ */
+void oracle_ngram_draft(const int *ctx, int L, int n_max, int n_min, int K, int *draft,
+                        int *draft_len, int *match_n, int *match_end)
+{
+    for (int k = 0; k < K; k++)
+        draft[k] = -1;
+    *draft_len = 0;
+    *match_n = 0;
+    *match_end = -1;
+    for (int n = n_max; n >= n_min && n >= 1; n--) {
+        for (int i = L - n - 1; i >= 0; i--) {
+            int same = 1;
+            for (int j = 0; j < n && same; j++)
+                if (ctx[i + j] != ctx[L - n + j])
+                    same = 0;
+            if (!same)
+                continue;
+            int e = i + n, m = 0;
+            for (int k = 0; k < K && e + k < L; k++) {
+                draft[k] = ctx[e + k];
+                m++;
+            }
+            *draft_len = m;
+            *match_n = n;
+            *match_end = e;
+            return;
+        }
+    }
+}
+
+/* Batched: ctx [B][Lmax] with lengths ctx_len[B] (a length outside [0, Lmax] gives an empty
+ * draft and err[b] = ORE_BAD_TOKEN); outputs draft [B][K], draft_len / match_n / match_end /
+ * err [B].  Requests [b0, b1). */
+void oracle_ngram_draft_batch(const int *ctx, const int *ctx_len, int B, int Lmax, int n_max,
+                              int n_min, int K, int b0, int b1, int *draft, int *draft_len,
+                              int *match_n, int *match_end, int *err)
+{
+    (void)B;
+    for (int b = b0; b < b1; b++) {
+        int L = ctx_len[b];
+        err[b] = 0;
+        if (L < 0 || L > Lmax) {
+            err[b] = ORE_BAD_TOKEN;
+            L = 0;
+        }
+        oracle_ngram_draft(ctx + (size_t)b * Lmax, L, n_max, n_min, K, draft + (size_t)b * K,
+                           draft_len + b, match_n + b, match_end + b);
+    }
+}

@@ -412,3 +412,19 @@ def tree_sample_tiny(seed: int = 0, trials: int = 100_000, V: int = 8, branching
                       meta={"t0": t0, "t1": t1, "t2": t2, "d0": d0, "d1": d1},
                       draft=draft, r=uniform_r(seed, (trials, N1)), u=uniform_u(seed, (trials,)),
                       temperature=np.float32(T))
+
+
+def ngram_contexts(seed: int = 0, B: int = 256, K: int = 5, V: int = 151936, prompt_len: int = 2048,
+                   ngram_n: int = 4) -> tuple[np.ndarray, np.ndarray]:
+    """The contexts behind the n-gram workload: per request, the prompt followed by the 4 prompt
+    tokens at the request's seeded start s (the generated text repeating a prompt 4-gram), so
+    that prompt lookup proposes prompt[s + 4 .. s + 4 + K), the workload's drafts.  Same streams
+    as `ngram`.  Returns ctx [B][prompt_len + ngram_n] int32 and the lengths [B]."""
+    prng = _rng(seed, _S_PROMPT)
+    prompt = prng.integers(0, V, size=prompt_len).astype(np.int32)
+    starts = prng.integers(0, prompt_len - ngram_n - K + 1, size=B)
+    ctx = np.empty((B, prompt_len + ngram_n), dtype=np.int32)
+    ctx[:, :prompt_len] = prompt
+    for b, s0 in enumerate(starts):
+        ctx[b, prompt_len:] = prompt[s0: s0 + ngram_n]
+    return ctx, np.full(B, prompt_len + ngram_n, dtype=np.int32)

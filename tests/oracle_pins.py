@@ -566,3 +566,63 @@ def pin_tree_sample_errors(lib):
 FAST_PINS += [pin_hand_tree_sample_cases, pin_tree_sample_chain_reduction,
               pin_tree_sample_residual_closed_form, pin_tree_sample_greedy_walk,
               pin_tree_sample_errors]
+
+
+# ------------------------------------------------------------- prompt lookup drafting ----
+def pin_hand_ngram_draft_cases(lib):
+    for case in _golden()["ngram_draft"]:
+        o = oracle.ngram_draft(np.asarray(case["ctx"], np.int32), case["K"], lib=lib)
+        assert list(o["draft"]) == case["draft"], (case["name"], o)
+        assert (o["draft_len"], o["match_n"], o["match_end"]) == (
+            case["draft_len"], case["match_n"], case["match_end"]), (case["name"], o)
+
+
+def _brute_ngram(ctx, K, n_max=4, n_min=1):
+    """Every (n, end) pair whose n tokens before `end` equal the context's last n tokens, the best
+    by (n, end); written independently of the oracle's loop order."""
+    L = len(ctx)
+    best = None
+    for e in range(1, L):
+        for n in range(n_min, n_max + 1):
+            if n <= e and list(ctx[e - n:e]) == list(ctx[L - n:L]):
+                if best is None or (n, e) > best:
+                    best = (n, e)
+    if best is None:
+        return [-1] * K, 0, 0, -1
+    n, e = best
+    d = list(ctx[e:e + K])
+    return d + [-1] * (K - len(d)), len(d), n, e
+
+
+def pin_ngram_draft_bruteforce(lib, n_cases=3000):
+    rng = np.random.default_rng(71)
+    for _ in range(n_cases):
+        L, Vs, K = int(rng.integers(0, 40)), int(rng.integers(1, 6)), int(rng.integers(1, 7))
+        ctx = rng.integers(0, Vs, L).astype(np.int32)
+        o = oracle.ngram_draft(ctx, K, lib=lib)
+        d, ln, n, e = _brute_ngram(ctx, K)
+        assert list(o["draft"]) == d and o["draft_len"] == ln, (ctx, K, o, d)
+        assert (o["match_n"], o["match_end"]) == (n, e), (ctx, o, n, e)
+
+
+def pin_ngram_draft_limits(lib):
+    """n_max / n_min bound the n tried; the batched form equals the single form; a bad length."""
+    ctx = np.array([1, 2, 3, 4, 0, 9, 1, 2, 3, 4], np.int32)
+    assert oracle.ngram_draft(ctx, 3, n_max=4, lib=lib)["match_n"] == 4
+    assert oracle.ngram_draft(ctx, 3, n_max=2, lib=lib)["match_n"] == 2
+    assert oracle.ngram_draft(ctx, 3, n_max=4, n_min=4, lib=lib)["match_end"] == 4
+    assert oracle.ngram_draft(np.array([1, 2, 1], np.int32), 3, n_min=2, lib=lib)["draft_len"] == 0
+    rng = np.random.default_rng(5)
+    ctxs = rng.integers(0, 4, (20, 30)).astype(np.int32)
+    lens = rng.integers(0, 31, 20).astype(np.int32)
+    lens[3] = 31  # longer than the array: invalid
+    bo = oracle.ngram_draft_batch(ctxs, lens, 4, lib=lib)
+    for b in range(20):
+        if b == 3:
+            assert bo["err"][b] == oracle.ERR_BAD_TOKEN and bo["draft_len"][b] == 0
+            continue
+        so = oracle.ngram_draft(ctxs[b, : lens[b]], 4, lib=lib)
+        assert list(bo["draft"][b]) == list(so["draft"]) and bo["match_end"][b] == so["match_end"]
+
+
+FAST_PINS += [pin_hand_ngram_draft_cases, pin_ngram_draft_bruteforce, pin_ngram_draft_limits]

@@ -56,6 +56,12 @@ MUTANTS = [
      "if ((double)r[c] < a) { /* step 2: accepted */"),
     ("tree_greedy_walk_final_token", "out_tokens[len] = a;\n            break;",
      "out_tokens[len] = tokens[cur];\n            break;"),
+    ("ngram_draft_earliest_occurrence", "for (int i = L - n - 1; i >= 0; i--) {",
+     "for (int i = 0; i <= L - n - 1; i++) {"),
+    ("ngram_draft_shortest_first", "for (int n = n_max; n >= n_min && n >= 1; n--) {",
+     "for (int n = (n_min > 1 ? n_min : 1); n <= n_max; n++) {"),
+    ("ngram_draft_no_overlap", "for (int i = L - n - 1; i >= 0; i--) {", "for (int i = L - 2 * n; i >= 0; i--) {"),
+    ("ngram_draft_shifted", "draft[k] = ctx[e + k];", "draft[k] = ctx[e + k - 1];"),
     ("bad_token_check_dropped", "if (xb[k] < 0 || xb[k] >= V)\n                e |= ORE_BAD_TOKEN;",
      "if (0)\n                e |= ORE_BAD_TOKEN;"),
 ]

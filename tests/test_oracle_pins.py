@@ -177,3 +177,14 @@ def test_chi2_detects_a_tree_walk_without_residual_update(lib, tmp_path):
                                   ti.parents, ti.r, ti.u, threads=8, lib=mlib)
     p0 = sp_softmax(ti.meta["t0"].astype(np.float64) / T)
     assert pins.chi2_pvalue(np.bincount(o["out_tokens"][:, 0], minlength=ti.V).astype(float), p0) < 1e-6
+
+
+def test_ngram_lookup_reproduces_the_workload_drafts(lib):
+    """The n-gram workload's drafts are the continuations of seeded prompt 4-grams; prompt lookup
+    on the matching contexts (prompt + that 4-gram) proposes exactly them (a 4-gram repeat in a
+    2048-token uniform prompt over 151936 tokens has probability below 1e-8)."""
+    ctx, lens = synth.ngram_contexts(seed=0)
+    o = oracle.ngram_draft_batch(ctx, lens, 5, threads=8, lib=lib)
+    ng = synth.ngram(seed=0, B=256, V=151936)
+    assert (o["match_n"] == 4).all() and (o["draft_len"] == 5).all()
+    assert np.array_equal(o["draft"], ng.draft_tokens)
