@@ -16,7 +16,7 @@ calls), against the measured HBM copy bandwidth; `cpu_baseline` = the CPU oracle
 cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W]
-                  [--workload chain_batched|tree_greedy|ngram|tree_sample|tree_walk_greedy]
+                  [--workload chain_batched|tree_greedy|ngram|tree_sample|tree_walk_greedy|ngram_pipeline]
   python bench.py --impl reference ...   (the CPU oracle as the reference arm)
 """
 
@@ -51,6 +51,10 @@ WORKLOADS = {
     "tree_sample": dict(kind="walk", B=16, N=60, V=128256, dtype="bf16", T=1.0,
                         desc="stochastic tree verify by walking: B=16, 61-node EAGLE-2-like tree, V=128256 "
                              "bf16 T=1.0, target + draft logits, children drawn from the draft"),
+    # prompt lookup drafting on the GPU feeding the n-gram verification (two launches a step)
+    "ngram_pipeline": dict(kind="ngram_pipe", B=256, K=5, V=151936, dtype="bf16", T=0.8, L=2052,
+                           desc="n-gram pipeline: GPU prompt lookup (n=4..1) over B=256 contexts of 2052 tokens, "
+                                "then n-gram verify K=5 V=151936 bf16 T=0.8"),
     "tree_walk_greedy": dict(kind="walk", B=16, N=60, V=128256, dtype="bf16", T=0.0,
                              desc="greedy tree verify by walking: B=16, 61-node EAGLE-2-like tree (depth 6), "
                                   "V=128256 bf16"),
@@ -79,6 +83,10 @@ def make_inputs(name: str, seed: int):
         return synth.tree_sample(seed=seed)
     if name == "tree_walk_greedy":
         return synth.tree_greedy(seed=seed)
+    if name == "ngram_pipeline":
+        ci = synth.ngram(seed=seed)
+        ci.meta["ctx"], ci.meta["ctx_len"] = synth.ngram_contexts(seed=seed)
+        return ci
     raise ValueError(name)
 
 
@@ -87,7 +95,7 @@ def rows_per_request(w: dict) -> int:
     rows that exist as the draft's output), 21 of the 61 nodes of the benchmark tree."""
     if w["kind"] == "chain":
         return 2 * w["K"] + 1
-    if w["kind"] == "ngram":
+    if w["kind"] in ("ngram", "ngram_pipe"):
         return w["K"] + 1
     if w["kind"] == "walk" and w["T"] > 0:
         from speculative_decoding_verification_82_gb300 import synth
@@ -104,9 +112,9 @@ def graph_calls(K: int) -> int:
 
 
 def launches_per_step(w: dict) -> int:
-    """Kernel launches of one call: verify_kernel, which also makes the residual pass of
-    draft-model chains."""
-    return 1
+    """Kernel launches of one step: verify_kernel (which also makes the residual pass of
+    draft-model chains) or walk_kernel; the n-gram pipeline adds the lookup kernel."""
+    return 2 if w["kind"] == "ngram_pipe" else 1
 
 
 def algorithmic_bytes(w: dict) -> int:
@@ -121,6 +129,9 @@ def algorithmic_bytes(w: dict) -> int:
         K = w["K"]
         small_in = B * K * 4 * 2 + B * 4
         out = B * 4 + B * (K + 1) * 4 + B * 4 + B * 4
+        if w["kind"] == "ngram_pipe":  # contexts and lengths read, drafts written (and read back)
+            small_in += B * w["L"] * 4 + B * 4 + B * K * 4
+            out += B * K * 4 + 4 * B * 4
     return logits + small_in + out
 
 
@@ -248,6 +259,13 @@ def oracle_run(w: dict, inp, requests, threads: int):
     if w["kind"] == "ngram":
         return oracle.verify_ngram(inp.dtype, inp.target, inp.B, inp.K, inp.V, float(inp.temperature),
                                    inp.draft_tokens, inp.r, inp.u, threads=threads, requests=requests)
+    if w["kind"] == "ngram_pipe":
+        b0, b1 = requests
+        d = oracle.ngram_draft_batch(inp.meta["ctx"][b0:b1], inp.meta["ctx_len"][b0:b1], inp.K)
+        x = inp.draft_tokens.copy()
+        x[b0:b1] = d["draft"]
+        return oracle.verify_ngram(inp.dtype, inp.target, inp.B, inp.K, inp.V, float(inp.temperature),
+                                   x, inp.r, inp.u, threads=threads, requests=requests)
     if w["kind"] == "walk":
         T = float(w["T"])
         return oracle.verify_tree_sample(inp.dtype, inp.target, inp.draft if T > 0 else None, inp.B,
@@ -368,6 +386,11 @@ class DeviceCase:
         else:
             self.draft = tens(inp.draft, tdt) if w["kind"] == "chain" else None
             self.x, self.r, self.u = tens(inp.draft_tokens), tens(inp.r), tens(inp.u)
+            if w["kind"] == "ngram_pipe":  # the drafts come from the lookup kernel every step
+                self.ctx, self.ctx_len = tens(inp.meta["ctx"]), tens(inp.meta["ctx_len"])
+                dshape = dict(draft_len=(B,), match_n=(B,), match_end=(B,), err_draft=(B,))
+                self.dout = {k: (torch.empty(v, dtype=torch.int32).pin_memory() if host_pinned
+                                 else torch.empty(v, dtype=torch.int32, device=dev)) for k, v in dshape.items()}
             self.T = float(inp.temperature)
             K1 = w["K"] + 1
             shapes = dict(num_accepted=(B,), out_tokens=(B, K1), residual_mass=(B,), err_flags=(B,))
@@ -384,6 +407,8 @@ class DeviceCase:
         if self.w["kind"] == "walk":
             return [t for t in (self.target, self.draft, self.tokens, self.parents, self.r, self.u)
                     if t is not None]
+        if self.w["kind"] == "ngram_pipe":
+            return [self.target, self.ctx, self.ctx_len, self.r, self.u]
         return [t for t in (self.target, self.draft, self.x, self.r, self.u) if t is not None]
 
     def abi_args(self):
@@ -400,25 +425,31 @@ class DeviceCase:
         o = self.out
         B = self.w["B"]
         if self.w["kind"] == "walk":
-            return ("spec_verify_tree_walk",
+            return [("spec_verify_tree_walk",
                     (ptr(self.target), ptr(self.draft), dt, B, self.w["N"], self.w["V"], ctypes.c_float(self.T),
                      ptr(self.tokens), ptr(self.parents), ptr(self.r), ptr(self.u), ptr(o["accept_len"]),
                      ptr(o["path_nodes"]), ptr(o["out_tokens"]), ptr(o["residual_mass"]), ptr(o["err_flags"]),
-                     None, stream))
+                     None, stream))]
         ws, nbytes = ptr(self.ws), self.ws.numel()
         if self.w["kind"] == "tree":
-            return ("spec_verify_tree_greedy",
-                    (ptr(self.target), dt, B, self.w["N"], self.w["V"], ptr(self.tokens), ptr(self.parents),
-                     ptr(o["accept_len"]), ptr(o["path_nodes"]), ptr(o["out_tokens"]), ptr(o["err_flags"]), None,
-                     ws, nbytes, stream))
+            return [("spec_verify_tree_greedy",
+                     (ptr(self.target), dt, B, self.w["N"], self.w["V"], ptr(self.tokens), ptr(self.parents),
+                      ptr(o["accept_len"]), ptr(o["path_nodes"]), ptr(o["out_tokens"]), ptr(o["err_flags"]), None,
+                      ws, nbytes, stream))]
         K, V = self.w["K"], self.w["V"]
         tail = (ptr(o["num_accepted"]), ptr(o["out_tokens"]), ptr(o["residual_mass"]), ptr(o["err_flags"]),
                 None, None, None, None)
+        verify = ("spec_verify_ngram", (ptr(self.target), dt, B, K, V, ctypes.c_float(self.T), ptr(self.x),
+                                        ptr(self.r), ptr(self.u), *tail, ws, nbytes, stream))
+        if self.w["kind"] == "ngram_pipe":
+            d = self.dout
+            return [("spec_ngram_draft", (ptr(self.ctx), ptr(self.ctx_len), B, self.ctx.shape[1], 4, 1, K,
+                                          ptr(self.x), ptr(d["draft_len"]), ptr(d["match_n"]), ptr(d["match_end"]),
+                                          ptr(d["err_draft"]), stream)), verify]
         if self.w["kind"] == "ngram":
-            return ("spec_verify_ngram", (ptr(self.target), dt, B, K, V, ctypes.c_float(self.T), ptr(self.x),
-                                          ptr(self.r), ptr(self.u), *tail, ws, nbytes, stream))
-        return ("spec_verify_chain", (ptr(self.target), ptr(self.draft), dt, B, K, V, ctypes.c_float(self.T),
-                                      ptr(self.x), ptr(self.r), ptr(self.u), *tail, None, ws, nbytes, stream))
+            return [verify]
+        return [("spec_verify_chain", (ptr(self.target), ptr(self.draft), dt, B, K, V, ctypes.c_float(self.T),
+                                       ptr(self.x), ptr(self.r), ptr(self.u), *tail, None, ws, nbytes, stream))]
 
     def call(self):
         b = self.binding
@@ -427,6 +458,13 @@ class DeviceCase:
                                            self.T, out=self.out)
         if self.w["kind"] == "tree":
             return b.spec_verify_tree_greedy(self.target, self.tokens, self.parents, workspace=self.ws, out=self.out)
+        if self.w["kind"] == "ngram_pipe":
+            d = b.spec_ngram_draft(self.ctx, self.ctx_len, self.w["K"],
+                                   out=dict(draft_tokens=self.x, draft_len=self.dout["draft_len"],
+                                            match_n=self.dout["match_n"], match_end=self.dout["match_end"],
+                                            err_flags=self.dout["err_draft"]))
+            return b.spec_verify_ngram(self.target, d["draft_tokens"], self.r, self.u, self.T, workspace=self.ws,
+                                       out=self.out)
         if self.w["kind"] == "ngram":
             return b.spec_verify_ngram(self.target, self.x, self.r, self.u, self.T, workspace=self.ws, out=self.out)
         return b.spec_verify_chain(self.target, self.draft, self.x, self.r, self.u, self.T, workspace=self.ws,
@@ -468,13 +506,13 @@ def run_gpu(args, w) -> None:
     lib = binding.library()
     abi = []
     for c in cases:
-        name, a = c.abi_args()
-        abi.append((getattr(lib, name), a))
+        abi.append([(getattr(lib, name), a) for name, a in c.abi_args()])
     visited = []
-    for c, (fn, a) in zip(cases, abi):
-        st = fn(*a)
-        if st != binding.SPEC_OK:
-            raise RuntimeError(f"C ABI call failed: {lib.spec_status_string(st).decode()}")
+    for c, calls in zip(cases, abi):
+        for fn, a in calls:
+            st = fn(*a)
+            if st != binding.SPEC_OK:
+                raise RuntimeError(f"C ABI call failed: {lib.spec_status_string(st).decode()}")
         if w["kind"] == "walk":
             torch.cuda.synchronize()
             visited.append(walk_read_bytes(w, c))
@@ -491,12 +529,11 @@ def run_gpu(args, w) -> None:
     with torch.cuda.graph(graph, stream=cap):
         gabi = []
         for c in cases:  # the calls' stream argument: the capturing stream
-            name, a = c.abi_args()
-            gabi.append((getattr(lib, name), a))
+            gabi.append([(getattr(lib, name), a) for name, a in c.abi_args()])
         status = 0
         for i in range(per_graph):
-            fn, a = gabi[i % n_sets]
-            status |= fn(*a)
+            for fn, a in gabi[i % n_sets]:
+                status |= fn(*a)
     if status != binding.SPEC_OK:
         raise RuntimeError("a captured C ABI call failed")
     graph.replay()  # one untimed replay
@@ -568,7 +605,9 @@ def run_gpu(args, w) -> None:
                      "frac": achieved / peak, "peak_source": peak_src,
                      "traffic": profiled_traffic(args.workload), "algorithmic_bytes_per_call": read_bytes,
                      "mean_call_us": mean_call_ms * 1e3,
-                     "kernel": f"verify_kernel<{w['kind']},{w['dtype']}> (one launch per call)"},
+                     "kernel": (f"verify_kernel<ngram,{w['dtype']}> after ngram_draft_kernel (two launches a step)"
+                                if w["kind"] == "ngram_pipe" else
+                                f"verify_kernel<{w['kind']},{w['dtype']}> (one launch per call)")},
         "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
         "gpu_launches": K * launches_per_step(w),

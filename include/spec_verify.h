@@ -80,6 +80,7 @@ typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1, SPEC_DTYPE_F16 = 2 } spe
 #define SPEC_MAX_TREE_NODES 4096 /* N + 1 for spec_verify_tree_greedy */
 #define SPEC_MAX_WALK_NODES 1024 /* N + 1 for spec_verify_tree_walk */
 #define SPEC_MAX_WALK_VOCAB 262144 /* V for spec_verify_tree_walk */
+#define SPEC_MAX_NGRAM 32          /* n_max for spec_ngram_draft */
 
 /* Bytes of workspace for a call on B requests with vocabulary V of `dtype`, where
  * rows_per_request is the number of logits rows the call reads per request:
@@ -219,6 +220,34 @@ spec_status_t spec_verify_tree_walk(const void *target_logits, const void *draft
                                     int32_t *path_nodes, int32_t *out_tokens,
                                     float *residual_mass, int32_t *err_flags,
                                     float *accept_prob, spec_stream_t stream);
+
+/*
+ * Prompt n-gram lookup drafting: the draft side of spec_verify_ngram, computed on the GPU.
+ * "Accelerating Autoregressive LLM Inference 3x with Lossless Speculative Decoding and EAGLE
+ * Heads" (x078.com), opening section: a zero-VRAM prompt n-gram lookup proposes K candidate
+ * tokens (its serving example uses K = 5 and --ngram-prompt-lookup-max 4).
+ *
+ * For n = n_max down to n_min, the last n tokens of the context are looked up in the context;
+ * their most recent earlier occurrence (the largest start i with i + n <= L - 1 whose n tokens
+ * equal them; it may overlap them) wins, and the draft is the tokens that follow it,
+ * context[i + n .. min(i + n + K, L)).  No match for any n gives an empty draft.
+ *
+ * context        [B][Lmax] int32 token ids (any values; only equality is used).
+ * context_len    [B] int32, L in [0, Lmax]; another value gives an empty draft and sets
+ *                SPEC_ERRF_BAD_TOKEN in err_flags.
+ * n_max, n_min   1 <= n_min <= n_max <= SPEC_MAX_NGRAM;  K in [1, SPEC_MAX_K].
+ * Outputs:
+ * draft_tokens   [B][K] int32: the draft, then -1.
+ * draft_len      [B] int32: its length (0..K).
+ * match_n        [B] int32 or NULL: the n that matched (0 for none).
+ * match_end      [B] int32 or NULL: i + n, where the draft starts in the context (-1 for none).
+ * err_flags      [B] int32 or NULL.
+ * One kernel launch (one CTA per context); the context is read once.  No workspace.
+ */
+spec_status_t spec_ngram_draft(const int32_t *context, const int32_t *context_len, int B,
+                               int Lmax, int n_max, int n_min, int K, int32_t *draft_tokens,
+                               int32_t *draft_len, int32_t *match_n, int32_t *match_end,
+                               int32_t *err_flags, spec_stream_t stream);
 
 /*
  * spec_verify_chain without a workspace argument, for callers that cannot allocate device memory

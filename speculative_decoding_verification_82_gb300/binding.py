@@ -18,11 +18,11 @@ from .build import LIB_PATH
 
 SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_CUDA, SPEC_ERR_WORKSPACE, SPEC_ERR_UNSUPPORTED = range(5)
 ERRF_BAD_TOKEN, ERRF_NONFINITE, ERRF_TIMEOUT, ERRF_BAD_TREE = 1, 2, 4, 8
-MAX_K, MAX_TREE_NODES, MAX_WALK_NODES, MAX_WALK_VOCAB = 256, 4096, 1024, 262144
+MAX_K, MAX_TREE_NODES, MAX_WALK_NODES, MAX_WALK_VOCAB, MAX_NGRAM = 256, 4096, 1024, 262144, 32
 DTYPE_CODE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 
 EXPORTED = ("spec_verify_workspace_bytes", "spec_verify_workspace_reset", "spec_verify_chain",
-            "spec_verify_ngram", "spec_verify_tree_greedy", "spec_verify_tree_walk",
+            "spec_verify_ngram", "spec_verify_tree_greedy", "spec_verify_tree_walk", "spec_ngram_draft",
             "spec_verify_chain_static", "spec_status_string")
 STATIC_WORKSPACE_BYTES = 4 << 20
 
@@ -55,6 +55,8 @@ def library(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_tree_greedy.restype = I
     lib.spec_verify_tree_walk.argtypes = [P, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P]
     lib.spec_verify_tree_walk.restype = I
+    lib.spec_ngram_draft.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, P]
+    lib.spec_ngram_draft.restype = I
     lib.spec_verify_chain_static.argtypes = [P, P, I, I, I, I, F, P, P, P, P, P, P, P, P]
     lib.spec_verify_chain_static.restype = I
     lib.spec_status_string.argtypes = [I]
@@ -242,3 +244,25 @@ def spec_verify_tree_walk(target_logits, draft_logits, node_tokens, parents, r, 
                                    _ptr(rm), _ptr(ef), _ptr(ap), _stream(dev))
     _check(st)
     return dict(accept_len=al, path_nodes=pn, out_tokens=ot, residual_mass=rm, err_flags=ef)
+
+
+def spec_ngram_draft(context, context_len, K: int, *, n_max: int = 4, n_min: int = 1, out=None) -> dict:
+    """Prompt n-gram lookup drafts of B contexts [B][Lmax] (int32) with lengths [B].  See
+    spec_verify.h."""
+    lib = library()
+    dev = context.device
+    if context.dim() != 2:
+        raise ValueError("context must be [B][Lmax]")
+    B, Lmax = context.shape
+    _need(context, "context", torch.int32, (B, Lmax), dev)
+    _need(context_len, "context_len", torch.int32, (B,), dev)
+    out = dict(out or {})
+    d = _out(out.get("draft_tokens"), "draft_tokens", torch.int32, (B, K), dev)
+    dl = _out(out.get("draft_len"), "draft_len", torch.int32, (B,), dev)
+    mn = _out(out.get("match_n"), "match_n", torch.int32, (B,), dev)
+    me = _out(out.get("match_end"), "match_end", torch.int32, (B,), dev)
+    ef = _out(out.get("err_flags"), "err_flags", torch.int32, (B,), dev)
+    st = lib.spec_ngram_draft(_ptr(context), _ptr(context_len), B, Lmax, n_max, n_min, K, _ptr(d),
+                              _ptr(dl), _ptr(mn), _ptr(me), _ptr(ef), _stream(dev))
+    _check(st)
+    return dict(draft_tokens=d, draft_len=dl, match_n=mn, match_end=me, err_flags=ef)

@@ -143,3 +143,25 @@ def test_tree_walk_validation(lib):
     assert call(d=0) == binding.SPEC_ERR_INVALID_ARG        # T > 0 needs draft logits
     assert call(r=0) == binding.SPEC_ERR_INVALID_ARG
     assert call(t=(1 << 20) + 1) == binding.SPEC_ERR_INVALID_ARG  # misaligned bf16
+
+
+def test_ngram_draft_validation(lib):
+    P = ctypes.c_void_p
+    f = lib.spec_ngram_draft
+    ok = dict(ctx=1 << 20, cl=2 << 20, B=4, Lmax=100, nmax=4, nmin=1, K=5, d=3 << 20, dl=4 << 20)
+
+    def call(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(P(a["ctx"]), P(a["cl"]), a["B"], a["Lmax"], a["nmax"], a["nmin"], a["K"], P(a["d"]),
+                 P(a["dl"]), None, None, None, None)
+
+    assert call(B=0) == binding.SPEC_OK
+    assert call(B=-1) == binding.SPEC_ERR_INVALID_ARG
+    assert call(K=0) == binding.SPEC_ERR_INVALID_ARG
+    assert call(nmin=0) == binding.SPEC_ERR_INVALID_ARG
+    assert call(nmin=5) == binding.SPEC_ERR_INVALID_ARG      # n_min > n_max
+    assert call(nmax=binding.MAX_NGRAM + 1) == binding.SPEC_ERR_UNSUPPORTED
+    assert call(K=binding.MAX_K + 1) == binding.SPEC_ERR_UNSUPPORTED
+    assert call(ctx=0) == binding.SPEC_ERR_INVALID_ARG
+    assert call(d=0) == binding.SPEC_ERR_INVALID_ARG
