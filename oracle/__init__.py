@@ -86,6 +86,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_ngram_draft.restype = None
     lib.oracle_ngram_draft_batch.argtypes = [P, P, I, I, I, I, I, I, I, P, P, P, P, P]
     lib.oracle_ngram_draft_batch.restype = None
+    lib.oracle_kv_compact.argtypes = [P, I, P, I, P]
+    lib.oracle_kv_compact.restype = None
+    lib.oracle_kv_compact_batch.argtypes = [P, I, ctypes.c_longlong, I, I, I, P, P, P, P, P]
+    lib.oracle_kv_compact_batch.restype = None
     lib.oracle_load.argtypes = [P, I, c_size_t]
     lib.oracle_load.restype = D
     return lib
@@ -358,6 +362,28 @@ def ngram_draft_batch(ctx, ctx_len, K: int, n_max: int = 4, n_min: int = 1, thre
 
     _run_threaded(run, B, threads)
     return o
+
+
+def kv_compact(cache, slots, accept_len: int, path, lib=None) -> np.ndarray:
+    """One request, one cache [num_slots][row_bytes] (uint8): returns the compacted copy (R17)."""
+    lib = lib or load()
+    out = np.array(cache, dtype=np.uint8, copy=True, order="C")
+    sl, pt = _c(slots, np.int32), _c(path, np.int32)
+    lib.oracle_kv_compact(_p(out), out.shape[1], _p(sl), int(accept_len), _p(pt))
+    return out
+
+
+def kv_compact_batch(caches, slots, parents, accept_len, path, lib=None) -> tuple[np.ndarray, np.ndarray]:
+    """caches [C][num_slots][row_bytes] uint8 (copied), slots / parents / path [B][N1],
+    accept_len [B]: the compacted caches and the per-request error bits."""
+    lib = lib or load()
+    out = np.array(caches, dtype=np.uint8, copy=True, order="C")
+    C, S, W = out.shape
+    sl, pa, pt, al = (_c(a, np.int32) for a in (slots, parents, path, accept_len))
+    B, N1 = sl.shape
+    err = np.zeros(B, np.int32)
+    lib.oracle_kv_compact_batch(_p(out), C, S, W, B, N1, _p(sl), _p(pa), _p(al), _p(pt), _p(err))
+    return out, err
 
 
 def load_elems(storage: np.ndarray, dtype: str, lib=None) -> np.ndarray:

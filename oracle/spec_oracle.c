@@ -866,3 +866,54 @@ void oracle_ngram_draft_batch(const int *ctx, const int *ctx_len, int B, int Lma
                            draft_len + b, match_n + b, match_end + b);
     }
 }
+
+/* ------------------------------------------------------------- accepted-path KV compaction ---- */
+/*
+ * "Speculative Decoding with Medusa, EAGLE and vLLM" (vikram-blog.pages.dev), "System Topology &
+ * Data Flow" diagram: after the tree is verified, the accepted branch's tokens are committed to
+ * the KV cache.
+ * R17: the target's forward pass wrote the KV row of tree node n into slot slots[n] of a cache of
+ * rows (row_bytes each).  With the accepted path p_0 = 0, p_1, ..., p_L (path[0..L]), the row of
+ * p_j moves to the slot of position j: new[slots[j]] = old[slots[p_j]] for j = 1..L; every other
+ * slot keeps its row.  (Position j's slot is that of node j in the tree's numbering, so the
+ * accepted tokens end up in the first L + 1 slots, in order.)
+ */
+void oracle_kv_compact(unsigned char *cache, int row_bytes, const int *slots, int L,
+                       const int *path)
+{
+    if (L <= 0)
+        return;
+    unsigned char *tmp = (unsigned char *)malloc((size_t)L * (size_t)row_bytes);
+    for (int j = 1; j <= L; j++) /* read every accepted row before any slot is written */
+        memcpy(tmp + (size_t)(j - 1) * row_bytes, cache + (size_t)slots[path[j]] * row_bytes,
+               (size_t)row_bytes);
+    for (int j = 1; j <= L; j++)
+        memcpy(cache + (size_t)slots[j] * row_bytes, tmp + (size_t)(j - 1) * row_bytes,
+               (size_t)row_bytes);
+    free(tmp);
+}
+
+/* Batched over requests and caches: caches [C][num_slots][row_bytes] (C caches, e.g. the K and V
+ * tensors of every layer), slots [B][N1], accept_len [B], path [B][N1].  A request whose path is
+ * not a valid accepted path (L outside [0, N1), path[0] != 0, a node not a child of the previous
+ * one, a slot outside [0, num_slots)) is left untouched and err[b] = ORE_BAD_TREE. */
+void oracle_kv_compact_batch(unsigned char *caches, int C, long long num_slots, int row_bytes,
+                             int B, int N1, const int *slots, const int *parents,
+                             const int *accept_len, const int *path, int *err)
+{
+    for (int b = 0; b < B; b++) {
+        const int *sl = slots + (size_t)b * N1, *pa = parents + (size_t)b * N1;
+        const int *pt = path + (size_t)b * N1;
+        int L = accept_len[b], ok = L >= 0 && L < N1 && pt[0] == 0;
+        for (int j = 1; ok && j <= L; j++)
+            ok = pt[j] > 0 && pt[j] < N1 && pa[pt[j]] == pt[j - 1];
+        for (int n = 0; ok && n < N1; n++)
+            ok = sl[n] >= 0 && sl[n] < num_slots;
+        err[b] = ok ? 0 : ORE_BAD_TREE;
+        if (!ok)
+            continue;
+        for (int c = 0; c < C; c++)
+            oracle_kv_compact(caches + (size_t)c * (size_t)num_slots * (size_t)row_bytes, row_bytes,
+                              sl, L, pt);
+    }
+}

@@ -626,3 +626,61 @@ def pin_ngram_draft_limits(lib):
 
 
 FAST_PINS += [pin_hand_ngram_draft_cases, pin_ngram_draft_bruteforce, pin_ngram_draft_limits]
+
+
+# ---------------------------------------------------------- accepted-path KV compaction ----
+def pin_hand_kv_compact_cases(lib):
+    for case in _golden()["kv_compact"]:
+        W, S = case["row_bytes"], len(case["slots"])
+        cache = np.arange(S * W, dtype=np.uint8).reshape(S, W)
+        out = oracle.kv_compact(cache, case["slots"], case["accept_len"], case["path"], lib=lib)
+        assert out.tolist() == case["expected_rows"], (case["name"], out)
+        ob, err = oracle.kv_compact_batch(cache[None], np.array([case["slots"]]), np.array([case["parents"]]),
+                                          np.array([case["accept_len"]]), np.array([case["path"]]), lib=lib)
+        assert err[0] == 0 and ob[0].tolist() == case["expected_rows"], case["name"]
+
+
+def pin_kv_compact_sequential_moves(lib, n_cases=300):
+    """Moving rows one at a time in increasing position, in place, gives the same cache: along an
+    accepted path p_j >= j, so no move overwrites a row a later move still reads."""
+    rng = np.random.default_rng(83)
+    for _ in range(n_cases):
+        N1, W = int(rng.integers(1, 30)), int(rng.integers(1, 9))
+        parents, _tok = random_tree(rng, N1, 50)
+        v = int(rng.integers(0, N1))
+        path = [v]
+        while path[-1] != 0:
+            path.append(int(parents[path[-1]]))
+        path = path[::-1]
+        L = len(path) - 1
+        slots = rng.permutation(N1 + 5)[:N1].astype(np.int32)
+        cache = rng.integers(0, 256, (N1 + 5, W)).astype(np.uint8)
+        pp = np.full(N1, -1, np.int32)
+        pp[: L + 1] = path
+        out = oracle.kv_compact(cache, slots, L, pp, lib=lib)
+        seq = cache.copy()
+        for j in range(1, L + 1):
+            assert path[j] >= j
+            seq[slots[j]] = seq[slots[path[j]]]
+        assert np.array_equal(out, seq)
+        moved = set(int(slots[j]) for j in range(1, L + 1))
+        for srow in range(N1 + 5):
+            if srow not in moved:
+                assert np.array_equal(out[srow], cache[srow])
+
+
+def pin_kv_compact_validation(lib):
+    """A path that is not parent-linked, a length out of range or a slot out of range leaves the
+    request untouched and flags it; the other requests of the batch are compacted."""
+    parents = np.array([[-1, 0, 1, 1]] * 4, np.int32)
+    slots = np.array([[0, 1, 2, 3], [4, 5, 6, 7], [8, 9, 10, 11], [12, 13, 14, 99]], np.int32)
+    path = np.array([[0, 1, 3, -1], [0, 2, -1, -1], [0, 1, 3, -1], [0, 1, -1, -1]], np.int32)
+    al = np.array([2, 1, 4, 1], np.int32)
+    caches = np.arange(2 * 16 * 3, dtype=np.uint8).reshape(2, 16, 3)
+    out, err = oracle.kv_compact_batch(caches, slots, parents, al, path, lib=lib)
+    assert list(err) == [0, oracle.ERR_BAD_TREE, oracle.ERR_BAD_TREE, oracle.ERR_BAD_TREE]
+    assert np.array_equal(out[:, 4:], caches[:, 4:])
+    assert np.array_equal(out[:, 2], caches[:, 3]) and np.array_equal(out[:, 1], caches[:, 1])
+
+
+FAST_PINS += [pin_hand_kv_compact_cases, pin_kv_compact_sequential_moves, pin_kv_compact_validation]

@@ -62,6 +62,12 @@ MUTANTS = [
      "for (int n = (n_min > 1 ? n_min : 1); n <= n_max; n++) {"),
     ("ngram_draft_no_overlap", "for (int i = L - n - 1; i >= 0; i--) {", "for (int i = L - 2 * n; i >= 0; i--) {"),
     ("ngram_draft_shifted", "draft[k] = ctx[e + k];", "draft[k] = ctx[e + k - 1];"),
+    ("kv_compact_wrong_destination",
+     "memcpy(cache + (size_t)slots[j] * row_bytes, tmp + (size_t)(j - 1) * row_bytes,",
+     "memcpy(cache + (size_t)slots[path[j]] * row_bytes, tmp + (size_t)(j - 1) * row_bytes,"),
+    ("kv_compact_last_row_dropped", "for (int j = 1; j <= L; j++) /* read every accepted row before any slot is written */",
+     "for (int j = 1; j < L; j++) /* read every accepted row before any slot is written */"),
+    ("kv_compact_path_check_dropped", "ok = pt[j] > 0 && pt[j] < N1 && pa[pt[j]] == pt[j - 1];", "ok = 1;"),
     ("bad_token_check_dropped", "if (xb[k] < 0 || xb[k] >= V)\n                e |= ORE_BAD_TOKEN;",
      "if (0)\n                e |= ORE_BAD_TOKEN;"),
 ]
