@@ -16,7 +16,8 @@ calls), against the measured HBM copy bandwidth; `cpu_baseline` = the CPU oracle
 cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W]
-                  [--workload chain_batched|tree_greedy|ngram|tree_sample|tree_walk_greedy|ngram_pipeline]
+                  [--workload chain_batched|tree_greedy|ngram|tree_sample|tree_walk_greedy|ngram_pipeline|
+                              kv_compact]
   python bench.py --impl reference ...   (the CPU oracle as the reference arm)
 """
 
@@ -55,6 +56,10 @@ WORKLOADS = {
     "ngram_pipeline": dict(kind="ngram_pipe", B=256, K=5, V=151936, dtype="bf16", T=0.8, L=2052,
                            desc="n-gram pipeline: GPU prompt lookup (n=4..1) over B=256 contexts of 2052 tokens, "
                                 "then n-gram verify K=5 V=151936 bf16 T=0.8"),
+    # accepted-path KV-cache compaction after tree verification (Llama-3.3-70B cache geometry)
+    "kv_compact": dict(kind="kv", B=16, N=60, V=0, C=160, W=2048, dtype="u8",
+                       desc="accepted-path KV compaction: B=16, 61-node tree, deepest accepted paths (6 tokens), "
+                            "160 K/V caches (80 layers x 8 KV heads x 128 bf16) of 2048-byte rows"),
     "tree_walk_greedy": dict(kind="walk", B=16, N=60, V=128256, dtype="bf16", T=0.0,
                              desc="greedy tree verify by walking: B=16, 61-node EAGLE-2-like tree (depth 6), "
                                   "V=128256 bf16"),
@@ -64,6 +69,7 @@ KERNEL_SOURCES = ["speculative_decoding_verification_82_gb300/csrc/verify_kernel
                   "speculative_decoding_verification_82_gb300/csrc/verify_common.cuh",
                   "speculative_decoding_verification_82_gb300/csrc/fastdiv.h",
                   "speculative_decoding_verification_82_gb300/csrc/spec_verify_api.cu"]
+KV_SOURCES = ["speculative_decoding_verification_82_gb300/csrc/kv_compact.cu"]
 WALK_SOURCES = ["speculative_decoding_verification_82_gb300/csrc/tree_walk.cuh",
                 "speculative_decoding_verification_82_gb300/csrc/verify_common.cuh",
                 "speculative_decoding_verification_82_gb300/csrc/spec_walk.cu"]
@@ -83,6 +89,8 @@ def make_inputs(name: str, seed: int):
         return synth.tree_sample(seed=seed)
     if name == "tree_walk_greedy":
         return synth.tree_greedy(seed=seed)
+    if name == "kv_compact":
+        return synth.kv_compact_case(seed=seed)
     if name == "ngram_pipeline":
         ci = synth.ngram(seed=seed)
         ci.meta["ctx"], ci.meta["ctx_len"] = synth.ngram_contexts(seed=seed)
@@ -97,12 +105,23 @@ def rows_per_request(w: dict) -> int:
         return 2 * w["K"] + 1
     if w["kind"] in ("ngram", "ngram_pipe"):
         return w["K"] + 1
+    if w["kind"] == "kv":
+        return w["C"] * w["moves"]  # rows moved per request (set from the inputs by kv_moves)
     if w["kind"] == "walk" and w["T"] > 0:
         from speculative_decoding_verification_82_gb300 import synth
 
         par = synth.eagle_tree_parents()
         return par.size + int(np.unique(par[1:]).size)
     return w["N"] + 1
+
+
+def kv_moves(inp) -> float:
+    """Mean number of rows a request's compaction moves in one cache: accepted positions j whose
+    node is not already in position j's slot (those are skipped).  Along the benchmark tree's
+    deepest paths the first accepted node is node 1, so 5 of the 6 accepted rows move."""
+    sl, pt, al = inp["slots"], inp["path"], inp["accept_len"]
+    n = [sum(int(sl[b, pt[b, j]] != sl[b, j]) for j in range(1, al[b] + 1)) for b in range(len(al))]
+    return float(np.mean(n))
 
 
 def graph_calls(K: int) -> int:
@@ -120,6 +139,8 @@ def launches_per_step(w: dict) -> int:
 def algorithmic_bytes(w: dict) -> int:
     """Logits read once, the small inputs read once, the outputs written once."""
     B, V = w["B"], w["V"]
+    if w["kind"] == "kv":  # every moved row read once and written once, plus the path arrays
+        return 2 * B * rows_per_request(w) * w["W"] + 4 * B * (w["N"] + 1) * 4 + B * 4
     es = 4 if w["dtype"] == "f32" else 2
     logits = B * rows_per_request(w) * V * es
     if w["kind"] in ("tree", "walk"):
@@ -228,7 +249,8 @@ def hbm_peak() -> tuple[float, str]:
 
 def kernel_source_hash(workload: str = "chain_batched") -> str:
     h = hashlib.sha256()
-    for rel in (WALK_SOURCES if WORKLOADS[workload]["kind"] == "walk" else KERNEL_SOURCES):
+    kind = WORKLOADS[workload]["kind"]
+    for rel in (WALK_SOURCES if kind == "walk" else KV_SOURCES if kind == "kv" else KERNEL_SOURCES):
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
@@ -259,6 +281,10 @@ def oracle_run(w: dict, inp, requests, threads: int):
     if w["kind"] == "ngram":
         return oracle.verify_ngram(inp.dtype, inp.target, inp.B, inp.K, inp.V, float(inp.temperature),
                                    inp.draft_tokens, inp.r, inp.u, threads=threads, requests=requests)
+    if w["kind"] == "kv":
+        b0, b1 = requests
+        return oracle.kv_compact_batch(inp["caches"][:8], inp["slots"][b0:b1], inp["parents"][b0:b1],
+                                       inp["accept_len"][b0:b1], inp["path"][b0:b1])
     if w["kind"] == "ngram_pipe":
         b0, b1 = requests
         d = oracle.ngram_draft_batch(inp.meta["ctx"][b0:b1], inp.meta["ctx_len"][b0:b1], inp.K)
@@ -300,6 +326,8 @@ def cpu_baseline(w: dict, inp, min_wall: float = 1.0) -> dict:
         wall += oracle_timed(w, inp, n_req, threads)
         reps += 1
     rows = reps * n_req * rows_per_request(w)
+    if w["kind"] == "kv":
+        rows = rows * 8 // w["C"]  # the oracle sample moves rows of 8 of the caches
     return {"value": rows / wall, "unit": "rows/s", "cores": threads, "kind": "oracle",
             "sample": f"all {n_req} requests of the workload ({n_req * rows_per_request(w)} rows), "
                       f"{reps} repetitions, requests split over {threads} threads, {wall:.2f} s wall"}
@@ -359,17 +387,27 @@ class DeviceCase:
         from speculative_decoding_verification_82_gb300 import binding
 
         self.w, self.binding = w, binding
-        tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w["dtype"]]
+        tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "u8": torch.uint8}[w["dtype"]]
 
         def tens(a, dt=None):
             a = np.ascontiguousarray(a)
             t = torch.from_numpy(a.view(np.int16)).view(torch.bfloat16) if dt == torch.bfloat16 else torch.from_numpy(a)
             return t.pin_memory() if host_pinned else t.to(dev)
 
-        self.target = tens(inp.target, tdt)
         B = w["B"]
         self.draft = None
-        if w["kind"] == "tree":
+        if w["kind"] == "kv":
+            self.cache_all = tens(inp["caches"])
+            self.caches = [self.cache_all[i] for i in range(w["C"])]
+            self.slots, self.parents = tens(inp["slots"]), tens(inp["parents"])
+            self.al, self.path = tens(inp["accept_len"]), tens(inp["path"])
+            self.target = self.cache_all
+            shapes = dict(err_flags=(B,))
+        else:
+            self.target = tens(inp.target, tdt)
+        if w["kind"] == "kv":
+            pass  # set above
+        elif w["kind"] == "tree":
             self.tokens, self.parents = tens(inp.node_tokens), tens(inp.parents)
             N1 = w["N"] + 1
             shapes = dict(accept_len=(B,), path_nodes=(B, N1), out_tokens=(B, N1), err_flags=(B,))
@@ -404,6 +442,8 @@ class DeviceCase:
     def inputs(self):
         if self.w["kind"] == "tree":
             return [self.target, self.tokens, self.parents]
+        if self.w["kind"] == "kv":
+            return [self.cache_all, self.slots, self.parents, self.al, self.path]
         if self.w["kind"] == "walk":
             return [t for t in (self.target, self.draft, self.tokens, self.parents, self.r, self.u)
                     if t is not None]
@@ -420,6 +460,12 @@ class DeviceCase:
 
         P = ctypes.c_void_p
         ptr = lambda t: P(t.data_ptr()) if t is not None else None  # noqa: E731
+        if self.w["kind"] == "kv":
+            stream = P(torch.cuda.current_stream().cuda_stream)
+            self._arr = (P * len(self.caches))(*[c.data_ptr() for c in self.caches])
+            return [("spec_kv_compact", (self._arr, len(self.caches), self.caches[0].shape[0], self.w["W"],
+                                         self.w["B"], self.w["N"], ptr(self.slots), ptr(self.parents),
+                                         ptr(self.al), ptr(self.path), ptr(self.out["err_flags"]), stream))]
         dt = self.binding.DTYPE_CODE[self.target.dtype]
         stream = P(torch.cuda.current_stream().cuda_stream)
         o = self.out
@@ -453,6 +499,9 @@ class DeviceCase:
 
     def call(self):
         b = self.binding
+        if self.w["kind"] == "kv":
+            return {"err_flags": b.spec_kv_compact(self.caches, self.slots, self.parents, self.al, self.path,
+                                                   err_flags=self.out["err_flags"])}
         if self.w["kind"] == "walk":
             return b.spec_verify_tree_walk(self.target, self.draft, self.tokens, self.parents, self.r, self.u,
                                            self.T, out=self.out)
@@ -489,11 +538,15 @@ def run_gpu(args, w) -> None:
     dev = torch.device("cuda", local)
     binding.library()  # fail loudly if the CUDA library is missing
 
-    n_sets = 2  # alternate two input sets; each is larger than L2 as well
+    # alternate input sets; each is larger than L2 as well, except the KV compaction's 63 MB of moved
+    # rows per step, which takes four sets (252 MB touched per round, about twice L2)
+    n_sets = 4 if w["kind"] == "kv" else 2
     inputs = [make_inputs(args.workload, seed=s) for s in rank_seeds(rank, n_sets)]
+    if w["kind"] == "kv":
+        w["moves"] = float(np.mean([kv_moves(inp) for inp in inputs]))
     rows_req = rows_per_request(w)
-    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[w["dtype"]]
-    ws = None if w["kind"] == "walk" else binding.make_workspace(w["B"], rows_req, w["V"], tdt, dev)
+    tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "u8": torch.uint8}[w["dtype"]]
+    ws = None if w["kind"] in ("walk", "kv") else binding.make_workspace(w["B"], rows_req, w["V"], tdt, dev)
     cases = [DeviceCase(w, inp, dev, ws) for inp in inputs]
     stream = torch.cuda.current_stream(dev)
 
@@ -599,7 +652,8 @@ def run_gpu(args, w) -> None:
         "config": {"workload": w["desc"], "B": w["B"], "V": w["V"],
                    **({"K": w["K"]} if "K" in w else {"N": w["N"]}),
                    "rows_per_step": rows_step, "requests_per_s": value / rows_req,
-                   "l2": f"inputs {alg_bytes / 2**20:.0f} MiB per step > 129 MiB L2; {n_sets} input sets alternated",
+                   "l2": f"{alg_bytes / 2**20:.0f} MiB touched per step, {n_sets} input sets alternated "
+                         f"({n_sets * alg_bytes / 2**20:.0f} MiB per round; L2 129 MiB)",
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
@@ -613,6 +667,11 @@ def run_gpu(args, w) -> None:
         "gpu_launches": K * launches_per_step(w),
         "clocks": clk,
     }
+    if w["kind"] == "kv":
+        line["metric"] = "KV-cache rows compacted per second (a row: one token's K or V in one layer) and achieved HBM GB/s"
+        line["roofline"]["kernel"] = "kv_compact_kernel (one launch per call)"
+        line["config"]["rows"] = (f"moved rows ({w['moves']:g} per request and cache: accepted positions whose node is "
+                                  f"not already in place) x 2048 bytes, read and written once")
     if w["kind"] == "walk":
         line["roofline"].update(
             kernel=f"walk_kernel<{w['dtype']},32>, clusters of 8 CTAs (one launch per call)",
@@ -633,6 +692,8 @@ def run_reference(args, w) -> None:
     if int(os.environ.get("RANK", "0")) != 0:
         return
     inp = make_inputs(args.workload, seed=0)
+    if w["kind"] == "kv":
+        w["moves"] = kv_moves(inp)
     cores = os.cpu_count() or 1
     t_one = oracle_timed(w, inp, 1, 1)
     budget = 150.0 / max(1, args.steps + args.warmup)  # keep the whole run within a few minutes

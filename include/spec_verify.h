@@ -81,6 +81,7 @@ typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1, SPEC_DTYPE_F16 = 2 } spe
 #define SPEC_MAX_WALK_NODES 1024 /* N + 1 for spec_verify_tree_walk */
 #define SPEC_MAX_WALK_VOCAB 262144 /* V for spec_verify_tree_walk */
 #define SPEC_MAX_NGRAM 32          /* n_max for spec_ngram_draft */
+#define SPEC_MAX_KV_CACHES 1024    /* caches (layers x K/V) per spec_kv_compact call */
 
 /* Bytes of workspace for a call on B requests with vocabulary V of `dtype`, where
  * rows_per_request is the number of logits rows the call reads per request:
@@ -248,6 +249,35 @@ spec_status_t spec_ngram_draft(const int32_t *context, const int32_t *context_le
                                int Lmax, int n_max, int n_min, int K, int32_t *draft_tokens,
                                int32_t *draft_len, int32_t *match_n, int32_t *match_end,
                                int32_t *err_flags, spec_stream_t stream);
+
+/*
+ * Accepted-path KV-cache compaction after tree verification: "Speculative Decoding with Medusa,
+ * EAGLE and vLLM" (vikram-blog.pages.dev), "System Topology & Data Flow" diagram (the accepted
+ * branch's tokens are committed to the KV cache).
+ *
+ * The target's forward pass over the flattened tree wrote the KV row of node n of request b into
+ * slot slots[b][n] of every cache.  With the accepted path p_0 = 0, p_1, ..., p_L (as written by
+ * spec_verify_tree_greedy / spec_verify_tree_walk), the row of p_j moves to slot slots[b][j] for
+ * j = 1..L, so the accepted tokens occupy the request's first L + 1 slots in order; every other
+ * slot keeps its contents.  Moves happen in place.
+ *
+ * caches         HOST array of num_caches DEVICE pointers (16-byte aligned), each a cache of
+ *                num_slots rows of row_bytes bytes (a layer's K or V tensor, any element type).
+ * row_bytes      a multiple of 16.
+ * slots          [B][N+1] int32: the slot of each tree node; distinct within a request, and the
+ *                requests' slots disjoint.
+ * parents        [B][N+1] int32 (the tree), accept_len [B], path_nodes [B][N+1] int32.
+ * err_flags      [B] int32 or NULL: SPEC_ERRF_BAD_TREE when accept_len is outside [0, N], the
+ *                path is not a chain of parent links from the root, or a slot is outside
+ *                [0, num_slots); that request's rows are left untouched.
+ * Limits: num_caches <= SPEC_MAX_KV_CACHES, N + 1 <= SPEC_MAX_WALK_NODES, B <= 65535.
+ * One kernel launch; reads and writes each moved row once.  No workspace.
+ */
+spec_status_t spec_kv_compact(void *const *caches, int num_caches, long long num_slots,
+                              int row_bytes, int B, int N, const int32_t *slots,
+                              const int32_t *parents, const int32_t *accept_len,
+                              const int32_t *path_nodes, int32_t *err_flags,
+                              spec_stream_t stream);
 
 /*
  * spec_verify_chain without a workspace argument, for callers that cannot allocate device memory

@@ -9,6 +9,7 @@ from .binding import (  # noqa: F401
     library,
     make_workspace,
     workspace_reset,
+    spec_kv_compact,
     spec_ngram_draft,
     spec_verify_chain,
     spec_verify_ngram,

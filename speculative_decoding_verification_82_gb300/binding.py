@@ -19,10 +19,12 @@ from .build import LIB_PATH
 SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_CUDA, SPEC_ERR_WORKSPACE, SPEC_ERR_UNSUPPORTED = range(5)
 ERRF_BAD_TOKEN, ERRF_NONFINITE, ERRF_TIMEOUT, ERRF_BAD_TREE = 1, 2, 4, 8
 MAX_K, MAX_TREE_NODES, MAX_WALK_NODES, MAX_WALK_VOCAB, MAX_NGRAM = 256, 4096, 1024, 262144, 32
+MAX_KV_CACHES = 1024
 DTYPE_CODE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 
 EXPORTED = ("spec_verify_workspace_bytes", "spec_verify_workspace_reset", "spec_verify_chain",
             "spec_verify_ngram", "spec_verify_tree_greedy", "spec_verify_tree_walk", "spec_ngram_draft",
+            "spec_kv_compact",
             "spec_verify_chain_static", "spec_status_string")
 STATIC_WORKSPACE_BYTES = 4 << 20
 
@@ -57,6 +59,8 @@ def library(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_tree_walk.restype = I
     lib.spec_ngram_draft.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, P]
     lib.spec_ngram_draft.restype = I
+    lib.spec_kv_compact.argtypes = [ctypes.POINTER(c_void_p), I, ctypes.c_longlong, I, I, I, P, P, P, P, P, P]
+    lib.spec_kv_compact.restype = I
     lib.spec_verify_chain_static.argtypes = [P, P, I, I, I, I, F, P, P, P, P, P, P, P, P]
     lib.spec_verify_chain_static.restype = I
     lib.spec_status_string.argtypes = [I]
@@ -266,3 +270,30 @@ def spec_ngram_draft(context, context_len, K: int, *, n_max: int = 4, n_min: int
                               _ptr(dl), _ptr(mn), _ptr(me), _ptr(ef), _stream(dev))
     _check(st)
     return dict(draft_tokens=d, draft_len=dl, match_n=mn, match_end=me, err_flags=ef)
+
+
+def spec_kv_compact(caches, slots, parents, accept_len, path_nodes, *, err_flags=None) -> torch.Tensor:
+    """Moves the accepted path's KV rows into the request's first slots, in place, in every cache
+    of `caches` (CUDA tensors whose first dimension is the slot).  See spec_verify.h."""
+    lib = library()
+    caches = list(caches)
+    if not caches:
+        raise ValueError("no caches")
+    dev = caches[0].device
+    S = caches[0].shape[0]
+    row = caches[0].numel() // max(S, 1) * caches[0].element_size()
+    for i, c in enumerate(caches):
+        if c.device != dev or c.shape[0] != S or not c.is_contiguous():
+            raise ValueError(f"cache {i}: every cache must be contiguous on {dev} with {S} slots")
+        if c.numel() // max(S, 1) * c.element_size() != row:
+            raise ValueError(f"cache {i}: rows of {row} bytes expected")
+    B, N1 = slots.shape
+    for name, t, shp in (("slots", slots, (B, N1)), ("parents", parents, (B, N1)), ("accept_len", accept_len, (B,)),
+                         ("path_nodes", path_nodes, (B, N1))):
+        _need(t, name, torch.int32, shp, dev)
+    ef = _out(err_flags, "err_flags", torch.int32, (B,), dev)
+    arr = (c_void_p * len(caches))(*[c.data_ptr() for c in caches])
+    st = lib.spec_kv_compact(arr, len(caches), S, row, B, N1 - 1, _ptr(slots), _ptr(parents), _ptr(accept_len),
+                             _ptr(path_nodes), _ptr(ef), _stream(dev))
+    _check(st)
+    return ef

@@ -16,7 +16,7 @@ LIB_NAME = "libspecverify.so"
 LIB_PATH = os.path.join(BUILD_DIR, LIB_NAME)
 SOURCES = ["spec_verify_api.cu", "spec_verify_f32.cu", "spec_verify_bf16.cu", "spec_verify_f16.cu",
            "spec_verify_static.cu", "spec_walk.cu",
-           "ngram_draft.cu"]
+           "ngram_draft.cu", "kv_compact.cu"]
 HEADERS = ["verify_kernel.cuh", "verify_common.cuh", "tree_walk.cuh", "fastdiv.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]

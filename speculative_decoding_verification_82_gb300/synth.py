@@ -428,3 +428,33 @@ def ngram_contexts(seed: int = 0, B: int = 256, K: int = 5, V: int = 151936, pro
     for b, s0 in enumerate(starts):
         ctx[b, prompt_len:] = prompt[s0: s0 + ngram_n]
     return ctx, np.full(B, prompt_len + ngram_n, dtype=np.int32)
+
+
+def kv_compact_case(seed: int = 0, B: int = 16, caches: int = 160, row_bytes: int = 2048,
+                    parents: np.ndarray | None = None, deepest: bool = True) -> dict:
+    """Inputs of accepted-path KV compaction: the draft tree of workload 4 (or `parents`), one
+    accepted path per request (from the root to a seeded deepest node, or to any seeded node), the
+    slots of request b's nodes b * (N + 1) + n, and `caches` caches of random bytes with one row
+    per slot.  The default sizes are those of Llama-3.3-70B (the page's serving example: 80 layers,
+    8 KV heads of 128 bf16 values: 160 K/V caches of 2048-byte rows)."""
+    par = eagle_tree_parents() if parents is None else np.asarray(parents, dtype=np.int32)
+    N1 = par.size
+    depth = np.zeros(N1, np.int64)
+    for i in range(1, N1):
+        depth[i] = depth[par[i]] + 1
+    rng = _rng(seed, _S_TREE)
+    pool = np.nonzero(depth == depth.max())[0] if deepest else np.arange(N1)
+    path = np.full((B, N1), -1, np.int32)
+    accept_len = np.zeros(B, np.int32)
+    for b in range(B):
+        v = int(rng.choice(pool))
+        chain = [v]
+        while chain[-1] != 0:
+            chain.append(int(par[chain[-1]]))
+        chain = chain[::-1]
+        path[b, : len(chain)] = chain
+        accept_len[b] = len(chain) - 1
+    slots = (np.arange(B, dtype=np.int32)[:, None] * N1 + np.arange(N1, dtype=np.int32)[None, :]).astype(np.int32)
+    data = _rng(seed, _S_TARGET).integers(0, 256, size=(caches, B * N1, row_bytes), dtype=np.uint8)
+    return dict(caches=data, slots=slots, parents=np.broadcast_to(par, (B, N1)).copy(),
+                accept_len=accept_len, path=path)

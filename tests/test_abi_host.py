@@ -165,3 +165,26 @@ def test_ngram_draft_validation(lib):
     assert call(K=binding.MAX_K + 1) == binding.SPEC_ERR_UNSUPPORTED
     assert call(ctx=0) == binding.SPEC_ERR_INVALID_ARG
     assert call(d=0) == binding.SPEC_ERR_INVALID_ARG
+
+
+def test_kv_compact_validation(lib):
+    P = ctypes.c_void_p
+    f = lib.spec_kv_compact
+    arr = (P * 2)(P(1 << 20), P(2 << 20))
+    ok = dict(C=2, S=100, W=64, B=3, N=5, sl=3 << 20, pa=4 << 20, al=5 << 20, pn=6 << 20)
+
+    def call(caches=arr, **kw):
+        a = dict(ok)
+        a.update(kw)
+        return f(caches, a["C"], a["S"], a["W"], a["B"], a["N"], P(a["sl"]), P(a["pa"]), P(a["al"]), P(a["pn"]),
+                 None, None)
+
+    assert call(B=0) == binding.SPEC_OK
+    assert call(C=0) == binding.SPEC_OK
+    assert call(W=24) == binding.SPEC_ERR_INVALID_ARG           # rows a multiple of 16 bytes
+    assert call(B=-1) == binding.SPEC_ERR_INVALID_ARG
+    assert call(N=binding.MAX_WALK_NODES) == binding.SPEC_ERR_UNSUPPORTED
+    assert call(C=binding.MAX_KV_CACHES + 1) == binding.SPEC_ERR_UNSUPPORTED
+    assert call(sl=0) == binding.SPEC_ERR_INVALID_ARG
+    assert call(caches=(P * 2)(P(1 << 20), P((2 << 20) + 8))) == binding.SPEC_ERR_INVALID_ARG  # misaligned
+    assert call(caches=(P * 2)(P(1 << 20), None)) == binding.SPEC_ERR_INVALID_ARG

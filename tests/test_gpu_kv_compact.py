@@ -1,0 +1,99 @@
+"""GPU parity of accepted-path KV-cache compaction (spec_kv_compact) against the CPU oracle:
+random trees, paths and slot permutations, several caches and row sizes, invalid requests, the
+benchmark configuration (160 caches of 2048-byte rows, deepest paths of the 61-node tree), and
+the verification-then-compaction sequence on the greedy tree workload."""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle_pins as pins
+import parity
+from speculative_decoding_verification_82_gb300 import binding, synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    binding.library()
+
+
+def _run(caches, slots, parents, accept_len, path):
+    dev = [torch.from_numpy(np.ascontiguousarray(c)).cuda() for c in caches]
+    err = binding.spec_kv_compact(dev, parity.i32(slots), parity.i32(parents), parity.i32(accept_len),
+                                  parity.i32(path))
+    torch.cuda.synchronize()
+    return np.stack([d.cpu().numpy() for d in dev]), err.cpu().numpy()
+
+
+@pytest.mark.parametrize("row_bytes,C", [(16, 1), (48, 3), (2048, 4), (4096, 2), (4112, 1)])
+def test_random_paths_and_slots(row_bytes, C):
+    rng = np.random.default_rng(row_bytes + C)
+    B, N1 = 40, int(rng.integers(2, 30))
+    parents = np.zeros((B, N1), np.int32)
+    path = np.full((B, N1), -1, np.int32)
+    al = np.zeros(B, np.int32)
+    for b in range(B):
+        par, _ = pins.random_tree(rng, N1, 50)
+        parents[b] = par
+        v = int(rng.integers(0, N1))
+        chain = [v]
+        while chain[-1] != 0:
+            chain.append(int(par[chain[-1]]))
+        chain = chain[::-1]
+        path[b, : len(chain)] = chain
+        al[b] = len(chain) - 1
+    S = B * N1 + 17
+    slots = rng.permutation(S)[: B * N1].reshape(B, N1).astype(np.int32)  # disjoint, scattered
+    caches = rng.integers(0, 256, (C, S, row_bytes), dtype=np.uint8)
+    g, gerr = _run(caches, slots, parents, al, path)
+    o, oerr = oracle.kv_compact_batch(caches, slots, parents, al, path)
+    assert np.array_equal(gerr, oerr) and (oerr == 0).all()
+    assert np.array_equal(g, o)
+
+
+def test_invalid_requests_are_left_untouched():
+    kc = synth.kv_compact_case(seed=3, B=6, caches=2, row_bytes=64)
+    al, path, slots = kc["accept_len"].copy(), kc["path"].copy(), kc["slots"].copy()
+    al[1] = kc["parents"].shape[1]       # length out of range
+    path[2, 2] = path[2, 3]              # not a parent link
+    slots[3, 5] = 10 ** 6                # slot outside the caches
+    al[4] = -1
+    g, gerr = _run(kc["caches"], slots, kc["parents"], al, path)
+    o, oerr = oracle.kv_compact_batch(kc["caches"], slots, kc["parents"], al, path)
+    assert list(gerr) == list(oerr) == [0] + [oracle.ERR_BAD_TREE] * 4 + [0]
+    assert np.array_equal(g, o)
+
+
+def test_benchmark_configuration():
+    kc = synth.kv_compact_case(seed=0)  # 160 caches x 976 slots x 2048 B, deepest paths (6)
+    g, gerr = _run(kc["caches"], kc["slots"], kc["parents"], kc["accept_len"], kc["path"])
+    o, oerr = oracle.kv_compact_batch(kc["caches"], kc["slots"], kc["parents"], kc["accept_len"], kc["path"])
+    assert (gerr == 0).all() and (oerr == 0).all()
+    assert np.array_equal(g, o)
+
+
+def test_after_greedy_tree_verification():
+    """spec_verify_tree_greedy's path feeds spec_kv_compact on the device: the request's first
+    accept_len + 1 slots then hold the accepted nodes' rows in order."""
+    ti = synth.tree_greedy(seed=1, B=8, V=20000, path_boost=40.0)
+    g = binding.spec_verify_tree_greedy(parity.to_device(ti.target, ti.dtype), parity.i32(ti.node_tokens),
+                                        parity.i32(ti.parents))
+    N1 = ti.N + 1
+    slots = (np.arange(ti.B)[:, None] * N1 + np.arange(N1)[None, :]).astype(np.int32)
+    rows = np.arange(ti.B * N1, dtype=np.int64)
+    cache = torch.from_numpy((rows[:, None] * 16 + np.arange(16)[None, :]).astype(np.uint8)).cuda()
+    err = binding.spec_kv_compact([cache], parity.i32(slots), parity.i32(ti.parents), g["accept_len"],
+                                  g["path_nodes"])
+    torch.cuda.synchronize()
+    c = cache.cpu().numpy()
+    L, P = g["accept_len"].cpu().numpy(), g["path_nodes"].cpu().numpy()
+    assert (err.cpu().numpy() == 0).all() and L.min() >= 1
+    for b in range(ti.B):
+        for j in range(L[b] + 1):
+            want = (rows[b * N1 + P[b, j]] * 16 + np.arange(16)).astype(np.uint8)
+            assert np.array_equal(c[b * N1 + j], want), (b, j)
