@@ -60,6 +60,10 @@ WORKLOADS = {
     "kv_compact": dict(kind="kv", B=16, N=60, V=0, C=160, W=2048, dtype="u8",
                        desc="accepted-path KV compaction: B=16, 61-node tree, deepest accepted paths (6 tokens), "
                             "160 K/V caches (80 layers x 8 KV heads x 128 bf16) of 2048-byte rows"),
+    "tree_sample_mixed": dict(kind="walk", B=16, N=60, V=128256, dtype="bf16", T=1.0,
+                              temps=(0.0, 0.6, 1.0, 1.4),
+                              desc="tree verify by walking, per-request temperature: B=16 requests at T = 0, 0.6, "
+                                   "1.0, 1.4 (cycled), 61-node EAGLE-2-like tree, V=128256 bf16, target + draft logits"),
     "tree_walk_greedy": dict(kind="walk", B=16, N=60, V=128256, dtype="bf16", T=0.0,
                              desc="greedy tree verify by walking: B=16, 61-node EAGLE-2-like tree (depth 6), "
                                   "V=128256 bf16"),
@@ -89,6 +93,8 @@ def make_inputs(name: str, seed: int):
         return synth.tree_sample(seed=seed)
     if name == "tree_walk_greedy":
         return synth.tree_greedy(seed=seed)
+    if name == "tree_sample_mixed":
+        return synth.tree_sample(seed=seed)
     if name == "kv_compact":
         return synth.kv_compact_case(seed=seed)
     if name == "ngram_pipeline":
@@ -107,7 +113,7 @@ def rows_per_request(w: dict) -> int:
         return w["K"] + 1
     if w["kind"] == "kv":
         return w["C"] * w["moves"]  # rows moved per request (set from the inputs by kv_moves)
-    if w["kind"] == "walk" and w["T"] > 0:
+    if w["kind"] == "walk" and (w["T"] > 0 or "temps" in w):
         from speculative_decoding_verification_82_gb300 import synth
 
         par = synth.eagle_tree_parents()
@@ -170,9 +176,10 @@ def walk_read_bytes(w: dict, case) -> int:
         has_kids = np.zeros(N1, bool)
         has_kids[par[b, 1:]] = True
         nodes = path[b, : L[b] + 1]
-        rows = len(nodes) + (int(has_kids[nodes].sum()) if w["T"] > 0 else 0)
+        Tb = np.resize(np.asarray(w["temps"], np.float32), B)[b] if "temps" in w else w["T"]
+        rows = len(nodes) + (int(has_kids[nodes].sum()) if Tb > 0 else 0)
         total += rows * V * es
-    small = B * N1 * 4 * 2 + (B * N1 * 4 + B * 4 if w["T"] > 0 else 0)
+    small = B * N1 * 4 * 2 + (B * N1 * 4 + B * 4 if (w["T"] > 0 or "temps" in w) else 0)
     out = B * 4 + 2 * B * N1 * 4 + B * 4 + B * 4
     return total + small + out
 
@@ -294,10 +301,12 @@ def oracle_run(w: dict, inp, requests, threads: int):
                                    x, inp.r, inp.u, threads=threads, requests=requests)
     if w["kind"] == "walk":
         T = float(w["T"])
-        return oracle.verify_tree_sample(inp.dtype, inp.target, inp.draft if T > 0 else None, inp.B,
+        temps = np.resize(np.asarray(w["temps"], np.float32), inp.B) if "temps" in w else None
+        sampled = T > 0 or temps is not None
+        return oracle.verify_tree_sample(inp.dtype, inp.target, inp.draft if sampled else None, inp.B,
                                          inp.N, inp.V, T, inp.node_tokens, inp.parents,
-                                         inp.r if T > 0 else None, inp.u if T > 0 else None,
-                                         threads=threads, requests=requests)
+                                         inp.r if sampled else None, inp.u if sampled else None,
+                                         threads=threads, requests=requests, temperatures=temps)
     return oracle.verify_tree_greedy(inp.dtype, inp.target, inp.B, inp.N, inp.V, inp.node_tokens,
                                      inp.parents, threads=threads, requests=requests)
 
@@ -414,7 +423,9 @@ class DeviceCase:
         elif w["kind"] == "walk":
             self.T = float(w["T"])
             self.tokens, self.parents = tens(inp.node_tokens), tens(inp.parents)
-            stoch = self.T > 0
+            if "temps" in w:
+                self.temps = tens(np.resize(np.asarray(w["temps"], np.float32), B))
+            stoch = self.T > 0 or "temps" in w
             self.draft = tens(inp.draft, tdt) if stoch else None
             self.r = tens(inp.r) if stoch else None
             self.u = tens(inp.u) if stoch else None
@@ -445,8 +456,8 @@ class DeviceCase:
         if self.w["kind"] == "kv":
             return [self.cache_all, self.slots, self.parents, self.al, self.path]
         if self.w["kind"] == "walk":
-            return [t for t in (self.target, self.draft, self.tokens, self.parents, self.r, self.u)
-                    if t is not None]
+            return [t for t in (self.target, self.draft, self.tokens, self.parents, self.r, self.u,
+                                getattr(self, "temps", None)) if t is not None]
         if self.w["kind"] == "ngram_pipe":
             return [self.target, self.ctx, self.ctx_len, self.r, self.u]
         return [t for t in (self.target, self.draft, self.x, self.r, self.u) if t is not None]
@@ -473,7 +484,7 @@ class DeviceCase:
         if self.w["kind"] == "walk":
             return [("spec_verify_tree_walk",
                     (ptr(self.target), ptr(self.draft), dt, B, self.w["N"], self.w["V"], ctypes.c_float(self.T),
-                     ptr(self.tokens), ptr(self.parents), ptr(self.r), ptr(self.u), ptr(o["accept_len"]),
+                     ptr(getattr(self, "temps", None)), ptr(self.tokens), ptr(self.parents), ptr(self.r), ptr(self.u), ptr(o["accept_len"]),
                      ptr(o["path_nodes"]), ptr(o["out_tokens"]), ptr(o["residual_mass"]), ptr(o["err_flags"]),
                      None, stream))]
         ws, nbytes = ptr(self.ws), self.ws.numel()
@@ -504,7 +515,7 @@ class DeviceCase:
                                                    err_flags=self.out["err_flags"])}
         if self.w["kind"] == "walk":
             return b.spec_verify_tree_walk(self.target, self.draft, self.tokens, self.parents, self.r, self.u,
-                                           self.T, out=self.out)
+                                           self.T, out=self.out, temperatures=getattr(self, "temps", None))
         if self.w["kind"] == "tree":
             return b.spec_verify_tree_greedy(self.target, self.tokens, self.parents, workspace=self.ws, out=self.out)
         if self.w["kind"] == "ngram_pipe":

@@ -74,6 +74,7 @@ typedef enum { SPEC_DTYPE_F32 = 0, SPEC_DTYPE_BF16 = 1, SPEC_DTYPE_F16 = 2 } spe
 #define SPEC_ERRF_NONFINITE 2 /* NaN logits, or +inf / all -inf where a softmax is taken */
 #define SPEC_ERRF_TIMEOUT 4   /* a bounded device wait gave up (should never happen) */
 #define SPEC_ERRF_BAD_TREE 8  /* parents[0] != -1 or parents[i] not in [0, i) */
+#define SPEC_ERRF_BAD_TEMPERATURE 16 /* a per-request temperature that is NaN, negative or infinite */
 
 /* Largest supported sizes. */
 #define SPEC_MAX_K 256           /* draft tokens per request (chain / n-gram) */
@@ -191,7 +192,11 @@ spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t dt
  * target_logits  [B][N+1][V] dtype; row n is the target's prediction after node n.
  * draft_logits   [B][N+1][V] dtype; row n is the draft distribution the children of node n were
  *                drawn from.  Rows of nodes without children are never read; not read at all
- *                (may be NULL) when temperature == 0.
+ *                (may be NULL) when temperature == 0 and temperatures is NULL.
+ * temperatures   [B] float or NULL: each request's own temperature, used instead of
+ *                `temperature` (the x078.com page's production section sets it per request).  0
+ *                walks that request greedily; NaN, a negative value or infinity fails the request
+ *                with SPEC_ERRF_BAD_TEMPERATURE.  When given, draft_logits, r and u are required.
  * node_tokens    [B][N+1] int32 (entry 0 ignored); parents [B][N+1] int32, parents[0] = -1 and
  *                0 <= parents[i] < i.
  * r              [B][N+1] float in (0, 1]: r[b][c] is the uniform of child c's test (entry 0
@@ -216,7 +221,7 @@ spec_status_t spec_verify_tree_greedy(const void *target_logits, spec_dtype_t dt
  */
 spec_status_t spec_verify_tree_walk(const void *target_logits, const void *draft_logits,
                                     spec_dtype_t dtype, int B, int N, int V, float temperature,
-                                    const int32_t *node_tokens, const int32_t *parents,
+                                    const float *temperatures, const int32_t *node_tokens, const int32_t *parents,
                                     const float *r, const float *u, int32_t *accept_len,
                                     int32_t *path_nodes, int32_t *out_tokens,
                                     float *residual_mass, int32_t *err_flags,

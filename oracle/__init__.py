@@ -29,7 +29,7 @@ LIB = os.path.join(BUILD_DIR, "libspec_oracle.so")
 
 DTYPE_CODE = {"f32": 0, "bf16": 1, "f16": 2}
 FLAG_ACCEPT_TIE, FLAG_CDF_TIE, FLAG_ZERO_RESIDUAL = 1, 2, 4
-ERR_BAD_TOKEN, ERR_NONFINITE, ERR_BAD_TREE = 1, 2, 8
+ERR_BAD_TOKEN, ERR_NONFINITE, ERR_BAD_TREE, ERR_BAD_TEMP = 1, 2, 8, 16
 DEFAULT_TOL = 1e-6
 
 _lock = threading.Lock()
@@ -79,7 +79,7 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_verify_tree_greedy.restype = None
     lib.oracle_tree_sample_probs.argtypes = [I, I, P, P, P, P, P, F, D, P, P, P, P, P, P]
     lib.oracle_tree_sample_probs.restype = None
-    lib.oracle_verify_tree_sample.argtypes = [I, P, P, I, I, I, F, P, P, P, P, D, I, I,
+    lib.oracle_verify_tree_sample.argtypes = [I, P, P, I, I, I, F, P, P, P, P, P, D, I, I,
                                               P, P, P, P, P, P, P]
     lib.oracle_verify_tree_sample.restype = None
     lib.oracle_ngram_draft.argtypes = [P, I, I, I, I, P, P, P, P]
@@ -306,8 +306,9 @@ def tree_sample_probs(p, q, parents, tokens, r, u, tol: float = DEFAULT_TOL, lib
 
 def verify_tree_sample(dtype: str, target, draft, B: int, N: int, V: int, T: float, node_tokens,
                        parents, r, u, tol: float = DEFAULT_TOL, threads: int = 1, requests=None,
-                       lib=None) -> dict:
-    """Tree verification by walking: stochastic (T > 0) or greedy (T == 0) on visited rows."""
+                       lib=None, temperatures=None) -> dict:
+    """Tree verification by walking: stochastic (T > 0) or greedy (T == 0) on visited rows;
+    `temperatures` [B] sets each request's own temperature (R18)."""
     lib = lib or load()
     target = np.ascontiguousarray(target)
     draft_p = _p(np.ascontiguousarray(draft)) if draft is not None else None
@@ -315,15 +316,17 @@ def verify_tree_sample(dtype: str, target, draft, B: int, N: int, V: int, T: flo
     N1 = N + 1
     rr = _c(r, np.float32) if r is not None else np.zeros((B, N1), np.float32)
     uu = _c(u, np.float32) if u is not None else np.zeros(B, np.float32)
+    tt = _c(temperatures, np.float32) if temperatures is not None else None
     o = dict(accept_len=np.zeros(B, np.int32), path=np.zeros((B, N1), np.int32),
              out_tokens=np.zeros((B, N1), np.int32), alpha=np.zeros((B, N1), np.float64),
              mass=np.zeros(B, np.float64), req_flag=np.zeros(B, np.int32),
              err=np.zeros(B, np.int32))
-    keep = (target, draft)
+    keep = (target, draft, tt)
 
     def run(b0, b1):
         lib.oracle_verify_tree_sample(DTYPE_CODE[dtype], _p(target), draft_p, B, N, V, float(T),
-                                      _p(tk), _p(pa), _p(rr), _p(uu), tol, b0, b1,
+                                      _p(tt) if tt is not None else None, _p(tk), _p(pa), _p(rr),
+                                      _p(uu), tol, b0, b1,
                                       *(_p(o[k]) for k in ("accept_len", "path", "out_tokens",
                                                            "alpha", "mass", "req_flag", "err")))
 

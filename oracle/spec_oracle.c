@@ -58,7 +58,7 @@ enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2 };
 /* per-request / per-position tie flags (R10, R5) */
 enum { ORF_ACCEPT_TIE = 1, ORF_CDF_TIE = 2, ORF_ZERO_RESIDUAL = 4 };
 /* per-request error bits (R11) */
-enum { ORE_BAD_TOKEN = 1, ORE_NONFINITE = 2, ORE_BAD_TREE = 8 };
+enum { ORE_BAD_TOKEN = 1, ORE_NONFINITE = 2, ORE_BAD_TREE = 8, ORE_BAD_TEMP = 16 };
 
 /* ---------------------------------------------------------------- exact input widening ---- */
 static double half_to_double(uint16_t h)
@@ -765,14 +765,17 @@ static int tree_greedy_visited(int dtype, const void *target, size_t row0, int N
 /*
  * Tree verification by walking (R13-R15).  target, draft: [B][N+1][V] (draft ignored when
  * T == 0); node_tokens, parents: [B][N+1]; r: [B][N+1]; u: [B].
+ * R18 per-request temperature (the x078.com page's production section sets the temperature per
+ * request): when temps is not NULL, request b uses temps[b] instead of T (0 = greedy); a value
+ * that is NaN, negative or infinite fails the request with ORE_BAD_TEMP.
  * Outputs: accept_len[B], path[B][N+1], out_tokens[B][N+1], alpha[B][N+1], mass[B],
  * req_flag[B], err[B].  Requests [b0, b1) only are processed.
  */
 void oracle_verify_tree_sample(int dtype, const void *target, const void *draft, int B, int N,
-                               int V, float T, const int *node_tokens, const int *parents,
-                               const float *r, const float *u, double tol, int b0, int b1,
-                               int *accept_len, int *path, int *out_tokens, double *alpha,
-                               double *mass, int *req_flag, int *err)
+                               int V, float T, const float *temps, const int *node_tokens,
+                               const int *parents, const float *r, const float *u, double tol,
+                               int b0, int b1, int *accept_len, int *path, int *out_tokens,
+                               double *alpha, double *mass, int *req_flag, int *err)
 {
     int N1 = N + 1;
     double *l = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
@@ -782,15 +785,18 @@ void oracle_verify_tree_sample(int dtype, const void *target, const void *draft,
         int *o_path = path + (size_t)b * N1, *o_tok = out_tokens + (size_t)b * N1;
         double *o_al = alpha + (size_t)b * N1;
         int e = oracle_tree_check(N1, V, pb, tb);
+        float Tb = temps ? temps[b] : T;
         req_flag[b] = 0;
         mass[b] = 0.0;
+        if (!(Tb >= 0.0f) || isinf(Tb))
+            e = ORE_BAD_TEMP;
         if (!e) {
-            if (T == 0.0f) {
+            if (Tb == 0.0f) {
                 e = tree_greedy_visited(dtype, target, (size_t)b * N1, N1, V, pb, tb,
                                         accept_len + b, o_path, o_tok, o_al);
                 mass[b] = 1.0;
             } else {
-                struct logits_ctx c = {dtype, V, (double)T, target, draft, (size_t)b * N1, l};
+                struct logits_ctx c = {dtype, V, (double)Tb, target, draft, (size_t)b * N1, l};
                 e = tree_sample_walk(N1, V, logits_rows, &c, pb, tb, r + (size_t)b * N1, u[b],
                                      tol, accept_len + b, o_path, o_tok, o_al, mass + b,
                                      req_flag + b);

@@ -17,7 +17,7 @@ import torch
 from .build import LIB_PATH
 
 SPEC_OK, SPEC_ERR_INVALID_ARG, SPEC_ERR_CUDA, SPEC_ERR_WORKSPACE, SPEC_ERR_UNSUPPORTED = range(5)
-ERRF_BAD_TOKEN, ERRF_NONFINITE, ERRF_TIMEOUT, ERRF_BAD_TREE = 1, 2, 4, 8
+ERRF_BAD_TOKEN, ERRF_NONFINITE, ERRF_TIMEOUT, ERRF_BAD_TREE, ERRF_BAD_TEMPERATURE = 1, 2, 4, 8, 16
 MAX_K, MAX_TREE_NODES, MAX_WALK_NODES, MAX_WALK_VOCAB, MAX_NGRAM = 256, 4096, 1024, 262144, 32
 MAX_KV_CACHES = 1024
 DTYPE_CODE = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
@@ -55,7 +55,7 @@ def library(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_ngram.restype = I
     lib.spec_verify_tree_greedy.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, P, Z, P]
     lib.spec_verify_tree_greedy.restype = I
-    lib.spec_verify_tree_walk.argtypes = [P, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P]
+    lib.spec_verify_tree_walk.argtypes = [P, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.spec_verify_tree_walk.restype = I
     lib.spec_ngram_draft.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P, P]
     lib.spec_ngram_draft.restype = I
@@ -218,9 +218,10 @@ def spec_verify_tree_greedy(target_logits, node_tokens, parents, *, workspace=No
 
 
 def spec_verify_tree_walk(target_logits, draft_logits, node_tokens, parents, r, u, temperature, *,
-                          out=None, accept_prob=None) -> dict:
+                          out=None, accept_prob=None, temperatures=None) -> dict:
     """Verification of a draft tree by walking it (stochastic for T > 0, greedy for T == 0),
-    reading only the visited rows.  See spec_verify.h."""
+    reading only the visited rows; `temperatures` [B] gives each request its own T.  See
+    spec_verify.h."""
     lib = library()
     dev = target_logits.device
     if target_logits.dtype not in DTYPE_CODE or target_logits.dim() != 3:
@@ -230,7 +231,10 @@ def spec_verify_tree_walk(target_logits, draft_logits, node_tokens, parents, r, 
     _need(target_logits, "target_logits", None, (B, N1, V), dev)
     _need(node_tokens, "node_tokens", torch.int32, (B, N1), dev)
     _need(parents, "parents", torch.int32, (B, N1), dev)
-    if T > 0:
+    if temperatures is not None:
+        _need(temperatures, "temperatures", torch.float32, (B,), dev)
+    sampled = T > 0 or temperatures is not None
+    if sampled:
         _need(draft_logits, "draft_logits", target_logits.dtype, (B, N1, V), dev)
         _need(r, "r", torch.float32, (B, N1), dev)
         _need(u, "u", torch.float32, (B,), dev)
@@ -241,10 +245,10 @@ def spec_verify_tree_walk(target_logits, draft_logits, node_tokens, parents, r, 
     rm = _out(out.get("residual_mass"), "residual_mass", torch.float32, (B,), dev)
     ef = _out(out.get("err_flags"), "err_flags", torch.int32, (B,), dev)
     ap = _opt(accept_prob, "accept_prob", torch.float32, (B, N1), dev)
-    st = lib.spec_verify_tree_walk(_ptr(target_logits), _ptr(draft_logits) if T > 0 else None,
-                                   DTYPE_CODE[target_logits.dtype], B, N1 - 1, V, T,
-                                   _ptr(node_tokens), _ptr(parents), _ptr(r) if T > 0 else None,
-                                   _ptr(u) if T > 0 else None, _ptr(al), _ptr(pn), _ptr(ot),
+    st = lib.spec_verify_tree_walk(_ptr(target_logits), _ptr(draft_logits) if sampled else None,
+                                   DTYPE_CODE[target_logits.dtype], B, N1 - 1, V, T, _ptr(temperatures),
+                                   _ptr(node_tokens), _ptr(parents), _ptr(r) if sampled else None,
+                                   _ptr(u) if sampled else None, _ptr(al), _ptr(pn), _ptr(ot),
                                    _ptr(rm), _ptr(ef), _ptr(ap), _stream(dev))
     _check(st)
     return dict(accept_len=al, path_nodes=pn, out_tokens=ot, residual_mass=rm, err_flags=ef)

@@ -94,7 +94,7 @@ bool aligned(const void* p, unsigned a) { return ((uintptr_t)p % a) == 0; }
 
 extern "C" spec_status_t spec_verify_tree_walk(const void* target_logits, const void* draft_logits,
                                                spec_dtype_t dtype, int B, int N, int V, float temperature,
-                                               const int32_t* node_tokens, const int32_t* parents, const float* r,
+                                               const float* temperatures, const int32_t* node_tokens, const int32_t* parents, const float* r,
                                                const float* u, int32_t* accept_len, int32_t* path_nodes,
                                                int32_t* out_tokens, float* residual_mass, int32_t* err_flags,
                                                float* accept_prob, spec_stream_t stream) {
@@ -105,7 +105,8 @@ extern "C" spec_status_t spec_verify_tree_walk(const void* target_logits, const 
   Geometry g;
   if (!plan(V, &g)) return SPEC_ERR_UNSUPPORTED;
   if (B == 0) return SPEC_OK;
-  const bool greedy = temperature == 0.f;
+  // with per-request temperatures any request may sample: draft logits, r and u are needed
+  const bool greedy = temperature == 0.f && !temperatures;
   if (!target_logits || !node_tokens || !parents || !accept_len || !path_nodes || !out_tokens)
     return SPEC_ERR_INVALID_ARG;
   if (!greedy && (!draft_logits || !r || !u)) return SPEC_ERR_INVALID_ARG;
@@ -124,6 +125,7 @@ extern "C" spec_status_t spec_verify_tree_walk(const void* target_logits, const 
   P.parents = parents;
   P.r = r;
   P.u = u;
+  P.temps = temperatures;
   P.accept_len = accept_len;
   P.path_nodes = path_nodes;
   P.out_tokens = out_tokens;

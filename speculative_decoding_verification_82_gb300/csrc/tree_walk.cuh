@@ -48,6 +48,7 @@ struct Params {
   const int32_t* parents;      // [B][N1]
   const float* r;              // [B][N1]
   const float* u;              // [B]
+  const float* temps;          // [B] or null: each request's own temperature (0 = greedy)
   int32_t* accept_len;         // [B]
   int32_t* path_nodes;         // [B][N1]
   int32_t* out_tokens;         // [B][N1]
@@ -247,8 +248,15 @@ template <typename T, int E>
 __device__ void walk_request(const Params& P, Shared& sm, int b, long long first, uint32_t rank, int& round) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int N1 = P.N1, V = P.V, cl = P.cl;
-  const bool greedy = P.c == 0.f, vec = P.vec != 0;
-  const float c = P.c;
+  // the request's temperature: log2(e) / T, formed in double as the host forms the call's own
+  float c = P.c;
+  bool bad_temp = false;
+  if (P.temps) {
+    const float Tb = __ldg(P.temps + b);
+    bad_temp = !(Tb >= 0.f) || isinf(Tb);
+    c = (bad_temp || Tb == 0.f) ? 0.f : (float)(1.4426950408889634 / (double)Tb);
+  }
+  const bool greedy = c == 0.f, vec = P.vec != 0;
 
   // Stage the tree; the first malformed node decides the error (its parent checked first).
   __syncthreads();  // the previous request's readers of the tree are done
@@ -263,8 +271,8 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
     if (code) key = min(key, (i << 4) | code);
   }
   key = block_min(sm, key);  // its barriers also publish sm.par / sm.tok
-  if (key != INT_MAX) {
-    if (rank == 0) write_failure(P, b, key & 15);
+  if (bad_temp || key != INT_MAX) {
+    if (rank == 0) write_failure(P, b, bad_temp ? SPEC_ERRF_BAD_TEMPERATURE : key & 15);
     return;
   }
   if (rank == 0 && P.accept_prob)

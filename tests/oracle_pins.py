@@ -684,3 +684,31 @@ def pin_kv_compact_validation(lib):
 
 
 FAST_PINS += [pin_hand_kv_compact_cases, pin_kv_compact_sequential_moves, pin_kv_compact_validation]
+
+
+def pin_tree_walk_per_request_temperature(lib):
+    """R18: a batch with one temperature per request (greedy ones included) gives, request by
+    request, what a call at that request's temperature gives; a bad temperature fails only its
+    request."""
+    rng = np.random.default_rng(97)
+    B, V = 8, 12
+    par = np.array([-1, 0, 0, 1, 1, 2], np.int32)
+    N1 = par.size
+    lt = rng.normal(0, 2, (B, N1, V)).astype(np.float32)
+    ld = (lt + rng.normal(0, 1, (B, N1, V))).astype(np.float32)
+    tok = rng.integers(0, V, (B, N1)).astype(np.int32)
+    parents = np.broadcast_to(par, (B, N1)).copy()
+    r = ((rng.integers(0, 1 << 24, (B, N1)) + 1) / float(1 << 24)).astype(np.float32)
+    u = (rng.integers(0, 1 << 24, B) / float(1 << 24)).astype(np.float32)
+    temps = np.array([0.5, 0.0, 1.0, 2.0, 0.0, 0.8, np.nan, -1.0], np.float32)
+    o = oracle.verify_tree_sample("f32", lt, ld, B, N1 - 1, V, 1.0, tok, parents, r, u, lib=lib,
+                                  temperatures=temps)
+    for b in range(6):
+        one = oracle.verify_tree_sample("f32", lt[b:b + 1], ld[b:b + 1], 1, N1 - 1, V, float(temps[b]),
+                                        tok[b:b + 1], parents[b:b + 1], r[b:b + 1], u[b:b + 1], lib=lib)
+        for k in ("accept_len", "path", "out_tokens", "alpha", "mass", "req_flag", "err"):
+            assert np.array_equal(o[k][b], one[k][0]), (b, k)
+    assert list(o["err"][6:]) == [oracle.ERR_BAD_TEMP] * 2 and (o["out_tokens"][6:] == -1).all()
+
+
+FAST_PINS.append(pin_tree_walk_per_request_temperature)

@@ -148,27 +148,30 @@ def compare_tree(g: dict, o: dict) -> dict:
 
 
 # ------------------------------------------------------------------------ tree walk ----
-def run_gpu_walk(ti, temperature=None) -> dict:
+def run_gpu_walk(ti, temperature=None, temperatures=None) -> dict:
     T = float(ti.temperature if temperature is None else temperature)
+    sampled = T > 0 or temperatures is not None
     tl = to_device(ti.target, ti.dtype)
-    dl = to_device(ti.draft, ti.dtype) if (T > 0 and ti.draft is not None) else None
-    r = f32(ti.r) if T > 0 else None
-    u = f32(ti.u) if T > 0 else None
+    dl = to_device(ti.draft, ti.dtype) if (sampled and ti.draft is not None) else None
+    r = f32(ti.r) if sampled else None
+    u = f32(ti.u) if sampled else None
+    tt = f32(temperatures) if temperatures is not None else None
     ap = torch.full((ti.B, ti.N + 1), -7.0, device="cuda")
     o = binding.spec_verify_tree_walk(tl, dl, i32(ti.node_tokens), i32(ti.parents), r, u, T,
-                                      accept_prob=ap)
+                                      accept_prob=ap, temperatures=tt)
     torch.cuda.synchronize()
     res = {k: v.cpu().numpy() for k, v in o.items()}
     res["accept_prob"] = ap.cpu().numpy()
     return res
 
 
-def run_oracle_walk(ti, temperature=None, threads: int = 8) -> dict:
+def run_oracle_walk(ti, temperature=None, threads: int = 8, temperatures=None) -> dict:
     T = float(ti.temperature if temperature is None else temperature)
-    return oracle.verify_tree_sample(ti.dtype, ti.target, ti.draft if T > 0 else None, ti.B, ti.N,
+    sampled = T > 0 or temperatures is not None
+    return oracle.verify_tree_sample(ti.dtype, ti.target, ti.draft if sampled else None, ti.B, ti.N,
                                      ti.V, T, ti.node_tokens, ti.parents,
-                                     ti.r if T > 0 else None, ti.u if T > 0 else None,
-                                     threads=threads)
+                                     ti.r if sampled else None, ti.u if sampled else None,
+                                     threads=threads, temperatures=temperatures)
 
 
 def compare_walk(g: dict, o: dict, ti) -> dict:

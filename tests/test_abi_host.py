@@ -127,7 +127,7 @@ def test_tree_walk_validation(lib):
     def call(**kw):
         a = dict(ok)
         a.update(kw)
-        return f(P(a["t"]), P(a["d"]), a["dt"], a["B"], a["N"], a["V"], a["T"], P(a["tok"]),
+        return f(P(a["t"]), P(a["d"]), a["dt"], a["B"], a["N"], a["V"], a["T"], P(a.get("temps", 0)), P(a["tok"]),
                  P(a["par"]), P(a["r"]), P(a["u"]), P(a["al"]), P(a["pn"]), P(a["ot"]), None, None,
                  None, None)
 
@@ -143,6 +143,7 @@ def test_tree_walk_validation(lib):
     assert call(d=0) == binding.SPEC_ERR_INVALID_ARG        # T > 0 needs draft logits
     assert call(r=0) == binding.SPEC_ERR_INVALID_ARG
     assert call(t=(1 << 20) + 1) == binding.SPEC_ERR_INVALID_ARG  # misaligned bf16
+    assert call(T=0.0, temps=9 << 20, d=0) == binding.SPEC_ERR_INVALID_ARG  # per-request T needs the draft
 
 
 def test_ngram_draft_validation(lib):

@@ -168,3 +168,21 @@ def test_walk_repeatable_and_on_a_side_stream():
         b = parity.run_gpu_walk(ti)
     for k in a:
         assert np.array_equal(a[k], b[k]), k
+
+
+def test_walk_per_request_temperatures():
+    """Each request at its own temperature (greedy ones included) in one call, against the oracle
+    with the same per-request temperatures; NaN and negative temperatures fail their request."""
+    rng = np.random.default_rng(61)
+    ti = synth.tree_sample(seed=61, B=14, V=32000, parents=_random_parents(rng, 12), draft_sigma=1.0)
+    temps = np.array([0.0, 0.6, 1.0, 1.6, 0.05, 4.0, 0.0, 0.9, 1.2, 0.3, np.nan, -0.5, 0.7, 2.2],
+                     np.float32)
+    g = parity.run_gpu_walk(ti, 1.0, temperatures=temps)
+    o = parity.run_oracle_walk(ti, 1.0, temperatures=temps)
+    st = parity.compare_walk(g, o, ti)
+    _show("walk per-request T", st)
+    assert list(o["err"][10:12]) == [oracle.ERR_BAD_TEMP] * 2
+    # a request's result equals a call at its own temperature
+    one = parity.run_gpu_walk(ti, 1.6)
+    assert np.array_equal(one["path_nodes"][3], g["path_nodes"][3])
+    assert np.array_equal(one["out_tokens"][3], g["out_tokens"][3])

@@ -68,6 +68,7 @@ MUTANTS = [
     ("kv_compact_last_row_dropped", "for (int j = 1; j <= L; j++) /* read every accepted row before any slot is written */",
      "for (int j = 1; j < L; j++) /* read every accepted row before any slot is written */"),
     ("kv_compact_path_check_dropped", "ok = pt[j] > 0 && pt[j] < N1 && pa[pt[j]] == pt[j - 1];", "ok = 1;"),
+    ("tree_walk_per_request_temperature_ignored", "float Tb = temps ? temps[b] : T;", "float Tb = T;"),
     ("bad_token_check_dropped", "if (xb[k] < 0 || xb[k] >= V)\n                e |= ORE_BAD_TOKEN;",
      "if (0)\n                e |= ORE_BAD_TOKEN;"),
 ]
