@@ -106,7 +106,7 @@ def make_inputs(name: str, seed: int):
 
 def rows_per_request(w: dict) -> int:
     """Logits rows a request supplies: a walk's draft rows count for the nodes with children (the
-    rows that exist as the draft's output), 21 of the 61 nodes of the benchmark tree."""
+    rows that exist as the draft's output), 20 of the 61 nodes of the benchmark tree."""
     if w["kind"] == "chain":
         return 2 * w["K"] + 1
     if w["kind"] in ("ngram", "ngram_pipe"):
