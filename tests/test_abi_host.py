@@ -189,3 +189,19 @@ def test_kv_compact_validation(lib):
     assert call(sl=0) == binding.SPEC_ERR_INVALID_ARG
     assert call(caches=(P * 2)(P(1 << 20), P((2 << 20) + 8))) == binding.SPEC_ERR_INVALID_ARG  # misaligned
     assert call(caches=(P * 2)(P(1 << 20), None)) == binding.SPEC_ERR_INVALID_ARG
+
+
+def test_header_is_plain_c(tmp_path):
+    """The ABI header compiles as strict C99 (no C++ or CUDA types in the signatures)."""
+    import shutil
+    import subprocess
+
+    if shutil.which("gcc") is None:
+        import pytest
+
+        pytest.skip("gcc not found")
+    src = tmp_path / "use.c"
+    src.write_text('#include "spec_verify.h"\nint main(void) { return spec_status_string(SPEC_OK) == 0; }\n')
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-fsyntax-only",
+                        "-I", os.path.dirname(HEADER), str(src)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
