@@ -121,6 +121,14 @@ def rows_per_request(w: dict) -> int:
     return w["N"] + 1
 
 
+KV_METRIC = "KV-cache rows compacted per second (a row: one token's K or V in one layer) and achieved HBM GB/s"
+KV_ORACLE_CACHES = 8  # the CPU oracle's sample moves the rows of this many of the caches
+
+
+def workload_metric(w: dict) -> str:
+    return KV_METRIC if w["kind"] == "kv" else METRIC
+
+
 def kv_moves(inp) -> float:
     """Mean number of rows a request's compaction moves in one cache: accepted positions j whose
     node is not already in position j's slot (those are skipped).  Along the benchmark tree's
@@ -290,7 +298,7 @@ def oracle_run(w: dict, inp, requests, threads: int):
                                    inp.draft_tokens, inp.r, inp.u, threads=threads, requests=requests)
     if w["kind"] == "kv":
         b0, b1 = requests
-        return oracle.kv_compact_batch(inp["caches"][:8], inp["slots"][b0:b1], inp["parents"][b0:b1],
+        return oracle.kv_compact_batch(inp["caches"][:KV_ORACLE_CACHES], inp["slots"][b0:b1], inp["parents"][b0:b1],
                                        inp["accept_len"][b0:b1], inp["path"][b0:b1])
     if w["kind"] == "ngram_pipe":
         b0, b1 = requests
@@ -336,9 +344,10 @@ def cpu_baseline(w: dict, inp, min_wall: float = 1.0) -> dict:
         reps += 1
     rows = reps * n_req * rows_per_request(w)
     if w["kind"] == "kv":
-        rows = rows * 8 // w["C"]  # the oracle sample moves rows of 8 of the caches
+        rows = rows * KV_ORACLE_CACHES / w["C"]
+    note = f", the rows of {KV_ORACLE_CACHES} of the {w['C']} caches" if w["kind"] == "kv" else ""
     return {"value": rows / wall, "unit": "rows/s", "cores": threads, "kind": "oracle",
-            "sample": f"all {n_req} requests of the workload ({n_req * rows_per_request(w)} rows), "
+            "sample": f"all {n_req} requests of the workload ({rows / reps:g} rows{note}), "
                       f"{reps} repetitions, requests split over {threads} threads, {wall:.2f} s wall"}
 
 
@@ -679,7 +688,7 @@ def run_gpu(args, w) -> None:
         "clocks": clk,
     }
     if w["kind"] == "kv":
-        line["metric"] = "KV-cache rows compacted per second (a row: one token's K or V in one layer) and achieved HBM GB/s"
+        line["metric"] = KV_METRIC
         line["roofline"]["kernel"] = "kv_compact_kernel (one launch per call)"
         line["config"]["rows"] = (f"moved rows ({w['moves']:g} per request and cache: accepted positions whose node is "
                                   f"not already in place) x 2048 bytes, read and written once")
@@ -715,19 +724,23 @@ def run_reference(args, w) -> None:
     t = 0.0
     for _ in range(args.steps):
         t += oracle_timed(w, inp, n_req, threads)
-    value = args.steps * n_req * rows_per_request(w) / t
+    # the KV compaction's oracle sample moves the rows of KV_ORACLE_CACHES of the caches
+    scale = KV_ORACLE_CACHES / w["C"] if w["kind"] == "kv" else 1
+    sample_note = f" of {KV_ORACLE_CACHES} of the {w['C']} caches" if w["kind"] == "kv" else ""
+    value = args.steps * n_req * rows_per_request(w) * scale / t
     line = {
         "impl": "reference",
-        "metric": METRIC,
+        "metric": workload_metric(w),
         "value": value, "unit": "rows/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w["dtype"],
         "data": "synthetic (seeded Philox)",
         "config": {"workload": w["desc"], "B": w["B"], "V": w["V"],
-                   "rows_per_step": n_req * rows_per_request(w)},
+                   "rows_per_step": n_req * rows_per_request(w) * scale},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
                          "sample": f"{n_req} request(s) of the workload per step "
-                                   f"({n_req * rows_per_request(w)} rows), split over {threads} threads"},
+                                   f"({n_req * rows_per_request(w) * scale:g} rows{sample_note}), "
+                                   f"split over {threads} threads"},
         "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
