@@ -5,7 +5,8 @@ trees over the vocabulary sizes that select every cluster size (1 to 16 CTAs), t
 types, ragged and misaligned rows, the EAGLE-2-like benchmark tree at V = 128256, more requests
 than clusters resident at once, extreme temperatures.  Greedy walks (T = 0): against the oracle and
 against spec_verify_tree_greedy (which reads every row).  Edge cases: the root alone, malformed
-trees and tokens, non-finite visited rows, non-finite rows the walk never reads.
+trees and tokens, non-finite visited rows, non-finite rows the walk never reads.  Per-request
+temperatures, greedy and invalid ones included, in one call.
 """
 
 import numpy as np
