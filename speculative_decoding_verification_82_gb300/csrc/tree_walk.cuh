@@ -433,8 +433,13 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
       break;
     }
     const float mct = __fmul_rn(mt, c), mcd = __fmul_rn(md, c);
-    {
-      // the thread's scale 2^(round(m c) - round(M c)) / Z, its exponent as an exact pair
+    // p and q themselves are formed only when a rejection or the draw needs them (a first child
+    // accepted on its test needs only the statistics): the thread's scale
+    // 2^(round(m c) - round(M c)) / Z, its exponent as an exact pair
+    bool formed = false;
+    auto form_pq = [&]() {
+      if (formed) return;
+      formed = true;
       Exp2 xt;
       two_sum(mcl_t, -mct, xt.hi, xt.lo);
       const float st = mtl == -INFINITY ? 0.f : exp2_times(xt, __frcp_rn(zt));
@@ -447,7 +452,7 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
 #pragma unroll
         for (int k = 0; k < E; ++k) q[k] = __fmul_rn(q[k], sd);
       }
-    }
+    };
 
     // ---- the children in order: accept test against the current residual target ----
     float cc = 0.f, R = 1.f;
@@ -468,6 +473,7 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
         next = sm.kid[j];
         break;
       }
+      form_pq();
       cc = __fadd_rn(cc, R);
       float s = 0.f;
 #pragma unroll
@@ -486,6 +492,7 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
     }
 
     // ---- the draw: smallest token whose cumulative weight exceeds u * S ----
+    form_pq();
     const bool resid = need_q && !empty && cc > 0.f;
     float s = 0.f;
 #pragma unroll
