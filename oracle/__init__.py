@@ -29,6 +29,10 @@ LIB = os.path.join(BUILD_DIR, "libspec_oracle.so")
 
 DTYPE_CODE = {"f32": 0, "bf16": 1, "f16": 2}
 FLAG_ACCEPT_TIE, FLAG_CDF_TIE, FLAG_ZERO_RESIDUAL = 1, 2, 4
+# the widened tie tier (reading R10 / R14): within tol / S (tol / R) of a boundary but not within tol
+FLAG_CDF_TIE_WIDE, FLAG_ACCEPT_TIE_WIDE = 8, 16
+FLAGS_STRICT = FLAG_ACCEPT_TIE | FLAG_CDF_TIE
+FLAGS_WIDE = FLAG_ACCEPT_TIE_WIDE | FLAG_CDF_TIE_WIDE
 ERR_BAD_TOKEN, ERR_NONFINITE, ERR_BAD_TREE, ERR_BAD_TEMP = 1, 2, 8, 16
 DEFAULT_TOL = 1e-6
 
@@ -77,11 +81,16 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_tree_bruteforce.restype = I
     lib.oracle_verify_tree_greedy.argtypes = [I, P, I, I, I, P, P, I, I, P, P, P, P, P]
     lib.oracle_verify_tree_greedy.restype = None
-    lib.oracle_tree_sample_probs.argtypes = [I, I, P, P, P, P, P, F, D, P, P, P, P, P, P]
+    lib.oracle_tree_sample_probs.argtypes = [I, I, P, P, P, P, P, F, D, I, P, P, P, P, P, P, P, P]
     lib.oracle_tree_sample_probs.restype = None
     lib.oracle_verify_tree_sample.argtypes = [I, P, P, I, I, I, F, P, P, P, P, P, D, I, I,
                                               P, P, P, P, P, P, P]
     lib.oracle_verify_tree_sample.restype = None
+    lib.oracle_chain_draw_rows.argtypes = [I, P, P, I, I, I, F, P, I, P, P]
+    lib.oracle_chain_draw_rows.restype = I
+    lib.oracle_tree_sample_alt.argtypes = [I, P, P, I, I, F, P, P, P, P, P, D, I, I,
+                                           P, P, P, P, P, P, P, P]
+    lib.oracle_tree_sample_alt.restype = I
     lib.oracle_ngram_draft.argtypes = [P, I, I, I, I, P, P, P, P]
     lib.oracle_ngram_draft.restype = None
     lib.oracle_ngram_draft_batch.argtypes = [P, P, I, I, I, I, I, I, I, P, P, P, P, P]
@@ -243,6 +252,48 @@ def verify_ngram(dtype: str, target, B: int, K: int, V: int, T: float, draft_tok
     return o
 
 
+def chain_draw_rows(dtype: str, target, draft, B: int, K: int, V: int, T: float, draft_tokens,
+                    b: int, ngram: bool = False, lib=None) -> tuple[np.ndarray, np.ndarray, int]:
+    """The draws of request b of a chain (or n-gram) call, for checking a flagged tie: w [K+1][V],
+    the weights each position's draw uses (residual, bonus row, or p after an empty residual), and
+    cdf [K+1][V], their normalised cumulative sums; token t is drawn at k for u in
+    [cdf[k][t-1], cdf[k][t]).  Returns (w, cdf, error bits)."""
+    lib = lib or load()
+    target = np.ascontiguousarray(target)
+    dr = np.ascontiguousarray(draft) if (draft is not None and not ngram) else None
+    x = _c(draft_tokens, np.int32)
+    w = np.zeros((K + 1, V), np.float64)
+    cdf = np.zeros((K + 1, V), np.float64)
+    e = lib.oracle_chain_draw_rows(DTYPE_CODE[dtype], _p(target), _p(dr) if dr is not None else None,
+                                   1 if ngram else 0, K, V, float(T), _p(x), int(b), _p(w), _p(cdf))
+    return w, cdf, e
+
+
+def tree_sample_alt(dtype: str, target, draft, B: int, N: int, V: int, T: float, node_tokens,
+                    parents, r, u, b: int, flip: bool, tol: float = DEFAULT_TOL, temperatures=None,
+                    lib=None) -> dict:
+    """Request b of `verify_tree_sample`, with the first flagged accept test decided the other way
+    when `flip`, plus the final draw's weights `draw_w` and normalised CDF `draw_cdf` ([V])."""
+    lib = lib or load()
+    target = np.ascontiguousarray(target)
+    dr = np.ascontiguousarray(draft) if draft is not None else None
+    tk, pa = _c(node_tokens, np.int32), _c(parents, np.int32)
+    N1 = N + 1
+    rr = _c(r, np.float32) if r is not None else np.zeros((B, N1), np.float32)
+    uu = _c(u, np.float32) if u is not None else np.zeros(B, np.float32)
+    tt = _c(temperatures, np.float32) if temperatures is not None else None
+    L, fl = np.zeros(1, np.int32), np.zeros(1, np.int32)
+    path, out = np.zeros(N1, np.int32), np.zeros(N1, np.int32)
+    alpha, mass = np.zeros(N1, np.float64), np.zeros(1, np.float64)
+    dw, dc = np.zeros(max(V, 1), np.float64), np.zeros(max(V, 1), np.float64)
+    e = lib.oracle_tree_sample_alt(DTYPE_CODE[dtype], _p(target), _p(dr) if dr is not None else None,
+                                   N, V, float(T), _p(tt) if tt is not None else None, _p(tk), _p(pa),
+                                   _p(rr), _p(uu), tol, int(b), 1 if flip else 0, _p(L), _p(path),
+                                   _p(out), _p(alpha), _p(mass), _p(fl), _p(dw), _p(dc))
+    return dict(accept_len=int(L[0]), path=path, out_tokens=out, alpha=alpha, mass=float(mass[0]),
+                req_flag=int(fl[0]), err=int(e), draw_w=dw, draw_cdf=dc)
+
+
 def tree_walk(parents, tokens, amax, lib=None) -> dict:
     lib = lib or load()
     pa, tk, am = _c(parents, np.int32), _c(tokens, np.int32), _c(amax, np.int32)
@@ -289,8 +340,11 @@ def verify_tree_greedy(dtype: str, target, B: int, N: int, V: int, node_tokens, 
     return o
 
 
-def tree_sample_probs(p, q, parents, tokens, r, u, tol: float = DEFAULT_TOL, lib=None) -> dict:
-    """One request of the stochastic tree walk from probability rows p, q [N+1][V]."""
+def tree_sample_probs(p, q, parents, tokens, r, u, tol: float = DEFAULT_TOL, lib=None,
+                      flip: bool = False) -> dict:
+    """One request of the stochastic tree walk from probability rows p, q [N+1][V]; with `flip`
+    the first flagged accept test is decided the other way.  Also returns the final draw's
+    weights `draw_w` and normalised CDF `draw_cdf` (zeros when the walk ends without a draw)."""
     lib = lib or load()
     p, q = _c(p, np.float64), _c(q, np.float64)
     N1, V = p.shape
@@ -298,10 +352,12 @@ def tree_sample_probs(p, q, parents, tokens, r, u, tol: float = DEFAULT_TOL, lib
     L, fl = np.zeros(1, np.int32), np.zeros(1, np.int32)
     path, out = np.zeros(N1, np.int32), np.zeros(N1, np.int32)
     alpha, mass = np.zeros(N1, np.float64), np.zeros(1, np.float64)
+    dw, dc = np.zeros(V, np.float64), np.zeros(V, np.float64)
     lib.oracle_tree_sample_probs(N1, V, _p(p), _p(q), _p(pa), _p(tk), _p(rr), float(u), tol,
-                                 _p(L), _p(path), _p(out), _p(alpha), _p(mass), _p(fl))
+                                 1 if flip else 0, _p(L), _p(path), _p(out), _p(alpha), _p(mass),
+                                 _p(fl), _p(dw), _p(dc))
     return dict(accept_len=int(L[0]), path=path, out_tokens=out, alpha=alpha,
-                mass=float(mass[0]), req_flag=int(fl[0]))
+                mass=float(mass[0]), req_flag=int(fl[0]), draw_w=dw, draw_cdf=dc)
 
 
 def verify_tree_sample(dtype: str, target, draft, B: int, N: int, V: int, T: float, node_tokens,

@@ -37,10 +37,15 @@
  *   R9  tree: from the root, move to the child whose token equals the argmax of the current
  *       node's row (lowest node index if several), until no child matches; the final token is
  *       the argmax of the last node's row.
- *   R10 flagged ties: |r_k - alpha_k| <= tol at an evaluated position, or u within tol of
- *       C_{i*-1}/S or C_{i*}/S at the drawn index i*.  For the draft-model residual
- *       max(0, p - q), whose total S < 1 comes from cancelling p against q, the band is tol / S
- *       (the resolution of that normalised CDF in fp32 arithmetic; tol at S = 1).
+ *   R10 flagged ties, in two tiers.  Strict (tol = 1e-6, the stated band): |r_k - alpha_k| <= tol
+ *       at an evaluated position, or u within tol of C_{i*-1}/S or C_{i*}/S at the drawn index
+ *       i*.  Widened (reported apart): for the draft-model residual max(0, p - q), whose total
+ *       S < 1 comes from cancelling p against q, its normalised CDF is resolved in fp32 only to
+ *       about tol / S, so a crossing within tol / S of u that is not within tol is flagged in a
+ *       second tier.  A flagged draw admits every positive-weight token whose CDF interval comes
+ *       within the band of u; oracle_chain_draw_rows gives the weights and the normalised CDF for
+ *       that check.  A flagged accept test admits either decision; for the tree walk
+ *       oracle_tree_sample_alt gives the outcome of the opposite decision.
  *   R11 invalid input: a draft token outside [0, V), a logits row holding NaN (or, when a softmax
  *       is taken, +inf, or only -inf), or a malformed parent array sets an error bit (every bit
  *       that applies, all rows checked); the request then accepts nothing and emits no token (-1).
@@ -55,8 +60,9 @@
 
 enum { OR_F32 = 0, OR_BF16 = 1, OR_F16 = 2 };
 
-/* per-request / per-position tie flags (R10, R5) */
-enum { ORF_ACCEPT_TIE = 1, ORF_CDF_TIE = 2, ORF_ZERO_RESIDUAL = 4 };
+/* per-request / per-position tie flags (R10, R5): strict tier, zero residual, widened tier */
+enum { ORF_ACCEPT_TIE = 1, ORF_CDF_TIE = 2, ORF_ZERO_RESIDUAL = 4, ORF_CDF_TIE_WIDE = 8,
+       ORF_ACCEPT_TIE_WIDE = 16 };
 /* per-request error bits (R11) */
 enum { ORE_BAD_TOKEN = 1, ORE_NONFINITE = 2, ORE_BAD_TREE = 8, ORE_BAD_TEMP = 16 };
 
@@ -181,6 +187,23 @@ int oracle_inverse_cdf(const double *w, int V, double u, double tol, double *S_o
  *   and the bonus draw at K), mass[K+1] (the residual mass S at k; sum of p at K),
  *   pos_flag[K+1] (CDF tie / zero-residual at k), req_flag (flags of the evaluated positions).
  */
+/* The weights of the draw at position k (p: [K+1][V], q: [K][V]): the step-3 residual
+ * max(0, p_k - q_k) at a draft position, p_K itself at the bonus row (R6). */
+static void draw_weights(int K, int V, const double *p, const double *q, int k, double *w)
+{
+    const double *pk = p + (size_t)k * V;
+    if (k < K) {
+        const double *qk = q + (size_t)k * V;
+        for (int i = 0; i < V; i++) { /* step 3 residual */
+            double d = pk[i] - qk[i];
+            w[i] = d > 0.0 ? d : 0.0;
+        }
+    } else {
+        for (int i = 0; i < V; i++) /* R6 bonus: draw from p */
+            w[i] = pk[i];
+    }
+}
+
 static void verify_probs_impl(int K, int V, const double *p, const double *q, const int *x,
                               const float *r, float u, double tol, int scale_band, int *n_acc,
                               int *out_tokens, double *alpha, int *cand, double *mass,
@@ -192,33 +215,28 @@ static void verify_probs_impl(int K, int V, const double *p, const double *q, co
         const double *pk = p + (size_t)k * V;
         int f = 0;
         if (k < K) {
-            const double *qk = q + (size_t)k * V;
-            double px = pk[x[k]], qx = qk[x[k]];
+            double px = pk[x[k]], qx = q[(size_t)k * V + x[k]];
             alpha[k] = (qx == 0.0 || px >= qx) ? 1.0 : px / qx; /* step 1, R2 */
-            for (int i = 0; i < V; i++) {                       /* step 3 residual */
-                double d = pk[i] - qk[i];
-                w[i] = d > 0.0 ? d : 0.0;
-            }
-        } else {
-            for (int i = 0; i < V; i++) /* R6 bonus: draw from p */
-                w[i] = pk[i];
         }
+        draw_weights(K, V, p, q, k, w);
         double S;
-        int fl;
+        int fl, flw = 0;
         int c = oracle_inverse_cdf(w, V, (double)u, tol, &S, &fl);
         mass[k] = S;
         if (c < 0) { /* R5: no residual mass left, draw from p instead */
             double S2;
             c = oracle_inverse_cdf(pk, V, (double)u, tol, &S2, &fl);
             f |= ORF_ZERO_RESIDUAL;
-        } else if (scale_band && k < K && S < 1.0) {
-            /* R10: the residual max(0, p - q) cancels where p and q overlap; its normalised CDF
-             * is resolved only to about tol / S, so the tie band widens to tol / S */
+        } else if (scale_band && k < K && S < 1.0 && !fl) {
+            /* R10, widened tier: the residual max(0, p - q) cancels where p and q overlap; its
+             * normalised CDF is resolved only to about tol / S */
             double S3;
-            oracle_inverse_cdf(w, V, (double)u, tol / S, &S3, &fl);
+            oracle_inverse_cdf(w, V, (double)u, tol / S, &S3, &flw);
         }
         if (fl)
             f |= ORF_CDF_TIE;
+        if (flw)
+            f |= ORF_CDF_TIE_WIDE;
         cand[k] = c;
         pos_flag[k] = f;
     }
@@ -442,6 +460,72 @@ void oracle_verify_ngram_direct(int K, int V, const double *p, const int *x, con
     free(w);
 }
 
+/* Cumulative sums of w in index order (as oracle_inverse_cdf sums them) divided by their total:
+ * cdf[i] = (w[0] + ... + w[i]) / S.  Returns S. */
+static double normalised_cdf(const double *w, int V, double *cdf)
+{
+    double S = 0.0, C = 0.0;
+    for (int i = 0; i < V; i++)
+        S += w[i];
+    for (int i = 0; i < V; i++) {
+        C += w[i];
+        cdf[i] = S > 0.0 ? C / S : 0.0;
+    }
+    return S;
+}
+
+/*
+ * The draws of request b, for checking a flagged tie (R10): for every position k = 0..K, the
+ * weights the draw at k uses, w[k][i] (the step-3 residual at a draft position, p_K at the bonus
+ * row, p_k itself when the residual is empty, R5), and cdf[k][i], their normalised cumulative
+ * sums.  Token t is drawn at k exactly when u lies in [cdf[k][t-1], cdf[k][t]) (cdf[k][-1] = 0).
+ * ngram != 0 takes q one-hot at the draft tokens (R8; draft unused).  T > 0.  Layout of the
+ * inputs as oracle_verify_chain; w and cdf are [K+1][V].  Returns the request's error bits (the
+ * outputs are unspecified when they are not 0).
+ */
+int oracle_chain_draw_rows(int dtype, const void *target, const void *draft, int ngram, int K,
+                           int V, float T, const int *x, int b, double *w_out, double *cdf_out)
+{
+    size_t rowsT = (size_t)(K + 1) * V, rowsD = (size_t)K * V;
+    double *l = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    double *p = (double *)malloc(sizeof(double) * (rowsT ? rowsT : 1));
+    double *q = (double *)malloc(sizeof(double) * (rowsD ? rowsD : 1));
+    const int *xb = x + (size_t)b * K;
+    int e = 0;
+    for (int k = 0; k < K; k++)
+        if (xb[k] < 0 || xb[k] >= V)
+            e |= ORE_BAD_TOKEN;
+    for (int k = 0; k <= K; k++) {
+        load_row(target, dtype, (size_t)b * (K + 1) + k, V, l);
+        e |= oracle_softmax(l, V, (double)T, p + (size_t)k * V);
+    }
+    for (size_t i = 0; i < rowsD; i++)
+        q[i] = 0.0;
+    for (int k = 0; k < K && !e; k++) {
+        if (ngram) {
+            q[(size_t)k * V + xb[k]] = 1.0;
+        } else {
+            load_row(draft, dtype, (size_t)b * K + k, V, l);
+            e |= oracle_softmax(l, V, (double)T, q + (size_t)k * V);
+        }
+    }
+    for (int k = 0; k <= K && !e; k++) {
+        double *w = w_out + (size_t)k * V;
+        draw_weights(K, V, p, q, k, w);
+        double S = 0.0;
+        for (int i = 0; i < V; i++)
+            S += w[i];
+        if (!(S > 0.0)) /* R5 */
+            for (int i = 0; i < V; i++)
+                w[i] = p[(size_t)k * V + i];
+        normalised_cdf(w, V, cdf_out + (size_t)k * V);
+    }
+    free(l);
+    free(p);
+    free(q);
+    return e;
+}
+
 /* ---------------------------------------------------------------------- greedy tree walk ---- */
 /* Parent array check: parents[0] == -1, 0 <= parents[i] < i; node tokens in [0, V) (root
  * excluded). */
@@ -560,10 +644,10 @@ void oracle_verify_tree_greedy(int dtype, const void *target, int B, int N, int 
  * or the node has none, the final token is drawn from the current p with the request's u (R4).
  * A chain (one child per node) is exactly the chain verification above.
  * R14: the mass R reported for a request is the product of the residual sums met at its final
- * node (1 when nothing was rejected there).  The tie band of an accept test, and of the final
- * draw, at mass R is tol / R (the resolution of the residual in fp32, as in R10).  A residual sum
- * that is not positive stops the sibling tests; the draw is then taken from the node's own p
- * (R5, flagged).
+ * node (1 when nothing was rejected there).  An accept test, and the final draw, is flagged in
+ * the strict tier within tol, and in the widened tier within tol / R (the resolution of the
+ * residual in fp32, as in R10) but not tol.  A residual sum that is not positive stops the
+ * sibling tests; the draw is then taken from the node's own p (R5, flagged).
  * R15: the walk reads only the rows of the nodes it visits (a node's draft row only when it has
  * children); a non-finite value in another row is not seen.  T == 0 is the greedy walk of R9,
  * with alpha = 1 for the matching child and 0 for the siblings tested before it.
@@ -585,11 +669,13 @@ static void tree_fail(int N1, int *accept_len, int *path, int *out_tokens, doubl
 }
 
 /* One request.  parents / tokens: [N1]; r: [N1] (r[c] is used when child c is tested; r[0] is
- * unused); outputs as oracle_verify_tree_sample.  Returns error bits (outputs failed when set). */
+ * unused); outputs as oracle_verify_tree_sample.  flip != 0 decides the first flagged accept test
+ * (either tier) the opposite way.  draw_w / draw_cdf (NULL to skip): [V], the final draw's weights
+ * and their normalised cumulative sums.  Returns error bits (outputs failed when set). */
 static int tree_sample_walk(int N1, int V, tree_rows_fn rows, void *ctx, const int *parents,
-                            const int *tokens, const float *r, float u, double tol,
+                            const int *tokens, const float *r, float u, double tol, int flip,
                             int *accept_len, int *path, int *out_tokens, double *alpha,
-                            double *mass, int *req_flag)
+                            double *mass, int *req_flag, double *draw_w, double *draw_cdf)
 {
     size_t n = (size_t)(V > 0 ? V : 1);
     double *p0 = (double *)malloc(sizeof(double) * n), *p = (double *)malloc(sizeof(double) * n);
@@ -620,9 +706,16 @@ static int tree_sample_walk(int N1, int V, tree_rows_fn rows, void *ctx, const i
             int x = tokens[c];
             double a = (q[x] == 0.0 || p[x] >= q[x]) ? 1.0 : p[x] / q[x]; /* step 1, R2 */
             alpha[c] = a;
-            if (fabs((double)r[c] - a) <= tol / R)
+            if (fabs((double)r[c] - a) <= tol)
                 *req_flag |= ORF_ACCEPT_TIE;
-            if ((double)r[c] <= a) { /* step 2: accepted */
+            else if (fabs((double)r[c] - a) <= tol / R)
+                *req_flag |= ORF_ACCEPT_TIE_WIDE;
+            int acc = (double)r[c] <= a; /* step 2: accepted */
+            if (flip && fabs((double)r[c] - a) <= tol / R) { /* the other decision of a flagged test */
+                acc = !acc;
+                flip = 0;
+            }
+            if (acc) {
                 next = c;
                 break;
             }
@@ -648,15 +741,26 @@ static int tree_sample_walk(int N1, int V, tree_rows_fn rows, void *ctx, const i
             continue;
         }
         double S2;
-        int fl, tok;
+        int fl, flw = 0, tok;
+        const double *wd = p;
         if (empty) { /* R14 / R5: nothing left of the residual, draw from the node's own p */
+            wd = p0;
             tok = oracle_inverse_cdf(p0, V, (double)u, tol, &S2, &fl);
             *req_flag |= ORF_ZERO_RESIDUAL;
         } else {
-            tok = oracle_inverse_cdf(p, V, (double)u, tol / R, &S2, &fl);
+            tok = oracle_inverse_cdf(p, V, (double)u, tol, &S2, &fl);
+            if (!fl && R < 1.0) /* R14, widened tier */
+                oracle_inverse_cdf(p, V, (double)u, tol / R, &S2, &flw);
         }
         if (fl)
             *req_flag |= ORF_CDF_TIE;
+        if (flw)
+            *req_flag |= ORF_CDF_TIE_WIDE;
+        if (draw_w) {
+            for (int i = 0; i < V; i++)
+                draw_w[i] = wd[i];
+            normalised_cdf(draw_w, V, draw_cdf);
+        }
         out_tokens[len] = tok;
         *mass = R;
         break;
@@ -687,16 +791,18 @@ static int probs_rows(void *ctx, int node, int need_q, double *p, double *q)
 
 /* Stochastic tree verification on probability rows p, q: [N1][V] (row n of q = the draft
  * distribution of node n's children).  Outputs: *accept_len, path[N1], out_tokens[N1],
- * alpha[N1] (alpha of each tested child, -1 elsewhere), *mass (R14), *req_flag. */
+ * alpha[N1] (alpha of each tested child, -1 elsewhere), *mass (R14), *req_flag.  flip and
+ * draw_w / draw_cdf as oracle_tree_sample_alt (0 and NULL for the walk itself). */
 void oracle_tree_sample_probs(int N1, int V, const double *p, const double *q,
                               const int *parents, const int *tokens, const float *r, float u,
-                              double tol, int *accept_len, int *path, int *out_tokens,
-                              double *alpha, double *mass, int *req_flag)
+                              double tol, int flip, int *accept_len, int *path, int *out_tokens,
+                              double *alpha, double *mass, int *req_flag, double *draw_w,
+                              double *draw_cdf)
 {
     struct probs_ctx c = {V, p, q};
     *mass = 0.0;
-    tree_sample_walk(N1, V, probs_rows, &c, parents, tokens, r, u, tol, accept_len, path,
-                     out_tokens, alpha, mass, req_flag);
+    tree_sample_walk(N1, V, probs_rows, &c, parents, tokens, r, u, tol, flip, accept_len, path,
+                     out_tokens, alpha, mass, req_flag, draw_w, draw_cdf);
 }
 
 struct logits_ctx {
@@ -762,6 +868,41 @@ static int tree_greedy_visited(int dtype, const void *target, size_t row0, int N
     return e;
 }
 
+/* Request b of the walk (outputs for that request alone: path / out_tokens / alpha [N+1]; draw_w /
+ * draw_cdf [V] or NULL).  Returns the request's error bits. */
+static int tree_sample_request(int dtype, const void *target, const void *draft, int N, int V,
+                               float T, const float *temps, const int *node_tokens,
+                               const int *parents, const float *r, const float *u, double tol,
+                               int b, int flip, double *l, int *accept_len, int *o_path,
+                               int *o_tok, double *o_al, double *mass, int *req_flag,
+                               double *draw_w, double *draw_cdf)
+{
+    int N1 = N + 1;
+    const int *pb = parents + (size_t)b * N1, *tb = node_tokens + (size_t)b * N1;
+    int e = oracle_tree_check(N1, V, pb, tb);
+    float Tb = temps ? temps[b] : T;
+    *req_flag = 0;
+    *mass = 0.0;
+    if (!(Tb >= 0.0f) || isinf(Tb))
+        e = ORE_BAD_TEMP;
+    if (!e) {
+        if (Tb == 0.0f) {
+            e = tree_greedy_visited(dtype, target, (size_t)b * N1, N1, V, pb, tb, accept_len, o_path,
+                                    o_tok, o_al);
+            *mass = 1.0;
+        } else {
+            struct logits_ctx c = {dtype, V, (double)Tb, target, draft, (size_t)b * N1, l};
+            e = tree_sample_walk(N1, V, logits_rows, &c, pb, tb, r + (size_t)b * N1, u[b], tol, flip,
+                                 accept_len, o_path, o_tok, o_al, mass, req_flag, draw_w, draw_cdf);
+        }
+    }
+    if (e) {
+        tree_fail(N1, accept_len, o_path, o_tok, o_al, mass);
+        *req_flag = 0;
+    }
+    return e;
+}
+
 /*
  * Tree verification by walking (R13-R15).  target, draft: [B][N+1][V] (draft ignored when
  * T == 0); node_tokens, parents: [B][N+1]; r: [B][N+1]; u: [B].
@@ -780,35 +921,33 @@ void oracle_verify_tree_sample(int dtype, const void *target, const void *draft,
     int N1 = N + 1;
     double *l = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
     (void)B;
-    for (int b = b0; b < b1; b++) {
-        const int *pb = parents + (size_t)b * N1, *tb = node_tokens + (size_t)b * N1;
-        int *o_path = path + (size_t)b * N1, *o_tok = out_tokens + (size_t)b * N1;
-        double *o_al = alpha + (size_t)b * N1;
-        int e = oracle_tree_check(N1, V, pb, tb);
-        float Tb = temps ? temps[b] : T;
-        req_flag[b] = 0;
-        mass[b] = 0.0;
-        if (!(Tb >= 0.0f) || isinf(Tb))
-            e = ORE_BAD_TEMP;
-        if (!e) {
-            if (Tb == 0.0f) {
-                e = tree_greedy_visited(dtype, target, (size_t)b * N1, N1, V, pb, tb,
-                                        accept_len + b, o_path, o_tok, o_al);
-                mass[b] = 1.0;
-            } else {
-                struct logits_ctx c = {dtype, V, (double)Tb, target, draft, (size_t)b * N1, l};
-                e = tree_sample_walk(N1, V, logits_rows, &c, pb, tb, r + (size_t)b * N1, u[b],
-                                     tol, accept_len + b, o_path, o_tok, o_al, mass + b,
-                                     req_flag + b);
-            }
-        }
-        if (e) {
-            tree_fail(N1, accept_len + b, o_path, o_tok, o_al, mass + b);
-            req_flag[b] = 0;
-        }
-        err[b] = e;
-    }
+    for (int b = b0; b < b1; b++)
+        err[b] = tree_sample_request(dtype, target, draft, N, V, T, temps, node_tokens, parents, r,
+                                     u, tol, b, 0, l, accept_len + b, path + (size_t)b * N1,
+                                     out_tokens + (size_t)b * N1, alpha + (size_t)b * N1, mass + b,
+                                     req_flag + b, NULL, NULL);
     free(l);
+}
+
+/*
+ * Request b of oracle_verify_tree_sample (same inputs; outputs for that request alone), for
+ * checking a flagged tie (R10, R14): with flip != 0 the first flagged accept test is decided the
+ * opposite way (the walk's other admissible outcome), and draw_w / draw_cdf ([V], or NULL)
+ * receive the final draw's weights and their normalised cumulative sums when the request ends in
+ * a draw (T > 0, no error).  Returns the request's error bits.
+ */
+int oracle_tree_sample_alt(int dtype, const void *target, const void *draft, int N, int V,
+                           float T, const float *temps, const int *node_tokens,
+                           const int *parents, const float *r, const float *u, double tol, int b,
+                           int flip, int *accept_len, int *path, int *out_tokens, double *alpha,
+                           double *mass, int *req_flag, double *draw_w, double *draw_cdf)
+{
+    double *l = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    int e = tree_sample_request(dtype, target, draft, N, V, T, temps, node_tokens, parents, r, u,
+                                tol, b, flip, l, accept_len, path, out_tokens, alpha, mass,
+                                req_flag, draw_w, draw_cdf);
+    free(l);
+    return e;
 }
 
 /* ------------------------------------------------------------- prompt n-gram lookup draft ---- */

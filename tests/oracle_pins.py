@@ -46,6 +46,7 @@ def pin_hand_chain_cases(lib):
             assert np.allclose(o["mass"], case["mass"], rtol=0, atol=1e-15), (tag, o["mass"])
             assert bool(o["req_flag"] & oracle.FLAG_ACCEPT_TIE) == run["accept_tie"], (tag, o)
             assert bool(o["req_flag"] & oracle.FLAG_CDF_TIE) == run["cdf_tie"], (tag, o)
+            assert bool(o["req_flag"] & oracle.FLAG_CDF_TIE_WIDE) == run.get("cdf_tie_wide", False), (tag, o)
             if "cand" in run:
                 assert list(o["cand"]) == run["cand"], (tag, o["cand"])
                 zr = [bool(f & oracle.FLAG_ZERO_RESIDUAL) for f in o["pos_flag"]]
@@ -403,20 +404,26 @@ FAST_PINS.append(pin_error_bits_accumulate)
 
 
 def pin_residual_band_scales_with_mass(lib):
-    """Reading R10: the tie band of the max(0, p - q) draw is tol / S (tol when S = 1)."""
+    """Reading R10: the max(0, p - q) draw is flagged in the strict tier within tol of a CDF
+    boundary, and in the widened tier within tol / S but not tol (tol when S = 1)."""
     p = np.array([[0.6, 0.4], [0.5, 0.5]])
     q = np.array([[0.5, 0.5]])  # residual [0.1, 0]: S = 0.1, C/S = [1, 1]
     x, r = [1], [0.9375]  # alpha = 0.8, rejected
-    for u, tie in [(2e-6, True), (5e-7, True), (2e-5, False), (0.5, False)]:
+    for u, strict, wide in [(2e-6, False, True), (9e-6, False, True), (5e-7, True, False),
+                            (2e-5, False, False), (0.5, False, False)]:
         o = oracle.verify_probs(p, q, x, r, u, TOL, lib=lib)
         assert o["num_accepted"] == 0 and o["out_tokens"][0] == 0
         assert abs(o["mass"][0] - 0.1) < 1e-15
-        assert bool(o["req_flag"] & oracle.FLAG_CDF_TIE) == tie, (u, o)
-    # disjoint supports: S = 1, the band stays tol
+        assert bool(o["req_flag"] & oracle.FLAG_CDF_TIE) == strict, (u, o)
+        assert bool(o["req_flag"] & oracle.FLAG_CDF_TIE_WIDE) == wide, (u, o)
+    # disjoint supports: S = 1, the band stays tol and no widened tier exists
     p2 = np.array([[1.0, 0.0], [0.5, 0.5]])
     q2 = np.array([[0.0, 1.0]])
     o = oracle.verify_probs(p2, q2, [1], [0.5], 2e-6, TOL, lib=lib)
-    assert not (o["req_flag"] & oracle.FLAG_CDF_TIE)
+    assert not (o["req_flag"] & (oracle.FLAG_CDF_TIE | oracle.FLAG_CDF_TIE_WIDE))
+    # the n-gram residual (p with x removed) takes no widened tier either
+    o = oracle.verify_ngram_direct(np.array([[0.25, 0.75], [0.5, 0.5]]), [1], [0.9375], 2e-6, TOL, lib=lib)
+    assert o["num_accepted"] == 0 and not (o["req_flag"] & oracle.FLAG_CDF_TIE_WIDE)
 
 
 FAST_PINS.append(pin_residual_band_scales_with_mass)
@@ -438,6 +445,22 @@ def pin_hand_tree_sample_cases(lib):
             assert abs(o["mass"] - run["mass"]) <= 1e-15, (tag, o["mass"])
             assert bool(o["req_flag"] & oracle.FLAG_ACCEPT_TIE) == run["accept_tie"], (tag, o)
             assert bool(o["req_flag"] & oracle.FLAG_CDF_TIE) == run["cdf_tie"], (tag, o)
+            assert bool(o["req_flag"] & oracle.FLAG_ACCEPT_TIE_WIDE) == run.get("accept_tie_wide", False), (tag, o)
+            assert bool(o["req_flag"] & oracle.FLAG_CDF_TIE_WIDE) == run.get("cdf_tie_wide", False), (tag, o)
+            if "draw_w" in run:  # the final draw's weights, and their cumulative sums over the total
+                assert np.allclose(o["draw_w"], run["draw_w"], rtol=0, atol=1e-15), (tag, o["draw_w"])
+                w = np.asarray(run["draw_w"])
+                assert np.allclose(o["draw_cdf"], np.cumsum(w) / w.sum(), rtol=0, atol=1e-15), (tag, o)
+            f = oracle.tree_sample_probs(p, q, case["parents"], case["tokens"], run["r"], run["u"],
+                                         TOL, lib=lib, flip=True)
+            if "flipped" in run:  # the other decision of the flagged test, worked by hand
+                alt = run["flipped"]
+                assert f["accept_len"] == alt["accept_len"], (tag, f)
+                assert list(f["path"]) == alt["path"] and list(f["out_tokens"]) == alt["out_tokens"], (tag, f)
+                assert np.allclose(f["draw_w"], alt["draw_w"], rtol=0, atol=1e-15), (tag, f["draw_w"])
+                assert bool(f["req_flag"] & oracle.FLAG_CDF_TIE) == alt["cdf_tie"], (tag, f)
+            elif not (run["accept_tie"] or run.get("accept_tie_wide", False)):  # nothing to flip
+                assert f["accept_len"] == o["accept_len"] and list(f["out_tokens"]) == list(o["out_tokens"]), tag
 
 
 def pin_tree_sample_chain_reduction(lib, n_cases=60):
@@ -712,3 +735,103 @@ def pin_tree_walk_per_request_temperature(lib):
 
 
 FAST_PINS.append(pin_tree_walk_per_request_temperature)
+
+
+def pin_chain_draw_rows(lib):
+    """The draw rows given for checking flagged ties: at a draft position the step-3 residual
+    max(0, p_k - q_k) of section I.1 (n-gram: p_k with x_k removed, q one-hot), at the bonus row
+    p_K, and p_k itself where the residual is empty (R5), with p and q from scipy's softmax; the
+    cdf is their cumulative sum over the total (numpy); and the inverse CDF over each row at u is
+    the position's candidate in the verification call."""
+    from scipy.special import softmax as sp_softmax
+
+    rng = np.random.default_rng(61)
+    for i in range(40):
+        B, K, V = 2, int(rng.integers(0, 5)), int(rng.integers(2, 40))
+        T = float(np.float32(rng.choice([0.6, 1.0, 1.5])))  # the temperature the calls take (fp32)
+        lt = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
+        ld = (lt[:, :K] + rng.normal(0, 1, (B, K, V))).astype(np.float32)
+        if i % 4 == 0 and K:
+            ld[1, 0] = lt[1, 0]  # q = p at a position: the residual is empty there
+        x = rng.integers(0, V, (B, K)).astype(np.int32)
+        r = ((rng.integers(0, 1 << 24, (B, K)) + 1) / float(1 << 24)).astype(np.float32)
+        u = (rng.integers(0, 1 << 24, B) / float(1 << 24)).astype(np.float32)
+        for ngram in (False, True):
+            if ngram:
+                o = oracle.verify_ngram("f32", lt, B, K, V, T, x, r, u, lib=lib)
+            else:
+                o = oracle.verify_chain("f32", lt, ld, B, K, V, T, x, r, u, lib=lib)
+            for b in range(B):
+                w, cdf, e = oracle.chain_draw_rows("f32", lt, ld, B, K, V, T, x, b, ngram=ngram, lib=lib)
+                assert e == 0
+                p = sp_softmax(lt[b].astype(np.float64) / T, axis=-1)
+                q = np.zeros((K, V))
+                if ngram:
+                    q[np.arange(K), x[b]] = 1.0
+                else:
+                    q = sp_softmax(ld[b].astype(np.float64) / T, axis=-1)
+                for k in range(K + 1):
+                    ref = np.maximum(0.0, p[k] - q[k]) if k < K else p[k]
+                    if not ref.sum() > 0:
+                        ref = p[k]
+                    assert np.allclose(w[k], ref, rtol=0, atol=1e-12), (i, ngram, b, k)
+                    assert np.allclose(cdf[k], np.cumsum(w[k]) / w[k].sum(), rtol=0, atol=1e-12)
+                    if not o["pos_flag"][b][k] & (oracle.FLAG_CDF_TIE | oracle.FLAG_CDF_TIE_WIDE):
+                        assert o["cand"][b][k] == _brute_inverse_cdf(w[k], float(u[b])), (i, ngram, b, k)
+
+
+FAST_PINS.append(pin_chain_draw_rows)
+
+
+def pin_tree_sample_alt(lib):
+    """The walk's outcome for one request without a flip is the walk itself (and its draw row is
+    the last node's p, from scipy's softmax, when nothing was rejected there); with the first
+    flagged accept test decided the other way it is, on a one-child tree, the chain verification
+    (pinned on its own) with that position's r moved to the other side of alpha."""
+    from scipy.special import softmax as sp_softmax
+
+    rng = np.random.default_rng(67)
+    done = 0
+    for i in range(200):
+        K, V = int(rng.integers(1, 6)), int(rng.integers(2, 12))
+        T = float(np.float32(rng.choice([0.5, 1.0, 1.7])))
+        lt = rng.normal(0, 2, (1, K + 1, V)).astype(np.float32)
+        ld = (lt[:, :K] + rng.normal(0, 1, (1, K, V))).astype(np.float32)
+        x = rng.integers(0, V, (1, K)).astype(np.int32)
+        parents = np.arange(-1, K, dtype=np.int32)[None]
+        tokens = np.concatenate([[[0]], x], axis=1).astype(np.int32)
+        dt = np.concatenate([ld, np.zeros((1, 1, V), np.float32)], axis=1)
+        u = (rng.integers(0, 1 << 24, 1) / float(1 << 24)).astype(np.float32)
+        j = int(rng.integers(0, K))  # the position whose test is put on alpha
+        rt = np.full((1, K + 1), 2.0 ** -24, np.float32)
+        rt[0, j + 2:] = ((rng.integers(0, 1 << 24, K - j - 1) + 1) / float(1 << 24)).astype(np.float32)
+        base = oracle.verify_tree_sample("f32", lt, dt, 1, K, V, T, tokens, parents, rt, u, lib=lib)
+        a = float(base["alpha"][0][j + 1])
+        if not (0.01 < a < 0.99):
+            continue
+        rt[0, j + 1] = np.float32(a)  # within tol of alpha: a flagged test
+        o = oracle.verify_tree_sample("f32", lt, dt, 1, K, V, T, tokens, parents, rt, u, lib=lib)
+        assert o["req_flag"][0] & oracle.FLAG_ACCEPT_TIE
+        same = oracle.tree_sample_alt("f32", lt, dt, 1, K, V, T, tokens, parents, rt, u, 0, False, lib=lib)
+        for k in ("accept_len", "mass", "req_flag"):
+            assert same[k] == o[k][0], (i, k)
+        assert list(same["out_tokens"]) == list(o["out_tokens"][0]) and list(same["path"]) == list(o["path"][0])
+        L = same["accept_len"]
+        if L == K or same["mass"] == 1.0:  # nothing rejected at the last node: the draw row is its p
+            pl = sp_softmax(lt[0, L].astype(np.float64) / T)
+            assert np.allclose(same["draw_w"], pl, rtol=0, atol=1e-12)
+            assert np.allclose(same["draw_cdf"], np.cumsum(pl) / pl.sum(), rtol=0, atol=1e-12)
+        f = oracle.tree_sample_alt("f32", lt, dt, 1, K, V, T, tokens, parents, rt, u, 0, True, lib=lib)
+        accepted = float(rt[0, j + 1]) <= a
+        rc = rt[:, 1:].copy()
+        rc[0, j] = np.float32(a + 1e-3) if accepted else np.float32(a - 1e-3)  # the other decision
+        ch = oracle.verify_chain("f32", lt, ld, 1, K, V, T, x, rc, u, lib=lib)
+        n = int(ch["num_accepted"][0])
+        assert f["accept_len"] == n and n == (j if accepted else max(j + 1, n)), (i, f, ch)
+        assert list(f["out_tokens"]) == list(ch["out_tokens"][0]), (i, f, ch)
+        assert list(f["path"][: n + 1]) == list(range(n + 1))
+        done += 1
+    assert done >= 50, done
+
+
+FAST_PINS.append(pin_tree_sample_alt)

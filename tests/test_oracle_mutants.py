@@ -21,8 +21,8 @@ MUTANTS = [
     ("accept_test_dropped", "if ((double)r[n] <= alpha[n])", "if (1)"),
     ("residual_sign_flipped", "double d = pk[i] - qk[i];", "double d = qk[i] - pk[i];"),
     ("residual_not_clamped", "w[i] = d > 0.0 ? d : 0.0;", "w[i] = d;"),
-    ("bonus_from_first_row", "/* R6 bonus: draw from p */\n                w[i] = pk[i];",
-     "/* R6 bonus: draw from p */\n                w[i] = p[i];"),
+    ("bonus_from_first_row", "/* R6 bonus: draw from p */\n            w[i] = pk[i];",
+     "/* R6 bonus: draw from p */\n            w[i] = p[i];"),
     ("softmax_temperature_dropped", "p[i] = exp((l[i] - m) / T);", "p[i] = exp(l[i] - m);"),
     ("softmax_temperature_multiplied", "p[i] = exp((l[i] - m) / T);", "p[i] = exp((l[i] - m) * T);"),
     ("softmax_not_normalised", "p[i] = p[i] / Z;", "p[i] = p[i];"),
@@ -42,18 +42,24 @@ MUTANTS = [
     ("f16_subnormal_scale", "ldexp((double)man, -24)", "ldexp((double)man, -25)"),
     ("ngram_onehot_weight", "q[(size_t)k * V + xb[k]] = 1.0;", "q[(size_t)k * V + xb[k]] = 0.5;"),
     ("greedy_compares_next_row", "while (n < K && x[n] == cand[n])", "while (n < K && x[n] == cand[n + 1])"),
-    ("residual_band_not_scaled", "oracle_inverse_cdf(w, V, (double)u, tol / S, &S3, &fl);",
-     "oracle_inverse_cdf(w, V, (double)u, tol, &S3, &fl);"),
+    ("residual_band_not_scaled", "oracle_inverse_cdf(w, V, (double)u, tol / S, &S3, &flw);",
+     "oracle_inverse_cdf(w, V, (double)u, tol, &S3, &flw);"),
+    ("residual_wide_tier_dropped", "        if (flw)\n            f |= ORF_CDF_TIE_WIDE;", ""),
     ("tree_sample_no_residual_update", "p[i] = w[i] / S;", "p[i] = p[i];"),
     ("tree_sample_residual_not_normalised", "p[i] = w[i] / S;", "p[i] = w[i];"),
     ("tree_sample_residual_sign_flipped", "double d = p[i] - q[i];", "double d = q[i] - p[i];"),
     ("tree_sample_alpha_inverted", "1.0 : p[x] / q[x]; /* step 1, R2 */", "1.0 : q[x] / p[x]; /* step 1, R2 */"),
-    ("tree_sample_draw_from_node_p", "tok = oracle_inverse_cdf(p, V, (double)u, tol / R, &S2, &fl);",
-     "tok = oracle_inverse_cdf(p0, V, (double)u, tol / R, &S2, &fl);"),
-    ("tree_sample_band_not_scaled", "if (fabs((double)r[c] - a) <= tol / R)", "if (fabs((double)r[c] - a) <= tol)"),
+    ("tree_sample_draw_from_node_p", "tok = oracle_inverse_cdf(p, V, (double)u, tol, &S2, &fl);",
+     "tok = oracle_inverse_cdf(p0, V, (double)u, tol, &S2, &fl);"),
+    ("tree_sample_draw_band_not_scaled", "oracle_inverse_cdf(p, V, (double)u, tol / R, &S2, &flw);",
+     "oracle_inverse_cdf(p, V, (double)u, tol, &S2, &flw);"),
+    ("tree_sample_band_not_scaled", "else if (fabs((double)r[c] - a) <= tol / R)",
+     "else if (fabs((double)r[c] - a) <= tol)"),
+    ("tree_sample_strict_band_scaled", "if (fabs((double)r[c] - a) <= tol)\n                *req_flag |= ORF_ACCEPT_TIE;",
+     "if (fabs((double)r[c] - a) <= tol / R)\n                *req_flag |= ORF_ACCEPT_TIE;"),
     ("tree_sample_mass_not_accumulated", "R *= S;", "R = S;"),
-    ("tree_sample_accept_strict_less", "if ((double)r[c] <= a) { /* step 2: accepted */",
-     "if ((double)r[c] < a) { /* step 2: accepted */"),
+    ("tree_sample_accept_strict_less", "int acc = (double)r[c] <= a; /* step 2: accepted */",
+     "int acc = (double)r[c] < a; /* step 2: accepted */"),
     ("tree_greedy_walk_final_token", "out_tokens[len] = a;\n            break;",
      "out_tokens[len] = tokens[cur];\n            break;"),
     ("ngram_draft_earliest_occurrence", "for (int i = L - n - 1; i >= 0; i--) {",
@@ -69,6 +75,11 @@ MUTANTS = [
      "for (int j = 1; j < L; j++) /* read every accepted row before any slot is written */"),
     ("kv_compact_path_check_dropped", "ok = pt[j] > 0 && pt[j] < N1 && pa[pt[j]] == pt[j - 1];", "ok = 1;"),
     ("tree_walk_per_request_temperature_ignored", "float Tb = temps ? temps[b] : T;", "float Tb = T;"),
+    ("draw_rows_no_empty_residual_fallback", "if (!(S > 0.0)) /* R5 */", "if (0) /* R5 */"),
+    ("draw_cdf_not_normalised", "cdf[i] = S > 0.0 ? C / S : 0.0;", "cdf[i] = C;"),
+    ("walk_draw_row_from_node_p", "const double *wd = p;", "const double *wd = p0;"),
+    ("walk_flip_not_applied", "acc = !acc;", "acc = acc;"),
+    ("walk_flip_any_test", "if (flip && fabs((double)r[c] - a) <= tol / R) {", "if (flip) {"),
     ("bad_token_check_dropped", "if (xb[k] < 0 || xb[k] >= V)\n                e |= ORE_BAD_TOKEN;",
      "if (0)\n                e |= ORE_BAD_TOKEN;"),
 ]
