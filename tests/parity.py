@@ -3,10 +3,13 @@ path through the C ABI (via the binding), run the oracle on the same host arrays
 
 The comparison rules follow the parity contract:
   * error bits, greedy results and tree results: bit-exact;
-  * accepted lengths and emitted tokens: bit-exact unless the oracle puts the request in the
-    flagged-tie set (|r - alpha| within 1e-6, or a CDF crossing within the tie band of u);
-    flagged requests must still produce one of the valid outcomes;
-  * per-position candidates: bit-exact unless that position's CDF crossing is flagged;
+  * accepted lengths and emitted tokens: bit-exact, except in the flagged-tie set, which the
+    oracle reports in two tiers (strict: |r - alpha| or a CDF crossing within 1e-6 of the uniform;
+    widened: within 1e-6 / S of a residual of total S < 1, not within 1e-6).  There an accept test
+    admits either decision (for a walk, the oracle's outcome with that test decided the other way
+    must then match), and a draw admits a positive-weight token whose CDF interval comes within
+    the band of u, as the oracle's weights and CDF of that draw decide;
+  * per-position candidates: likewise;
   * probabilities (alpha, residual masses, optional p / q rows): within 1e-5 absolute.
 """
 
@@ -73,52 +76,134 @@ def run_gpu_chain(ci, ngram: bool = False, probs: bool = False, workspace=None, 
 
 def run_oracle_chain(ci, ngram: bool = False, threads: int = 8, requests=None) -> dict:
     if ngram:
-        return oracle.verify_ngram(ci.dtype, ci.target, ci.B, ci.K, ci.V, float(ci.temperature),
-                                   ci.draft_tokens, ci.r, ci.u, threads=threads, requests=requests)
-    return oracle.verify_chain(ci.dtype, ci.target, ci.draft, ci.B, ci.K, ci.V,
-                               float(ci.temperature), ci.draft_tokens, ci.r, ci.u, threads=threads,
-                               requests=requests)
+        o = oracle.verify_ngram(ci.dtype, ci.target, ci.B, ci.K, ci.V, float(ci.temperature),
+                                ci.draft_tokens, ci.r, ci.u, threads=threads, requests=requests)
+    else:
+        o = oracle.verify_chain(ci.dtype, ci.target, ci.draft, ci.B, ci.K, ci.V,
+                                float(ci.temperature), ci.draft_tokens, ci.r, ci.u, threads=threads,
+                                requests=requests)
+    o["ngram"] = ngram
+    return o
 
 
-def compare_chain(g: dict, o: dict, ci, requests=None) -> dict:
-    """Asserts parity of a chain / n-gram call; returns counts (flagged-tie set size etc.)."""
+def draw_admissible(w: np.ndarray, cdf: np.ndarray, u: float, t: int, band: float) -> bool:
+    """Token t is an admissible outcome of a draw with weights w and normalised CDF cdf (the
+    oracle's): it has positive weight and its interval [cdf[t-1], cdf[t]) of u comes within `band`
+    of the uniform u that was used."""
+    if not (0 <= t < w.size) or not w[t] > 0:
+        return False
+    lo = cdf[t - 1] if t > 0 else 0.0
+    return lo - band <= u <= cdf[t] + band
+
+
+def _tie_band(mass: float, widened: bool) -> float:
+    """The band of a flagged draw: 1e-6, or 1e-6 / S where reading R10 / R14 widens it (a residual
+    of total S < 1)."""
+    return TIE_TOL / mass if (widened and 0.0 < mass < 1.0) else TIE_TOL
+
+
+def check_chain(g: dict, o: dict, ci, requests=None) -> dict:
+    """Parity of a chain / n-gram call without asserting: returns counts and a list of failures.
+
+    Error bits, alpha (1e-5) and residual masses (1e-5) must match.  A request's accepted length
+    must follow the oracle's decisions, except that an accept test within 1e-6 of alpha admits
+    either decision.  Its emitted token must be the oracle's candidate at that position, or, where
+    the oracle flags the draw as a tie, a positive-weight token whose CDF interval comes within
+    the tie band of u (the oracle's weights and CDF of that draw decide)."""
     idx = np.arange(ci.B) if requests is None else np.arange(*requests)
-    K = ci.K
-    greedy = float(ci.temperature) == 0.0
+    K, V = ci.K, ci.V
+    T = float(ci.temperature)
+    greedy = T == 0.0
+    ngram = bool(o.get("ngram", False))
+    fails = []
     err_o, err_g = o["err"][idx], g["err_flags"][idx]
-    assert np.array_equal(err_o, err_g), ("error bits differ", np.nonzero(err_o != err_g)[0][:10])
+    if not np.array_equal(err_o, err_g):
+        fails.append(("error bits differ", np.nonzero(err_o != err_g)[0][:10].tolist()))
     ok = err_o == 0
     bad = idx[~ok]
-    assert (g["num_accepted"][bad] == 0).all() and (g["out_tokens"][bad] == -1).all()
+    if not ((g["num_accepted"][bad] == 0).all() and (g["out_tokens"][bad] == -1).all()):
+        fails.append(("failed requests emit something", bad[:10].tolist()))
     good = idx[ok]
     if K:
         da = np.abs(g["accept_prob"][good] - o["alpha"][good])
-        assert da.size == 0 or da.max() <= (0 if greedy else PROB_TOL), ("alpha", da.max())
-    cdf_flag = (o["pos_flag"][good] & oracle.FLAG_CDF_TIE) != 0
+        if da.size and da.max() > (0 if greedy else PROB_TOL):
+            fails.append(("alpha", float(da.max())))
+    cdf_flag = (o["pos_flag"][good] & (oracle.FLAG_CDF_TIE | oracle.FLAG_CDF_TIE_WIDE)) != 0
     if "pos_mass" in g:
         dm = np.abs(g["pos_mass"][good] - o["mass"][good])
-        assert dm.size == 0 or dm.max() <= PROB_TOL, ("position mass", dm.max())
-        cm = (g["cand_tokens"][good] != o["cand"][good]) & ~cdf_flag
-        assert not cm.any(), ("candidate tokens differ", np.argwhere(cm)[:10])
-    flagged = (o["req_flag"][good] & (oracle.FLAG_ACCEPT_TIE | oracle.FLAG_CDF_TIE)) != 0
-    ex = good[~flagged]
-    assert np.array_equal(g["num_accepted"][ex], o["num_accepted"][ex]), "accepted lengths differ"
-    assert np.array_equal(g["out_tokens"][ex], o["out_tokens"][ex]), "emitted tokens differ"
+        if dm.size and dm.max() > PROB_TOL:
+            fails.append(("position mass", float(dm.max())))
+    rf = o["req_flag"][good]
+    strict = (rf & oracle.FLAGS_STRICT) != 0
+    wide_only = ((rf & oracle.FLAGS_WIDE) != 0) & ~strict
     n_g = g["num_accepted"][good]
-    dmass = np.abs(g["residual_mass"][good] - o["mass"][good, n_g])
-    assert dmass.size == 0 or dmass.max() <= PROB_TOL, ("residual mass", dmass.max())
-    for b in good[flagged]:  # flagged ties: any valid outcome
+    dmass = np.abs(g["residual_mass"][good] - o["mass"][good, np.minimum(n_g, K)])
+    if dmass.size and dmass.max() > PROB_TOL:
+        fails.append(("residual mass", float(dmass.max())))
+    rows = {}
+
+    def draw_rows(b):
+        if b not in rows:
+            rows[b] = oracle.chain_draw_rows(ci.dtype, ci.target, ci.draft, ci.B, K, V, T,
+                                             ci.draft_tokens, int(b), ngram=ngram)
+        return rows[b]
+
+    def admissible(b, k, t):
+        """Token t at position k of request b: the candidate, or an admissible tie outcome."""
+        if t == o["cand"][b][k]:
+            return True, False
+        if greedy or not (o["pos_flag"][b][k] & (oracle.FLAG_CDF_TIE | oracle.FLAG_CDF_TIE_WIDE)):
+            return False, False
+        w, cdf, e = draw_rows(b)
+        widened = (not ngram) and k < K
+        band = _tie_band(float(o["mass"][b][k]), widened)
+        return (e == 0 and draw_admissible(w[k], cdf[k], float(ci.u[b]), int(t), band)), True
+
+    deviations = 0
+    cand_dev = 0
+    if "cand_tokens" in g:
+        for b in good:
+            for k in range(K + 1):
+                t = int(g["cand_tokens"][b][k])
+                good_t, dev = admissible(b, k, t)
+                if not good_t:
+                    fails.append(("candidate token", int(b), k, t, int(o["cand"][b][k])))
+                cand_dev += int(dev)
+    for b in good:
         n = int(g["num_accepted"][b])
-        a, r = o["alpha"][b], ci.r[b]
-        assert all(r[k] <= a[k] + TIE_TOL for k in range(n))
-        assert n == K or r[n] > a[n] - TIE_TOL
         out = g["out_tokens"][b]
-        assert list(out[:n]) == list(ci.draft_tokens[b][:n])
-        assert 0 <= out[n] < ci.V
-        assert (out[n + 1:] == -1).all()
-    return dict(requests=int(idx.size), errors=int((~ok).sum()), flagged=int(flagged.sum()),
-                cdf_flagged_positions=int(cdf_flag.sum()),
-                mean_accepted=float(n_g.mean()) if n_g.size else 0.0)
+        a, r = o["alpha"][b], ci.r[b]
+        if greedy:
+            if n != o["num_accepted"][b] or not np.array_equal(out, o["out_tokens"][b]):
+                fails.append(("greedy outcome differs", int(b)))
+            continue
+
+        def tie(k):
+            return abs(float(r[k]) - float(a[k])) <= TIE_TOL
+
+        if not (0 <= n <= K and all(float(r[k]) <= a[k] or tie(k) for k in range(n))
+                and (n == K or float(r[n]) > a[n] or tie(n))):
+            fails.append(("accepted length not admissible", int(b), n, int(o["num_accepted"][b])))
+            continue
+        if list(out[:n]) != list(ci.draft_tokens[b][:n]) or not (out[n + 1:] == -1).all():
+            fails.append(("accepted prefix or padding differs", int(b)))
+            continue
+        good_t, dev = admissible(b, n, int(out[n]))
+        if not good_t:
+            fails.append(("emitted token not admissible", int(b), n, int(out[n]), int(o["cand"][b][n])))
+        deviations += int(dev or n != o["num_accepted"][b])
+    return dict(requests=int(idx.size), errors=int((~ok).sum()), flagged=int((strict | wide_only).sum()),
+                flagged_strict=int(strict.sum()), flagged_wide_only=int(wide_only.sum()),
+                admissible_deviations=deviations, cdf_flagged_positions=int(cdf_flag.sum()),
+                candidate_deviations=cand_dev,
+                mean_accepted=float(n_g.mean()) if n_g.size else 0.0, failures=fails)
+
+
+def compare_chain(g: dict, o: dict, ci, requests=None) -> dict:
+    """Asserts parity of a chain / n-gram call (see check_chain); returns the counts."""
+    st = check_chain(g, o, ci, requests)
+    assert not st["failures"], st["failures"][:10]
+    return st
 
 
 def run_gpu_tree(ti, workspace=None) -> dict:
@@ -168,41 +253,92 @@ def run_gpu_walk(ti, temperature=None, temperatures=None) -> dict:
 def run_oracle_walk(ti, temperature=None, threads: int = 8, temperatures=None) -> dict:
     T = float(ti.temperature if temperature is None else temperature)
     sampled = T > 0 or temperatures is not None
-    return oracle.verify_tree_sample(ti.dtype, ti.target, ti.draft if sampled else None, ti.B, ti.N,
-                                     ti.V, T, ti.node_tokens, ti.parents,
-                                     ti.r if sampled else None, ti.u if sampled else None,
-                                     threads=threads, temperatures=temperatures)
+    o = oracle.verify_tree_sample(ti.dtype, ti.target, ti.draft if sampled else None, ti.B, ti.N,
+                                  ti.V, T, ti.node_tokens, ti.parents,
+                                  ti.r if sampled else None, ti.u if sampled else None,
+                                  threads=threads, temperatures=temperatures)
+    o["temperature"], o["temperatures"] = T, temperatures  # (the settings the walk was run with)
+    return o
 
 
-def compare_walk(g: dict, o: dict, ti) -> dict:
-    """Parity of a tree walk: error bits exact; unflagged requests exact (path, tokens, the set of
-    children tested); alpha of the children tested and the residual mass within 1e-5; flagged
-    requests end on a valid path."""
-    assert np.array_equal(g["err_flags"], o["err"]), ("walk error bits differ",
-                                                      np.nonzero(g["err_flags"] != o["err"])[0][:10])
+def check_walk(g: dict, o: dict, ti, temperature=None, temperatures=None) -> dict:
+    """Parity of a tree walk without asserting: returns counts and a list of failures.
+
+    Error bits must match.  A request whose path is the oracle's must emit the oracle's tokens,
+    except that a draw the oracle flags as a tie admits a positive-weight token whose CDF interval
+    comes within the tie band of u; the children it tested, their alpha (1e-5) and its residual
+    mass (1e-5) must match.  A request whose path differs must be flagged for an accept tie and
+    match the oracle's walk with the first flagged test decided the other way (same rules)."""
+    if temperature is None:
+        temperature = o.get("temperature", ti.temperature)
+    if temperatures is None:
+        temperatures = o.get("temperatures")
+    T = float(temperature)
+    sampled = T > 0 or temperatures is not None
+    fails = []
+    if not np.array_equal(g["err_flags"], o["err"]):
+        fails.append(("walk error bits differ", np.nonzero(g["err_flags"] != o["err"])[0][:10].tolist()))
     ok = o["err"] == 0
     bad = np.nonzero(~ok)[0]
-    assert (g["accept_len"][bad] == 0).all() and (g["out_tokens"][bad] == -1).all()
-    assert (g["path_nodes"][bad] == -1).all() and (g["accept_prob"][bad] == -1).all()
-    flagged = (o["req_flag"] & (oracle.FLAG_ACCEPT_TIE | oracle.FLAG_CDF_TIE)) != 0
-    ex = np.nonzero(ok & ~flagged)[0]
-    assert np.array_equal(g["accept_len"][ex], o["accept_len"][ex]), "accepted lengths differ"
-    assert np.array_equal(g["path_nodes"][ex], o["path"][ex]), "paths differ"
-    assert np.array_equal(g["out_tokens"][ex], o["out_tokens"][ex]), "emitted tokens differ"
-    tested_g, tested_o = g["accept_prob"][ex] >= 0, o["alpha"][ex] >= 0
-    assert np.array_equal(tested_g, tested_o), "children tested differ"
-    da = np.abs(g["accept_prob"][ex] - o["alpha"][ex])[tested_o]
-    assert da.size == 0 or da.max() <= PROB_TOL, ("alpha", da.max())
-    dm = np.abs(g["residual_mass"][ex] - o["mass"][ex])
-    assert dm.size == 0 or dm.max() <= PROB_TOL, ("residual mass", dm.max())
-    for b in np.nonzero(ok & flagged)[0]:  # any valid outcome
+    if not ((g["accept_len"][bad] == 0).all() and (g["out_tokens"][bad] == -1).all()
+            and (g["path_nodes"][bad] == -1).all() and (g["accept_prob"][bad] == -1).all()):
+        fails.append(("failed requests emit something", bad[:10].tolist()))
+    rf = o["req_flag"]
+    strict = ok & ((rf & oracle.FLAGS_STRICT) != 0)
+    wide_only = ok & ((rf & oracle.FLAGS_WIDE) != 0) & ~strict
+    deviations, flipped, worst = 0, 0, 0.0
+
+    def alt(b, flip):
+        return oracle.tree_sample_alt(ti.dtype, ti.target, ti.draft if sampled else None, ti.B, ti.N,
+                                      ti.V, T, ti.node_tokens, ti.parents, ti.r if sampled else None,
+                                      ti.u if sampled else None, int(b), flip, temperatures=temperatures)
+
+    for b in np.nonzero(ok)[0]:
         L = int(g["accept_len"][b])
-        path = g["path_nodes"][b]
-        assert path[0] == 0 and (path[L + 1:] == -1).all()
-        for j in range(1, L + 1):
-            assert ti.parents[b][path[j]] == path[j - 1]
-            assert g["out_tokens"][b][j - 1] == ti.node_tokens[b][path[j]]
-        assert 0 <= g["out_tokens"][b][L] < ti.V and (g["out_tokens"][b][L + 1:] == -1).all()
-    return dict(requests=int(ok.size), errors=int((~ok).sum()), flagged=int(flagged.sum()),
+        ref = dict(accept_len=int(o["accept_len"][b]), path=o["path"][b], out_tokens=o["out_tokens"][b],
+                   alpha=o["alpha"][b], mass=float(o["mass"][b]), req_flag=int(rf[b]))
+        if L != ref["accept_len"] or not np.array_equal(g["path_nodes"][b], ref["path"]):
+            if not rf[b] & (oracle.FLAG_ACCEPT_TIE | oracle.FLAG_ACCEPT_TIE_WIDE):
+                fails.append(("path differs", int(b)))
+                continue
+            ref = alt(b, True)  # the other decision of the flagged test
+            flipped += 1
+            if L != ref["accept_len"] or not np.array_equal(g["path_nodes"][b], ref["path"]):
+                fails.append(("path differs from both outcomes of the flagged test", int(b)))
+                continue
+        out = g["out_tokens"][b]
+        if not np.array_equal(out[:L], ref["out_tokens"][:L]) or not (out[L + 1:] == -1).all():
+            fails.append(("accepted tokens or padding differ", int(b)))
+            continue
+        t = int(out[L])
+        if t != ref["out_tokens"][L]:
+            full = ref if "draw_w" in ref else alt(b, False)
+            flagged_draw = ref["req_flag"] & (oracle.FLAG_CDF_TIE | oracle.FLAG_CDF_TIE_WIDE)
+            if not (sampled and flagged_draw and draw_admissible(
+                    full["draw_w"], full["draw_cdf"], float(ti.u[b]), t, _tie_band(ref["mass"], True))):
+                fails.append(("emitted token not admissible", int(b), t, int(ref["out_tokens"][L])))
+                continue
+            deviations += 1
+        tested_g, tested_o = g["accept_prob"][b] >= 0, np.asarray(ref["alpha"]) >= 0
+        if not np.array_equal(tested_g, tested_o):
+            fails.append(("children tested differ", int(b)))
+            continue
+        da = np.abs(g["accept_prob"][b] - np.asarray(ref["alpha"]))[tested_o]
+        if da.size:
+            worst = max(worst, float(da.max()))
+            if da.max() > PROB_TOL:
+                fails.append(("alpha", int(b), float(da.max())))
+        if abs(float(g["residual_mass"][b]) - ref["mass"]) > PROB_TOL:
+            fails.append(("residual mass", int(b), float(g["residual_mass"][b]), ref["mass"]))
+    return dict(requests=int(ok.size), errors=int((~ok).sum()), flagged=int((strict | wide_only).sum()),
+                flagged_strict=int(strict.sum()), flagged_wide_only=int(wide_only.sum()),
+                admissible_deviations=deviations, flipped_accept_ties=flipped,
                 mean_accepted=float(g["accept_len"][ok].mean()) if ok.any() else 0.0,
-                max_alpha_diff=float(da.max()) if da.size else 0.0)
+                max_alpha_diff=worst, failures=fails)
+
+
+def compare_walk(g: dict, o: dict, ti, temperature=None, temperatures=None) -> dict:
+    """Asserts parity of a tree walk (see check_walk); returns the counts."""
+    st = check_walk(g, o, ti, temperature, temperatures)
+    assert not st["failures"], st["failures"][:10]
+    return st

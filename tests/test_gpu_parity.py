@@ -101,14 +101,23 @@ def test_chain_batched_reduced_with_probabilities(seed):
     _show(f"chain batched B=6 seed={seed}", st)
 
 
-@pytest.mark.parametrize("diag", [False, True])
-def test_chain_batched_full_size(diag):
+# Bounds on the flagged-tie set at the headline sizes.  The strict tier (a draw's CDF crossing
+# within 1e-6 of u) takes about 2e-6 x (tokens of weight above 2e-6) + (mass of the lighter
+# tokens) of the draws; at V = 128256 and these logit spreads that is a few per cent of the
+# requests.  The seeded inputs give 1-8 of 64 (chain) and about 8 of 256 (n-gram).
+FLAG_BOUND = {"chain": 12 / 64, "ngram": 20 / 256}
+
+
+@pytest.mark.parametrize("seed,diag", [(0, False), (0, True), (1, False)])
+def test_chain_batched_full_size(seed, diag):
     """B = 64, K = 5, V = 128256, fp32: every request against the oracle, in the benchmark's
-    configuration (diag=False) and with per-position outputs."""
-    ci = synth.chain_batched(seed=0)
+    configuration (diag=False) and with per-position outputs; flagged requests checked against
+    their admissible outcomes, and the flagged share bounded."""
+    ci = synth.chain_batched(seed=seed)
     g = parity.run_gpu_chain(ci, diag=diag)
     st = parity.compare_chain(g, parity.run_oracle_chain(ci, threads=16), ci)
-    _show(f"chain batched full diag={diag}", st)
+    _show(f"chain batched full seed={seed} diag={diag}", st)
+    assert st["flagged"] <= FLAG_BOUND["chain"] * ci.B, st
 
 
 # ---------------------------------------------------------------- workload 4: greedy tree ----
@@ -132,6 +141,7 @@ def test_ngram_full_size(boost, diag):
     g = parity.run_gpu_chain(ci, ngram=True, diag=diag)
     st = parity.compare_chain(g, parity.run_oracle_chain(ci, ngram=True, threads=16), ci)
     _show(f"ngram boost={boost} diag={diag}", st)
+    assert st["flagged"] <= FLAG_BOUND["ngram"] * ci.B, st
 
 
 def test_ngram_probabilities_and_greedy():
