@@ -295,9 +295,12 @@ spec_status_t spec_kv_compact(void *const *caches, int num_caches, long long num
  * (spec_verify_workspace_bytes(B, 2K + 1, V, dtype) above the limit, K + 1 rows for T == 0) return
  * SPEC_ERR_UNSUPPORTED.  The first call on a device looks up that device's copy of the array
  * (cudaGetSymbolAddress, with the device current); make that first call before any stream
- * capture.  Every call on a device shares the same array and leaves its contents behind; each call
- * clears the counters it needs, but calls that may overlap on the GPU (other streams, other host
- * threads) race on the array and must be serialised by the caller.  The call allocates nothing.
+ * capture.  Every call on a device shares the same array and leaves its contents behind: the first
+ * call of a shape (B, rows, V) clears it, and every later call of that shape relies on the previous
+ * call having left its counters at zero, which every call does, one whose device wait timed out
+ * included.  Calls that may overlap on the GPU (other streams, other host threads) race on the
+ * array and must be serialised by the caller.  K > SPEC_MAX_K returns SPEC_ERR_UNSUPPORTED, as
+ * spec_verify_chain does.  The call allocates nothing.
  * Arguments and outputs as spec_verify_chain, without the optional per-position outputs.
  */
 #define SPEC_STATIC_WORKSPACE_BYTES (4u << 20)

@@ -47,6 +47,7 @@ extern "C" spec_status_t spec_verify_chain_static(const void* target_logits, con
                                                   float* residual_mass, int32_t* err_flags,
                                                   spec_stream_t stream) {
   if (B < 0 || K < 0 || V < 1) return SPEC_ERR_INVALID_ARG;
+  if (K > SPEC_MAX_K) return SPEC_ERR_UNSUPPORTED;  // as spec_verify_chain reports it (and 2K + 1 stays small)
   if (B == 0) return SPEC_OK;
   // Scratch this call needs (rows read per request: 2K + 1 with draft logits, K + 1 greedy).
   const int rows = (temperature > 0.f && K > 0) ? 2 * K + 1 : K + 1;
@@ -56,8 +57,11 @@ extern "C" spec_status_t spec_verify_chain_static(const void* target_logits, con
   void* scratch = nullptr;
   const spec_status_t st = scratch_for_current_device(&scratch);
   if (st != SPEC_OK) return st;
-  // The existing entry point clears the ticket counters at the start of the call, so whatever an
-  // earlier call left in the array does not matter.
+  // spec_verify_chain clears the array (one memset of this call's layout) on the first call of a
+  // shape at this address; every later call of that shape relies on the previous call having left
+  // the counters at zero, which each call does before it ends, a call whose device wait timed out
+  // included (its last CTA zeroes them).  Statistics left behind carry an older call's tag and are
+  // never taken.
   return spec_verify_chain(target_logits, draft_logits, dtype, B, K, V, temperature, draft_tokens, r, u,
                            num_accepted, out_tokens, residual_mass, err_flags, nullptr, nullptr, nullptr,
                            nullptr, nullptr, scratch, (size_t)SPEC_STATIC_WORKSPACE_BYTES, stream);

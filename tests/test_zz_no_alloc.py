@@ -29,17 +29,19 @@ def lib():
 
 def _static_call(lib, ci):
     dev = "cuda"
-    tl, dl = parity.to_device(ci.target, ci.dtype), parity.to_device(ci.draft, ci.dtype)
+    greedy = float(ci.temperature) == 0.0
+    tl = parity.to_device(ci.target, ci.dtype)
+    dl = None if greedy else parity.to_device(ci.draft, ci.dtype)
     x, r, u = parity.i32(ci.draft_tokens), parity.f32(ci.r), parity.f32(ci.u)
     na = torch.full((ci.B,), -9, dtype=torch.int32, device=dev)
     ot = torch.full((ci.B, ci.K + 1), -9, dtype=torch.int32, device=dev)
     rm = torch.full((ci.B,), -9.0, device=dev)
     ef = torch.full((ci.B,), -9, dtype=torch.int32, device=dev)
     P = ctypes.c_void_p
-    st = lib.spec_verify_chain_static(P(tl.data_ptr()), P(dl.data_ptr()), binding.DTYPE_CODE[tl.dtype],
-                                      ci.B, ci.K, ci.V, float(ci.temperature), P(x.data_ptr()),
-                                      P(r.data_ptr()), P(u.data_ptr()), P(na.data_ptr()),
-                                      P(ot.data_ptr()), P(rm.data_ptr()), P(ef.data_ptr()),
+    ptr = lambda t: P(t.data_ptr()) if t is not None else None  # noqa: E731
+    st = lib.spec_verify_chain_static(ptr(tl), ptr(dl), binding.DTYPE_CODE[tl.dtype],
+                                      ci.B, ci.K, ci.V, float(ci.temperature), ptr(x),
+                                      ptr(r), ptr(u), ptr(na), ptr(ot), ptr(rm), ptr(ef),
                                       P(torch.cuda.current_stream().cuda_stream))
     assert st == binding.SPEC_OK, lib.spec_status_string(st)
     torch.cuda.synchronize()
@@ -47,23 +49,43 @@ def _static_call(lib, ci):
                 residual_mass=rm.cpu().numpy(), err_flags=ef.cpu().numpy())
 
 
+def _check(lib, ci):
+    got = _static_call(lib, ci)
+    ref = parity.run_gpu_chain(ci, diag=False)
+    for key in ("num_accepted", "out_tokens", "err_flags"):
+        assert np.array_equal(got[key], ref[key]), key
+    assert np.abs(got["residual_mass"] - ref["residual_mass"]).max() <= parity.PROB_TOL
+    parity.compare_chain(dict(ref, **got), parity.run_oracle_chain(ci, threads=16), ci)
+
+
 def test_static_scratch_matches_workspace_entry_point(lib):
     for seed, dtype in ((21, "f32"), (22, "bf16")):  # two calls in a row share the array
-        ci = synth.chain_batched(seed=seed, B=8, V=20011, dtype=dtype)
-        got = _static_call(lib, ci)
-        ref = parity.run_gpu_chain(ci, diag=False)
-        for key in ("num_accepted", "out_tokens", "err_flags"):
-            assert np.array_equal(got[key], ref[key]), (seed, key)
-        assert np.abs(got["residual_mass"] - ref["residual_mass"]).max() <= parity.PROB_TOL
-        parity.compare_chain(dict(ref, **got), parity.run_oracle_chain(ci), ci)
+        _check(lib, synth.chain_batched(seed=seed, B=8, V=20011, dtype=dtype))
+
+
+def test_static_scratch_greedy_and_headline_size(lib):
+    """Greedy verification (K + 1 rows of scratch per request) and the largest headline batch that
+    the array holds (B = 64, K = 5, V = 128256, fp32 with draft logits: 2K + 1 rows)."""
+    ci = synth.chain_small_vocab(seed=3, B=16, temperature=0.0)
+    _check(lib, ci)
+    full = synth.chain_batched(seed=4)
+    need = lib.spec_verify_workspace_bytes(full.B, 2 * full.K + 1, full.V, 0)
+    assert need <= binding.STATIC_WORKSPACE_BYTES
+    _check(lib, full)
 
 
 def test_static_scratch_rejects_too_large_a_call(lib):
-    # 4096 requests of 11 rows at V = 128256 need more scratch than the fixed array holds; the
-    # host rejects the call before touching any pointer.
-    need = lib.spec_verify_workspace_bytes(4096, 11, 128256, 0)
-    assert need > binding.STATIC_WORKSPACE_BYTES
-    P = ctypes.c_void_p
-    st = lib.spec_verify_chain_static(P(1 << 20), P(2 << 20), 0, 4096, 5, 128256, 1.0, P(3 << 20),
-                                      P(4 << 20), P(5 << 20), P(6 << 20), P(7 << 20), None, None, None)
+    # The smallest batch of 11-row requests at V = 128256 whose scratch exceeds the fixed array is
+    # rejected before anything is launched; every pointer is NULL, so a call that got past the size
+    # check would fail on the pointers (SPEC_ERR_INVALID_ARG) instead of reaching a kernel.
+    B = 1
+    while lib.spec_verify_workspace_bytes(B, 11, 128256, 0) <= binding.STATIC_WORKSPACE_BYTES:
+        B += 1
+    for b in (B, 4096):
+        st = lib.spec_verify_chain_static(None, None, 0, b, 5, 128256, ctypes.c_float(1.0), None, None,
+                                          None, None, None, None, None, None)
+        assert st == binding.SPEC_ERR_UNSUPPORTED
+    # a draft length beyond SPEC_MAX_K: the same status as spec_verify_chain gives
+    st = lib.spec_verify_chain_static(None, None, 0, 1, 1 << 30, 16, ctypes.c_float(1.0), None, None,
+                                      None, None, None, None, None, None)
     assert st == binding.SPEC_ERR_UNSUPPORTED
