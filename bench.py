@@ -69,6 +69,7 @@ WORKLOADS = {
                                   "V=128256 bf16"),
 }
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # GB300's nominal HBM3e bandwidth (~8 TB/s), for context beside the measured peak
 KERNEL_SOURCES = ["speculative_decoding_verification_82_gb300/csrc/verify_kernel.cuh",
                   "speculative_decoding_verification_82_gb300/csrc/verify_common.cuh",
                   "speculative_decoding_verification_82_gb300/csrc/fastdiv.h",
@@ -548,20 +549,76 @@ def _e2e_step(dev_case: DeviceCase, host_case: DeviceCase):
         host_case.out[k].copy_(t, non_blocking=True)
 
 
-def run_gpu(args, w) -> None:
+def parity_summary(w: dict, name: str, inp, dev, ws) -> dict:
+    """One call of the workload on its seed-0 inputs, outside the timed region, checked against the
+    oracle on the same inputs with the parity rule of the tests: counts of the requests that match
+    exactly, of the oracle's flagged-tie set (strict: within 1e-6; widened-only: within the 1e-6 / S
+    band of a residual, not 1e-6), of flagged requests that took an admissible alternative, and of
+    failures (0 is the bar)."""
+    import torch
+
+    sys.path.insert(0, os.path.join(ROOT, "tests"))
+    import parity
+
+    from speculative_decoding_verification_82_gb300 import binding
+
+    kind = w["kind"]
+    if kind == "kv":
+        import oracle
+
+        caches = torch.from_numpy(np.ascontiguousarray(inp["caches"][:KV_ORACLE_CACHES])).to(dev)
+        ii = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.int32)).to(dev)  # noqa: E731
+        e = binding.spec_kv_compact([caches[i] for i in range(caches.shape[0])], ii(inp["slots"]),
+                                    ii(inp["parents"]), ii(inp["accept_len"]), ii(inp["path"]))
+        torch.cuda.synchronize()
+        ref, err = oracle.kv_compact_batch(inp["caches"][:KV_ORACLE_CACHES], inp["slots"], inp["parents"],
+                                           inp["accept_len"], inp["path"])
+        same = bool(np.array_equal(caches.cpu().numpy(), ref)) and bool(np.array_equal(e.cpu().numpy(), err))
+        return {"seed": 0, "requests": int(w["B"]), "caches_checked": KV_ORACLE_CACHES,
+                "bytes_exact": same, "failures": 0 if same else 1}
+    threads = os.cpu_count() or 1
+    if kind == "tree":
+        g = parity.run_gpu_tree(inp, workspace=ws)
+        o = parity.run_oracle_tree(inp, threads=threads)
+        fails = sum(int(not np.array_equal(g[a][b], o[c][b])) for b in range(inp.B)
+                    for a, c in (("accept_len", "accept_len"), ("path_nodes", "path"), ("out_tokens", "out_tokens"),
+                                 ("node_argmax", "amax"), ("err_flags", "err")))
+        return {"seed": 0, "requests": int(inp.B), "exact": int(inp.B) if not fails else None, "failures": fails,
+                "rule": "bit-exact (argmax, path, tokens, error bits)"}
+    if kind == "walk":
+        temps = np.resize(np.asarray(w["temps"], np.float32), inp.B) if "temps" in w else None
+        g = parity.run_gpu_walk(inp, float(w["T"]), temperatures=temps)
+        o = parity.run_oracle_walk(inp, float(w["T"]), threads=threads, temperatures=temps)
+        st = parity.check_walk(g, o, inp)
+    else:
+        ngram = kind in ("ngram", "ngram_pipe")
+        g = parity.run_gpu_chain(inp, ngram=ngram, workspace=ws, diag=False)
+        o = parity.run_oracle_chain(inp, ngram=ngram, threads=threads)
+        st = parity.check_chain(g, o, inp)
+    out = {k: st[k] for k in ("requests", "errors", "flagged_strict", "flagged_wide_only",
+                              "admissible_deviations")}
+    out["exact"] = st["requests"] - st["admissible_deviations"] - len(st["failures"])
+    out["failures"] = len(st["failures"])
+    out["seed"] = 0
+    out["rule"] = ("bit-exact outside the flagged-tie set; flagged requests: an admissible outcome "
+                   "(the other decision of a tied accept test, or a positive-weight token whose CDF "
+                   "interval comes within the tie band of u)")
+    return out
+
+
+def measure(args, name: str, w: dict, rank: int, world: int, local: int, primary: bool) -> dict:
+    """Times K steps of workload `name` (a replayed CUDA graph of C ABI calls) and returns its JSON
+    fields; the primary workload also gets the end-to-end figure, the CPU oracle and the parity
+    summary."""
     import torch
 
     from speculative_decoding_verification_82_gb300 import binding
 
-    rank, world, local = dist_setup()
-    torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    binding.library()  # fail loudly if the CUDA library is missing
-
     # alternate input sets; each is larger than L2 as well, except the KV compaction's 63 MB of moved
     # rows per step, which takes four sets (252 MB touched per round, about twice L2)
     n_sets = 4 if w["kind"] == "kv" else 2
-    inputs = [make_inputs(args.workload, seed=s) for s in rank_seeds(rank, n_sets)]
+    inputs = [make_inputs(name, seed=s) for s in rank_seeds(rank, n_sets)]
     if w["kind"] == "kv":
         w["moves"] = float(np.mean([kv_moves(inp) for inp in inputs]))
     rows_req = rows_per_request(w)
@@ -579,7 +636,7 @@ def run_gpu(args, w) -> None:
     lib = binding.library()
     abi = []
     for c in cases:
-        abi.append([(getattr(lib, name), a) for name, a in c.abi_args()])
+        abi.append([(getattr(lib, fn_name), a) for fn_name, a in c.abi_args()])
     visited = []
     for c, calls in zip(cases, abi):
         for fn, a in calls:
@@ -602,7 +659,7 @@ def run_gpu(args, w) -> None:
     with torch.cuda.graph(graph, stream=cap):
         gabi = []
         for c in cases:  # the calls' stream argument: the capturing stream
-            gabi.append([(getattr(lib, name), a) for name, a in c.abi_args()])
+            gabi.append([(getattr(lib, fn_name), a) for fn_name, a in c.abi_args()])
         status = 0
         for i in range(per_graph):
             for fn, a in gabi[i % n_sets]:
@@ -628,6 +685,7 @@ def run_gpu(args, w) -> None:
     clk = clocks.stop(t_host0, t_host1)
     elapsed_ms = max_over_ranks(start.elapsed_time(end), world)
     mean_call_ms = start.elapsed_time(end) / K  # device time per call, back to back
+    del graph
 
     rows_step = w["B"] * rows_req
     value = job_rows_per_s(world, rows_step, K, elapsed_ms)
@@ -635,40 +693,8 @@ def run_gpu(args, w) -> None:
     read_bytes = float(np.mean(visited)) if visited else float(alg_bytes)
     achieved = read_bytes / (mean_call_ms / 1e3) / 1e9
     peak, peak_src = hbm_peak()
-
-    # ---- end to end through the public API: pinned host -> device, call, results -> host ----
-    host = [DeviceCase(w, inp, dev, ws, host_pinned=True) for inp in inputs]
-    e2e_steps = max(3, min(K, args.e2e_steps))
-    h2d = sum(t.numel() * t.element_size() for t in host[0].inputs())
-    d2h = sum(t.numel() * t.element_size() for t in host[0].out.values())
-    for i in range(2):
-        _e2e_step(cases[i % n_sets], host[i % n_sets])
-    torch.cuda.synchronize()
-    barrier(world)
-    e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e_s.record(stream)
-    for i in range(e2e_steps):
-        _e2e_step(cases[i % n_sets], host[i % n_sets])
-    e_e.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e_s.elapsed_time(e_e), world)
-    e2e_value = world * rows_step * e2e_steps / (e2e_ms / 1e3)
-
-    if rank != 0:
-        return
-    line = {
-        "metric": METRIC,
-        "value": value,
-        "unit": "rows/s",
-        "n_gpus": world,
-        "steps": K,
-        "warmup": args.warmup,
-        "ms_per_step": elapsed_ms / K,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": w["dtype"],
-        "data": "synthetic (seeded Philox; logits, tokens and uniforms per the workload recipe)",
+    res = {
+        "value": value, "ms_per_step": elapsed_ms / K, "steps": K,
         "config": {"workload": w["desc"], "B": w["B"], "V": w["V"],
                    **({"K": w["K"]} if "K" in w else {"N": w["N"]}),
                    "rows_per_step": rows_step, "requests_per_s": value / rows_req,
@@ -677,23 +703,21 @@ def run_gpu(args, w) -> None:
                    "parallelism": f"replicas x{world}"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_source": peak_src,
-                     "traffic": profiled_traffic(args.workload), "algorithmic_bytes_per_call": read_bytes,
+                     "frac_of_nominal_8TBs": achieved / NOMINAL_HBM_GBS,
+                     "traffic": profiled_traffic(name), "algorithmic_bytes_per_call": read_bytes,
                      "mean_call_us": mean_call_ms * 1e3,
                      "kernel": (f"verify_kernel<ngram,{w['dtype']}> after ngram_draft_kernel (two launches a step)"
                                 if w["kind"] == "ngram_pipe" else
                                 f"verify_kernel<{w['kind']},{w['dtype']}> (one launch per call)")},
-        "e2e": {"value": e2e_value, "unit": "rows/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "steps": e2e_steps, "ms_per_step": e2e_ms / e2e_steps},
         "gpu_launches": K * launches_per_step(w),
         "clocks": clk,
     }
     if w["kind"] == "kv":
-        line["metric"] = KV_METRIC
-        line["roofline"]["kernel"] = "kv_compact_kernel (one launch per call)"
-        line["config"]["rows"] = (f"moved rows ({w['moves']:g} per request and cache: accepted positions whose node is "
-                                  f"not already in place) x 2048 bytes, read and written once")
+        res["roofline"]["kernel"] = "kv_compact_kernel (one launch per call)"
+        res["config"]["rows"] = (f"moved rows ({w['moves']:g} per request and cache: accepted positions whose node is "
+                                 f"not already in place) x 2048 bytes, read and written once")
     if w["kind"] == "walk":
-        line["roofline"].update(
+        res["roofline"].update(
             kernel=f"walk_kernel<{w['dtype']},32>, clusters of 8 CTAs (one launch per call)",
             algorithmic_bytes_note="acceptance-aware: the rows the walk reads (visited nodes' target rows, and "
                                    "draft rows of visited nodes with children), mean over the input sets",
@@ -701,8 +725,87 @@ def run_gpu(args, w) -> None:
             all_rows_equivalent_GBs=alg_bytes / (mean_call_ms / 1e3) / 1e9,
             note="latency-bound: one row pair per tree level, read by one cluster per request; the "
                  "all-rows figure is the bandwidth a pass over every row would need to match this time")
-    if not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, inputs[0])
+    if primary:
+        # ---- end to end through the public API: pinned host -> device, call, results -> host ----
+        host = [DeviceCase(w, inp, dev, ws, host_pinned=True) for inp in inputs]
+        e2e_steps = max(3, min(K, args.e2e_steps))
+        h2d = sum(t.numel() * t.element_size() for t in host[0].inputs())
+        d2h = sum(t.numel() * t.element_size() for t in host[0].out.values())
+        for i in range(2):
+            _e2e_step(cases[i % n_sets], host[i % n_sets])
+        torch.cuda.synchronize()
+        barrier(world)
+        e_s, e_e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e_s.record(stream)
+        for i in range(e2e_steps):
+            _e2e_step(cases[i % n_sets], host[i % n_sets])
+        e_e.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms = max_over_ranks(e_s.elapsed_time(e_e), world)
+        res["e2e"] = {"value": world * rows_step * e2e_steps / (e2e_ms / 1e3), "unit": "rows/s",
+                      "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                      "ms_per_step": e2e_ms / e2e_steps}
+        del host
+    if rank == 0 and not args.no_cpu_baseline:
+        if primary:
+            res["cpu_baseline"] = cpu_baseline(w, inputs[0])
+        if world == 1:  # the seed-0 inputs are rank 0's first set
+            res["parity"] = parity_summary(w, name, inputs[0], dev, ws)
+    del cases
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+# workloads the default run also times, reported under "secondary" (same process, same GPU)
+SECONDARY = ("tree_greedy", "ngram")
+
+
+def run_gpu(args, w) -> None:
+    import torch
+
+    from speculative_decoding_verification_82_gb300 import binding
+
+    rank, world, local = dist_setup()
+    torch.cuda.set_device(local)
+    binding.library()  # fail loudly if the CUDA library is missing
+    res = measure(args, args.workload, w, rank, world, local, primary=True)
+    secondary = {}
+    if args.workload == "chain_batched" and not args.no_secondary:
+        for name in SECONDARY:
+            sw = WORKLOADS[name]
+            r2 = measure(args, name, sw, rank, world, local, primary=False)
+            secondary[name] = {"workload": sw["desc"], "value": r2["value"], "unit": "rows/s",
+                               "ms_per_step": r2["ms_per_step"], "roofline": r2["roofline"],
+                               "clocks": r2["clocks"], "gpu_launches": r2["gpu_launches"],
+                               **({"parity": r2["parity"]} if "parity" in r2 else {})}
+    if rank != 0:
+        return
+    line = {
+        "metric": workload_metric(w),
+        "value": res["value"],
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": res["ms_per_step"],
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w["dtype"],
+        "data": "synthetic (seeded Philox; logits, tokens and uniforms per the workload recipe)",
+        "config": res["config"],
+        "roofline": res["roofline"],
+        "e2e": res["e2e"],
+        "gpu_launches": res["gpu_launches"] + sum(v["gpu_launches"] for v in secondary.values()),
+        "gpu_launches_primary": res["gpu_launches"],
+        "clocks": res["clocks"],
+    }
+    for k in ("cpu_baseline", "parity"):
+        if k in res:
+            line[k] = res[k]
+    if secondary:
+        line["secondary"] = secondary
     print(json.dumps(line), flush=True)
 
 
@@ -746,6 +849,23 @@ def run_reference(args, w) -> None:
     print(json.dumps(line), flush=True)
 
 
+def free_port() -> int:
+    import socket
+
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        return sk.getsockname()[1]
+
+
+def spawn_ranks(n: int) -> int:
+    """`--gpus N` without a launcher: starts N local ranks (one per GPU) through torch's launcher on
+    127.0.0.1, with the same arguments; rank 0 prints the line.  Returns the launcher's status."""
+    cmd = [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+           "--master-addr", "127.0.0.1", "--master-port", str(free_port()), os.path.abspath(__file__),
+           *sys.argv[1:]]
+    return subprocess.call(cmd)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
@@ -755,9 +875,19 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=40)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="time only the chosen workload (the default run also times tree_greedy and ngram)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
+    if args.gpus < 1:
+        ap.error("--gpus must be at least 1")
+    launched = os.environ.get("WORLD_SIZE")
+    if launched is None and args.gpus > 1:
+        sys.exit(spawn_ranks(args.gpus))
+    if int(launched or "1") != args.gpus:
+        print(f"bench.py: --gpus {args.gpus} but the launcher started {launched} rank(s)", file=sys.stderr)
+        sys.exit(2)
     w = WORKLOADS[args.workload]
     if args.impl == "reference":
         run_reference(args, w)

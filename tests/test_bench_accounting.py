@@ -7,6 +7,7 @@ import sys
 from types import SimpleNamespace
 
 import numpy as np
+import pytest
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 if ROOT not in sys.path:
@@ -70,3 +71,25 @@ def test_algorithmic_bytes_cover_the_logits_once():
     assert bench.rows_per_request(bench.WORKLOADS["tree_sample"]) == 61 + 20
     assert bench.rows_per_request(bench.WORKLOADS["tree_walk_greedy"]) == 61
     assert bench.launches_per_step(bench.WORKLOADS["ngram_pipeline"]) == 2
+
+
+def test_gpus_flag_never_silently_times_one_gpu(monkeypatch):
+    """`--gpus N` that disagrees with the launcher's WORLD_SIZE fails; without a launcher, N > 1
+    starts N ranks through torch's launcher (127.0.0.1) instead of timing one GPU."""
+    import subprocess
+    import sys
+
+    env = dict(os.environ, WORLD_SIZE="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--gpus", "2"], env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode == 2 and "--gpus 2" in r.stderr
+    calls = []
+    monkeypatch.setattr(bench.subprocess, "call", lambda cmd: calls.append(cmd) or 0)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--gpus", "4", "--steps", "10"])
+    with pytest.raises(SystemExit) as ex:
+        bench.main()
+    assert ex.value.code == 0
+    cmd = calls[0]
+    assert cmd[1:3] == ["-m", "torch.distributed.run"] and "--nproc-per-node=4" in cmd
+    assert cmd[cmd.index("--master-addr") + 1] == "127.0.0.1" and cmd[-4:] == ["--gpus", "4", "--steps", "10"]
