@@ -67,10 +67,10 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_verify_probs.restype = None
     lib.oracle_verify_ngram_direct.argtypes = [I, I, P, P, P, F, D, P, P, P, P, P, P, P]
     lib.oracle_verify_ngram_direct.restype = None
-    lib.oracle_verify_chain.argtypes = [I, P, P, I, I, I, F, P, P, P, D, I, I,
+    lib.oracle_verify_chain.argtypes = [I, P, P, I, I, I, F, P, P, P, P, D, I, I,
                                         P, P, P, P, P, P, P, P]
     lib.oracle_verify_chain.restype = None
-    lib.oracle_verify_ngram.argtypes = [I, P, I, I, I, F, P, P, P, D, I, I,
+    lib.oracle_verify_ngram.argtypes = [I, P, I, I, I, F, P, P, P, P, D, I, I,
                                         P, P, P, P, P, P, P, P]
     lib.oracle_verify_ngram.restype = None
     lib.oracle_tree_check.argtypes = [I, I, P, P]
@@ -205,19 +205,24 @@ def _run_threaded(fn, B: int, threads: int):
 
 
 def verify_chain(dtype: str, target, draft, B: int, K: int, V: int, T: float, draft_tokens, r, u,
-                 tol: float = DEFAULT_TOL, threads: int = 1, requests=None, lib=None) -> dict:
-    """Chain verification of `B` requests (or only the index range `requests`=(b0, b1))."""
+                 tol: float = DEFAULT_TOL, threads: int = 1, requests=None, lib=None,
+                 temperatures=None) -> dict:
+    """Chain verification of `B` requests (or only the index range `requests`=(b0, b1));
+    `temperatures` [B] sets each request's own temperature (R18)."""
     lib = lib or load()
     target = np.ascontiguousarray(target)
-    draft_p = _p(np.ascontiguousarray(draft)) if draft is not None else None
+    draft_a = np.ascontiguousarray(draft) if draft is not None else None
+    draft_p = _p(draft_a) if draft_a is not None else None
     x = _c(draft_tokens, np.int32)
     rr = _c(r, np.float32) if r is not None else np.zeros((B, K), np.float32)
     uu = _c(u, np.float32) if u is not None else np.zeros(B, np.float32)
+    tt = _c(temperatures, np.float32) if temperatures is not None else None
     o = _alloc_chain_out(B, K)
-    keep = (target, draft)
+    keep = (target, draft_a, tt)
 
     def run(b0, b1):
-        lib.oracle_verify_chain(DTYPE_CODE[dtype], _p(target), draft_p, B, K, V, float(T), _p(x),
+        lib.oracle_verify_chain(DTYPE_CODE[dtype], _p(target), draft_p, B, K, V, float(T),
+                                _p(tt) if tt is not None else None, _p(x),
                                 _p(rr), _p(uu), tol, b0, b1, *(_p(o[k]) for k in (
                                     "num_accepted", "out_tokens", "alpha", "cand", "mass",
                                     "pos_flag", "req_flag", "err")))
@@ -231,16 +236,20 @@ def verify_chain(dtype: str, target, draft, B: int, K: int, V: int, T: float, dr
 
 
 def verify_ngram(dtype: str, target, B: int, K: int, V: int, T: float, draft_tokens, r, u,
-                 tol: float = DEFAULT_TOL, threads: int = 1, requests=None, lib=None) -> dict:
+                 tol: float = DEFAULT_TOL, threads: int = 1, requests=None, lib=None,
+                 temperatures=None) -> dict:
+    """n-gram (one-hot draft) verification; `temperatures` as in `verify_chain`."""
     lib = lib or load()
     target = np.ascontiguousarray(target)
     x = _c(draft_tokens, np.int32)
     rr = _c(r, np.float32) if r is not None else np.zeros((B, K), np.float32)
     uu = _c(u, np.float32) if u is not None else np.zeros(B, np.float32)
+    tt = _c(temperatures, np.float32) if temperatures is not None else None
     o = _alloc_chain_out(B, K)
 
     def run(b0, b1):
-        lib.oracle_verify_ngram(DTYPE_CODE[dtype], _p(target), B, K, V, float(T), _p(x), _p(rr),
+        lib.oracle_verify_ngram(DTYPE_CODE[dtype], _p(target), B, K, V, float(T),
+                                _p(tt) if tt is not None else None, _p(x), _p(rr),
                                 _p(uu), tol, b0, b1, *(_p(o[k]) for k in (
                                     "num_accepted", "out_tokens", "alpha", "cand", "mass",
                                     "pos_flag", "req_flag", "err")))

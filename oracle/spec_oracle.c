@@ -52,6 +52,10 @@
  *   R12 tree layout: node 0 is the root, parents[0] = -1, 0 <= parents[i] < i; row n of the
  *       logits scores the children of node n.
  *   R13-R15 the stochastic tree walk: see the section "stochastic tree verification" below.
+ *   R18 per-request temperature (the x078.com page's production section sets the temperature per
+ *       request): with a temperatures array, request b uses temps[b] (0 = greedy for that
+ *       request); NaN, a negative value or infinity fails that request (ORE_BAD_TEMP alone).  On
+ *       the chain, the n-gram chain and the tree walk.
  */
 #include <math.h>
 #include <stdint.h>
@@ -300,16 +304,27 @@ static int greedy_chain(int K, int V, const double *lt, const int *x, int *n_acc
     return 0;
 }
 
+/* R18 per-request temperature: request b's temperature (temps[b] when given, else T), and
+ * whether it is valid (not NaN, negative or infinite). */
+static int request_temperature(float T, const float *temps, int b, float *Tb)
+{
+    *Tb = temps ? temps[b] : T;
+    return (*Tb >= 0.0f) && !isinf(*Tb);
+}
+
 /*
  * Chain verification on logits (draft model / EAGLE head: the draft side is logits).
  * target: [B][K+1][V], draft: [B][K][V] (ignored when T == 0), dtype OR_*.
+ * temps: NULL, or [B] per-request temperatures used instead of T (R18: 0 = greedy for that
+ * request; NaN, negative or infinite fails the request with ORE_BAD_TEMP alone).
  * Per request b the outputs are laid out as in oracle_verify_probs:
  *   n_acc[B], out_tokens[B][K+1], alpha[B][K], cand[B][K+1], mass[B][K+1],
  *   pos_flag[B][K+1], req_flag[B], err[B].
  * Requests [b0, b1) only are processed (lets a caller split the batch across threads).
  */
 void oracle_verify_chain(int dtype, const void *target, const void *draft, int B, int K, int V,
-                         float T, const int *x, const float *r, const float *u, double tol,
+                         float T, const float *temps, const int *x, const float *r,
+                         const float *u, double tol,
                          int b0, int b1, int *n_acc, int *out_tokens, double *alpha, int *cand,
                          double *mass, int *pos_flag, int *req_flag, int *err)
 {
@@ -331,17 +346,22 @@ void oracle_verify_chain(int dtype, const void *target, const void *draft, int B
         for (int k = 0; k < K; k++)
             if (xb[k] < 0 || xb[k] >= V)
                 e |= ORE_BAD_TOKEN;
-        for (int k = 0; k <= K; k++)
-            load_row(target, dtype, (size_t)b * (K + 1) + k, V, lt + (size_t)k * V);
-        if (T == 0.0f) {
+        float Tb;
+        if (!request_temperature(T, temps, b, &Tb)) {
+            e = ORE_BAD_TEMP;
+        } else if (Tb == 0.0f) {
+            for (int k = 0; k <= K; k++)
+                load_row(target, dtype, (size_t)b * (K + 1) + k, V, lt + (size_t)k * V);
             e |= greedy_chain(K, V, lt, xb, o_n, o_tok, o_al, o_cd, o_ms);
         } else {
+            for (int k = 0; k <= K; k++)
+                load_row(target, dtype, (size_t)b * (K + 1) + k, V, lt + (size_t)k * V);
             for (int k = 0; k < K; k++)
                 load_row(draft, dtype, (size_t)b * K + k, V, ld + (size_t)k * V);
             for (int k = 0; k <= K; k++)
-                e |= oracle_softmax(lt + (size_t)k * V, V, (double)T, p + (size_t)k * V);
+                e |= oracle_softmax(lt + (size_t)k * V, V, (double)Tb, p + (size_t)k * V);
             for (int k = 0; k < K; k++)
-                e |= oracle_softmax(ld + (size_t)k * V, V, (double)T, q + (size_t)k * V);
+                e |= oracle_softmax(ld + (size_t)k * V, V, (double)Tb, q + (size_t)k * V);
             if (!e)
                 oracle_verify_probs(K, V, p, q, xb, r + (size_t)b * K, u[b], tol, o_n, o_tok, o_al,
                                     o_cd, o_ms, o_pf, req_flag + b);
@@ -360,10 +380,12 @@ void oracle_verify_chain(int dtype, const void *target, const void *draft, int B
 
 /*
  * n-gram (prompt lookup) verification, R8: q_k is one-hot at x_k.  This is the general path of
- * oracle_verify_probs with explicit one-hot q rows.  Same layout as oracle_verify_chain.
+ * oracle_verify_probs with explicit one-hot q rows.  Same layout (and temps) as
+ * oracle_verify_chain.
  */
 void oracle_verify_ngram(int dtype, const void *target, int B, int K, int V, float T,
-                         const int *x, const float *r, const float *u, double tol, int b0, int b1,
+                         const float *temps, const int *x, const float *r, const float *u,
+                         double tol, int b0, int b1,
                          int *n_acc, int *out_tokens, double *alpha, int *cand, double *mass,
                          int *pos_flag, int *req_flag, int *err)
 {
@@ -384,13 +406,18 @@ void oracle_verify_ngram(int dtype, const void *target, int B, int K, int V, flo
         for (int k = 0; k < K; k++)
             if (xb[k] < 0 || xb[k] >= V)
                 e |= ORE_BAD_TOKEN;
-        for (int k = 0; k <= K; k++)
-            load_row(target, dtype, (size_t)b * (K + 1) + k, V, lt + (size_t)k * V);
-        if (T == 0.0f) {
+        float Tb;
+        if (!request_temperature(T, temps, b, &Tb)) {
+            e = ORE_BAD_TEMP;
+        } else if (Tb == 0.0f) {
+            for (int k = 0; k <= K; k++)
+                load_row(target, dtype, (size_t)b * (K + 1) + k, V, lt + (size_t)k * V);
             e |= greedy_chain(K, V, lt, xb, o_n, o_tok, o_al, o_cd, o_ms);
         } else {
             for (int k = 0; k <= K; k++)
-                e |= oracle_softmax(lt + (size_t)k * V, V, (double)T, p + (size_t)k * V);
+                load_row(target, dtype, (size_t)b * (K + 1) + k, V, lt + (size_t)k * V);
+            for (int k = 0; k <= K; k++)
+                e |= oracle_softmax(lt + (size_t)k * V, V, (double)Tb, p + (size_t)k * V);
             for (size_t i = 0; i < rowsD; i++)
                 q[i] = 0.0;
             for (int k = 0; k < K && !e; k++)

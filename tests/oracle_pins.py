@@ -835,3 +835,38 @@ def pin_tree_sample_alt(lib):
 
 
 FAST_PINS.append(pin_tree_sample_alt)
+
+
+def pin_chain_per_request_temperature(lib):
+    """R18 on the chain and n-gram verification: a batch with one temperature per request (greedy
+    ones included) gives, request by request, what a call at that request's temperature gives; a
+    NaN, negative or infinite temperature fails its request alone, with the bad-temperature bit."""
+    rng = np.random.default_rng(101)
+    B, K, V = 9, 3, 14
+    lt = rng.normal(0, 2, (B, K + 1, V)).astype(np.float32)
+    ld = (lt[:, :K] + rng.normal(0, 1, (B, K, V))).astype(np.float32)
+    x = rng.integers(0, V, (B, K)).astype(np.int32)
+    x[:, 0] = np.argmax(lt[:, 0], axis=-1)  # greedy requests accept their first draft
+    r = ((rng.integers(0, 1 << 24, (B, K)) + 1) / float(1 << 24)).astype(np.float32)
+    u = (rng.integers(0, 1 << 24, B) / float(1 << 24)).astype(np.float32)
+    temps = np.array([0.5, 0.0, 1.0, 2.0, 0.0, 0.8, np.nan, -1.0, np.inf], np.float32)
+    for ngram in (False, True):
+        if ngram:
+            o = oracle.verify_ngram("f32", lt, B, K, V, 1.0, x, r, u, lib=lib, temperatures=temps)
+        else:
+            o = oracle.verify_chain("f32", lt, ld, B, K, V, 1.0, x, r, u, lib=lib, temperatures=temps)
+        for b in range(6):
+            s = slice(b, b + 1)
+            if ngram:
+                one = oracle.verify_ngram("f32", lt[s], 1, K, V, float(temps[b]), x[s], r[s], u[s], lib=lib)
+            else:
+                one = oracle.verify_chain("f32", lt[s], ld[s], 1, K, V, float(temps[b]), x[s], r[s], u[s],
+                                          lib=lib)
+            for k in ("num_accepted", "out_tokens", "alpha", "cand", "mass", "pos_flag", "req_flag", "err"):
+                assert np.array_equal(o[k][b], one[k][0]), (ngram, b, k)
+        assert o["num_accepted"][1] >= 1 and o["num_accepted"][4] >= 1  # greedy: argmax drafts accepted
+        assert list(o["err"][6:]) == [oracle.ERR_BAD_TEMP] * 3
+        assert (o["out_tokens"][6:] == -1).all() and (o["num_accepted"][6:] == 0).all()
+
+
+FAST_PINS.append(pin_chain_per_request_temperature)

@@ -80,6 +80,8 @@ MUTANTS = [
     ("walk_draw_row_from_node_p", "const double *wd = p;", "const double *wd = p0;"),
     ("walk_flip_not_applied", "acc = !acc;", "acc = acc;"),
     ("walk_flip_any_test", "if (flip && fabs((double)r[c] - a) <= tol / R) {", "if (flip) {"),
+    ("chain_per_request_temperature_ignored", "*Tb = temps ? temps[b] : T;", "*Tb = T;"),
+    ("chain_bad_temperature_accepted", "return (*Tb >= 0.0f) && !isinf(*Tb);", "return 1;"),
     ("bad_token_check_dropped", "if (xb[k] < 0 || xb[k] >= V)\n                e |= ORE_BAD_TOKEN;",
      "if (0)\n                e |= ORE_BAD_TOKEN;"),
 ]
