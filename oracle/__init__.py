@@ -81,15 +81,15 @@ def _bind(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_tree_bruteforce.restype = I
     lib.oracle_verify_tree_greedy.argtypes = [I, P, I, I, I, P, P, I, I, P, P, P, P, P]
     lib.oracle_verify_tree_greedy.restype = None
-    lib.oracle_tree_sample_probs.argtypes = [I, I, P, P, P, P, P, F, D, I, P, P, P, P, P, P, P, P]
+    lib.oracle_tree_sample_probs.argtypes = [I, I, P, P, P, P, P, F, D, I, P, P, P, P, P, P, P, P, P]
     lib.oracle_tree_sample_probs.restype = None
     lib.oracle_verify_tree_sample.argtypes = [I, P, P, I, I, I, F, P, P, P, P, P, D, I, I,
                                               P, P, P, P, P, P, P]
     lib.oracle_verify_tree_sample.restype = None
-    lib.oracle_chain_draw_rows.argtypes = [I, P, P, I, I, I, F, P, I, P, P]
+    lib.oracle_chain_draw_rows.argtypes = [I, P, P, I, I, I, F, P, I, D, P, P, P]
     lib.oracle_chain_draw_rows.restype = I
     lib.oracle_tree_sample_alt.argtypes = [I, P, P, I, I, F, P, P, P, P, P, D, I, I,
-                                           P, P, P, P, P, P, P, P]
+                                           P, P, P, P, P, P, P, P, P]
     lib.oracle_tree_sample_alt.restype = I
     lib.oracle_ngram_draft.argtypes = [P, I, I, I, I, P, P, P, P]
     lib.oracle_ngram_draft.restype = None
@@ -262,20 +262,23 @@ def verify_ngram(dtype: str, target, B: int, K: int, V: int, T: float, draft_tok
 
 
 def chain_draw_rows(dtype: str, target, draft, B: int, K: int, V: int, T: float, draft_tokens,
-                    b: int, ngram: bool = False, lib=None) -> tuple[np.ndarray, np.ndarray, int]:
-    """The draws of request b of a chain (or n-gram) call, for checking a flagged tie: w [K+1][V],
-    the weights each position's draw uses (residual, bonus row, or p after an empty residual), and
-    cdf [K+1][V], their normalised cumulative sums; token t is drawn at k for u in
-    [cdf[k][t-1], cdf[k][t]).  Returns (w, cdf, error bits)."""
+                    b: int, ngram: bool = False, tol: float = DEFAULT_TOL, lib=None) -> dict:
+    """The draws of request b of a chain (or n-gram) call, for checking a flagged tie:
+    w [K+1][V], the weights each position's draw uses (residual, bonus row, or p after an empty
+    residual); cdf [K+1][V], their normalised cumulative sums (token t is drawn at k for u in
+    [cdf[k][t-1], cdf[k][t])); wmax [K+1][V], each token's largest weight within the widened
+    tier's precision (R10); err, the request's error bits."""
     lib = lib or load()
     target = np.ascontiguousarray(target)
     dr = np.ascontiguousarray(draft) if (draft is not None and not ngram) else None
     x = _c(draft_tokens, np.int32)
     w = np.zeros((K + 1, V), np.float64)
     cdf = np.zeros((K + 1, V), np.float64)
+    wmax = np.zeros((K + 1, V), np.float64)
     e = lib.oracle_chain_draw_rows(DTYPE_CODE[dtype], _p(target), _p(dr) if dr is not None else None,
-                                   1 if ngram else 0, K, V, float(T), _p(x), int(b), _p(w), _p(cdf))
-    return w, cdf, e
+                                   1 if ngram else 0, K, V, float(T), _p(x), int(b), tol, _p(w), _p(cdf),
+                                   _p(wmax))
+    return dict(w=w, cdf=cdf, wmax=wmax, err=int(e))
 
 
 def tree_sample_alt(dtype: str, target, draft, B: int, N: int, V: int, T: float, node_tokens,
@@ -294,13 +297,13 @@ def tree_sample_alt(dtype: str, target, draft, B: int, N: int, V: int, T: float,
     L, fl = np.zeros(1, np.int32), np.zeros(1, np.int32)
     path, out = np.zeros(N1, np.int32), np.zeros(N1, np.int32)
     alpha, mass = np.zeros(N1, np.float64), np.zeros(1, np.float64)
-    dw, dc = np.zeros(max(V, 1), np.float64), np.zeros(max(V, 1), np.float64)
+    dw, dc, dm = (np.zeros(max(V, 1), np.float64) for _ in range(3))
     e = lib.oracle_tree_sample_alt(DTYPE_CODE[dtype], _p(target), _p(dr) if dr is not None else None,
                                    N, V, float(T), _p(tt) if tt is not None else None, _p(tk), _p(pa),
                                    _p(rr), _p(uu), tol, int(b), 1 if flip else 0, _p(L), _p(path),
-                                   _p(out), _p(alpha), _p(mass), _p(fl), _p(dw), _p(dc))
+                                   _p(out), _p(alpha), _p(mass), _p(fl), _p(dw), _p(dc), _p(dm))
     return dict(accept_len=int(L[0]), path=path, out_tokens=out, alpha=alpha, mass=float(mass[0]),
-                req_flag=int(fl[0]), err=int(e), draw_w=dw, draw_cdf=dc)
+                req_flag=int(fl[0]), err=int(e), draw_w=dw, draw_cdf=dc, draw_wmax=dm)
 
 
 def tree_walk(parents, tokens, amax, lib=None) -> dict:
@@ -361,12 +364,12 @@ def tree_sample_probs(p, q, parents, tokens, r, u, tol: float = DEFAULT_TOL, lib
     L, fl = np.zeros(1, np.int32), np.zeros(1, np.int32)
     path, out = np.zeros(N1, np.int32), np.zeros(N1, np.int32)
     alpha, mass = np.zeros(N1, np.float64), np.zeros(1, np.float64)
-    dw, dc = np.zeros(V, np.float64), np.zeros(V, np.float64)
+    dw, dc, dm = (np.zeros(V, np.float64) for _ in range(3))
     lib.oracle_tree_sample_probs(N1, V, _p(p), _p(q), _p(pa), _p(tk), _p(rr), float(u), tol,
                                  1 if flip else 0, _p(L), _p(path), _p(out), _p(alpha), _p(mass),
-                                 _p(fl), _p(dw), _p(dc))
+                                 _p(fl), _p(dw), _p(dc), _p(dm))
     return dict(accept_len=int(L[0]), path=path, out_tokens=out, alpha=alpha,
-                mass=float(mass[0]), req_flag=int(fl[0]), draw_w=dw, draw_cdf=dc)
+                mass=float(mass[0]), req_flag=int(fl[0]), draw_w=dw, draw_cdf=dc, draw_wmax=dm)
 
 
 def verify_tree_sample(dtype: str, target, draft, B: int, N: int, V: int, T: float, node_tokens,

@@ -44,8 +44,11 @@
  *       about tol / S, so a crossing within tol / S of u that is not within tol is flagged in a
  *       second tier.  A flagged draw admits every positive-weight token whose CDF interval comes
  *       within the band of u; oracle_chain_draw_rows gives the weights and the normalised CDF for
- *       that check.  A flagged accept test admits either decision; for the tree walk
- *       oracle_tree_sample_alt gives the outcome of the opposite decision.
+ *       that check.  In the widened tier a token whose residual weight is 0 only by a margin below
+ *       that resolution (p_t - q_t > -(tol / 2)(p_t + q_t), the per-token precision the band tol / S
+ *       stands for) is admissible too; the draw rows give that bound as wmax.  A flagged accept
+ *       test admits either decision; for the tree walk oracle_tree_sample_alt gives the outcome of
+ *       the opposite decision.
  *   R11 invalid input: a draft token outside [0, V), a logits row holding NaN (or, when a softmax
  *       is taken, +inf, or only -inf), or a malformed parent array sets an error bit (every bit
  *       that applies, all rows checked); the request then accepts nothing and emits no token (-1).
@@ -501,17 +504,30 @@ static double normalised_cdf(const double *w, int V, double *cdf)
     return S;
 }
 
+/* The largest weight of each token of the residual max(0, p - q) when p and q are each known to a
+ * relative tol / 2 (the widened tier of R10): max(0, p_i - q_i + (tol / 2)(p_i + q_i)). */
+static void residual_wmax(const double *p, const double *q, int V, double tol, double *wmax)
+{
+    for (int i = 0; i < V; i++) {
+        double d = p[i] - q[i] + 0.5 * tol * (p[i] + q[i]);
+        wmax[i] = d > 0.0 ? d : 0.0;
+    }
+}
+
 /*
  * The draws of request b, for checking a flagged tie (R10): for every position k = 0..K, the
  * weights the draw at k uses, w[k][i] (the step-3 residual at a draft position, p_K at the bonus
  * row, p_k itself when the residual is empty, R5), and cdf[k][i], their normalised cumulative
  * sums.  Token t is drawn at k exactly when u lies in [cdf[k][t-1], cdf[k][t]) (cdf[k][-1] = 0).
+ * wmax[k][i]: the largest weight of token i within the widened tier's precision (residual_wmax) at
+ * a draft-model residual position, w[k][i] elsewhere (no cancellation there).
  * ngram != 0 takes q one-hot at the draft tokens (R8; draft unused).  T > 0.  Layout of the
- * inputs as oracle_verify_chain; w and cdf are [K+1][V].  Returns the request's error bits (the
- * outputs are unspecified when they are not 0).
+ * inputs as oracle_verify_chain; w, cdf and wmax are [K+1][V].  Returns the request's error bits
+ * (the outputs are unspecified when they are not 0).
  */
 int oracle_chain_draw_rows(int dtype, const void *target, const void *draft, int ngram, int K,
-                           int V, float T, const int *x, int b, double *w_out, double *cdf_out)
+                           int V, float T, const int *x, int b, double tol, double *w_out,
+                           double *cdf_out, double *wmax_out)
 {
     size_t rowsT = (size_t)(K + 1) * V, rowsD = (size_t)K * V;
     double *l = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
@@ -537,7 +553,7 @@ int oracle_chain_draw_rows(int dtype, const void *target, const void *draft, int
         }
     }
     for (int k = 0; k <= K && !e; k++) {
-        double *w = w_out + (size_t)k * V;
+        double *w = w_out + (size_t)k * V, *wm = wmax_out + (size_t)k * V;
         draw_weights(K, V, p, q, k, w);
         double S = 0.0;
         for (int i = 0; i < V; i++)
@@ -546,6 +562,11 @@ int oracle_chain_draw_rows(int dtype, const void *target, const void *draft, int
             for (int i = 0; i < V; i++)
                 w[i] = p[(size_t)k * V + i];
         normalised_cdf(w, V, cdf_out + (size_t)k * V);
+        if (!ngram && k < K && S > 0.0)
+            residual_wmax(p + (size_t)k * V, q + (size_t)k * V, V, tol, wm);
+        else
+            for (int i = 0; i < V; i++)
+                wm[i] = w[i];
     }
     free(l);
     free(p);
@@ -702,11 +723,14 @@ static void tree_fail(int N1, int *accept_len, int *path, int *out_tokens, doubl
 static int tree_sample_walk(int N1, int V, tree_rows_fn rows, void *ctx, const int *parents,
                             const int *tokens, const float *r, float u, double tol, int flip,
                             int *accept_len, int *path, int *out_tokens, double *alpha,
-                            double *mass, int *req_flag, double *draw_w, double *draw_cdf)
+                            double *mass, int *req_flag, double *draw_w, double *draw_cdf,
+                            double *draw_wmax)
 {
     size_t n = (size_t)(V > 0 ? V : 1);
     double *p0 = (double *)malloc(sizeof(double) * n), *p = (double *)malloc(sizeof(double) * n);
     double *q = (double *)malloc(sizeof(double) * n), *w = (double *)malloc(sizeof(double) * n);
+    double *pprev = (double *)malloc(sizeof(double) * n); /* the target before the last rejection */
+    double Slast = 1.0;
     int e = 0, cur = 0, len = 0;
     *req_flag = 0;
     for (int i = 0; i < N1; i++) {
@@ -757,8 +781,11 @@ static int tree_sample_walk(int N1, int V, tree_rows_fn rows, void *ctx, const i
                 empty = 1;
                 break;
             }
-            for (int i = 0; i < V; i++)
+            for (int i = 0; i < V; i++) {
+                pprev[i] = p[i];
                 p[i] = w[i] / S;
+            }
+            Slast = S;
         }
         if (next >= 0) {
             out_tokens[len] = tokens[next];
@@ -787,6 +814,16 @@ static int tree_sample_walk(int N1, int V, tree_rows_fn rows, void *ctx, const i
             for (int i = 0; i < V; i++)
                 draw_w[i] = wd[i];
             normalised_cdf(draw_w, V, draw_cdf);
+            /* the widened tier's largest weights: the last residual with p and q each known to a
+             * relative tol / 2 (no rejection at the node: p itself) */
+            if (!empty && R < 1.0) {
+                residual_wmax(pprev, q, V, tol, draw_wmax);
+                for (int i = 0; i < V; i++)
+                    draw_wmax[i] /= Slast;
+            } else {
+                for (int i = 0; i < V; i++)
+                    draw_wmax[i] = wd[i];
+            }
         }
         out_tokens[len] = tok;
         *mass = R;
@@ -797,6 +834,7 @@ static int tree_sample_walk(int N1, int V, tree_rows_fn rows, void *ctx, const i
     free(p);
     free(q);
     free(w);
+    free(pprev);
     return e;
 }
 
@@ -819,17 +857,17 @@ static int probs_rows(void *ctx, int node, int need_q, double *p, double *q)
 /* Stochastic tree verification on probability rows p, q: [N1][V] (row n of q = the draft
  * distribution of node n's children).  Outputs: *accept_len, path[N1], out_tokens[N1],
  * alpha[N1] (alpha of each tested child, -1 elsewhere), *mass (R14), *req_flag.  flip and
- * draw_w / draw_cdf as oracle_tree_sample_alt (0 and NULL for the walk itself). */
+ * draw_w / draw_cdf / draw_wmax as oracle_tree_sample_alt (0 and NULL for the walk itself). */
 void oracle_tree_sample_probs(int N1, int V, const double *p, const double *q,
                               const int *parents, const int *tokens, const float *r, float u,
                               double tol, int flip, int *accept_len, int *path, int *out_tokens,
                               double *alpha, double *mass, int *req_flag, double *draw_w,
-                              double *draw_cdf)
+                              double *draw_cdf, double *draw_wmax)
 {
     struct probs_ctx c = {V, p, q};
     *mass = 0.0;
     tree_sample_walk(N1, V, probs_rows, &c, parents, tokens, r, u, tol, flip, accept_len, path,
-                     out_tokens, alpha, mass, req_flag, draw_w, draw_cdf);
+                     out_tokens, alpha, mass, req_flag, draw_w, draw_cdf, draw_wmax);
 }
 
 struct logits_ctx {
@@ -902,7 +940,7 @@ static int tree_sample_request(int dtype, const void *target, const void *draft,
                                const int *parents, const float *r, const float *u, double tol,
                                int b, int flip, double *l, int *accept_len, int *o_path,
                                int *o_tok, double *o_al, double *mass, int *req_flag,
-                               double *draw_w, double *draw_cdf)
+                               double *draw_w, double *draw_cdf, double *draw_wmax)
 {
     int N1 = N + 1;
     const int *pb = parents + (size_t)b * N1, *tb = node_tokens + (size_t)b * N1;
@@ -920,7 +958,8 @@ static int tree_sample_request(int dtype, const void *target, const void *draft,
         } else {
             struct logits_ctx c = {dtype, V, (double)Tb, target, draft, (size_t)b * N1, l};
             e = tree_sample_walk(N1, V, logits_rows, &c, pb, tb, r + (size_t)b * N1, u[b], tol, flip,
-                                 accept_len, o_path, o_tok, o_al, mass, req_flag, draw_w, draw_cdf);
+                                 accept_len, o_path, o_tok, o_al, mass, req_flag, draw_w, draw_cdf,
+                                 draw_wmax);
         }
     }
     if (e) {
@@ -952,27 +991,29 @@ void oracle_verify_tree_sample(int dtype, const void *target, const void *draft,
         err[b] = tree_sample_request(dtype, target, draft, N, V, T, temps, node_tokens, parents, r,
                                      u, tol, b, 0, l, accept_len + b, path + (size_t)b * N1,
                                      out_tokens + (size_t)b * N1, alpha + (size_t)b * N1, mass + b,
-                                     req_flag + b, NULL, NULL);
+                                     req_flag + b, NULL, NULL, NULL);
     free(l);
 }
 
 /*
  * Request b of oracle_verify_tree_sample (same inputs; outputs for that request alone), for
  * checking a flagged tie (R10, R14): with flip != 0 the first flagged accept test is decided the
- * opposite way (the walk's other admissible outcome), and draw_w / draw_cdf ([V], or NULL)
- * receive the final draw's weights and their normalised cumulative sums when the request ends in
- * a draw (T > 0, no error).  Returns the request's error bits.
+ * opposite way (the walk's other admissible outcome), and draw_w / draw_cdf / draw_wmax ([V], or
+ * NULL) receive the final draw's weights, their normalised cumulative sums and the widened tier's
+ * largest weights (residual_wmax of the last residual) when the request ends in a draw (T > 0, no
+ * error).  Returns the request's error bits.
  */
 int oracle_tree_sample_alt(int dtype, const void *target, const void *draft, int N, int V,
                            float T, const float *temps, const int *node_tokens,
                            const int *parents, const float *r, const float *u, double tol, int b,
                            int flip, int *accept_len, int *path, int *out_tokens, double *alpha,
-                           double *mass, int *req_flag, double *draw_w, double *draw_cdf)
+                           double *mass, int *req_flag, double *draw_w, double *draw_cdf,
+                           double *draw_wmax)
 {
     double *l = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
     int e = tree_sample_request(dtype, target, draft, N, V, T, temps, node_tokens, parents, r, u,
                                 tol, b, flip, l, accept_len, path, out_tokens, alpha, mass,
-                                req_flag, draw_w, draw_cdf);
+                                req_flag, draw_w, draw_cdf, draw_wmax);
     free(l);
     return e;
 }

@@ -449,6 +449,7 @@ def pin_hand_tree_sample_cases(lib):
             assert bool(o["req_flag"] & oracle.FLAG_CDF_TIE_WIDE) == run.get("cdf_tie_wide", False), (tag, o)
             if "draw_w" in run:  # the final draw's weights, and their cumulative sums over the total
                 assert np.allclose(o["draw_w"], run["draw_w"], rtol=0, atol=1e-15), (tag, o["draw_w"])
+                assert np.allclose(o["draw_wmax"], run["draw_wmax"], rtol=0, atol=1e-12), (tag, o["draw_wmax"])
                 w = np.asarray(run["draw_w"])
                 assert np.allclose(o["draw_cdf"], np.cumsum(w) / w.sum(), rtol=0, atol=1e-15), (tag, o)
             f = oracle.tree_sample_probs(p, q, case["parents"], case["tokens"], run["r"], run["u"],
@@ -458,6 +459,7 @@ def pin_hand_tree_sample_cases(lib):
                 assert f["accept_len"] == alt["accept_len"], (tag, f)
                 assert list(f["path"]) == alt["path"] and list(f["out_tokens"]) == alt["out_tokens"], (tag, f)
                 assert np.allclose(f["draw_w"], alt["draw_w"], rtol=0, atol=1e-15), (tag, f["draw_w"])
+                assert np.allclose(f["draw_wmax"], alt["draw_wmax"], rtol=0, atol=1e-12), (tag, f["draw_wmax"])
                 assert bool(f["req_flag"] & oracle.FLAG_CDF_TIE) == alt["cdf_tie"], (tag, f)
             elif not (run["accept_tie"] or run.get("accept_tie_wide", False)):  # nothing to flip
                 assert f["accept_len"] == o["accept_len"] and list(f["out_tokens"]) == list(o["out_tokens"]), tag
@@ -762,8 +764,9 @@ def pin_chain_draw_rows(lib):
             else:
                 o = oracle.verify_chain("f32", lt, ld, B, K, V, T, x, r, u, lib=lib)
             for b in range(B):
-                w, cdf, e = oracle.chain_draw_rows("f32", lt, ld, B, K, V, T, x, b, ngram=ngram, lib=lib)
-                assert e == 0
+                d = oracle.chain_draw_rows("f32", lt, ld, B, K, V, T, x, b, ngram=ngram, lib=lib)
+                w, cdf, wmax = d["w"], d["cdf"], d["wmax"]
+                assert d["err"] == 0
                 p = sp_softmax(lt[b].astype(np.float64) / T, axis=-1)
                 q = np.zeros((K, V))
                 if ngram:
@@ -772,9 +775,16 @@ def pin_chain_draw_rows(lib):
                     q = sp_softmax(ld[b].astype(np.float64) / T, axis=-1)
                 for k in range(K + 1):
                     ref = np.maximum(0.0, p[k] - q[k]) if k < K else p[k]
-                    if not ref.sum() > 0:
+                    empty = not ref.sum() > 0
+                    if empty:
                         ref = p[k]
                     assert np.allclose(w[k], ref, rtol=0, atol=1e-12), (i, ngram, b, k)
+                    if k < K and not ngram and not empty:
+                        # the widened tier's largest weights: p and q each known to a relative tol / 2
+                        wm = np.maximum(0.0, p[k] - q[k] + 0.5 * TOL * (p[k] + q[k]))
+                        assert np.allclose(wmax[k], wm, rtol=0, atol=1e-12), (i, b, k)
+                    else:
+                        assert np.array_equal(wmax[k], w[k])
                     assert np.allclose(cdf[k], np.cumsum(w[k]) / w[k].sum(), rtol=0, atol=1e-12)
                     if not o["pos_flag"][b][k] & (oracle.FLAG_CDF_TIE | oracle.FLAG_CDF_TIE_WIDE):
                         assert o["cand"][b][k] == _brute_inverse_cdf(w[k], float(u[b])), (i, ngram, b, k)
@@ -820,6 +830,7 @@ def pin_tree_sample_alt(lib):
         if L == K or same["mass"] == 1.0:  # nothing rejected at the last node: the draw row is its p
             pl = sp_softmax(lt[0, L].astype(np.float64) / T)
             assert np.allclose(same["draw_w"], pl, rtol=0, atol=1e-12)
+            assert np.array_equal(same["draw_wmax"], same["draw_w"])
             assert np.allclose(same["draw_cdf"], np.cumsum(pl) / pl.sum(), rtol=0, atol=1e-12)
         f = oracle.tree_sample_alt("f32", lt, dt, 1, K, V, T, tokens, parents, rt, u, 0, True, lib=lib)
         accepted = float(rt[0, j + 1]) <= a

@@ -86,11 +86,14 @@ def run_oracle_chain(ci, ngram: bool = False, threads: int = 8, requests=None) -
     return o
 
 
-def draw_admissible(w: np.ndarray, cdf: np.ndarray, u: float, t: int, band: float) -> bool:
+def draw_admissible(w: np.ndarray, cdf: np.ndarray, u: float, t: int, band: float, wmax=None) -> bool:
     """Token t is an admissible outcome of a draw with weights w and normalised CDF cdf (the
-    oracle's): it has positive weight and its interval [cdf[t-1], cdf[t]) of u comes within `band`
-    of the uniform u that was used."""
-    if not (0 <= t < w.size) or not w[t] > 0:
+    oracle's): it has positive weight (or, in the widened tier, a positive largest weight wmax
+    within fp32 precision) and its interval [cdf[t-1], cdf[t]) of u comes within `band` of the
+    uniform u that was used."""
+    if not (0 <= t < w.size):
+        return False
+    if not (w[t] > 0 or (wmax is not None and wmax[t] > 0)):
         return False
     lo = cdf[t - 1] if t > 0 else 0.0
     return lo - band <= u <= cdf[t] + band
@@ -154,10 +157,12 @@ def check_chain(g: dict, o: dict, ci, requests=None) -> dict:
             return True, False
         if greedy or not (o["pos_flag"][b][k] & (oracle.FLAG_CDF_TIE | oracle.FLAG_CDF_TIE_WIDE)):
             return False, False
-        w, cdf, e = draw_rows(b)
+        d = draw_rows(b)
         widened = (not ngram) and k < K
         band = _tie_band(float(o["mass"][b][k]), widened)
-        return (e == 0 and draw_admissible(w[k], cdf[k], float(ci.u[b]), int(t), band)), True
+        wmax = d["wmax"][k] if (widened and o["pos_flag"][b][k] & oracle.FLAG_CDF_TIE_WIDE) else None
+        return (d["err"] == 0 and draw_admissible(d["w"][k], d["cdf"][k], float(ci.u[b]), int(t), band,
+                                                  wmax)), True
 
     deviations = 0
     cand_dev = 0
@@ -314,8 +319,9 @@ def check_walk(g: dict, o: dict, ti, temperature=None, temperatures=None) -> dic
         if t != ref["out_tokens"][L]:
             full = ref if "draw_w" in ref else alt(b, False)
             flagged_draw = ref["req_flag"] & (oracle.FLAG_CDF_TIE | oracle.FLAG_CDF_TIE_WIDE)
+            wmax = full["draw_wmax"] if ref["req_flag"] & oracle.FLAG_CDF_TIE_WIDE else None
             if not (sampled and flagged_draw and draw_admissible(
-                    full["draw_w"], full["draw_cdf"], float(ti.u[b]), t, _tie_band(ref["mass"], True))):
+                    full["draw_w"], full["draw_cdf"], float(ti.u[b]), t, _tie_band(ref["mass"], True), wmax)):
                 fails.append(("emitted token not admissible", int(b), t, int(ref["out_tokens"][L])))
                 continue
             deviations += 1

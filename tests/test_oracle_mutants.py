@@ -79,6 +79,9 @@ MUTANTS = [
     ("draw_cdf_not_normalised", "cdf[i] = S > 0.0 ? C / S : 0.0;", "cdf[i] = C;"),
     ("walk_draw_row_from_node_p", "const double *wd = p;", "const double *wd = p0;"),
     ("walk_flip_not_applied", "acc = !acc;", "acc = acc;"),
+    ("wmax_margin_subtracted", "double d = p[i] - q[i] + 0.5 * tol * (p[i] + q[i]);",
+     "double d = p[i] - q[i] - 0.5 * tol * (p[i] + q[i]);"),
+    ("walk_wmax_not_normalised", "draw_wmax[i] /= Slast;", "draw_wmax[i] /= 1.0;"),
     ("walk_flip_any_test", "if (flip && fabs((double)r[c] - a) <= tol / R) {", "if (flip) {"),
     ("chain_per_request_temperature_ignored", "*Tb = temps ? temps[b] : T;", "*Tb = T;"),
     ("chain_bad_temperature_accepted", "return (*Tb >= 0.0f) && !isinf(*Tb);", "return 1;"),

@@ -49,9 +49,10 @@ def test_chain_flagged_draw(ngram):
     o = parity.run_oracle_chain(ci, ngram=ngram)
     b = 0
     n = int(o["num_accepted"][b])
-    w, cdf, e = oracle.chain_draw_rows(ci.dtype, ci.target, ci.draft, ci.B, ci.K, ci.V,
-                                       float(ci.temperature), ci.draft_tokens, b, ngram=ngram)
-    assert e == 0
+    d = oracle.chain_draw_rows(ci.dtype, ci.target, ci.draft, ci.B, ci.K, ci.V,
+                               float(ci.temperature), ci.draft_tokens, b, ngram=ngram)
+    w, cdf = d["w"], d["cdf"]
+    assert d["err"] == 0
     pos = _positive(w[n], 0, ci.V)
     t = pos[len(pos) // 2]  # a boundary in the middle of the CDF: u onto cdf[t]
     ci.u[b] = np.float32(round(cdf[n][t] * U24) / U24)
@@ -75,8 +76,9 @@ def test_chain_flagged_draw(ngram):
     g3 = _as_gpu(o, ci.K)
     g3["out_tokens"][b][n] = far
     assert parity.check_chain(g3, o, ci)["failures"]
-    # a zero-weight token is never admissible, wherever its (empty) interval lies
-    zeros = [i for i in range(ci.V) if w[n][i] == 0]
+    # a zero-weight token is never admissible, wherever its (empty) interval lies (unless its largest
+    # weight within fp32 precision is positive and the draw is in the widened tier)
+    zeros = [i for i in range(ci.V) if d["wmax"][n][i] == 0]
     if zeros:
         z = min(zeros, key=lambda i: abs(cdf[n][i] - float(ci.u[b])))
         g4 = _as_gpu(o, ci.K)
