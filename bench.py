@@ -67,6 +67,13 @@ WORKLOADS = {
     "tree_walk_greedy": dict(kind="walk", B=16, N=60, V=128256, dtype="bf16", T=0.0,
                              desc="greedy tree verify by walking: B=16, 61-node EAGLE-2-like tree (depth 6), "
                                   "V=128256 bf16"),
+    # per-request temperature on the streaming calls (T = 0 requests verified greedily)
+    "chain_mixed": dict(kind="chain", B=64, K=5, V=128256, dtype="f32", T=1.0, temps=(0.0, 0.6, 1.0, 1.4),
+                        desc="chain verify, per-request temperature: B=64 K=5 V=128256 fp32, draft-model logits, "
+                             "T = 0, 0.6, 1.0, 1.4 cycled over the requests (T = 0: greedy, draft rows not read)"),
+    "ngram_mixed": dict(kind="ngram", B=256, K=5, V=151936, dtype="bf16", T=0.8, temps=(0.0, 0.6, 1.0, 1.4),
+                        desc="n-gram prompt-lookup verify, per-request temperature: B=256 K=5 V=151936 bf16, "
+                             "one-hot draft, T = 0, 0.6, 1.0, 1.4 cycled over the requests"),
 }
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 8000.0  # GB300's nominal HBM3e bandwidth (~8 TB/s), for context beside the measured peak
@@ -84,11 +91,11 @@ WALK_SOURCES = ["speculative_decoding_verification_82_gb300/csrc/tree_walk.cuh",
 def make_inputs(name: str, seed: int):
     from speculative_decoding_verification_82_gb300 import synth
 
-    if name == "chain_batched":
+    if name in ("chain_batched", "chain_mixed"):
         return synth.chain_batched(seed=seed)
     if name == "tree_greedy":
         return synth.tree_greedy(seed=seed)
-    if name == "ngram":
+    if name in ("ngram", "ngram_mixed"):
         return synth.ngram(seed=seed)
     if name == "tree_sample":
         return synth.tree_sample(seed=seed)
@@ -105,9 +112,19 @@ def make_inputs(name: str, seed: int):
     raise ValueError(name)
 
 
-def rows_per_request(w: dict) -> int:
+def request_temps(w: dict, B: int):
+    """The per-request temperatures of a workload that has them (cycled over the requests), else None."""
+    return np.resize(np.asarray(w["temps"], np.float32), B) if "temps" in w else None
+
+
+def rows_per_request(w: dict) -> float:
     """Logits rows a request supplies: a walk's draft rows count for the nodes with children (the
-    rows that exist as the draft's output), 20 of the 61 nodes of the benchmark tree."""
+    rows that exist as the draft's output), 20 of the 61 nodes of the benchmark tree; with
+    per-request temperatures a chain request verified greedily reads its K + 1 target rows only
+    (the mean over the batch)."""
+    if w["kind"] == "chain" and "temps" in w:
+        t = request_temps(w, w["B"])
+        return float(np.mean(np.where(t == 0, w["K"] + 1, 2 * w["K"] + 1)))
     if w["kind"] == "chain":
         return 2 * w["K"] + 1
     if w["kind"] in ("ngram", "ngram_pipe"):
@@ -157,7 +174,7 @@ def algorithmic_bytes(w: dict) -> int:
     if w["kind"] == "kv":  # every moved row read once and written once, plus the path arrays
         return 2 * B * rows_per_request(w) * w["W"] + 4 * B * (w["N"] + 1) * 4 + B * 4
     es = 4 if w["dtype"] == "f32" else 2
-    logits = B * rows_per_request(w) * V * es
+    logits = int(round(B * rows_per_request(w))) * V * es
     if w["kind"] in ("tree", "walk"):
         small_in = 2 * B * (w["N"] + 1) * 4
         out = B * 4 + 2 * B * (w["N"] + 1) * 4 + B * 4
@@ -293,10 +310,11 @@ def oracle_run(w: dict, inp, requests, threads: int):
     if w["kind"] == "chain":
         return oracle.verify_chain(inp.dtype, inp.target, inp.draft, inp.B, inp.K, inp.V,
                                    float(inp.temperature), inp.draft_tokens, inp.r, inp.u,
-                                   threads=threads, requests=requests)
+                                   threads=threads, requests=requests, temperatures=request_temps(w, inp.B))
     if w["kind"] == "ngram":
         return oracle.verify_ngram(inp.dtype, inp.target, inp.B, inp.K, inp.V, float(inp.temperature),
-                                   inp.draft_tokens, inp.r, inp.u, threads=threads, requests=requests)
+                                   inp.draft_tokens, inp.r, inp.u, threads=threads, requests=requests,
+                                   temperatures=request_temps(w, inp.B))
     if w["kind"] == "kv":
         b0, b1 = requests
         return oracle.kv_compact_batch(inp["caches"][:KV_ORACLE_CACHES], inp["slots"][b0:b1], inp["parents"][b0:b1],
@@ -445,6 +463,8 @@ class DeviceCase:
         else:
             self.draft = tens(inp.draft, tdt) if w["kind"] == "chain" else None
             self.x, self.r, self.u = tens(inp.draft_tokens), tens(inp.r), tens(inp.u)
+            if "temps" in w:
+                self.temps = tens(request_temps(w, B))
             if w["kind"] == "ngram_pipe":  # the drafts come from the lookup kernel every step
                 self.ctx, self.ctx_len = tens(inp.meta["ctx"]), tens(inp.meta["ctx_len"])
                 dshape = dict(draft_len=(B,), match_n=(B,), match_end=(B,), err_draft=(B,))
@@ -470,7 +490,8 @@ class DeviceCase:
                                 getattr(self, "temps", None)) if t is not None]
         if self.w["kind"] == "ngram_pipe":
             return [self.target, self.ctx, self.ctx_len, self.r, self.u]
-        return [t for t in (self.target, self.draft, self.x, self.r, self.u) if t is not None]
+        return [t for t in (self.target, self.draft, self.x, self.r, self.u, getattr(self, "temps", None))
+                if t is not None]
 
     def abi_args(self):
         """Arguments of the C ABI call itself (device pointers, sizes, the current stream), built once
@@ -506,7 +527,8 @@ class DeviceCase:
         K, V = self.w["K"], self.w["V"]
         tail = (ptr(o["num_accepted"]), ptr(o["out_tokens"]), ptr(o["residual_mass"]), ptr(o["err_flags"]),
                 None, None, None, None)
-        verify = ("spec_verify_ngram", (ptr(self.target), dt, B, K, V, ctypes.c_float(self.T), ptr(self.x),
+        verify = ("spec_verify_ngram", (ptr(self.target), dt, B, K, V, ctypes.c_float(self.T),
+                                        ptr(getattr(self, "temps", None)), ptr(self.x),
                                         ptr(self.r), ptr(self.u), *tail, ws, nbytes, stream))
         if self.w["kind"] == "ngram_pipe":
             d = self.dout
@@ -516,6 +538,7 @@ class DeviceCase:
         if self.w["kind"] == "ngram":
             return [verify]
         return [("spec_verify_chain", (ptr(self.target), ptr(self.draft), dt, B, K, V, ctypes.c_float(self.T),
+                                       ptr(getattr(self, "temps", None)),
                                        ptr(self.x), ptr(self.r), ptr(self.u), *tail, None, ws, nbytes, stream))]
 
     def call(self):
@@ -535,10 +558,12 @@ class DeviceCase:
                                             err_flags=self.dout["err_draft"]))
             return b.spec_verify_ngram(self.target, d["draft_tokens"], self.r, self.u, self.T, workspace=self.ws,
                                        out=self.out)
+        tt = getattr(self, "temps", None)
         if self.w["kind"] == "ngram":
-            return b.spec_verify_ngram(self.target, self.x, self.r, self.u, self.T, workspace=self.ws, out=self.out)
+            return b.spec_verify_ngram(self.target, self.x, self.r, self.u, self.T, workspace=self.ws, out=self.out,
+                                       temperatures=tt)
         return b.spec_verify_chain(self.target, self.draft, self.x, self.r, self.u, self.T, workspace=self.ws,
-                                   out=self.out)
+                                   out=self.out, temperatures=tt)
 
 
 def _e2e_step(dev_case: DeviceCase, host_case: DeviceCase):
@@ -592,8 +617,9 @@ def parity_summary(w: dict, name: str, inp, dev, ws) -> dict:
         st = parity.check_walk(g, o, inp)
     else:
         ngram = kind in ("ngram", "ngram_pipe")
-        g = parity.run_gpu_chain(inp, ngram=ngram, workspace=ws, diag=False)
-        o = parity.run_oracle_chain(inp, ngram=ngram, threads=threads)
+        temps = request_temps(w, inp.B)
+        g = parity.run_gpu_chain(inp, ngram=ngram, workspace=ws, diag=False, temperatures=temps)
+        o = parity.run_oracle_chain(inp, ngram=ngram, threads=threads, temperatures=temps)
         st = parity.check_chain(g, o, inp)
     out = {k: st[k] for k in ("requests", "errors", "flagged_strict", "flagged_wide_only",
                               "admissible_deviations")}
@@ -623,7 +649,8 @@ def measure(args, name: str, w: dict, rank: int, world: int, local: int, primary
         w["moves"] = float(np.mean([kv_moves(inp) for inp in inputs]))
     rows_req = rows_per_request(w)
     tdt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16, "u8": torch.uint8}[w["dtype"]]
-    ws = None if w["kind"] in ("walk", "kv") else binding.make_workspace(w["B"], rows_req, w["V"], tdt, dev)
+    ws_rows = 2 * w["K"] + 1 if w["kind"] == "chain" else int(rows_req)  # (any request may read its draft rows)
+    ws = None if w["kind"] in ("walk", "kv") else binding.make_workspace(w["B"], ws_rows, w["V"], tdt, dev)
     cases = [DeviceCase(w, inp, dev, ws) for inp in inputs]
     stream = torch.cuda.current_stream(dev)
 
@@ -687,7 +714,7 @@ def measure(args, name: str, w: dict, rank: int, world: int, local: int, primary
     mean_call_ms = start.elapsed_time(end) / K  # device time per call, back to back
     del graph
 
-    rows_step = w["B"] * rows_req
+    rows_step = int(round(w["B"] * rows_req))
     value = job_rows_per_s(world, rows_step, K, elapsed_ms)
     alg_bytes = algorithmic_bytes(w)
     read_bytes = float(np.mean(visited)) if visited else float(alg_bytes)

@@ -103,7 +103,13 @@ void spec_verify_workspace_reset(const void *workspace);
  * target_logits  [B][K+1][V] dtype; row k scores draft position k given the accepted prefix,
  *                row K scores the bonus position.
  * draft_logits   [B][K][V] dtype; the draft distribution at each draft position.  Not read
- *                (may be NULL) when temperature == 0.
+ *                (may be NULL) when temperature == 0 and temperatures is NULL.
+ * temperatures   [B] float or NULL: each request's own temperature, used instead of
+ *                `temperature` (the x078.com page's production section sets the temperature per
+ *                request).  0 verifies that request greedily (its draft rows are not read); NaN, a
+ *                negative value or infinity fails the request with SPEC_ERRF_BAD_TEMPERATURE alone.
+ *                When given, draft_logits (K > 0), r and u are required and the workspace is sized
+ *                for 2K + 1 rows.
  * draft_tokens   [B][K] int32, the drafted tokens x_k.
  * r              [B][K] float, acceptance uniforms in (0, 1].  Not read when temperature == 0.
  * u              [B] float, uniforms in [0, 1) for the residual / bonus draw.  Not read when
@@ -122,14 +128,16 @@ void spec_verify_workspace_reset(const void *workspace);
  * cand_tokens    [B][K+1] int32: the token the draw would emit at position k (residual at
  *                k < K, bonus at K; greedy: the argmax of row k).
  * pos_mass       [B][K+1] float: the residual mass at each position (bonus row: 1).
- * target_probs   [B][K+1][V] float: p rows (T > 0 only; an extra launch, for testing).
+ * target_probs   [B][K+1][V] float: p rows (T > 0 only; an extra launch, for testing; with
+ *                per-request temperatures, the rows of greedy requests are left untouched).
  * draft_probs    [B][K][V] float: q rows (T > 0 only).
  * Requesting cand_tokens or pos_mass makes the call draw at every position, which re-reads the
  * pair (draft-model chain) or one chunk per row (n-gram); leave them NULL on the hot path.
  */
 spec_status_t spec_verify_chain(const void *target_logits, const void *draft_logits,
                                 spec_dtype_t dtype, int B, int K, int V, float temperature,
-                                const int32_t *draft_tokens, const float *r, const float *u,
+                                const float *temperatures, const int32_t *draft_tokens,
+                                const float *r, const float *u,
                                 int32_t *num_accepted, int32_t *out_tokens, float *residual_mass,
                                 int32_t *err_flags, float *accept_prob, int32_t *cand_tokens,
                                 float *pos_mass, float *target_probs, float *draft_probs,
@@ -138,11 +146,13 @@ spec_status_t spec_verify_chain(const void *target_logits, const void *draft_log
 /*
  * Chain verification with a prompt n-gram lookup draft: q_k is one-hot at x_k, so
  * alpha_k = p_k(x_k) and the residual at a rejected position is p_k with x_k removed.  No draft
- * logits exist.  Arguments and outputs as spec_verify_chain (target_probs likewise optional);
- * temperature == 0 gives the greedy chain.
+ * logits exist.  Arguments and outputs as spec_verify_chain (target_probs and temperatures
+ * likewise optional; the workspace takes K + 1 rows either way); temperature == 0 gives the
+ * greedy chain.
  */
 spec_status_t spec_verify_ngram(const void *target_logits, spec_dtype_t dtype, int B, int K,
-                                int V, float temperature, const int32_t *draft_tokens,
+                                int V, float temperature, const float *temperatures,
+                                const int32_t *draft_tokens,
                                 const float *r, const float *u, int32_t *num_accepted,
                                 int32_t *out_tokens, float *residual_mass, int32_t *err_flags,
                                 float *accept_prob, int32_t *cand_tokens, float *pos_mass,

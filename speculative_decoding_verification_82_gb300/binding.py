@@ -49,9 +49,9 @@ def library(path: str | None = None) -> ctypes.CDLL:
     lib.spec_verify_workspace_bytes.restype = Z
     lib.spec_verify_workspace_reset.argtypes = [P]
     lib.spec_verify_workspace_reset.restype = None
-    lib.spec_verify_chain.argtypes = [P, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
+    lib.spec_verify_chain.argtypes = [P, P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
     lib.spec_verify_chain.restype = I
-    lib.spec_verify_ngram.argtypes = [P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
+    lib.spec_verify_ngram.argtypes = [P, I, I, I, I, F, P, P, P, P, P, P, P, P, P, P, P, P, P, Z, P]
     lib.spec_verify_ngram.restype = I
     lib.spec_verify_tree_greedy.argtypes = [P, I, I, I, I, P, P, P, P, P, P, P, P, Z, P]
     lib.spec_verify_tree_greedy.restype = I
@@ -129,7 +129,8 @@ def _opt(given, name, dtype, shape, device):
 
 
 def _chain_like(ngram: bool, target_logits, draft_logits, draft_tokens, r, u, temperature,
-                workspace, out, accept_prob, cand_tokens, pos_mass, target_probs, draft_probs):
+                workspace, out, accept_prob, cand_tokens, pos_mass, target_probs, draft_probs,
+                temperatures=None):
     lib = library()
     dev = target_logits.device
     if target_logits.dtype not in DTYPE_CODE or target_logits.dim() != 3:
@@ -141,13 +142,16 @@ def _chain_like(ngram: bool, target_logits, draft_logits, draft_tokens, r, u, te
     if draft_tokens is None:
         draft_tokens = torch.empty((B, K), dtype=torch.int32, device=dev)
     _need(draft_tokens, "draft_tokens", torch.int32, (B, K), dev)
-    if not ngram and T > 0 and K > 0:
+    sampled = T > 0 or temperatures is not None  # per-request temperatures: any request may sample
+    if temperatures is not None:
+        _need(temperatures, "temperatures", torch.float32, (B,), dev)
+    if not ngram and sampled and K > 0:
         _need(draft_logits, "draft_logits", target_logits.dtype, (B, K, V), dev)
-    if T > 0:
+    if sampled:
         _need(r, "r", torch.float32, (B, K), dev)
         _need(u, "u", torch.float32, (B,), dev)
     if workspace is None:
-        rows = 2 * K + 1 if (not ngram and T > 0 and K > 0) else K1
+        rows = 2 * K + 1 if (not ngram and sampled and K > 0) else K1
         workspace = make_workspace(B, rows, V, target_logits.dtype, dev)
     out = dict(out or {})
     na = _out(out.get("num_accepted"), "num_accepted", torch.int32, (B,), dev)
@@ -161,12 +165,13 @@ def _chain_like(ngram: bool, target_logits, draft_logits, draft_tokens, r, u, te
     tail = (_ptr(na), _ptr(ot), _ptr(rm), _ptr(ef), _ptr(ap), _ptr(ct), _ptr(pm), _ptr(tp))
     if ngram:
         st = lib.spec_verify_ngram(_ptr(target_logits), DTYPE_CODE[target_logits.dtype], B, K, V, T,
-                                   _ptr(draft_tokens), _ptr(r), _ptr(u), *tail, _ptr(workspace),
+                                   _ptr(temperatures), _ptr(draft_tokens), _ptr(r), _ptr(u), *tail, _ptr(workspace),
                                    workspace.numel(), _stream(dev))
     else:
         dp = _opt(draft_probs, "draft_probs", torch.float32, (B, K, V), dev)
         st = lib.spec_verify_chain(_ptr(target_logits), _ptr(draft_logits),
-                                   DTYPE_CODE[target_logits.dtype], B, K, V, T, _ptr(draft_tokens),
+                                   DTYPE_CODE[target_logits.dtype], B, K, V, T, _ptr(temperatures),
+                                   _ptr(draft_tokens),
                                    _ptr(r), _ptr(u), *tail, _ptr(dp), _ptr(workspace),
                                    workspace.numel(), _stream(dev))
     _check(st)
@@ -175,19 +180,21 @@ def _chain_like(ngram: bool, target_logits, draft_logits, draft_tokens, r, u, te
 
 def spec_verify_chain(target_logits, draft_logits, draft_tokens, r, u, temperature, *,
                       workspace=None, out=None, accept_prob=None, cand_tokens=None, pos_mass=None,
-                      target_probs=None, draft_probs=None) -> dict:
-    """Chain verification with draft logits (draft model / EAGLE head).  See spec_verify.h."""
+                      target_probs=None, draft_probs=None, temperatures=None) -> dict:
+    """Chain verification with draft logits (draft model / EAGLE head); `temperatures` [B] gives
+    each request its own T.  See spec_verify.h."""
     return _chain_like(False, target_logits, draft_logits, draft_tokens, r, u, temperature,
                        workspace, out, accept_prob, cand_tokens, pos_mass, target_probs,
-                       draft_probs)
+                       draft_probs, temperatures)
 
 
 def spec_verify_ngram(target_logits, draft_tokens, r, u, temperature, *, workspace=None, out=None,
                       accept_prob=None, cand_tokens=None, pos_mass=None,
-                      target_probs=None) -> dict:
-    """Chain verification with a one-hot (prompt n-gram lookup) draft.  See spec_verify.h."""
+                      target_probs=None, temperatures=None) -> dict:
+    """Chain verification with a one-hot (prompt n-gram lookup) draft; `temperatures` [B] gives
+    each request its own T.  See spec_verify.h."""
     return _chain_like(True, target_logits, None, draft_tokens, r, u, temperature, workspace, out,
-                       accept_prob, cand_tokens, pos_mass, target_probs, None)
+                       accept_prob, cand_tokens, pos_mass, target_probs, None, temperatures)
 
 
 def spec_verify_tree_greedy(target_logits, node_tokens, parents, *, workspace=None, out=None,

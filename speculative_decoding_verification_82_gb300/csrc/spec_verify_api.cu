@@ -199,7 +199,8 @@ spec_status_t launch(spec_dtype_t dtype, int mode, Params& P, specv::LaunchPlan&
 
 // Shared body of spec_verify_chain / spec_verify_ngram.
 spec_status_t verify_chain_common(bool ngram, const void* target, const void* draft, spec_dtype_t dtype, int B,
-                                  int K, int V, float T, const int32_t* x, const float* r, const float* u,
+                                  int K, int V, float T, const float* temps, const int32_t* x, const float* r,
+                                  const float* u,
                                   int32_t* num_accepted, int32_t* out_tokens, float* residual_mass,
                                   int32_t* err_flags, float* accept_prob, int32_t* cand_tokens, float* pos_mass,
                                   float* target_probs, float* draft_probs, void* ws, size_t ws_bytes,
@@ -208,7 +209,8 @@ spec_status_t verify_chain_common(bool ngram, const void* target, const void* dr
   if (!(T >= 0.f) || isinf(T)) return SPEC_ERR_INVALID_ARG;
   if (K > SPEC_MAX_K) return SPEC_ERR_UNSUPPORTED;
   if (B == 0) return SPEC_OK;
-  const bool greedy = (T == 0.f);
+  // with per-request temperatures any request may sample: draft logits (chain), r and u are needed
+  const bool greedy = (T == 0.f) && !temps;
   const bool two_rows = !ngram && !greedy && K > 0;
   if (!target || !num_accepted || !out_tokens) return SPEC_ERR_INVALID_ARG;
   if (K > 0 && !x) return SPEC_ERR_INVALID_ARG;
@@ -243,7 +245,8 @@ spec_status_t verify_chain_common(bool ngram, const void* target, const void* dr
   P.R = K + 1;
   P.rows = rows;
   P.diag = diag;
-  P.c = greedy ? 0.f : (float)(1.4426950408889634 / (double)T);  // log2(e) / T
+  P.c = (greedy || temps) ? 0.f : (float)(1.4426950408889634 / (double)T);  // log2(e) / T
+  P.temps = temps;
   P.draft_tokens = x;
   P.r = r;
   P.u = u;
@@ -260,7 +263,8 @@ spec_status_t verify_chain_common(bool ngram, const void* target, const void* dr
   L.sm_count = sms;
   L.device = device;
   L.launch_probs = (P.target_probs || P.draft_probs) ? 1 : 0;
-  const int mode = greedy ? specv::kGreedy : (ngram ? specv::kNgram : specv::kChain);
+  const int mode = temps ? (int)(ngram ? specv::kNgramPT : specv::kChainPT)
+                         : (int)(greedy ? specv::kGreedy : (ngram ? specv::kNgram : specv::kChain));
   return launch(dtype, mode, P, L, reinterpret_cast<cudaStream_t>(stream));
 }
 
@@ -281,22 +285,25 @@ void spec_verify_workspace_reset(const void* workspace) {
 }
 
 spec_status_t spec_verify_chain(const void* target_logits, const void* draft_logits, spec_dtype_t dtype, int B,
-                                int K, int V, float temperature, const int32_t* draft_tokens, const float* r,
-                                const float* u, int32_t* num_accepted, int32_t* out_tokens, float* residual_mass,
-                                int32_t* err_flags, float* accept_prob, int32_t* cand_tokens, float* pos_mass,
-                                float* target_probs, float* draft_probs, void* workspace, size_t workspace_bytes,
-                                spec_stream_t stream) {
-  return verify_chain_common(false, target_logits, draft_logits, dtype, B, K, V, temperature, draft_tokens, r, u,
+                                int K, int V, float temperature, const float* temperatures,
+                                const int32_t* draft_tokens, const float* r, const float* u, int32_t* num_accepted,
+                                int32_t* out_tokens, float* residual_mass, int32_t* err_flags, float* accept_prob,
+                                int32_t* cand_tokens, float* pos_mass, float* target_probs, float* draft_probs,
+                                void* workspace, size_t workspace_bytes, spec_stream_t stream) {
+  return verify_chain_common(false, target_logits, draft_logits, dtype, B, K, V, temperature, temperatures,
+                             draft_tokens, r, u,
                              num_accepted, out_tokens, residual_mass, err_flags, accept_prob, cand_tokens, pos_mass,
                              target_probs, draft_probs, workspace, workspace_bytes, stream);
 }
 
 spec_status_t spec_verify_ngram(const void* target_logits, spec_dtype_t dtype, int B, int K, int V,
-                                float temperature, const int32_t* draft_tokens, const float* r, const float* u,
-                                int32_t* num_accepted, int32_t* out_tokens, float* residual_mass, int32_t* err_flags,
-                                float* accept_prob, int32_t* cand_tokens, float* pos_mass, float* target_probs,
-                                void* workspace, size_t workspace_bytes, spec_stream_t stream) {
-  return verify_chain_common(true, target_logits, nullptr, dtype, B, K, V, temperature, draft_tokens, r, u,
+                                float temperature, const float* temperatures, const int32_t* draft_tokens,
+                                const float* r, const float* u, int32_t* num_accepted, int32_t* out_tokens,
+                                float* residual_mass, int32_t* err_flags, float* accept_prob, int32_t* cand_tokens,
+                                float* pos_mass, float* target_probs, void* workspace, size_t workspace_bytes,
+                                spec_stream_t stream) {
+  return verify_chain_common(true, target_logits, nullptr, dtype, B, K, V, temperature, temperatures,
+                             draft_tokens, r, u,
                              num_accepted, out_tokens, residual_mass, err_flags, accept_prob, cand_tokens, pos_mass,
                              target_probs, nullptr, workspace, workspace_bytes, stream);
 }

@@ -62,7 +62,7 @@ extern "C" spec_status_t spec_verify_chain_static(const void* target_logits, con
   // the counters at zero, which each call does before it ends, a call whose device wait timed out
   // included (its last CTA zeroes them).  Statistics left behind carry an older call's tag and are
   // never taken.
-  return spec_verify_chain(target_logits, draft_logits, dtype, B, K, V, temperature, draft_tokens, r, u,
+  return spec_verify_chain(target_logits, draft_logits, dtype, B, K, V, temperature, nullptr, draft_tokens, r, u,
                            num_accepted, out_tokens, residual_mass, err_flags, nullptr, nullptr, nullptr,
                            nullptr, nullptr, scratch, (size_t)SPEC_STATIC_WORKSPACE_BYTES, stream);
 }

@@ -36,6 +36,12 @@
 namespace specv {
 
 enum Mode : int { kChain = 0, kNgram = 1, kGreedy = 2, kTree = 3 };
+// Host-side launch modes of the per-request-temperature chain and n-gram calls (the kernel runs
+// MODE kChain / kNgram with PT = true).
+enum LaunchMode : int { kChainPT = 4, kNgramPT = 5 };
+// The high half of a request's first result word: n | kNoResid for a request verified greedily in a
+// per-request-temperature call (no residual pass follows), | err << 16.
+constexpr unsigned kNoResid = 0x8000u;
 enum Kind : int { kFullP = 0, kExcl = 1 };
 enum ItemKind : int { kItemStats = 0, kItemResid = 1, kItemSkip = 2, kItemEnd = 3 };
 
@@ -91,7 +97,8 @@ struct Params {
   int nchunk_r;    // residual items per row (kResVec target vectors each)
   int npos;          // residual positions per request (K with per-position outputs, else 1); 0: none
   int diag;          // 1: draw at every position (per-position outputs requested)
-  float c;           // log2(e) / T
+  float c;           // log2(e) / T (calls with one temperature)
+  const float* temps;  // [B] per-request temperatures (calls with PT = true), else nullptr
   unsigned total;    // stats items (A per request)
   unsigned total_r;  // residual items (R per request)
   // the divisors of the item decoding: A = rows * nchunk stats items per request, R = npos *
@@ -140,6 +147,31 @@ __device__ __forceinline__ const char* row_ptr(const Params& P, int b, int r) {
   constexpr int S = Elem<T>::kSize;
   if (r < P.R) return static_cast<const char*>(P.target) + ((size_t)b * P.R + r) * (size_t)P.V * S;
   return static_cast<const char*>(P.draft) + ((size_t)b * P.K + (r - P.R)) * (size_t)P.V * S;
+}
+
+// A request's temperature as the kernel uses it: c = log2(e) / T, and whether the request is
+// verified greedily (T == 0, or a temperature that fails it, which is read like a greedy one).
+// With one temperature per call (PT = false) every request takes the call's.
+struct ReqTemp {
+  float c;
+  int greedy;  // argmax statistics; no draft rows, no draws
+  int bad;     // a NaN, negative or infinite temperature: the request fails
+};
+template <int MODE, bool PT>
+__device__ __forceinline__ ReqTemp req_temp(const Params& P, int b) {
+  ReqTemp t;
+  if constexpr (!PT) {
+    t.c = P.c;
+    t.greedy = (MODE == kGreedy || MODE == kTree) ? 1 : 0;
+    t.bad = 0;
+  } else {
+    const float T = __ldg(P.temps + b);
+    t.bad = (!(T >= 0.f) || isinf(T)) ? 1 : 0;
+    t.greedy = (t.bad || T == 0.f) ? 1 : 0;
+    // formed in double exactly as the host forms a call's own c
+    t.c = t.greedy ? 0.f : (float)(1.4426950408889634 / (double)T);
+  }
+  return t;
 }
 
 // Weight of a chunk (or sub-chunk) relative to the row maximum: s * 2^(RN(a c) - mc), in fp32 (the
@@ -211,6 +243,8 @@ struct StageMeta {
   int e_lo, e_hi;  // residual: elements [e_lo, e_hi)
   int dshift;      // residual: draft position = kDraftSlot * VE + (e - e_base) + dshift
   float mct, mcd, rho;
+  float c;     // log2(e) / T of the item's request
+  int greedy;  // the item's request is verified greedily (argmax statistics)
 };
 struct SlotMeta {
   int kind;        // ItemKind
@@ -338,7 +372,7 @@ __device__ __forceinline__ void resid_weights(const unsigned char* buf, int dslo
 // result words at the start of each stats batch and uses them at the next, so that the read does
 // not hold it up.  Only once its stats items are out does it wait (bounded) for a result.  Once
 // both kinds are exhausted it publishes one end marker.
-template <int MODE, typename T>
+template <int MODE, typename T, bool PT>
 __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages, int grp) {
   const int lane = threadIdx.x & 31;
   // stats claims: batches of consecutive items, the next batch claimed one batch ahead.  Each
@@ -363,7 +397,10 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
   int it = grp;
   // residual parameters of the last request seen (consecutive residual items share them)
   int rb = -1, rk = 0, rerr = 1;
-  float rmct = 0.f, rmcd = 0.f, rrho = 0.f;
+  float rmct = 0.f, rmcd = 0.f, rrho = 0.f, rcc = P.c;
+  // per-request temperatures: the temperature of the last request whose stats item was seen
+  int tb = -1;
+  ReqTemp trt{P.c, 0, 0};
   for (;; it += kGroups) {
     const int s = it % kStages;
     if (!mbar_wait_warp(&sm.empty[s], ((uint32_t)(it / kStages) & 1u) ^ 1u, &sm.abort)) {
@@ -377,6 +414,8 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
     m.e_base = 0;
     m.e_lo = m.e_hi = m.dshift = 0;
     m.mct = m.mcd = m.rho = 0.f;
+    m.c = P.c;
+    m.greedy = 0;
     m.kind = kItemEnd;
     long long t_poll = 0;
     for (;;) {  // until this stage has an item (a residual batch of a request without a draw is dropped)
@@ -454,6 +493,15 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
         decode_stats(P, w, m.b, off);
         m.row = (int)fdiv((unsigned)off, P.fd_nchunk);
         m.ch = off - m.row * P.nchunk;
+        if constexpr (PT) {
+          if (m.b != tb) {
+            tb = m.b;
+            trt = req_temp<MODE, PT>(P, m.b);
+          }
+          if (trt.greedy && m.row >= P.R) continue;  // a greedy request's draft rows are not read
+          m.c = trt.c;
+          m.greedy = trt.greedy;
+        }
         const RowGrid<T> g = row_grid<T>(row_ptr<T>(P, m.b, m.row), P.V);
         const int v0 = m.ch * kChunkVec, v1 = min(v0 + kChunkVec, g.nvec);
         m.nvec = max(0, v1 - v0);
@@ -481,8 +529,9 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
           const unsigned h3 = __shfl_sync(kFull, req_word_hi(q3), 0);
           rb = m.b;
           const int n = (int)(h0 & 0xFFFFu);
-          rerr = (int)(h0 >> 16);
+          rerr = (int)(h0 >> 16) | (int)(h0 & kNoResid);  // (a greedy request has no residual pass)
           rk = P.diag ? m.kk : n;
+          if constexpr (PT) rcc = req_temp<MODE, PT>(P, m.b).c;
           if (!rerr && rk < P.K) {
             if (P.diag) {
               // per-position parameters come from the row statistics, written before the result
@@ -508,6 +557,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
         m.mct = rmct;
         m.mcd = rmcd;
         m.rho = rrho;
+        m.c = rcc;
         const ResGeo<T> q = res_geo<T>(P, m.b, rk, m.ch * kResVec, kResVec);
         m.nvec = max(0, q.vt1 - q.vt0);
         m.e_base = q.e_base;
@@ -637,13 +687,14 @@ __device__ __forceinline__ float4 consume_resid(const unsigned char* buf, const 
 // The group's last warp to leave its partial in slot j merges the partials, writes the chunk's
 // statistics (stats items: the chunk and its sub-chunks; residual items: the sum and the sub-range
 // sums) and hands the slot to the bookkeeping warp.
-template <int MODE>
+template <int MODE, bool PT>
 __device__ __forceinline__ void publish_chunk(const Params& P, Shared& sm, const StageMeta& m, int j) {
   constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
+  const bool soft = PT ? !m.greedy : kSoftmax;  // (per request with per-request temperatures)
   const int lane = threadIdx.x & 31;
   const bool mine = lane < kGroupWarps;
   const float4 pw = sm.part[j][lane % kGroupWarps];
-  const float c = P.c;
+  const float c = PT ? m.c : P.c;
   SlotMeta pm;
   pm.kind = m.kind;
   pm.tick = nullptr;
@@ -651,7 +702,7 @@ __device__ __forceinline__ void publish_chunk(const Params& P, Shared& sm, const
     const size_t ci = ((size_t)m.b * P.rows + m.row) * P.nchunk + m.ch;
     uint4 q;
     // lanes 0..kGroupWarps-1 hold the warp partials; xor-shuffles within those lanes merge them
-    if constexpr (kSoftmax) {
+    if (soft) {
       float M = mine ? pw.x : -INFINITY;
 #pragma unroll
       for (int o = 1; o < kGroupWarps; o <<= 1) M = fmax_nan(M, __shfl_xor_sync(kFull, M, o));
@@ -693,7 +744,7 @@ __device__ __forceinline__ void publish_chunk(const Params& P, Shared& sm, const
 }
 
 // Group g takes items g, g + 2, g + 4, ... (stage it % kStages, slot it % kSlots).
-template <int MODE, typename T>
+template <int MODE, typename T, bool PT>
 __device__ void consumer_loop(const Params& P, Shared& sm, const unsigned char* stages) {
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int grp = warp / kGroupWarps, gw = warp % kGroupWarps;
@@ -706,10 +757,14 @@ __device__ void consumer_loop(const Params& P, Shared& sm, const unsigned char* 
     const StageMeta m = sm.meta[s];
     const unsigned char* buf = stages + (size_t)s * kStageBytes;
     float4 part = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (m.kind == kItemStats)
-      part = consume_stats<MODE, T>(buf, m, P.c, gw);
-    else if (m.kind == kItemResid)
-      part = consume_resid<T>(buf, m, P.c, gw);
+    if (m.kind == kItemStats) {
+      if constexpr (PT)  // the item's request decides between softmax and argmax statistics
+        part = m.greedy ? consume_stats<kGreedy, T>(buf, m, 0.f, gw) : consume_stats<MODE, T>(buf, m, m.c, gw);
+      else
+        part = consume_stats<MODE, T>(buf, m, P.c, gw);
+    } else if (m.kind == kItemResid) {
+      part = consume_resid<T>(buf, m, PT ? m.c : P.c, gw);
+    }
     __syncwarp();
     if (lane == 0) mbar_arrive(&sm.empty[s]);
     const int j = it % kSlots;
@@ -724,7 +779,7 @@ __device__ void consumer_loop(const Params& P, Shared& sm, const unsigned char* 
       last = atomicAdd(&sm.pcnt[j], 1) == kGroupWarps - 1;
       __threadfence_block();
     }
-    if (__shfl_sync(kFull, last, 0)) publish_chunk<MODE>(P, sm, m, j);
+    if (__shfl_sync(kFull, last, 0)) publish_chunk<MODE, PT>(P, sm, m, j);
     if (m.kind == kItemEnd) return;
   }
 }
@@ -903,11 +958,11 @@ __device__ __forceinline__ bool await_tagged(const Params& P, Shared& sm, const 
 // orders that acquisition, and the group's earlier reads of the buffers, before the copies.  When
 // the statistics do not fit, the group waits for their tags in global memory instead.
 __device__ __forceinline__ CsReader stage_request_stats(const Params& P, Shared& sm, int b, SsRows& ss,
-                                                        uint32_t& csph) {
-  const int n = P.rows * P.nchunk;
+                                                        uint32_t& csph, int rows) {
+  const int n = rows * P.nchunk;  // the request's first `rows` rows (a greedy request: no draft rows)
   const int nss = P.nchunk * kGroupWarps;
   CsReader rd;
-  rd.g = P.cstat + (size_t)b * n;
+  rd.g = P.cstat + (size_t)b * P.rows * P.nchunk;  // (the request's block holds P.rows rows)
   rd.nchunk = P.nchunk;
   rd.s = nullptr;
   if (n > kFinCs) {
@@ -1022,10 +1077,11 @@ __device__ DrawPlan draw_begin(const Params& P, Shared& sm, unsigned char* fbuf,
 
 template <typename T>
 __device__ int draw_end(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph, int b,
-                        const DrawPlan& d, const CsReader& rd, const RowStat& rs, float u, float* mass_out) {
+                        const DrawPlan& d, const CsReader& rd, const RowStat& rs, float u, float c,
+                        float* mass_out) {
   constexpr int VE = Elem<T>::kPerVec;
   const int ft = fin_thread(), lane = ft & 31;
-  const float c = P.c, mc = rs.mc;
+  const float mc = rs.mc;
   const int row = d.row;
   const RowGrid<T> g = row_grid<T>(row_ptr<T>(P, b, row), P.V);
   const ChunkStat* srow = P.sstat + ((size_t)b * P.rows + row) * P.nchunk * kGroupWarps;
@@ -1146,23 +1202,29 @@ __device__ int draw_end(const Params& P, Shared& sm, unsigned char* fbuf, uint32
 // Combines the chunk statistics of every row of request b into RowStat.  G threads share a row
 // (G a power of two: each takes chunks g, g + G, ... and a butterfly over the G threads merges
 // them); G grows while the group still covers every row in one pass.
-template <int MODE>
-__device__ void combine_rows(const Params& P, Shared& sm, int b, const CsReader& rd) {
-  constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
+// With per-request temperatures (PT) `soft` (softmax or argmax statistics), `cr` (log2(e) / T) and
+// `rows` (the rows the request read) are the request's; otherwise the call's.
+template <int MODE, bool PT>
+__device__ void combine_rows(const Params& P, Shared& sm, int b, const CsReader& rd, bool soft_r, float cr,
+                             int rows_r) {
+  constexpr bool kSoftmaxMode = (MODE == kChain || MODE == kNgram);
+  const bool kSoftmax = PT ? soft_r : kSoftmaxMode;
+  const float c = PT ? cr : P.c;
+  const int rows = PT ? rows_r : P.rows;
   const int ft = fin_thread();
   const int nch = P.nchunk;
   int G = 1;
-  while (G < 32 && G < nch && P.rows * 2 * G <= kFinThreads) G <<= 1;
+  while (G < 32 && G < nch && rows * 2 * G <= kFinThreads) G <<= 1;
   const int g = ft & (G - 1);
   const int rpp = kFinThreads / G;
-  for (int r0 = 0; r0 < P.rows; r0 += rpp) {
+  for (int r0 = 0; r0 < rows; r0 += rpp) {
     const int r = r0 + ft / G;
-    const bool act = r < P.rows;
+    const bool act = r < rows;
     float m = -INFINITY;
     int fl = 0;
     if (act) {
-      for (int c = g; c < nch; c += G) {
-        const ChunkStat q = rd(r, c);
+      for (int ch = g; ch < nch; ch += G) {
+        const ChunkStat q = rd(r, ch);
         m = fmax_nan(m, q.a);
         if (isnan(q.a) || (kSoftmax && q.a == INFINITY)) fl |= SPEC_ERRF_NONFINITE;
       }
@@ -1174,13 +1236,13 @@ __device__ void combine_rows(const Params& P, Shared& sm, int b, const CsReader&
     RowStat rs;
     rs.pad[0] = rs.pad[1] = rs.pad[2] = 0;
     if (kSoftmax) {
-      const float mc = __fmul_rn(m, P.c);
+      const float mc = __fmul_rn(m, c);
       const bool finite_m = !isnan(m) && m != INFINITY && m != -INFINITY;
       float z = 0.f;
       if (act && !fl && finite_m) {
-        for (int c = g; c < nch; c += G) {
-          const ChunkStat q = rd(r, c);
-          z = __fadd_rn(z, chunk_weight(q.a, q.s, P.c, mc));
+        for (int ch = g; ch < nch; ch += G) {
+          const ChunkStat q = rd(r, ch);
+          z = __fadd_rn(z, chunk_weight(q.a, q.s, c, mc));
         }
       }
       for (int o = G >> 1; o > 0; o >>= 1) z = __fadd_rn(z, __shfl_xor_sync(kFull, z, o));
@@ -1193,8 +1255,8 @@ __device__ void combine_rows(const Params& P, Shared& sm, int b, const CsReader&
       // lowest index among the chunks whose maximum equals the row maximum
       int idx = INT_MAX;
       if (act) {
-        for (int c = g; c < nch; c += G) {
-          const ChunkStat q = rd(r, c);
+        for (int ch = g; ch < nch; ch += G) {
+          const ChunkStat q = rd(r, ch);
           if (q.a == m) idx = min(idx, __float_as_int(q.s));
         }
       }
@@ -1243,17 +1305,21 @@ __device__ __forceinline__ ReqPrefetch prefetch_request(const Params& P, int b) 
 // Chain / n-gram / greedy-chain finishing: alpha, acceptance scan (section I.1 step 2), outputs,
 // publication of the acceptance result, and the draws made here (bonus row; n-gram residual).
 // Returns the accepted length (or -1 after an error) in every thread.  pf is the leader's.
-template <int MODE, typename T>
+template <int MODE, typename T, bool PT>
 __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& csph,
-                            uint32_t& ssph, int b, const ReqPrefetch& pf) {
+                            uint32_t& ssph, int b, const ReqPrefetch& pf, const ReqTemp& rt) {
   constexpr int S = Elem<T>::kSize;
   constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
+  // per-request temperatures: this request's statistics kind, c and rows (greedy: target rows only)
+  const bool soft = PT ? !rt.greedy : kSoftmax;
+  const float c = PT ? rt.c : P.c;
+  const int rows = (PT && rt.greedy) ? P.R : P.rows;
   const int ft = fin_thread(), lane = ft & 31;
   const int K = P.K;
   // the rows a draw here may read: every n-gram target row, the bonus row of a draft-model chain
-  SsRows st{MODE == kNgram ? 0 : K, kSoftmax ? (MODE == kNgram ? K + 1 : 1) : 0};
-  const CsReader rd = stage_request_stats(P, sm, b, st, csph);
-  combine_rows<MODE>(P, sm, b, rd);
+  SsRows st{MODE == kNgram ? 0 : K, soft ? (MODE == kNgram ? K + 1 : 1) : 0};
+  const CsReader rd = stage_request_stats(P, sm, b, st, csph, rows);
+  combine_rows<MODE, PT>(P, sm, b, rd, soft, c, rows);
   if (ft < 32) {
     const int x0 = pf.x0;
     const float r0 = pf.r0, lx0 = pf.lx0, dx0 = pf.dx0;
@@ -1265,11 +1331,11 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
         e |= SPEC_ERRF_BAD_TOKEN;
       } else {
         const RowStat t = read_rowstat(P, sm, b, k);
-        if (kSoftmax) {
+        if (soft) {
           // alpha = p(x) / q(x) = 2^((l_x c - mc_t) - (d_x c - mc_d)) Z_d / Z_t (draft model), or
           // p(x) = 2^(l_x c - mc_t) / Z_t (one-hot draft); capped at 1
           const float lx = k < 32 ? lx0 : Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, k) + (size_t)x * S));
-          const Exp2 ext = scaled_logit(lx, P.c, t.mc);
+          const Exp2 ext = scaled_logit(lx, c, t.mc);
           if (MODE == kChain) {
             const RowStat d = read_rowstat(P, sm, b, P.R + k);
             const float dx =
@@ -1280,7 +1346,7 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
               alpha = 0.f;  // p(x) = 0
             } else {
               const float ratio =
-                  exp2_times(exp2_sub(ext, scaled_logit(dx, P.c, d.mc)), __fdiv_rn((float)d.Z, (float)t.Z));
+                  exp2_times(exp2_sub(ext, scaled_logit(dx, c, d.mc)), __fdiv_rn((float)d.Z, (float)t.Z));
               alpha = fminf(ratio, 1.f);
             }
           } else {
@@ -1293,8 +1359,9 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
       }
       sm.alpha[k] = alpha;
     }
-    for (int r = lane; r < P.rows; r += 32) e |= read_rowstat(P, sm, b, r).err;
-    const int err = warp_or(e);
+    for (int r = lane; r < rows; r += 32) e |= read_rowstat(P, sm, b, r).err;
+    // a bad per-request temperature fails the request with that bit alone
+    const int err = (PT && rt.bad) ? SPEC_ERRF_BAD_TEMPERATURE : warp_or(e);
     __syncwarp();
     int n = 0;
     if (!err) {
@@ -1305,7 +1372,7 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
         if (k < K) {
           const float a = sm.alpha[k];
           const float rk = k < 32 ? r0 : __ldg(P.r + (size_t)b * K + k);
-          rej = kSoftmax ? !(rk <= a) : (a != 1.f);
+          rej = soft ? !(rk <= a) : (a != 1.f);
         }
         const unsigned msk = __ballot_sync(kFull, rej);
         if (msk) {
@@ -1322,9 +1389,9 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
       __syncwarp();
       __threadfence();
     }
-    const bool resid = MODE == kChain && P.npos > 0 && !P.diag && !err && n < K;
+    const bool resid = MODE == kChain && P.npos > 0 && !P.diag && !err && n < K && soft;
     if (lane == 0 || (resid && lane < 4)) {
-      unsigned hi = (unsigned)n | ((unsigned)err << 16);
+      unsigned hi = (unsigned)n | ((unsigned)err << 16) | (soft ? 0u : kNoResid);
       if (lane > 0) {
         const RowStat t = read_rowstat(P, sm, b, n), d = read_rowstat(P, sm, b, P.R + n);
         hi = __float_as_uint(lane == 1 ? t.mc : lane == 2 ? d.mc : __fdiv_rn((float)t.Z, (float)d.Z));
@@ -1342,7 +1409,7 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
   const int n = sm.gs.out[0], err = sm.gs.out[1], xn = sm.gs.out[2];
   // The emitted token's draw (n-gram at any n, the bonus row of a draft-model chain) starts its
   // copies now, so that they overlap the outputs and the publication below.
-  const bool early = kSoftmax && !err && !P.diag && (MODE == kNgram || n == K);
+  const bool early = soft && !err && !P.diag && (MODE == kNgram || n == K);
   DrawPlan dp{};
   if (early) dp = draw_begin<T>(P, sm, fbuf, b, n, (MODE == kNgram && n < K) ? kExcl : kFullP, n < K ? xn : -1, st);
   if (ft < 32) {
@@ -1351,20 +1418,21 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
       const size_t o_i = (size_t)b * (K + 1) + i;
       int o = -1;
       if (!err && i < n) o = i < 32 ? x0 : __ldg(P.draft_tokens + (size_t)b * K + i);
-      if (!err && i == n && !kSoftmax) o = read_rowstat(P, sm, b, n).amax;
+      if (!err && i == n && !soft) o = read_rowstat(P, sm, b, n).amax;
       P.out_tokens[o_i] = o;
       if (P.accept_prob && i < K) P.accept_prob[(size_t)b * K + i] = err ? 0.f : sm.alpha[i];
-      if (P.cand_tokens && (err || !kSoftmax)) P.cand_tokens[o_i] = err ? -1 : read_rowstat(P, sm, b, i).amax;
-      if (P.pos_mass && (err || !kSoftmax)) P.pos_mass[o_i] = err ? 0.f : 1.f;
+      if (P.cand_tokens && (err || !soft)) P.cand_tokens[o_i] = err ? -1 : read_rowstat(P, sm, b, i).amax;
+      if (P.pos_mass && (err || !soft)) P.pos_mass[o_i] = err ? 0.f : 1.f;
     }
     if (lane == 0) {
       P.num_accepted[b] = n;
       if (P.err_flags) P.err_flags[b] = err;
-      if (P.residual_mass && (err || !kSoftmax)) P.residual_mass[b] = err ? 0.f : 1.f;
+      if (P.residual_mass && (err || !soft)) P.residual_mass[b] = err ? 0.f : 1.f;
     }
   }
   if constexpr (kSoftmax) {
     if (err) return -1;
+    if (!soft) return n;  // a greedy request of a per-request-temperature call: no draw
     auto emit = [&](int k, int tok, float mass) {
       if (ft == 0) {
         const size_t o_k = (size_t)b * (K + 1) + k;
@@ -1379,7 +1447,7 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
     const float u = pf.u;  // used by the leader only
     if (early) {
       float mass;
-      const int tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, dp, rd, read_rowstat(P, sm, b, n), u, &mass);
+      const int tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, dp, rd, read_rowstat(P, sm, b, n), u, c, &mass);
       emit(n, tok, mass);
     } else if (P.diag) {
       // per-position outputs: a draw at every position made here (the bonus row, and for
@@ -1389,7 +1457,7 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
         const int x = k < K ? __ldg(P.draft_tokens + (size_t)b * K + k) : -1;
         const DrawPlan d = draw_begin<T>(P, sm, fbuf, b, k, kind, x, st);
         float mass;
-        const int tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, d, rd, read_rowstat(P, sm, b, k), u, &mass);
+        const int tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, d, rd, read_rowstat(P, sm, b, k), u, c, &mass);
         emit(k, tok, mass);
       }
     }
@@ -1401,7 +1469,7 @@ __device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, ui
 // slot kk) is in.
 template <typename T>
 __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph,
-                              int b, int kk, int n) {
+                              int b, int kk, int n, float c) {
   constexpr int VE = Elem<T>::kPerVec;
   const int ft = fin_thread(), lane = ft & 31;
   const int k = P.diag ? kk : n;
@@ -1481,7 +1549,7 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
   if (state == 1) {
     const bool ok = fin_wait_only(P, sm, &sm.fin_bar, fph);
     const ResGeo<T> q = res_geo<T>(P, b, k, cstar * kResVec + sstar * kResSub, kResSub);
-    const float c = P.c, mct = ts.mc, mcd = ds.mc;
+    const float mct = ts.mc, mcd = ds.mc;
     const float rho = __fdiv_rn((float)ts.Z, (float)ds.Z);
     auto wf = [&](int v, float (&w)[VE]) {
       resid_weights<T>(fbuf, kFinDraftSlot, v, q.e_base, q.e_lo, q.e_hi, q.dshift, c, mct, mcd, rho, w);
@@ -1496,7 +1564,7 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
     rd.s = nullptr;
     rd.nchunk = P.nchunk;
     const DrawPlan d = draw_begin<T>(P, sm, fbuf, b, k, kFullP, -1, none);
-    tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, d, rd, ts, u, &unused);
+    tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, d, rd, ts, u, c, &unused);
   }
   if (ft == 0) {
     const size_t o_k = (size_t)b * (P.K + 1) + k;
@@ -1601,7 +1669,7 @@ __device__ __forceinline__ bool wait_count(const Params& P, Shared& sm, const un
 
 // The finishing group's loop over its requests.  A request's inputs are loaded while its chunks
 // are still being read.
-template <int MODE, typename T>
+template <int MODE, typename T, bool PT>
 __device__ void fin_loop(const Params& P, Shared& sm, unsigned char* fbuf) {
   const int ft = fin_thread();
   uint32_t fph = 0, csph = 0, ssph = 0;
@@ -1618,23 +1686,26 @@ __device__ void fin_loop(const Params& P, Shared& sm, unsigned char* fbuf) {
       if (!wait_count(P, sm, P.tick_a + b, per_req)) return;
       if (ft == 0) P.tick_a[b] = 0;  // complete: the count is left as the next call expects it
       SsRows none{0, 0};
-      const CsReader rd = stage_request_stats(P, sm, b, none, csph);
-      combine_rows<MODE>(P, sm, b, rd);
+      const CsReader rd = stage_request_stats(P, sm, b, none, csph, P.rows);
+      combine_rows<MODE, false>(P, sm, b, rd, false, 0.f, P.rows);
       walk_tree(P, sm, b);
       fin_sync();  // the walk's reads of the shared copies come before the next request's writes
     } else {
+      const ReqTemp rt = req_temp<MODE, PT>(P, b);
+      // a greedy request of a per-request-temperature call has its target rows' chunks only
+      const unsigned want = (PT && rt.greedy) ? (unsigned)(P.R * P.nchunk) : per_req;
       ReqPrefetch pf{0, 0.f, 0.f, 0.f, 0.f};
       if (ft < 32) pf = prefetch_request<MODE, T>(P, b);
-      if (!wait_count(P, sm, P.tick_a + b, per_req)) return;
+      if (!wait_count(P, sm, P.tick_a + b, want)) return;
       if (ft == 0) P.tick_a[b] = 0;  // complete: the count is left as the next call expects it
-      const int n = finish_chain<MODE, T>(P, sm, fbuf, fph, csph, ssph, b, pf);
+      const int n = finish_chain<MODE, T, PT>(P, sm, fbuf, fph, csph, ssph, b, pf, rt);
       if constexpr (MODE == kChain) {
-        if (P.npos > 0 && n >= 0) {
+        if (P.npos > 0 && n >= 0 && !(PT && rt.greedy)) {
           for (int kk = 0; kk < P.npos; ++kk) {
             if (!P.diag && n >= P.K) break;  // everything accepted: the bonus draw was made above
             if (!wait_count(P, sm, P.tick_b + (size_t)b * P.npos + kk, (unsigned)P.nchunk_r)) return;
             if (ft == 0) P.tick_b[(size_t)b * P.npos + kk] = 0;
-            residual_draw<T>(P, sm, fbuf, fph, ssph, b, kk, n);
+            residual_draw<T>(P, sm, fbuf, fph, ssph, b, kk, n, rt.c);
           }
         }
       }
@@ -1643,7 +1714,7 @@ __device__ void fin_loop(const Params& P, Shared& sm, unsigned char* fbuf) {
 }
 
 // --------------------------------------------------------------------------- kernel ----
-template <int MODE, typename T>
+template <int MODE, typename T, bool PT>
 __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ Shared sm;
@@ -1672,13 +1743,13 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
   __syncthreads();
   unsigned char* fbuf = smem + (size_t)kStages * kStageBytes;
   if (warp < kConsWarps)
-    consumer_loop<MODE, T>(P, sm, smem);
+    consumer_loop<MODE, T, PT>(P, sm, smem);
   else if (warp < kProducerWarp + kGroups)
-    producer_loop<MODE, T>(P, sm, smem, warp - kProducerWarp);
+    producer_loop<MODE, T, PT>(P, sm, smem, warp - kProducerWarp);
   else if (warp == kBookWarp)
     book_loop<MODE>(P, sm);
   else
-    fin_loop<MODE, T>(P, sm, fbuf);  // warps kFinWarp .. kFinWarp + kFinWarps - 1
+    fin_loop<MODE, T, PT>(P, sm, fbuf);  // warps kFinWarp .. kFinWarp + kFinWarps - 1
   __syncthreads();
   // The last CTA out reports a timed-out call (never expected) on every request, and leaves the
   // counters zero for the next call (after a timeout the counts too: finishing groups that gave
@@ -1730,12 +1801,18 @@ __global__ void __launch_bounds__(256) probs_kernel(const Params P) {
   float* out = r < P.R ? (P.target_probs ? P.target_probs + ((size_t)b * P.R + r) * P.V : nullptr)
                        : (P.draft_probs ? P.draft_probs + ((size_t)b * P.K + (r - P.R)) * P.V : nullptr);
   if (!out) return;
+  float c = P.c;
+  if (P.temps) {  // per-request temperatures: rows of greedy requests have no softmax to write
+    const float Tb = P.temps[b];
+    if (!(Tb > 0.f) || isinf(Tb)) return;
+    c = (float)(1.4426950408889634 / (double)Tb);
+  }
   const RowStat rs = P.rstat[rowid];
   const char* rp = row_ptr<T>(P, b, r);
   const float invZ = (float)(1.0 / rs.Z);
   for (int i = (int)threadIdx.x; i < P.V; i += 256) {
     const float l = Elem<T>::to_float(Elem<T>::load_raw(rp + (size_t)i * Elem<T>::kSize));
-    out[i] = __fmul_rn(ex2(__fmaf_rn(l, P.c, -rs.mc)), invZ);
+    out[i] = __fmul_rn(ex2(__fmaf_rn(l, c, -rs.mc)), invZ);
   }
 }
 
@@ -1747,9 +1824,9 @@ struct LaunchPlan {
   int device;        // the current device
 };
 
-template <int MODE, typename T>
+template <int MODE, typename T, bool PT>
 cudaError_t launch_mode(const Params& P, const LaunchPlan& L, cudaStream_t stream) {
-  auto ks = verify_kernel<MODE, T>;
+  auto ks = verify_kernel<MODE, T, PT>;
   // the shared-memory opt-in and the occupancy, once per device (the same values every call)
   constexpr int kMaxDev = 64;
   static int resident[kMaxDev] = {0};
@@ -1778,10 +1855,12 @@ cudaError_t launch_mode(const Params& P, const LaunchPlan& L, cudaStream_t strea
 template <typename T>
 cudaError_t launch_verify(int mode, const Params& P, const LaunchPlan& L, cudaStream_t stream) {
   switch (mode) {
-    case kChain: return launch_mode<kChain, T>(P, L, stream);
-    case kNgram: return launch_mode<kNgram, T>(P, L, stream);
-    case kGreedy: return launch_mode<kGreedy, T>(P, L, stream);
-    case kTree: return launch_mode<kTree, T>(P, L, stream);
+    case kChain: return launch_mode<kChain, T, false>(P, L, stream);
+    case kNgram: return launch_mode<kNgram, T, false>(P, L, stream);
+    case kGreedy: return launch_mode<kGreedy, T, false>(P, L, stream);
+    case kTree: return launch_mode<kTree, T, false>(P, L, stream);
+    case kChainPT: return launch_mode<kChain, T, true>(P, L, stream);
+    case kNgramPT: return launch_mode<kNgram, T, true>(P, L, stream);
     default: return cudaErrorInvalidValue;
   }
 }

@@ -44,7 +44,8 @@ def f32(a, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(device)
 
 
-def run_gpu_chain(ci, ngram: bool = False, probs: bool = False, workspace=None, diag: bool = True) -> dict:
+def run_gpu_chain(ci, ngram: bool = False, probs: bool = False, workspace=None, diag: bool = True,
+                  temperatures=None) -> dict:
     dev = "cuda"
     B, K, V = ci.B, ci.K, ci.V
     tl = to_device(ci.target, ci.dtype)
@@ -55,13 +56,15 @@ def run_gpu_chain(ci, ngram: bool = False, probs: bool = False, workspace=None, 
     pm = torch.full((B, K + 1), -1.0, device=dev) if diag else None
     tp = torch.zeros((B, K + 1, V), device=dev) if probs else None
     dp = torch.zeros((B, K, V), device=dev) if (probs and not ngram) else None
+    tt = f32(temperatures) if temperatures is not None else None
     if ngram:
         o = binding.spec_verify_ngram(tl, x, r, u, float(ci.temperature), workspace=workspace,
-                                      accept_prob=ap, cand_tokens=ct, pos_mass=pm, target_probs=tp)
+                                      accept_prob=ap, cand_tokens=ct, pos_mass=pm, target_probs=tp,
+                                      temperatures=tt)
     else:
         o = binding.spec_verify_chain(tl, dl, x, r, u, float(ci.temperature), workspace=workspace,
                                       accept_prob=ap, cand_tokens=ct, pos_mass=pm, target_probs=tp,
-                                      draft_probs=dp)
+                                      draft_probs=dp, temperatures=tt)
     torch.cuda.synchronize()
     res = {k: v.cpu().numpy() for k, v in o.items()}
     res["accept_prob"] = ap.cpu().numpy()
@@ -74,15 +77,17 @@ def run_gpu_chain(ci, ngram: bool = False, probs: bool = False, workspace=None, 
     return res
 
 
-def run_oracle_chain(ci, ngram: bool = False, threads: int = 8, requests=None) -> dict:
+def run_oracle_chain(ci, ngram: bool = False, threads: int = 8, requests=None, temperatures=None) -> dict:
     if ngram:
         o = oracle.verify_ngram(ci.dtype, ci.target, ci.B, ci.K, ci.V, float(ci.temperature),
-                                ci.draft_tokens, ci.r, ci.u, threads=threads, requests=requests)
+                                ci.draft_tokens, ci.r, ci.u, threads=threads, requests=requests,
+                                temperatures=temperatures)
     else:
         o = oracle.verify_chain(ci.dtype, ci.target, ci.draft, ci.B, ci.K, ci.V,
                                 float(ci.temperature), ci.draft_tokens, ci.r, ci.u, threads=threads,
-                                requests=requests)
+                                requests=requests, temperatures=temperatures)
     o["ngram"] = ngram
+    o["temperatures"] = None if temperatures is None else np.asarray(temperatures, np.float32)
     return o
 
 
@@ -116,7 +121,12 @@ def check_chain(g: dict, o: dict, ci, requests=None) -> dict:
     idx = np.arange(ci.B) if requests is None else np.arange(*requests)
     K, V = ci.K, ci.V
     T = float(ci.temperature)
-    greedy = T == 0.0
+    temps = o.get("temperatures")  # per-request temperatures, when the call took them
+
+    def temp(b):
+        return T if temps is None else float(temps[b])
+
+    greedy = T == 0.0 and temps is None
     ngram = bool(o.get("ngram", False))
     fails = []
     err_o, err_g = o["err"][idx], g["err_flags"][idx]
@@ -147,7 +157,7 @@ def check_chain(g: dict, o: dict, ci, requests=None) -> dict:
 
     def draw_rows(b):
         if b not in rows:
-            rows[b] = oracle.chain_draw_rows(ci.dtype, ci.target, ci.draft, ci.B, K, V, T,
+            rows[b] = oracle.chain_draw_rows(ci.dtype, ci.target, ci.draft, ci.B, K, V, temp(b),
                                              ci.draft_tokens, int(b), ngram=ngram)
         return rows[b]
 
@@ -155,7 +165,7 @@ def check_chain(g: dict, o: dict, ci, requests=None) -> dict:
         """Token t at position k of request b: the candidate, or an admissible tie outcome."""
         if t == o["cand"][b][k]:
             return True, False
-        if greedy or not (o["pos_flag"][b][k] & (oracle.FLAG_CDF_TIE | oracle.FLAG_CDF_TIE_WIDE)):
+        if temp(b) == 0.0 or not (o["pos_flag"][b][k] & (oracle.FLAG_CDF_TIE | oracle.FLAG_CDF_TIE_WIDE)):
             return False, False
         d = draw_rows(b)
         widened = (not ngram) and k < K
@@ -178,7 +188,7 @@ def check_chain(g: dict, o: dict, ci, requests=None) -> dict:
         n = int(g["num_accepted"][b])
         out = g["out_tokens"][b]
         a, r = o["alpha"][b], ci.r[b]
-        if greedy:
+        if temp(b) == 0.0:
             if n != o["num_accepted"][b] or not np.array_equal(out, o["out_tokens"][b]):
                 fails.append(("greedy outcome differs", int(b)))
             continue

@@ -63,13 +63,14 @@ def test_status_strings(lib):
 
 
 def _chain(lib, **kw):
-    a = dict(target=1 << 20, draft=2 << 20, dtype=0, B=2, K=3, V=100, T=1.0, x=3 << 20, r=4 << 20,
+    a = dict(target=1 << 20, draft=2 << 20, dtype=0, B=2, K=3, V=100, T=1.0, temps=0, x=3 << 20, r=4 << 20,
              u=5 << 20, na=6 << 20, ot=7 << 20, ws=1 << 30, wsb=10 ** 6)
     a.update(kw)
     P = ctypes.c_void_p
     return lib.spec_verify_chain(P(a["target"]), P(a["draft"]), a["dtype"], a["B"], a["K"], a["V"],
-                                 a["T"], P(a["x"]), P(a["r"]), P(a["u"]), P(a["na"]), P(a["ot"]),
-                                 None, None, None, None, None, None, None, P(a["ws"]), a["wsb"], None)
+                                 a["T"], P(a["temps"]), P(a["x"]), P(a["r"]), P(a["u"]), P(a["na"]),
+                                 P(a["ot"]), None, None, None, None, None, None, None, P(a["ws"]), a["wsb"],
+                                 None)
 
 
 def test_host_validation_rejects_before_launch(lib):
@@ -90,6 +91,13 @@ def test_host_validation_rejects_before_launch(lib):
     assert _chain(lib, wsb=100) == binding.SPEC_ERR_WORKSPACE
     assert _chain(lib, ws=(1 << 30) + 16) == binding.SPEC_ERR_WORKSPACE  # workspace 256-B aligned
     assert _chain(lib, wsb=20000, V=10 ** 6) == binding.SPEC_ERR_WORKSPACE  # too small for this V
+    # per-request temperatures: any request may sample, so draft logits, r and u are required even
+    # when the call's own temperature is 0, and the workspace holds 2K + 1 rows per request
+    assert _chain(lib, T=0.0, temps=8 << 20, draft=0) == binding.SPEC_ERR_INVALID_ARG
+    assert _chain(lib, T=0.0, temps=8 << 20, u=0) == binding.SPEC_ERR_INVALID_ARG
+    need = lib.spec_verify_workspace_bytes(2, 7, 100, 0)
+    assert _chain(lib, T=0.0, temps=8 << 20, wsb=lib.spec_verify_workspace_bytes(2, 4, 100, 0)) == \
+        binding.SPEC_ERR_WORKSPACE and need > lib.spec_verify_workspace_bytes(2, 4, 100, 0)
 
 
 def test_tree_validation(lib):

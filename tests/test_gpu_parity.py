@@ -321,3 +321,64 @@ def test_graph_replays_get_fresh_tags():
         res = {k: v.cpu().numpy() for k, v in out.items()}
         res["accept_prob"] = ap.cpu().numpy()
         parity.compare_chain(res, parity.run_oracle_chain(ci), ci)
+
+
+# ------------------------------------------------------------ per-request temperature ----
+MIXED_T = np.array([0.0, 0.6, 1.0, 1.4], np.float32)
+
+
+@pytest.mark.parametrize("ngram,diag", [(False, False), (False, True), (True, False), (True, True)])
+def test_per_request_temperatures_full_size(ngram, diag):
+    """Per-request temperatures on the streaming calls at the headline sizes (chain: B=64 K=5
+    V=128256 fp32 with draft logits; n-gram: B=256 K=5 V=151936 bf16), T cycling 0 / 0.6 / 1.0 /
+    1.4 over the requests (0: that request verified greedily, its draft rows not read)."""
+    ci = synth.ngram(seed=0) if ngram else synth.chain_batched(seed=0)
+    temps = np.resize(MIXED_T, ci.B)
+    g = parity.run_gpu_chain(ci, ngram=ngram, diag=diag, temperatures=temps)
+    st = parity.compare_chain(g, parity.run_oracle_chain(ci, ngram=ngram, threads=16, temperatures=temps), ci)
+    _show(f"per-request T ngram={ngram} diag={diag}", st)
+    assert st["flagged"] <= FLAG_BOUND["ngram" if ngram else "chain"] * ci.B, st
+
+
+def test_per_request_temperatures_edge_cases():
+    """Greedy, sampled and failed requests in one call: each request gets what a call at its own
+    temperature gives; NaN, negative and infinite temperatures fail their request alone with the
+    bad-temperature bit; probability rows are written for the sampled requests only."""
+    ci = _random_chain(17, 12, 4, 5003, "bf16")
+    temps = np.array([0.5, 0.0, 1.0, 2.0, 0.0, 0.8, np.nan, -1.0, np.inf, 0.05, 8.0, 0.0], np.float32)
+    for ngram in (False, True):
+        g = parity.run_gpu_chain(ci, ngram=ngram, probs=True, temperatures=temps)
+        parity.compare_chain(g, parity.run_oracle_chain(ci, ngram=ngram, temperatures=temps), ci)
+        assert list(g["err_flags"][6:9]) == [binding.ERRF_BAD_TEMPERATURE] * 3
+        for b, T in enumerate(temps):
+            one = synth.ChainInputs(**{**ci.__dict__, "B": 1, "temperature": np.float32(T if np.isfinite(T) and T >= 0
+                                                                                            else 1.0),
+                                       "target": ci.target[b:b + 1], "draft": ci.draft[b:b + 1],
+                                       "draft_tokens": ci.draft_tokens[b:b + 1], "r": ci.r[b:b + 1],
+                                       "u": ci.u[b:b + 1]})
+            if 6 <= b <= 8:
+                assert (g["out_tokens"][b] == -1).all() and (g["target_probs"][b] == 0).all()
+                continue
+            alone = parity.run_gpu_chain(one, ngram=ngram)
+            for key in ("num_accepted", "out_tokens", "err_flags"):
+                assert np.array_equal(g[key][b], alone[key][0]), (ngram, b, key)
+            if T == 0:
+                assert (g["target_probs"][b] == 0).all()  # greedy: no softmax rows
+                continue
+            for k in range(ci.K + 1):
+                p, e = oracle.softmax(synth.decode(ci.target[b, k], ci.dtype).astype(np.float64), float(T))
+                assert e == 0 and np.abs(g["target_probs"][b, k] - p).max() <= parity.PROB_TOL
+
+
+def test_per_request_temperatures_share_a_workspace():
+    """Calls with and without per-request temperatures in turn on one workspace: each leaves it
+    ready for the next (the greedy requests' skipped draft rows and residual items included)."""
+    ci = synth.chain_batched(seed=7, B=8, V=30011)
+    ws = binding.make_workspace(ci.B, 2 * ci.K + 1, ci.V, torch.float32, "cuda")
+    temps = np.resize(MIXED_T, ci.B)
+    o_mixed = parity.run_oracle_chain(ci, temperatures=temps)
+    o_one = parity.run_oracle_chain(ci)
+    for _ in range(2):
+        parity.compare_chain(parity.run_gpu_chain(ci, workspace=ws, diag=False, temperatures=temps), o_mixed, ci)
+        parity.compare_chain(parity.run_gpu_chain(ci, workspace=ws, diag=False), o_one, ci)
+        parity.compare_chain(parity.run_gpu_chain(ci, workspace=ws, temperatures=temps), o_mixed, ci)
