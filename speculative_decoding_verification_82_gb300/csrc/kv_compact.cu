@@ -8,13 +8,16 @@
 // slot of position j, slots[b][j], so the accepted tokens end up in order in the request's first
 // L + 1 slots; every other slot is left alone.
 //
-// One CTA moves one request's rows in one cache (a layer's K or V tensor), each thread 16 bytes of
-// every row.  Along an accepted path p_j >= j (a node's index exceeds its parent's), so no move
-// writes a slot that a later move reads: a thread loads up to kBatch source vectors, then stores
-// them, batch after batch in increasing position, in place.  Moves with p_j == j are skipped.
-// The kernel is a gather bound by HBM bandwidth: each moved row is read once and written once.
-// (Staging whole rows through shared memory with bulk copies, one to three CTAs per SM, measured
-// 10 to 15% slower on the benchmark's 2048-byte rows: each CTA's reads and writes then serialise.)
+// One CTA moves one request's rows in a group of consecutive caches (layers' K or V tensors).  It
+// checks the path in two dependent rounds of loads (the length, the path and every slot at once;
+// then the parents and slots of the path's nodes) and builds the move list; the grid is sized to
+// about kCtasPerSm CTAs per SM, so that every CTA is resident from the start and their checks
+// overlap.  A unit of work is one 16-byte column of the moved rows of one cache: the thread loads
+// the column of every moved row, then stores them, in increasing position.  Along an accepted path
+// p_j >= j (a node's index exceeds its parent's) and slots are distinct, so no store lands on a
+// row that a later move still reads, and moving in place is safe.  Moves with p_j == j are
+// skipped.  The kernel is a gather bound by HBM bandwidth: each moved row is read once and written
+// once.
 #include <stdint.h>
 
 #include "spec_verify.h"
@@ -23,11 +26,14 @@ namespace {
 
 constexpr int kMaxCaches = SPEC_MAX_KV_CACHES;
 constexpr int kMaxNodes = SPEC_MAX_WALK_NODES;
-constexpr int kBatch = 8;
+constexpr int kThreads = 256;
+constexpr int kBatch = 8;      // moved rows of one column loaded before they are stored
+constexpr int kCtasPerSm = 4;  // grid target: every CTA resident at once
 
 struct KvParams {
   unsigned char* caches[kMaxCaches];  // each [num_slots][row_bytes]
   int C, row_bytes, B, N1;
+  int group;                  // caches per CTA
   long long num_slots;
   const int32_t* slots;       // [B][N1]
   const int32_t* parents;     // [B][N1]
@@ -36,52 +42,84 @@ struct KvParams {
   int32_t* err_flags;         // [B] or null
 };
 
-__global__ void __launch_bounds__(256) kv_compact_kernel(const KvParams P) {
-  __shared__ int32_t src[kMaxNodes], dst[kMaxNodes];
-  const int c = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
+__global__ void __launch_bounds__(kThreads) kv_compact_kernel(const KvParams P) {
+  __shared__ int32_t node[kMaxNodes];                 // path[j]
+  __shared__ int32_t slot[kMaxNodes];                 // slots[n]
+  __shared__ int32_t from[kMaxNodes];                 // slots[path[j]]: the source of position j
+  __shared__ int32_t src[kMaxNodes], dst[kMaxNodes];  // the move list, in increasing position
+  __shared__ int nmove;
+  const int grp = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
   const int N1 = P.N1;
-  const int32_t* sl = P.slots + (size_t)b * N1;
   const int32_t* pa = P.parents + (size_t)b * N1;
-  const int32_t* pt = P.path + (size_t)b * N1;
+  // round 1: the length, the path and every slot, all at once
   const int L = __ldg(P.accept_len + b);
-  // the path must be an accepted path of the tree and every slot inside the cache
-  bool ok = L >= 0 && L < N1 && __ldg(pt) == 0;
-  if (ok) {
-    for (int j = 1 + t; j <= L; j += blockDim.x) {
-      const int n = __ldg(pt + j), prev = __ldg(pt + j - 1);
-      ok = ok && n > 0 && n < N1 && __ldg(pa + n) == prev;
-    }
-    for (int n = t; n < N1; n += blockDim.x) {
-      const int s = __ldg(sl + n);
-      ok = ok && s >= 0 && s < P.num_slots;
-    }
-  }
-  ok = __syncthreads_and(ok);
-  if (c == 0 && t == 0 && P.err_flags) P.err_flags[b] = ok ? 0 : SPEC_ERRF_BAD_TREE;
-  if (!ok) return;
-  for (int j = 1 + t; j <= L; j += blockDim.x) {
-    src[j] = __ldg(sl + __ldg(pt + j));
-    dst[j] = __ldg(sl + j);
+  bool ok = true;
+  for (int j = t; j < N1; j += kThreads) {
+    node[j] = __ldg(P.path + (size_t)b * N1 + j);
+    const int s = __ldg(P.slots + (size_t)b * N1 + j);
+    slot[j] = s;
+    ok = ok && s >= 0 && s < P.num_slots;
   }
   __syncthreads();
-  unsigned char* base = P.caches[c];
+  ok = ok && L >= 0 && L < N1 && node[0] == 0;
+  // round 2: each accepted node is a child of the previous one (its slot, known from round 1, is
+  // the move's source)
+  for (int j = 1 + t; j <= L && j < N1; j += kThreads) {
+    const int n = node[j], prev = node[j - 1];
+    const bool in = n > 0 && n < N1;
+    ok = ok && in && __ldg(pa + n) == prev;
+    from[j] = in ? slot[n] : -1;
+  }
+  ok = __syncthreads_and(ok);
+  if (grp == 0 && t == 0 && P.err_flags) P.err_flags[b] = ok ? 0 : SPEC_ERRF_BAD_TREE;
+  if (!ok) return;
+  // the move list in increasing position (a warp ballot keeps the order); moves in place skipped
+  if (t < 32) {
+    int base = 0;
+    for (int j0 = 1; j0 <= L; j0 += 32) {
+      const int j = j0 + t;
+      const bool mv = j <= L && from[j] != slot[j];
+      const unsigned bal = __ballot_sync(0xffffffffu, mv);
+      if (mv) {
+        const int k = base + __popc(bal & ((1u << t) - 1u));
+        src[k] = from[j];
+        dst[k] = slot[j];
+      }
+      base += __popc(bal);
+    }
+    if (t == 0) nmove = base;
+  }
+  __syncthreads();
+  const int M = nmove;
+  if (M == 0) return;
+  const int c0 = grp * P.group, c1 = min(P.C, c0 + P.group);
   const size_t W = (size_t)P.row_bytes;
   const int nvec = P.row_bytes / 16;
-  for (int v = t; v < nvec; v += blockDim.x) {
-    for (int j0 = 1; j0 <= L; j0 += kBatch) {
+  const int units = (c1 - c0) * nvec;  // (cache, 16-byte column) pairs of this CTA
+  for (int i = t; i < units; i += kThreads) {
+    const int cl = i / nvec, v = i - cl * nvec;
+    unsigned char* base = P.caches[c0 + cl] + (size_t)v * 16;
+    for (int k0 = 0; k0 < M; k0 += kBatch) {
       uint4 tmp[kBatch];
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int j = j0 + i;
-        if (j <= L && src[j] != dst[j]) tmp[i] = *reinterpret_cast<const uint4*>(base + src[j] * W + v * 16);
-      }
+      for (int k = 0; k < kBatch; ++k)
+        if (k0 + k < M) tmp[k] = *reinterpret_cast<const uint4*>(base + (size_t)src[k0 + k] * W);
 #pragma unroll
-      for (int i = 0; i < kBatch; ++i) {
-        const int j = j0 + i;
-        if (j <= L && src[j] != dst[j]) *reinterpret_cast<uint4*>(base + dst[j] * W + v * 16) = tmp[i];
-      }
+      for (int k = 0; k < kBatch; ++k)
+        if (k0 + k < M) *reinterpret_cast<uint4*>(base + (size_t)dst[k0 + k] * W) = tmp[k];
     }
   }
+}
+
+int sm_count_cached() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return -1;
+  static int cache[64] = {0};
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+  if (dev < 64) cache[dev] = n;
+  return n;
 }
 
 }  // namespace
@@ -100,6 +138,15 @@ extern "C" spec_status_t spec_kv_compact(void* const* caches, int num_caches, lo
     if (!caches[i] || ((uintptr_t)caches[i] & 15u)) return SPEC_ERR_INVALID_ARG;
     P.caches[i] = static_cast<unsigned char*>(caches[i]);
   }
+  const int sms = sm_count_cached();
+  if (sms <= 0) return SPEC_ERR_CUDA;
+  // caches per CTA: about kCtasPerSm CTAs per SM over the (request, cache group) grid
+  const long long target = (long long)kCtasPerSm * sms;
+  long long groups = target / B;
+  if (groups < 1) groups = 1;
+  if (groups > num_caches) groups = num_caches;
+  P.group = (int)((num_caches + groups - 1) / groups);
+  const int ngroups = (num_caches + P.group - 1) / P.group;
   P.C = num_caches;
   P.row_bytes = row_bytes;
   P.B = B;
@@ -110,8 +157,6 @@ extern "C" spec_status_t spec_kv_compact(void* const* caches, int num_caches, lo
   P.accept_len = accept_len;
   P.path = path_nodes;
   P.err_flags = err_flags;
-  const int nvec = row_bytes / 16;
-  const int threads = nvec >= 256 ? 256 : (nvec >= 32 ? (nvec + 31) / 32 * 32 : 32);
-  kv_compact_kernel<<<dim3((unsigned)num_caches, (unsigned)B), threads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(P);
+  kv_compact_kernel<<<dim3((unsigned)ngroups, (unsigned)B), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(P);
   return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
