@@ -46,18 +46,19 @@ Chunking plan_chunks(int V, int S) {
 }
 
 // Workspace layout:
-//   work, gerr, exit_tick, epoch u32 (128 B line)   } counters: zero between calls of one
+//   work, gerr, exit_tick, epoch, rq_tail u32 (128 B line) } counters: zero between calls of one
 //   rc                           u32 (128 B line)   } shape (each call leaves them zero; the
-//   tick_a  [B] u32              request tickets    } first call of a shape clears them)
-//   tick_b  [B][rows] u32        residual tickets   }
+//   tick_a  [B][rows] u32        chunk counts       } first call of a shape clears them)
+//   tick_b  [B][rows] u32        residual counts    }
 //   req     [B]                  ReqState           (16-byte aligned; tagged per call)
+//   rq      [B] u64              residual queue     (tagged per call)
 //   cstat   [B][rows][nchunk]    ChunkStat          (256-byte aligned regions from here on)
 //   sstat   [B][rows][nchunk][G] ChunkStat          sub-chunk partials (G consumer warps a group)
 //   rstat   [B][rows]            RowStat
 //   wsum    [B][rows][nchunk_r]  TagSum (float and tag)
 //   wsub    [B][rows][nchunk_r][G] TagSum
 struct Layout {
-  size_t work, tick_a, tick_b, req, hdr_end, cstat, sstat, rstat, wsum, wsub, total;
+  size_t work, tick_a, tick_b, req, rq, hdr_end, cstat, sstat, rstat, wsum, wsub, total;
 };
 
 Layout layout(int B, int rows, const Chunking& ck) {
@@ -67,11 +68,13 @@ Layout layout(int B, int rows, const Chunking& ck) {
   L.work = off;
   off += 2 * 128;
   L.tick_a = off;
-  off += b * 4;
+  off += b * r * 4;
   L.tick_b = off;
   off = align_up(off + b * r * 4, 16);
   L.req = off;
   off += b * sizeof(ReqState);
+  L.rq = off;
+  off += b * 8;
   L.hdr_end = off;
   off = align_up(off, 256);
   const size_t G = specv::kGroupWarps;
@@ -113,10 +116,12 @@ spec_status_t attach_workspace(Params& P, void* ws, size_t bytes, int B, int row
   P.gerr = P.work + 1;
   P.exit_tick = P.work + 2;
   P.epoch = P.work + 3;
+  P.rq_tail = P.work + 4;
   P.rc = reinterpret_cast<unsigned*>(w + L.work + 128);  // residual cursor (a line of its own)
   P.tick_a = reinterpret_cast<unsigned*>(w + L.tick_a);
   P.tick_b = reinterpret_cast<unsigned*>(w + L.tick_b);
   P.req = reinterpret_cast<ReqState*>(w + L.req);
+  P.rq = reinterpret_cast<unsigned long long*>(w + L.rq);
   P.cstat = reinterpret_cast<ChunkStat*>(w + L.cstat);
   P.sstat = reinterpret_cast<ChunkStat*>(w + L.sstat);
   P.rstat = reinterpret_cast<RowStat*>(w + L.rstat);
@@ -168,14 +173,18 @@ bool workspace_needs_clear(const Params& P, bool forget) {
   return true;
 }
 
-// Constants of the item decoding's divisions (see fastdiv.h).
-void set_divisors(Params& P, int rows) {
+// Constants of the item decoding's divisions (see fastdiv.h).  pair_rows: the rows a request reads
+// per position in the chain modes (2 with draft logits, else 1).
+void set_divisors(Params& P, int B, int rows, int pair_rows) {
   const unsigned A = (unsigned)rows * (unsigned)P.nchunk;
   const unsigned R = (unsigned)P.npos * (unsigned)P.nchunk_r;
+  const unsigned pair = (unsigned)pair_rows * (unsigned)P.nchunk;
   P.fd_A = specv::make_fastdiv(A);
   P.fd_R = specv::make_fastdiv(R > 0 ? R : 1u);
   P.fd_nchunk = specv::make_fastdiv((unsigned)P.nchunk);
   P.fd_nchunk_r = specv::make_fastdiv((unsigned)P.nchunk_r);
+  P.fd_pair = specv::make_fastdiv(pair);
+  P.fd_S1 = specv::make_fastdiv((unsigned)B * pair);
 }
 
 spec_status_t launch(spec_dtype_t dtype, int mode, Params& P, specv::LaunchPlan& L, cudaStream_t stream) {
@@ -236,7 +245,7 @@ spec_status_t verify_chain_common(bool ngram, const void* target, const void* dr
   if (sms <= 0) return SPEC_ERR_CUDA;
   P.total = (unsigned)((long long)B * rows * ck.nchunk);
   P.total_r = (unsigned)((long long)B * P.npos * ck.nchunk_r);
-  set_divisors(P, rows);
+  set_divisors(P, B, rows, two_rows ? 2 : 1);
   P.target = target;
   P.draft = two_rows ? draft : nullptr;
   P.B = B;
@@ -333,7 +342,7 @@ spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t dt
   if (sms <= 0) return SPEC_ERR_CUDA;
   P.total = (unsigned)((long long)B * rows * P.nchunk);
   P.npos = 0;
-  set_divisors(P, rows);
+  set_divisors(P, B, rows, 1);
   P.target = target_logits;
   P.B = B;
   P.K = 0;

@@ -31,7 +31,6 @@ constexpr int kThreads = (kFinWarp + kFinWarps) * 32;
 constexpr int kStages = 6;                         // staged-chunk ring depth (a multiple of kGroups)
 constexpr int kSlots = 16;                         // ring of per-chunk results (partials, merged)
 constexpr int kClaim = 4;                          // work items claimed per atomic
-constexpr int kL2KeepPositions = 1;                // chains: positions whose rows L2 keeps longer
 constexpr int kChunkVec = 2048;                    // 16-byte vectors per chunk of a row (32 KB)
 constexpr int kSubVec = kChunkVec / kGroupWarps;   // vectors per consumer warp (a sub-chunk)
 constexpr int kVecPerLane = kSubVec / 32;

@@ -104,6 +104,9 @@ struct Params {
   // the divisors of the item decoding: A = rows * nchunk stats items per request, R = npos *
   // nchunk_r residual items per request, nchunk, nchunk_r
   FastDiv fd_A, fd_R, fd_nchunk, fd_nchunk_r;
+  // chain modes, stage-major stats items: the items of one non-bonus stage (B * rs * nchunk, rs the
+  // rows a request reads per position) and of one request within it (rs * nchunk)
+  FastDiv fd_S1, fd_pair;
   const int32_t* draft_tokens;
   const float* r;
   const float* u;
@@ -138,7 +141,11 @@ struct Params {
   unsigned* gerr;            // timeout flag
   unsigned* exit_tick;       // exiting CTAs
   unsigned* rc;              // next residual item
-  unsigned* tick_a;     // [B] chunks in, per request (zeroed by its finishing group once complete)
+  unsigned* rq_tail;         // entries published in the residual queue
+  unsigned* tick_a;     // chunks in (zeroed by the finishing group once complete): per request and
+                        // position [B][K+1] in the chain modes, per request [B] for trees
+  unsigned long long* rq;  // [B] the residual queue: request ids in the order their results were
+                           // published (each a 64-bit word: id in the high half, the call's tag low)
   unsigned* tick_b;     // [B][npos] residual items in (likewise)
 };
 
@@ -250,6 +257,20 @@ struct SlotMeta {
   int kind;        // ItemKind
   unsigned* tick;  // the count this chunk adds to (stats and residual items)
 };
+// A request of the chain modes while its finishing group takes its positions in turn.
+constexpr int kOwnMax = 4;  // requests one finishing group interleaves, position by position
+struct FinReq {
+  int b;       // the request
+  int n;       // its accepted length once decided, -1 before
+  int err;     // error bits seen so far
+  int tok;     // the emitted token once drawn
+  int resid;   // a residual pass was published for position n (draft-model chains)
+  int drawn;   // the emitted token is known
+  int written; // the outputs were written (no error seen then; rewritten if one turns up later)
+  int greedy, bad;
+  float c, u, mass;
+  RowStat rt, rd;  // target and draft row statistics at position n
+};
 constexpr int kFinCs = 512;   // chunk statistics of one request staged for its finishing
 constexpr int kFinSs = 512;   // sub-chunk statistics of the rows a draw may read
 constexpr int kFinRows = 64;  // row statistics kept in shared memory for finishing
@@ -266,6 +287,8 @@ struct Shared {
   RowStat fin_rs[kFinRows];
   int fin_par[kFinRows], fin_tok[kFinRows];  // a small tree's parents and tokens
   GroupScratch gs;                            // the finishing group's reductions and broadcasts
+  FinReq fr[kOwnMax];                         // chain modes: the requests being finished
+  RowStat srs[2];                             // chain modes: a position's row statistics
   unsigned tag;  // this call's tag: the workspace's epoch + 1 (never 0, the value of cleared memory)
 };
 
@@ -278,20 +301,52 @@ __device__ __forceinline__ bool aborted(const Shared& sm) {
 }
 
 // -------------------------------------------------------------------- item decoding ----
-// Stats items are request-major, then row, then chunk: item w < P.total is chunk item w mod A of
-// request w / A.  Residual items are request-major, then position slot, then residual chunk:
-// residual item w < P.total_r is item w mod R of request w / R.  The stats items are handed out
-// by the counter `work`, the residual items by the cursor `rc`; a producer stages a residual item
-// only once its request's acceptance result is published, and never waits for one while it still
-// has stats items.
-__device__ __forceinline__ void decode_stats(const Params& P, unsigned w, int& b, int& off) {
-  b = (int)fdiv(w, P.fd_A);
-  off = (int)(w - (unsigned)b * P.fd_A.d);
+// Stats items of trees are request-major, then row, then chunk: item w < P.total is chunk item
+// w mod A of request w / A.  Stats items of the chain modes are position-major ("stages"): stage
+// s < K holds the rows of position s of every request (target row s, and draft row s when the
+// call reads draft logits), request by request, then row, then chunk; the last stage holds every
+// request's bonus row (target row K).  So the acceptance test at position s of every request can
+// be made once stage s is in, and the residual pass of a request rejected there overlaps the
+// later stages.  Residual items come in the order of the residual queue (requests in the order
+// their results were published), then position slot, then residual chunk: residual item
+// w < P.total_r is item w mod R of queue entry w / R.  The stats items are handed out by the
+// counter `work`, the residual items by the cursor `rc`; a producer stages a residual item only
+// once its queue entry and its request's result are published, and never waits for one while it
+// still has stats items.
+template <int MODE>
+__device__ __forceinline__ void decode_stats(const Params& P, unsigned w, int& b, int& row, int& ch) {
+  if constexpr (MODE == kTree) {
+    b = (int)fdiv(w, P.fd_A);
+    const int off = (int)(w - (unsigned)b * P.fd_A.d);
+    row = (int)fdiv((unsigned)off, P.fd_nchunk);
+    ch = off - row * P.nchunk;
+  } else {
+    const unsigned st = fdiv(w, P.fd_S1);
+    if (st >= (unsigned)P.K) {  // the bonus stage: one row per request
+      const unsigned off = w - (unsigned)P.K * P.fd_S1.d;
+      b = (int)fdiv(off, P.fd_nchunk);
+      ch = (int)(off - (unsigned)b * P.fd_nchunk.d);
+      row = P.K;
+    } else {
+      const unsigned off = w - st * P.fd_S1.d;
+      b = (int)fdiv(off, P.fd_pair);
+      const int r2off = (int)(off - (unsigned)b * P.fd_pair.d);
+      const int r2 = r2off >= P.nchunk ? 1 : 0;  // 0: target row, 1: draft row
+      ch = r2off - r2 * P.nchunk;
+      row = r2 ? P.R + (int)st : (int)st;
+    }
+  }
 }
-// Lane 0 of a producer that found request b without a residual draw: moves the cursor past the
-// request's items (when it still points into them).
-__device__ __forceinline__ void skip_residual(const Params& P, unsigned b) {
-  const unsigned lo = b * P.fd_R.d, end = lo + P.fd_R.d;
+// The count a stats chunk of (request b, row) adds to.
+template <int MODE>
+__device__ __forceinline__ unsigned* stats_tick(const Params& P, int b, int row) {
+  if constexpr (MODE == kTree) return P.tick_a + b;
+  return P.tick_a + (size_t)b * P.R + (row < P.R ? row : row - P.R);
+}
+// Lane 0 of a producer that found queue entry e without a residual draw: moves the cursor past the
+// entry's items (when it still points into them).
+__device__ __forceinline__ void skip_residual(const Params& P, unsigned e) {
+  const unsigned lo = e * P.fd_R.d, end = lo + P.fd_R.d;
   unsigned c = *reinterpret_cast<const volatile unsigned*>(P.rc);
   for (int tries = 0; tries < 8 && c >= lo && c < end; ++tries) {
     const unsigned old = atomicCAS(P.rc, c, end);
@@ -368,10 +423,10 @@ __device__ __forceinline__ void resid_weights(const unsigned char* buf, int dslo
 // Producer of group grp: items it = grp, grp + kGroups, ... of this CTA's sequence (stage
 // it % kStages).  The producer holds one batch of up to kClaim residual items from the cursor at a
 // time (claimed at the start of a batch of stats items, or at any item once those are out) and
-// stages its items, ahead of stats items, once their request's result is published; it reads the
-// result words at the start of each stats batch and uses them at the next, so that the read does
-// not hold it up.  Only once its stats items are out does it wait (bounded) for a result.  Once
-// both kinds are exhausted it publishes one end marker.
+// stages its items, ahead of stats items, once their queue entry and their request's result are
+// published; it reads the entry and the result words at the start of each stats batch and uses
+// them at the next, so that the reads do not hold it up.  Only once its stats items are out does it
+// wait (bounded) for a result.  Once both kinds are exhausted it publishes one end marker.
 template <int MODE, typename T, bool PT>
 __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages, int grp) {
   const int lane = threadIdx.x & 31;
@@ -388,11 +443,11 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
     cur = (unsigned)kClaim * (blockIdx.x * (unsigned)kGroups + (unsigned)grp);
     nxt = fixed + atomicAdd(P.work, (unsigned)kClaim);
   }
-  // residual claims (lane 0): the held items rfirst .. rfirst + rcnt - 1, and q0..q3, the result
-  // words of request qb as last read
-  unsigned rfirst = 0, qb = 0xffffffffu, rseen = 0;  // rseen: the cursor as this producer last saw it
-  int rcnt = 0;
-  bool rdone = P.npos == 0, qok = false;  // qok: request qb's result is complete
+  // residual claims (lane 0): the held items rfirst .. rfirst + rcnt - 1; qreq, the request of queue
+  // entry qe once that entry is published; q0..q3, qreq's result words as last read
+  unsigned rfirst = 0, qe = 0xffffffffu, rseen = 0;  // rseen: the cursor as this producer last saw it
+  int rcnt = 0, qreq = -1;
+  bool rdone = P.npos == 0, qok = false;  // qok: request qreq's result is complete
   unsigned long long q0 = 0, q1 = 0, q2 = 0, q3 = 0;
   int it = grp;
   // residual parameters of the last request seen (consecutive residual items share them)
@@ -438,22 +493,31 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
             rcnt = (int)min(rk, P.total_r - c);
           }
         }
-        const unsigned nb = rcnt > 0 ? fdiv(rfirst, P.fd_R) : 0xffffffffu;
-        bool rready = rcnt > 0 && nb == qb && qok;
+        const unsigned ne = rcnt > 0 ? fdiv(rfirst, P.fd_R) : 0xffffffffu;  // the held items' entry
+        bool rready = rcnt > 0 && ne == qe && qok;
         if (rcnt > 0 && !rready && boundary) {
-          // the words read at the previous batch start (in by now), else read them again: used at
-          // the next batch start, or now once the stats items are out
-          if (nb == qb && result_complete(P, sm.tag, q0, q1, q2, q3)) {
+          // the entry and words read at the previous batch start (in by now), else read them again:
+          // used at the next batch start, or now once the stats items are out
+          if (ne == qe && qreq >= 0 && result_complete(P, sm.tag, q0, q1, q2, q3)) {
             qok = rready = true;
           } else {
-            const unsigned long long* rw = P.req[nb].w;
-            qb = nb;
-            q0 = ld_volatile_u64(rw);
-            q1 = ld_volatile_u64(rw + 1);
-            q2 = ld_volatile_u64(rw + 2);
-            q3 = ld_volatile_u64(rw + 3);
+            if (ne != qe) {
+              qe = ne;
+              qreq = -1;
+            }
+            if (qreq < 0) {
+              const unsigned long long ev = ld_volatile_u64(P.rq + ne);
+              if (req_word_ok(ev, sm.tag)) qreq = (int)req_word_hi(ev);
+            }
             qok = false;
-            if (sdone) qok = rready = result_complete(P, sm.tag, q0, q1, q2, q3);
+            if (qreq >= 0) {
+              const unsigned long long* rw = P.req[qreq].w;
+              q0 = ld_volatile_u64(rw);
+              q1 = ld_volatile_u64(rw + 1);
+              q2 = ld_volatile_u64(rw + 2);
+              q3 = ld_volatile_u64(rw + 3);
+              if (sdone) qok = rready = result_complete(P, sm.tag, q0, q1, q2, q3);
+            }
           }
         }
         if (rready) {
@@ -489,10 +553,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
       if (kind == kItemSkip) continue;
       m.kind = kind;
       if (kind == kItemStats) {
-        int off = 0;
-        decode_stats(P, w, m.b, off);
-        m.row = (int)fdiv((unsigned)off, P.fd_nchunk);
-        m.ch = off - m.row * P.nchunk;
+        decode_stats<MODE>(P, w, m.b, m.row, m.ch);
         if constexpr (PT) {
           if (m.b != tb) {
             tb = m.b;
@@ -507,18 +568,15 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
         m.nvec = max(0, v1 - v0);
         constexpr int VE = Elem<T>::kPerVec;
         m.e_base = v0 * VE - g.phase;
-        // With a residual pass, the pair at the rejected position is read again soon after; the
-        // first rejection falls at the early positions far more often (acceptances compound),
-        // so their rows are kept in L2 ahead of the rest
-        int hint = kL2Normal;
-        if (P.npos > 0) {
-          const int k = m.row < P.R ? m.row : m.row - P.R;
-          hint = (k < kL2KeepPositions && k < P.K) ? kL2Last : kL2First;
-        }
+        // Rows stream once: evict-first keeps them from crowding out other lines.  (Keeping the
+        // pairs of a draft-model chain in L2 for a later residual re-read measured slower: the
+        // re-read of a stage comes one stage later, after more bytes than L2 holds.)
+        const int hint = P.npos > 0 ? kL2First : kL2Normal;
         warp_stage<T>(buf, g, P.V, v0, v1, &sm.full[s], lane, hint);
       } else if (kind == kItemResid) {
-        m.b = (int)fdiv(w, P.fd_R);
-        const int off = (int)(w - (unsigned)m.b * P.fd_R.d);
+        const int e = (int)fdiv(w, P.fd_R);  // the queue entry (published: the item was taken only then)
+        const int off = (int)(w - (unsigned)e * P.fd_R.d);
+        m.b = __shfl_sync(kFull, qreq, 0);
         m.kk = (int)fdiv((unsigned)off, P.fd_nchunk_r);
         m.ch = off - m.kk * P.nchunk_r;
         if (m.b != rb || P.diag) {
@@ -550,7 +608,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
           }
         }
         if (rerr || rk >= P.K) {  // no residual draw for this request: drop the item
-          if (lane == 0) skip_residual(P, (unsigned)m.b);
+          if (lane == 0) skip_residual(P, (unsigned)e);
           continue;
         }
         m.row = rk;
@@ -724,7 +782,7 @@ __device__ __forceinline__ void publish_chunk(const Params& P, Shared& sm, const
       q = make_uint4(__float_as_uint(v), sm.tag, (unsigned)i, sm.tag);
     }
     if (lane == 0) *reinterpret_cast<uint4*>(P.cstat + ci) = q;
-    pm.tick = P.tick_a + m.b;
+    pm.tick = stats_tick<MODE>(P, m.b, m.row);
   } else if (m.kind == kItemResid) {
     float sum = mine ? pw.x : 0.f;
 #pragma unroll
@@ -1274,209 +1332,120 @@ __device__ void combine_rows(const Params& P, Shared& sm, int b, const CsReader&
   fin_sync();
 }
 
-// Inputs of request b that do not depend on its statistics, loaded by the leader while the group
-// waits for them (positions k < 32 in lane k): the draft token, its uniform, and the target and
-// draft logits at the token.
-struct ReqPrefetch {
-  int x0;
-  float r0, lx0, dx0, u;
-};
-template <int MODE, typename T>
-__device__ __forceinline__ ReqPrefetch prefetch_request(const Params& P, int b) {
-  constexpr int S = Elem<T>::kSize;
-  constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
-  const int lane = threadIdx.x & 31;
-  ReqPrefetch f{0, 0.f, 0.f, 0.f, 0.f};
-  if (kSoftmax) f.u = __ldg(P.u + b);
-  if (lane < P.K) {
-    f.x0 = __ldg(P.draft_tokens + (size_t)b * P.K + lane);
-    if (kSoftmax) {
-      f.r0 = __ldg(P.r + (size_t)b * P.K + lane);
-      if (f.x0 >= 0 && f.x0 < P.V) {
-        f.lx0 = Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, lane) + (size_t)f.x0 * S));
-        if (MODE == kChain)
-          f.dx0 = Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, P.R + lane) + (size_t)f.x0 * S));
+// Waits (bounded) until *count reaches `want`: the leader polls (with acquire semantics, so the
+// statistics counted before it are visible afterwards), then the group agrees.  False on a
+// timeout or abort.
+__device__ __forceinline__ bool wait_count(const Params& P, Shared& sm, const unsigned* count, unsigned want) {
+  int ok = 1;
+  if (fin_thread() == 0) {
+    ok = 0;
+    const long long t0 = clock64();
+    for (;;) {
+      if (ld_acquire_u32(count) >= want) {
+        ok = 1;
+        break;
       }
+      if (aborted(sm)) break;
+      if (clock64() - t0 > kWaitLimitCycles) {
+        raise_abort(P, sm);
+        break;
+      }
+      __nanosleep(64);
     }
   }
-  return f;
+  return fin_all(ok != 0);
 }
 
-// Chain / n-gram / greedy-chain finishing: alpha, acceptance scan (section I.1 step 2), outputs,
-// publication of the acceptance result, and the draws made here (bonus row; n-gram residual).
-// Returns the accepted length (or -1 after an error) in every thread.  pf is the leader's.
-template <int MODE, typename T, bool PT>
-__device__ int finish_chain(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& csph,
-                            uint32_t& ssph, int b, const ReqPrefetch& pf, const ReqTemp& rt) {
-  constexpr int S = Elem<T>::kSize;
-  constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
-  // per-request temperatures: this request's statistics kind, c and rows (greedy: target rows only)
-  const bool soft = PT ? !rt.greedy : kSoftmax;
-  const float c = PT ? rt.c : P.c;
-  const int rows = (PT && rt.greedy) ? P.R : P.rows;
-  const int ft = fin_thread(), lane = ft & 31;
-  const int K = P.K;
-  // the rows a draw here may read: every n-gram target row, the bonus row of a draft-model chain
-  SsRows st{MODE == kNgram ? 0 : K, soft ? (MODE == kNgram ? K + 1 : 1) : 0};
-  const CsReader rd = stage_request_stats(P, sm, b, st, csph, rows);
-  combine_rows<MODE, PT>(P, sm, b, rd, soft, c, rows);
-  if (ft < 32) {
-    const int x0 = pf.x0;
-    const float r0 = pf.r0, lx0 = pf.lx0, dx0 = pf.dx0;
-    int e = 0;
-    for (int k = lane; k < K; k += 32) {
-      const int x = k < 32 ? x0 : __ldg(P.draft_tokens + (size_t)b * K + k);
-      float alpha = 0.f;
-      if (x < 0 || x >= P.V) {
-        e |= SPEC_ERRF_BAD_TOKEN;
-      } else {
-        const RowStat t = read_rowstat(P, sm, b, k);
-        if (soft) {
-          // alpha = p(x) / q(x) = 2^((l_x c - mc_t) - (d_x c - mc_d)) Z_d / Z_t (draft model), or
-          // p(x) = 2^(l_x c - mc_t) / Z_t (one-hot draft); capped at 1
-          const float lx = k < 32 ? lx0 : Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, k) + (size_t)x * S));
-          const Exp2 ext = scaled_logit(lx, c, t.mc);
-          if (MODE == kChain) {
-            const RowStat d = read_rowstat(P, sm, b, P.R + k);
-            const float dx =
-                k < 32 ? dx0 : Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, P.R + k) + (size_t)x * S));
-            if (dx == -INFINITY) {
-              alpha = 1.f;  // q(x) = 0
-            } else if (lx == -INFINITY) {
-              alpha = 0.f;  // p(x) = 0
-            } else {
-              const float ratio =
-                  exp2_times(exp2_sub(ext, scaled_logit(dx, c, d.mc)), __fdiv_rn((float)d.Z, (float)t.Z));
-              alpha = fminf(ratio, 1.f);
-            }
-          } else {
-            const float px = lx == -INFINITY ? 0.f : exp2_times(ext, __frcp_rn((float)t.Z));
-            alpha = fminf(px, 1.f);
-          }
-        } else {
-          alpha = (x == t.amax) ? 1.f : 0.f;
-        }
-      }
-      sm.alpha[k] = alpha;
+// ------------------------------------------------------------------ chain-mode finishing ----
+// The finishing group of a CTA finishes the requests b = blockIdx.x + j gridDim.x (j = 0, 1, ...),
+// kOwnMax at a time, taking their positions in turn as the stages of the stream come in: at stage
+// s it combines the chunk statistics of row s (and draft row s) into row normalisers, computes
+// alpha_s and makes the acceptance test (section I.1, steps 1-2).  At a request's first rejection,
+// or after its last accepted position, its accepted length n is decided: the n-gram residual and
+// the bonus draw are made at once from the row's statistics; a draft-model chain that rejected
+// publishes its residual parameters and queues the request for the residual pass (section I.1,
+// step 3), which the producers run while later stages stream in, and draws at the end.  A
+// request's error bits (a NaN row, a bad token) are known only once all its rows are in, so its
+// outputs are final only then: a request that fails is written as failed whatever was decided.
+
+// Combines the chunk statistics of rows r0 and r1 (r1 < 0: none) of request b into RowStat
+// (P.rstat, and sm.srs[0] / sm.srs[1]): softmax statistics (soft, c = log2(e) / T) or argmax.  The
+// group waits (bounded) until every chunk statistic carries the call's tag (the count only says
+// when to look).  G threads share a row, as in combine_rows.
+__device__ inline void combine_stage(const Params& P, Shared& sm, int b, int r0, int r1, bool soft, float c) {
+  const int nr = r1 >= 0 ? 2 : 1;
+  const ChunkStat* g0 = P.cstat + ((size_t)b * P.rows + r0) * P.nchunk;
+  const ChunkStat* g1 = r1 >= 0 ? P.cstat + ((size_t)b * P.rows + r1) * P.nchunk : g0;
+  await_tagged(P, sm, g0, P.nchunk);
+  if (r1 >= 0) await_tagged(P, sm, g1, P.nchunk);
+  const int ft = fin_thread(), nch = P.nchunk;
+  int G = 1;
+  while (G < 32 && G < nch && nr * 2 * G <= kFinThreads) G <<= 1;
+  const int g = ft & (G - 1), i = ft / G;
+  const bool act = i < nr;
+  const ChunkStat* gp = i == 1 ? g1 : g0;
+  float m = -INFINITY;
+  int fl = 0;
+  if (act) {
+    for (int ch = g; ch < nch; ch += G) {
+      const ChunkStat q = ld_chunkstat(gp + ch);
+      m = fmax_nan(m, q.a);
+      if (isnan(q.a) || (soft && q.a == INFINITY)) fl |= SPEC_ERRF_NONFINITE;
     }
-    for (int r = lane; r < rows; r += 32) e |= read_rowstat(P, sm, b, r).err;
-    // a bad per-request temperature fails the request with that bit alone
-    const int err = (PT && rt.bad) ? SPEC_ERRF_BAD_TEMPERATURE : warp_or(e);
-    __syncwarp();
-    int n = 0;
-    if (!err) {
-      n = K;
-      for (int k0 = 0; k0 < K; k0 += 32) {
-        const int k = k0 + lane;
-        bool rej = false;
-        if (k < K) {
-          const float a = sm.alpha[k];
-          const float rk = k < 32 ? r0 : __ldg(P.r + (size_t)b * K + k);
-          rej = soft ? !(rk <= a) : (a != 1.f);
-        }
-        const unsigned msk = __ballot_sync(kFull, rej);
-        if (msk) {
-          n = k0 + __ffs(msk) - 1;
-          break;
-        }
+  }
+  for (int o = G >> 1; o > 0; o >>= 1) {
+    m = fmax_nan(m, __shfl_xor_sync(kFull, m, o));
+    fl |= __shfl_xor_sync(kFull, fl, o);
+  }
+  RowStat rs;
+  rs.pad[0] = rs.pad[1] = rs.pad[2] = 0;
+  if (soft) {
+    const float mc = __fmul_rn(m, c);
+    const bool finite_m = !isnan(m) && m != INFINITY && m != -INFINITY;
+    float z = 0.f;
+    if (act && !fl && finite_m) {
+      for (int ch = g; ch < nch; ch += G) {
+        const ChunkStat q = ld_chunkstat(gp + ch);
+        z = __fadd_rn(z, chunk_weight(q.a, q.s, c, mc));
       }
     }
-    int xn = __shfl_sync(kFull, x0, n < 32 ? n : 0);
-    if (n >= 32 && n < K) xn = __ldg(P.draft_tokens + (size_t)b * K + n);
-    // publication of the acceptance result first (read by residual work items, which can start
-    // now, and by the probability rows)
-    if (MODE == kChain && P.npos > 0 && P.diag) {  // per-position residuals read the row statistics
-      __syncwarp();
-      __threadfence();
-    }
-    const bool resid = MODE == kChain && P.npos > 0 && !P.diag && !err && n < K && soft;
-    if (lane == 0 || (resid && lane < 4)) {
-      unsigned hi = (unsigned)n | ((unsigned)err << 16) | (soft ? 0u : kNoResid);
-      if (lane > 0) {
-        const RowStat t = read_rowstat(P, sm, b, n), d = read_rowstat(P, sm, b, P.R + n);
-        hi = __float_as_uint(lane == 1 ? t.mc : lane == 2 ? d.mc : __fdiv_rn((float)t.Z, (float)d.Z));
+    for (int o = G >> 1; o > 0; o >>= 1) z = __fadd_rn(z, __shfl_xor_sync(kFull, z, o));
+    const double Z = (!fl && finite_m) ? (double)z : 0.0;
+    rs.Z = Z;
+    rs.mc = mc;
+    rs.amax = -1;
+    rs.err = (fl || !finite_m || !(Z > 0.0) || isinf(Z)) ? (fl | SPEC_ERRF_NONFINITE) : 0;
+  } else {
+    int idx = INT_MAX;
+    if (act) {
+      for (int ch = g; ch < nch; ch += G) {
+        const ChunkStat q = ld_chunkstat(gp + ch);
+        if (q.a == m) idx = min(idx, __float_as_int(q.s));
       }
-      st_volatile_u64(P.req[b].w + lane, ((unsigned long long)hi << 32) | sm.tag);
     }
-    __syncwarp();
-    if (lane == 0) {
-      sm.gs.out[0] = n;
-      sm.gs.out[1] = err;
-      sm.gs.out[2] = xn;
-    }
+    for (int o = G >> 1; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(kFull, idx, o));
+    rs.Z = 0.0;
+    rs.mc = m;
+    rs.amax = (fl || idx == INT_MAX) ? -1 : idx;
+    rs.err = fl ? SPEC_ERRF_NONFINITE : 0;
+  }
+  if (act && g == 0) {
+    P.rstat[(size_t)b * P.rows + (i == 1 ? r1 : r0)] = rs;
+    sm.srs[i] = rs;
   }
   fin_sync();
-  const int n = sm.gs.out[0], err = sm.gs.out[1], xn = sm.gs.out[2];
-  // The emitted token's draw (n-gram at any n, the bonus row of a draft-model chain) starts its
-  // copies now, so that they overlap the outputs and the publication below.
-  const bool early = soft && !err && !P.diag && (MODE == kNgram || n == K);
-  DrawPlan dp{};
-  if (early) dp = draw_begin<T>(P, sm, fbuf, b, n, (MODE == kNgram && n < K) ? kExcl : kFullP, n < K ? xn : -1, st);
-  if (ft < 32) {
-    const int x0 = pf.x0;
-    for (int i = lane; i <= K; i += 32) {
-      const size_t o_i = (size_t)b * (K + 1) + i;
-      int o = -1;
-      if (!err && i < n) o = i < 32 ? x0 : __ldg(P.draft_tokens + (size_t)b * K + i);
-      if (!err && i == n && !soft) o = read_rowstat(P, sm, b, n).amax;
-      P.out_tokens[o_i] = o;
-      if (P.accept_prob && i < K) P.accept_prob[(size_t)b * K + i] = err ? 0.f : sm.alpha[i];
-      if (P.cand_tokens && (err || !soft)) P.cand_tokens[o_i] = err ? -1 : read_rowstat(P, sm, b, i).amax;
-      if (P.pos_mass && (err || !soft)) P.pos_mass[o_i] = err ? 0.f : 1.f;
-    }
-    if (lane == 0) {
-      P.num_accepted[b] = n;
-      if (P.err_flags) P.err_flags[b] = err;
-      if (P.residual_mass && (err || !soft)) P.residual_mass[b] = err ? 0.f : 1.f;
-    }
-  }
-  if constexpr (kSoftmax) {
-    if (err) return -1;
-    if (!soft) return n;  // a greedy request of a per-request-temperature call: no draw
-    auto emit = [&](int k, int tok, float mass) {
-      if (ft == 0) {
-        const size_t o_k = (size_t)b * (K + 1) + k;
-        if (k == n) {
-          P.out_tokens[o_k] = tok;
-          if (P.residual_mass) P.residual_mass[b] = mass;
-        }
-        if (P.cand_tokens) P.cand_tokens[o_k] = tok;
-        if (P.pos_mass) P.pos_mass[o_k] = mass;
-      }
-    };
-    const float u = pf.u;  // used by the leader only
-    if (early) {
-      float mass;
-      const int tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, dp, rd, read_rowstat(P, sm, b, n), u, c, &mass);
-      emit(n, tok, mass);
-    } else if (P.diag) {
-      // per-position outputs: a draw at every position made here (the bonus row, and for
-      // n-gram every residual; draft-model residuals are drawn by residual work items)
-      for (int k = MODE == kChain ? K : 0; k <= K; ++k) {
-        const int kind = (MODE == kNgram && k < K) ? kExcl : kFullP;
-        const int x = k < K ? __ldg(P.draft_tokens + (size_t)b * K + k) : -1;
-        const DrawPlan d = draw_begin<T>(P, sm, fbuf, b, k, kind, x, st);
-        float mass;
-        const int tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, d, rd, read_rowstat(P, sm, b, k), u, c, &mass);
-        emit(k, tok, mass);
-      }
-    }
-  }
-  return err ? -1 : n;
 }
 
-// Draft-model chain: the draw from max(0, p_k - q_k) once every residual item of (b, position
-// slot kk) is in.
+// Draft-model chain: the draw from max(0, p_k - q_k) at position k once every residual item of
+// (b, position slot kk) is in (ts, ds: the statistics of target and draft row k).  Every thread
+// gets the token (-1 after a timeout) and the residual mass.
 template <typename T>
 __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph,
-                              int b, int kk, int n, float c) {
+                              int b, int kk, int k, float c, float u, const RowStat& ts, const RowStat& ds,
+                              int* tok_out, float* mass_out) {
   constexpr int VE = Elem<T>::kPerVec;
   const int ft = fin_thread(), lane = ft & 31;
-  const int k = P.diag ? kk : n;
-  const RowStat ts = read_rowstat(P, sm, b, k);
-  const RowStat ds = read_rowstat(P, sm, b, P.R + k);
   const size_t bk = (size_t)b * P.npos + kk;
-  const float u = __ldg(P.u + b);
   // the residual sums and sub-range sums of the position, once all carry the call's tag, copied
   // into shared memory when they fit (the sub-chunk statistics' buffer is free here)
   const TagSum* ws = P.wsum + bk * P.nchunk_r;
@@ -1506,7 +1475,7 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
   // the leader picks the residual chunk and sub-range and stages the crossing pair (no draw
   // after a timeout)
   if (ft < 32) {
-    auto weight = [&](int c) { return cached ? cache[c] : ld_tagsum(ws + c).v; };
+    auto weight = [&](int ch) { return cached ? cache[ch] : ld_tagsum(ws + ch).v; };
     const float S = sums_ok ? total_weight(P.nchunk_r, weight) : 0.f;
     int state = sums_ok ? 0 : 2;  // 0: no residual mass, 1: the crossing pair is being staged, 2: none
     int cstar = -1, sstar = -1;
@@ -1566,14 +1535,414 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
     const DrawPlan d = draw_begin<T>(P, sm, fbuf, b, k, kFullP, -1, none);
     tok = draw_end<T>(P, sm, fbuf, fph, ssph, b, d, rd, ts, u, c, &unused);
   }
-  if (ft == 0) {
-    const size_t o_k = (size_t)b * (P.K + 1) + k;
-    if (k == n) {
-      P.out_tokens[o_k] = tok;
-      if (P.residual_mass) P.residual_mass[b] = rmass;
+  *tok_out = tok;
+  *mass_out = rmass;
+}
+
+// A draw by inverse CDF from target row `row` of request b (p, or p without token x for kExcl),
+// from the row's chunk and sub-chunk statistics.  Every thread gets the token and the mass.
+template <typename T>
+__device__ int row_draw(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph, int b,
+                        int row, int kind, int x, const RowStat& rs, float u, float c, float* mass) {
+  SsRows none{0, 0};
+  const DrawPlan d = draw_begin<T>(P, sm, fbuf, b, row, kind, x, none);
+  CsReader rd;
+  rd.g = P.cstat + (size_t)b * P.rows * P.nchunk;
+  rd.s = nullptr;
+  rd.nchunk = P.nchunk;
+  return draw_end<T>(P, sm, fbuf, fph, ssph, b, d, rd, rs, u, c, mass);
+}
+
+// The outputs of a request (the leader warp): n, the token and the mass, or a failed request when
+// err is set.  The accepted prefix was written as it was accepted.
+__device__ __forceinline__ void write_outputs(const Params& P, int b, int n, int tok, float mass, int err) {
+  const int lane = fin_thread() & 31, K = P.K;
+  for (int i = lane; i <= K; i += 32) {
+    const size_t o_i = (size_t)b * (K + 1) + i;
+    if (err) {
+      P.out_tokens[o_i] = -1;
+      if (P.accept_prob && i < K) P.accept_prob[(size_t)b * K + i] = 0.f;
+      if (P.cand_tokens) P.cand_tokens[o_i] = -1;
+      if (P.pos_mass) P.pos_mass[o_i] = 0.f;
+    } else if (i >= n) {
+      P.out_tokens[o_i] = i == n ? tok : -1;
     }
-    if (P.cand_tokens) P.cand_tokens[o_k] = tok;
-    if (P.pos_mass) P.pos_mass[o_k] = rmass;
+  }
+  if (lane == 0) {
+    P.num_accepted[b] = err ? 0 : n;
+    if (P.err_flags) P.err_flags[b] = err;
+    if (P.residual_mass) P.residual_mass[b] = err ? 0.f : mass;
+  }
+}
+
+// The error bits of rows r0 and r1 (r1 < 0: none) of request b from their chunk maxima alone (a
+// NaN; where a softmax is taken, +inf or only -inf): all a decided request still needs of a
+// later position (the group waits for the tags; the leader warp decides).
+__device__ inline int stage_errors(const Params& P, Shared& sm, int b, int r0, int r1, bool soft) {
+  const ChunkStat* g0 = P.cstat + ((size_t)b * P.rows + r0) * P.nchunk;
+  const ChunkStat* g1 = r1 >= 0 ? P.cstat + ((size_t)b * P.rows + r1) * P.nchunk : g0;
+  await_tagged(P, sm, g0, P.nchunk);
+  if (r1 >= 0) await_tagged(P, sm, g1, P.nchunk);
+  int e = 0;
+  if (fin_thread() < 32) {
+    const int lane = fin_thread() & 31;
+    float m0 = -INFINITY, m1 = -INFINITY;
+    int f = 0;
+    for (int i = lane; i < P.nchunk; i += 32) {
+      const float a = ld_chunkstat(g0 + i).a, d = r1 >= 0 ? ld_chunkstat(g1 + i).a : -INFINITY;
+      m0 = fmax_nan(m0, a);
+      m1 = fmax_nan(m1, d);
+      f |= (isnan(a) || isnan(d) || (soft && (a == INFINITY || d == INFINITY))) ? 1 : 0;
+    }
+    m0 = warp_max_nan(m0);
+    m1 = warp_max_nan(m1);
+    f = warp_or(f);
+    if (f || (soft && (m0 == -INFINITY || (r1 >= 0 && m1 == -INFINITY)))) e = SPEC_ERRF_NONFINITE;
+  }
+  return e;
+}
+
+// The result of request j is decided at its position n (x: the draft token there).
+template <int MODE, typename T, bool PT>
+__device__ void decide(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph, int j,
+                       int x) {
+  constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
+  const int ft = fin_thread(), lane = ft & 31;
+  FinReq& q = sm.fr[j];
+  const int b = q.b, n = q.n, K = P.K, err = q.err;
+  const bool soft = PT ? !q.greedy : kSoftmax;
+  const float c = PT ? q.c : P.c;
+  const bool resid_calls = MODE == kChain && P.npos > 0;           // the call runs residual passes
+  const bool late = P.diag && (MODE == kNgram || resid_calls);     // per-position draws, all at the end
+  if (resid_calls && !P.diag) {
+    // publish the result (with the error bits seen so far), then queue the request: its residual
+    // items are handed out in queue order, once the producers see the words complete
+    if (ft < 32) {
+      const bool resid = soft && !err && n < K;
+      if (lane == 0 || (resid && lane < 4)) {
+        unsigned hi = (unsigned)n | ((unsigned)err << 16) | (soft ? 0u : kNoResid);
+        if (lane > 0)
+          hi = __float_as_uint(lane == 1 ? q.rt.mc : lane == 2 ? q.rd.mc : __fdiv_rn((float)q.rt.Z, (float)q.rd.Z));
+        st_volatile_u64(P.req[b].w + lane, ((unsigned long long)hi << 32) | sm.tag);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        const unsigned slot = atomicAdd(P.rq_tail, 1u);
+        st_volatile_u64(P.rq + slot, ((unsigned long long)(unsigned)b << 32) | sm.tag);
+        q.resid = resid ? 1 : 0;
+      }
+    }
+  } else if (!(resid_calls && P.diag) && ft == 0) {
+    // the result word (read by the probability rows' kernel)
+    const unsigned hi = (unsigned)n | ((unsigned)err << 16);
+    st_volatile_u64(P.req[b].w, ((unsigned long long)hi << 32) | sm.tag);
+  }
+  if (!soft || err) {  // greedy: the argmax of row n; a failed request draws nothing
+    if (ft == 0) {
+      q.tok = err ? -1 : q.rt.amax;
+      q.mass = err ? 0.f : 1.f;
+      q.drawn = 1;
+    }
+  } else if ((MODE == kNgram || n == K) && !late) {  // the n-gram residual or the bonus draw, now
+    float mass;
+    const int tok = row_draw<T>(P, sm, fbuf, fph, ssph, b, n, (MODE == kNgram && n < K) ? kExcl : kFullP,
+                                n < K ? x : -1, q.rt, q.u, c, &mass);
+    if (ft == 0) {
+      q.tok = tok;
+      q.mass = mass;
+      q.drawn = 1;
+      // (per-position outputs of a chain without residual passes: its one position, the bonus row)
+      if (P.cand_tokens) P.cand_tokens[(size_t)b * (K + 1) + n] = tok;
+      if (P.pos_mass) P.pos_mass[(size_t)b * (K + 1) + n] = mass;
+    }
+  }
+  fin_sync();
+  // the outputs as far as known now (a later error rewrites them)
+  if (q.drawn && !err && !late) {
+    if (ft < 32) write_outputs(P, b, n, q.tok, q.mass, 0);
+    if (ft == 0) q.written = 1;
+  }
+  fin_sync();
+}
+
+// The residual draw of request j, whose residual items are all in; its outputs follow when no
+// error has turned up so far (draft-model chains without per-position outputs).
+template <typename T, bool PT>
+__device__ void early_residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph,
+                                    uint32_t& ssph, int j) {
+  const int ft = fin_thread();
+  FinReq& q = sm.fr[j];
+  if (ft == 0) P.tick_b[(size_t)q.b * P.npos] = 0;  // complete: left as the next call expects it
+  int tok;
+  float mass;
+  residual_draw<T>(P, sm, fbuf, fph, ssph, q.b, 0, q.n, PT ? q.c : P.c, q.u, q.rt, q.rd, &tok, &mass);
+  if (ft == 0) {
+    q.tok = tok;
+    q.mass = mass;
+    q.drawn = 1;
+  }
+  fin_sync();
+  if (!q.err) {
+    if (ft < 32) write_outputs(P, q.b, q.n, tok, mass, 0);
+    if (ft == 0) q.written = 1;
+  }
+  fin_sync();
+}
+
+// Waits (bounded) until *count reaches `want`, making meanwhile the residual draws of the requests
+// j < own whose residual items come in (draft-model chains without per-position outputs), so that
+// a late rejection's draw does not wait for the end of the stream.  False after a timeout.
+template <int MODE, typename T, bool PT>
+__device__ bool wait_stage(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph,
+                           int own, const unsigned* count, unsigned want) {
+  if (!(MODE == kChain && P.npos > 0 && !P.diag)) return wait_count(P, sm, count, want);
+  const int ft = fin_thread();
+  long long t0 = clock64();
+  for (;;) {
+    if (ft == 0) {
+      int act = 0;  // 1: the count is in; 2 + j: request j's residual items are in; -1: gave up
+      if (ld_acquire_u32(count) >= want) {
+        act = 1;
+      } else {
+        for (int j = 0; j < own && !act; ++j) {
+          const FinReq& q = sm.fr[j];
+          if (q.resid && !q.drawn && ld_acquire_u32(P.tick_b + (size_t)q.b * P.npos) >= (unsigned)P.nchunk_r)
+            act = 2 + j;
+        }
+        if (!act && (aborted(sm) || clock64() - t0 > kWaitLimitCycles)) {
+          raise_abort(P, sm);
+          act = -1;
+        }
+      }
+      sm.gs.out[3] = act;
+    }
+    fin_sync();
+    const int act = sm.gs.out[3];
+    fin_sync();
+    if (act == 1) return true;
+    if (act < 0) return false;
+    if (act >= 2) {
+      early_residual_draw<T, PT>(P, sm, fbuf, fph, ssph, act - 2);
+      t0 = clock64();
+      continue;
+    }
+    __nanosleep(64);
+  }
+}
+
+// Stage s of request j: waits for the stage's rows, combines them, makes the acceptance test.
+// False after a timeout.
+template <int MODE, typename T, bool PT>
+__device__ bool finish_stage(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph,
+                             int j, int s, int own) {
+  constexpr int S = Elem<T>::kSize;
+  constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
+  const int ft = fin_thread();
+  FinReq& q = sm.fr[j];
+  const int b = q.b, K = P.K, R = P.R;
+  const bool soft = PT ? !q.greedy : kSoftmax;
+  const float c = PT ? q.c : P.c;
+  const bool pair = MODE == kChain && soft && s < K;  // the stage holds the draft row too
+  // the position's inputs, loaded by the leader while the stage's rows stream in
+  int x = 0;
+  float rr = 0.f, lx = 0.f, dx = 0.f;
+  if (ft == 0 && s < K) {
+    x = __ldg(P.draft_tokens + (size_t)b * K + s);
+    if (soft) {
+      rr = __ldg(P.r + (size_t)b * K + s);
+      if (x >= 0 && x < P.V) {
+        lx = Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, s) + (size_t)x * S));
+        if (MODE == kChain) dx = Elem<T>::to_float(Elem<T>::load_raw(row_ptr<T>(P, b, R + s) + (size_t)x * S));
+      }
+    }
+  }
+  unsigned* tick = P.tick_a + (size_t)b * R + s;
+  if (!wait_stage<MODE, T, PT>(P, sm, fbuf, fph, ssph, own, tick, (unsigned)P.nchunk * (pair ? 2u : 1u)))
+    return false;
+  if (ft == 0) *tick = 0;  // complete: the count is left as the next call expects it
+  // a request already decided needs only the error bits of its later rows, unless the call asks
+  // for outputs at every position (or the rows' statistics)
+  if (q.n >= 0 && !P.diag && !P.accept_prob && !P.target_probs && !P.draft_probs) {
+    const int e = stage_errors(P, sm, b, s, pair ? R + s : -1, soft);
+    if (ft == 0) q.err |= e | ((s < K && (x < 0 || x >= P.V)) ? SPEC_ERRF_BAD_TOKEN : 0);
+    fin_sync();
+    return true;
+  }
+  combine_stage(P, sm, b, s, pair ? R + s : -1, soft, c);
+  if (ft == 0) {
+    const RowStat t = sm.srs[0], d = sm.srs[1];
+    int e = t.err | (pair ? d.err : 0);
+    float alpha = 0.f;
+    bool acc = false;
+    const size_t o_s = (size_t)b * (K + 1) + s;
+    if (s < K) {
+      if (x < 0 || x >= P.V) {
+        e |= SPEC_ERRF_BAD_TOKEN;
+      } else if (soft) {
+        // alpha = p(x) / q(x) = 2^((l_x c - mc_t) - (d_x c - mc_d)) Z_d / Z_t (draft model), or
+        // p(x) = 2^(l_x c - mc_t) / Z_t (one-hot draft); capped at 1
+        const Exp2 ext = scaled_logit(lx, c, t.mc);
+        if (MODE == kChain) {
+          if (dx == -INFINITY)
+            alpha = 1.f;  // q(x) = 0
+          else if (lx == -INFINITY)
+            alpha = 0.f;  // p(x) = 0
+          else
+            alpha = fminf(exp2_times(exp2_sub(ext, scaled_logit(dx, c, d.mc)), __fdiv_rn((float)d.Z, (float)t.Z)),
+                          1.f);
+        } else {
+          alpha = fminf(lx == -INFINITY ? 0.f : exp2_times(ext, __frcp_rn((float)t.Z)), 1.f);
+        }
+        acc = rr <= alpha;
+      } else {
+        alpha = (x == t.amax) ? 1.f : 0.f;
+        acc = alpha == 1.f;
+      }
+      if (P.accept_prob) P.accept_prob[(size_t)b * K + s] = alpha;
+    }
+    if (!soft) {  // greedy per-position outputs: the row's argmax
+      if (P.cand_tokens) P.cand_tokens[o_s] = t.amax;
+      if (P.pos_mass) P.pos_mass[o_s] = 1.f;
+    }
+    q.err |= e;
+    int decided = 0;
+    if (q.n < 0) {
+      if (acc) {
+        P.out_tokens[o_s] = x;
+      } else {
+        q.n = s;
+        q.rt = t;
+        q.rd = d;
+        decided = 1;
+      }
+    }
+    sm.gs.out[0] = decided;
+    sm.gs.out[1] = x;
+  }
+  fin_sync();
+  const int decided = sm.gs.out[0], xs = sm.gs.out[1];
+  fin_sync();
+  if (decided) decide<MODE, T, PT>(P, sm, fbuf, fph, ssph, j, xs);
+  return true;
+}
+
+// Request j once every stage is in: the remaining draws, then the outputs.  False after a timeout.
+template <int MODE, typename T, bool PT>
+__device__ bool finalize_request(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph,
+                                 int j) {
+  constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
+  const int ft = fin_thread(), lane = ft & 31;
+  FinReq& q = sm.fr[j];
+  const int b = q.b, n = q.n, K = P.K, R = P.R;
+  const bool soft = PT ? !q.greedy : kSoftmax;
+  const float c = PT ? q.c : P.c;
+  const int err = (PT && q.bad) ? SPEC_ERRF_BAD_TEMPERATURE : q.err;
+  const bool draws = soft && !err;
+  auto put_cand = [&](int k, int tok, float mass) {
+    if (ft == 0) {
+      if (P.cand_tokens) P.cand_tokens[(size_t)b * (K + 1) + k] = tok;
+      if (P.pos_mass) P.pos_mass[(size_t)b * (K + 1) + k] = mass;
+    }
+  };
+  if (MODE == kChain && P.npos > 0) {
+    if (P.diag) {
+      // per-position outputs: now that every row's statistics are in, publish the result and queue
+      // the request; the producers read each position's parameters from the row statistics
+      if (ft == 0) {
+        __threadfence();
+        const unsigned hi = (unsigned)n | ((unsigned)err << 16) | (soft ? 0u : kNoResid);
+        st_volatile_u64(P.req[b].w, ((unsigned long long)hi << 32) | sm.tag);
+        const unsigned slot = atomicAdd(P.rq_tail, 1u);
+        st_volatile_u64(P.rq + slot, ((unsigned long long)(unsigned)b << 32) | sm.tag);
+      }
+      if (draws) {
+        for (int kk = 0; kk < K; ++kk) {
+          if (!wait_count(P, sm, P.tick_b + (size_t)b * P.npos + kk, (unsigned)P.nchunk_r)) return false;
+          if (ft == 0) P.tick_b[(size_t)b * P.npos + kk] = 0;
+          const RowStat ts = ld_rowstat(P.rstat + (size_t)b * P.rows + kk);
+          const RowStat ds = ld_rowstat(P.rstat + (size_t)b * P.rows + R + kk);
+          int tok;
+          float mass;
+          residual_draw<T>(P, sm, fbuf, fph, ssph, b, kk, kk, c, q.u, ts, ds, &tok, &mass);
+          put_cand(kk, tok, mass);
+          if (ft == 0 && kk == n) {
+            q.tok = tok;
+            q.mass = mass;
+          }
+        }
+        float mass;
+        const RowStat tb = ld_rowstat(P.rstat + (size_t)b * P.rows + K);
+        const int tok = row_draw<T>(P, sm, fbuf, fph, ssph, b, K, kFullP, -1, tb, q.u, c, &mass);
+        put_cand(K, tok, mass);
+        if (ft == 0 && n == K) {
+          q.tok = tok;
+          q.mass = mass;
+        }
+      }
+    } else if (q.resid && !q.drawn) {  // the residual pass published at the decision (its result is
+                                       // used only when no error turned up since)
+      if (!wait_count(P, sm, P.tick_b + (size_t)b * P.npos, (unsigned)P.nchunk_r)) return false;
+      if (ft == 0) P.tick_b[(size_t)b * P.npos] = 0;
+      int tok;
+      float mass;
+      residual_draw<T>(P, sm, fbuf, fph, ssph, b, 0, n, c, q.u, q.rt, q.rd, &tok, &mass);
+      if (ft == 0) {
+        q.tok = tok;
+        q.mass = mass;
+      }
+    }
+  }
+  if (MODE == kNgram && P.diag && draws) {  // per-position outputs: a draw at every position
+    for (int k = 0; k <= K; ++k) {
+      const RowStat rs = ld_rowstat(P.rstat + (size_t)b * P.rows + k);
+      const int x = k < K ? __ldg(P.draft_tokens + (size_t)b * K + k) : -1;
+      float mass;
+      const int tok = row_draw<T>(P, sm, fbuf, fph, ssph, b, k, k < K ? kExcl : kFullP, x, rs, q.u, c, &mass);
+      put_cand(k, tok, mass);
+      if (ft == 0 && k == n) {
+        q.tok = tok;
+        q.mass = mass;
+      }
+    }
+  }
+  fin_sync();
+  // the outputs, unless they were written already and no error turned up since
+  if ((err || !q.written) && ft < 32) write_outputs(P, b, n, q.tok, q.mass, err);
+  fin_sync();
+  return true;
+}
+
+// The finishing group of a chain mode: its requests, kOwnMax at a time, position by position.
+template <int MODE, typename T, bool PT>
+__device__ void fin_loop_chain(const Params& P, Shared& sm, unsigned char* fbuf) {
+  constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
+  const int ft = fin_thread();
+  uint32_t fph = 0, ssph = 0;
+  const int G = (int)gridDim.x;
+  for (int b0 = blockIdx.x; b0 < P.B; b0 += kOwnMax * G) {
+    const int own = min(kOwnMax, (P.B - b0 + G - 1) / G);
+    if (ft < own) {
+      FinReq& q = sm.fr[ft];
+      q.b = b0 + ft * G;
+      q.n = -1;
+      q.err = 0;
+      q.tok = -1;
+      q.resid = 0;
+      q.drawn = 0;
+      q.written = 0;
+      q.mass = 0.f;
+      const ReqTemp rt = req_temp<MODE, PT>(P, q.b);
+      q.c = rt.c;
+      q.greedy = rt.greedy;
+      q.bad = rt.bad;
+      q.u = kSoftmax ? __ldg(P.u + q.b) : 0.f;
+    }
+    fin_sync();
+    for (int s = 0; s <= P.K; ++s)
+      for (int j = 0; j < own; ++j)
+        if (!finish_stage<MODE, T, PT>(P, sm, fbuf, fph, ssph, j, s, own)) return;
+    for (int j = 0; j < own; ++j)
+      if (!finalize_request<MODE, T, PT>(P, sm, fbuf, fph, ssph, j)) return;
   }
 }
 
@@ -1643,39 +2012,16 @@ __device__ inline void walk_tree(const Params& P, Shared& sm, int b) {
   }
 }
 
-// Waits (bounded) until *count reaches `want`: the leader polls (with acquire semantics, so the
-// statistics counted before it are visible afterwards), then the group agrees.  False on a
-// timeout or abort.
-__device__ __forceinline__ bool wait_count(const Params& P, Shared& sm, const unsigned* count, unsigned want) {
-  int ok = 1;
-  if (fin_thread() == 0) {
-    ok = 0;
-    const long long t0 = clock64();
-    for (;;) {
-      if (ld_acquire_u32(count) >= want) {
-        ok = 1;
-        break;
-      }
-      if (aborted(sm)) break;
-      if (clock64() - t0 > kWaitLimitCycles) {
-        raise_abort(P, sm);
-        break;
-      }
-      __nanosleep(64);
-    }
-  }
-  return fin_all(ok != 0);
-}
-
-// The finishing group's loop over its requests.  A request's inputs are loaded while its chunks
-// are still being read.
+// The finishing group's loop over its requests (trees; the chain modes take fin_loop_chain).
 template <int MODE, typename T, bool PT>
 __device__ void fin_loop(const Params& P, Shared& sm, unsigned char* fbuf) {
-  const int ft = fin_thread();
-  uint32_t fph = 0, csph = 0, ssph = 0;
-  const unsigned per_req = (unsigned)(P.rows * P.nchunk);
-  for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
-    if constexpr (MODE == kTree) {
+  if constexpr (MODE != kTree) {
+    fin_loop_chain<MODE, T, PT>(P, sm, fbuf);
+  } else {
+    const int ft = fin_thread();
+    uint32_t csph = 0;
+    const unsigned per_req = (unsigned)(P.rows * P.nchunk);
+    for (int b = blockIdx.x; b < P.B; b += gridDim.x) {
       const int N1 = P.R;
       if (N1 <= kFinRows) {
         for (int i = ft; i < N1; i += kFinThreads) {
@@ -1690,25 +2036,6 @@ __device__ void fin_loop(const Params& P, Shared& sm, unsigned char* fbuf) {
       combine_rows<MODE, false>(P, sm, b, rd, false, 0.f, P.rows);
       walk_tree(P, sm, b);
       fin_sync();  // the walk's reads of the shared copies come before the next request's writes
-    } else {
-      const ReqTemp rt = req_temp<MODE, PT>(P, b);
-      // a greedy request of a per-request-temperature call has its target rows' chunks only
-      const unsigned want = (PT && rt.greedy) ? (unsigned)(P.R * P.nchunk) : per_req;
-      ReqPrefetch pf{0, 0.f, 0.f, 0.f, 0.f};
-      if (ft < 32) pf = prefetch_request<MODE, T>(P, b);
-      if (!wait_count(P, sm, P.tick_a + b, want)) return;
-      if (ft == 0) P.tick_a[b] = 0;  // complete: the count is left as the next call expects it
-      const int n = finish_chain<MODE, T, PT>(P, sm, fbuf, fph, csph, ssph, b, pf, rt);
-      if constexpr (MODE == kChain) {
-        if (P.npos > 0 && n >= 0 && !(PT && rt.greedy)) {
-          for (int kk = 0; kk < P.npos; ++kk) {
-            if (!P.diag && n >= P.K) break;  // everything accepted: the bonus draw was made above
-            if (!wait_count(P, sm, P.tick_b + (size_t)b * P.npos + kk, (unsigned)P.nchunk_r)) return;
-            if (ft == 0) P.tick_b[(size_t)b * P.npos + kk] = 0;
-            residual_draw<T>(P, sm, fbuf, fph, ssph, b, kk, n, rt.c);
-          }
-        }
-      }
     }
   }
 }
@@ -1766,12 +2093,14 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
     if (tid == 0) {
       *P.work = 0u;
       *P.rc = 0u;
+      if (P.rq_tail) *P.rq_tail = 0u;
       *P.gerr = 0u;
       *P.exit_tick = 0u;
       *P.epoch = sm.tag;
     }
     if (timed_out) {
-      for (int i = tid; i < P.B; i += kThreads) P.tick_a[i] = 0u;
+      const int na = (MODE == kTree) ? P.B : P.B * P.R;  // counts per request, or per request and position
+      for (int i = tid; i < na; i += kThreads) P.tick_a[i] = 0u;
       for (int i = tid; i < P.B * P.npos; i += kThreads) P.tick_b[i] = 0u;
       const int width = (MODE == kTree) ? P.R : P.K + 1;
       for (int b = tid; b < P.B; b += kThreads) {
@@ -1796,8 +2125,9 @@ __global__ void __launch_bounds__(256) probs_kernel(const Params P) {
   const int rowid = blockIdx.x;  // b * rows + r
   const int b = rowid / P.rows, r = rowid - b * P.rows;
   const unsigned long long w0 = P.req[b].w[0];
-  // (the verification kernel before this one left its tag as the epoch)
-  if (!req_word_ok(w0, *P.epoch) || (req_word_hi(w0) >> 16) != 0u) return;  // no result, or an error
+  // (the verification kernel before this one left its tag as the epoch; a row with an error, or of
+  // a request that failed, has no distribution to write)
+  if (!req_word_ok(w0, *P.epoch) || (req_word_hi(w0) >> 16) != 0u) return;
   float* out = r < P.R ? (P.target_probs ? P.target_probs + ((size_t)b * P.R + r) * P.V : nullptr)
                        : (P.draft_probs ? P.draft_probs + ((size_t)b * P.K + (r - P.R)) * P.V : nullptr);
   if (!out) return;
@@ -1808,6 +2138,7 @@ __global__ void __launch_bounds__(256) probs_kernel(const Params P) {
     c = (float)(1.4426950408889634 / (double)Tb);
   }
   const RowStat rs = P.rstat[rowid];
+  if (rs.err || !(rs.Z > 0.0)) return;
   const char* rp = row_ptr<T>(P, b, r);
   const float invZ = (float)(1.0 / rs.Z);
   for (int i = (int)threadIdx.x; i < P.V; i += 256) {

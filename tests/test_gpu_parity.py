@@ -114,7 +114,7 @@ def test_chain_batched_full_size(seed, diag):
     configuration (diag=False) and with per-position outputs; flagged requests checked against
     their admissible outcomes, and the flagged share bounded."""
     ci = synth.chain_batched(seed=seed)
-    g = parity.run_gpu_chain(ci, diag=diag)
+    g = parity.run_gpu_chain(ci, diag=diag, hot=not diag)
     st = parity.compare_chain(g, parity.run_oracle_chain(ci, threads=16), ci)
     _show(f"chain batched full seed={seed} diag={diag}", st)
     assert st["flagged"] <= FLAG_BOUND["chain"] * ci.B, st
@@ -138,7 +138,7 @@ def test_tree_full_size(path_boost):
 def test_ngram_full_size(boost, diag):
     """B = 256, K = 5, V = 151936 bf16, T = 0.8; boost 14 makes drafts likely (bonus path)."""
     ci = synth.ngram(seed=0, boost=boost)
-    g = parity.run_gpu_chain(ci, ngram=True, diag=diag)
+    g = parity.run_gpu_chain(ci, ngram=True, diag=diag, hot=not diag)
     st = parity.compare_chain(g, parity.run_oracle_chain(ci, ngram=True, threads=16), ci)
     _show(f"ngram boost={boost} diag={diag}", st)
     assert st["flagged"] <= FLAG_BOUND["ngram"] * ci.B, st
@@ -211,9 +211,13 @@ def test_masked_tokens_and_invalid_inputs():
         o = parity.run_oracle_chain(ci)
         parity.compare_chain(parity.run_gpu_chain(ci), o, ci)
         parity.compare_chain(parity.run_gpu_chain(ci, diag=False), o, ci)
+        # no optional outputs: a request decided before its bad row streams in has its outputs
+        # written early, then rewritten as failed
+        parity.compare_chain(parity.run_gpu_chain(ci, diag=False, hot=True), o, ci)
         assert (o["err"] != 0).sum() >= 4
         on = parity.run_oracle_chain(ci, ngram=True)
         parity.compare_chain(parity.run_gpu_chain(ci, ngram=True), on, ci)
+        parity.compare_chain(parity.run_gpu_chain(ci, ngram=True, diag=False, hot=True), on, ci)
 
 
 def test_malformed_trees():
@@ -334,7 +338,7 @@ def test_per_request_temperatures_full_size(ngram, diag):
     1.4 over the requests (0: that request verified greedily, its draft rows not read)."""
     ci = synth.ngram(seed=0) if ngram else synth.chain_batched(seed=0)
     temps = np.resize(MIXED_T, ci.B)
-    g = parity.run_gpu_chain(ci, ngram=ngram, diag=diag, temperatures=temps)
+    g = parity.run_gpu_chain(ci, ngram=ngram, diag=diag, temperatures=temps, hot=not diag)
     st = parity.compare_chain(g, parity.run_oracle_chain(ci, ngram=ngram, threads=16, temperatures=temps), ci)
     _show(f"per-request T ngram={ngram} diag={diag}", st)
     assert st["flagged"] <= FLAG_BOUND["ngram" if ngram else "chain"] * ci.B, st
