@@ -254,6 +254,10 @@ spec_status_t verify_chain_common(bool ngram, const void* target, const void* dr
   P.R = K + 1;
   P.rows = rows;
   P.diag = diag;
+  // the bonus rows stream first when the call runs residual passes at one temperature (the stream
+  // then ends on the last position, which few requests reach); measured slower for calls without
+  // residual passes and for per-request temperatures
+  P.bonus_first = (P.npos > 0 && !temps) ? 1 : 0;
   P.c = (greedy || temps) ? 0.f : (float)(1.4426950408889634 / (double)T);  // log2(e) / T
   P.temps = temps;
   P.draft_tokens = x;

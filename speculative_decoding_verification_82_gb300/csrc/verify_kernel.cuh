@@ -97,6 +97,7 @@ struct Params {
   int nchunk_r;    // residual items per row (kResVec target vectors each)
   int npos;          // residual positions per request (K with per-position outputs, else 1); 0: none
   int diag;          // 1: draw at every position (per-position outputs requested)
+  int bonus_first;   // chain modes: the bonus rows stream first (else last)
   float c;           // log2(e) / T (calls with one temperature)
   const float* temps;  // [B] per-request temperatures (calls with PT = true), else nullptr
   unsigned total;    // stats items (A per request)
@@ -267,6 +268,8 @@ struct FinReq {
   int resid;   // a residual pass was published for position n (draft-model chains)
   int drawn;   // the emitted token is known
   int written; // the outputs were written (no error seen then; rewritten if one turns up later)
+  int btok;    // the bonus token, made from the first stage (-1 until then)
+  float bmass;
   int greedy, bad;
   float c, u, mass;
   RowStat rt, rd;  // target and draft row statistics at position n
@@ -304,9 +307,11 @@ __device__ __forceinline__ bool aborted(const Shared& sm) {
 // Stats items of trees are request-major, then row, then chunk: item w < P.total is chunk item
 // w mod A of request w / A.  Stats items of the chain modes are position-major ("stages"): stage
 // s < K holds the rows of position s of every request (target row s, and draft row s when the
-// call reads draft logits), request by request, then row, then chunk; the last stage holds every
-// request's bonus row (target row K).  So the acceptance test at position s of every request can
-// be made once stage s is in, and the residual pass of a request rejected there overlaps the
+// call reads draft logits), request by request, then row, then chunk; the bonus stage holds every
+// request's bonus row (target row K), last, or first when P.bonus_first (calls with residual
+// passes: the bonus draw is then made before the acceptance tests end, and the stream ends on the
+// last position, which few requests reach).  So the acceptance test at position s of every request
+// can be made once stage s is in, and the residual pass of a request rejected there overlaps the
 // later stages.  Residual items come in the order of the residual queue (requests in the order
 // their results were published), then position slot, then residual chunk: residual item
 // w < P.total_r is item w mod R of queue entry w / R.  The stats items are handed out by the
@@ -321,14 +326,17 @@ __device__ __forceinline__ void decode_stats(const Params& P, unsigned w, int& b
     row = (int)fdiv((unsigned)off, P.fd_nchunk);
     ch = off - row * P.nchunk;
   } else {
-    const unsigned st = fdiv(w, P.fd_S1);
-    if (st >= (unsigned)P.K) {  // the bonus stage: one row per request
-      const unsigned off = w - (unsigned)P.K * P.fd_S1.d;
+    const unsigned nb = (unsigned)P.B * P.fd_nchunk.d;          // the bonus stage's items
+    const unsigned w0 = P.bonus_first ? nb : 0u;                  // the positions' first item
+    const unsigned wb = P.bonus_first ? 0u : (unsigned)P.K * P.fd_S1.d;  // the bonus stage's first
+    if (w - wb < nb) {  // the bonus stage: one row per request
+      const unsigned off = w - wb;
       b = (int)fdiv(off, P.fd_nchunk);
       ch = (int)(off - (unsigned)b * P.fd_nchunk.d);
       row = P.K;
     } else {
-      const unsigned off = w - st * P.fd_S1.d;
+      const unsigned st = fdiv(w - w0, P.fd_S1);
+      const unsigned off = w - w0 - st * P.fd_S1.d;
       b = (int)fdiv(off, P.fd_pair);
       const int r2off = (int)(off - (unsigned)b * P.fd_pair.d);
       const int r2 = r2off >= P.nchunk ? 1 : 0;  // 0: target row, 1: draft row
@@ -1372,27 +1380,63 @@ __device__ __forceinline__ bool wait_count(const Params& P, Shared& sm, const un
 // (P.rstat, and sm.srs[0] / sm.srs[1]): softmax statistics (soft, c = log2(e) / T) or argmax.  The
 // group waits (bounded) until every chunk statistic carries the call's tag (the count only says
 // when to look).  G threads share a row, as in combine_rows.
+constexpr int kStagePer = 4;  // chunk statistics a thread keeps in registers while combining a stage
 __device__ inline void combine_stage(const Params& P, Shared& sm, int b, int r0, int r1, bool soft, float c) {
   const int nr = r1 >= 0 ? 2 : 1;
   const ChunkStat* g0 = P.cstat + ((size_t)b * P.rows + r0) * P.nchunk;
   const ChunkStat* g1 = r1 >= 0 ? P.cstat + ((size_t)b * P.rows + r1) * P.nchunk : g0;
-  await_tagged(P, sm, g0, P.nchunk);
-  if (r1 >= 0) await_tagged(P, sm, g1, P.nchunk);
   const int ft = fin_thread(), nch = P.nchunk;
   int G = 1;
   while (G < 32 && G < nch && nr * 2 * G <= kFinThreads) G <<= 1;
   const int g = ft & (G - 1), i = ft / G;
   const bool act = i < nr;
   const ChunkStat* gp = i == 1 ? g1 : g0;
+  // Stages of two rows (a target and a draft row): every chunk statistic is read once (one round
+  // trip), the copies in registers are checked for the call's tag and read again (bounded) until
+  // every tag matches.  Single rows, and rows of more than kStagePer * G chunks, take the passes
+  // over global memory below instead (measured faster for the single rows of the n-gram chain).
+  const bool held = nr == 2 && nch <= kStagePer * G;
+  ChunkStat hq[kStagePer];
+  if (held) {
+    const long long t0 = clock64();
+    for (;;) {
+      bool good = true;
+#pragma unroll
+      for (int k = 0; k < kStagePer; ++k) {
+        const int ch = g + k * G;
+        if (act && ch < nch) {
+          hq[k] = ld_chunkstat(gp + ch);
+          good = good && cs_ok(hq[k], sm.tag);
+        }
+      }
+      if (fin_all(good)) break;
+      if (fin_timed_out(t0)) {
+        if (ft == 0) raise_abort(P, sm);
+        break;
+      }
+      __nanosleep(64);
+    }
+  } else {
+    await_tagged(P, sm, g0, P.nchunk);
+    if (r1 >= 0) await_tagged(P, sm, g1, P.nchunk);
+  }
+  // f(q) over this thread's chunks of its row (from the registers when held)
+  auto each = [&](auto&& f) {
+    if (!act) return;
+    if (held) {
+#pragma unroll
+      for (int k = 0; k < kStagePer; ++k)
+        if (g + k * G < nch) f(hq[k]);
+    } else {
+      for (int ch = g; ch < nch; ch += G) f(ld_chunkstat(gp + ch));
+    }
+  };
   float m = -INFINITY;
   int fl = 0;
-  if (act) {
-    for (int ch = g; ch < nch; ch += G) {
-      const ChunkStat q = ld_chunkstat(gp + ch);
-      m = fmax_nan(m, q.a);
-      if (isnan(q.a) || (soft && q.a == INFINITY)) fl |= SPEC_ERRF_NONFINITE;
-    }
-  }
+  each([&](const ChunkStat& q) {
+    m = fmax_nan(m, q.a);
+    if (isnan(q.a) || (soft && q.a == INFINITY)) fl |= SPEC_ERRF_NONFINITE;
+  });
   for (int o = G >> 1; o > 0; o >>= 1) {
     m = fmax_nan(m, __shfl_xor_sync(kFull, m, o));
     fl |= __shfl_xor_sync(kFull, fl, o);
@@ -1403,12 +1447,7 @@ __device__ inline void combine_stage(const Params& P, Shared& sm, int b, int r0,
     const float mc = __fmul_rn(m, c);
     const bool finite_m = !isnan(m) && m != INFINITY && m != -INFINITY;
     float z = 0.f;
-    if (act && !fl && finite_m) {
-      for (int ch = g; ch < nch; ch += G) {
-        const ChunkStat q = ld_chunkstat(gp + ch);
-        z = __fadd_rn(z, chunk_weight(q.a, q.s, c, mc));
-      }
-    }
+    if (!fl && finite_m) each([&](const ChunkStat& q) { z = __fadd_rn(z, chunk_weight(q.a, q.s, c, mc)); });
     for (int o = G >> 1; o > 0; o >>= 1) z = __fadd_rn(z, __shfl_xor_sync(kFull, z, o));
     const double Z = (!fl && finite_m) ? (double)z : 0.0;
     rs.Z = Z;
@@ -1417,12 +1456,9 @@ __device__ inline void combine_stage(const Params& P, Shared& sm, int b, int r0,
     rs.err = (fl || !finite_m || !(Z > 0.0) || isinf(Z)) ? (fl | SPEC_ERRF_NONFINITE) : 0;
   } else {
     int idx = INT_MAX;
-    if (act) {
-      for (int ch = g; ch < nch; ch += G) {
-        const ChunkStat q = ld_chunkstat(gp + ch);
-        if (q.a == m) idx = min(idx, __float_as_int(q.s));
-      }
-    }
+    each([&](const ChunkStat& q) {
+      if (q.a == m) idx = min(idx, __float_as_int(q.s));
+    });
     for (int o = G >> 1; o > 0; o >>= 1) idx = min(idx, __shfl_xor_sync(kFull, idx, o));
     rs.Z = 0.0;
     rs.mc = m;
@@ -1602,6 +1638,35 @@ __device__ inline int stage_errors(const Params& P, Shared& sm, int b, int r0, i
   return e;
 }
 
+// The bonus token of request j from its bonus row's statistics (q.rt): the row's argmax for a
+// greedy request, else the draw from p_K (section I.1's bonus read as R6).  With the bonus stage
+// streamed first it is made then, ahead of the acceptance tests, so that a request that accepts
+// every draft has its token at once.  Per-position outputs of the draft-model and n-gram chains
+// make their draws at the end instead.
+template <int MODE, typename T, bool PT>
+__device__ void bonus_token(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph,
+                            int j) {
+  constexpr bool kSoftmax = (MODE == kChain || MODE == kNgram);
+  const int ft = fin_thread();
+  FinReq& q = sm.fr[j];
+  const bool soft = PT ? !q.greedy : kSoftmax;
+  const bool late = P.diag && (MODE == kNgram || (MODE == kChain && P.npos > 0));
+  if (!soft) {
+    if (ft == 0) {
+      q.btok = q.rt.amax;
+      q.bmass = 1.f;
+    }
+  } else if (!q.err && !late) {
+    float mass;
+    const int tok = row_draw<T>(P, sm, fbuf, fph, ssph, q.b, P.K, kFullP, -1, q.rt, q.u, PT ? q.c : P.c, &mass);
+    if (ft == 0) {
+      q.btok = tok;
+      q.bmass = mass;
+    }
+  }
+  fin_sync();
+}
+
 // The result of request j is decided at its position n (x: the draft token there).
 template <int MODE, typename T, bool PT>
 __device__ void decide(const Params& P, Shared& sm, unsigned char* fbuf, uint32_t& fph, uint32_t& ssph, int j,
@@ -1639,11 +1704,20 @@ __device__ void decide(const Params& P, Shared& sm, unsigned char* fbuf, uint32_
   }
   if (!soft || err) {  // greedy: the argmax of row n; a failed request draws nothing
     if (ft == 0) {
-      q.tok = err ? -1 : q.rt.amax;
+      q.tok = err ? -1 : (n == K ? q.btok : q.rt.amax);
       q.mass = err ? 0.f : 1.f;
       q.drawn = 1;
     }
-  } else if ((MODE == kNgram || n == K) && !late) {  // the n-gram residual or the bonus draw, now
+  } else if (n == K && !late) {  // the bonus token, made from the first stage
+    if (ft == 0) {
+      q.tok = q.btok;
+      q.mass = q.bmass;
+      q.drawn = 1;
+      // (per-position outputs of a chain without residual passes: its one position, the bonus row)
+      if (P.cand_tokens) P.cand_tokens[(size_t)b * (K + 1) + n] = q.btok;
+      if (P.pos_mass) P.pos_mass[(size_t)b * (K + 1) + n] = q.bmass;
+    }
+  } else if (MODE == kNgram && !late) {  // the n-gram residual, now
     float mass;
     const int tok = row_draw<T>(P, sm, fbuf, fph, ssph, b, n, (MODE == kNgram && n < K) ? kExcl : kFullP,
                                 n < K ? x : -1, q.rt, q.u, c, &mass);
@@ -1806,9 +1880,22 @@ __device__ bool finish_stage(const Params& P, Shared& sm, unsigned char* fbuf, u
     }
     q.err |= e;
     int decided = 0;
-    if (q.n < 0) {
+    if (s == K) {  // the bonus row: its statistics are kept for the bonus draw
+      if (q.n < 0) {
+        q.rt = t;
+        q.rd = d;
+        if (!P.bonus_first || K == 0) {  // (streamed last: every draft was accepted)
+          q.n = K;
+          decided = 1;
+        }
+      }
+    } else if (q.n < 0) {
       if (acc) {
         P.out_tokens[o_s] = x;
+        if (P.bonus_first && s == K - 1) {  // every draft accepted: the bonus token, made already
+          q.n = K;
+          decided = 1;
+        }
       } else {
         q.n = s;
         q.rt = t;
@@ -1822,6 +1909,7 @@ __device__ bool finish_stage(const Params& P, Shared& sm, unsigned char* fbuf, u
   fin_sync();
   const int decided = sm.gs.out[0], xs = sm.gs.out[1];
   fin_sync();
+  if (s == K && (P.bonus_first || decided)) bonus_token<MODE, T, PT>(P, sm, fbuf, fph, ssph, j);
   if (decided) decide<MODE, T, PT>(P, sm, fbuf, fph, ssph, j, xs);
   return true;
 }
@@ -1930,6 +2018,8 @@ __device__ void fin_loop_chain(const Params& P, Shared& sm, unsigned char* fbuf)
       q.resid = 0;
       q.drawn = 0;
       q.written = 0;
+      q.btok = -1;
+      q.bmass = 0.f;
       q.mass = 0.f;
       const ReqTemp rt = req_temp<MODE, PT>(P, q.b);
       q.c = rt.c;
@@ -1938,9 +2028,11 @@ __device__ void fin_loop_chain(const Params& P, Shared& sm, unsigned char* fbuf)
       q.u = kSoftmax ? __ldg(P.u + q.b) : 0.f;
     }
     fin_sync();
-    for (int s = 0; s <= P.K; ++s)
+    for (int it = 0; it <= P.K; ++it) {  // the stages in stream order
+      const int s = P.bonus_first ? (it == 0 ? P.K : it - 1) : it;
       for (int j = 0; j < own; ++j)
         if (!finish_stage<MODE, T, PT>(P, sm, fbuf, fph, ssph, j, s, own)) return;
+    }
     for (int j = 0; j < own; ++j)
       if (!finalize_request<MODE, T, PT>(P, sm, fbuf, fph, ssph, j)) return;
   }
