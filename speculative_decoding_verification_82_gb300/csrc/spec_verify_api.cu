@@ -258,6 +258,9 @@ spec_status_t verify_chain_common(bool ngram, const void* target, const void* dr
   // then ends on the last position, which few requests reach); measured slower for calls without
   // residual passes and for per-request temperatures
   P.bonus_first = (P.npos > 0 && !temps) ? 1 : 0;
+  // larger stats batches when the call runs residual passes: a producer then looks for residual
+  // items less often, and the stats stream, which every later position waits for, runs ahead
+  P.claim = P.npos > 0 ? 2 * specv::kClaim : specv::kClaim;
   P.c = (greedy || temps) ? 0.f : (float)(1.4426950408889634 / (double)T);  // log2(e) / T
   P.temps = temps;
   P.draft_tokens = x;
@@ -346,6 +349,7 @@ spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t dt
   if (sms <= 0) return SPEC_ERR_CUDA;
   P.total = (unsigned)((long long)B * rows * P.nchunk);
   P.npos = 0;
+  P.claim = specv::kClaim;
   set_divisors(P, B, rows, 1);
   P.target = target_logits;
   P.B = B;

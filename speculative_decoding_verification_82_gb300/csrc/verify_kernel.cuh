@@ -98,6 +98,7 @@ struct Params {
   int npos;          // residual positions per request (K with per-position outputs, else 1); 0: none
   int diag;          // 1: draw at every position (per-position outputs requested)
   int bonus_first;   // chain modes: the bonus rows stream first (else last)
+  int claim;         // stats items a producer claims per atomic (fewer near the end)
   float c;           // log2(e) / T (calls with one temperature)
   const float* temps;  // [B] per-request temperatures (calls with PT = true), else nullptr
   unsigned total;    // stats items (A per request)
@@ -439,17 +440,18 @@ template <int MODE, typename T, bool PT>
 __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages, int grp) {
   const int lane = threadIdx.x & 31;
   // stats claims: batches of consecutive items, the next batch claimed one batch ahead.  Each
-  // producer's first batch is fixed (kClaim items from kClaim * (blockIdx.x * kGroups + grp)), so
+  // producer's first batch is fixed (P.claim items from P.claim * (blockIdx.x * kGroups + grp)), so
   // that its first copies start without waiting for an atomic; the counter hands out the rest, in
-  // batches of kClaim until fewer than two batches per producer remain, then smaller ones, so that
+  // batches of P.claim until fewer than two batches per producer remain, then smaller ones, so that
   // the producers run out of items at about the same time.
-  const unsigned fixed = (unsigned)kClaim * gridDim.x * (unsigned)kGroups;
+  const unsigned claim = (unsigned)max(1, P.claim);
+  const unsigned fixed = claim * gridDim.x * (unsigned)kGroups;
   const unsigned nprod = gridDim.x * (unsigned)kGroups;
-  unsigned cur = 0, nxt = 0, ccnt = kClaim, ncnt = kClaim;
+  unsigned cur = 0, nxt = 0, ccnt = claim, ncnt = claim;
   int pos = 0;
   if (lane == 0) {
-    cur = (unsigned)kClaim * (blockIdx.x * (unsigned)kGroups + (unsigned)grp);
-    nxt = fixed + atomicAdd(P.work, (unsigned)kClaim);
+    cur = claim * (blockIdx.x * (unsigned)kGroups + (unsigned)grp);
+    nxt = fixed + atomicAdd(P.work, claim);
   }
   // residual claims (lane 0): the held items rfirst .. rfirst + rcnt - 1; qreq, the request of queue
   // entry qe once that entry is published; q0..q3, qreq's result words as last read
@@ -491,7 +493,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
           // batches shrink as the cursor nears the end (one item once the stats items are out), so
           // that the last requests' residual items spread over as many producers as possible
           const unsigned rrem = P.total_r > rseen ? P.total_r - rseen : 0u;
-          const unsigned rk = sdone ? 1u : max(1u, min((unsigned)kClaim, rrem / (2u * nprod)));
+          const unsigned rk = sdone ? 1u : max(1u, min((unsigned)kClaim, rrem / (2u * nprod)));  // (kClaim: residual batches)
           const unsigned c = atomicAdd(P.rc, rk);
           rseen = c + rk;
           if (c >= P.total_r) {
@@ -541,7 +543,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
             ccnt = ncnt;
             if (cur < P.total) {
               const unsigned front = nxt + ncnt, rem = P.total > front ? P.total - front : 0u;
-              ncnt = max(1u, min((unsigned)kClaim, rem / (2u * nprod)));
+              ncnt = max(1u, min(claim, rem / (2u * nprod)));
               nxt = fixed + atomicAdd(P.work, ncnt);
             }
           }
