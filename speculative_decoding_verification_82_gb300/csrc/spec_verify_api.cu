@@ -55,10 +55,9 @@ Chunking plan_chunks(int V, int S) {
 //   cstat   [B][rows][nchunk]    ChunkStat          (256-byte aligned regions from here on)
 //   sstat   [B][rows][nchunk][G] ChunkStat          sub-chunk partials (G consumer warps a group)
 //   rstat   [B][rows]            RowStat
-//   wsum    [B][rows][nchunk_r]  TagSum (float and tag)
-//   wsub    [B][rows][nchunk_r][G] TagSum
+//   wsub    [B][rows][nchunk_r][G] TagSum (float and tag): residual sums per sub-range
 struct Layout {
-  size_t work, tick_a, tick_b, req, rq, hdr_end, cstat, sstat, rstat, wsum, wsub, total;
+  size_t work, tick_a, tick_b, req, rq, hdr_end, cstat, sstat, rstat, wsub, total;
 };
 
 Layout layout(int B, int rows, const Chunking& ck) {
@@ -84,8 +83,6 @@ Layout layout(int B, int rows, const Chunking& ck) {
   off = align_up(off + b * r * (size_t)ck.nchunk * G * sizeof(ChunkStat), 256);
   L.rstat = off;
   off = align_up(off + b * r * sizeof(RowStat), 256);
-  L.wsum = off;
-  off = align_up(off + b * r * (size_t)ck.nchunk_r * sizeof(specv::TagSum), 256);
   L.wsub = off;
   off = align_up(off + b * r * (size_t)ck.nchunk_r * G * sizeof(specv::TagSum), 256);
   L.total = off;
@@ -125,7 +122,6 @@ spec_status_t attach_workspace(Params& P, void* ws, size_t bytes, int B, int row
   P.cstat = reinterpret_cast<ChunkStat*>(w + L.cstat);
   P.sstat = reinterpret_cast<ChunkStat*>(w + L.sstat);
   P.rstat = reinterpret_cast<RowStat*>(w + L.rstat);
-  P.wsum = reinterpret_cast<specv::TagSum*>(w + L.wsum);
   P.wsub = reinterpret_cast<specv::TagSum*>(w + L.wsub);
   P.ws_base = ws;
   P.ws_bytes = L.total;
@@ -258,9 +254,12 @@ spec_status_t verify_chain_common(bool ngram, const void* target, const void* dr
   // then ends on the last position, which few requests reach); measured slower for calls without
   // residual passes and for per-request temperatures
   P.bonus_first = (P.npos > 0 && !temps) ? 1 : 0;
-  // larger stats batches when the call runs residual passes: a producer then looks for residual
-  // items less often, and the stats stream, which every later position waits for, runs ahead
+  // Calls with residual passes: larger stats batches, so that a producer looks for residual items
+  // less often and the stats stream, which every later position waits for, runs ahead; and near
+  // the end of the stats stream the stats items go first (measured: 72.3 against 77.6 us with
+  // per-request temperatures, no change at one temperature)
   P.claim = P.npos > 0 ? 2 * specv::kClaim : specv::kClaim;
+  P.tail_first = P.npos > 0 ? 1 : 0;
   P.c = (greedy || temps) ? 0.f : (float)(1.4426950408889634 / (double)T);  // log2(e) / T
   P.temps = temps;
   P.draft_tokens = x;

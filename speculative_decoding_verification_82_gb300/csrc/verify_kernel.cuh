@@ -99,6 +99,7 @@ struct Params {
   int diag;          // 1: draw at every position (per-position outputs requested)
   int bonus_first;   // chain modes: the bonus rows stream first (else last)
   int claim;         // stats items a producer claims per atomic (fewer near the end)
+  int tail_first;    // 1: near the end of the stats stream, stats items go before residual items
   float c;           // log2(e) / T (calls with one temperature)
   const float* temps;  // [B] per-request temperatures (calls with PT = true), else nullptr
   unsigned total;    // stats items (A per request)
@@ -130,7 +131,6 @@ struct Params {
   ChunkStat* sstat;     // [B][rows][nchunk][kGroupWarps] sub-chunk partials (softmax modes)
   RowStat* rstat;       // [B][rows]
   ReqState* req;        // [B]
-  TagSum* wsum;         // [B][npos][nchunk_r] residual weight per residual item
   TagSum* wsub;         // [B][npos][nchunk_r][kGroupWarps] residual weight per sub-range
   unsigned* epoch;      // the tag of the workspace's last call (0 after the workspace is cleared)
   // host only: the workspace, its bytes in this call's layout, and the shape of that layout
@@ -457,7 +457,8 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
   // entry qe once that entry is published; q0..q3, qreq's result words as last read
   unsigned rfirst = 0, qe = 0xffffffffu, rseen = 0;  // rseen: the cursor as this producer last saw it
   int rcnt = 0, qreq = -1;
-  bool rdone = P.npos == 0, qok = false;  // qok: request qreq's result is complete
+  // qok: request qreq's result is complete (only draft-model chains have residual items)
+  bool rdone = MODE != kChain || P.npos == 0, qok = false;
   unsigned long long q0 = 0, q1 = 0, q2 = 0, q3 = 0;
   int it = grp;
   // residual parameters of the last request seen (consecutive residual items share them)
@@ -530,7 +531,12 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
             }
           }
         }
-        if (rready) {
+        // ready residual items go ahead of stats items, except, when P.tail_first is set, near the
+        // end of the stats stream (less than one item per producer left to claim), where the stats
+        // items go first so that the producers run out of them together
+        const bool hold = MODE == kChain && P.tail_first && !sdone &&
+                          (P.total > nxt + ncnt ? P.total - nxt - ncnt : 0u) < nprod;
+        if (rready && !hold) {
           kind = kItemResid;
           w = rfirst++;
           --rcnt;
@@ -579,11 +585,12 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
         constexpr int VE = Elem<T>::kPerVec;
         m.e_base = v0 * VE - g.phase;
         // Rows stream once: evict-first keeps them from crowding out other lines.  (Keeping the
-        // pairs of a draft-model chain in L2 for a later residual re-read measured slower: the
-        // re-read of a stage comes one stage later, after more bytes than L2 holds.)
+        // first position's pairs of a draft-model chain in L2 with evict-last, for the residual
+        // re-read, cut DRAM reads by 35 MB on the headline chain but measured slower: the re-read
+        // passes through the SMs' bulk copies either way.)
         const int hint = P.npos > 0 ? kL2First : kL2Normal;
         warp_stage<T>(buf, g, P.V, v0, v1, &sm.full[s], lane, hint);
-      } else if (kind == kItemResid) {
+      } else if (MODE == kChain && kind == kItemResid) {
         const int e = (int)fdiv(w, P.fd_R);  // the queue entry (published: the item was taken only then)
         const int off = (int)(w - (unsigned)e * P.fd_R.d);
         m.b = __shfl_sync(kFull, qreq, 0);
@@ -793,13 +800,9 @@ __device__ __forceinline__ void publish_chunk(const Params& P, Shared& sm, const
     }
     if (lane == 0) *reinterpret_cast<uint4*>(P.cstat + ci) = q;
     pm.tick = stats_tick<MODE>(P, m.b, m.row);
-  } else if (m.kind == kItemResid) {
-    float sum = mine ? pw.x : 0.f;
-#pragma unroll
-    for (int o = 1; o < kGroupWarps; o <<= 1) sum = __fadd_rn(sum, __shfl_xor_sync(kFull, sum, o));
+  } else if (MODE == kChain && m.kind == kItemResid) {
     const size_t bk = (size_t)m.b * P.npos + m.kk;
     const size_t ri = bk * P.nchunk_r + m.ch;
-    if (lane == 0) *reinterpret_cast<uint2*>(P.wsum + ri) = make_uint2(__float_as_uint(sum), sm.tag);
     if (mine) *reinterpret_cast<uint2*>(P.wsub + ri * kGroupWarps + lane) = make_uint2(__float_as_uint(pw.x), sm.tag);
     pm.tick = P.tick_b + bk;
   }
@@ -830,7 +833,7 @@ __device__ void consumer_loop(const Params& P, Shared& sm, const unsigned char* 
         part = m.greedy ? consume_stats<kGreedy, T>(buf, m, 0.f, gw) : consume_stats<MODE, T>(buf, m, m.c, gw);
       else
         part = consume_stats<MODE, T>(buf, m, P.c, gw);
-    } else if (m.kind == kItemResid) {
+    } else if (MODE == kChain && m.kind == kItemResid) {
       part = consume_resid<T>(buf, m, PT ? m.c : P.c, gw);
     }
     __syncwarp();
@@ -1482,24 +1485,32 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
                               int b, int kk, int k, float c, float u, const RowStat& ts, const RowStat& ds,
                               int* tok_out, float* mass_out) {
   constexpr int VE = Elem<T>::kPerVec;
-  const int ft = fin_thread(), lane = ft & 31;
+  const int ft = fin_thread(), lane = ft & 31, fw = ft >> 5;
   const size_t bk = (size_t)b * P.npos + kk;
-  // the residual sums and sub-range sums of the position, once all carry the call's tag, copied
-  // into shared memory when they fit (the sub-chunk statistics' buffer is free here)
-  const TagSum* ws = P.wsum + bk * P.nchunk_r;
+  // The position's sub-range sums in index order (kGroupWarps per residual item).  Thread ft takes
+  // nper consecutive ones, reading them until every one carries the call's tag, and keeps them in
+  // shared memory when they all fit (the sub-chunk statistics' buffer is free here).
   const TagSum* wsb0 = P.wsub + bk * P.nchunk_r * kGroupWarps;
-  const int nsum = P.nchunk_r * (1 + kGroupWarps);
+  const int nsub = P.nchunk_r * kGroupWarps;
+  const int nper = (nsub + kFinThreads - 1) / kFinThreads;
+  const int j0 = ft * nper;
   float* cache = reinterpret_cast<float*>(sm.fin_ss);
-  const bool cached = nsum <= kFinSs * 4;
+  const bool cached = nsub <= kFinSs * 4;
   bool sums_ok = true;
+  float s = 0.f;
   {
     const long long t0 = clock64();
     for (;;) {
       bool good = true;
-      for (int i = ft; i < nsum; i += kFinThreads) {
-        const TagSum e = i < P.nchunk_r ? ld_tagsum(ws + i) : ld_tagsum(wsb0 + (i - P.nchunk_r));
-        good = good && e.t == sm.tag;
-        if (cached) cache[i] = e.v;
+      s = 0.f;
+      for (int i = 0; i < nper; ++i) {
+        const int j = j0 + i;
+        if (j < nsub) {
+          const TagSum e = ld_tagsum(wsb0 + j);
+          good = good && e.t == sm.tag;
+          if (cached) cache[j] = e.v;
+          s = __fadd_rn(s, e.v);
+        }
       }
       if (fin_all(good)) break;
       if (fin_timed_out(t0)) {
@@ -1510,47 +1521,86 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
       __nanosleep(128);
     }
   }
-  // the leader picks the residual chunk and sub-range and stages the crossing pair (no draw
-  // after a timeout)
-  if (ft < 32) {
-    auto weight = [&](int ch) { return cached ? cache[ch] : ld_tagsum(ws + ch).v; };
-    const float S = sums_ok ? total_weight(P.nchunk_r, weight) : 0.f;
-    int state = sums_ok ? 0 : 2;  // 0: no residual mass, 1: the crossing pair is being staged, 2: none
-    int cstar = -1, sstar = -1;
-    float t = 0.f;
-    if (sums_ok && S > 0.f) {
-      state = 2;
-      const float tgt = __fmul_rn(u, S);
-      float bstar, sbase;
-      select_part(P.nchunk_r, tgt, weight, cstar, bstar);
-      if (cstar >= 0) {
-        const TagSum* wsb = wsb0 + (size_t)cstar * kGroupWarps;
-        const float* csb = cache + P.nchunk_r + cstar * kGroupWarps;
-        select_part(kGroupWarps, __fsub_rn(tgt, bstar),
-                    [&](int i) { return cached ? csb[i] : ld_tagsum(wsb + i).v; }, sstar, sbase);
-        if (sstar >= 0) {
-          t = __fsub_rn(__fsub_rn(tgt, bstar), sbase);
-          const ResGeo<T> q = res_geo<T>(P, b, k, cstar * kResVec + sstar * kResSub, kResSub);
-          if (lane == 0) fence_proxy_async_shared();  // the group's earlier reads of fbuf come first
-          warp_stage<T>(fbuf, q.gt, P.V, q.vt0, q.vt1, &sm.fin_bar, lane);
-          warp_stage<T>(fbuf + (size_t)kFinDraftSlot * 16, q.gd, P.V, q.vd0, q.vd1, &sm.fin_bar, lane);
-          __syncwarp();
-          if (lane == 0) mbar_arrive(&sm.fin_bar);
-          state = 1;
+  // One scan of the thread sums over the group (each warp, then the warps in order) gives the
+  // total S and the thread whose running total first exceeds u S (else the last one with
+  // positive weight); that thread's warp picks the sub-range the same way among the thread's
+  // own, and stages the crossing pair.  No draw after a timeout.
+  const float incl = warp_incl_scan(s, lane);
+  float excl = __shfl_up_sync(kFull, incl, 1);
+  if (lane == 0) excl = 0.f;
+  if (lane == 31) sm.gs.wsum[fw] = incl;
+  fin_sync();
+  float base = 0.f, S = 0.f;
+#pragma unroll
+  for (int w = 0; w < kFinWarps; ++w) {
+    const float ws = sm.gs.wsum[w];
+    if (w < fw) base = __fadd_rn(base, ws);
+    S = __fadd_rn(S, ws);
+  }
+  const bool any = sums_ok && S > 0.f;
+  const float tgt = __fmul_rn(u, S);
+  const unsigned hmask = __ballot_sync(kFull, any && s > 0.f && __fadd_rn(base, incl) > tgt);
+  const unsigned pmask = __ballot_sync(kFull, any && s > 0.f);
+  if (lane == 0) {
+    sm.gs.hit[fw] = hmask;
+    sm.gs.pos[fw] = pmask;
+  }
+  fin_sync();
+  int L = -1;
+#pragma unroll
+  for (int w = 0; w < kFinWarps; ++w)
+    if (L < 0 && sm.gs.hit[w]) L = w * 32 + __ffs(sm.gs.hit[w]) - 1;
+#pragma unroll
+  for (int w = kFinWarps - 1; w >= 0; --w)
+    if (L < 0 && sm.gs.pos[w]) L = w * 32 + 31 - __clz(sm.gs.pos[w]);
+  const int state = !sums_ok ? 2 : (L < 0 ? 0 : 1);  // 0: no residual mass, 1: the pair is staged
+  if (state == 1 && fw == (L >> 5)) {
+    int jstar = -1;
+    float tj = 0.f;
+    if (lane == (L & 31)) {
+      float acc = __fadd_rn(base, excl);
+      int pj = -1, lj = -1;
+      float pacc = 0.f, lacc = 0.f;
+      for (int i = 0; i < nper; ++i) {
+        const int j = j0 + i;
+        if (j >= nsub) break;
+        const float w = cached ? cache[j] : ld_tagsum(wsb0 + j).v;
+        if (w > 0.f) {
+          if (pj < 0 && __fadd_rn(acc, w) > tgt) {
+            pj = j;
+            pacc = acc;
+          }
+          lj = j;
+          lacc = acc;
         }
+        acc = __fadd_rn(acc, w);
       }
+      if (pj < 0) {
+        pj = lj;
+        pacc = lacc;
+      }
+      jstar = pj;
+      tj = __fsub_rn(tgt, pacc);
     }
+    jstar = __shfl_sync(kFull, jstar, L & 31);
+    tj = __shfl_sync(kFull, tj, L & 31);
+    const int cs = jstar / kGroupWarps, ss = jstar - cs * kGroupWarps;
+    const ResGeo<T> g = res_geo<T>(P, b, k, cs * kResVec + ss * kResSub, kResSub);
+    if (lane == 0) fence_proxy_async_shared();  // the group's earlier reads of fbuf come first
+    warp_stage<T>(fbuf, g.gt, P.V, g.vt0, g.vt1, &sm.fin_bar, lane);
+    warp_stage<T>(fbuf + (size_t)kFinDraftSlot * 16, g.gd, P.V, g.vd0, g.vd1, &sm.fin_bar, lane);
+    __syncwarp();
     if (lane == 0) {
-      sm.gs.out[0] = state;
-      sm.gs.out[1] = cstar;
-      sm.gs.out[2] = sstar;
-      sm.gs.fout[0] = t;
-      sm.gs.fout[1] = (float)((double)S / ts.Z);
+      mbar_arrive(&sm.fin_bar);
+      sm.gs.out[1] = cs;
+      sm.gs.out[2] = ss;
+      sm.gs.fout[0] = tj;
     }
   }
   fin_sync();
-  const int state = sm.gs.out[0], cstar = sm.gs.out[1], sstar = sm.gs.out[2];
-  const float t = sm.gs.fout[0], rmass = sm.gs.fout[1];
+  const int cstar = sm.gs.out[1], sstar = sm.gs.out[2];
+  const float t = sm.gs.fout[0];
+  const float rmass = sums_ok ? __fdiv_rn(S, (float)ts.Z) : 0.f;  // S in units of 1 / Z_t
   fin_sync();
   int tok = -1;
   if (state == 1) {

@@ -47,7 +47,7 @@ def test_workspace_size(lib):
 
     B, rows, n, nr = 64, 11, 16, 32
     want = (up(up(256 + 2 * B * rows * 4, 16) + B * 32 + B * 8) + up(B * rows * n * 16)
-            + up(B * rows * n * 8 * 16) + up(B * rows * 32) + up(B * rows * nr * 8) + up(B * rows * nr * 8 * 8))
+            + up(B * rows * n * 8 * 16) + up(B * rows * 32) + up(B * rows * nr * 8 * 8))
     assert lib.spec_verify_workspace_bytes(B, rows, 128256, 0) == want
     assert lib.spec_verify_workspace_bytes(-1, 6, 100, 0) == 0
     assert lib.spec_verify_workspace_bytes(4, 0, 100, 0) == 0
