@@ -9,11 +9,13 @@
 // L + 1 slots; every other slot is left alone.
 //
 // One CTA moves one request's rows in a group of consecutive caches (layers' K or V tensors).  It
-// checks the path in two dependent rounds of loads (the length, the path and every slot at once;
-// then the parents and slots of the path's nodes) and builds the move list; the grid is sized to
-// about kCtasPerSm CTAs per SM, so that every CTA is resident from the start and their checks
-// overlap.  A unit of work is one 16-byte column of the moved rows of one cache: the thread loads
-// the column of every moved row, then stores them, in increasing position.  Along an accepted path
+// checks the path in two dependent rounds of loads: first the length, the path and every slot at
+// once, which give the moves' sources and the move list; then the parent links of the path's
+// nodes, loaded together with the first rows to move, so that the check costs no extra round trip
+// (nothing is stored unless it holds).  The grid is sized to about kCtasPerSm CTAs per SM, so that
+// every CTA is resident from the start and their checks overlap.  A unit of work is one 16-byte
+// column of the moved rows of one cache: the thread loads the column of up to kBatch moved rows,
+// then stores them, in increasing position.  Along an accepted path
 // p_j >= j (a node's index exceeds its parent's) and slots are distinct, so no store lands on a
 // row that a later move still reads, and moving in place is safe.  Moves with p_j == j are
 // skipped.  The kernel is a gather bound by HBM bandwidth: each moved row is read once and written
@@ -27,8 +29,8 @@ namespace {
 constexpr int kMaxCaches = SPEC_MAX_KV_CACHES;
 constexpr int kMaxNodes = SPEC_MAX_WALK_NODES;
 constexpr int kThreads = 256;
-constexpr int kBatch = 8;      // moved rows of one column loaded before they are stored
-constexpr int kCtasPerSm = 4;  // grid target: every CTA resident at once
+constexpr int kBatch = 5;      // moved rows of one column loaded before they are stored
+constexpr int kCtasPerSm = 6;  // grid target: every CTA resident at once
 
 struct KvParams {
   unsigned char* caches[kMaxCaches];  // each [num_slots][row_bytes]
@@ -42,7 +44,7 @@ struct KvParams {
   int32_t* err_flags;         // [B] or null
 };
 
-__global__ void __launch_bounds__(kThreads) kv_compact_kernel(const KvParams P) {
+__global__ void __launch_bounds__(kThreads, kCtasPerSm) kv_compact_kernel(const KvParams P) {
   __shared__ int32_t node[kMaxNodes];                 // path[j]
   __shared__ int32_t slot[kMaxNodes];                 // slots[n]
   __shared__ int32_t from[kMaxNodes];                 // slots[path[j]]: the source of position j
@@ -62,17 +64,18 @@ __global__ void __launch_bounds__(kThreads) kv_compact_kernel(const KvParams P) 
   }
   __syncthreads();
   ok = ok && L >= 0 && L < N1 && node[0] == 0;
-  // round 2: each accepted node is a child of the previous one (its slot, known from round 1, is
-  // the move's source)
+  // the sources (every accepted node must be a valid index; its parent link is checked below)
   for (int j = 1 + t; j <= L && j < N1; j += kThreads) {
-    const int n = node[j], prev = node[j - 1];
+    const int n = node[j];
     const bool in = n > 0 && n < N1;
-    ok = ok && in && __ldg(pa + n) == prev;
+    ok = ok && in;
     from[j] = in ? slot[n] : -1;
   }
   ok = __syncthreads_and(ok);
-  if (grp == 0 && t == 0 && P.err_flags) P.err_flags[b] = ok ? 0 : SPEC_ERRF_BAD_TREE;
-  if (!ok) return;
+  if (!ok) {
+    if (grp == 0 && t == 0 && P.err_flags) P.err_flags[b] = SPEC_ERRF_BAD_TREE;
+    return;
+  }
   // the move list in increasing position (a warp ballot keeps the order); moves in place skipped
   if (t < 32) {
     int base = 0;
@@ -91,19 +94,32 @@ __global__ void __launch_bounds__(kThreads) kv_compact_kernel(const KvParams P) 
   }
   __syncthreads();
   const int M = nmove;
-  if (M == 0) return;
   const int c0 = grp * P.group, c1 = min(P.C, c0 + P.group);
   const size_t W = (size_t)P.row_bytes;
   const int nvec = P.row_bytes / 16;
   const int units = (c1 - c0) * nvec;  // (cache, 16-byte column) pairs of this CTA
+  // the first unit's first batch loads while the parent links are checked
+  uint4 tmp[kBatch];
+  if (t < units) {
+    const int cl = t / nvec, v = t - cl * nvec;
+    const unsigned char* base = P.caches[c0 + cl] + (size_t)v * 16;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+      if (k < M) tmp[k] = *reinterpret_cast<const uint4*>(base + (size_t)src[k] * W);
+  }
+  for (int j = 1 + t; j <= L; j += kThreads) ok = ok && __ldg(pa + node[j]) == node[j - 1];
+  ok = __syncthreads_and(ok);
+  if (grp == 0 && t == 0 && P.err_flags) P.err_flags[b] = ok ? 0 : SPEC_ERRF_BAD_TREE;
+  if (!ok || M == 0) return;
   for (int i = t; i < units; i += kThreads) {
     const int cl = i / nvec, v = i - cl * nvec;
     unsigned char* base = P.caches[c0 + cl] + (size_t)v * 16;
     for (int k0 = 0; k0 < M; k0 += kBatch) {
-      uint4 tmp[kBatch];
+      if (i != t || k0 != 0) {
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k)
-        if (k0 + k < M) tmp[k] = *reinterpret_cast<const uint4*>(base + (size_t)src[k0 + k] * W);
+        for (int k = 0; k < kBatch; ++k)
+          if (k0 + k < M) tmp[k] = *reinterpret_cast<const uint4*>(base + (size_t)src[k0 + k] * W);
+      }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k)
         if (k0 + k < M) *reinterpret_cast<uint4*>(base + (size_t)dst[k0 + k] * W) = tmp[k];
