@@ -1477,6 +1477,83 @@ __device__ inline void combine_stage(const Params& P, Shared& sm, int b, int r0,
   fin_sync();
 }
 
+// The crossing inside one sub-range of a residual item: the element of target vectors
+// [vt0, vt0 + kResSub) of the pair at position k where the running residual weight, taken in
+// index order, first exceeds t (else the last element with positive weight; -1 when none has).
+// Thread i of the finishing group reads the elements of vector vt0 + i of both rows straight from
+// global memory (elements outside the row weigh 0) and keeps their weights in registers; one scan
+// over the group finds the crossing thread, which finds the element.  Every thread gets the
+// position relative to the range's first element.
+template <typename T>
+__device__ int resid_crossing(const Params& P, Shared& sm, const ResGeo<T>& q, int b, int k, float t, float c,
+                              float mct, float mcd, float rho) {
+  constexpr int VE = Elem<T>::kPerVec, S = Elem<T>::kSize;
+  static_assert(kResSub == kFinThreads, "one vector of the sub-range per finishing thread");
+  const int ft = fin_thread(), lane = ft & 31, fw = ft >> 5;
+  const char* trow = row_ptr<T>(P, b, k);
+  const char* drow = row_ptr<T>(P, b, P.R + k);
+  float w[VE];
+  float s = 0.f;
+  {
+    uint32_t lt[VE], ld[VE];
+#pragma unroll
+    for (int j = 0; j < VE; ++j) {  // every load first, then the arithmetic
+      const int e = q.e_base + ft * VE + j;
+      const bool in = ft < q.vt1 - q.vt0 && (unsigned)(e - q.e_lo) < (unsigned)(q.e_hi - q.e_lo);
+      lt[j] = in ? Elem<T>::load_raw(trow + (size_t)e * S) : Elem<T>::kNegInf;
+      ld[j] = in ? Elem<T>::load_raw(drow + (size_t)e * S) : Elem<T>::kNegInf;
+    }
+#pragma unroll
+    for (int j = 0; j < VE; ++j) {
+      const int e = q.e_base + ft * VE + j;
+      const bool in = ft < q.vt1 - q.vt0 && (unsigned)(e - q.e_lo) < (unsigned)(q.e_hi - q.e_lo);
+      const float et = ex2(__fmaf_rn(Elem<T>::to_float(lt[j]), c, -mct));
+      const float qd = ex2(__fmaf_rn(Elem<T>::to_float(ld[j]), c, -mcd));
+      w[j] = in ? fmaxf(0.f, __fmaf_rn(-qd, rho, et)) : 0.f;
+      s = __fadd_rn(s, w[j]);
+    }
+  }
+  const float incl = warp_incl_scan(s, lane);
+  float excl = __shfl_up_sync(kFull, incl, 1);
+  if (lane == 0) excl = 0.f;
+  if (lane == 31) sm.gs.wsum[fw] = incl;
+  fin_sync();
+  float base = 0.f;
+  for (int i = 0; i < fw; ++i) base = __fadd_rn(base, sm.gs.wsum[i]);
+  const unsigned hmask = __ballot_sync(kFull, s > 0.f && __fadd_rn(base, incl) > t);
+  const unsigned pmask = __ballot_sync(kFull, s > 0.f);
+  if (lane == 0) {
+    sm.gs.hit[fw] = hmask;
+    sm.gs.pos[fw] = pmask;
+  }
+  fin_sync();
+  int L = -1;
+#pragma unroll
+  for (int i = 0; i < kFinWarps; ++i)
+    if (L < 0 && sm.gs.hit[i]) L = i * 32 + __ffs(sm.gs.hit[i]) - 1;
+#pragma unroll
+  for (int i = kFinWarps - 1; i >= 0; --i)
+    if (L < 0 && sm.gs.pos[i]) L = i * 32 + 31 - __clz(sm.gs.pos[i]);
+  if (L < 0) return -1;  // (uniform: no element with positive weight)
+  if (ft == L) {
+    float acc = __fadd_rn(base, excl);
+    int pj = -1, lj = -1;
+#pragma unroll
+    for (int j = 0; j < VE; ++j) {
+      if (w[j] > 0.f) {
+        if (pj < 0 && __fadd_rn(acc, w[j]) > t) pj = j;
+        lj = j;
+      }
+      acc = __fadd_rn(acc, w[j]);
+    }
+    sm.gs.out[3] = ft * VE + (pj >= 0 ? pj : lj);
+  }
+  fin_sync();
+  const int pos = sm.gs.out[3];
+  fin_sync();  // gs is free again
+  return pos;
+}
+
 // Draft-model chain: the draw from max(0, p_k - q_k) at position k once every residual item of
 // (b, position slot kk) is in (ts, ds: the statistics of target and draft row k).  Every thread
 // gets the token (-1 after a timeout) and the residual mass.
@@ -1523,8 +1600,8 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
   }
   // One scan of the thread sums over the group (each warp, then the warps in order) gives the
   // total S and the thread whose running total first exceeds u S (else the last one with
-  // positive weight); that thread's warp picks the sub-range the same way among the thread's
-  // own, and stages the crossing pair.  No draw after a timeout.
+  // positive weight); that thread picks the sub-range the same way among its own, and the group
+  // searches it (resid_crossing).  No draw after a timeout.
   const float incl = warp_incl_scan(s, lane);
   float excl = __shfl_up_sync(kFull, incl, 1);
   if (lane == 0) excl = 0.f;
@@ -1553,49 +1630,32 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
 #pragma unroll
   for (int w = kFinWarps - 1; w >= 0; --w)
     if (L < 0 && sm.gs.pos[w]) L = w * 32 + 31 - __clz(sm.gs.pos[w]);
-  const int state = !sums_ok ? 2 : (L < 0 ? 0 : 1);  // 0: no residual mass, 1: the pair is staged
-  if (state == 1 && fw == (L >> 5)) {
-    int jstar = -1;
-    float tj = 0.f;
-    if (lane == (L & 31)) {
-      float acc = __fadd_rn(base, excl);
-      int pj = -1, lj = -1;
-      float pacc = 0.f, lacc = 0.f;
-      for (int i = 0; i < nper; ++i) {
-        const int j = j0 + i;
-        if (j >= nsub) break;
-        const float w = cached ? cache[j] : ld_tagsum(wsb0 + j).v;
-        if (w > 0.f) {
-          if (pj < 0 && __fadd_rn(acc, w) > tgt) {
-            pj = j;
-            pacc = acc;
-          }
-          lj = j;
-          lacc = acc;
+  const int state = !sums_ok ? 2 : (L < 0 ? 0 : 1);  // 0: no residual mass, 1: a crossing to find
+  if (state == 1 && ft == L) {  // the sub-range among the thread's own
+    float acc = __fadd_rn(base, excl);
+    int pj = -1, lj = -1;
+    float pacc = 0.f, lacc = 0.f;
+    for (int i = 0; i < nper; ++i) {
+      const int j = j0 + i;
+      if (j >= nsub) break;
+      const float w = cached ? cache[j] : ld_tagsum(wsb0 + j).v;
+      if (w > 0.f) {
+        if (pj < 0 && __fadd_rn(acc, w) > tgt) {
+          pj = j;
+          pacc = acc;
         }
-        acc = __fadd_rn(acc, w);
+        lj = j;
+        lacc = acc;
       }
-      if (pj < 0) {
-        pj = lj;
-        pacc = lacc;
-      }
-      jstar = pj;
-      tj = __fsub_rn(tgt, pacc);
+      acc = __fadd_rn(acc, w);
     }
-    jstar = __shfl_sync(kFull, jstar, L & 31);
-    tj = __shfl_sync(kFull, tj, L & 31);
-    const int cs = jstar / kGroupWarps, ss = jstar - cs * kGroupWarps;
-    const ResGeo<T> g = res_geo<T>(P, b, k, cs * kResVec + ss * kResSub, kResSub);
-    if (lane == 0) fence_proxy_async_shared();  // the group's earlier reads of fbuf come first
-    warp_stage<T>(fbuf, g.gt, P.V, g.vt0, g.vt1, &sm.fin_bar, lane);
-    warp_stage<T>(fbuf + (size_t)kFinDraftSlot * 16, g.gd, P.V, g.vd0, g.vd1, &sm.fin_bar, lane);
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(&sm.fin_bar);
-      sm.gs.out[1] = cs;
-      sm.gs.out[2] = ss;
-      sm.gs.fout[0] = tj;
+    if (pj < 0) {
+      pj = lj;
+      pacc = lacc;
     }
+    sm.gs.out[1] = pj / kGroupWarps;
+    sm.gs.out[2] = pj % kGroupWarps;
+    sm.gs.fout[0] = __fsub_rn(tgt, pacc);
   }
   fin_sync();
   const int cstar = sm.gs.out[1], sstar = sm.gs.out[2];
@@ -1604,15 +1664,10 @@ __device__ void residual_draw(const Params& P, Shared& sm, unsigned char* fbuf, 
   fin_sync();
   int tok = -1;
   if (state == 1) {
-    const bool ok = fin_wait_only(P, sm, &sm.fin_bar, fph);
     const ResGeo<T> q = res_geo<T>(P, b, k, cstar * kResVec + sstar * kResSub, kResSub);
-    const float mct = ts.mc, mcd = ds.mc;
     const float rho = __fdiv_rn((float)ts.Z, (float)ds.Z);
-    auto wf = [&](int v, float (&w)[VE]) {
-      resid_weights<T>(fbuf, kFinDraftSlot, v, q.e_base, q.e_lo, q.e_hi, q.dshift, c, mct, mcd, rho, w);
-    };
-    const int pos = group_crossing<VE>(sm.gs, q.vt1 - q.vt0, t, wf);
-    tok = (ok && pos >= 0) ? q.e_base + pos : -1;
+    const int pos = resid_crossing<T>(P, sm, q, b, k, t, c, ts.mc, ds.mc, rho);
+    tok = pos >= 0 ? q.e_base + pos : -1;
   } else if (state == 0) {  // no residual mass: draw from p
     float unused;
     SsRows none{0, 0};
