@@ -42,6 +42,7 @@ enum LaunchMode : int { kChainPT = 4, kNgramPT = 5 };
 // The high half of a request's first result word: n | kNoResid for a request verified greedily in a
 // per-request-temperature call (no residual pass follows), | err << 16.
 constexpr unsigned kNoResid = 0x8000u;
+constexpr unsigned kExitAbort = 1u << 16;  // added to the exit count by a CTA that gave up (grids < 2^16)
 enum Kind : int { kFullP = 0, kExcl = 1 };
 enum ItemKind : int { kItemStats = 0, kItemResid = 1, kItemSkip = 2, kItemEnd = 3 };
 
@@ -284,7 +285,7 @@ struct Shared {
   float4 part[kSlots][kGroupWarps];  // warp partials
   SlotMeta pmeta[kSlots];
   int pcnt[kSlots];  // warps of the group that have left their partial
-  int abort, last;
+  int abort, last, timed_out;
   float alpha[SPEC_MAX_K];
   ChunkStat fin_cs[kFinCs];
   ChunkStat fin_ss[kFinSs];
@@ -2281,14 +2282,18 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
   // counters zero for the next call (after a timeout the counts too: finishing groups that gave
   // up did not zero theirs).
   if (tid == 0) {
-    __threadfence();
-    sm.last = atomicAdd(P.exit_tick, 1u) == gridDim.x - 1;
+    // count this CTA out, with release and acquire semantics in one atomic; a CTA that gave up
+    // (the only way the timeout flag gets set) adds kExitAbort as well, so that the last one out
+    // learns of a timeout from the count alone
+    const unsigned add = 1u + (aborted(sm) ? kExitAbort : 0u);
+    unsigned old;
+    asm volatile("atom.add.acq_rel.gpu.global.u32 %0, [%1], %2;" : "=r"(old) : "l"(P.exit_tick), "r"(add) : "memory");
+    sm.last = ((old + add) & (kExitAbort - 1u)) == gridDim.x;
+    sm.timed_out = (old + add) >= kExitAbort;
   }
   __syncthreads();
   if (sm.last) {
-    __threadfence();
-    const bool timed_out = ld_volatile(reinterpret_cast<const int*>(P.gerr)) != 0;
-    __syncthreads();  // every thread has read the flag before it is reset
+    const bool timed_out = sm.timed_out;
     if (tid == 0) {
       *P.work = 0u;
       *P.rc = 0u;
@@ -2372,6 +2377,7 @@ cudaError_t launch_mode(const Params& P, const LaunchPlan& L, cudaStream_t strea
   }
   const long long cap = (long long)per_sm * L.sm_count;
   const long long grid = (long long)P.total < cap ? (long long)P.total : cap;
+  if (grid >= (long long)kExitAbort) return cudaErrorInvalidConfiguration;  // (the exit count's range)
   ks<<<(unsigned)grid, kThreads, L.smem, stream>>>(P);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
