@@ -27,6 +27,7 @@ constexpr int kFinWarp = 19;   // first of the finishing group's warps
 constexpr int kFinWarps = 4;
 constexpr int kFinThreads = kFinWarps * 32;
 constexpr int kFinBarrier = 1;  // named barrier of the finishing group (0 is __syncthreads)
+constexpr int kTagBarrier = 2;  // named barrier of every role but the producers, once the tag is set
 constexpr int kThreads = (kFinWarp + kFinWarps) * 32;
 constexpr int kStages = 6;                         // staged-chunk ring depth (a multiple of kGroups)
 constexpr int kSlots = 16;                         // ring of per-chunk results (partials, merged)

@@ -286,6 +286,7 @@ struct Shared {
   SlotMeta pmeta[kSlots];
   int pcnt[kSlots];  // warps of the group that have left their partial
   int abort, last, timed_out;
+  int tag_ready;  // sm.tag is set (the producers start before it is)
   float alpha[SPEC_MAX_K];
   ChunkStat fin_cs[kFinCs];
   ChunkStat fin_ss[kFinSs];
@@ -460,6 +461,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
   int rcnt = 0, qreq = -1;
   // qok: request qreq's result is complete (only draft-model chains have residual items)
   bool rdone = MODE != kChain || P.npos == 0, qok = false;
+  bool tag_known = false;  // the call's tag is set (residual words are compared with it)
   unsigned long long q0 = 0, q1 = 0, q2 = 0, q3 = 0;
   int it = grp;
   // residual parameters of the last request seen (consecutive residual items share them)
@@ -491,7 +493,11 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
       if (lane == 0) {
         const bool sdone = cur + (unsigned)pos >= P.total;
         const bool boundary = pos == 0 || sdone;
-        if (boundary && rcnt == 0 && !rdone) {
+        if (!tag_known && !rdone && ld_volatile(&sm.tag_ready)) {
+          __threadfence_block();  // sm.tag was written before the flag
+          tag_known = true;
+        }
+        if (boundary && rcnt == 0 && !rdone && tag_known) {
           // batches shrink as the cursor nears the end (one item once the stats items are out), so
           // that the last requests' residual items spread over as many producers as possible
           const unsigned rrem = P.total_r > rseen ? P.total_r - rseen : 0u;
@@ -507,7 +513,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
         }
         const unsigned ne = rcnt > 0 ? fdiv(rfirst, P.fd_R) : 0xffffffffu;  // the held items' entry
         bool rready = rcnt > 0 && ne == qe && qok;
-        if (rcnt > 0 && !rready && boundary) {
+        if (rcnt > 0 && !rready && boundary && tag_known) {
           // the entry and words read at the previous batch start (in by now), else read them again:
           // used at the next batch start, or now once the stats items are out
           if (ne == qe && qreq >= 0 && result_complete(P, sm.tag, q0, q1, q2, q3)) {
@@ -2246,10 +2252,6 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ Shared sm;
   const int tid = threadIdx.x, warp = tid >> 5;
-  // this call's tag: one past the workspace's last (its epoch, left by the last CTA of the
-  // previous call), so that calls replayed from a captured graph get fresh tags too; read first,
-  // so that its latency overlaps the barrier setup
-  const unsigned e = tid == 0 ? __ldg(P.epoch) : 0u;
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.full[s], 1);
@@ -2264,19 +2266,32 @@ __global__ void __launch_bounds__(kThreads, 1) verify_kernel(const Params P) {
     mbar_init(&sm.cs_bar, 1);
     mbar_init(&sm.ss_bar, 1);
     sm.abort = 0;
-    sm.tag = (e + 1u) != 0u ? e + 1u : 1u;
+    sm.tag_ready = 0;
     fence_mbar_init();
   }
   __syncthreads();
   unsigned char* fbuf = smem + (size_t)kStages * kStageBytes;
-  if (warp < kConsWarps)
-    consumer_loop<MODE, T, PT>(P, sm, smem);
-  else if (warp < kProducerWarp + kGroups)
+  if (warp >= kProducerWarp && warp < kProducerWarp + kGroups) {
+    // the producers start the stream at once: a stats copy needs no tag
     producer_loop<MODE, T, PT>(P, sm, smem, warp - kProducerWarp);
-  else if (warp == kBookWarp)
-    book_loop<MODE>(P, sm);
-  else
-    fin_loop<MODE, T, PT>(P, sm, fbuf);  // warps kFinWarp .. kFinWarp + kFinWarps - 1
+  } else {
+    // this call's tag: one past the workspace's last (its epoch, left by the last CTA of the
+    // previous call), so that calls replayed from a captured graph get fresh tags too; every
+    // other role waits for it (named barrier kTagBarrier), while the first copies are in flight
+    if (tid == 0) {
+      const unsigned e = __ldg(P.epoch);
+      sm.tag = (e + 1u) != 0u ? e + 1u : 1u;
+      __threadfence_block();
+      *reinterpret_cast<volatile int*>(&sm.tag_ready) = 1;
+    }
+    asm volatile("bar.sync %0, %1;" ::"n"(kTagBarrier), "n"(kThreads - kGroups * 32) : "memory");
+    if (warp < kConsWarps)
+      consumer_loop<MODE, T, PT>(P, sm, smem);
+    else if (warp == kBookWarp)
+      book_loop<MODE>(P, sm);
+    else
+      fin_loop<MODE, T, PT>(P, sm, fbuf);  // warps kFinWarp .. kFinWarp + kFinWarps - 1
+  }
   __syncthreads();
   // The last CTA out reports a timed-out call (never expected) on every request, and leaves the
   // counters zero for the next call (after a timeout the counts too: finishing groups that gave
