@@ -498,10 +498,12 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
           tag_known = true;
         }
         if (boundary && rcnt == 0 && !rdone && tag_known) {
-          // batches shrink as the cursor nears the end (one item once the stats items are out), so
-          // that the last requests' residual items spread over as many producers as possible
+          // batches shrink as the cursor nears the end, so that the last requests' residual items
+          // spread over as many producers as possible; once the stats items are out, batches of
+          // up to two halve the claims and entry reads each item waits for (measured: 68.6 ->
+          // 67.8 us on the headline chain; up to 4: 68.1, up to 8: 69.5)
           const unsigned rrem = P.total_r > rseen ? P.total_r - rseen : 0u;
-          const unsigned rk = sdone ? 1u : max(1u, min((unsigned)kClaim, rrem / (2u * nprod)));  // (kClaim: residual batches)
+          const unsigned rk = max(1u, min(sdone ? 2u : (unsigned)kClaim, rrem / ((sdone ? 1u : 2u) * nprod)));
           const unsigned c = atomicAdd(P.rc, rk);
           rseen = c + rk;
           if (c >= P.total_r) {
