@@ -51,7 +51,7 @@ Chunking plan_chunks(int V, int S) {
 //   tick_a  [B][rows] u32        chunk counts       } first call of a shape clears them)
 //   tick_b  [B][rows] u32        residual counts    }
 //   req     [B]                  ReqState           (16-byte aligned; tagged per call)
-//   rq      [B] u64              residual queue     (tagged per call)
+//   rq      [B][5] u64           residual queue     (result words and request index, tagged per call)
 //   cstat   [B][rows][nchunk]    ChunkStat          (256-byte aligned regions from here on)
 //   sstat   [B][rows][nchunk][G] ChunkStat          sub-chunk partials (G consumer warps a group)
 //   rstat   [B][rows]            RowStat
@@ -73,7 +73,7 @@ Layout layout(int B, int rows, const Chunking& ck) {
   L.req = off;
   off += b * sizeof(ReqState);
   L.rq = off;
-  off += b * 8;
+  off += b * 8 * (size_t)specv::kQWords;
   L.hdr_end = off;
   off = align_up(off, 256);
   const size_t G = specv::kGroupWarps;

@@ -42,6 +42,9 @@ enum LaunchMode : int { kChainPT = 4, kNgramPT = 5 };
 // The high half of a request's first result word: n | kNoResid for a request verified greedily in a
 // per-request-temperature call (no residual pass follows), | err << 16.
 constexpr unsigned kNoResid = 0x8000u;
+// A residual queue entry: the request's four result words (as in ReqState), then its index in the
+// high half of a fifth word; every word tagged with the call's tag in its low half.
+constexpr int kQWords = 5;
 constexpr unsigned kExitAbort = 1u << 16;  // added to the exit count by a CTA that gave up (grids < 2^16)
 enum Kind : int { kFullP = 0, kExcl = 1 };
 enum ItemKind : int { kItemStats = 0, kItemResid = 1, kItemSkip = 2, kItemEnd = 3 };
@@ -147,8 +150,8 @@ struct Params {
   unsigned* rq_tail;         // entries published in the residual queue
   unsigned* tick_a;     // chunks in (zeroed by the finishing group once complete): per request and
                         // position [B][K+1] in the chain modes, per request [B] for trees
-  unsigned long long* rq;  // [B] the residual queue: request ids in the order their results were
-                           // published (each a 64-bit word: id in the high half, the call's tag low)
+  unsigned long long* rq;  // [B][kQWords] the residual queue, in the order the results were
+                           // published: each entry the result words, then the request's index
   unsigned* tick_b;     // [B][npos] residual items in (likewise)
 };
 
@@ -462,7 +465,8 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
   // qok: request qreq's result is complete (only draft-model chains have residual items)
   bool rdone = MODE != kChain || P.npos == 0, qok = false;
   bool tag_known = false;  // the call's tag is set (residual words are compared with it)
-  unsigned long long q0 = 0, q1 = 0, q2 = 0, q3 = 0;
+  unsigned long long q0 = 0, q1 = 0, q2 = 0, q3 = 0, qb = 0;
+  bool qload = false;  // q0..q3 and qb were loaded for entry qe and are not looked at yet
   int it = grp;
   // residual parameters of the last request seen (consecutive residual items share them)
   int rb = -1, rk = 0, rerr = 1;
@@ -516,27 +520,28 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
         const unsigned ne = rcnt > 0 ? fdiv(rfirst, P.fd_R) : 0xffffffffu;  // the held items' entry
         bool rready = rcnt > 0 && ne == qe && qok;
         if (rcnt > 0 && !rready && boundary && tag_known) {
-          // the entry and words read at the previous batch start (in by now), else read them again:
-          // used at the next batch start, or now once the stats items are out
-          if (ne == qe && qreq >= 0 && result_complete(P, sm.tag, q0, q1, q2, q3)) {
-            qok = rready = true;
-          } else {
-            if (ne != qe) {
-              qe = ne;
-              qreq = -1;
-            }
-            if (qreq < 0) {
-              const unsigned long long ev = ld_volatile_u64(P.rq + ne);
-              if (req_word_ok(ev, sm.tag)) qreq = (int)req_word_hi(ev);
-            }
-            qok = false;
-            if (qreq >= 0) {
-              const unsigned long long* rw = P.req[qreq].w;
-              q0 = ld_volatile_u64(rw);
-              q1 = ld_volatile_u64(rw + 1);
-              q2 = ld_volatile_u64(rw + 2);
-              q3 = ld_volatile_u64(rw + 3);
-              if (sdone) qok = rready = result_complete(P, sm.tag, q0, q1, q2, q3);
+          // the entry's five words (its request and the request's result) in one read: issued at
+          // one batch start and looked at the next, when they are in, or at once when the stats
+          // items are out
+          if (ne == qe && qload) {
+            qload = false;
+            qreq = req_word_ok(qb, sm.tag) ? (int)req_word_hi(qb) : -1;
+            qok = rready = qreq >= 0 && result_complete(P, sm.tag, q0, q1, q2, q3);
+          }
+          if (!rready) {
+            qe = ne;
+            qok = false;  // (until these words are looked at)
+            const unsigned long long* qw = P.rq + (size_t)ne * kQWords;
+            q0 = ld_volatile_u64(qw);
+            q1 = ld_volatile_u64(qw + 1);
+            q2 = ld_volatile_u64(qw + 2);
+            q3 = ld_volatile_u64(qw + 3);
+            qb = ld_volatile_u64(qw + 4);
+            qload = true;
+            if (sdone) {
+              qload = false;
+              qreq = req_word_ok(qb, sm.tag) ? (int)req_word_hi(qb) : -1;
+              qok = rready = qreq >= 0 && result_complete(P, sm.tag, q0, q1, q2, q3);
             }
           }
         }
@@ -1800,16 +1805,23 @@ __device__ void decide(const Params& P, Shared& sm, unsigned char* fbuf, uint32_
     // items are handed out in queue order, once the producers see the words complete
     if (ft < 32) {
       const bool resid = soft && !err && n < K;
-      if (lane == 0 || (resid && lane < 4)) {
+      const bool wl = lane == 0 || (resid && lane < 4);  // the lanes that write a result word
+      unsigned long long word = 0ull;
+      if (wl) {
         unsigned hi = (unsigned)n | ((unsigned)err << 16) | (soft ? 0u : kNoResid);
         if (lane > 0)
           hi = __float_as_uint(lane == 1 ? q.rt.mc : lane == 2 ? q.rd.mc : __fdiv_rn((float)q.rt.Z, (float)q.rd.Z));
-        st_volatile_u64(P.req[b].w + lane, ((unsigned long long)hi << 32) | sm.tag);
+        word = ((unsigned long long)hi << 32) | sm.tag;
+        st_volatile_u64(P.req[b].w + lane, word);
       }
-      __syncwarp();
+      // the queue entry: its slot, then the same words and the request's index
+      unsigned slot = 0u;
+      if (lane == 0) slot = atomicAdd(P.rq_tail, 1u);
+      slot = __shfl_sync(kFull, slot, 0);
+      unsigned long long* qw = P.rq + (size_t)slot * kQWords;
+      if (wl) st_volatile_u64(qw + lane, word);
       if (lane == 0) {
-        const unsigned slot = atomicAdd(P.rq_tail, 1u);
-        st_volatile_u64(P.rq + slot, ((unsigned long long)(unsigned)b << 32) | sm.tag);
+        st_volatile_u64(qw + 4, ((unsigned long long)(unsigned)b << 32) | sm.tag);
         q.resid = resid ? 1 : 0;
       }
     }
@@ -2055,9 +2067,12 @@ __device__ bool finalize_request(const Params& P, Shared& sm, unsigned char* fbu
       if (ft == 0) {
         __threadfence();
         const unsigned hi = (unsigned)n | ((unsigned)err << 16) | (soft ? 0u : kNoResid);
-        st_volatile_u64(P.req[b].w, ((unsigned long long)hi << 32) | sm.tag);
+        const unsigned long long word = ((unsigned long long)hi << 32) | sm.tag;
+        st_volatile_u64(P.req[b].w, word);
         const unsigned slot = atomicAdd(P.rq_tail, 1u);
-        st_volatile_u64(P.rq + slot, ((unsigned long long)(unsigned)b << 32) | sm.tag);
+        unsigned long long* qw = P.rq + (size_t)slot * kQWords;
+        st_volatile_u64(qw, word);
+        st_volatile_u64(qw + 4, ((unsigned long long)(unsigned)b << 32) | sm.tag);
       }
       if (draws) {
         for (int kk = 0; kk < K; ++kk) {

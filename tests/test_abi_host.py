@@ -38,15 +38,15 @@ def test_every_declared_symbol_is_exported(lib):
 def test_workspace_size(lib):
     # V = 128256 fp32 spans at most 32064 16-byte vectors: 16 stats chunks of 2048 vectors and 32
     # residual chunks of 1024.  Layout: counters (two 128-byte lines, 2 * B * rows u32 counts,
-    # padded to 16 B), request states (32 B each) and the residual queue (8 B per request),
-    # together padded to 256 B; then chunk stats, sub-chunk stats (8 per chunk), row stats, residual
-    # sums and residual sub-sums (8 per residual chunk; 8 bytes each: the value and the call's tag),
-    # each padded to 256 B.
+    # padded to 16 B), request states (32 B each) and the residual queue (five 8-byte words per
+    # request), together padded to 256 B; then chunk stats, sub-chunk stats (8 per chunk), row stats
+    # and residual sub-sums (8 per residual chunk; 8 bytes each: the value and the call's tag), each
+    # padded to 256 B.
     def up(x, a=256):
         return (x + a - 1) // a * a
 
     B, rows, n, nr = 64, 11, 16, 32
-    want = (up(up(256 + 2 * B * rows * 4, 16) + B * 32 + B * 8) + up(B * rows * n * 16)
+    want = (up(up(256 + 2 * B * rows * 4, 16) + B * 32 + B * 40) + up(B * rows * n * 16)
             + up(B * rows * n * 8 * 16) + up(B * rows * 32) + up(B * rows * nr * 8 * 8))
     assert lib.spec_verify_workspace_bytes(B, rows, 128256, 0) == want
     assert lib.spec_verify_workspace_bytes(-1, 6, 100, 0) == 0
