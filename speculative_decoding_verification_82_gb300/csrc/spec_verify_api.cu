@@ -250,10 +250,9 @@ spec_status_t verify_chain_common(bool ngram, const void* target, const void* dr
   P.R = K + 1;
   P.rows = rows;
   P.diag = diag;
-  // the bonus rows stream first when the call runs residual passes at one temperature (the stream
-  // then ends on the last position, which few requests reach); measured slower for calls without
-  // residual passes and for per-request temperatures
-  P.bonus_first = (P.npos > 0 && !temps) ? 1 : 0;
+  // the bonus rows stream first when the call runs residual passes (the stream then ends on the
+  // last position, which few requests reach); measured slower for calls without residual passes
+  P.bonus_first = P.npos > 0 ? 1 : 0;
   // Calls with residual passes: larger stats batches, so that a producer looks for residual items
   // less often and the stats stream, which every later position waits for, runs ahead; and near
   // the end of the stats stream the stats items go first (measured: 72.3 against 77.6 us with
