@@ -348,7 +348,7 @@ spec_status_t spec_verify_tree_greedy(const void* target_logits, spec_dtype_t dt
   if (sms <= 0) return SPEC_ERR_CUDA;
   P.total = (unsigned)((long long)B * rows * P.nchunk);
   P.npos = 0;
-  P.claim = specv::kClaim;
+  P.claim = 2;  // (measured: 42.9 us against 43.7 with 4 on the 61-node greedy tree workload)
   set_divisors(P, B, rows, 1);
   P.target = target_logits;
   P.B = B;
