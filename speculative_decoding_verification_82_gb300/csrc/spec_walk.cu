@@ -1,9 +1,10 @@
 // spec_walk.cu -- spec_verify_tree_walk: argument checks, cluster geometry, launch.
 //
 // Host side of the tree walk (tree_walk.cuh).  A request goes to one thread-block cluster of
-// `cl` CTAs of 512 threads; each thread holds E consecutive tokens of the visited rows in
-// registers, so a cluster covers V <= cl * 512 * E.  The grid is as many clusters as fit on the
-// device at once (at most B), each taking requests b, b + grid, ...
+// `cl` CTAs of 512 threads; each thread holds E consecutive tokens of the visited rows (in
+// registers, or in shared memory for the 6-CTA geometry), so a cluster covers V <= cl * 512 * E.
+// The grid is as many clusters as fit on the device at once (at most B), each taking requests
+// b, b + grid, ...
 #include <math.h>
 #include <stdint.h>
 
@@ -18,6 +19,8 @@ using specv::walk::Params;
 
 constexpr int kSmallE = 8;   // V <= 4096: one CTA
 constexpr int kLargeE = 32;  // otherwise clusters of 1..16 CTAs
+constexpr int kShE = 48;     // clusters of kShCl CTAs with p and q in shared memory (196 KB a CTA)
+constexpr int kShCl = 6;
 
 struct Geometry {
   int E, cl;
@@ -41,51 +44,84 @@ bool plan(int V, Geometry* g) {
   return false;
 }
 
-template <typename T, int E>
+// Clusters of `cl` CTAs of instantiation (T, E, SM) resident at once, with `dyn` bytes of dynamic
+// shared memory a CTA; found once per device, instantiation and cluster size.
+template <typename T, int E, bool SM>
+int clusters_that_fit(int cl, size_t dyn) {
+  auto kern = specv::walk::walk_kernel<T, E, SM>;
+  static std::mutex mu;
+  static int cache[64][specv::walk::kMaxCluster + 1] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return -1;
+  {
+    std::lock_guard<std::mutex> g(mu);
+    if (cache[dev][cl] > 0) return cache[dev][cl];
+  }
+  if (cl > 8 && cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    return -1;
+  if (dyn > 0 && cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)dyn) != cudaSuccess)
+    return -1;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = (unsigned)cl;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3((unsigned)cl);
+  cfg.blockDim = dim3(specv::walk::kThreads);
+  cfg.dynamicSmemBytes = dyn;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int fit = 0;
+  if (cudaOccupancyMaxActiveClusters(&fit, kern, &cfg) != cudaSuccess || fit <= 0) return -1;
+  std::lock_guard<std::mutex> g(mu);
+  cache[dev][cl] = fit;
+  return fit;
+}
+
+template <typename T, int E, bool SM>
 cudaError_t launch_one(const Params& P, cudaStream_t stream) {
-  auto kern = specv::walk::walk_kernel<T, E>;
+  const size_t dyn = SM ? (size_t)2 * E * specv::walk::kThreads * sizeof(float) : 0;
+  const int fit = clusters_that_fit<T, E, SM>(P.cl, dyn);
+  if (fit <= 0) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)P.cl;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  const int clusters = P.B < fit ? P.B : fit;
+  cfg.gridDim = dim3((unsigned)(clusters * P.cl));
   cfg.blockDim = dim3(specv::walk::kThreads);
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = dyn;
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  // clusters resident at once, per (device, instantiation, cluster size); found once
-  static std::mutex mu;
-  static int cache[64][specv::walk::kMaxCluster + 1] = {};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return e;
-  int fit = 0;
-  {
-    std::lock_guard<std::mutex> g(mu);
-    if (dev >= 0 && dev < 64) fit = cache[dev][P.cl];
-  }
-  if (fit <= 0) {
-    if (P.cl > 8) {
-      e = cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-      if (e != cudaSuccess) return e;
-    }
-    cfg.gridDim = dim3((unsigned)P.cl);
-    e = cudaOccupancyMaxActiveClusters(&fit, kern, &cfg);
-    if (e != cudaSuccess) return e;
-    if (fit <= 0) return cudaErrorInvalidConfiguration;
-    std::lock_guard<std::mutex> g(mu);
-    if (dev >= 0 && dev < 64) cache[dev][P.cl] = fit;
-  }
-  const int clusters = P.B < fit ? P.B : fit;
-  cfg.gridDim = dim3((unsigned)(clusters * P.cl));
-  return cudaLaunchKernelEx(&cfg, kern, P);
+  return cudaLaunchKernelEx(&cfg, specv::walk::walk_kernel<T, E, SM>, P);
 }
 
+// The geometry of the call: the smallest cluster with p and q in registers, unless the walk
+// samples at one temperature and clusters of kShCl CTAs with p and q in shared memory cover V and
+// take the batch in fewer waves (their threads hold 1.5 times the tokens, but more of them fit at
+// once).  Measured on 16 requests of 61 nodes at V = 128256: 50.4 against 51.6 us at T = 1, but
+// 11.7 against 10.3 us for the greedy walk and 51.9 against 39.0 us with per-request temperatures,
+// whose requests' times differ more, so those keep the register geometry.
 template <typename T>
-cudaError_t launch_typed(int E, const Params& P, cudaStream_t stream) {
-  return E == kSmallE ? launch_one<T, kSmallE>(P, stream) : launch_one<T, kLargeE>(P, stream);
+cudaError_t launch_typed(const Geometry& g, Params& P, cudaStream_t stream) {
+  if (g.E == kSmallE) {
+    P.cl = g.cl;
+    return launch_one<T, kSmallE, false>(P, stream);
+  }
+  if (P.c > 0.f && !P.temps && g.cl > kShCl && (long long)kShCl * specv::walk::kThreads * kShE >= P.V) {
+    const int f1 = clusters_that_fit<T, kLargeE, false>(g.cl, 0);
+    const int f2 = clusters_that_fit<T, kShE, true>(kShCl, (size_t)2 * kShE * specv::walk::kThreads * sizeof(float));
+    if (f1 > 0 && f2 > 0 && (P.B + f2 - 1) / f2 < (P.B + f1 - 1) / f1) {
+      P.cl = kShCl;
+      return launch_one<T, kShE, true>(P, stream);
+    }
+  }
+  P.cl = g.cl;
+  return launch_one<T, kLargeE, false>(P, stream);
 }
 
 bool aligned(const void* p, unsigned a) { return ((uintptr_t)p % a) == 0; }
@@ -135,9 +171,9 @@ extern "C" spec_status_t spec_verify_tree_walk(const void* target_logits, const 
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e;
   switch (dtype) {
-    case SPEC_DTYPE_F32: e = launch_typed<float>(g.E, P, st); break;
-    case SPEC_DTYPE_BF16: e = launch_typed<__nv_bfloat16>(g.E, P, st); break;
-    default: e = launch_typed<__half>(g.E, P, st); break;
+    case SPEC_DTYPE_F32: e = launch_typed<float>(g, P, st); break;
+    case SPEC_DTYPE_BF16: e = launch_typed<__nv_bfloat16>(g, P, st); break;
+    default: e = launch_typed<__half>(g, P, st); break;
   }
   if (e == cudaErrorInvalidConfiguration) return SPEC_ERR_UNSUPPORTED;
   return e == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;

@@ -177,10 +177,25 @@ template <typename T>
 __device__ __forceinline__ const char* row_of(const void* base, const Params& P, int b, int node) {
   return static_cast<const char*>(base) + ((size_t)b * P.N1 + node) * (size_t)P.V * Elem<T>::kSize;
 }
+// A thread's E values of the visited node's p or q: in registers, or (SM) in shared memory at
+// stride kThreads, for geometries whose E does not fit the register file.
+template <int E, bool SM>
+struct PQ {
+  float v[E];
+  __device__ __forceinline__ explicit PQ(float*) {}
+  __device__ __forceinline__ float& operator[](int k) { return v[k]; }
+};
+template <int E>
+struct PQ<E, true> {
+  float* base;  // this thread's first value
+  __device__ __forceinline__ explicit PQ(float* b) : base(b) {}
+  __device__ __forceinline__ float& operator[](int k) { return base[k * kThreads]; }
+};
+
 // This thread's E consecutive elements of a row from element `first` on, as floats; elements
 // past the row's end read as -inf.
-template <typename T, int E>
-__device__ __forceinline__ void load_seg(const char* row, long long first, int V, bool vec, float (&v)[E]) {
+template <typename T, int E, typename A>
+__device__ __forceinline__ void load_seg(const char* row, long long first, int V, bool vec, A& v) {
   constexpr int S = Elem<T>::kSize, VE = Elem<T>::kPerVec;
   static_assert(E % VE == 0, "a segment is whole 16-byte vectors");
   if (vec && first + E <= V) {
@@ -244,8 +259,9 @@ __device__ __forceinline__ void write_failure(const Params& P, int b, int err) {
 }
 
 // ------------------------------------------------------------------ one request ----
-template <typename T, int E>
-__device__ void walk_request(const Params& P, Shared& sm, int b, long long first, uint32_t rank, int& round) {
+template <typename T, int E, bool SM>
+__device__ void walk_request(const Params& P, Shared& sm, float* dyn, int b, long long first, uint32_t rank,
+                             int& round) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
   const int N1 = P.N1, V = P.V, cl = P.cl;
   // the request's temperature: log2(e) / T, formed in double as the host forms the call's own
@@ -286,7 +302,7 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
     const bool need_q = !greedy && nk > 0;
     const char* trow = row_of<T>(P.target, P, b, cur);
     const char* drow = need_q ? row_of<T>(P.draft, P, b, cur) : nullptr;
-    float p[E], q[E];
+    PQ<E, SM> p(dyn + threadIdx.x), q(dyn + (size_t)E * kThreads + threadIdx.x);
     load_seg<T, E>(trow, first, V, vec, p);
     if (need_q) {
       load_seg<T, E>(drow, first, V, vec, q);
@@ -603,14 +619,17 @@ __device__ void walk_request(const Params& P, Shared& sm, int b, long long first
   }
 }
 
-template <typename T, int E>
+// SM: p and q in dynamic shared memory (2 E kThreads floats), else in registers.
+template <typename T, int E, bool SM>
 __global__ void __launch_bounds__(kThreads, 1) walk_kernel(const Params P) {
   __shared__ Shared sm;
+  extern __shared__ float walk_dyn[];
   const uint32_t rank = cta_rank();
   const long long first = ((long long)rank * kThreads + threadIdx.x) * E;
   int round = 0;
   cluster_barrier();  // every CTA of the cluster runs before any peer writes to it
-  for (int b = (int)cluster_index(); b < P.B; b += (int)cluster_count()) walk_request<T, E>(P, sm, b, first, rank, round);
+  for (int b = (int)cluster_index(); b < P.B; b += (int)cluster_count())
+    walk_request<T, E, SM>(P, sm, walk_dyn, b, first, rank, round);
   cluster_barrier();  // none leaves while a peer may still write to it
 }
 
