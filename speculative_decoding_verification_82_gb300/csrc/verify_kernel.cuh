@@ -437,10 +437,11 @@ __device__ __forceinline__ void resid_weights(const unsigned char* buf, int dslo
 // Producer of group grp: items it = grp, grp + kGroups, ... of this CTA's sequence (stage
 // it % kStages).  The producer holds one batch of up to kClaim residual items from the cursor at a
 // time (claimed at the start of a batch of stats items, or at any item once those are out) and
-// stages its items, ahead of stats items, once their queue entry and their request's result are
-// published; it reads the entry and the result words at the start of each stats batch and uses
-// them at the next, so that the reads do not hold it up.  Only once its stats items are out does it
-// wait (bounded) for a result.  Once both kinds are exhausted it publishes one end marker.
+// stages its items, ahead of stats items, once their queue entry is published and complete; it
+// reads the entry (which carries the request's result words) at the start of a stats batch and
+// looks at it at the next, so that the read does not hold it up.  Only once its stats items are
+// out does it wait (bounded) for an entry.  Once both kinds are exhausted it publishes one end
+// marker.
 template <int MODE, typename T, bool PT>
 __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages, int grp) {
   const int lane = threadIdx.x & 31;
@@ -459,7 +460,7 @@ __device__ void producer_loop(const Params& P, Shared& sm, unsigned char* stages
     nxt = fixed + atomicAdd(P.work, claim);
   }
   // residual claims (lane 0): the held items rfirst .. rfirst + rcnt - 1; qreq, the request of queue
-  // entry qe once that entry is published; q0..q3, qreq's result words as last read
+  // entry qe once that entry is published; q0..q3 and qb, the entry's words as last read
   unsigned rfirst = 0, qe = 0xffffffffu, rseen = 0;  // rseen: the cursor as this producer last saw it
   int rcnt = 0, qreq = -1;
   // qok: request qreq's result is complete (only draft-model chains have residual items)
