@@ -2101,8 +2101,10 @@ __device__ bool finalize_request(const Params& P, Shared& sm, unsigned char* fbu
       }
     } else if (q.resid && !q.drawn) {  // the residual pass published at the decision (its result is
                                        // used only when no error turned up since)
-      if (!wait_count(P, sm, P.tick_b + (size_t)b * P.npos, (unsigned)P.nchunk_r)) return false;
-      if (ft == 0) P.tick_b[(size_t)b * P.npos] = 0;
+      // The draw waits for the residual sums themselves (their tags), not for their count, which
+      // saves a round trip; the count returns to zero once its last increments land, as the next
+      // call expects it.
+      if (ft == 0) atomicAdd(P.tick_b + (size_t)b * P.npos, 0u - (unsigned)P.nchunk_r);
       int tok;
       float mass;
       residual_draw<T>(P, sm, fbuf, fph, ssph, b, 0, n, c, q.u, q.rt, q.rd, &tok, &mass);
