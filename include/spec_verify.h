@@ -286,7 +286,10 @@ spec_status_t spec_ngram_draft(const int32_t *context, const int32_t *context_le
  *                path is not a chain of parent links from the root, or a slot is outside
  *                [0, num_slots); that request's rows are left untouched.
  * Limits: num_caches <= SPEC_MAX_KV_CACHES, N + 1 <= SPEC_MAX_WALK_NODES, B <= 65535.
- * One kernel launch; reads and writes each moved row once.  No workspace.
+ * One kernel launch; reads and writes each moved row once.  No workspace.  The launch allows
+ * programmatic stream serialisation: its blocks may start while the previous kernel in the stream
+ * drains, but they wait for that kernel to complete before reading or writing anything, so the
+ * call keeps stream order.
  */
 spec_status_t spec_kv_compact(void *const *caches, int num_caches, long long num_slots,
                               int row_bytes, int B, int N, const int32_t *slots,

@@ -19,7 +19,13 @@
 // p_j >= j (a node's index exceeds its parent's) and slots are distinct, so no store lands on a
 // row that a later move still reads, and moving in place is safe.  Moves with p_j == j are
 // skipped.  The kernel is a gather bound by HBM bandwidth: each moved row is read once and written
-// once.
+// once.  Both go through the streaming cache policy (evict first): the call touches each moved
+// byte once, and its dirty rows leave L2 ahead of data that is still in use.
+//
+// The kernel is launched with programmatic stream serialisation: its CTAs may be placed on the
+// SMs while the previous kernel in the stream drains, and each one waits for that kernel's
+// completion (griddepcontrol.wait) before its first memory access, so stream order holds for
+// every byte it reads or writes.  Each CTA at once lets the next such launch do the same.
 #include <stdint.h>
 
 #include "spec_verify.h"
@@ -52,6 +58,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kv_compact_kernel(const 
   __shared__ int nmove;
   const int grp = blockIdx.x, b = blockIdx.y, t = threadIdx.x;
   const int N1 = P.N1;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  if (t == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int32_t* pa = P.parents + (size_t)b * N1;
   // round 1: the length, the path and every slot, all at once
   const int L = __ldg(P.accept_len + b);
@@ -105,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kv_compact_kernel(const 
     const unsigned char* base = P.caches[c0 + cl] + (size_t)v * 16;
 #pragma unroll
     for (int k = 0; k < kBatch; ++k)
-      if (k < M) tmp[k] = *reinterpret_cast<const uint4*>(base + (size_t)src[k] * W);
+      if (k < M) tmp[k] = __ldcs(reinterpret_cast<const uint4*>(base + (size_t)src[k] * W));
   }
   for (int j = 1 + t; j <= L; j += kThreads) ok = ok && __ldg(pa + node[j]) == node[j - 1];
   ok = __syncthreads_and(ok);
@@ -118,11 +126,11 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kv_compact_kernel(const 
       if (i != t || k0 != 0) {
 #pragma unroll
         for (int k = 0; k < kBatch; ++k)
-          if (k0 + k < M) tmp[k] = *reinterpret_cast<const uint4*>(base + (size_t)src[k0 + k] * W);
+          if (k0 + k < M) tmp[k] = __ldcs(reinterpret_cast<const uint4*>(base + (size_t)src[k0 + k] * W));
       }
 #pragma unroll
       for (int k = 0; k < kBatch; ++k)
-        if (k0 + k < M) *reinterpret_cast<uint4*>(base + (size_t)dst[k0 + k] * W) = tmp[k];
+        if (k0 + k < M) __stcs(reinterpret_cast<uint4*>(base + (size_t)dst[k0 + k] * W), tmp[k]);
     }
   }
 }
@@ -173,6 +181,14 @@ extern "C" spec_status_t spec_kv_compact(void* const* caches, int num_caches, lo
   P.accept_len = accept_len;
   P.path = path_nodes;
   P.err_flags = err_flags;
-  kv_compact_kernel<<<dim3((unsigned)ngroups, (unsigned)B), kThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(P);
-  return cudaGetLastError() == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)ngroups, (unsigned)B);
+  cfg.blockDim = dim3(kThreads);
+  cfg.stream = reinterpret_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kv_compact_kernel, P) == cudaSuccess ? SPEC_OK : SPEC_ERR_CUDA;
 }
