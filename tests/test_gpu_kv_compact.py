@@ -1,7 +1,8 @@
 """GPU parity of accepted-path KV-cache compaction (spec_kv_compact) against the CPU oracle:
 random trees, paths and slot permutations, several caches and row sizes, invalid requests, the
-benchmark configuration (160 caches of 2048-byte rows, deepest paths of the 61-node tree), and
-the verification-then-compaction sequence on the greedy tree workload."""
+benchmark configuration (160 caches of 2048-byte rows, deepest paths of the 61-node tree) and
+the verification-then-compaction sequence on the greedy tree workload; also stream order around
+each call, eagerly and in a replayed CUDA graph."""
 
 import numpy as np
 import pytest
@@ -97,3 +98,47 @@ def test_after_greedy_tree_verification():
         for j in range(L[b] + 1):
             want = (rows[b * N1 + P[b, j]] * 16 + np.arange(16)).astype(np.uint8)
             assert np.array_equal(c[b * N1 + j], want), (b, j)
+
+
+def test_stream_order_around_each_call():
+    """The call may be placed on the SMs while the previous kernel in the stream drains, but it
+    must see all of that kernel's writes, and the next kernel must see all of its own.  A copy
+    kernel refills the caches before each call and a clone reads them after it, 20 times on one
+    stream, then the same sequence as a replayed CUDA graph; every result equals the oracle's."""
+    kc = synth.kv_compact_case(seed=5, B=16, caches=8, row_bytes=2048)
+    rng = np.random.default_rng(11)
+    sets = [rng.integers(0, 256, kc["caches"].shape, dtype=np.uint8) for _ in range(4)]
+    want = [oracle.kv_compact_batch(s, kc["slots"], kc["parents"], kc["accept_len"], kc["path"])[0] for s in sets]
+    dev_sets = [torch.from_numpy(s).cuda() for s in sets]
+    slots, parents = parity.i32(kc["slots"]), parity.i32(kc["parents"])
+    al, path = parity.i32(kc["accept_len"]), parity.i32(kc["path"])
+    cache = torch.empty_like(dev_sets[0])
+    views = [cache[i] for i in range(cache.shape[0])]
+    outs = []
+    for it in range(20):
+        cache.copy_(dev_sets[it % 4])
+        binding.spec_kv_compact(views, slots, parents, al, path)
+        outs.append(cache.clone())
+    torch.cuda.synchronize()
+    for it, o in enumerate(outs):
+        assert np.array_equal(o.cpu().numpy(), want[it % 4]), it
+
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    gouts = [torch.empty_like(cache) for _ in range(4)]
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):
+        binding.spec_kv_compact(views, slots, parents, al, path)  # warm-up outside the capture
+        with torch.cuda.graph(graph, stream=side):
+            for k in range(4):
+                cache.copy_(dev_sets[k])
+                binding.spec_kv_compact(views, slots, parents, al, path)
+                gouts[k].copy_(cache)
+    torch.cuda.current_stream().wait_stream(side)
+    for _ in range(3):
+        for g in gouts:
+            g.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        for k in range(4):
+            assert np.array_equal(gouts[k].cpu().numpy(), want[k]), k
