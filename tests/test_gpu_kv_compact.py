@@ -142,3 +142,41 @@ def test_stream_order_around_each_call():
         torch.cuda.synchronize()
         for k in range(4):
             assert np.array_equal(gouts[k].cpu().numpy(), want[k]), k
+
+
+def test_limits():
+    """The largest call shapes: SPEC_MAX_KV_CACHES caches and trees of SPEC_MAX_WALK_NODES nodes
+    with paths of 511 and 512 moves (the move list in many batches); then 65535 requests (the
+    grid's largest y extent), each moving one row."""
+    N1, C = binding.MAX_WALK_NODES, binding.MAX_KV_CACHES
+    par = np.array([-1, 0] + [i - 2 for i in range(2, N1)], np.int32)  # two interleaved chains
+    parents = np.stack([par, par])
+    path = np.full((2, N1), -1, np.int32)
+    for b, last in enumerate((N1 - 2, N1 - 1)):
+        chain = [last]
+        while chain[-1] != 0:
+            chain.append(int(par[chain[-1]]))
+        chain = chain[::-1]
+        path[b, : len(chain)] = chain
+    al = (path >= 0).sum(1).astype(np.int32) - 1
+    assert list(al) == [511, 512]
+    rng = np.random.default_rng(3)
+    S = 2 * N1 + 5
+    slots = rng.permutation(S)[: 2 * N1].reshape(2, N1).astype(np.int32)
+    caches = rng.integers(0, 256, (C, S, 16), dtype=np.uint8)
+    g, gerr = _run(caches, slots, parents, al, path)
+    o, oerr = oracle.kv_compact_batch(caches, slots, parents, al, path)
+    assert (gerr == 0).all() and (oerr == 0).all()
+    assert np.array_equal(g, o)
+
+    B = 65535
+    parents = np.tile(np.array([-1, 0, 0], np.int32), (B, 1))
+    path = np.tile(np.array([0, 2, -1], np.int32), (B, 1))
+    al = np.ones(B, np.int32)
+    slots = (np.arange(B)[:, None] * 3 + np.arange(3)[None, :]).astype(np.int32)
+    caches = rng.integers(0, 256, (1, 3 * B, 16), dtype=np.uint8)
+    g, gerr = _run(caches, slots, parents, al, path)
+    o, oerr = oracle.kv_compact_batch(caches, slots, parents, al, path)
+    assert (gerr == 0).all() and (oerr == 0).all()
+    assert np.array_equal(g, o)
+    assert np.array_equal(g[0, 1::3], caches[0, 2::3])  # every request's node 2 moved to its slot 1

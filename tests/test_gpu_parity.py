@@ -254,6 +254,43 @@ def test_very_large_vocab():
         parity.compare_chain(parity.run_gpu_chain(ci, ngram=True), parity.run_oracle_chain(ci, ngram=True), ci)
 
 
+def test_limits():
+    """The largest draft length, SPEC_MAX_K = 256 positions (513 rows a request), in every mode,
+    with request 0 built to pass every test so that its bonus row is drawn after 256
+    acceptances; then the largest streaming tree, SPEC_MAX_TREE_NODES nodes, along whose boosted
+    root-to-leaf path the greedy walk descends hundreds of levels."""
+    import dataclasses
+
+    K = binding.MAX_K
+    ci = _random_chain(21, 3, K, 1500)
+    ci.draft[0] = ci.target[0, :K]  # q = p at every position of request 0: alpha = 1
+    o = parity.run_oracle_chain(ci)
+    assert o["num_accepted"][0] == K
+    parity.compare_chain(parity.run_gpu_chain(ci), o, ci)
+    parity.compare_chain(parity.run_gpu_chain(ci, diag=False), o, ci)
+    t = ci.target.copy()
+    t[0, np.arange(K), ci.draft_tokens[0]] += 80.0  # p(x_k) = 1 to fp32 precision
+    cn = dataclasses.replace(ci, target=t)
+    o = parity.run_oracle_chain(cn, ngram=True)
+    assert o["num_accepted"][0] == K
+    parity.compare_chain(parity.run_gpu_chain(cn, ngram=True), o, cn)
+    x = ci.draft_tokens.copy()
+    x[0] = ci.target[0, :K].argmax(-1)  # greedy: every draft is its row's argmax
+    cg = dataclasses.replace(ci, draft_tokens=x, temperature=np.float32(0.0))
+    o = parity.run_oracle_chain(cg)
+    assert o["num_accepted"][0] == K
+    parity.compare_chain(parity.run_gpu_chain(cg), o, cg)
+    parity.compare_chain(parity.run_gpu_chain(cg, ngram=True), parity.run_oracle_chain(cg, ngram=True), cg)
+
+    rng = np.random.default_rng(5)
+    N1 = binding.MAX_TREE_NODES
+    par = np.array([-1] + [int(rng.integers(max(0, i - 6), i)) for i in range(1, N1)], np.int32)
+    ti = synth.tree_greedy(seed=4, B=2, V=300, parents=par, path_boost=40.0)
+    st = parity.compare_tree(parity.run_gpu_tree(ti), parity.run_oracle_tree(ti))
+    _show(f"tree of {N1} nodes", st)
+    assert st["mean_accepted"] >= 100
+
+
 def test_many_small_requests():
     ci = _random_chain(11, 4096, 5, 64)
     parity.compare_chain(parity.run_gpu_chain(ci), parity.run_oracle_chain(ci, threads=16), ci)

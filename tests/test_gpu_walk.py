@@ -113,6 +113,28 @@ def test_walk_single_wave_geometry(B, V, dtype):
     assert st["errors"] == 0
 
 
+def test_walk_limits():
+    """The largest walk shapes: a tree of SPEC_MAX_WALK_NODES nodes (two interleaved chains)
+    whose draft rows nearly equal its target rows, so that the stochastic walk descends over a
+    hundred levels, and the greedy walk on it; then the largest vocabulary, SPEC_MAX_WALK_VOCAB
+    (16-CTA clusters, no ragged tail)."""
+    rng = np.random.default_rng(17)
+    N1 = binding.MAX_WALK_NODES
+    par = np.array([-1, 0] + [i - 2 for i in range(2, N1)], np.int32)  # two interleaved chains
+    ti = synth.tree_sample(seed=17, B=2, V=3000, temperature=1.0, dtype="bf16", parents=par,
+                           draft_sigma=0.05)
+    o = parity.run_oracle_walk(ti)
+    assert o["accept_len"].max() >= 100
+    st = parity.compare_walk(parity.run_gpu_walk(ti), o, ti)
+    st0 = parity.compare_walk(parity.run_gpu_walk(ti, 0.0), parity.run_oracle_walk(ti, 0.0), ti)
+    _show(f"walk of {N1} nodes", (st, st0))
+    ti = synth.tree_sample(seed=18, B=2, V=binding.MAX_WALK_VOCAB, temperature=1.0, dtype="f16",
+                           parents=_random_parents(rng, 6), draft_sigma=1.0)
+    st = parity.compare_walk(parity.run_gpu_walk(ti), parity.run_oracle_walk(ti), ti)
+    st0 = parity.compare_walk(parity.run_gpu_walk(ti, 0.0), parity.run_oracle_walk(ti, 0.0), ti)
+    _show(f"walk V={ti.V}", (st, st0))
+
+
 @pytest.mark.parametrize("T", [0.05, 0.3, 2.5, 8.0])
 def test_walk_temperatures(T):
     rng = np.random.default_rng(int(T * 100))
