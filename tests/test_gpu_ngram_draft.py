@@ -33,7 +33,8 @@ def _compare(g, o):
     assert np.array_equal(g["match_end"], o["match_end"])
 
 
-@pytest.mark.parametrize("K,n_max,n_min", [(5, 4, 1), (1, 4, 1), (16, 8, 2), (5, 1, 1), (7, 32, 3)])
+@pytest.mark.parametrize("K,n_max,n_min", [(5, 4, 1), (1, 4, 1), (16, 8, 2), (5, 1, 1), (7, 32, 3),
+                                         (256, 32, 1)])  # the largest K and n_max
 def test_random_contexts(K, n_max, n_min):
     rng = np.random.default_rng(K * 100 + n_max)
     B, Lmax = 600, 300
