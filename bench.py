@@ -745,7 +745,10 @@ def measure(args, name: str, w: dict, rank: int, world: int, local: int, primary
                                  f"not already in place) x 2048 bytes, read and written once")
     if w["kind"] == "walk":
         res["roofline"].update(
-            kernel=f"walk_kernel<{w['dtype']},32>, clusters of 8 CTAs (one launch per call)",
+            kernel=("walk_kernel (one launch per call): 6-CTA clusters with 48 tokens a thread when they take "
+                    "the batch in fewer waves than 8-CTA clusters with 32 (greedy: p in registers; one "
+                    "temperature: p and q in shared memory), else 8-CTA clusters; per-request temperatures: "
+                    "8-CTA clusters"),
             algorithmic_bytes_note="acceptance-aware: the rows the walk reads (visited nodes' target rows, and "
                                    "draft rows of visited nodes with children), mean over the input sets",
             all_rows_bytes_per_call=alg_bytes,

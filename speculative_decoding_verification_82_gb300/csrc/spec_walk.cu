@@ -2,7 +2,8 @@
 //
 // Host side of the tree walk (tree_walk.cuh).  A request goes to one thread-block cluster of
 // `cl` CTAs of 512 threads; each thread holds E consecutive tokens of the visited rows (in
-// registers, or in shared memory for the 6-CTA geometry), so a cluster covers V <= cl * 512 * E.
+// registers, or in shared memory for the 6-CTA geometry of the stochastic walk), so a cluster
+// covers V <= cl * 512 * E.
 // The grid is as many clusters as fit on the device at once (at most B), each taking requests
 // b, b + grid, ...
 #include <math.h>
@@ -19,8 +20,8 @@ using specv::walk::Params;
 
 constexpr int kSmallE = 8;   // V <= 4096: one CTA
 constexpr int kLargeE = 32;  // otherwise clusters of 1..16 CTAs
-constexpr int kShE = 48;     // clusters of kShCl CTAs with p and q in shared memory (196 KB a CTA)
-constexpr int kShCl = 6;
+constexpr int kShE = 48;     // clusters of kShCl CTAs: p and q in shared memory (196 KB a CTA), or
+constexpr int kShCl = 6;     // for greedy calls p alone in registers
 
 struct Geometry {
   int E, cl;
@@ -46,9 +47,9 @@ bool plan(int V, Geometry* g) {
 
 // Clusters of `cl` CTAs of instantiation (T, E, SM) resident at once, with `dyn` bytes of dynamic
 // shared memory a CTA; found once per device, instantiation and cluster size.
-template <typename T, int E, bool SM>
+template <typename T, int E, bool SM, bool G = false>
 int clusters_that_fit(int cl, size_t dyn) {
-  auto kern = specv::walk::walk_kernel<T, E, SM>;
+  auto kern = specv::walk::walk_kernel<T, E, SM, G>;
   static std::mutex mu;
   static int cache[64][specv::walk::kMaxCluster + 1] = {};
   int dev = 0;
@@ -79,10 +80,10 @@ int clusters_that_fit(int cl, size_t dyn) {
   return fit;
 }
 
-template <typename T, int E, bool SM>
+template <typename T, int E, bool SM, bool G = false>
 cudaError_t launch_one(const Params& P, cudaStream_t stream) {
   const size_t dyn = SM ? (size_t)2 * E * specv::walk::kThreads * sizeof(float) : 0;
-  const int fit = clusters_that_fit<T, E, SM>(P.cl, dyn);
+  const int fit = clusters_that_fit<T, E, SM, G>(P.cl, dyn);
   if (fit <= 0) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -97,20 +98,30 @@ cudaError_t launch_one(const Params& P, cudaStream_t stream) {
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, specv::walk::walk_kernel<T, E, SM>, P);
+  return cudaLaunchKernelEx(&cfg, specv::walk::walk_kernel<T, E, SM, G>, P);
 }
 
-// The geometry of the call: the smallest cluster with p and q in registers, unless the walk
-// samples at one temperature and clusters of kShCl CTAs with p and q in shared memory cover V and
-// take the batch in fewer waves (their threads hold 1.5 times the tokens, but more of them fit at
-// once).  Measured on 16 requests of 61 nodes at V = 128256: 50.4 against 51.6 us at T = 1, but
-// 11.7 against 10.3 us for the greedy walk and 51.9 against 39.0 us with per-request temperatures,
-// whose requests' times differ more, so those keep the register geometry.
+// The geometry of the call: the smallest cluster with p and q in registers, unless clusters of
+// kShCl CTAs cover V and take the batch in fewer waves (their threads hold 1.5 times the tokens,
+// but more of them fit at once: 23 against 15 of 8 CTAs on a 152-SM GB300).  A greedy call then
+// runs an instantiation without q, whose 48 tokens a thread stay in registers; a walk that samples
+// at one temperature keeps p and q in shared memory.  Measured on 16 requests of 61 nodes at
+// V = 128256: greedy 8.66 against 10.33 us, T = 1 50.4 against 51.6 us; with per-request
+// temperatures 51.9 against 39.0 us, whose requests' times differ more, so those keep the
+// register geometry.
 template <typename T>
 cudaError_t launch_typed(const Geometry& g, Params& P, cudaStream_t stream) {
   if (g.E == kSmallE) {
     P.cl = g.cl;
     return launch_one<T, kSmallE, false>(P, stream);
+  }
+  if (P.c == 0.f && !P.temps && g.cl > kShCl && (long long)kShCl * specv::walk::kThreads * kShE >= P.V) {
+    const int f1 = clusters_that_fit<T, kLargeE, false>(g.cl, 0);
+    const int f2 = clusters_that_fit<T, kShE, false, true>(kShCl, 0);
+    if (f1 > 0 && f2 > 0 && (P.B + f2 - 1) / f2 < (P.B + f1 - 1) / f1) {
+      P.cl = kShCl;
+      return launch_one<T, kShE, false, true>(P, stream);
+    }
   }
   if (P.c > 0.f && !P.temps && g.cl > kShCl && (long long)kShCl * specv::walk::kThreads * kShE >= P.V) {
     const int f1 = clusters_that_fit<T, kLargeE, false>(g.cl, 0);

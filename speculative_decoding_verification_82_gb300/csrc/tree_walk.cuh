@@ -259,7 +259,9 @@ __device__ __forceinline__ void write_failure(const Params& P, int b, int err) {
 }
 
 // ------------------------------------------------------------------ one request ----
-template <typename T, int E, bool SM>
+// G: an instantiation for greedy calls only, whose threads hold no q (so 48 tokens a thread fit
+// in registers).
+template <typename T, int E, bool SM, bool G>
 __device__ void walk_request(const Params& P, Shared& sm, float* dyn, int b, long long first, uint32_t rank,
                              int& round) {
   const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
@@ -272,7 +274,7 @@ __device__ void walk_request(const Params& P, Shared& sm, float* dyn, int b, lon
     bad_temp = !(Tb >= 0.f) || isinf(Tb);
     c = (bad_temp || Tb == 0.f) ? 0.f : (float)(1.4426950408889634 / (double)Tb);
   }
-  const bool greedy = c == 0.f, vec = P.vec != 0;
+  const bool greedy = G || c == 0.f, vec = P.vec != 0;
 
   // Stage the tree; the first malformed node decides the error (its parent checked first).
   __syncthreads();  // the previous request's readers of the tree are done
@@ -619,8 +621,9 @@ __device__ void walk_request(const Params& P, Shared& sm, float* dyn, int b, lon
   }
 }
 
-// SM: p and q in dynamic shared memory (2 E kThreads floats), else in registers.
-template <typename T, int E, bool SM>
+// SM: p and q in dynamic shared memory (2 E kThreads floats), else in registers; G: greedy calls
+// only.
+template <typename T, int E, bool SM, bool G>
 __global__ void __launch_bounds__(kThreads, 1) walk_kernel(const Params P) {
   __shared__ Shared sm;
   extern __shared__ float walk_dyn[];
@@ -629,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 1) walk_kernel(const Params P) {
   int round = 0;
   cluster_barrier();  // every CTA of the cluster runs before any peer writes to it
   for (int b = (int)cluster_index(); b < P.B; b += (int)cluster_count())
-    walk_request<T, E, SM>(P, sm, walk_dyn, b, first, rank, round);
+    walk_request<T, E, SM, G>(P, sm, walk_dyn, b, first, rank, round);
   cluster_barrier();  // none leaves while a peer may still write to it
 }
 

@@ -103,14 +103,16 @@ def test_walk_more_requests_than_clusters():
 
 @pytest.mark.parametrize("B,V,dtype", [(40, 128256, "bf16"), (20, 131075, "f32"), (20, 147456, "f16")])
 def test_walk_single_wave_geometry(B, V, dtype):
-    """Batches that need more waves of register-resident clusters than of the 6-CTA clusters that
-    keep p and q in shared memory: the stochastic walk takes the latter (several requests per
-    cluster at B = 40; a ragged vocabulary; the largest vocabulary 6 CTAs cover)."""
+    """Batches that need more waves of 8-CTA clusters than of 6-CTA clusters: the stochastic walk
+    takes the 6-CTA clusters that keep p and q in shared memory, and the greedy walk the 6-CTA
+    instantiation without q (several requests per cluster at B = 40; a ragged vocabulary; the
+    largest vocabulary 6 CTAs cover)."""
     rng = np.random.default_rng(B + V)
     ti = synth.tree_sample(seed=V % 97, B=B, V=V, dtype=dtype, parents=_random_parents(rng, 7), draft_sigma=1.0)
     st = parity.compare_walk(parity.run_gpu_walk(ti), parity.run_oracle_walk(ti, threads=16), ti)
-    _show(f"walk single wave B={B} V={V} {dtype}", st)
-    assert st["errors"] == 0
+    st0 = parity.compare_walk(parity.run_gpu_walk(ti, 0.0), parity.run_oracle_walk(ti, 0.0, threads=16), ti)
+    _show(f"walk single wave B={B} V={V} {dtype}", (st, st0))
+    assert st["errors"] == 0 and st0["errors"] == 0
 
 
 def test_walk_limits():
