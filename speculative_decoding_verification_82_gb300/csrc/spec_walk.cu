@@ -2,7 +2,7 @@
 //
 // Host side of the tree walk (tree_walk.cuh).  A request goes to one thread-block cluster of
 // `cl` CTAs of 512 threads; each thread holds E consecutive tokens of the visited rows (in
-// registers, or in shared memory for the 6-CTA geometry of the stochastic walk), so a cluster
+// registers; q in shared memory for the 6-CTA geometry of the stochastic walk), so a cluster
 // covers V <= cl * 512 * E.
 // The grid is as many clusters as fit on the device at once (at most B), each taking requests
 // b, b + grid, ...
@@ -20,8 +20,8 @@ using specv::walk::Params;
 
 constexpr int kSmallE = 8;   // V <= 4096: one CTA
 constexpr int kLargeE = 32;  // otherwise clusters of 1..16 CTAs
-constexpr int kShE = 48;     // clusters of kShCl CTAs: p and q in shared memory (196 KB a CTA), or
-constexpr int kShCl = 6;     // for greedy calls p alone in registers
+constexpr int kShE = 48;     // clusters of kShCl CTAs: p in registers and q in shared memory (96 KB
+constexpr int kShCl = 6;     // a CTA), or for greedy calls p alone
 
 struct Geometry {
   int E, cl;
@@ -82,7 +82,7 @@ int clusters_that_fit(int cl, size_t dyn) {
 
 template <typename T, int E, bool SM, bool G = false>
 cudaError_t launch_one(const Params& P, cudaStream_t stream) {
-  const size_t dyn = SM ? (size_t)2 * E * specv::walk::kThreads * sizeof(float) : 0;
+  const size_t dyn = SM ? (size_t)E * specv::walk::kThreads * sizeof(float) : 0;
   const int fit = clusters_that_fit<T, E, SM, G>(P.cl, dyn);
   if (fit <= 0) return cudaErrorInvalidConfiguration;
   cudaLaunchConfig_t cfg = {};
@@ -105,9 +105,9 @@ cudaError_t launch_one(const Params& P, cudaStream_t stream) {
 // kShCl CTAs cover V and take the batch in fewer waves (their threads hold 1.5 times the tokens,
 // but more of them fit at once: 23 against 15 of 8 CTAs on a 152-SM GB300).  A greedy call then
 // runs an instantiation without q, whose 48 tokens a thread stay in registers; a walk that samples
-// at one temperature keeps p and q in shared memory.  Measured on 16 requests of 61 nodes at
-// V = 128256: greedy 8.66 against 10.33 us, T = 1 50.4 against 51.6 us; with per-request
-// temperatures 51.9 against 39.0 us, whose requests' times differ more, so those keep the
+// at one temperature keeps p in registers and q in shared memory.  Measured on 16 requests of 61
+// nodes at V = 128256: greedy 8.66 against 10.33 us, T = 1 41.9 against 51.6 us; with per-request
+// temperatures 43.3 against 39.2 us, whose requests' times differ more, so those keep the
 // register geometry.
 template <typename T>
 cudaError_t launch_typed(const Geometry& g, Params& P, cudaStream_t stream) {
@@ -125,7 +125,7 @@ cudaError_t launch_typed(const Geometry& g, Params& P, cudaStream_t stream) {
   }
   if (P.c > 0.f && !P.temps && g.cl > kShCl && (long long)kShCl * specv::walk::kThreads * kShE >= P.V) {
     const int f1 = clusters_that_fit<T, kLargeE, false>(g.cl, 0);
-    const int f2 = clusters_that_fit<T, kShE, true>(kShCl, (size_t)2 * kShE * specv::walk::kThreads * sizeof(float));
+    const int f2 = clusters_that_fit<T, kShE, true>(kShCl, (size_t)kShE * specv::walk::kThreads * sizeof(float));
     if (f1 > 0 && f2 > 0 && (P.B + f2 - 1) / f2 < (P.B + f1 - 1) / f1) {
       P.cl = kShCl;
       return launch_one<T, kShE, true>(P, stream);

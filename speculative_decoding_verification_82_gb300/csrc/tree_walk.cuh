@@ -11,8 +11,8 @@
 //
 // One thread-block cluster verifies one request at a time.  CTA `rank` of the cluster owns the
 // vocabulary slice [rank * 512 E, (rank + 1) * 512 E) and each of its 512 threads E consecutive
-// tokens of it, so the probabilities p and q of the node being visited live in registers for
-// the whole visit.  Row statistics, residual masses and the draw's prefix sums are reduced in
+// tokens of it, so the probabilities p and q of the node being visited stay on the SM for the
+// whole visit (in registers; q in shared memory where both do not fit).  Row statistics, residual masses and the draw's prefix sums are reduced in
 // a fixed order (warp, block, then the cluster's CTAs in rank order through distributed shared
 // memory), so every CTA computes bit-identical values and takes identical decisions; the
 // cluster barrier is the only synchronisation, and no thread ever spins on memory.
@@ -178,7 +178,7 @@ __device__ __forceinline__ const char* row_of(const void* base, const Params& P,
   return static_cast<const char*>(base) + ((size_t)b * P.N1 + node) * (size_t)P.V * Elem<T>::kSize;
 }
 // A thread's E values of the visited node's p or q: in registers, or (SM) in shared memory at
-// stride kThreads, for geometries whose E does not fit the register file.
+// stride kThreads, for the q of geometries whose p and q together do not fit the register file.
 template <int E, bool SM>
 struct PQ {
   float v[E];
@@ -304,7 +304,8 @@ __device__ void walk_request(const Params& P, Shared& sm, float* dyn, int b, lon
     const bool need_q = !greedy && nk > 0;
     const char* trow = row_of<T>(P.target, P, b, cur);
     const char* drow = need_q ? row_of<T>(P.draft, P, b, cur) : nullptr;
-    PQ<E, SM> p(dyn + threadIdx.x), q(dyn + (size_t)E * kThreads + threadIdx.x);
+    PQ<E, false> p(dyn + threadIdx.x);
+    PQ<E, SM> q(dyn + threadIdx.x);
     load_seg<T, E>(trow, first, V, vec, p);
     if (need_q) {
       load_seg<T, E>(drow, first, V, vec, q);
@@ -621,8 +622,8 @@ __device__ void walk_request(const Params& P, Shared& sm, float* dyn, int b, lon
   }
 }
 
-// SM: p and q in dynamic shared memory (2 E kThreads floats), else in registers; G: greedy calls
-// only.
+// SM: q in dynamic shared memory (E kThreads floats), else in registers; p is always in
+// registers.  G: greedy calls only.
 template <typename T, int E, bool SM, bool G>
 __global__ void __launch_bounds__(kThreads, 1) walk_kernel(const Params P) {
   __shared__ Shared sm;
