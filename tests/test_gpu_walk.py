@@ -104,7 +104,7 @@ def test_walk_more_requests_than_clusters():
 @pytest.mark.parametrize("B,V,dtype", [(40, 128256, "bf16"), (20, 131075, "f32"), (20, 147456, "f16")])
 def test_walk_single_wave_geometry(B, V, dtype):
     """Batches that need more waves of 8-CTA clusters than of 6-CTA clusters: the stochastic walk
-    takes the 6-CTA clusters that keep p and q in shared memory, and the greedy walk the 6-CTA
+    takes the 6-CTA clusters that keep q in shared memory, and the greedy walk the 6-CTA
     instantiation without q (several requests per cluster at B = 40; a ragged vocabulary; the
     largest vocabulary 6 CTAs cover)."""
     rng = np.random.default_rng(B + V)
