@@ -12,10 +12,11 @@
 // One thread-block cluster verifies one request at a time.  CTA `rank` of the cluster owns the
 // vocabulary slice [rank * 512 E, (rank + 1) * 512 E) and each of its 512 threads E consecutive
 // tokens of it, so the probabilities p and q of the node being visited stay on the SM for the
-// whole visit (in registers; q in shared memory where both do not fit).  Row statistics, residual masses and the draw's prefix sums are reduced in
-// a fixed order (warp, block, then the cluster's CTAs in rank order through distributed shared
-// memory), so every CTA computes bit-identical values and takes identical decisions; the
-// cluster barrier is the only synchronisation, and no thread ever spins on memory.
+// whole visit (in registers; q in shared memory where both do not fit).  Row statistics, residual
+// masses and the draw's prefix sums are reduced in a fixed order (warp, block, then the cluster's
+// CTAs in rank order through distributed shared memory), so every CTA computes bit-identical
+// values and takes identical decisions; the cluster barrier is the only synchronisation, and no
+// thread ever spins on memory.
 //
 // Residual algebra: after rejecting siblings with masses R_1 = 1, R_2, ..., the target is
 // max(0, p - c q) / R with c = R_1 + ... + R_j (max(0, max(0, p - c q) - R q) equals
