@@ -61,7 +61,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm) kv_compact_kernel(const 
   asm volatile("griddepcontrol.wait;" ::: "memory");
   if (t == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int32_t* pa = P.parents + (size_t)b * N1;
-  // round 1: the length, the path and every slot, all at once
+  // first pass: the length, the path and every slot, all at once
   const int L = __ldg(P.accept_len + b);
   bool ok = true;
   for (int j = t; j < N1; j += kThreads) {
